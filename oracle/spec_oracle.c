@@ -1,0 +1,536 @@
+/*
+ * spec_oracle.c -- plain fp64 CPU oracle of the batched speculative-decoding
+ * verify/commit step and of the confidence-scheduled verify-length pre-pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the independent checker for the CUDA
+ * library: only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline /
+ * reference arm load it.  It shares no code, header, table or helper with the
+ * CUDA path (speculative_decoding_verification_15_gb300/csrc), and the product
+ * path never calls it.
+ *
+ * Sources (page title -- section):
+ *  [ALX]  "From draft-then-verify to DSpark" (alexine.rip) -- "How speculative
+ *         decoding works": accept x with probability min(1, p(x)/q(x)); on
+ *         rejection resample from normalise(max(0, p - q)); lossless.
+ *  [PPR]  "Accelerating Large-Model Inference ..." (princepride.github.io) --
+ *         Sec. 1 "Producing Multiple Tokens in a Single Forward Pass" (propose /
+ *         verify / commit table: accept the longest prefix, resample at the first
+ *         disagreement) and its worked examples.
+ *  [VBK]  "DSpark paper review" (vllmbangkok.com) -- Sec. 4.2.1 (prefix survival
+ *         c_1 x ... x c_k, non-increasing) and Sec. 4.2.2 (hardware-aware prefix
+ *         scheduler: rank all draft tokens by survival, add one at a time, look up
+ *         the startup step-time table; production variant searches the whole
+ *         table instead of stopping at the first drop).
+ *  [MTL]  "Bringing DSpark to vLLM Metal" (mhdimo.github.io) -- "Correctness is
+ *         the feature": greedy path compares the target's argmax with the draft.
+ *  [SC11] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2,
+ *         3", SC'11 -- Philox4x32-10.
+ *
+ * Readings where the pages are silent are stated at each function.  Everything
+ * is fp64 with the host libm (exp, log); no blocking, fusion or reordering
+ * beyond what the definitions state.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_BF16 0
+#define OR_F32 1
+
+/* per-request status codes (same meaning as the library's out_status) */
+#define ST_OK 0
+#define ST_BAD_TOKEN 1
+#define ST_BAD_K 2
+#define ST_BAD_T 3
+#define ST_NONFINITE 4
+
+/* near-tie flag bits */
+#define FL_THRESH 1     /* |u - P/Q| < 1e-5 * P/Q at a scanned position            */
+#define FL_GUMBEL 2     /* top-2 Gumbel scores closer than 1e-5 * max(1,|top|)      */
+#define FL_DEGENERATE 4 /* residual max(0, p - q) has empty support                 */
+#define FL_ILLCOND 8    /* residual top-2 gap within the log(p-q) conditioning band */
+
+#define REL_TIE 1e-5
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 [SC11]: 10 rounds of the 4x32 S-box with multipliers         */
+/* M0, M1 and the Weyl key schedule W0, W1.                                   */
+/* ------------------------------------------------------------------------- */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    const uint64_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    int round;
+    for (round = 0; round < 10; ++round) {
+        uint64_t prod0 = M0 * (uint64_t)x0;
+        uint64_t prod1 = M1 * (uint64_t)x2;
+        uint32_t y0 = (uint32_t)(prod1 >> 32) ^ x1 ^ k0;
+        uint32_t y1 = (uint32_t)prod1;
+        uint32_t y2 = (uint32_t)(prod0 >> 32) ^ x3 ^ k1;
+        uint32_t y3 = (uint32_t)prod0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/*
+ * Random word for vocabulary entry v of draw `purpose` at logit row `row` of
+ * request b.  Reading (the pages define no RNG): key = (seed lo, seed hi);
+ * counter = (v >> 2, b, (row << 4) | purpose, step lo); word v & 3.
+ * Purposes: 0 = acceptance uniform (v = 0), 1 = residual Gumbel noise at the
+ * first rejected row, 2 = bonus Gumbel noise at row k_b.
+ */
+uint32_t oracle_rand_word(uint64_t seed, uint64_t step, int b, int row, int purpose, int v) {
+    uint32_t ctr[4], key[2], out[4];
+    key[0] = (uint32_t)(seed & 0xffffffffu);
+    key[1] = (uint32_t)(seed >> 32);
+    ctr[0] = (uint32_t)v >> 2;
+    ctr[1] = (uint32_t)b;
+    ctr[2] = ((uint32_t)row << 4) | (uint32_t)purpose;
+    ctr[3] = (uint32_t)(step & 0xffffffffu);
+    oracle_philox4x32_10(ctr, key, out);
+    return out[(uint32_t)v & 3u];
+}
+
+/* Uniform in (0,1): (2 * (w >> 9) + 1) * 2^-24, exact in fp32 and fp64. */
+double oracle_u01(uint32_t w) { return (double)(2u * (w >> 9) + 1u) * (1.0 / 16777216.0); }
+
+/* Gumbel(0,1) noise: g = -log(-log u). */
+double oracle_gumbel(uint32_t w) { return -log(-log(oracle_u01(w))); }
+
+/* ------------------------------------------------------------------------- */
+/* Decoding and the temperature softmax                                      */
+/* ------------------------------------------------------------------------- */
+static double decode(const void *base, int dtype, int64_t idx) {
+    if (dtype == OR_BF16) {
+        uint16_t h = ((const uint16_t *)base)[idx];
+        uint32_t bits = (uint32_t)h << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)base)[idx];
+}
+
+/* Max over a row with NaN propagation: NaN if any element is NaN. */
+static double row_max_nan(const double *x, int V) {
+    double m = -INFINITY;
+    int v;
+    for (v = 0; v < V; ++v) {
+        if (isnan(x[v])) return NAN;
+        if (x[v] > m) m = x[v];
+    }
+    return m;
+}
+
+/*
+ * log p_v for p = softmax(x / T) over the full vocabulary [ALX] (p and q are the
+ * target's and the draft's next-token distributions).  Reading: both target and
+ * draft logits are divided by the request's temperature T > 0 before the
+ * softmax; the max is subtracted for stability (it cancels exactly).
+ */
+void oracle_row_logprobs(const double *x, int V, double T, double *logp) {
+    double m = -INFINITY, s = 0.0, ls;
+    int v;
+    for (v = 0; v < V; ++v) {
+        double z = x[v] / T;
+        if (z > m) m = z;
+    }
+    for (v = 0; v < V; ++v) s += exp(x[v] / T - m);
+    ls = log(s);
+    for (v = 0; v < V; ++v) logp[v] = x[v] / T - m - ls;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The acceptance rule and the residual [ALX]                                 */
+/* ------------------------------------------------------------------------- */
+
+/* Acceptance probability of a draft token with target probability P and draft
+ * probability Q: min(1, P/Q).  Q = 0 (the draft could not have proposed it):
+ * reading -- accept iff P > 0. */
+double oracle_accept_prob(double P, double Q) {
+    if (Q > 0.0) return P / Q < 1.0 ? P / Q : 1.0;
+    return P > 0.0 ? 1.0 : 0.0;
+}
+
+/* Unnormalised residual weights r_v = max(0, p_v - q_v). */
+void oracle_residual_weights(const double *p, const double *q, int V, double *r) {
+    int v;
+    for (v = 0; v < V; ++v) r[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
+}
+
+/*
+ * Gumbel-max draw over log-weights lw (entries of -inf excluded): returns
+ * argmax_v (lw_v + g_v), lowest v on exact ties, or -1 if every entry is -inf.
+ * g_v comes from oracle_rand_word(seed, step, b, row, purpose, v).
+ * *gap receives the difference between the two best scores (+inf if < 2);
+ * *top the best score; *second_v the runner-up's index (-1 if none).
+ */
+static int gumbel_argmax(const double *lw, int V, uint64_t seed, uint64_t step, int b, int row,
+                         int purpose, double *gap, double *top, int *second_v) {
+    double best = -INFINITY, second = -INFINITY;
+    int bi = -1, si = -1, v;
+    for (v = 0; v < V; ++v) {
+        double s;
+        if (lw[v] == -INFINITY) continue;
+        s = lw[v] + oracle_gumbel(oracle_rand_word(seed, step, b, row, purpose, v));
+        if (s > best) {
+            second = best; si = bi;
+            best = s; bi = v;
+        } else if (s > second) {
+            second = s; si = v;
+        }
+    }
+    *gap = (si >= 0) ? best - second : INFINITY;
+    *top = best;
+    *second_v = si;
+    return bi;
+}
+
+/* Exposed for the Gumbel-max pin: draw from weights w (w_v = 0 excluded). */
+int oracle_gumbel_sample(const double *w, int V, uint64_t seed, uint64_t step, int b, int row, int purpose) {
+    double *lw = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    double gap, top;
+    int sv, v, r;
+    for (v = 0; v < V; ++v) lw[v] = w[v] > 0.0 ? log(w[v]) : -INFINITY;
+    r = gumbel_argmax(lw, V, seed, step, b, row, purpose, &gap, &top, &sv);
+    free(lw);
+    return r;
+}
+
+/* Greedy argmax over raw values, lowest index on ties [MTL]. */
+static int argmax_lowest(const double *x, int V) {
+    int bi = 0, v;
+    for (v = 1; v < V; ++v)
+        if (x[v] > x[bi]) bi = v;
+    return bi;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Per-request verify                                                         */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    const void *target, *draft;
+    int dtype, B, Kmax, V;
+    int64_t ld_row;
+    const int32_t *draft_tokens, *num_draft;
+    const float *temperature; /* NULL: greedy for every request */
+    uint64_t seed, step;
+    int32_t *out_tokens, *out_accepted, *out_status, *out_flags;
+    double *out_p, *out_q, *out_gap;
+} verify_args;
+
+static void load_row(const void *base, int dtype, int64_t row, int64_t ld_row, int V, double *dst) {
+    int v;
+    for (v = 0; v < V; ++v) dst[v] = decode(base, dtype, row * ld_row + v);
+}
+
+static void verify_one(const verify_args *a, int b, double *xt, double *xd, double *lpt, double *lpd,
+                       double *tmp) {
+    const int K1 = a->Kmax + 1, V = a->V;
+    int32_t *tok = a->out_tokens + (int64_t)b * K1;
+    const int32_t *x = a->draft_tokens + (int64_t)b * a->Kmax;
+    int kb = a->num_draft ? a->num_draft[b] : a->Kmax;
+    int i, v, status = ST_OK, greedy, A = 0, flags = 0;
+    double T = 0.0;
+    double min_gap = INFINITY;
+
+    for (i = 0; i < K1; ++i) tok[i] = -1;
+    for (i = 0; i < a->Kmax; ++i) {
+        if (a->out_p) a->out_p[(int64_t)b * a->Kmax + i] = -1.0;
+        if (a->out_q) a->out_q[(int64_t)b * a->Kmax + i] = -1.0;
+    }
+
+    /* status checks, in this order: k_b, temperature, tokens, non-finite rows */
+    if (kb < 0 || kb > a->Kmax) status = ST_BAD_K;
+    if (!status && a->temperature) {
+        T = (double)a->temperature[b];
+        if (!(T >= 0.0) || isinf(T)) status = ST_BAD_T;
+    }
+    greedy = (a->temperature == NULL) || (T == 0.0);
+    if (!status)
+        for (i = 0; i < kb; ++i)
+            if (x[i] < 0 || x[i] >= V) status = ST_BAD_TOKEN;
+    if (!status) {
+        /* needed rows: target 0..k_b, draft 0..k_b-1 (sampling only) */
+        for (i = 0; i <= kb && !status; ++i) {
+            load_row(a->target, a->dtype, (int64_t)b * K1 + i, a->ld_row, V, xt);
+            if (!isfinite(row_max_nan(xt, V))) status = ST_NONFINITE;
+        }
+        for (i = 0; i < kb && !greedy && !status; ++i) {
+            load_row(a->draft, a->dtype, (int64_t)b * a->Kmax + i, a->ld_row, V, xd);
+            if (!isfinite(row_max_nan(xd, V))) status = ST_NONFINITE;
+        }
+    }
+    a->out_status[b] = status;
+    if (status) {
+        a->out_accepted[b] = 0;
+        if (a->out_flags) a->out_flags[b] = 0;
+        if (a->out_gap) a->out_gap[b] = INFINITY;
+        return;
+    }
+
+    if (greedy) {
+        /* greedy: y_i = argmax of the raw target row; accept while y_i == x_i [MTL] */
+        int y = 0;
+        for (i = 0; i <= kb; ++i) {
+            load_row(a->target, a->dtype, (int64_t)b * K1 + i, a->ld_row, V, xt);
+            y = argmax_lowest(xt, V);
+            if (i == kb || y != x[i]) break;
+            tok[i] = x[i];
+            ++A;
+        }
+        tok[A] = y;
+        a->out_accepted[b] = A;
+        if (a->out_flags) a->out_flags[b] = 0;
+        if (a->out_gap) a->out_gap[b] = INFINITY;
+        return;
+    }
+
+    /* sampling: P_i = p_i(x_i), Q_i = q_i(x_i) for every draft position */
+    {
+        int rejected = 0;
+        for (i = 0; i < kb; ++i) {
+            double P, Q, u, ratio;
+            load_row(a->target, a->dtype, (int64_t)b * K1 + i, a->ld_row, V, xt);
+            load_row(a->draft, a->dtype, (int64_t)b * a->Kmax + i, a->ld_row, V, xd);
+            oracle_row_logprobs(xt, V, T, lpt);
+            oracle_row_logprobs(xd, V, T, lpd);
+            P = exp(lpt[x[i]]);
+            Q = exp(lpd[x[i]]);
+            if (a->out_p) a->out_p[(int64_t)b * a->Kmax + i] = P;
+            if (a->out_q) a->out_q[(int64_t)b * a->Kmax + i] = Q;
+            if (rejected) continue;
+            /* accept with probability min(1, P/Q): u < P/Q with u uniform in (0,1) [ALX] */
+            u = oracle_u01(oracle_rand_word(a->seed, a->step, b, i, 0, 0));
+            if (Q > 0.0) {
+                ratio = P / Q;
+                if (fabs(u - ratio) < REL_TIE * ratio) flags |= FL_THRESH;
+                if (u < ratio) { tok[i] = x[i]; ++A; continue; }
+            } else if (P > 0.0) {
+                tok[i] = x[i]; ++A; continue;
+            }
+            rejected = 1; /* first rejection: position A == i [PPR] */
+        }
+    }
+
+    if (A < kb) {
+        /* correction at j = A: Gumbel-max over log max(0, p_j - q_j) [ALX] */
+        const int j = A;
+        double gap, top;
+        int tk, sv;
+        load_row(a->target, a->dtype, (int64_t)b * K1 + j, a->ld_row, V, xt);
+        load_row(a->draft, a->dtype, (int64_t)b * a->Kmax + j, a->ld_row, V, xd);
+        oracle_row_logprobs(xt, V, T, lpt);
+        oracle_row_logprobs(xd, V, T, lpd);
+        for (v = 0; v < V; ++v) { lpt[v] = exp(lpt[v]); lpd[v] = exp(lpd[v]); }
+        oracle_residual_weights(lpt, lpd, V, tmp);
+        for (v = 0; v < V; ++v) tmp[v] = tmp[v] > 0.0 ? log(tmp[v]) : -INFINITY;
+        tk = gumbel_argmax(tmp, V, a->seed, a->step, b, j, 1, &gap, &top, &sv);
+        if (tk >= 0) {
+            double tol = REL_TIE * (fabs(top) > 1.0 ? fabs(top) : 1.0);
+            if (gap < tol) flags |= FL_GUMBEL;
+            /* conditioning of log(p - q) = log p + log(1 - q/p): an fp32 error e in
+             * log(q/p) moves the score by ~ e * q / (p - q); widen the band by that
+             * factor for the two contenders */
+            if (sv >= 0) {
+                double k1 = lpd[tk] / (lpt[tk] - lpd[tk]);
+                double k2 = lpd[sv] / (lpt[sv] - lpd[sv]);
+                if (gap < tol * (k1 + k2)) flags |= FL_ILLCOND;
+            }
+            min_gap = gap;
+        } else {
+            /* reading: empty support (p <= q everywhere, only possible by rounding):
+             * draw from the target row j with the same purpose-1 noise */
+            flags |= FL_DEGENERATE;
+            oracle_row_logprobs(xt, V, T, lpt);
+            tk = gumbel_argmax(lpt, V, a->seed, a->step, b, j, 1, &gap, &top, &sv);
+            min_gap = gap;
+        }
+        tok[j] = tk;
+    } else {
+        /* bonus: every draft accepted; sample from the target's row k_b */
+        double gap, top;
+        int tk, sv;
+        load_row(a->target, a->dtype, (int64_t)b * K1 + kb, a->ld_row, V, xt);
+        oracle_row_logprobs(xt, V, T, lpt);
+        tk = gumbel_argmax(lpt, V, a->seed, a->step, b, kb, 2, &gap, &top, &sv);
+        if (gap < REL_TIE * (fabs(top) > 1.0 ? fabs(top) : 1.0)) flags |= FL_GUMBEL;
+        min_gap = gap;
+        tok[kb] = tk;
+    }
+    a->out_accepted[b] = A;
+    if (a->out_flags) a->out_flags[b] = flags;
+    if (a->out_gap) a->out_gap[b] = min_gap;
+}
+
+static int run_verify(const verify_args *a, int nthreads) {
+    int b;
+    if (a->B <= 0) return 0;
+    (void)nthreads;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : 1)
+#endif
+    {
+        double *buf = (double *)malloc(sizeof(double) * (size_t)a->V * 5);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (b = 0; b < a->B; ++b)
+            verify_one(a, b, buf, buf + a->V, buf + 2 * (size_t)a->V, buf + 3 * (size_t)a->V,
+                       buf + 4 * (size_t)a->V);
+        free(buf);
+    }
+    return 0;
+}
+
+/*
+ * Sampling verify for a batch.  Layout as the library's: target row (b,i) at
+ * (b*(Kmax+1)+i)*ld_row, draft row (b,i) at (b*Kmax+i)*ld_row, V contiguous.
+ * temperature[b] == 0 marks a greedy request (reading).  out_tokens [B,Kmax+1]
+ * (-1 = unused), out_accepted [B], out_p/out_q [B,Kmax] (-1 where not computed),
+ * out_status [B], out_flags [B] (near-tie bits), out_gap [B] (top-2 gap of the
+ * Gumbel draw, +inf if none).  nthreads: OpenMP threads over requests.
+ */
+int oracle_verify_sample(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                         int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                         const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+                         int32_t *out_accepted, double *out_p, double *out_q, int32_t *out_status,
+                         int32_t *out_flags, double *out_gap, int nthreads) {
+    verify_args a;
+    a.target = target; a.draft = draft; a.dtype = dtype; a.B = B; a.Kmax = Kmax; a.V = V;
+    a.ld_row = ld_row; a.draft_tokens = draft_tokens; a.num_draft = num_draft;
+    a.temperature = temperature; a.seed = seed; a.step = step;
+    a.out_tokens = out_tokens; a.out_accepted = out_accepted; a.out_status = out_status;
+    a.out_flags = out_flags; a.out_p = out_p; a.out_q = out_q; a.out_gap = out_gap;
+    return run_verify(&a, nthreads);
+}
+
+/* Greedy verify for a batch (draft logits are never read). */
+int oracle_verify_greedy(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                         const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
+                         int32_t *out_accepted, int32_t *out_status, int nthreads) {
+    verify_args a;
+    memset(&a, 0, sizeof a);
+    a.target = target; a.dtype = dtype; a.B = B; a.Kmax = Kmax; a.V = V; a.ld_row = ld_row;
+    a.draft_tokens = draft_tokens; a.num_draft = num_draft;
+    a.out_tokens = out_tokens; a.out_accepted = out_accepted; a.out_status = out_status;
+    return run_verify(&a, nthreads);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Confidence-scheduled verify length [VBK Sec. 4.2.1, 4.2.2]                 */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    double s;
+    int b, i;
+} cand_t;
+
+static int cand_cmp(const void *pa, const void *pb) {
+    const cand_t *x = (const cand_t *)pa, *y = (const cand_t *)pb;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    if (x->b != y->b) return x->b < y->b ? -1 : 1;
+    return x->i < y->i ? -1 : (x->i > y->i);
+}
+
+/*
+ * Survival S_{b,i} = c_{b,0} * ... * c_{b,i} (fp64, left to right) [VBK 4.2.1];
+ * E_b(L) = sum_{i<L} S_{b,i} is the expected number of accepted drafts when L
+ * are verified.  Every request keeps m_b = min(min_len, maxlen_b) slots; the
+ * other slots (b,i), m_b <= i < maxlen_b, are ranked by S descending (ties: b
+ * then i ascending) and added one at a time [VBK 4.2.2].  For every total
+ * n = n0 .. min(budget, n0 + #candidates, n_table - 1) the expected throughput
+ * F(n) = (B + sum_b E_b) / tau[n] is evaluated (B: the one target token every
+ * request emits) and the best n over the whole table is kept, ties to the
+ * smallest n (full search, [VBK 4.2.2] production variant).
+ * Readings: n counts draft slots; confidences are clamped to [0,1] (NaN -> 0);
+ * maxlen_b = clamp(max_len[b], 0, Kmax) (NULL: Kmax); tau[n] <= 0 or
+ * non-finite makes n unusable.
+ * out_len [B]; out_info[3] = {n*, B + sum E, F(n*)}; *out_flags: 1 = the best
+ * two F values within 1e-9 relative, 2 = survival tie (1e-12) across the cut.
+ * Returns 0, or 1 for invalid arguments.
+ */
+int oracle_schedule_verify_len(const float *conf, const int32_t *max_len, int B, int Kmax,
+                               const float *step_time_us, int n_table, int budget, int min_len,
+                               int32_t *out_len, double *out_info, int32_t *out_flags) {
+    double *S = (double *)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1) * (size_t)(Kmax > 0 ? Kmax : 1));
+    int *mand = (int *)malloc(sizeof(int) * (size_t)(B > 0 ? B : 1));
+    int *mlen = (int *)malloc(sizeof(int) * (size_t)(B > 0 ? B : 1));
+    cand_t *cand = (cand_t *)malloc(sizeof(cand_t) * ((size_t)(B > 0 ? B : 1) * (size_t)(Kmax > 0 ? Kmax : 1)));
+    int b, i, nc = 0, n0 = 0, nhi, n, nbest, take, flags = 0;
+    double E0 = 0.0, E, Fbest = -INFINITY, Fsecond = -INFINITY;
+
+    if (B < 0 || Kmax < 0 || min_len < 0 || n_table < 1 || budget < 0 ||
+        (int64_t)budget < (int64_t)B * min_len || (int64_t)n_table - 1 < (int64_t)B * min_len) {
+        free(S); free(mand); free(mlen); free(cand);
+        return 1;
+    }
+    for (b = 0; b < B; ++b) {
+        double surv = 1.0;
+        int ml = max_len ? max_len[b] : Kmax;
+        if (ml < 0) ml = 0;
+        if (ml > Kmax) ml = Kmax;
+        mlen[b] = ml;
+        mand[b] = min_len < ml ? min_len : ml;
+        for (i = 0; i < Kmax; ++i) {
+            double c = (double)conf[(int64_t)b * Kmax + i];
+            if (isnan(c) || c < 0.0) c = 0.0;
+            if (c > 1.0) c = 1.0;
+            surv = surv * c;
+            S[(int64_t)b * Kmax + i] = surv;
+        }
+        n0 += mand[b];
+        for (i = 0; i < mand[b]; ++i) E0 += S[(int64_t)b * Kmax + i];
+        for (i = mand[b]; i < ml; ++i) {
+            cand[nc].s = S[(int64_t)b * Kmax + i];
+            cand[nc].b = b;
+            cand[nc].i = i;
+            ++nc;
+        }
+    }
+    qsort(cand, (size_t)nc, sizeof(cand_t), cand_cmp);
+
+    nhi = n0 + nc;
+    if (budget < nhi) nhi = budget;
+    if (n_table - 1 < nhi) nhi = n_table - 1;
+    nbest = n0;
+    E = E0;
+    for (n = n0; n <= nhi; ++n) {
+        double tau, F;
+        if (n > n0) E += cand[n - n0 - 1].s;
+        tau = (double)step_time_us[n];
+        F = (tau > 0.0 && isfinite(tau)) ? ((double)B + E) / tau : -INFINITY;
+        if (F > Fbest) {
+            Fsecond = Fbest;
+            Fbest = F;
+            nbest = n;
+        } else if (F > Fsecond) {
+            Fsecond = F;
+        }
+    }
+    if (isfinite(Fbest) && isfinite(Fsecond) && Fbest - Fsecond < 1e-9 * Fbest) flags |= 1;
+
+    take = nbest - n0;
+    if (take < 0) take = 0;
+    for (b = 0; b < B; ++b) out_len[b] = mand[b];
+    for (i = 0; i < take; ++i) out_len[cand[i].b] += 1;
+    if (take > 0 && take < nc && fabs(cand[take - 1].s - cand[take].s) < 1e-12) flags |= 2;
+
+    E = E0;
+    for (i = 0; i < take; ++i) E += cand[i].s;
+    if (out_info) {
+        out_info[0] = (double)nbest;
+        out_info[1] = (double)B + E;
+        out_info[2] = (nbest >= 0 && nbest < n_table && step_time_us[nbest] > 0.0f)
+                          ? ((double)B + E) / (double)step_time_us[nbest]
+                          : 0.0;
+    }
+    if (out_flags) *out_flags = flags;
+    free(S); free(mand); free(mlen); free(cand);
+    return 0;
+}
