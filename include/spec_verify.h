@@ -1,0 +1,174 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding verify/commit
+ * library (libspecverify.so).
+ *
+ * What it computes (page title -- section):
+ *  - "From draft-then-verify to DSpark" (alexine.rip) -- "How speculative decoding
+ *    works": each draft token x is accepted with probability min(1, p(x)/q(x)),
+ *    p the target's and q the draft's next-token distribution; at the first
+ *    rejection a token is drawn from normalise(max(0, p - q)); the emitted tokens
+ *    are distributed exactly as the target's.
+ *  - "Accelerating Large-Model Inference ... DSpark Speculative Decoding"
+ *    (princepride.github.io) -- Sec. 1, propose/verify/commit table: the target
+ *    scores all draft positions in one pass; the longest accepted prefix is kept
+ *    and one more token is emitted (a correction at the first rejection, or a
+ *    bonus token from the target's row after the last draft).
+ *  - "Bringing DSpark to vLLM Metal" (mhdimo.github.io) -- greedy path: compare the
+ *    target's argmax with each draft token.  The target's logits cover the K draft
+ *    positions plus the one after them (K+1 rows), where the bonus token comes from.
+ *  - "DSpark paper review" (vllmbangkok.com) -- Sec. 4.2.1 prefix survival
+ *    c_1 x ... x c_k; Sec. 4.2.2 hardware-aware prefix scheduler over a step-time
+ *    table profiled at startup, searching the whole table; Sec. 5.3 ragged batches
+ *    where each request verifies its own number of drafts.
+ *
+ * Conventions for every entry point:
+ *  - Array pointers are DEVICE pointers owned by the caller; the library keeps no
+ *    reference after the call returns and allocates no device memory per call.
+ *    Scratch space is the caller's workspace (size from the *_workspace_size query).
+ *  - Calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronise the host.
+ *  - Logits are row-major with V contiguous and a row stride of ld_row elements
+ *    (ld_row >= V).  Target row (b, i), i = 0..Kmax, starts at element
+ *    (b*(Kmax+1) + i) * ld_row; draft row (b, i), i = 0..Kmax-1, at
+ *    (b*Kmax + i) * ld_row.  Requests verify k_b = num_draft[b] <= Kmax drafts;
+ *    target rows i > k_b and draft rows i >= k_b are never read.
+ *  - Host-checkable argument errors return SPEC_EINVAL / SPEC_EWORKSPACE /
+ *    SPEC_EUNSUPPORTED before anything is launched; a failed launch returns
+ *    SPEC_ECUDA.  Data-dependent errors are reported per request in out_status.
+ *  - Emitted tokens: out_tokens[b, 0 .. out_accepted[b]] (accepted drafts, then
+ *    the correction or bonus token); unused slots are -1.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_EINVAL = 1,        /* bad argument (null pointer, size out of range) */
+    SPEC_ECUDA = 2,         /* a CUDA runtime call or launch failed           */
+    SPEC_EUNSUPPORTED = 3,  /* valid but outside what this build supports     */
+    SPEC_EWORKSPACE = 4     /* workspace pointer null or too small            */
+} spec_err;
+
+/* Logit element types. */
+typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
+
+/* Per-request status codes written to out_status (checked in this order). */
+#define SPEC_STATUS_OK 0
+#define SPEC_STATUS_BAD_TOKEN 1        /* a draft token x_i (i < k_b) is outside [0, V)          */
+#define SPEC_STATUS_BAD_K 2            /* num_draft[b] outside [0, Kmax]                          */
+#define SPEC_STATUS_BAD_TEMPERATURE 3  /* temperature[b] < 0, NaN or infinite                     */
+#define SPEC_STATUS_NONFINITE 4        /* a needed logit row holds NaN or +inf, or is all -inf    */
+/* A request with a non-zero status has out_accepted[b] = 0 and every token -1. */
+
+/* Limits of this build. */
+#define SPEC_MAX_BATCH 8192        /* B                                   */
+#define SPEC_MAX_DRAFTS 255        /* Kmax                                */
+#define SPEC_MAX_SCHED_ITEMS 8192  /* B * Kmax for the scheduler          */
+
+/*
+ * Bytes of device workspace that spec_verify_greedy / spec_verify_sample need for
+ * (B, Kmax, V, dtype) on the current device.  Returns 0 for invalid sizes.  The
+ * workspace holds per-segment row statistics and the residual-draw job list; its
+ * contents need no initialisation and are garbage after a call.
+ */
+size_t spec_verify_workspace_size(int B, int Kmax, int V, int dtype);
+
+/*
+ * Greedy verify ("Bringing DSpark to vLLM Metal" -- greedy serving path; the
+ * propose/verify/commit table of "Accelerating Large-Model Inference", Sec. 1).
+ * For each request b and i = 0..k_b, y_i = argmax_v target[b, i, v] over the raw
+ * logits, lowest v on ties.  A = first i < k_b with y_i != x_i, else k_b.
+ * Emits x_0 .. x_{A-1}, then y_A.  Draft logits are not an input.
+ *
+ *  target        [B, Kmax+1, ld_row] logits of type dtype
+ *  draft_tokens  [B, Kmax] int32 draft tokens x_i
+ *  num_draft     [B] int32 k_b, or NULL for k_b = Kmax
+ *  out_tokens    [B, Kmax+1] int32; out_accepted [B] int32 (= A); out_status [B]
+ *  ws, ws_bytes  workspace of at least spec_verify_workspace_size(B, Kmax, V, dtype)
+ * B = 0 is a no-op.  Kmax = 0 verifies nothing and emits y_0.
+ */
+int spec_verify_greedy(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                       const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
+                       int32_t *out_accepted, int32_t *out_status, void *ws, size_t ws_bytes,
+                       void *cuda_stream);
+
+/*
+ * Sampling verify by rejection sampling ("From draft-then-verify to DSpark" --
+ * "How speculative decoding works").  For request b with temperature T_b > 0:
+ *   p_i = softmax(target[b, i, :] / T_b), q_i = softmax(draft[b, i, :] / T_b) over
+ *   all V entries (numerically stable, fp32 with per-segment maxima);
+ *   draft i is accepted iff u_i * q_i(x_i) < p_i(x_i), u_i uniform in (0, 1)
+ *   (probability min(1, p/q)); scanning stops at the first rejection j;
+ *   correction at j: argmax_v over {p_j(v) > q_j(v)} of log(p_j(v) - q_j(v)) + g_v
+ *   (Gumbel-max draw from normalise(max(0, p_j - q_j))), lowest v on ties;
+ *   bonus when all k_b are accepted: argmax_v log p_{k_b}(v) + g_v from the
+ *   target's row k_b.
+ * temperature[b] == 0 makes request b greedy (as spec_verify_greedy).
+ * Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key (seed lo, seed hi)
+ * and counter (v >> 2, b, (row << 4) | purpose, step lo), word v & 3; purpose 0 =
+ * acceptance uniform (v = 0), 1 = correction noise at row j, 2 = bonus noise at
+ * row k_b.  A word w maps to u = (2 (w >> 9) + 1) 2^-24 and g = -log(-log u).
+ * Outputs p_i(x_i) / q_i(x_i) for i < k_b go to out_p / out_q (may be NULL; -1
+ * where not computed).  out_tokens, out_accepted, out_status as for greedy.
+ * If p_j <= q_j everywhere (only possible by rounding), the correction is drawn
+ * from p_j with the same noise.
+ */
+int spec_verify_sample(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                       int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                       const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+                       int32_t *out_accepted, float *out_p, float *out_q, int32_t *out_status, void *ws,
+                       size_t ws_bytes, void *cuda_stream);
+
+/*
+ * Confidence-scheduled verify lengths ("DSpark paper review", Sec. 4.2.1 and
+ * 4.2.2).  Survival S_{b,i} = c_{b,0} * ... * c_{b,i} in fp64 (confidences clamped
+ * to [0, 1], NaN as 0); E_b(L) = sum_{i<L} S_{b,i} is the expected accepted length.
+ * Every request keeps m_b = min(min_len, maxlen_b) slots, maxlen_b =
+ * clamp(max_len[b], 0, Kmax) (max_len NULL: Kmax).  The remaining slots of all
+ * requests are ranked by survival (ties: lower b, then lower i) and granted one at
+ * a time; for every total n from sum m_b to min(budget, n_table - 1, all slots)
+ * the expected throughput F(n) = (B + sum_b E_b) / step_time_us[n] is evaluated
+ * and the largest is kept (ties: smallest n) -- a search of the whole table, not
+ * a stop at the first drop.  Entries step_time_us[n] <= 0 make n unusable.
+ *
+ *  conf          [B, Kmax] float32 per-token confidences c_{b,i}
+ *  max_len       [B] int32 or NULL
+ *  step_time_us  [n_table] float32 step time with n verified draft slots
+ *  out_len       [B] int32 verify length L_b (feed it to num_draft)
+ *  out_info      [3] double {n*, B + sum E, F(n*)} or NULL
+ * Errors: SPEC_EINVAL if budget < B*min_len or n_table - 1 < B*min_len;
+ * SPEC_EUNSUPPORTED if B*Kmax > SPEC_MAX_SCHED_ITEMS.  Uses no workspace.
+ */
+int spec_schedule_verify_len(const float *conf, const int32_t *max_len, int B, int Kmax,
+                             const float *step_time_us, int n_table, int budget, int min_len,
+                             int32_t *out_len, double *out_info, void *cuda_stream);
+
+/* Short text for a return code. */
+const char *spec_error_string(int err);
+
+/* The CUDA error (cudaError_t value) behind the last SPEC_ECUDA on this thread. */
+int spec_last_cuda_error(void);
+
+/*
+ * Kernel timing for measurement.  While enabled, every verify call records CUDA
+ * events on its stream around each kernel it launches; spec_profile_read waits for
+ * the last call's events and writes up to n durations in milliseconds, in launch
+ * order (greedy: rows, accept; sample: rows, accept, residual, final), returning
+ * how many were written (negative spec_err on failure).
+ */
+int spec_profile_enable(int on);
+int spec_profile_read(float *ms, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

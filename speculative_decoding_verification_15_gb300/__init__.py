@@ -1,0 +1,14 @@
+"""GB300-native batched speculative-decoding verify/commit (CUDA kernels for sm_103a).
+
+The compute path is libspecverify.so (C ABI in include/spec_verify.h); this package
+only builds it and marshals torch tensors into it.
+"""
+from . import _build, binding  # noqa: F401
+from .api import (schedule_verify_len, verify_greedy, verify_sample,  # noqa: F401
+                  verify_sample_host, workspace)
+from .binding import (SpecError, spec_schedule_verify_len, spec_verify_greedy,  # noqa: F401
+                      spec_verify_sample, spec_verify_workspace_size)
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)

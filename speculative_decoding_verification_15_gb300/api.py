@@ -1,0 +1,104 @@
+"""Convenience layer over the C ABI: allocates outputs and a cached workspace.
+
+Every call goes through the C entry points in ``binding``; this module only
+manages tensors.  Shapes follow the C ABI: target logits [B, K+1, V], draft logits
+[B, K, V] (bfloat16 or float32), draft tokens [B, K] int32.
+"""
+from __future__ import annotations
+
+import threading
+
+import torch
+
+from . import binding
+
+_ws_lock = threading.Lock()
+_ws_cache: dict[int, torch.Tensor] = {}
+
+
+def workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    """A cached uint8 workspace of at least nbytes on device (grown on demand)."""
+    idx = torch.device(device).index
+    if idx is None:
+        idx = torch.cuda.current_device()
+    with _ws_lock:
+        ws = _ws_cache.get(idx)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=torch.device("cuda", idx))
+            _ws_cache[idx] = ws
+        return ws
+
+
+def _as_i32(t, device):
+    return None if t is None else t.to(device=device, dtype=torch.int32).contiguous()
+
+
+def verify_sample(target, draft, draft_tokens, temperature, seed: int, step: int, num_draft=None,
+                  stream=None, want_probs: bool = True) -> dict:
+    dev = target.device
+    B, K1, V = target.shape
+    K = K1 - 1
+    x = _as_i32(draft_tokens, dev)
+    nd = _as_i32(num_draft, dev)
+    T = temperature.to(device=dev, dtype=torch.float32).contiguous()
+    out = dict(tokens=torch.empty((B, K1), dtype=torch.int32, device=dev),
+               accepted=torch.empty(B, dtype=torch.int32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev),
+               p=torch.empty((B, K), dtype=torch.float32, device=dev) if want_probs else None,
+               q=torch.empty((B, K), dtype=torch.float32, device=dev) if want_probs else None)
+    ws = workspace(dev, binding.spec_verify_workspace_size(B, K, V, binding._dtype_code(target)))
+    binding.spec_verify_sample(target, draft, x, nd, T, seed, step, out["tokens"], out["accepted"], out["p"],
+                               out["q"], out["status"], ws, stream)
+    return out
+
+
+def verify_greedy(target, draft_tokens, num_draft=None, stream=None) -> dict:
+    dev = target.device
+    B, K1, V = target.shape
+    x = _as_i32(draft_tokens, dev)
+    nd = _as_i32(num_draft, dev)
+    out = dict(tokens=torch.empty((B, K1), dtype=torch.int32, device=dev),
+               accepted=torch.empty(B, dtype=torch.int32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    ws = workspace(dev, binding.spec_verify_workspace_size(B, K1 - 1, V, binding._dtype_code(target)))
+    binding.spec_verify_greedy(target, x, nd, out["tokens"], out["accepted"], out["status"], ws, stream)
+    return out
+
+
+def schedule_verify_len(conf, step_time_us, budget: int, min_len: int, max_len=None, stream=None):
+    dev = conf.device
+    B = conf.shape[0]
+    out_len = torch.empty(B, dtype=torch.int32, device=dev)
+    info = torch.empty(3, dtype=torch.float64, device=dev)
+    binding.spec_schedule_verify_len(conf.to(torch.float32).contiguous(), _as_i32(max_len, dev),
+                                     step_time_us.to(device=dev, dtype=torch.float32).contiguous(), budget,
+                                     min_len, out_len, info, stream)
+    return out_len, info
+
+
+def verify_sample_host(target_h, draft_h, tokens_h, temperature_h, seed: int, step: int, num_draft_h=None,
+                       device=None, dev_buffers: dict | None = None) -> dict:
+    """End-to-end call from host (ideally pinned) tensors: copy in, verify, copy the
+    emitted tokens, accepted counts and statuses back.  Returns host tensors."""
+    device = torch.device(device or "cuda")
+    bufs = dev_buffers if dev_buffers is not None else {}
+
+    def dev_copy(name, t):
+        if t is None:
+            return None
+        d = bufs.get(name)
+        if d is None or d.shape != t.shape or d.dtype != t.dtype:
+            d = torch.empty(t.shape, dtype=t.dtype, device=device)
+            bufs[name] = d
+        d.copy_(t, non_blocking=True)
+        return d
+
+    t = dev_copy("target", target_h)
+    d = dev_copy("draft", draft_h)
+    x = dev_copy("tokens", tokens_h)
+    T = dev_copy("temperature", temperature_h)
+    nd = dev_copy("num_draft", num_draft_h)
+    out = verify_sample(t, d, x, T, seed, step, num_draft=nd, want_probs=False)
+    host = {k: v.to("cpu", non_blocking=True) for k, v in out.items() if v is not None}
+    torch.cuda.current_stream().synchronize()
+    return host

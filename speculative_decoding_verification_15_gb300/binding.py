@@ -1,0 +1,223 @@
+"""ctypes binding of libspecverify.so (include/spec_verify.h).
+
+Argument marshalling only: every step of the verify path runs in the library's
+CUDA kernels.  Functions named like the C entry points take torch CUDA tensors,
+check shapes / dtypes / devices, pass raw pointers and the current stream, and
+raise SpecError on a non-zero return code.  The library must be built
+(``__graft_entry__.build()`` or ``_build.build()``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import _build
+
+SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EUNSUPPORTED, SPEC_EWORKSPACE = 0, 1, 2, 3, 4
+SPEC_BF16, SPEC_F32 = 0, 1
+STATUS_OK, STATUS_BAD_TOKEN, STATUS_BAD_K, STATUS_BAD_TEMPERATURE, STATUS_NONFINITE = 0, 1, 2, 3, 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn: str, rc: int, lib=None):
+        msg = f"{fn} failed: {rc}"
+        if lib is not None:
+            msg += f" ({lib.spec_error_string(rc).decode()})"
+            if rc == SPEC_ECUDA:
+                msg += f", cudaError {lib.spec_last_cuda_error()}"
+        super().__init__(msg)
+        self.rc = rc
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libspecverify.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or lib_path()
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with __graft_entry__.build() (needs nvcc)")
+        lib = ctypes.CDLL(p)
+        P, I32, I64, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+        lib.spec_verify_workspace_size.argtypes = [I32, I32, I32, I32]
+        lib.spec_verify_workspace_size.restype = SZ
+        lib.spec_verify_greedy.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, P, P, P, SZ, P]
+        lib.spec_verify_greedy.restype = I32
+        lib.spec_verify_sample.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P, P, P,
+                                           P, SZ, P]
+        lib.spec_verify_sample.restype = I32
+        lib.spec_schedule_verify_len.argtypes = [P, P, I32, I32, P, I32, I32, I32, P, P, P]
+        lib.spec_schedule_verify_len.restype = I32
+        lib.spec_error_string.argtypes = [I32]
+        lib.spec_error_string.restype = ctypes.c_char_p
+        lib.spec_last_cuda_error.argtypes = []
+        lib.spec_last_cuda_error.restype = I32
+        lib.spec_profile_enable.argtypes = [I32]
+        lib.spec_profile_enable.restype = I32
+        lib.spec_profile_read.argtypes = [P, I32]
+        lib.spec_profile_read.restype = I32
+        _lib = lib
+        return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/spec_verify.h declares."""
+    hdr = os.path.join(_build.INCLUDE, "spec_verify.h")
+    text = open(hdr).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------------ marshalling
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _logits_layout(t: torch.Tensor, rows_per_req: int):
+    """(B, V, ld_row) of a [B, rows, V] logits tensor whose last dim is contiguous."""
+    if t.dim() != 3 or t.shape[1] != rows_per_req:
+        raise ValueError(f"logits must be [B, {rows_per_req}, V], got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError("logits must be a CUDA tensor")
+    B, R, V = t.shape
+    ld = t.stride(1) if R > 1 else (t.stride(0) if B > 1 else V)
+    if V > 1 and t.stride(2) != 1:
+        raise ValueError("logits must have V contiguous")
+    if ld < V or (R > 1 and B > 1 and t.stride(0) != R * ld) or (R == 1 and B > 1 and t.stride(0) != ld):
+        raise ValueError("logit rows must be evenly strided: row (b, i) at (b * rows + i) * ld_row")
+    return B, V, ld
+
+
+def spec_verify_workspace_size(B: int, Kmax: int, V: int, dtype: int) -> int:
+    return int(load().spec_verify_workspace_size(B, Kmax, V, dtype))
+
+
+def spec_verify_greedy(target, draft_tokens, num_draft, out_tokens, out_accepted, out_status, workspace,
+                       stream=None) -> None:
+    lib = load()
+    K1 = target.shape[1]
+    Kmax = K1 - 1
+    B, V, ld = _logits_layout(target, K1)
+    dev = target.device
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, Kmax), dev)
+    if num_draft is not None:
+        _need(num_draft, "num_draft", torch.int32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K1), dev)
+    _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    rc = lib.spec_verify_greedy(_ptr(target), _dtype_code(target), B, Kmax, V, ld, _ptr(draft_tokens),
+                                _ptr(num_draft), _ptr(out_tokens), _ptr(out_accepted), _ptr(out_status),
+                                _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_greedy", rc, lib)
+
+
+def spec_verify_sample(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int, out_tokens,
+                       out_accepted, out_p, out_q, out_status, workspace, stream=None) -> None:
+    lib = load()
+    K1 = target.shape[1]
+    Kmax = K1 - 1
+    B, V, ld = _logits_layout(target, K1)
+    dev = target.device
+    if draft.dtype != target.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    if Kmax > 0:
+        Bd, Vd, ldd = _logits_layout(draft, Kmax)
+        if (Bd, Vd, ldd) != (B, V, ld):
+            raise ValueError("draft logits must be [B, Kmax, V] with the target's row stride")
+    if draft.device != dev:
+        raise ValueError("draft logits must be on the target's device")
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, Kmax), dev)
+    if num_draft is not None:
+        _need(num_draft, "num_draft", torch.int32, (B,), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K1), dev)
+    _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
+    if out_p is not None:
+        _need(out_p, "out_p", torch.float32, (B, Kmax), dev)
+    if out_q is not None:
+        _need(out_q, "out_q", torch.float32, (B, Kmax), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    rc = lib.spec_verify_sample(_ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
+                                _ptr(draft_tokens), _ptr(num_draft), _ptr(temperature),
+                                int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_tokens),
+                                _ptr(out_accepted), _ptr(out_p), _ptr(out_q), _ptr(out_status),
+                                _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_sample", rc, lib)
+
+
+def spec_schedule_verify_len(conf, max_len, step_time_us, budget: int, min_len: int, out_len, out_info=None,
+                             stream=None) -> None:
+    lib = load()
+    if conf.dim() != 2:
+        raise ValueError("conf must be [B, Kmax]")
+    B, Kmax = conf.shape
+    dev = conf.device
+    _need(conf, "conf", torch.float32, None, dev)
+    if max_len is not None:
+        _need(max_len, "max_len", torch.int32, (B,), dev)
+    _need(step_time_us, "step_time_us", torch.float32, None, dev)
+    _need(out_len, "out_len", torch.int32, (B,), dev)
+    if out_info is not None:
+        _need(out_info, "out_info", torch.float64, (3,), dev)
+    rc = lib.spec_schedule_verify_len(_ptr(conf), _ptr(max_len), B, Kmax, _ptr(step_time_us),
+                                      step_time_us.numel(), int(budget), int(min_len), _ptr(out_len),
+                                      _ptr(out_info), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_schedule_verify_len", rc, lib)
+
+
+def profile_enable(on: bool) -> None:
+    load().spec_profile_enable(1 if on else 0)
+
+
+def profile_read(n: int = 4) -> list[float]:
+    buf = (ctypes.c_float * n)()
+    k = load().spec_profile_read(buf, n)
+    if k < 0:
+        raise SpecError("spec_profile_read", -k, load())
+    return [float(buf[i]) for i in range(k)]

@@ -1,0 +1,241 @@
+// spec_common.cuh -- device building blocks of the verify/commit kernels (sm_103a).
+//
+// Counter-based RNG: Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw,
+// "Parallel random numbers: as easy as 1, 2, 3" (SC'11): ten rounds of the 4x32
+// S-box with multipliers 0xD2511F53 / 0xCD9E8D57 and the Weyl key increments
+// 0x9E3779B9 / 0xBB67AE85.  Stream layout of this library: key = (seed lo, seed hi),
+// counter = (v >> 2, b, (row << 4) | purpose, step lo), word v & 3.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace specv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegInf = -__builtin_huge_valf();
+// Largest Gumbel noise a 32-bit word can give is -ln(-ln(1 - 2^-24)) = 16.64; pruning
+// bounds use 17 so that rounding can never make a pruned element win.
+constexpr float kGumbelMax = 17.0f;
+
+enum RowKind : int { ROW_STATS = 0, ROW_BONUS = 1, ROW_ARGMAX = 2 };
+enum Purpose : uint32_t { PURPOSE_ACCEPT = 0, PURPOSE_RESIDUAL = 1, PURPOSE_BONUS = 2 };
+
+// One partial result per (warp, row segment).
+//   ROW_STATS : m = raw max (NaN-propagating), s = sum 2^(x*c - fl(m*c))
+//   ROW_ARGMAX: m = raw max, idx = lowest index holding it
+//   ROW_BONUS : m = raw max, best = max (x/T + g), idx = its lowest index
+struct __align__(16) Part {
+    float m;
+    float s;
+    float best;
+    int idx;
+};
+
+// ------------------------------------------------------------------ Philox
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t a = x.x, c = x.z;
+        const uint32_t hi_a = __umulhi(0xD2511F53u, a), lo_a = 0xD2511F53u * a;
+        const uint32_t hi_c = __umulhi(0xCD9E8D57u, c), lo_c = 0xCD9E8D57u * c;
+        x = make_uint4(hi_c ^ x.y ^ k0, lo_c, hi_a ^ x.w ^ k1, lo_a);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return x;
+}
+
+// The four words of the group holding vocabulary entries 4*grp .. 4*grp+3.
+__device__ __forceinline__ uint4 rand_group(uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
+                                            uint32_t purpose, uint32_t grp) {
+    return philox4x32_10(make_uint4(grp, b, (row << 4) | purpose, step), (uint32_t)seed,
+                         (uint32_t)(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &r, int k) {
+    return k == 0 ? r.x : (k == 1 ? r.y : (k == 2 ? r.z : r.w));
+}
+
+// u = (2 (w >> 9) + 1) 2^-24, exact in fp32; and 1 - u, also exact.
+__device__ __forceinline__ float u01(uint32_t w) {
+    return __uint2float_rn(((w >> 9) << 1) | 1u) * 5.9604644775390625e-8f;
+}
+__device__ __forceinline__ float one_minus_u01(uint32_t w) {
+    return __uint2float_rn(((0x7FFFFFu - (w >> 9)) << 1) | 1u) * 5.9604644775390625e-8f;
+}
+
+// Gumbel noise g = -log(-log u) from the word, accurate for u near 1 (where the
+// winners of a Gumbel-max draw come from): -log u = -log1p(-(1 - u)) with 1 - u exact.
+__device__ __noinline__ float gumbel_of_word(uint32_t w) {
+    const float e = -log1pf(-one_minus_u01(w));
+    return -logf(e);
+}
+
+// ------------------------------------------------------------------ loads
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float max_nan_f32(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ------------------------------------------------------------------ vector views
+// A "vector" is what one lane loads at a time: 16 bytes when rows are 16-byte
+// aligned, a single element otherwise.
+struct VecBF16 {
+    static constexpr int VE = 8;
+    static constexpr int ESIZE = 2;
+    uint4 v;
+    __device__ __forceinline__ static VecBF16 load(const void *row, int64_t vi) {
+        return {ld_stream_v4((const uint4 *)row + vi)};
+    }
+    __device__ __forceinline__ static VecBF16 neg_inf() {
+        return {make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)};
+    }
+    __device__ __forceinline__ float get(int e) const {
+        const uint32_t w = (e >> 1) == 0 ? v.x : ((e >> 1) == 1 ? v.y : ((e >> 1) == 2 ? v.z : v.w));
+        return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+    __device__ __forceinline__ float vmax() const {
+        const uint32_t m = max_nan_bf16x2(max_nan_bf16x2(v.x, v.y), max_nan_bf16x2(v.z, v.w));
+        return max_nan_f32(bf16_lo(m), bf16_hi(m));
+    }
+    // max over elements 4g .. 4g+3
+    __device__ __forceinline__ float gmax(int g) const {
+        const uint32_t m = g == 0 ? max_nan_bf16x2(v.x, v.y) : max_nan_bf16x2(v.z, v.w);
+        return max_nan_f32(bf16_lo(m), bf16_hi(m));
+    }
+};
+
+struct VecF32 {
+    static constexpr int VE = 4;
+    static constexpr int ESIZE = 4;
+    uint4 v;
+    __device__ __forceinline__ static VecF32 load(const void *row, int64_t vi) {
+        return {ld_stream_v4((const uint4 *)row + vi)};
+    }
+    __device__ __forceinline__ static VecF32 neg_inf() {
+        return {make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u)};
+    }
+    __device__ __forceinline__ float get(int e) const {
+        return __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w)));
+    }
+    __device__ __forceinline__ float vmax() const {
+        return max_nan_f32(max_nan_f32(get(0), get(1)), max_nan_f32(get(2), get(3)));
+    }
+    __device__ __forceinline__ float gmax(int) const { return vmax(); }
+};
+
+struct ScalarBF16 {
+    static constexpr int VE = 1;
+    static constexpr int ESIZE = 2;
+    float x;
+    __device__ __forceinline__ static ScalarBF16 load(const void *row, int64_t vi) {
+        return {__uint_as_float((uint32_t)__ldg((const unsigned short *)row + vi) << 16)};
+    }
+    __device__ __forceinline__ static ScalarBF16 neg_inf() { return {kNegInf}; }
+    __device__ __forceinline__ float get(int) const { return x; }
+    __device__ __forceinline__ float vmax() const { return x; }
+    __device__ __forceinline__ float gmax(int) const { return x; }
+};
+
+struct ScalarF32 {
+    static constexpr int VE = 1;
+    static constexpr int ESIZE = 4;
+    float x;
+    __device__ __forceinline__ static ScalarF32 load(const void *row, int64_t vi) {
+        return {__ldg((const float *)row + vi)};
+    }
+    __device__ __forceinline__ static ScalarF32 neg_inf() { return {kNegInf}; }
+    __device__ __forceinline__ float get(int) const { return x; }
+    __device__ __forceinline__ float vmax() const { return x; }
+    __device__ __forceinline__ float gmax(int) const { return x; }
+};
+
+// Scalar read of one logit (token gathers).
+__device__ __forceinline__ float load_logit(const void *base, int dtype, int64_t idx) {
+    if (dtype == 0) return __uint_as_float((uint32_t)__ldg((const unsigned short *)base + idx) << 16);
+    return __ldg((const float *)base + idx);
+}
+
+// ------------------------------------------------------------------ warp reductions
+__device__ __forceinline__ float warp_max_nan(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = max_nan_f32(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ double warp_sum_d(double x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ int warp_sum_i(int x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// (score, idx) argmax with the lowest idx on equal scores; idx < 0 means "none".
+__device__ __forceinline__ bool better(float s1, int i1, float s2, int i2) {
+    if (i2 < 0) return i1 >= 0;
+    if (i1 < 0) return false;
+    return s1 > s2 || (s1 == s2 && i1 < i2);
+}
+
+__device__ __forceinline__ void warp_argmax(float &s, int &i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+        if (better(s2, i2, s, i)) { s = s2; i = i2; }
+    }
+}
+
+// ------------------------------------------------------------------ work split
+// Flat element space of all needed rows (row r covers [r*V, (r+1)*V)) split into
+// equal contiguous ranges, one per warp, each a multiple of the vector width.
+constexpr int64_t kMinWarpRange = 2048;
+
+__host__ __device__ __forceinline__ int64_t warp_range(int64_t total, int64_t nwarps, int ve) {
+    int64_t p = (total + nwarps - 1) / nwarps;
+    if (p < kMinWarpRange) p = kMinWarpRange;
+    return (p + ve - 1) / ve * ve;
+}
+
+// Rows one warp range can touch, an upper bound.
+__host__ __device__ __forceinline__ int segs_per_warp(int64_t range, int V) {
+    return (int)((range - 1) / V) + 2;
+}
+
+}  // namespace specv
