@@ -35,7 +35,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["speculative_decoding_verification_15_gb300/csrc/verify.cu",
                   "speculative_decoding_verification_15_gb300/csrc/spec_common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "rows_kernel_main.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "main_kernel_main.md")
 
 
 def kernel_source_sha() -> str:
@@ -47,7 +47,7 @@ def kernel_source_sha() -> str:
 
 
 def measured_traffic() -> float | None:
-    """dram read+write bytes per rows_kernel launch from the committed ncu summary,
+    """dram read+write bytes per main_kernel launch from the committed ncu summary,
     if it was taken on the current kernel source."""
     try:
         text = open(TRAFFIC_FILE).read()
@@ -225,7 +225,8 @@ def run_ours(args) -> None:
     stream = torch.cuda.current_stream(dev)
     verified = B * K  # every request verifies all K drafts
     esz = t.element_size()
-    algo_bytes = B * (2 * K + 1) * V * esz  # one read of every needed logit row
+    algo_bytes = B * (2 * K + 1) * V * esz  # step: one read of every needed logit row
+    main_bytes = B * 2 * K * V * esz        # main_kernel: the target and draft rows of the drafts
 
     def step(i):
         binding.spec_verify_sample(t, d, x, None, T, 3, i, tokens, acc, pp, qq, st, ws, stream)
@@ -290,7 +291,7 @@ def run_ours(args) -> None:
 
     if rank == 0:
         peak, peak_kind = hbm_peak()
-        achieved = algo_bytes / (rows_ms * 1e-3) / 1e9
+        achieved = main_bytes / (rows_ms * 1e-3) / 1e9
         cpu = oracle_cpu_rate(batch, 3, min_seconds=2.0, max_reps=8) if world == 1 else None
         clocks = clk.summary()
         line = {
@@ -305,12 +306,13 @@ def run_ours(args) -> None:
                        "parallelism": f"replicas x{world}"},
             "emitted_tokens_per_s": world * emitted * args.steps / (total_ms * 1e-3),
             "step_hbm_gbs": algo_bytes / (total_ms / args.steps * 1e-3) / 1e9,
-            "kernel_ms": {"rows": per_kernel[0], "accept": per_kernel[1] if len(per_kernel) > 1 else None,
-                          "resid": per_kernel[2] if len(per_kernel) > 2 else None,
+            "kernel_ms": {"main": per_kernel[0], "accept": per_kernel[1] if len(per_kernel) > 1 else None,
+                          "tail": per_kernel[2] if len(per_kernel) > 2 else None,
                           "final": per_kernel[3] if len(per_kernel) > 3 else None},
-            "roofline": {"bound": "hbm", "kernel": "rows_kernel", "achieved": achieved, "peak": peak,
+            "roofline": {"bound": "hbm", "kernel": "main_kernel", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "algorithmic_bytes": algo_bytes, "traffic": measured_traffic()},
+                         "algorithmic_bytes": main_bytes, "traffic": measured_traffic()},
+            "step_algorithmic_bytes": algo_bytes,
             "e2e": {"value": world * verified / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": 4 * args.steps,

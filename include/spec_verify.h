@@ -31,7 +31,8 @@
  *    (ld_row >= V).  Target row (b, i), i = 0..Kmax, starts at element
  *    (b*(Kmax+1) + i) * ld_row; draft row (b, i), i = 0..Kmax-1, at
  *    (b*Kmax + i) * ld_row.  Requests verify k_b = num_draft[b] <= Kmax drafts;
- *    target rows i > k_b and draft rows i >= k_b are never read.
+ *    target rows i > k_b and draft rows i >= k_b are never read.  Logit pointers
+ *    must be aligned to their element size; rows need no further alignment.
  *  - Host-checkable argument errors return SPEC_EINVAL / SPEC_EWORKSPACE /
  *    SPEC_EUNSUPPORTED before anything is launched; a failed launch returns
  *    SPEC_ECUDA.  Data-dependent errors are reported per request in out_status.
@@ -65,8 +66,12 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
 #define SPEC_STATUS_BAD_TOKEN 1        /* a draft token x_i (i < k_b) is outside [0, V)          */
 #define SPEC_STATUS_BAD_K 2            /* num_draft[b] outside [0, Kmax]                          */
 #define SPEC_STATUS_BAD_TEMPERATURE 3  /* temperature[b] < 0, NaN or infinite                     */
-#define SPEC_STATUS_NONFINITE 4        /* a needed logit row holds NaN or +inf, or is all -inf    */
-/* A request with a non-zero status has out_accepted[b] = 0 and every token -1. */
+#define SPEC_STATUS_NONFINITE 4        /* a row that was read holds NaN or +inf, or is all -inf   */
+#define SPEC_STATUS_INTERNAL 5         /* a bounded internal wait gave up; results are not valid */
+/* Rows read: target and draft rows 0..k_b-1 (target only for greedy requests); the
+ * target row k_b only when every draft is accepted (it holds the bonus token).
+ * A request with a non-zero status has out_accepted[b] = 0, every token -1 and
+ * out_p / out_q -1. */
 
 /* Limits of this build. */
 #define SPEC_MAX_BATCH 8192        /* B                                   */

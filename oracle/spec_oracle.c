@@ -43,7 +43,7 @@
 #define ST_BAD_TOKEN 1
 #define ST_BAD_K 2
 #define ST_BAD_T 3
-#define ST_NONFINITE 4
+#define ST_NONFINITE 4 /* a row that is read holds NaN or +inf, or is all -inf */
 
 /* near-tie flag bits */
 #define FL_THRESH 1     /* |u - P/Q| < 1e-5 * P/Q at a scanned position            */
@@ -229,6 +229,20 @@ static void load_row(const void *base, int dtype, int64_t row, int64_t ld_row, i
     for (v = 0; v < V; ++v) dst[v] = decode(base, dtype, row * ld_row + v);
 }
 
+/* A request with a non-zero status emits nothing: accepted 0, tokens and p/q -1. */
+static void fail_request(const verify_args *a, int b, int status) {
+    int i;
+    for (i = 0; i <= a->Kmax; ++i) a->out_tokens[(int64_t)b * (a->Kmax + 1) + i] = -1;
+    for (i = 0; i < a->Kmax; ++i) {
+        if (a->out_p) a->out_p[(int64_t)b * a->Kmax + i] = -1.0;
+        if (a->out_q) a->out_q[(int64_t)b * a->Kmax + i] = -1.0;
+    }
+    a->out_status[b] = status;
+    a->out_accepted[b] = 0;
+    if (a->out_flags) a->out_flags[b] = 0;
+    if (a->out_gap) a->out_gap[b] = INFINITY;
+}
+
 static void verify_one(const verify_args *a, int b, double *xt, double *xd, double *lpt, double *lpd,
                        double *tmp) {
     const int K1 = a->Kmax + 1, V = a->V;
@@ -256,8 +270,10 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
         for (i = 0; i < kb; ++i)
             if (x[i] < 0 || x[i] >= V) status = ST_BAD_TOKEN;
     if (!status) {
-        /* needed rows: target 0..k_b, draft 0..k_b-1 (sampling only) */
-        for (i = 0; i <= kb && !status; ++i) {
+        /* rows of the draft positions: target 0..k_b-1, draft 0..k_b-1 (sampling only).
+         * Reading: the target row k_b is checked only when it is read, i.e. when every
+         * draft is accepted and the bonus (or greedy) token comes from it. */
+        for (i = 0; i < kb && !status; ++i) {
             load_row(a->target, a->dtype, (int64_t)b * K1 + i, a->ld_row, V, xt);
             if (!isfinite(row_max_nan(xt, V))) status = ST_NONFINITE;
         }
@@ -279,6 +295,10 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
         int y = 0;
         for (i = 0; i <= kb; ++i) {
             load_row(a->target, a->dtype, (int64_t)b * K1 + i, a->ld_row, V, xt);
+            if (i == kb && !isfinite(row_max_nan(xt, V))) {
+                fail_request(a, b, ST_NONFINITE);
+                return;
+            }
             y = argmax_lowest(xt, V);
             if (i == kb || y != x[i]) break;
             tok[i] = x[i];
@@ -357,6 +377,10 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
         double gap, top;
         int tk, sv;
         load_row(a->target, a->dtype, (int64_t)b * K1 + kb, a->ld_row, V, xt);
+        if (!isfinite(row_max_nan(xt, V))) {
+            fail_request(a, b, ST_NONFINITE);
+            return;
+        }
         oracle_row_logprobs(xt, V, T, lpt);
         tk = gumbel_argmax(lpt, V, a->seed, a->step, b, kb, 2, &gap, &top, &sv);
         if (gap < REL_TIE * (fabs(top) > 1.0 ? fabs(top) : 1.0)) flags |= FL_GUMBEL;

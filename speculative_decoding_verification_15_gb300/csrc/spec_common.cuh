@@ -103,8 +103,7 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ------------------------------------------------------------------ vector views
-// A "vector" is what one lane loads at a time: 16 bytes when rows are 16-byte
-// aligned, a single element otherwise.
+// A "vector" is 16 bytes of a row: 8 bf16 or 4 fp32 logits.
 struct VecBF16 {
     static constexpr int VE = 8;
     static constexpr int ESIZE = 2;
@@ -149,36 +148,103 @@ struct VecF32 {
     __device__ __forceinline__ float gmax(int) const { return vmax(); }
 };
 
-struct ScalarBF16 {
-    static constexpr int VE = 1;
-    static constexpr int ESIZE = 2;
-    float x;
-    __device__ __forceinline__ static ScalarBF16 load(const void *row, int64_t vi) {
-        return {__uint_as_float((uint32_t)__ldg((const unsigned short *)row + vi) << 16)};
-    }
-    __device__ __forceinline__ static ScalarBF16 neg_inf() { return {kNegInf}; }
-    __device__ __forceinline__ float get(int) const { return x; }
-    __device__ __forceinline__ float vmax() const { return x; }
-    __device__ __forceinline__ float gmax(int) const { return x; }
-};
-
-struct ScalarF32 {
-    static constexpr int VE = 1;
-    static constexpr int ESIZE = 4;
-    float x;
-    __device__ __forceinline__ static ScalarF32 load(const void *row, int64_t vi) {
-        return {__ldg((const float *)row + vi)};
-    }
-    __device__ __forceinline__ static ScalarF32 neg_inf() { return {kNegInf}; }
-    __device__ __forceinline__ float get(int) const { return x; }
-    __device__ __forceinline__ float vmax() const { return x; }
-    __device__ __forceinline__ float gmax(int) const { return x; }
-};
-
 // Scalar read of one logit (token gathers).
 __device__ __forceinline__ float load_logit(const void *base, int dtype, int64_t idx) {
     if (dtype == 0) return __uint_as_float((uint32_t)__ldg((const unsigned short *)base + idx) << 16);
     return __ldg((const float *)base + idx);
+}
+
+// ------------------------------------------------------------------ async copies
+// Bulk (TMA) copies global -> shared, completed on an mbarrier, and bounded waits.
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps in
+// the barrier (up to the hint, in ns) instead of spinning and taking issue slots
+// from the warps that compute.
+constexpr uint32_t kSuspendHintNs = 100000;
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+// cp.async.bulk: `bytes` (multiple of 16) from 16-byte aligned global to shared memory.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// launch early, and wait for the previous kernel's results.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_addr(p)));
+    return r;
+}
+
+// Packed fp32 pair arithmetic (sm_100 family): two lanes of work per instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&d);
 }
 
 // ------------------------------------------------------------------ warp reductions
@@ -220,22 +286,6 @@ __device__ __forceinline__ void warp_argmax(float &s, int &i) {
         const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
         if (better(s2, i2, s, i)) { s = s2; i = i2; }
     }
-}
-
-// ------------------------------------------------------------------ work split
-// Flat element space of all needed rows (row r covers [r*V, (r+1)*V)) split into
-// equal contiguous ranges, one per warp, each a multiple of the vector width.
-constexpr int64_t kMinWarpRange = 2048;
-
-__host__ __device__ __forceinline__ int64_t warp_range(int64_t total, int64_t nwarps, int ve) {
-    int64_t p = (total + nwarps - 1) / nwarps;
-    if (p < kMinWarpRange) p = kMinWarpRange;
-    return (p + ve - 1) / ve * ve;
-}
-
-// Rows one warp range can touch, an upper bound.
-__host__ __device__ __forceinline__ int segs_per_warp(int64_t range, int V) {
-    return (int)((range - 1) / V) + 2;
 }
 
 }  // namespace specv

@@ -9,22 +9,23 @@
 //    committed plus one token (correction, or bonus from the row after the drafts).
 //  * "Bringing DSpark to vLLM Metal" -- greedy path: target argmax vs draft token.
 //
-// Kernels per call (fixed grids, no host synchronisation, so a call can be captured
-// in a CUDA graph):
-//  rows_kernel    one streaming pass over every needed logit row, split into equal
-//                 contiguous per-warp ranges of the flattened rows.  Per segment:
-//                 softmax statistics (max and sum of 2^(x*log2e/T - max')) for the
-//                 target and draft rows of the draft positions, the Gumbel-max bonus
-//                 draw on the target row after the last draft, or the raw argmax of
-//                 greedy requests.  This is the HBM-bound kernel.
-//  accept_kernel  one warp per request: combines the segments, sets the status,
-//                 computes p(x_i) and q(x_i), runs the acceptance scan, emits the
-//                 accepted drafts and the bonus / greedy token, and queues a
-//                 correction job at the first rejection.
-//  resid_kernel   second streaming pass, over the target row of each queued job:
-//                 Gumbel-max over log(max(0, p - q)); draft values are gathered only
-//                 at the few entries that can still win.
-//  final_kernel   one warp per job: combines the residual segments into the token.
+// Kernels per call (fixed grids, no host synchronisation; each launch after the
+// first is a programmatic dependent launch):
+//  main_kernel    streams the rows of every draft position once -- target and draft
+//                 rows of sampling requests, target rows of greedy ones -- through a
+//                 bulk-copy (TMA) ring in shared memory: one persistent CTA per SM, a
+//                 producer warp issuing 16 KB cp.async.bulk copies, eight consumer
+//                 warps reducing them.  Per (CTA, row, warp): max, sum of
+//                 2^(x log2e / T - max'), and the lowest argmax.  HBM-bound.
+//  accept_kernel  one CTA per request: combines the partials of its rows, sets the
+//                 status, computes p(x_i) and q(x_i), runs the acceptance scan,
+//                 emits the accepted drafts, and queues one job: the correction at
+//                 the first rejected row j (seeded with the segment argmaxes of row
+//                 j), the bonus draw on row k_b, or the greedy argmax of row k_b.
+//  tail_kernel    streams the one row of each job through the same ring: Gumbel-max
+//                 over log(max(0, p - q)) (draft values gathered only at entries
+//                 that can still win), Gumbel-max over the target row, or argmax.
+//  final_kernel   one warp per job: combines the tail partials into the token.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -38,283 +39,256 @@ using namespace specv;
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarpsPerBlock = kThreads / 32;
-constexpr int kBlocksPerSM = 4;
-constexpr int kBatch = 4;  // vectors each lane loads before reducing them
+// ------------------------------------------------------------------ configuration
+constexpr int kCW = 16;                          // consumer warps per CTA (4 per scheduler)
+constexpr int kCT = kCW * 32;                    // consumer threads
+constexpr int kPipeThreads = kCT + 32;           // + one producer warp
+constexpr int kMaxStages = 8;                    // ring depth: as many as shared memory allows
+constexpr int kStageBytes = 32768;               // one chunk (plus alignment slack)
+constexpr int kChunkMaxBytes = kStageBytes - 32; // payload; an aligned superset fits a stage
+constexpr int kVPT = kStageBytes / 16 / kCT;     // 16-byte vectors per consumer thread (4)
+constexpr size_t kSmemBudget = 226 * 1024;       // dynamic shared memory per CTA (227 KB minus static)
+constexpr uint64_t kWaitNs = 2000000000ull;      // bound on every mbarrier wait (2 s)
+constexpr int kAcceptThreads = 256;
+constexpr int kFinalThreads = 256;
+constexpr int kMaxRowsPerRequest = 2 * SPEC_MAX_DRAFTS;
+constexpr int kMaxDesc = 512;                    // per-CTA row descriptors kept in smem
 
-struct ResJob {
-    int b, j;
-    float invT, Ct, Cd;
-    int pad[3];
+enum JobKind : int { JOB_RESID = 0, JOB_BONUS = 1, JOB_ARGMAX = 2 };
+
+struct Part {
+    float m;     // raw max of the segment (NaN-propagating)
+    float s;     // main pass: sum 2^(x c - fl(m c)); unused in the tail pass
+    int idx;     // lowest index of the max (main pass, argmax jobs) or of the best score
+    float best;  // tail pass: best Gumbel score
 };
 
-// =================================================================== segments
+struct Job {
+    int b, row, kind;
+    float invT, Ct, Cd;  // log p_v = x_v invT - Ct, log q_v = y_v invT - Cd (correction)
+    float seed_best;     // exact score of the best candidate found by accept_kernel
+    int seed_idx;
+};
+
+struct Ctrl {
+    int err;        // non-zero: a bounded wait gave up
+    int job_count;  // jobs queued by accept_kernel
+};
+
+// ------------------------------------------------------------------ chunking
+// Rows are cut into cpr chunks of ce elements (ce a multiple of 8, at most
+// kChunkMaxBytes); the flattened chunk list of all rows is split into G equal
+// contiguous ranges, one per CTA.
+struct Chunking {
+    int cpr, ce;
+};
+
+__host__ __device__ inline Chunking make_chunking(int V, int esz) {
+    const int max_e = kChunkMaxBytes / esz;
+    int cpr = (V + max_e - 1) / max_e;
+    int ce = (V + cpr - 1) / cpr;
+    ce = (ce + 7) & ~7;
+    cpr = (V + ce - 1) / ce;
+    return {cpr, ce};
+}
+
+__host__ __device__ inline int64_t cta_first(int64_t total, int G, int i) { return total * i / G; }
+__host__ __device__ inline int cta_of(int64_t total, int G, int64_t c) { return (int)(((c + 1) * G - 1) / total); }
+
+// Rows one CTA can touch, an upper bound.
+__host__ inline int segs_per_cta(int64_t total_max, int G, int cpr) {
+    const int64_t per = (total_max + G - 1) / G;
+    return (int)((per + cpr - 1) / cpr) + 1;
+}
+
+__device__ __forceinline__ int64_t part_slot(int cta, int nseg, int seg, int warp) {
+    return ((int64_t)cta * nseg + seg) * kCW + warp;
+}
+
+// Global byte window of chunk k of a row: the 16-byte aligned superset [a0, a1) of
+// elements [e0, e1); smem element 0 is global element e0 - shift.
+struct ChunkWin {
+    const char *a0;
+    uint32_t bytes;
+    int e0, e1, shift;
+};
+
+__device__ __forceinline__ ChunkWin chunk_window(const char *row, int esz, int V, const Chunking &ck, int k) {
+    ChunkWin w;
+    w.e0 = k * ck.ce;
+    w.e1 = min(w.e0 + ck.ce, V);
+    const uintptr_t g0 = (uintptr_t)(row + (int64_t)w.e0 * esz);
+    const uintptr_t g1 = (uintptr_t)(row + (int64_t)w.e1 * esz);
+    const uintptr_t a0 = g0 & ~(uintptr_t)15, a1 = (g1 + 15) & ~(uintptr_t)15;
+    w.a0 = (const char *)a0;
+    w.bytes = (uint32_t)(a1 - a0);
+    w.shift = (int)((g0 - a0) / esz);
+    return w;
+}
+
+// ------------------------------------------------------------------ vectors from smem
 template <class Vec>
-__device__ __forceinline__ void load_batch(Vec (&d)[kBatch], const void *row, int64_t b0, int64_t vend) {
-    const int lane = threadIdx.x & 31;
+__device__ __forceinline__ void mask_vec(Vec &d, int64_t first, int e0, int e1);
+
+template <>
+__device__ __forceinline__ void mask_vec<VecBF16>(VecBF16 &d, int64_t first, int e0, int e1) {
+    uint32_t w[4] = {d.v.x, d.v.y, d.v.z, d.v.w};
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-        const int64_t vi = b0 + lane + 32 * u;
-        d[u] = vi < vend ? Vec::load(row, vi) : Vec::neg_inf();
+    for (int e = 0; e < 8; ++e) {
+        const int64_t g = first + e;
+        if (g < e0 || g >= e1) w[e >> 1] = (e & 1) ? ((w[e >> 1] & 0x0000FFFFu) | 0xFF800000u)
+                                                   : ((w[e >> 1] & 0xFFFF0000u) | 0x0000FF80u);
+    }
+    d.v = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <>
+__device__ __forceinline__ void mask_vec<VecF32>(VecF32 &d, int64_t first, int e0, int e1) {
+    uint32_t w[4] = {d.v.x, d.v.y, d.v.z, d.v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int64_t g = first + e;
+        if (g < e0 || g >= e1) w[e] = 0xFF800000u;
+    }
+    d.v = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Loads this consumer thread's vectors of a staged chunk; out-of-window entries -inf.
+// Vector t of thread ct holds global elements ebase + (ct + kCT t) VE + e.
+template <class Vec>
+__device__ __forceinline__ void load_chunk(Vec (&d)[kVPT], const char *stage, const ChunkWin &w, int ct) {
+    const int nvec = (int)(w.bytes >> 4);
+    const int64_t ebase = (int64_t)w.e0 - w.shift;
+#pragma unroll
+    for (int t = 0; t < kVPT; ++t) {
+        const int j = ct + kCT * t;
+        if (j < nvec) {
+            d[t].v = lds128(stage + 16 * j);
+            if (j == 0 || j == nvec - 1) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, w.e0, w.e1);
+        } else {
+            d[t] = Vec::neg_inf();
+        }
     }
 }
 
 template <class Vec>
-__device__ __forceinline__ float batch_max(const Vec (&d)[kBatch]) {
+__device__ __forceinline__ float chunk_max(const Vec (&d)[kVPT]) {
     float tm = d[0].vmax();
 #pragma unroll
-    for (int u = 1; u < kBatch; ++u) tm = max_nan_f32(tm, d[u].vmax());
+    for (int t = 1; t < kVPT; ++t) tm = max_nan_f32(tm, d[t].vmax());
     return tm;
 }
 
-// first (lowest-index) element of this lane's batch equal to x, or -1
 template <class Vec>
-__device__ __forceinline__ int batch_find(const Vec (&d)[kBatch], int64_t b0, float x) {
-    const int lane = threadIdx.x & 31;
+__device__ __forceinline__ int chunk_find(const Vec (&d)[kVPT], int64_t ebase, int ct, float x) {
     int found = -1;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u)
+    for (int t = 0; t < kVPT; ++t)
 #pragma unroll
         for (int e = 0; e < Vec::VE; ++e)
-            if (found < 0 && d[u].get(e) == x) found = (int)((b0 + lane + 32 * u) * Vec::VE + e);
+            if (found < 0 && d[t].get(e) == x) found = (int)(ebase + (int64_t)(ct + kCT * t) * Vec::VE + e);
     return found;
 }
 
-// Softmax statistics of a row segment: m = max x (NaN-propagating), and
-// s = sum_v 2^(x_v c - fl(m c)) with c = log2(e) / T.
+// sum_e 2^(x_e c - ms) over the thread's vectors, two lanes per instruction
 template <class Vec>
-__device__ Part seg_stats(const void *row, int64_t vb, int64_t vend, float c) {
-    float m = kNegInf, mc = 0.f, s = 0.f;
-    for (int64_t b0 = vb; b0 < vend; b0 += 32 * kBatch) {
-        Vec d[kBatch];
-        load_batch(d, row, b0, vend);
-        const float tm = batch_max(d);
-        if (!(tm <= m)) {  // new maximum, or NaN
-            const float mcn = tm * c;
-            s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
-            m = tm;
-            mc = mcn;
-        }
-        const float ms = (m == kNegInf) ? 0.f : mc;
-        float acc = 0.f;
+__device__ __forceinline__ float chunk_expsum(const Vec (&d)[kVPT], float c, float ms) {
+    const float2 cc = make_float2(c, c), mm = make_float2(-ms, -ms);
+    float2 acc[Vec::VE / 2];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            float t = 0.f;
+    for (int e = 0; e < Vec::VE / 2; ++e) acc[e] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < Vec::VE; ++e) t += ex2_approx(fmaf(d[u].get(e), c, -ms));
-            acc += t;
+    for (int t = 0; t < kVPT; ++t)
+#pragma unroll
+        for (int e = 0; e < Vec::VE; e += 2) {
+            const float2 y = ffma2(make_float2(d[t].get(e), d[t].get(e + 1)), cc, mm);
+            acc[e / 2] = fadd2(acc[e / 2], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
         }
-        s += acc;
-    }
-    const float M = warp_max_nan(m);
-    const float MC = M * c;
-    const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - MC);
-    Part p;
-    p.m = M;
-    p.s = (float)warp_sum_d((double)sc);
-    p.best = 0.f;
-    p.idx = -1;
-    return p;
+#pragma unroll
+    for (int e = 1; e < Vec::VE / 2; ++e) acc[0] = fadd2(acc[0], acc[e]);
+    return acc[0].x + acc[0].y;
 }
 
-// Raw argmax of a row segment, lowest index on ties; m = NaN if any NaN.
-template <class Vec>
-__device__ Part seg_argmax(const void *row, int64_t vb, int64_t vend) {
-    float m = kNegInf;
-    int idx = -1;
-    bool nan_seen = false;
-    for (int64_t b0 = vb; b0 < vend; b0 += 32 * kBatch) {
-        Vec d[kBatch];
-        load_batch(d, row, b0, vend);
-        const float tm = batch_max(d);
-        if (tm != tm) {
-            nan_seen = true;
-        } else if (tm > m) {
-            idx = batch_find(d, b0, tm);
-            m = tm;
-        }
-    }
-    const bool any_nan = __any_sync(0xffffffffu, nan_seen);
-    warp_argmax(m, idx);
-    Part p;
-    p.m = any_nan ? __int_as_float(0x7fc00000) : m;
-    p.s = 0.f;
-    p.best = 0.f;
-    p.idx = idx;
-    return p;
-}
-
-// Gumbel-max over z_v + g_v, z = x / T, on the target row after the last draft.
-// The argmax is exact: an entry is skipped only when it provably cannot reach the
-// best score this warp has already seen, either because z + 17 < best (no 32-bit
-// word gives more than 16.64 of noise) or because 1 - u > 1.001 exp(z - best)
-// (then -log u >= 1 - u makes g < best - z).
-template <class Vec>
-__device__ Part seg_bonus(const void *row, int64_t vb, int64_t vend, float invT, uint64_t seed,
-                          uint32_t step, uint32_t b, uint32_t rowid) {
-    float m = kNegInf, best = kNegInf, thr = kNegInf;
-    int bidx = -1;
-    bool seeded = false;
-    for (int64_t b0 = vb; b0 < vend; b0 += 32 * kBatch) {
-        Vec d[kBatch];
-        load_batch(d, row, b0, vend);
-        const float tm = batch_max(d);
-        m = max_nan_f32(m, tm);
-        if (!seeded) {  // seed the bound with each lane's largest entry
-            seeded = true;
-            if (tm == tm && tm > kNegInf) {
-                const int v = batch_find(d, b0, tm);
-                const uint4 r4 = rand_group(seed, step, b, rowid, PURPOSE_BONUS, (uint32_t)v >> 2);
-                best = tm * invT + gumbel_of_word(word_of(r4, v & 3));
-                bidx = v;
-            }
-            thr = warp_max(best);
-        }
-        if (tm * invT + kGumbelMax >= thr) {
-            const int lane = threadIdx.x & 31;
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int64_t vi = b0 + lane + 32 * u;
-                if (vi >= vend) continue;
-#pragma unroll
-                for (int g = 0; g < (Vec::VE + 3) / 4; ++g) {
-                    if (!(d[u].gmax(g) * invT + kGumbelMax >= thr)) continue;
-                    const int64_t v0 = vi * Vec::VE + 4 * g;
-                    const uint4 r4 = rand_group(seed, step, b, rowid, PURPOSE_BONUS, (uint32_t)(v0 >> 2));
-#pragma unroll
-                    for (int k = 0; k < (Vec::VE < 4 ? Vec::VE : 4); ++k) {
-                        const int v = (int)(v0 + k);
-                        const float z = d[u].get(4 * g + k) * invT;
-                        const uint32_t w = word_of(r4, v & 3);
-                        const float lim = ex2_approx((z - thr) * kLog2e) * 1.001f;
-                        if (one_minus_u01(w) <= lim) {
-                            const float sc = z + gumbel_of_word(w);
-                            if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
-                        }
-                    }
-                }
-            }
-        }
-        thr = warp_max(best);
-    }
-    m = warp_max_nan(m);
-    warp_argmax(best, bidx);
-    Part p;
-    p.m = m;
-    p.s = 0.f;
-    p.best = best;
-    p.idx = bidx;
-    return p;
-}
-
-// Correction draw at the first rejected row j: argmax over {v : p_v > q_v} of
-// log(p_v - q_v) + g_v, with log p_v = x_v / T - Ct and log q_v = y_v / T - Cd.
-// Same exact pruning as seg_bonus, using log(p - q) <= log p; the draft row is read
-// only at the entries that survive it.
-template <class Vec>
-__device__ Part seg_residual(const void *trow, const void *drow, int dtype, int64_t vb, int64_t vend,
-                             float invT, float Ct, float Cd, uint64_t seed, uint32_t step, uint32_t b,
-                             uint32_t rowid) {
-    float best = kNegInf, thr = kNegInf;
-    int bidx = -1;
-    bool seeded = false;
-    for (int64_t b0 = vb; b0 < vend; b0 += 32 * kBatch) {
-        Vec d[kBatch];
-        load_batch(d, trow, b0, vend);
-        const float tm = batch_max(d);
-        if (!seeded) {
-            seeded = true;
-            if (tm > kNegInf) {
-                const int v = batch_find(d, b0, tm);
-                const float lp = fmaf(tm, invT, -Ct);
-                const float lq = fmaf(load_logit(drow, dtype, v), invT, -Cd);
-                if (lq < lp) {
-                    const uint4 r4 = rand_group(seed, step, b, rowid, PURPOSE_RESIDUAL, (uint32_t)v >> 2);
-                    best = lp + logf(-expm1f(lq - lp)) + gumbel_of_word(word_of(r4, v & 3));
-                    bidx = v;
-                }
-            }
-            thr = warp_max(best);
-        }
-        if (fmaf(tm, invT, -Ct) + kGumbelMax >= thr) {
-            const int lane = threadIdx.x & 31;
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int64_t vi = b0 + lane + 32 * u;
-                if (vi >= vend) continue;
-#pragma unroll
-                for (int g = 0; g < (Vec::VE + 3) / 4; ++g) {
-                    if (!(fmaf(d[u].gmax(g), invT, -Ct) + kGumbelMax >= thr)) continue;
-                    const int64_t v0 = vi * Vec::VE + 4 * g;
-                    const uint4 r4 = rand_group(seed, step, b, rowid, PURPOSE_RESIDUAL, (uint32_t)(v0 >> 2));
-#pragma unroll
-                    for (int k = 0; k < (Vec::VE < 4 ? Vec::VE : 4); ++k) {
-                        const int v = (int)(v0 + k);
-                        const float lp = fmaf(d[u].get(4 * g + k), invT, -Ct);
-                        const uint32_t w = word_of(r4, v & 3);
-                        const float lim = ex2_approx((lp - thr) * kLog2e) * 1.001f;
-                        if (one_minus_u01(w) <= lim) {
-                            const float lq = fmaf(load_logit(drow, dtype, v), invT, -Cd);
-                            if (lq < lp) {
-                                const float sc = lp + logf(-expm1f(lq - lp)) + gumbel_of_word(w);
-                                if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
-                            }
-                        }
-                    }
-                }
-            }
-        }
-        thr = warp_max(best);
-    }
-    warp_argmax(best, bidx);
-    Part p;
-    p.m = 0.f;
-    p.s = 0.f;
-    p.best = best;
-    p.idx = bidx;
-    return p;
-}
-
-// =================================================================== rows_kernel
-struct RowsParams {
-    const void *target;
-    const void *draft;
-    int64_t ld_row;
-    int B, Kmax, V;
-    const int32_t *num_draft;
-    const float *temperature;  // NULL: every request greedy
-    uint64_t seed;
-    uint32_t step;
-    int *row_start;  // [B+1], written by block 0 for accept_kernel
-    Part *parts;     // [warps * nseg]
-    int nseg;
-    int *job_count;  // reset by block 0
+// ------------------------------------------------------------------ ring
+struct Ring {
+    char *stages;
+    uint64_t *full;
+    uint64_t *empty;
+    int n;  // stages
 };
 
-__device__ __forceinline__ int request_rows(const int32_t *num_draft, const float *temperature, int Kmax,
-                                            int b) {
+__host__ __device__ constexpr size_t ring_bytes(int n) {
+    return (size_t)n * kStageBytes + 2 * (size_t)kMaxStages * sizeof(uint64_t);
+}
+
+__device__ __forceinline__ Ring ring_at(unsigned char *smem, int n) {
+    Ring r;
+    r.stages = (char *)smem;
+    r.full = (uint64_t *)(smem + (size_t)n * kStageBytes);
+    r.empty = r.full + kMaxStages;
+    r.n = n;
+    return r;
+}
+
+__device__ __forceinline__ void ring_init(const Ring &r) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < r.n; ++s) {
+            mbar_init(&r.full[s], 1);
+            mbar_init(&r.empty[s], kCW);
+        }
+        mbar_init_fence();
+    }
+}
+
+// Producer (one thread): stage chunks c0 .. c1-1; window(c) gives the source.
+template <class Window>
+__device__ void ring_produce(const Ring &r, int64_t c0, int64_t c1, Window window, int *err) {
+    int s = 0;
+    uint32_t ph = 0;
+    for (int64_t c = c0; c < c1; ++c) {
+        if (!mbar_wait(&r.empty[s], ph ^ 1u, kWaitNs)) {
+            atomicOr(err, 1);
+            // wait (bounded) for the copies this thread still has in flight
+            const int64_t issued = c - c0;
+            for (int64_t back = 1; back <= r.n && issued - back >= 0; ++back) {
+                const int64_t i2 = issued - back;
+                mbar_wait(&r.full[i2 % r.n], (uint32_t)(i2 / r.n) & 1u, kWaitNs);
+            }
+            return;
+        }
+        const ChunkWin w = window(c);
+        mbar_arrive_expect_tx(&r.full[s], w.bytes);
+        bulk_g2s(r.stages + (size_t)s * kStageBytes, w.a0, w.bytes, &r.full[s]);
+        if (++s == r.n) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ per-request rows
+__device__ __forceinline__ int request_main_rows(const int32_t *num_draft, const float *temperature, int Kmax,
+                                                 int b) {
     const int kb = num_draft ? num_draft[b] : Kmax;
     if (kb < 0 || kb > Kmax) return 0;
     if (temperature) {
         const float T = temperature[b];
         if (!(T >= 0.f) || isinf(T)) return 0;
-        return T == 0.f ? kb + 1 : 2 * kb + 1;
+        return T == 0.f ? kb : 2 * kb;
     }
-    return kb + 1;
+    return kb;
 }
 
-// s[b] = number of needed rows of requests 0..b-1 (s[B] = total), in shared memory.
-// Row order inside a request: sampling [target 0..k-1 | target k | draft 0..k-1],
-// greedy [target 0..k].
-__device__ void scan_request_rows(int *s, int B, const int32_t *num_draft, const float *temperature,
-                                  int Kmax) {
-    __shared__ int warp_tot[kWarpsPerBlock];
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int per = (B + kThreads - 1) / kThreads;
+// s[b] = main-pass rows of requests 0..b-1 (s[B] = total), in shared memory.
+// Row order inside a request: sampling [target 0..k-1 | draft 0..k-1], greedy
+// [target 0..k-1].
+__device__ void scan_request_rows(int *s, int B, const int32_t *num_draft, const float *temperature, int Kmax) {
+    __shared__ int warp_tot[32];
+    const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int per = (B + nthr - 1) / nthr;
     const int lo = min(tid * per, B), hi = min(lo + per, B);
     int local = 0;
-    for (int i = lo; i < hi; ++i) local += request_rows(num_draft, temperature, Kmax, i);
+    for (int i = lo; i < hi; ++i) local += request_main_rows(num_draft, temperature, Kmax, i);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -328,9 +302,9 @@ __device__ void scan_request_rows(int *s, int B, const int32_t *num_draft, const
     int run = wbase + incl - local;
     for (int i = lo; i < hi; ++i) {
         s[i] = run;
-        run += request_rows(num_draft, temperature, Kmax, i);
+        run += request_main_rows(num_draft, temperature, Kmax, i);
     }
-    if (tid == kThreads - 1) s[B] = wbase + incl;
+    if (tid == nthr - 1) s[B] = wbase + incl;
     __syncthreads();
 }
 
@@ -343,98 +317,200 @@ __device__ __forceinline__ int find_request(const int *rs, int B, int r) {
     return lo;
 }
 
+// =================================================================== main_kernel
+struct MainParams {
+    const void *target;
+    const void *draft;
+    int64_t ld_row;
+    int B, Kmax, V;
+    const int32_t *num_draft;
+    const float *temperature;  // NULL: every request greedy
+    int *row_start;            // [B+1], written by block 0 for accept_kernel
+    Part *parts;
+    int nseg;
+    int stages;
+    Ctrl *ctrl;
+};
+
+struct MainRow {
+    const char *ptr;
+    float c;      // log2(e) / T, or 0 for a greedy row
+};
+
 template <class Vec>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSM) rows_kernel(RowsParams p) {
-    extern __shared__ int s_rs[];
-    scan_request_rows(s_rs, p.B, p.num_draft, p.temperature, p.Kmax);
-    if (blockIdx.x == 0) {
-        for (int i = threadIdx.x; i <= p.B; i += kThreads) p.row_start[i] = s_rs[i];
-        if (threadIdx.x == 0) *p.job_count = 0;
+__device__ __forceinline__ MainRow main_row(const MainParams &p, const int *rs, int r) {
+    const int b = find_request(rs, p.B, r);
+    const int local = r - rs[b];
+    const int kb = p.num_draft ? p.num_draft[b] : p.Kmax;
+    const float T = p.temperature ? p.temperature[b] : 0.f;
+    const int64_t rowbytes = p.ld_row * Vec::ESIZE;
+    MainRow m;
+    if (T == 0.f || local < kb) {
+        m.ptr = (const char *)p.target + ((int64_t)b * (p.Kmax + 1) + local) * rowbytes;
+    } else {
+        m.ptr = (const char *)p.draft + ((int64_t)b * p.Kmax + (local - kb)) * rowbytes;
     }
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerBlock;
-    const int64_t w = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    const int64_t V = p.V;
-    const int64_t total = (int64_t)s_rs[p.B] * V;
-    const int64_t range = warp_range(total, nwarps, Vec::VE);
-    const int64_t f1 = min(w * range + range, total);
-    const int64_t esz = Vec::ESIZE;
-    int seg = 0;
-    for (int64_t f = w * range; f < f1; ++seg) {
-        const int r = (int)(f / V);
-        const int64_t rowbase = (int64_t)r * V;
-        const int64_t v1 = min(f1 - rowbase, V);
-        const int64_t vb = (f - rowbase) / Vec::VE, ve = v1 / Vec::VE;
-        const int b = find_request(s_rs, p.B, r);
-        const int local = r - s_rs[b];
-        const int kb = p.num_draft ? p.num_draft[b] : p.Kmax;
-        const float T = p.temperature ? p.temperature[b] : 0.f;
-        const char *tb = (const char *)p.target + (int64_t)b * (p.Kmax + 1) * p.ld_row * esz;
-        Part part;
-        if (T == 0.f) {
-            part = seg_argmax<Vec>(tb + local * p.ld_row * esz, vb, ve);
-        } else if (local < kb) {
-            part = seg_stats<Vec>(tb + local * p.ld_row * esz, vb, ve, __fdiv_rn(kLog2e, T));
-        } else if (local == kb) {
-            part = seg_bonus<Vec>(tb + (int64_t)kb * p.ld_row * esz, vb, ve, __fdiv_rn(1.f, T), p.seed,
-                                  p.step, (uint32_t)b, (uint32_t)kb);
-        } else {
-            const char *drow = (const char *)p.draft +
-                               ((int64_t)b * p.Kmax + (local - kb - 1)) * p.ld_row * esz;
-            part = seg_stats<Vec>(drow, vb, ve, __fdiv_rn(kLog2e, T));
+    m.c = T == 0.f ? 0.f : __fdiv_rn(kLog2e, T);
+    return m;
+}
+
+template <class Vec>
+__global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Ring ring = ring_at(smem, p.stages);
+    int *s_rs = (int *)(smem + ring_bytes(p.stages));
+    MainRow *s_desc = (MainRow *)(smem + ring_bytes(p.stages) + sizeof(int) * (size_t)(((p.B + 1) + 3) & ~3));
+    ring_init(ring);
+    scan_request_rows(s_rs, p.B, p.num_draft, p.temperature, p.Kmax);  // ends with __syncthreads
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.row_start[i] = s_rs[i];
+    pdl_launch_dependents();
+
+    const Chunking ck = make_chunking(p.V, Vec::ESIZE);
+    const int G = gridDim.x;
+    const int64_t total = (int64_t)s_rs[p.B] * ck.cpr;
+    if (total == 0) return;
+    const int64_t c0 = cta_first(total, G, blockIdx.x), c1 = cta_first(total, G, blockIdx.x + 1);
+    if (c0 == c1) return;
+    const int first_row = (int)(c0 / ck.cpr);
+    const int nrows = (int)((c1 - 1) / ck.cpr) - first_row + 1;
+    const bool table = nrows <= kMaxDesc;
+    if (table)
+        for (int i = threadIdx.x; i < nrows; i += blockDim.x) s_desc[i] = main_row<Vec>(p, s_rs, first_row + i);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k0 = (int)(c0 - (int64_t)first_row * ck.cpr);
+
+    if (warp == kCW) {  // producer
+        if (lane == 0) {
+            int r = first_row, k = k0;
+            MainRow mr = table ? s_desc[0] : main_row<Vec>(p, s_rs, r);
+            ring_produce(ring, c0, c1, [&](int64_t) {
+                const ChunkWin w = chunk_window(mr.ptr, Vec::ESIZE, p.V, ck, k);
+                if (++k == ck.cpr) {
+                    k = 0;
+                    ++r;
+                    if (r < first_row + nrows) mr = table ? s_desc[r - first_row] : main_row<Vec>(p, s_rs, r);
+                }
+                return w;
+            }, &p.ctrl->err);
         }
-        if (lane == 0 && seg < p.nseg) p.parts[w * p.nseg + seg] = part;
-        f = rowbase + v1;
+        return;
+    }
+
+    const int ct = threadIdx.x;  // consumer thread 0 .. kCT-1
+    int r = first_row, k = k0;
+    MainRow mr = table ? s_desc[0] : main_row<Vec>(p, s_rs, r);
+    float m = kNegInf, mc = 0.f, s = 0.f;
+    int aidx = -1;
+    bool nan_seen = false;
+    auto flush = [&]() {
+        Part out;
+        if (mr.c != 0.f) {
+            const float M = warp_max_nan(m);
+            const float MC = M * mr.c;
+            const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - MC);
+            out.s = (float)warp_sum_d((double)sc);
+            float mm = m;
+            int ii = aidx;
+            warp_argmax(mm, ii);
+            out.m = M;
+            out.idx = ii;
+        } else {
+            const bool any_nan = __any_sync(0xffffffffu, nan_seen);
+            float mm = m;
+            int ii = aidx;
+            warp_argmax(mm, ii);
+            out.m = any_nan ? __int_as_float(0x7fc00000) : mm;
+            out.s = 0.f;
+            out.idx = ii;
+        }
+        out.best = 0.f;
+        if (lane == 0) p.parts[part_slot(blockIdx.x, p.nseg, r - first_row, warp)] = out;
+    };
+
+    int st = 0;
+    uint32_t ph = 0;
+    for (int64_t cc = c0; cc < c1; ++cc) {
+        if (!mbar_wait(&ring.full[st], ph, kWaitNs)) {
+            atomicOr(&p.ctrl->err, 2);
+            break;
+        }
+        const ChunkWin w = chunk_window(mr.ptr, Vec::ESIZE, p.V, ck, k);
+        Vec d[kVPT];
+        load_chunk(d, ring.stages + (size_t)st * kStageBytes, w, ct);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[st]);
+        if (++st == ring.n) {
+            st = 0;
+            ph ^= 1u;
+        }
+        const int64_t ebase = (int64_t)w.e0 - w.shift;
+        const float tm = chunk_max(d);
+        if (mr.c != 0.f) {
+            if (!(tm <= m)) {  // new maximum, or NaN
+                const float mcn = tm * mr.c;
+                s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
+                m = tm;
+                mc = mcn;
+                aidx = chunk_find(d, ebase, ct, tm);
+            }
+            s += chunk_expsum(d, mr.c, m == kNegInf ? 0.f : mc);
+        } else {
+            if (tm != tm) {
+                nan_seen = true;
+            } else if (tm > m) {
+                m = tm;
+                aidx = chunk_find(d, ebase, ct, tm);
+            }
+        }
+        if (++k == ck.cpr || cc + 1 == c1) {  // row segment ends
+            flush();
+            k = 0;
+            ++r;
+            if (r < first_row + nrows) mr = table ? s_desc[r - first_row] : main_row<Vec>(p, s_rs, r);
+            m = kNegInf;
+            mc = 0.f;
+            s = 0.f;
+            aidx = -1;
+            nan_seen = false;
+        }
     }
 }
 
 // =================================================================== combine helpers
-// Warps whose ranges intersect flat row r, and the slot of row r in warp w.
-struct Split {
-    int64_t range;
-    int64_t V;
-    int nseg;
-    __device__ __forceinline__ int64_t w_lo(int r) const { return ((int64_t)r * V) / range; }
-    __device__ __forceinline__ int64_t w_hi(int r) const { return ((int64_t)r * V + V - 1) / range; }
-    __device__ __forceinline__ int64_t slot(int64_t w, int r) const {
-        return w * nseg + (r - (w * range) / V);
-    }
+// Partials of flat row r: CTAs [lo, hi] x kCW warps.
+struct RowParts {
+    int lo, hi, seg_lo;
+    __device__ __forceinline__ int n() const { return (hi - lo + 1) * kCW; }
 };
 
-__device__ float combine_max(const Part *parts, const Split &sp, int r) {
-    const int lane = threadIdx.x & 31;
-    float m = kNegInf;
-    for (int64_t w = sp.w_lo(r) + lane; w <= sp.w_hi(r); w += 32) m = max_nan_f32(m, parts[sp.slot(w, r)].m);
-    return warp_max_nan(m);
+__device__ __forceinline__ RowParts row_parts(int64_t total, int G, int cpr, int r) {
+    RowParts rp;
+    rp.lo = cta_of(total, G, (int64_t)r * cpr);
+    rp.hi = cta_of(total, G, (int64_t)r * cpr + cpr - 1);
+    rp.seg_lo = r;
+    return rp;
 }
 
-// Row statistics: M (raw max), MC = fl(M c), l2S = log2 sum_v 2^(x_v c - MC).
-__device__ void combine_stats(const Part *parts, const Split &sp, int r, float c, float &M, float &MC,
-                              float &l2S) {
-    const int lane = threadIdx.x & 31;
-    M = combine_max(parts, sp, r);
-    MC = M * c;
-    double s = 0.0;
-    for (int64_t w = sp.w_lo(r) + lane; w <= sp.w_hi(r); w += 32) {
-        const Part q = parts[sp.slot(w, r)];
-        if (q.m != kNegInf && q.s != 0.f) s += (double)q.s * (double)exp2f(q.m * c - MC);
-    }
-    s = warp_sum_d(s);
-    l2S = (float)log2(s);
+// Partial q of row r, or nullptr when its CTA has an empty chunk range (possible
+// when there are fewer chunks than CTAs): such CTAs lie between the row's first
+// and last CTA but wrote nothing.
+__device__ __forceinline__ const Part *part_of(const Part *parts, int64_t total, int G, int cpr, int nseg, int r,
+                                                const RowParts &rp, int q) {
+    const int cta = rp.lo + q / kCW;
+    const int64_t c0 = cta_first(total, G, cta);
+    if (c0 == cta_first(total, G, cta + 1)) return nullptr;
+    const int seg = r - (int)(c0 / cpr);
+    return &parts[part_slot(cta, nseg, seg, q % kCW)];
 }
 
-__device__ void combine_argmax(const Part *parts, const Split &sp, int r, bool use_best, float &score,
-                               int &idx) {
-    const int lane = threadIdx.x & 31;
-    score = kNegInf;
-    idx = -1;
-    for (int64_t w = sp.w_lo(r) + lane; w <= sp.w_hi(r); w += 32) {
-        const Part q = parts[sp.slot(w, r)];
-        const float s = use_best ? q.best : q.m;
-        if (better(s, q.idx, score, idx)) { score = s; idx = q.idx; }
-    }
-    warp_argmax(score, idx);
-}
+struct RowRes {
+    float M;    // raw row max
+    float l2S;  // log2 sum_v 2^(x_v c - fl(M c)) (stats rows)
+    float xv;   // logit at the draft token (stats rows)
+    int idx;    // lowest argmax
+};
 
 // =================================================================== accept_kernel
 struct AcceptParams {
@@ -450,30 +526,35 @@ struct AcceptParams {
     uint32_t step;
     const int *row_start;
     const Part *parts;
-    int nseg;
-    int64_t nwarps;  // warps of rows_kernel
-    int ve;          // vector width rows_kernel used
+    int nseg, G, cpr;
     int32_t *out_tokens;
     int32_t *out_accepted;
     float *out_p;
     float *out_q;
     int32_t *out_status;
-    ResJob *jobs;
+    Job *jobs;
     int *job_list;
-    int *job_count;
+    Ctrl *ctrl;
 };
 
-__global__ void __launch_bounds__(kThreads) accept_kernel(AcceptParams p) {
-    const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    if (b >= p.B) return;
+// Exact score of the correction draw at one entry: log(p - q) + g, with p > q.
+__device__ __forceinline__ float resid_score(float lp, float lq, uint32_t w) {
+    return lp + logf(-expm1f(lq - lp)) + gumbel_of_word(w);
+}
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(AcceptParams p) {
+    __shared__ RowRes s_rows[kMaxRowsPerRequest];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     const int K1 = p.Kmax + 1;
     int32_t *tok = p.out_tokens + (int64_t)b * K1;
-    for (int i = lane; i < K1; i += 32) tok[i] = -1;
+    for (int i = tid; i < K1; i += blockDim.x) tok[i] = -1;
     if (p.out_p)
-        for (int i = lane; i < p.Kmax; i += 32) p.out_p[(int64_t)b * p.Kmax + i] = -1.f;
+        for (int i = tid; i < p.Kmax; i += blockDim.x) p.out_p[(int64_t)b * p.Kmax + i] = -1.f;
     if (p.out_q)
-        for (int i = lane; i < p.Kmax; i += 32) p.out_q[(int64_t)b * p.Kmax + i] = -1.f;
+        for (int i = tid; i < p.Kmax; i += blockDim.x) p.out_q[(int64_t)b * p.Kmax + i] = -1.f;
 
     // statuses, in order: k_b, temperature, tokens, non-finite rows
     const int kb = p.num_draft ? p.num_draft[b] : p.Kmax;
@@ -484,99 +565,140 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(AcceptParams p) {
         T = p.temperature[b];
         if (!(T >= 0.f) || isinf(T)) status = SPEC_STATUS_BAD_TEMPERATURE;
     }
+    if (p.ctrl->err) status = SPEC_STATUS_INTERNAL;
     const bool greedy = (T == 0.f);
     const int32_t *x = p.draft_tokens + (int64_t)b * p.Kmax;
     if (status == SPEC_STATUS_OK) {
         bool bad = false;
-        for (int i = lane; i < kb; i += 32) bad |= (x[i] < 0 || x[i] >= p.V);
-        if (__any_sync(0xffffffffu, bad)) status = SPEC_STATUS_BAD_TOKEN;
+        for (int i = tid; i < kb; i += blockDim.x) bad |= (x[i] < 0 || x[i] >= p.V);
+        if (__syncthreads_or(bad)) status = SPEC_STATUS_BAD_TOKEN;
     }
-    Split sp;
-    sp.range = warp_range((int64_t)p.row_start[p.B] * p.V, p.nwarps, p.ve);
-    sp.V = p.V;
-    sp.nseg = p.nseg;
+    const float c = greedy ? 0.f : __fdiv_rn(kLog2e, T);
+    const int64_t total = (int64_t)p.row_start[p.B] * p.cpr;
     const int r0 = p.row_start[b];
-    if (status == SPEC_STATUS_OK) {
-        const int nrows = greedy ? kb + 1 : 2 * kb + 1;
-        bool nonfinite = false;
-        for (int rr = 0; rr < nrows; ++rr) {
-            const float M = combine_max(p.parts, sp, r0 + rr);
-            nonfinite |= !(fabsf(M) < __int_as_float(0x7f800000));
+    const int nrows = status == SPEC_STATUS_OK ? (greedy ? kb : 2 * kb) : 0;
+
+    // combine the partials of every row of this request, one warp per row
+    bool nonfinite = false;
+    for (int rr = warp; rr < nrows; rr += nwarps) {
+        const int r = r0 + rr;
+        const RowParts rp = row_parts(total, p.G, p.cpr, r);
+        float m = kNegInf;
+        for (int q = lane; q < rp.n(); q += 32) {
+            const Part *pt = part_of(p.parts, total, p.G, p.cpr, p.nseg, r, rp, q);
+            if (pt) m = max_nan_f32(m, pt->m);
         }
-        if (nonfinite) status = SPEC_STATUS_NONFINITE;
+        const float M = warp_max_nan(m);
+        double sum = 0.0;
+        float bm = kNegInf;
+        int bi = -1;
+        const float MC = M * c;
+        for (int q = lane; q < rp.n(); q += 32) {
+            const Part *pt = part_of(p.parts, total, p.G, p.cpr, p.nseg, r, rp, q);
+            if (!pt) continue;
+            if (!greedy && pt->m != kNegInf && pt->s != 0.f) sum += (double)pt->s * (double)exp2f(pt->m * c - MC);
+            if (better(pt->m, pt->idx, bm, bi)) { bm = pt->m; bi = pt->idx; }
+        }
+        warp_argmax(bm, bi);
+        RowRes res;
+        res.M = M;
+        res.idx = bi;
+        res.l2S = 0.f;
+        res.xv = 0.f;
+        if (!greedy) {
+            sum = warp_sum_d(sum);
+            res.l2S = (float)log2(sum);
+            const bool is_draft = rr >= kb;
+            const int i = is_draft ? rr - kb : rr;
+            const int64_t row = is_draft ? ((int64_t)b * p.Kmax + i) : ((int64_t)b * K1 + i);
+            res.xv = load_logit(is_draft ? p.draft : p.target, p.dtype, row * p.ld_row + x[i]);
+        }
+        nonfinite |= !(fabsf(M) < __int_as_float(0x7f800000));
+        if (lane == 0) s_rows[rr] = res;
     }
+    if (__syncthreads_or(nonfinite) && status == SPEC_STATUS_OK) status = SPEC_STATUS_NONFINITE;
+
     if (status != SPEC_STATUS_OK) {
-        if (lane == 0) {
+        if (tid == 0) {
             p.out_status[b] = status;
             p.out_accepted[b] = 0;
         }
         return;
     }
+    if (warp != 0) return;
 
-    int A = 0;
+    // acceptance scan, 32 positions at a time; A = first rejected position
+    int A = kb;
+    int token = -1;
     if (greedy) {
-        int y = -1;
-        for (int i = 0; i <= kb; ++i) {
-            float m;
-            combine_argmax(p.parts, sp, r0 + i, false, m, y);
-            if (i == kb || y != x[i]) break;
-            ++A;
+        for (int i0 = 0; i0 < kb && A == kb; i0 += 32) {
+            const int i = i0 + lane;
+            const bool mism = i < kb && s_rows[i].idx != x[i];
+            const unsigned msk = __ballot_sync(0xffffffffu, mism);
+            if (msk) A = i0 + __ffs(msk) - 1;
         }
-        if (lane == 0) {
-            for (int i = 0; i < A; ++i) tok[i] = x[i];
-            tok[A] = y;
-        }
+        if (A < kb) token = s_rows[A].idx;
     } else {
-        const float c = __fdiv_rn(kLog2e, T);
-        const int64_t esz = p.dtype == SPEC_BF16 ? 2 : 4;
-        bool rejected = false;
-        float rej_Ct = 0.f, rej_Cd = 0.f;
-        for (int i = 0; i < kb; ++i) {
-            float Mt, MCt, l2St, Md, MCd, l2Sd;
-            combine_stats(p.parts, sp, r0 + i, c, Mt, MCt, l2St);
-            combine_stats(p.parts, sp, r0 + kb + 1 + i, c, Md, MCd, l2Sd);
-            const int64_t trow = ((int64_t)b * K1 + i) * p.ld_row;
-            const int64_t drow = ((int64_t)b * p.Kmax + i) * p.ld_row;
-            const float xt = load_logit(p.target, p.dtype, trow + x[i]);
-            const float xd = load_logit(p.draft, p.dtype, drow + x[i]);
-            const float l2p = fmaf(xt, c, -MCt) - l2St;  // log2 p_i(x_i)
-            const float l2q = fmaf(xd, c, -MCd) - l2Sd;  // log2 q_i(x_i)
-            (void)esz;
-            if (lane == 0) {
+        for (int i0 = 0; i0 < kb; i0 += 32) {
+            const int i = i0 + lane;
+            bool rej = false;
+            if (i < kb) {
+                const RowRes tr = s_rows[i], dr = s_rows[kb + i];
+                const float l2p = fmaf(tr.xv, c, -(tr.M * c)) - tr.l2S;  // log2 p_i(x_i)
+                const float l2q = fmaf(dr.xv, c, -(dr.M * c)) - dr.l2S;  // log2 q_i(x_i)
                 if (p.out_p) p.out_p[(int64_t)b * p.Kmax + i] = exp2f(l2p);
                 if (p.out_q) p.out_q[(int64_t)b * p.Kmax + i] = exp2f(l2q);
+                // accept iff u q < p, i.e. log2 u < log2 p - log2 q (Q = 0 < P accepts; P = 0 rejects)
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
+                rej = !(log2f(u01(r4.x)) < l2p - l2q);
             }
-            if (rejected) continue;
-            // accept iff u q < p, i.e. log2 u < log2 p - log2 q (Q = 0 < P accepts; P = 0 rejects)
-            const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
-            const float u = u01(r4.x);
-            if (log2f(u) < l2p - l2q) {
-                ++A;
-            } else {
-                rejected = true;
-                // natural-log offsets: log p_v = x_v / T - Ct, log q_v = y_v / T - Cd
-                rej_Ct = (float)(((double)MCt + (double)l2St) * 0.6931471805599453);
-                rej_Cd = (float)(((double)MCd + (double)l2Sd) * 0.6931471805599453);
+            const unsigned msk = __ballot_sync(0xffffffffu, rej);
+            if (msk && A == kb) A = i0 + __ffs(msk) - 1;
+        }
+    }
+    for (int i = lane; i < A; i += 32) tok[i] = x[i];
+
+    if (greedy && A < kb) {
+        if (lane == 0) tok[A] = token;
+    } else {
+        Job job;
+        job.b = b;
+        job.row = A;
+        job.kind = greedy ? JOB_ARGMAX : (A < kb ? JOB_RESID : JOB_BONUS);
+        job.invT = greedy ? 0.f : __fdiv_rn(1.f, T);
+        job.Ct = job.Cd = 0.f;
+        job.seed_best = kNegInf;
+        job.seed_idx = -1;
+        if (job.kind == JOB_RESID) {
+            const int j = A;
+            const RowRes tr = s_rows[j], dr = s_rows[kb + j];
+            job.Ct = (float)(((double)(tr.M * c) + (double)tr.l2S) * 0.6931471805599453);
+            job.Cd = (float)(((double)(dr.M * c) + (double)dr.l2S) * 0.6931471805599453);
+            // seed the correction draw with the segment argmaxes of target row j
+            const int r = r0 + j;
+            const RowParts rp = row_parts(total, p.G, p.cpr, r);
+            const int64_t drow = ((int64_t)b * p.Kmax + j) * p.ld_row;
+            float best = kNegInf;
+            int bidx = -1;
+            for (int q = lane; q < rp.n(); q += 32) {
+                const Part *pt = part_of(p.parts, total, p.G, p.cpr, p.nseg, r, rp, q);
+                if (!pt || pt->idx < 0) continue;
+                const int v = pt->idx;
+                const float lp = fmaf(pt->m, job.invT, -job.Ct);
+                const float lq = fmaf(load_logit(p.draft, p.dtype, drow + v), job.invT, -job.Cd);
+                if (!(lq < lp)) continue;
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)j, PURPOSE_RESIDUAL,
+                                            (uint32_t)v >> 2);
+                const float sc = resid_score(lp, lq, word_of(r4, v & 3));
+                if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
             }
+            warp_argmax(best, bidx);
+            job.seed_best = best;
+            job.seed_idx = bidx;
         }
         if (lane == 0) {
-            for (int i = 0; i < A; ++i) tok[i] = x[i];
-        }
-        if (A == kb) {
-            float best;
-            int idx;
-            combine_argmax(p.parts, sp, r0 + kb, true, best, idx);
-            if (lane == 0) tok[kb] = idx;
-        } else if (lane == 0) {
-            ResJob job;
-            job.b = b;
-            job.j = A;
-            job.invT = __fdiv_rn(1.f, T);
-            job.Ct = rej_Ct;
-            job.Cd = rej_Cd;
-            job.pad[0] = job.pad[1] = job.pad[2] = 0;
             p.jobs[b] = job;
-            const int pos = atomicAdd(p.job_count, 1);
+            const int pos = atomicAdd(&p.ctrl->job_count, 1);
             p.job_list[pos] = b;
         }
     }
@@ -586,8 +708,63 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(AcceptParams p) {
     }
 }
 
-// =================================================================== residual
-struct ResidParams {
+// =================================================================== tail_kernel
+// Exact score of one entry that survived the bound (rare; kept out of line so the
+// hot loop stays small).  Returns -inf when the entry has no residual mass.
+struct GumbelRow {
+    const char *drow;  // draft row (correction only)
+    int dtype;
+    bool resid;
+    float invT, shift_c, Cd;
+};
+
+__device__ __noinline__ float exact_score(const GumbelRow &gr, float z, int v, uint32_t wd) {
+    if (gr.resid) {
+        const float lq = fmaf(load_logit(gr.drow, gr.dtype, v), gr.invT, -gr.Cd);
+        if (!(lq < z)) return kNegInf;
+        return resid_score(z, lq, wd);
+    }
+    return z + gumbel_of_word(wd);
+}
+
+// One staged chunk of a Gumbel-max row: z = x invT - shift_c is log p (correction)
+// or x / T (bonus).  Exact pruning, in order: the chunk or group bound
+// z + 17 < thr (no word gives more than 16.64 of noise), then per entry
+// 1 - u > 1.001 e^(z - thr) (g >= thr - z needs -log u <= e^(z - thr), and
+// -log u >= 1 - u).  Random words come from one Philox call per aligned group of
+// four, issued by the whole warp together.
+template <class Vec>
+__device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase, int ct, const GumbelRow &gr,
+                                             uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
+                                             uint32_t purpose, float tm, float thr, float &best, int &bidx) {
+    const bool live = fmaf(tm, gr.invT, -gr.shift_c) + kGumbelMax >= thr;
+    if (!__any_sync(0xffffffffu, live)) return;
+    const bool aligned = (ebase & 3) == 0;
+#pragma unroll
+    for (int t = 0; t < kVPT; ++t) {
+        const int64_t first = ebase + (int64_t)(ct + kCT * t) * Vec::VE;
+#pragma unroll
+        for (int g = 0; g < Vec::VE / 4; ++g) {
+            const bool glive = live && fmaf(d[t].gmax(g), gr.invT, -gr.shift_c) + kGumbelMax >= thr;
+            if (!__any_sync(0xffffffffu, glive)) continue;
+            const int v0 = (int)(first + 4 * g);
+            uint4 r4 = rand_group(seed, step, b, row, purpose, (uint32_t)v0 >> 2);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int v = v0 + k;
+                const float z = fmaf(d[t].get(4 * g + k), gr.invT, -gr.shift_c);
+                uint32_t wd = word_of(r4, k);
+                if (!aligned) wd = word_of(rand_group(seed, step, b, row, purpose, (uint32_t)v >> 2), v & 3);
+                if (glive && one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
+                    const float sc = exact_score(gr, z, v, wd);
+                    if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
+                }
+            }
+        }
+    }
+}
+
+struct TailParams {
     const void *target;
     const void *draft;
     int dtype;
@@ -595,109 +772,246 @@ struct ResidParams {
     int Kmax, V;
     uint64_t seed;
     uint32_t step;
-    const ResJob *jobs;
+    const Job *jobs;
     const int *job_list;
-    const int *job_count;
     Part *parts;
     int nseg;
+    int stages;
+    Ctrl *ctrl;
 };
 
 template <class Vec>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSM) resid_kernel(ResidParams p) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerBlock;
-    const int64_t w = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    const int64_t V = p.V;
-    const int64_t total = (int64_t)(*p.job_count) * V;
-    const int64_t range = warp_range(total, nwarps, Vec::VE);
-    const int64_t f1 = min(w * range + range, total);
-    const int64_t esz = Vec::ESIZE;
-    int seg = 0;
-    for (int64_t f = w * range; f < f1; ++seg) {
-        const int r = (int)(f / V);
-        const int64_t rowbase = (int64_t)r * V;
-        const int64_t v1 = min(f1 - rowbase, V);
-        const int64_t vb = (f - rowbase) / Vec::VE, ve = v1 / Vec::VE;
-        const ResJob job = p.jobs[p.job_list[r]];
-        const char *trow = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.j) * p.ld_row * esz;
-        const char *drow = (const char *)p.draft + ((int64_t)job.b * p.Kmax + job.j) * p.ld_row * esz;
-        const Part part = seg_residual<Vec>(trow, drow, p.dtype, vb, ve, job.invT, job.Ct, job.Cd, p.seed,
-                                            p.step, (uint32_t)job.b, (uint32_t)job.j);
-        if (lane == 0 && seg < p.nseg) p.parts[w * p.nseg + seg] = part;
-        f = rowbase + v1;
+__global__ void __launch_bounds__(kPipeThreads, 1) tail_kernel(TailParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Ring ring = ring_at(smem, p.stages);
+    Job *s_jobs = (Job *)(smem + ring_bytes(p.stages));
+    ring_init(ring);
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+    const Chunking ck = make_chunking(p.V, Vec::ESIZE);
+    const int G = gridDim.x;
+    const int njobs = p.ctrl->job_count;
+    const int64_t total = (int64_t)njobs * ck.cpr;
+    if (total == 0) return;
+    const int64_t c0 = cta_first(total, G, blockIdx.x), c1 = cta_first(total, G, blockIdx.x + 1);
+    if (c0 == c1) return;
+    const int first_row = (int)(c0 / ck.cpr);
+    const int nrows = (int)((c1 - 1) / ck.cpr) - first_row + 1;
+    const bool table = nrows <= kMaxDesc;
+    if (table)
+        for (int i = threadIdx.x; i < nrows; i += blockDim.x) s_jobs[i] = p.jobs[p.job_list[first_row + i]];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rowbytes = p.ld_row * Vec::ESIZE;
+    const int k0 = (int)(c0 - (int64_t)first_row * ck.cpr);
+    auto job_at = [&](int r) { return table ? s_jobs[r - first_row] : p.jobs[p.job_list[r]]; };
+
+    if (warp == kCW) {
+        if (lane == 0) {
+            int r = first_row, k = k0;
+            Job job = job_at(r);
+            ring_produce(ring, c0, c1, [&](int64_t) {
+                const char *row = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
+                const ChunkWin w = chunk_window(row, Vec::ESIZE, p.V, ck, k);
+                if (++k == ck.cpr) {
+                    k = 0;
+                    ++r;
+                    if (r < first_row + nrows) job = job_at(r);
+                }
+                return w;
+            }, &p.ctrl->err);
+        }
+        return;
+    }
+
+    const int ct = threadIdx.x;
+    int r = first_row, k = k0;
+    Job job = job_at(r);
+    float m = kNegInf, best = kNegInf;
+    int bidx = -1;
+    bool seeded = false, nan_seen = false;
+    auto start_row = [&]() {
+        m = kNegInf;
+        nan_seen = false;
+        seeded = job.kind != JOB_BONUS;
+        best = job.kind == JOB_RESID ? job.seed_best : kNegInf;
+        bidx = job.kind == JOB_RESID ? job.seed_idx : -1;
+    };
+    start_row();
+    auto flush = [&]() {
+        Part out;
+        if (job.kind == JOB_ARGMAX) {
+            const bool any_nan = __any_sync(0xffffffffu, nan_seen);
+            float mm = m;
+            warp_argmax(mm, bidx);
+            out.m = any_nan ? __int_as_float(0x7fc00000) : mm;
+            out.best = 0.f;
+        } else {
+            out.m = warp_max_nan(m);
+            warp_argmax(best, bidx);
+            out.best = best;
+        }
+        out.s = 0.f;
+        out.idx = bidx;
+        if (lane == 0) p.parts[part_slot(blockIdx.x, p.nseg, r - first_row, warp)] = out;
+    };
+
+    int st = 0;
+    uint32_t ph = 0;
+    for (int64_t cc = c0; cc < c1; ++cc) {
+        if (!mbar_wait(&ring.full[st], ph, kWaitNs)) {
+            atomicOr(&p.ctrl->err, 4);
+            break;
+        }
+        const char *trow = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
+        const ChunkWin w = chunk_window(trow, Vec::ESIZE, p.V, ck, k);
+        Vec d[kVPT];
+        load_chunk(d, ring.stages + (size_t)st * kStageBytes, w, ct);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[st]);
+        if (++st == ring.n) {
+            st = 0;
+            ph ^= 1u;
+        }
+        const int64_t ebase = (int64_t)w.e0 - w.shift;
+        const float tm = chunk_max(d);
+        if (job.kind == JOB_ARGMAX) {
+            if (tm != tm) {
+                nan_seen = true;
+            } else if (tm > m) {
+                m = tm;
+                bidx = chunk_find(d, ebase, ct, tm);
+            }
+        } else {
+            m = max_nan_f32(m, tm);
+            const bool resid = job.kind == JOB_RESID;
+            GumbelRow gr;
+            gr.drow = (const char *)p.draft + ((int64_t)job.b * p.Kmax + job.row) * rowbytes;
+            gr.dtype = p.dtype;
+            gr.resid = resid;
+            gr.invT = job.invT;
+            gr.shift_c = resid ? job.Ct : 0.f;
+            gr.Cd = job.Cd;
+            if (!seeded) {  // bonus: seed the bound with each lane's largest entry
+                seeded = true;
+                if (tm == tm && tm > kNegInf) {
+                    const int v = chunk_find(d, ebase, ct, tm);
+                    const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row, PURPOSE_BONUS,
+                                                (uint32_t)v >> 2);
+                    best = tm * job.invT + gumbel_of_word(word_of(r4, v & 3));
+                    bidx = v;
+                }
+            }
+            const float thr = warp_max(best);
+            gumbel_chunk(d, ebase, ct, gr, p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row,
+                         resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS, tm, thr, best, bidx);
+        }
+        if (++k == ck.cpr || cc + 1 == c1) {  // row segment ends
+            flush();
+            k = 0;
+            ++r;
+            if (r < first_row + nrows) {
+                job = job_at(r);
+                start_row();
+            }
+        }
     }
 }
 
+// =================================================================== final_kernel
 struct FinalParams {
     const void *target;
     int dtype;
     int64_t ld_row;
-    int B, Kmax, V;
+    int Kmax, V, G, cpr, nseg;
     uint64_t seed;
     uint32_t step;
-    const ResJob *jobs;
+    const Job *jobs;
     const int *job_list;
-    const int *job_count;
     const Part *parts;
-    int nseg;
-    int64_t nwarps;  // warps of resid_kernel
-    int ve;
+    Ctrl *ctrl;
     int32_t *out_tokens;
+    int32_t *out_accepted;
+    float *out_p;
+    float *out_q;
+    int32_t *out_status;
 };
 
-__global__ void __launch_bounds__(kThreads) final_kernel(FinalParams p) {
+__global__ void __launch_bounds__(kFinalThreads) final_kernel(FinalParams p) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
-    const int jb = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    const int njobs = *p.job_count;
+    const int jb = blockIdx.x * (kFinalThreads / 32) + (threadIdx.x >> 5);
+    const int njobs = p.ctrl->job_count;
     if (jb >= njobs) return;
-    Split sp;
-    sp.range = warp_range((int64_t)njobs * p.V, p.nwarps, p.ve);
-    sp.V = p.V;
-    sp.nseg = p.nseg;
-    float best;
-    int idx;
-    combine_argmax(p.parts, sp, jb, true, best, idx);
-    const ResJob job = p.jobs[p.job_list[jb]];
-    if (idx < 0) {
+    const Job job = p.jobs[p.job_list[jb]];
+    const int64_t total = (int64_t)njobs * p.cpr;
+    const RowParts rp = row_parts(total, p.G, p.cpr, jb);
+    float m = kNegInf, best = kNegInf;
+    int idx = -1;
+    for (int q = lane; q < rp.n(); q += 32) {
+        const Part *pt = part_of(p.parts, total, p.G, p.cpr, p.nseg, jb, rp, q);
+        if (!pt) continue;
+        m = max_nan_f32(m, pt->m);
+        const float sc = job.kind == JOB_ARGMAX ? pt->m : pt->best;
+        if (better(sc, pt->idx, best, idx)) { best = sc; idx = pt->idx; }
+    }
+    m = warp_max_nan(m);
+    warp_argmax(best, idx);
+    const int64_t K1 = p.Kmax + 1;
+    int status = SPEC_STATUS_OK;
+    if (p.ctrl->err) status = SPEC_STATUS_INTERNAL;
+    else if (job.kind != JOB_RESID && !(fabsf(m) < __int_as_float(0x7f800000))) status = SPEC_STATUS_NONFINITE;
+    if (status == SPEC_STATUS_OK && job.kind == JOB_RESID && idx < 0) {
         // p <= q everywhere (only by rounding): draw from p_j with the same noise
-        const int64_t trow = ((int64_t)job.b * (p.Kmax + 1) + job.j) * p.ld_row;
+        const int64_t trow = ((int64_t)job.b * K1 + job.row) * p.ld_row;
         best = kNegInf;
         for (int v = lane; v < p.V; v += 32) {
             const float lp = fmaf(load_logit(p.target, p.dtype, trow + v), job.invT, -job.Ct);
             if (!(lp > kNegInf)) continue;
-            const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)job.b, (uint32_t)job.j, PURPOSE_RESIDUAL,
+            const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row, PURPOSE_RESIDUAL,
                                         (uint32_t)v >> 2);
             const float sc = lp + gumbel_of_word(word_of(r4, v & 3));
             if (better(sc, v, best, idx)) { best = sc; idx = v; }
         }
         warp_argmax(best, idx);
     }
-    if (lane == 0) p.out_tokens[(int64_t)job.b * (p.Kmax + 1) + job.j] = idx;
+    if (status != SPEC_STATUS_OK) {
+        for (int i = lane; i < K1; i += 32) p.out_tokens[job.b * K1 + i] = -1;
+        for (int i = lane; i < p.Kmax; i += 32) {
+            if (p.out_p) p.out_p[(int64_t)job.b * p.Kmax + i] = -1.f;
+            if (p.out_q) p.out_q[(int64_t)job.b * p.Kmax + i] = -1.f;
+        }
+        if (lane == 0) {
+            p.out_status[job.b] = status;
+            p.out_accepted[job.b] = 0;
+        }
+        return;
+    }
+    if (lane == 0) p.out_tokens[job.b * K1 + job.row] = idx;
 }
 
 // =================================================================== host side
 thread_local int t_last_cuda_error = 0;
 
-struct DeviceInfo {
-    int sms = 0;
-};
-
 std::mutex g_mu;
-DeviceInfo g_dev[64];
+int g_sms[64];
+bool g_attr_set[64][4];
 
-int device_sms(int *out) {
+int device_info(int *dev_out, int *sms_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     if (dev < 0 || dev >= 64) return SPEC_EUNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_dev[dev].sms == 0) {
+    if (g_sms[dev] == 0) {
         int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
-        g_dev[dev].sms = sms;
+        g_sms[dev] = sms;
     }
-    *out = g_dev[dev].sms;
+    *dev_out = dev;
+    *sms_out = g_sms[dev];
     return SPEC_OK;
 }
 
@@ -714,10 +1028,9 @@ int prof_prepare() {
     cudaGetDevice(&dev);
     if (g_prof_dev != dev) {
         if (g_prof_dev >= 0) {
-            int cur = dev;
             cudaSetDevice(g_prof_dev);
             for (auto &e : g_prof_ev) cudaEventDestroy(e);
-            cudaSetDevice(cur);
+            cudaSetDevice(dev);
         }
         for (auto &e : g_prof_ev) {
             cudaError_t err = cudaEventCreate(&e);
@@ -732,7 +1045,7 @@ int prof_prepare() {
 struct ProfScope {
     cudaStream_t s;
     int k;
-    ProfScope(cudaStream_t st) : s(st), k(-1) {
+    explicit ProfScope(cudaStream_t st) : s(st), k(-1) {
         if (g_prof && g_prof_n < kMaxProfKernels) {
             k = g_prof_n++;
             cudaEventRecord(g_prof_ev[2 * k], s);
@@ -744,44 +1057,34 @@ struct ProfScope {
 };
 
 struct Layout {
-    size_t off_row_start, off_parts, off_jobs, off_job_list, off_job_count, off_rparts, total;
-    int nseg_rows, nseg_res;
-    int64_t nwarps;
+    size_t off_ctrl, off_row_start, off_parts, off_jobs, off_job_list, off_parts2, total;
+    int nseg, nseg2, G, cpr;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// rows_per_request: 2*Kmax+1 (sampling) or Kmax+1 (greedy); ve: vector width used
-Layout make_layout(int B, int Kmax, int V, int sms, int rows_per_request, int ve) {
+Layout make_layout(int B, int Kmax, int V, int esz, int sms, int main_rows_per_request) {
     Layout L;
-    L.nwarps = (int64_t)sms * kBlocksPerSM * kWarpsPerBlock;
-    const int64_t tot_rows = (int64_t)B * rows_per_request * V;
-    L.nseg_rows = segs_per_warp(warp_range(tot_rows, L.nwarps, ve), V);
-    L.nseg_res = segs_per_warp(warp_range((int64_t)B * V, L.nwarps, ve), V);
+    L.G = sms;
+    const Chunking ck = make_chunking(V, esz);
+    L.cpr = ck.cpr;
+    L.nseg = segs_per_cta((int64_t)B * main_rows_per_request * ck.cpr, L.G, ck.cpr);
+    L.nseg2 = segs_per_cta((int64_t)B * ck.cpr, L.G, ck.cpr);
     size_t o = 0;
+    L.off_ctrl = o;
+    o = align256(o + sizeof(Ctrl));
     L.off_row_start = o;
     o = align256(o + sizeof(int) * (size_t)(B + 1));
     L.off_parts = o;
-    o = align256(o + sizeof(Part) * (size_t)L.nwarps * (size_t)L.nseg_rows);
+    o = align256(o + sizeof(Part) * (size_t)L.G * L.nseg * kCW);
     L.off_jobs = o;
-    o = align256(o + sizeof(ResJob) * (size_t)B);
+    o = align256(o + sizeof(Job) * (size_t)B);
     L.off_job_list = o;
     o = align256(o + sizeof(int) * (size_t)B);
-    L.off_job_count = o;
-    o = align256(o + sizeof(int));
-    L.off_rparts = o;
-    o = align256(o + sizeof(Part) * (size_t)L.nwarps * (size_t)L.nseg_res);
+    L.off_parts2 = o;
+    o = align256(o + sizeof(Part) * (size_t)L.G * L.nseg2 * kCW);
     L.total = o;
     return L;
-}
-
-bool vector_ok(const void *a, const void *b, int64_t ld_row, int V, int dtype) {
-    const int esz = dtype == SPEC_BF16 ? 2 : 4;
-    const int ve = 16 / esz;
-    if (((uintptr_t)a & 15) != 0) return false;
-    if (b && ((uintptr_t)b & 15) != 0) return false;
-    if (((ld_row * esz) & 15) != 0) return false;
-    return V % ve == 0;
 }
 
 int check_launch() {
@@ -790,35 +1093,75 @@ int check_launch() {
     return SPEC_OK;
 }
 
+template <class K, class P>
+int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const P &params) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, params);
+    if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
+    return SPEC_OK;
+}
+
+// Ring depth from the shared-memory budget left after the per-CTA tables.
+int stages_for(size_t extra) {
+    const size_t avail = kSmemBudget - extra - 2 * (size_t)kMaxStages * sizeof(uint64_t);
+    int n = (int)(avail / kStageBytes);
+    return n > kMaxStages ? kMaxStages : n;
+}
+size_t main_extra(int B) { return sizeof(int) * (size_t)(((B + 1) + 3) & ~3) + sizeof(MainRow) * kMaxDesc; }
+constexpr size_t kTailExtra = sizeof(Job) * kMaxDesc;
+
 template <class Vec>
-int launch_all(const RowsParams &rp, AcceptParams ap, ResidParams qp, FinalParams fp, int sms, bool sample,
-               cudaStream_t st) {
-    const int grid = sms * kBlocksPerSM;
-    const size_t smem = sizeof(int) * (size_t)(rp.B + 1);
-    {
-        ProfScope ps(st);
-        rows_kernel<Vec><<<grid, kThreads, smem, st>>>(rp);
-    }
-    int rc = check_launch();
+int set_smem_attrs(int dev, size_t main_smem) {
+    const int which = Vec::ESIZE == 2 ? 0 : 1;
+    if (g_attr_set[dev][which]) return SPEC_OK;
+    cudaError_t e = cudaFuncSetAttribute(main_kernel<Vec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)main_smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tail_kernel<Vec>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+    if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
+    g_attr_set[dev][which] = true;
+    return SPEC_OK;
+}
+
+template <class Vec>
+int launch_all(int dev, const Layout &L, const MainParams &mp, const AcceptParams &ap, const TailParams &tp,
+               const FinalParams &fp, cudaStream_t st) {
+    int rc = set_smem_attrs<Vec>(dev, kSmemBudget);
     if (rc) return rc;
-    const int ablocks = (rp.B + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    cudaError_t e = cudaMemsetAsync(mp.ctrl, 0, sizeof(Ctrl), st);
+    if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
+    const size_t main_smem = ring_bytes(mp.stages) + main_extra(mp.B);
+    const size_t tail_smem = ring_bytes(tp.stages) + kTailExtra;
     {
         ProfScope ps(st);
-        accept_kernel<<<ablocks, kThreads, 0, st>>>(ap);
+        main_kernel<Vec><<<L.G, kPipeThreads, main_smem, st>>>(mp);
     }
-    rc = check_launch();
-    if (rc || !sample) return rc;
+    if ((rc = check_launch())) return rc;
     {
         ProfScope ps(st);
-        resid_kernel<Vec><<<grid, kThreads, 0, st>>>(qp);
+        rc = launch_pdl(accept_kernel, dim3(mp.B), dim3(kAcceptThreads), 0, st, ap);
     }
-    rc = check_launch();
     if (rc) return rc;
     {
         ProfScope ps(st);
-        final_kernel<<<ablocks, kThreads, 0, st>>>(fp);
+        rc = launch_pdl(tail_kernel<Vec>, dim3(L.G), dim3(kPipeThreads), tail_smem, st, tp);
     }
-    return check_launch();
+    if (rc) return rc;
+    {
+        ProfScope ps(st);
+        const int wpb = kFinalThreads / 32;
+        rc = launch_pdl(final_kernel, dim3((mp.B + wpb - 1) / wpb), dim3(kFinalThreads), 0, st, fp);
+    }
+    return rc;
 }
 
 int verify_impl(const void *target, const void *draft, int dtype, int B, int Kmax, int V, int64_t ld_row,
@@ -833,34 +1176,36 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     if (!target || !out_tokens || !out_accepted || !out_status) return SPEC_EINVAL;
     if (Kmax > 0 && !draft_tokens) return SPEC_EINVAL;
     if (sample && (!temperature || (Kmax > 0 && !draft))) return SPEC_EINVAL;
+    const int esz = dtype == SPEC_BF16 ? 2 : 4;
+    if (((uintptr_t)target % esz) || (draft && ((uintptr_t)draft % esz))) return SPEC_EINVAL;
     if ((int64_t)B * (2 * Kmax + 1) * (int64_t)V > ((int64_t)1 << 50)) return SPEC_EUNSUPPORTED;
-    int sms = 0;
-    int rc = device_sms(&sms);
+    int dev = 0, sms = 0;
+    int rc = device_info(&dev, &sms);
     if (rc) return rc;
-    const bool vec = vector_ok(target, sample ? draft : nullptr, ld_row, V, dtype);
-    const int ve = vec ? (dtype == SPEC_BF16 ? 8 : 4) : 1;
-    const Layout L = make_layout(B, Kmax, V, sms, sample ? 2 * Kmax + 1 : Kmax + 1, ve);
+    const Layout L = make_layout(B, Kmax, V, esz, sms, sample ? 2 * Kmax : Kmax);
     if (!ws) return SPEC_EWORKSPACE;
     if (ws_bytes < L.total) return SPEC_EWORKSPACE;
     rc = prof_prepare();
     if (rc) return rc;
 
     char *w = (char *)ws;
-    RowsParams rp;
-    rp.target = target;
-    rp.draft = draft;
-    rp.ld_row = ld_row;
-    rp.B = B;
-    rp.Kmax = Kmax;
-    rp.V = V;
-    rp.num_draft = num_draft;
-    rp.temperature = sample ? temperature : nullptr;
-    rp.seed = seed;
-    rp.step = (uint32_t)step;
-    rp.row_start = (int *)(w + L.off_row_start);
-    rp.parts = (Part *)(w + L.off_parts);
-    rp.nseg = L.nseg_rows;
-    rp.job_count = (int *)(w + L.off_job_count);
+    Ctrl *ctrl = (Ctrl *)(w + L.off_ctrl);
+    const float *temps = sample ? temperature : nullptr;
+
+    MainParams mp;
+    mp.target = target;
+    mp.draft = draft;
+    mp.ld_row = ld_row;
+    mp.B = B;
+    mp.Kmax = Kmax;
+    mp.V = V;
+    mp.num_draft = num_draft;
+    mp.temperature = temps;
+    mp.row_start = (int *)(w + L.off_row_start);
+    mp.parts = (Part *)(w + L.off_parts);
+    mp.nseg = L.nseg;
+    mp.stages = stages_for(main_extra(B));
+    mp.ctrl = ctrl;
 
     AcceptParams ap;
     ap.target = target;
@@ -872,62 +1217,63 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     ap.V = V;
     ap.draft_tokens = draft_tokens;
     ap.num_draft = num_draft;
-    ap.temperature = rp.temperature;
+    ap.temperature = temps;
     ap.seed = seed;
     ap.step = (uint32_t)step;
-    ap.row_start = rp.row_start;
-    ap.parts = rp.parts;
-    ap.nseg = L.nseg_rows;
-    ap.nwarps = L.nwarps;
-    ap.ve = ve;
+    ap.row_start = mp.row_start;
+    ap.parts = mp.parts;
+    ap.nseg = L.nseg;
+    ap.G = L.G;
+    ap.cpr = L.cpr;
     ap.out_tokens = out_tokens;
     ap.out_accepted = out_accepted;
     ap.out_p = sample ? out_p : nullptr;
     ap.out_q = sample ? out_q : nullptr;
     ap.out_status = out_status;
-    ap.jobs = (ResJob *)(w + L.off_jobs);
+    ap.jobs = (Job *)(w + L.off_jobs);
     ap.job_list = (int *)(w + L.off_job_list);
-    ap.job_count = rp.job_count;
+    ap.ctrl = ctrl;
 
-    ResidParams qp;
-    qp.target = target;
-    qp.draft = draft;
-    qp.dtype = dtype;
-    qp.ld_row = ld_row;
-    qp.Kmax = Kmax;
-    qp.V = V;
-    qp.seed = seed;
-    qp.step = (uint32_t)step;
-    qp.jobs = ap.jobs;
-    qp.job_list = ap.job_list;
-    qp.job_count = rp.job_count;
-    qp.parts = (Part *)(w + L.off_rparts);
-    qp.nseg = L.nseg_res;
+    TailParams tp;
+    tp.target = target;
+    tp.draft = draft;
+    tp.dtype = dtype;
+    tp.ld_row = ld_row;
+    tp.Kmax = Kmax;
+    tp.V = V;
+    tp.seed = seed;
+    tp.step = (uint32_t)step;
+    tp.jobs = ap.jobs;
+    tp.job_list = ap.job_list;
+    tp.parts = (Part *)(w + L.off_parts2);
+    tp.nseg = L.nseg2;
+    tp.stages = stages_for(kTailExtra);
+    tp.ctrl = ctrl;
 
     FinalParams fp;
     fp.target = target;
     fp.dtype = dtype;
     fp.ld_row = ld_row;
-    fp.B = B;
     fp.Kmax = Kmax;
     fp.V = V;
+    fp.G = L.G;
+    fp.cpr = L.cpr;
+    fp.nseg = L.nseg2;
     fp.seed = seed;
     fp.step = (uint32_t)step;
     fp.jobs = ap.jobs;
     fp.job_list = ap.job_list;
-    fp.job_count = rp.job_count;
-    fp.parts = qp.parts;
-    fp.nseg = L.nseg_res;
-    fp.nwarps = L.nwarps;
-    fp.ve = ve;
+    fp.parts = tp.parts;
+    fp.ctrl = ctrl;
     fp.out_tokens = out_tokens;
+    fp.out_accepted = out_accepted;
+    fp.out_p = ap.out_p;
+    fp.out_q = ap.out_q;
+    fp.out_status = out_status;
 
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    if (dtype == SPEC_BF16)
-        return vec ? launch_all<VecBF16>(rp, ap, qp, fp, sms, sample, st)
-                   : launch_all<ScalarBF16>(rp, ap, qp, fp, sms, sample, st);
-    return vec ? launch_all<VecF32>(rp, ap, qp, fp, sms, sample, st)
-               : launch_all<ScalarF32>(rp, ap, qp, fp, sms, sample, st);
+    return dtype == SPEC_BF16 ? launch_all<VecBF16>(dev, L, mp, ap, tp, fp, st)
+                              : launch_all<VecF32>(dev, L, mp, ap, tp, fp, st);
 }
 
 }  // namespace
@@ -937,10 +1283,9 @@ extern "C" {
 size_t spec_verify_workspace_size(int B, int Kmax, int V, int dtype) {
     if (B < 0 || Kmax < 0 || V <= 0 || (dtype != SPEC_BF16 && dtype != SPEC_F32)) return 0;
     if (B > SPEC_MAX_BATCH || Kmax > SPEC_MAX_DRAFTS) return 0;
-    int sms = 0;
-    if (device_sms(&sms)) return 0;
-    // the widest vector gives the largest per-warp range, hence the most segments
-    return make_layout(B, Kmax, V, sms, 2 * Kmax + 1, 8).total;
+    int dev = 0, sms = 0;
+    if (device_info(&dev, &sms)) return 0;
+    return make_layout(B, Kmax, V, dtype == SPEC_BF16 ? 2 : 4, sms, 2 * Kmax).total;
 }
 
 int spec_verify_greedy(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,

@@ -207,3 +207,20 @@ def test_empty_batch_and_repeat_calls():
     b = run_gpu_sample(batch, 1, 1)
     for k in ("tokens", "accepted", "status", "p", "q"):
         assert (a[k] == b[k]).all()
+
+
+def test_bonus_row_status_on_gpu():
+    from test_oracle_verify import _bonus_row_case
+    import speculative_decoding_verification_15_gb300 as pkg
+
+    for kind in ("accept", "reject"):
+        t, d, x = _bonus_row_case(kind)
+        batch = dict(target=torch.from_numpy(t), draft=torch.from_numpy(d), draft_tokens=torch.from_numpy(x),
+                     num_draft=None, temperature=torch.ones(1))
+        gpu = run_gpu_sample(batch, 1, 1)
+        ref = run_oracle_sample(batch, 1, 1)
+        compare_sample(gpu, ref, np.ones(1, np.float32))
+        g = pkg.verify_greedy(torch.from_numpy(t).cuda(), torch.from_numpy(x).cuda())
+        gref = oracle.verify_greedy(t, x, None)
+        assert int(g["status"][0]) == int(gref["status"][0])
+        assert g["tokens"].cpu().numpy().tolist() == gref["tokens"].tolist()

@@ -454,3 +454,34 @@ def test_zero_drafts_is_a_bonus_draw(oracle_mod):
     out = oracle_mod.verify_sample(t, d, np.zeros((N, 0), np.int32), None, np.ones(N, np.float32), 2, 2)
     assert (out["accepted"] == 0).all()
     assert _chi2_ok(np.bincount(out["tokens"][:, 0], minlength=V), p)
+
+
+def _bonus_row_case(kind):
+    """Request with K = 2 whose target row 2 (after the last draft) is NaN."""
+    V, K = 16, 2
+    rng = np.random.default_rng(21)
+    p = [_rand_dist(rng, V, 0.0) for _ in range(K)]
+    t = np.zeros((1, K + 1, V), np.float32)
+    d = np.zeros((1, K, V), np.float32)
+    for i in range(K):
+        t[0, i] = np.log(p[i])
+        d[0, i] = np.log(p[i])  # q == p: every draft accepted
+    t[0, K] = np.nan
+    x = np.array([[int(np.argmax(p[0])), int(np.argmax(p[1]))]], np.int32)
+    if kind == "reject":
+        t[0, 0, x[0, 0]] = -np.inf  # p(x_0) = 0: rejected at position 0, row 2 never read
+    return t, d, x
+
+
+def test_bonus_row_checked_only_when_read(oracle_mod):
+    t, d, x = _bonus_row_case("accept")
+    out = oracle_mod.verify_sample(t, d, x, None, np.ones(1, np.float32), 1, 1)
+    assert out["status"][0] == 4 and out["accepted"][0] == 0
+    assert (out["tokens"] == -1).all() and (out["p"] == -1).all()
+    g = oracle_mod.verify_greedy(t, x, None)
+    assert g["status"][0] == 4 and (g["tokens"] == -1).all()
+    t, d, x = _bonus_row_case("reject")
+    out = oracle_mod.verify_sample(t, d, x, None, np.ones(1, np.float32), 1, 1)
+    assert out["status"][0] == 0 and out["accepted"][0] == 0 and out["tokens"][0, 0] >= 0
+    g = oracle_mod.verify_greedy(t, x, None)
+    assert g["status"][0] == 0 and g["accepted"][0] == 0
