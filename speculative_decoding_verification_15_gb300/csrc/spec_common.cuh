@@ -36,10 +36,10 @@ struct __align__(16) Part {
 __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t a = x.x, c = x.z;
-        const uint32_t hi_a = __umulhi(0xD2511F53u, a), lo_a = 0xD2511F53u * a;
-        const uint32_t hi_c = __umulhi(0xCD9E8D57u, c), lo_c = 0xCD9E8D57u * c;
-        x = make_uint4(hi_c ^ x.y ^ k0, lo_c, hi_a ^ x.w ^ k1, lo_a);
+        // one 32x32 -> 64-bit product per multiplier gives both halves
+        const uint64_t pa = (uint64_t)x.x * 0xD2511F53u;
+        const uint64_t pc = (uint64_t)x.z * 0xCD9E8D57u;
+        x = make_uint4((uint32_t)(pc >> 32) ^ x.y ^ k0, (uint32_t)pc, (uint32_t)(pa >> 32) ^ x.w ^ k1, (uint32_t)pa);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }

@@ -53,6 +53,7 @@ constexpr int kAcceptThreads = 256;
 constexpr int kFinalThreads = 256;
 constexpr int kMaxRowsPerRequest = 2 * SPEC_MAX_DRAFTS;
 constexpr int kMaxDesc = 512;                    // per-CTA row descriptors kept in smem
+constexpr float kRescaleAt = 1024.f;             // lane chunk sum that moves the reference
 
 enum JobKind : int { JOB_RESID = 0, JOB_BONUS = 1, JOB_ARGMAX = 2 };
 
@@ -154,19 +155,30 @@ __device__ __forceinline__ void mask_vec<VecF32>(VecF32 &d, int64_t first, int e
 }
 
 // Loads this consumer thread's vectors of a staged chunk; out-of-window entries -inf.
-// Vector t of thread ct holds global elements ebase + (ct + kCT t) VE + e.
+// Vector t of thread ct holds global elements ebase + (ct + kCT t) VE + e.  Only a
+// window that does not start and end on 16-byte boundaries needs masking, which
+// is decided once per chunk (the branch is uniform across the CTA).
 template <class Vec>
 __device__ __forceinline__ void load_chunk(Vec (&d)[kVPT], const char *stage, const ChunkWin &w, int ct) {
     const int nvec = (int)(w.bytes >> 4);
     const int64_t ebase = (int64_t)w.e0 - w.shift;
+    const bool ragged = w.shift != 0 || ebase + (int64_t)nvec * Vec::VE != w.e1;
+    if (!ragged) {
 #pragma unroll
-    for (int t = 0; t < kVPT; ++t) {
-        const int j = ct + kCT * t;
-        if (j < nvec) {
-            d[t].v = lds128(stage + 16 * j);
-            if (j == 0 || j == nvec - 1) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, w.e0, w.e1);
-        } else {
-            d[t] = Vec::neg_inf();
+        for (int t = 0; t < kVPT; ++t) {
+            const int j = ct + kCT * t;
+            d[t] = j < nvec ? Vec{lds128(stage + 16 * j)} : Vec::neg_inf();
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < kVPT; ++t) {
+            const int j = ct + kCT * t;
+            if (j < nvec) {
+                d[t].v = lds128(stage + 16 * j);
+                if (j == 0 || j == nvec - 1) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, w.e0, w.e1);
+            } else {
+                d[t] = Vec::neg_inf();
+            }
         }
     }
 }
@@ -446,17 +458,28 @@ __global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
             ph ^= 1u;
         }
         const int64_t ebase = (int64_t)w.e0 - w.shift;
-        const float tm = chunk_max(d);
         if (mr.c != 0.f) {
-            if (!(tm <= m)) {  // new maximum, or NaN
-                const float mcn = tm * mr.c;
-                s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
-                m = tm;
-                mc = mcn;
-                aidx = chunk_find(d, ebase, ct, tm);
+            // s is kept relative to a per-lane reference entry m (mc = fl(m c)); any
+            // reference gives the exact sum, so it only moves when this chunk's terms
+            // grow past kRescaleAt (an entry more than 5 log2-units above m), on the
+            // first finite chunk, or for NaN / +inf.
+            float cs = chunk_expsum(d, mr.c, mc);
+            if (m == kNegInf || !(cs < kRescaleAt)) {
+                const float tm = chunk_max(d);
+                if (!(tm <= m)) {  // new reference, or NaN
+                    const float mcn = tm * mr.c;
+                    s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
+                    m = tm;
+                    mc = mcn;
+                    aidx = chunk_find(d, ebase, ct, tm);
+                    cs = chunk_expsum(d, mr.c, mc);
+                } else if (m == kNegInf) {
+                    cs = 0.f;  // every entry so far is -inf
+                }
             }
-            s += chunk_expsum(d, mr.c, m == kNegInf ? 0.f : mc);
+            s += cs;
         } else {
+            const float tm = chunk_max(d);
             if (tm != tm) {
                 nan_seen = true;
             } else if (tm > m) {
@@ -727,38 +750,78 @@ __device__ __noinline__ float exact_score(const GumbelRow &gr, float z, int v, u
     return z + gumbel_of_word(wd);
 }
 
+// Random word of entry v when the window is not aligned to groups of four.
+__device__ __noinline__ uint32_t rand_word_slow(uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
+                                                uint32_t purpose, int v) {
+    return word_of(rand_group(seed, step, b, row, purpose, (uint32_t)v >> 2), v & 3);
+}
+
+// Words of group slot s (vector s / G, group s % G) of a thread's chunk data.
+template <class Vec>
+__device__ __forceinline__ void slot_values(const Vec (&d)[kVPT], int s, float (&x)[4]);
+
+template <>
+__device__ __forceinline__ void slot_values<VecBF16>(const VecBF16 (&d)[kVPT], int s, float (&x)[4]) {
+    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+    for (int t = 0; t < kVPT; ++t) {
+        if (s == 2 * t) { w0 = d[t].v.x; w1 = d[t].v.y; }
+        if (s == 2 * t + 1) { w0 = d[t].v.z; w1 = d[t].v.w; }
+    }
+    x[0] = bf16_lo(w0);
+    x[1] = bf16_hi(w0);
+    x[2] = bf16_lo(w1);
+    x[3] = bf16_hi(w1);
+}
+
+template <>
+__device__ __forceinline__ void slot_values<VecF32>(const VecF32 (&d)[kVPT], int s, float (&x)[4]) {
+    uint4 v = d[0].v;
+#pragma unroll
+    for (int t = 1; t < kVPT; ++t)
+        if (s == t) v = d[t].v;
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+}
+
 // One staged chunk of a Gumbel-max row: z = x invT - shift_c is log p (correction)
 // or x / T (bonus).  Exact pruning, in order: the chunk or group bound
 // z + 17 < thr (no word gives more than 16.64 of noise), then per entry
 // 1 - u > 1.001 e^(z - thr) (g >= thr - z needs -log u <= e^(z - thr), and
-// -log u >= 1 - u).  Random words come from one Philox call per aligned group of
-// four, issued by the whole warp together.
+// -log u >= 1 - u).  A cheap unrolled pass marks the live groups of four; a
+// compact loop then draws one Philox block per live group.
 template <class Vec>
 __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase, int ct, const GumbelRow &gr,
                                              uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
                                              uint32_t purpose, float tm, float thr, float &best, int &bidx) {
-    const bool live = fmaf(tm, gr.invT, -gr.shift_c) + kGumbelMax >= thr;
-    if (!__any_sync(0xffffffffu, live)) return;
+    constexpr int G = Vec::VE / 4;  // groups of four per vector
+    uint32_t live = 0;
+    if (fmaf(tm, gr.invT, -gr.shift_c) + kGumbelMax >= thr) {
+#pragma unroll
+        for (int t = 0; t < kVPT; ++t)
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                if (fmaf(d[t].gmax(g), gr.invT, -gr.shift_c) + kGumbelMax >= thr) live |= 1u << (t * G + g);
+    }
     const bool aligned = (ebase & 3) == 0;
+#pragma unroll 1
+    while (live) {
+        const int sl = __ffs(live) - 1;
+        live &= live - 1;
+        float x[4];
+        slot_values(d, sl, x);
+        const int v0 = (int)(ebase + (int64_t)(ct + kCT * (sl / G)) * Vec::VE + 4 * (sl % G));
+        uint4 r4 = rand_group(seed, step, b, row, purpose, (uint32_t)v0 >> 2);
 #pragma unroll
-    for (int t = 0; t < kVPT; ++t) {
-        const int64_t first = ebase + (int64_t)(ct + kCT * t) * Vec::VE;
-#pragma unroll
-        for (int g = 0; g < Vec::VE / 4; ++g) {
-            const bool glive = live && fmaf(d[t].gmax(g), gr.invT, -gr.shift_c) + kGumbelMax >= thr;
-            if (!__any_sync(0xffffffffu, glive)) continue;
-            const int v0 = (int)(first + 4 * g);
-            uint4 r4 = rand_group(seed, step, b, row, purpose, (uint32_t)v0 >> 2);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int v = v0 + k;
-                const float z = fmaf(d[t].get(4 * g + k), gr.invT, -gr.shift_c);
-                uint32_t wd = word_of(r4, k);
-                if (!aligned) wd = word_of(rand_group(seed, step, b, row, purpose, (uint32_t)v >> 2), v & 3);
-                if (glive && one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
-                    const float sc = exact_score(gr, z, v, wd);
-                    if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
-                }
+        for (int k = 0; k < 4; ++k) {
+            const int v = v0 + k;
+            const float z = fmaf(x[k], gr.invT, -gr.shift_c);
+            const uint32_t wd = aligned ? word_of(r4, k) : rand_word_slow(seed, step, b, row, purpose, v);
+            if (one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
+                const float sc = exact_score(gr, z, v, wd);
+                if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
             }
         }
     }
