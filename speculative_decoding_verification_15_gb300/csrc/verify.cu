@@ -49,7 +49,7 @@ constexpr int kChunkMaxBytes = kStageBytes - 32; // payload; an aligned superset
 constexpr int kVPT = kStageBytes / 16 / kCT;     // 16-byte vectors per consumer thread (4)
 constexpr size_t kSmemBudget = 226 * 1024;       // dynamic shared memory per CTA (227 KB minus static)
 constexpr uint64_t kWaitNs = 2000000000ull;      // bound on every mbarrier wait (2 s)
-constexpr int kAcceptThreads = 256;
+constexpr int kAcceptThreads = 512;
 constexpr int kFinalThreads = 256;
 constexpr int kMaxRowsPerRequest = 2 * SPEC_MAX_DRAFTS;
 constexpr int kMaxDesc = 512;                    // per-CTA row descriptors kept in smem
@@ -74,7 +74,18 @@ struct Job {
 struct Ctrl {
     int err;        // non-zero: a bounded wait gave up
     int job_count;  // jobs queued by accept_kernel
+    int tail_next;  // next tail chunk to hand out
+    int pad;
 };
+
+// Order-preserving map of a float onto uint32 (for atomicMax on scores).
+__device__ __forceinline__ uint32_t ord_of(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float float_of_ord(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
 
 // ------------------------------------------------------------------ chunking
 // Rows are cut into cpr chunks of ce elements (ce a multiple of 8, at most
@@ -557,6 +568,7 @@ struct AcceptParams {
     int32_t *out_status;
     Job *jobs;
     int *job_list;
+    uint32_t *job_best;
     Ctrl *ctrl;
 };
 
@@ -605,6 +617,14 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(AcceptParams p) 
     bool nonfinite = false;
     for (int rr = warp; rr < nrows; rr += nwarps) {
         const int r = r0 + rr;
+        // the draft token's logit: independent of the partials, so issued first
+        float xv = 0.f;
+        if (!greedy) {
+            const bool is_draft = rr >= kb;
+            const int i = is_draft ? rr - kb : rr;
+            const int64_t row = is_draft ? ((int64_t)b * p.Kmax + i) : ((int64_t)b * K1 + i);
+            xv = load_logit(is_draft ? p.draft : p.target, p.dtype, row * p.ld_row + x[i]);
+        }
         const RowParts rp = row_parts(total, p.G, p.cpr, r);
         float m = kNegInf;
         for (int q = lane; q < rp.n(); q += 32) {
@@ -630,11 +650,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(AcceptParams p) 
         res.xv = 0.f;
         if (!greedy) {
             sum = warp_sum_d(sum);
-            res.l2S = (float)log2(sum);
-            const bool is_draft = rr >= kb;
-            const int i = is_draft ? rr - kb : rr;
-            const int64_t row = is_draft ? ((int64_t)b * p.Kmax + i) : ((int64_t)b * K1 + i);
-            res.xv = load_logit(is_draft ? p.draft : p.target, p.dtype, row * p.ld_row + x[i]);
+            res.l2S = log2f((float)sum);
+            res.xv = xv;
         }
         nonfinite |= !(fabsf(M) < __int_as_float(0x7f800000));
         if (lane == 0) s_rows[rr] = res;
@@ -723,6 +740,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(AcceptParams p) 
             p.jobs[b] = job;
             const int pos = atomicAdd(&p.ctrl->job_count, 1);
             p.job_list[pos] = b;
+            p.job_best[pos] = ord_of(job.seed_best);
         }
     }
     if (lane == 0) {
@@ -756,47 +774,65 @@ __device__ __noinline__ uint32_t rand_word_slow(uint64_t seed, uint32_t step, ui
     return word_of(rand_group(seed, step, b, row, purpose, (uint32_t)v >> 2), v & 3);
 }
 
-// Words of group slot s (vector s / G, group s % G) of a thread's chunk data.
+// Raw words of group slot s (vector s / G, group s % G) of a thread's chunk data,
+// and the four logits they hold.
 template <class Vec>
-__device__ __forceinline__ void slot_values(const Vec (&d)[kVPT], int s, float (&x)[4]);
+struct GroupWords;
 
 template <>
-__device__ __forceinline__ void slot_values<VecBF16>(const VecBF16 (&d)[kVPT], int s, float (&x)[4]) {
-    uint32_t w0 = 0, w1 = 0;
+struct GroupWords<VecBF16> {
+    static constexpr int N = 2;  // 4 bf16 = 2 words
+    __device__ __forceinline__ static void get(const VecBF16 (&d)[kVPT], int s, uint32_t (&w)[4]) {
+        uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-    for (int t = 0; t < kVPT; ++t) {
-        if (s == 2 * t) { w0 = d[t].v.x; w1 = d[t].v.y; }
-        if (s == 2 * t + 1) { w0 = d[t].v.z; w1 = d[t].v.w; }
+        for (int t = 0; t < kVPT; ++t) {
+            if (s == 2 * t) { w0 = d[t].v.x; w1 = d[t].v.y; }
+            if (s == 2 * t + 1) { w0 = d[t].v.z; w1 = d[t].v.w; }
+        }
+        w[0] = w0;
+        w[1] = w1;
     }
-    x[0] = bf16_lo(w0);
-    x[1] = bf16_hi(w0);
-    x[2] = bf16_lo(w1);
-    x[3] = bf16_hi(w1);
-}
+    __device__ __forceinline__ static float value(const uint32_t (&w)[4], int k) {
+        return (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]);
+    }
+};
 
 template <>
-__device__ __forceinline__ void slot_values<VecF32>(const VecF32 (&d)[kVPT], int s, float (&x)[4]) {
-    uint4 v = d[0].v;
+struct GroupWords<VecF32> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void get(const VecF32 (&d)[kVPT], int s, uint32_t (&w)[4]) {
+        uint4 v = d[0].v;
 #pragma unroll
-    for (int t = 1; t < kVPT; ++t)
-        if (s == t) v = d[t].v;
-    x[0] = __uint_as_float(v.x);
-    x[1] = __uint_as_float(v.y);
-    x[2] = __uint_as_float(v.z);
-    x[3] = __uint_as_float(v.w);
-}
+        for (int t = 1; t < kVPT; ++t)
+            if (s == t) v = d[t].v;
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    }
+    __device__ __forceinline__ static float value(const uint32_t (&w)[4], int k) { return __uint_as_float(w[k]); }
+};
+
+// Per-warp list of live groups in shared memory (raw words + first index).
+constexpr int kLiveMax = 32 * kVPT * 2;  // groups of four a warp can hold per chunk (bf16: 2 per vector)
+constexpr size_t kLiveBytesPerWarp = (size_t)kLiveMax * (2 * sizeof(uint32_t) + sizeof(int));
+constexpr size_t kLiveBytes = kLiveBytesPerWarp * kCW;
 
 // One staged chunk of a Gumbel-max row: z = x invT - shift_c is log p (correction)
 // or x / T (bonus).  Exact pruning, in order: the chunk or group bound
 // z + 17 < thr (no word gives more than 16.64 of noise), then per entry
 // 1 - u > 1.001 e^(z - thr) (g >= thr - z needs -log u <= e^(z - thr), and
-// -log u >= 1 - u).  A cheap unrolled pass marks the live groups of four; a
-// compact loop then draws one Philox block per live group.
+// -log u >= 1 - u).  Each lane appends its live groups of four to the warp's
+// list; the warp then draws one Philox block per listed group, 32 at a time, so
+// the work follows the number of live groups rather than the busiest lane.
 template <class Vec>
 __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase, int ct, const GumbelRow &gr,
                                              uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
-                                             uint32_t purpose, float tm, float thr, float &best, int &bidx) {
+                                             uint32_t purpose, float tm, float thr, unsigned char *live_buf,
+                                             float &best, int &bidx) {
+    using GW = GroupWords<Vec>;
     constexpr int G = Vec::VE / 4;  // groups of four per vector
+    const int lane = ct & 31;
     uint32_t live = 0;
     if (fmaf(tm, gr.invT, -gr.shift_c) + kGumbelMax >= thr) {
 #pragma unroll
@@ -805,19 +841,45 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase
             for (int g = 0; g < G; ++g)
                 if (fmaf(d[t].gmax(g), gr.invT, -gr.shift_c) + kGumbelMax >= thr) live |= 1u << (t * G + g);
     }
-    const bool aligned = (ebase & 3) == 0;
+    const int cnt = __popc(live);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total == 0) return;
+    constexpr int kItems = 32 * kVPT * G;  // most groups one warp can list per chunk
+    static_assert((size_t)kItems * (GW::N * sizeof(uint32_t) + sizeof(int)) <= kLiveBytesPerWarp,
+                  "live list exceeds its per-warp region");
+    uint32_t *lw = (uint32_t *)live_buf;
+    int *lv0 = (int *)(live_buf + (size_t)kItems * GW::N * sizeof(uint32_t));
+    int pos = incl - cnt;
 #pragma unroll 1
     while (live) {
         const int sl = __ffs(live) - 1;
         live &= live - 1;
-        float x[4];
-        slot_values(d, sl, x);
-        const int v0 = (int)(ebase + (int64_t)(ct + kCT * (sl / G)) * Vec::VE + 4 * (sl % G));
-        uint4 r4 = rand_group(seed, step, b, row, purpose, (uint32_t)v0 >> 2);
+        uint32_t w[4];
+        GW::get(d, sl, w);
+#pragma unroll
+        for (int q = 0; q < GW::N; ++q) lw[pos * GW::N + q] = w[q];
+        lv0[pos] = (int)(ebase + (int64_t)(ct + kCT * (sl / G)) * Vec::VE + 4 * (sl % G));
+        ++pos;
+    }
+    __syncwarp();
+    const bool aligned = (ebase & 3) == 0;
+#pragma unroll 1
+    for (int item = lane; item < total; item += 32) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < GW::N; ++q) w[q] = lw[item * GW::N + q];
+        const int v0 = lv0[item];
+        const uint4 r4 = rand_group(seed, step, b, row, purpose, (uint32_t)v0 >> 2);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int v = v0 + k;
-            const float z = fmaf(x[k], gr.invT, -gr.shift_c);
+            const float z = fmaf(GW::value(w, k), gr.invT, -gr.shift_c);
             const uint32_t wd = aligned ? word_of(r4, k) : rand_word_slow(seed, step, b, row, purpose, v);
             if (one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
                 const float sc = exact_score(gr, z, v, wd);
@@ -825,6 +887,7 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase
             }
         }
     }
+    __syncwarp();  // the list is rewritten by the next chunk
 }
 
 struct TailParams {
@@ -837,98 +900,87 @@ struct TailParams {
     uint32_t step;
     const Job *jobs;
     const int *job_list;
-    Part *parts;
-    int nseg;
+    uint32_t *job_best;  // [jobs] ord_of(best score seen), shared across CTAs
+    Part *parts;         // [chunk * kCW + warp]
     int stages;
     Ctrl *ctrl;
 };
 
+// What the producer tells the consumers about the chunk in a ring slot.
+struct SlotInfo {
+    int chunk;  // -1: no more chunks
+    int pad;
+    Job job;
+};
+
+// The tail hands chunks out dynamically (an atomic ticket per chunk): rows differ
+// several-fold in how many entries survive the bounds, so a static split would
+// leave the CTA with the hardest rows as the tail.  One partial per (chunk, warp).
 template <class Vec>
 __global__ void __launch_bounds__(kPipeThreads, 1) tail_kernel(TailParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     const Ring ring = ring_at(smem, p.stages);
-    Job *s_jobs = (Job *)(smem + ring_bytes(p.stages));
+    SlotInfo *s_slot = (SlotInfo *)(smem + ring_bytes(p.stages));
+    unsigned char *s_live = smem + ring_bytes(p.stages) + sizeof(SlotInfo) * kMaxStages;
     ring_init(ring);
     __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
     const Chunking ck = make_chunking(p.V, Vec::ESIZE);
-    const int G = gridDim.x;
     const int njobs = p.ctrl->job_count;
-    const int64_t total = (int64_t)njobs * ck.cpr;
+    const int total = njobs * ck.cpr;
     if (total == 0) return;
-    const int64_t c0 = cta_first(total, G, blockIdx.x), c1 = cta_first(total, G, blockIdx.x + 1);
-    if (c0 == c1) return;
-    const int first_row = (int)(c0 / ck.cpr);
-    const int nrows = (int)((c1 - 1) / ck.cpr) - first_row + 1;
-    const bool table = nrows <= kMaxDesc;
-    if (table)
-        for (int i = threadIdx.x; i < nrows; i += blockDim.x) s_jobs[i] = p.jobs[p.job_list[first_row + i]];
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t rowbytes = p.ld_row * Vec::ESIZE;
-    const int k0 = (int)(c0 - (int64_t)first_row * ck.cpr);
-    auto job_at = [&](int r) { return table ? s_jobs[r - first_row] : p.jobs[p.job_list[r]]; };
 
-    if (warp == kCW) {
-        if (lane == 0) {
-            int r = first_row, k = k0;
-            Job job = job_at(r);
-            ring_produce(ring, c0, c1, [&](int64_t) {
-                const char *row = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
-                const ChunkWin w = chunk_window(row, Vec::ESIZE, p.V, ck, k);
-                if (++k == ck.cpr) {
-                    k = 0;
-                    ++r;
-                    if (r < first_row + nrows) job = job_at(r);
-                }
-                return w;
-            }, &p.ctrl->err);
+    if (warp == kCW) {  // producer: take tickets, stage chunks, pass the job along
+        if (lane != 0) return;
+        int s = 0, cached = -1;
+        uint32_t ph = 0;
+        Job job;
+        for (;;) {
+            if (!mbar_wait(&ring.empty[s], ph ^ 1u, kWaitNs)) {
+                atomicOr(&p.ctrl->err, 1);
+                return;  // consumers give up on their own bounded waits
+            }
+            const int c = atomicAdd(&p.ctrl->tail_next, 1);
+            if (c >= total) {
+                s_slot[s].chunk = -1;
+                mbar_arrive(&ring.full[s]);
+                return;
+            }
+            const int r = c / ck.cpr;
+            if (r != cached) {
+                job = p.jobs[p.job_list[r]];
+                cached = r;
+            }
+            s_slot[s].chunk = c;
+            s_slot[s].job = job;
+            const char *row = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
+            const ChunkWin w = chunk_window(row, Vec::ESIZE, p.V, ck, c - r * ck.cpr);
+            mbar_arrive_expect_tx(&ring.full[s], w.bytes);
+            bulk_g2s(ring.stages + (size_t)s * kStageBytes, w.a0, w.bytes, &ring.full[s]);
+            if (++s == ring.n) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
-        return;
     }
 
     const int ct = threadIdx.x;
-    int r = first_row, k = k0;
-    Job job = job_at(r);
-    float m = kNegInf, best = kNegInf;
-    int bidx = -1;
-    bool seeded = false, nan_seen = false;
-    auto start_row = [&]() {
-        m = kNegInf;
-        nan_seen = false;
-        seeded = job.kind != JOB_BONUS;
-        best = job.kind == JOB_RESID ? job.seed_best : kNegInf;
-        bidx = job.kind == JOB_RESID ? job.seed_idx : -1;
-    };
-    start_row();
-    auto flush = [&]() {
-        Part out;
-        if (job.kind == JOB_ARGMAX) {
-            const bool any_nan = __any_sync(0xffffffffu, nan_seen);
-            float mm = m;
-            warp_argmax(mm, bidx);
-            out.m = any_nan ? __int_as_float(0x7fc00000) : mm;
-            out.best = 0.f;
-        } else {
-            out.m = warp_max_nan(m);
-            warp_argmax(best, bidx);
-            out.best = best;
-        }
-        out.s = 0.f;
-        out.idx = bidx;
-        if (lane == 0) p.parts[part_slot(blockIdx.x, p.nseg, r - first_row, warp)] = out;
-    };
-
     int st = 0;
     uint32_t ph = 0;
-    for (int64_t cc = c0; cc < c1; ++cc) {
+    for (;;) {
         if (!mbar_wait(&ring.full[st], ph, kWaitNs)) {
             atomicOr(&p.ctrl->err, 4);
             break;
         }
+        const int c = s_slot[st].chunk;
+        if (c < 0) break;
+        const Job job = s_slot[st].job;
+        const int r = c / ck.cpr;
         const char *trow = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
-        const ChunkWin w = chunk_window(trow, Vec::ESIZE, p.V, ck, k);
+        const ChunkWin w = chunk_window(trow, Vec::ESIZE, p.V, ck, c - r * ck.cpr);
         Vec d[kVPT];
         load_chunk(d, ring.stages + (size_t)st * kStageBytes, w, ct);
         __syncwarp();
@@ -939,16 +991,29 @@ __global__ void __launch_bounds__(kPipeThreads, 1) tail_kernel(TailParams p) {
         }
         const int64_t ebase = (int64_t)w.e0 - w.shift;
         const float tm = chunk_max(d);
+        Part out;
+        out.s = 0.f;
         if (job.kind == JOB_ARGMAX) {
-            if (tm != tm) {
-                nan_seen = true;
-            } else if (tm > m) {
-                m = tm;
-                bidx = chunk_find(d, ebase, ct, tm);
-            }
+            const bool any_nan = __any_sync(0xffffffffu, tm != tm);
+            float mm = (tm == tm) ? tm : kNegInf;
+            int ii = (tm == tm && tm > kNegInf) ? chunk_find(d, ebase, ct, tm) : -1;
+            warp_argmax(mm, ii);
+            out.m = any_nan ? __int_as_float(0x7fc00000) : mm;
+            out.idx = ii;
+            out.best = 0.f;
         } else {
-            m = max_nan_f32(m, tm);
             const bool resid = job.kind == JOB_RESID;
+            float best = resid ? job.seed_best : kNegInf;
+            int bidx = resid ? job.seed_idx : -1;
+            if (!resid && tm == tm && tm > kNegInf) {  // bonus: seed the bound with each lane's largest entry
+                const int v = chunk_find(d, ebase, ct, tm);
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row, PURPOSE_BONUS,
+                                            (uint32_t)v >> 2);
+                best = tm * job.invT + gumbel_of_word(word_of(r4, v & 3));
+                bidx = v;
+            }
+            // bound: the best score any warp has published for this job so far
+            const float thr = fmaxf(warp_max(best), float_of_ord(p.job_best[r]));
             GumbelRow gr;
             gr.drow = (const char *)p.draft + ((int64_t)job.b * p.Kmax + job.row) * rowbytes;
             gr.dtype = p.dtype;
@@ -956,29 +1021,16 @@ __global__ void __launch_bounds__(kPipeThreads, 1) tail_kernel(TailParams p) {
             gr.invT = job.invT;
             gr.shift_c = resid ? job.Ct : 0.f;
             gr.Cd = job.Cd;
-            if (!seeded) {  // bonus: seed the bound with each lane's largest entry
-                seeded = true;
-                if (tm == tm && tm > kNegInf) {
-                    const int v = chunk_find(d, ebase, ct, tm);
-                    const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row, PURPOSE_BONUS,
-                                                (uint32_t)v >> 2);
-                    best = tm * job.invT + gumbel_of_word(word_of(r4, v & 3));
-                    bidx = v;
-                }
-            }
-            const float thr = warp_max(best);
             gumbel_chunk(d, ebase, ct, gr, p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row,
-                         resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS, tm, thr, best, bidx);
+                         resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS, tm, thr, s_live + kLiveBytesPerWarp * warp,
+                         best, bidx);
+            out.m = warp_max_nan(tm);
+            warp_argmax(best, bidx);
+            out.best = best;
+            out.idx = bidx;
+            if (lane == 0 && bidx >= 0) atomicMax(&p.job_best[r], ord_of(best));
         }
-        if (++k == ck.cpr || cc + 1 == c1) {  // row segment ends
-            flush();
-            k = 0;
-            ++r;
-            if (r < first_row + nrows) {
-                job = job_at(r);
-                start_row();
-            }
-        }
+        if (lane == 0) p.parts[(int64_t)c * kCW + warp] = out;
     }
 }
 
@@ -987,7 +1039,7 @@ struct FinalParams {
     const void *target;
     int dtype;
     int64_t ld_row;
-    int Kmax, V, G, cpr, nseg;
+    int Kmax, V, cpr;
     uint64_t seed;
     uint32_t step;
     const Job *jobs;
@@ -1008,16 +1060,14 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(FinalParams p) {
     const int njobs = p.ctrl->job_count;
     if (jb >= njobs) return;
     const Job job = p.jobs[p.job_list[jb]];
-    const int64_t total = (int64_t)njobs * p.cpr;
-    const RowParts rp = row_parts(total, p.G, p.cpr, jb);
     float m = kNegInf, best = kNegInf;
     int idx = -1;
-    for (int q = lane; q < rp.n(); q += 32) {
-        const Part *pt = part_of(p.parts, total, p.G, p.cpr, p.nseg, jb, rp, q);
-        if (!pt) continue;
-        m = max_nan_f32(m, pt->m);
-        const float sc = job.kind == JOB_ARGMAX ? pt->m : pt->best;
-        if (better(sc, pt->idx, best, idx)) { best = sc; idx = pt->idx; }
+    const Part *parts = p.parts + (int64_t)jb * p.cpr * kCW;
+    for (int q = lane; q < p.cpr * kCW; q += 32) {
+        const Part pt = parts[q];
+        m = max_nan_f32(m, pt.m);
+        const float sc = job.kind == JOB_ARGMAX ? pt.m : pt.best;
+        if (better(sc, pt.idx, best, idx)) { best = sc; idx = pt.idx; }
     }
     m = warp_max_nan(m);
     warp_argmax(best, idx);
@@ -1120,8 +1170,8 @@ struct ProfScope {
 };
 
 struct Layout {
-    size_t off_ctrl, off_row_start, off_parts, off_jobs, off_job_list, off_parts2, total;
-    int nseg, nseg2, G, cpr;
+    size_t off_ctrl, off_row_start, off_parts, off_jobs, off_job_list, off_job_best, off_parts2, total;
+    int nseg, G, cpr;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1132,7 +1182,6 @@ Layout make_layout(int B, int Kmax, int V, int esz, int sms, int main_rows_per_r
     const Chunking ck = make_chunking(V, esz);
     L.cpr = ck.cpr;
     L.nseg = segs_per_cta((int64_t)B * main_rows_per_request * ck.cpr, L.G, ck.cpr);
-    L.nseg2 = segs_per_cta((int64_t)B * ck.cpr, L.G, ck.cpr);
     size_t o = 0;
     L.off_ctrl = o;
     o = align256(o + sizeof(Ctrl));
@@ -1144,8 +1193,10 @@ Layout make_layout(int B, int Kmax, int V, int esz, int sms, int main_rows_per_r
     o = align256(o + sizeof(Job) * (size_t)B);
     L.off_job_list = o;
     o = align256(o + sizeof(int) * (size_t)B);
+    L.off_job_best = o;
+    o = align256(o + sizeof(uint32_t) * (size_t)B);
     L.off_parts2 = o;
-    o = align256(o + sizeof(Part) * (size_t)L.G * L.nseg2 * kCW);
+    o = align256(o + sizeof(Part) * (size_t)B * ck.cpr * kCW);
     L.total = o;
     return L;
 }
@@ -1180,7 +1231,7 @@ int stages_for(size_t extra) {
     return n > kMaxStages ? kMaxStages : n;
 }
 size_t main_extra(int B) { return sizeof(int) * (size_t)(((B + 1) + 3) & ~3) + sizeof(MainRow) * kMaxDesc; }
-constexpr size_t kTailExtra = sizeof(Job) * kMaxDesc;
+constexpr size_t kTailExtra = sizeof(SlotInfo) * kMaxStages + kLiveBytes;
 
 template <class Vec>
 int set_smem_attrs(int dev, size_t main_smem) {
@@ -1295,6 +1346,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     ap.out_status = out_status;
     ap.jobs = (Job *)(w + L.off_jobs);
     ap.job_list = (int *)(w + L.off_job_list);
+    ap.job_best = (uint32_t *)(w + L.off_job_best);
     ap.ctrl = ctrl;
 
     TailParams tp;
@@ -1309,7 +1361,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     tp.jobs = ap.jobs;
     tp.job_list = ap.job_list;
     tp.parts = (Part *)(w + L.off_parts2);
-    tp.nseg = L.nseg2;
+    tp.job_best = (uint32_t *)(w + L.off_job_best);
     tp.stages = stages_for(kTailExtra);
     tp.ctrl = ctrl;
 
@@ -1319,9 +1371,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     fp.ld_row = ld_row;
     fp.Kmax = Kmax;
     fp.V = V;
-    fp.G = L.G;
     fp.cpr = L.cpr;
-    fp.nseg = L.nseg2;
     fp.seed = seed;
     fp.step = (uint32_t)step;
     fp.jobs = ap.jobs;
