@@ -74,8 +74,6 @@ struct Job {
 struct Ctrl {
     int err;        // non-zero: a bounded wait gave up
     int job_count;  // jobs queued by accept_kernel
-    int tail_next;  // next tail chunk to hand out
-    int pad;
 };
 
 // Order-preserving map of a float onto uint32 (for atomicMax on scores).
@@ -194,22 +192,24 @@ __device__ __forceinline__ void load_chunk(Vec (&d)[kVPT], const char *stage, co
     }
 }
 
-template <class Vec>
-__device__ __forceinline__ float chunk_max(const Vec (&d)[kVPT]) {
+template <class Vec, int NV>
+__device__ __forceinline__ float chunk_max(const Vec (&d)[NV]) {
     float tm = d[0].vmax();
 #pragma unroll
-    for (int t = 1; t < kVPT; ++t) tm = max_nan_f32(tm, d[t].vmax());
+    for (int t = 1; t < NV; ++t) tm = max_nan_f32(tm, d[t].vmax());
     return tm;
 }
 
-template <class Vec>
-__device__ __forceinline__ int chunk_find(const Vec (&d)[kVPT], int64_t ebase, int ct, float x) {
+// First entry equal to x among a thread's vectors; vector t of thread ct holds
+// entries ebase + (ct + STRIDE t) VE + e.
+template <int STRIDE, class Vec, int NV>
+__device__ __forceinline__ int chunk_find(const Vec (&d)[NV], int64_t ebase, int ct, float x) {
     int found = -1;
 #pragma unroll
-    for (int t = 0; t < kVPT; ++t)
+    for (int t = 0; t < NV; ++t)
 #pragma unroll
         for (int e = 0; e < Vec::VE; ++e)
-            if (found < 0 && d[t].get(e) == x) found = (int)(ebase + (int64_t)(ct + kCT * t) * Vec::VE + e);
+            if (found < 0 && d[t].get(e) == x) found = (int)(ebase + (int64_t)(ct + STRIDE * t) * Vec::VE + e);
     return found;
 }
 
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
                     s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
                     m = tm;
                     mc = mcn;
-                    aidx = chunk_find(d, ebase, ct, tm);
+                    aidx = chunk_find<kCT>(d, ebase, ct, tm);
                     cs = chunk_expsum(d, mr.c, mc);
                 } else if (m == kNegInf) {
                     cs = 0.f;  // every entry so far is -inf
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
                 nan_seen = true;
             } else if (tm > m) {
                 m = tm;
-                aidx = chunk_find(d, ebase, ct, tm);
+                aidx = chunk_find<kCT>(d, ebase, ct, tm);
             }
         }
         if (++k == ck.cpr || cc + 1 == c1) {  // row segment ends
@@ -782,10 +782,11 @@ struct GroupWords;
 template <>
 struct GroupWords<VecBF16> {
     static constexpr int N = 2;  // 4 bf16 = 2 words
-    __device__ __forceinline__ static void get(const VecBF16 (&d)[kVPT], int s, uint32_t (&w)[4]) {
+    template <int NV>
+    __device__ __forceinline__ static void get(const VecBF16 (&d)[NV], int s, uint32_t (&w)[4]) {
         uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-        for (int t = 0; t < kVPT; ++t) {
+        for (int t = 0; t < NV; ++t) {
             if (s == 2 * t) { w0 = d[t].v.x; w1 = d[t].v.y; }
             if (s == 2 * t + 1) { w0 = d[t].v.z; w1 = d[t].v.w; }
         }
@@ -800,10 +801,11 @@ struct GroupWords<VecBF16> {
 template <>
 struct GroupWords<VecF32> {
     static constexpr int N = 4;
-    __device__ __forceinline__ static void get(const VecF32 (&d)[kVPT], int s, uint32_t (&w)[4]) {
+    template <int NV>
+    __device__ __forceinline__ static void get(const VecF32 (&d)[NV], int s, uint32_t (&w)[4]) {
         uint4 v = d[0].v;
 #pragma unroll
-        for (int t = 1; t < kVPT; ++t)
+        for (int t = 1; t < NV; ++t)
             if (s == t) v = d[t].v;
         w[0] = v.x;
         w[1] = v.y;
@@ -813,10 +815,16 @@ struct GroupWords<VecF32> {
     __device__ __forceinline__ static float value(const uint32_t (&w)[4], int k) { return __uint_as_float(w[k]); }
 };
 
+// Tail pass: one warp per unit of 32 lanes x kVPT vectors of a row, loaded with its
+// own 16-byte loads (one extra vector per lane covers a window that does not start
+// on a 16-byte boundary).
+constexpr int kTailNV = kVPT + 1;
+constexpr int kTailWarps = 8;
+constexpr int kTailThreads = kTailWarps * 32;
+constexpr int kTailBlocksPerSM = 3;
 // Per-warp list of live groups in shared memory (raw words + first index).
-constexpr int kLiveMax = 32 * kVPT * 2;  // groups of four a warp can hold per chunk (bf16: 2 per vector)
+constexpr int kLiveMax = 32 * kTailNV * 2;  // groups of four a warp can hold per unit (bf16: 2 per vector)
 constexpr size_t kLiveBytesPerWarp = (size_t)kLiveMax * (2 * sizeof(uint32_t) + sizeof(int));
-constexpr size_t kLiveBytes = kLiveBytesPerWarp * kCW;
 
 // One staged chunk of a Gumbel-max row: z = x invT - shift_c is log p (correction)
 // or x / T (bonus).  Exact pruning, in order: the chunk or group bound
@@ -825,8 +833,8 @@ constexpr size_t kLiveBytes = kLiveBytesPerWarp * kCW;
 // -log u >= 1 - u).  Each lane appends its live groups of four to the warp's
 // list; the warp then draws one Philox block per listed group, 32 at a time, so
 // the work follows the number of live groups rather than the busiest lane.
-template <class Vec>
-__device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase, int ct, const GumbelRow &gr,
+template <int STRIDE, class Vec, int NV>
+__device__ __forceinline__ void gumbel_chunk(const Vec (&d)[NV], int64_t ebase, int ct, const GumbelRow &gr,
                                              uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
                                              uint32_t purpose, float tm, float thr, unsigned char *live_buf,
                                              float &best, int &bidx) {
@@ -836,7 +844,7 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase
     uint32_t live = 0;
     if (fmaf(tm, gr.invT, -gr.shift_c) + kGumbelMax >= thr) {
 #pragma unroll
-        for (int t = 0; t < kVPT; ++t)
+        for (int t = 0; t < NV; ++t)
 #pragma unroll
             for (int g = 0; g < G; ++g)
                 if (fmaf(d[t].gmax(g), gr.invT, -gr.shift_c) + kGumbelMax >= thr) live |= 1u << (t * G + g);
@@ -850,7 +858,7 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (total == 0) return;
-    constexpr int kItems = 32 * kVPT * G;  // most groups one warp can list per chunk
+    constexpr int kItems = 32 * NV * G;  // most groups one warp can list per chunk
     static_assert((size_t)kItems * (GW::N * sizeof(uint32_t) + sizeof(int)) <= kLiveBytesPerWarp,
                   "live list exceeds its per-warp region");
     uint32_t *lw = (uint32_t *)live_buf;
@@ -864,7 +872,7 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[kVPT], int64_t ebase
         GW::get(d, sl, w);
 #pragma unroll
         for (int q = 0; q < GW::N; ++q) lw[pos * GW::N + q] = w[q];
-        lv0[pos] = (int)(ebase + (int64_t)(ct + kCT * (sl / G)) * Vec::VE + 4 * (sl % G));
+        lv0[pos] = (int)(ebase + (int64_t)(ct + STRIDE * (sl / G)) * Vec::VE + 4 * (sl % G));
         ++pos;
     }
     __syncwarp();
@@ -900,95 +908,64 @@ struct TailParams {
     uint32_t step;
     const Job *jobs;
     const int *job_list;
-    uint32_t *job_best;  // [jobs] ord_of(best score seen), shared across CTAs
-    Part *parts;         // [chunk * kCW + warp]
-    int stages;
+    uint32_t *job_best;  // [jobs] ord_of(best score seen), shared across warps
+    Part *parts;         // [job * units per row + unit]
     Ctrl *ctrl;
 };
 
-// What the producer tells the consumers about the chunk in a ring slot.
-struct SlotInfo {
-    int chunk;  // -1: no more chunks
-    int pad;
-    Job job;
-};
-
-// The tail hands chunks out dynamically (an atomic ticket per chunk): rows differ
-// several-fold in how many entries survive the bounds, so a static split would
-// leave the CTA with the hardest rows as the tail.  One partial per (chunk, warp).
-template <class Vec>
-__global__ void __launch_bounds__(kPipeThreads, 1) tail_kernel(TailParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const Ring ring = ring_at(smem, p.stages);
-    SlotInfo *s_slot = (SlotInfo *)(smem + ring_bytes(p.stages));
-    unsigned char *s_live = smem + ring_bytes(p.stages) + sizeof(SlotInfo) * kMaxStages;
-    ring_init(ring);
-    __syncthreads();
-    pdl_wait();
-    pdl_launch_dependents();
-    const Chunking ck = make_chunking(p.V, Vec::ESIZE);
-    const int njobs = p.ctrl->job_count;
-    const int total = njobs * ck.cpr;
-    if (total == 0) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t rowbytes = p.ld_row * Vec::ESIZE;
-
-    if (warp == kCW) {  // producer: take tickets, stage chunks, pass the job along
-        if (lane != 0) return;
-        int s = 0, cached = -1;
-        uint32_t ph = 0;
-        Job job;
-        for (;;) {
-            if (!mbar_wait(&ring.empty[s], ph ^ 1u, kWaitNs)) {
-                atomicOr(&p.ctrl->err, 1);
-                return;  // consumers give up on their own bounded waits
-            }
-            const int c = atomicAdd(&p.ctrl->tail_next, 1);
-            if (c >= total) {
-                s_slot[s].chunk = -1;
-                mbar_arrive(&ring.full[s]);
-                return;
-            }
-            const int r = c / ck.cpr;
-            if (r != cached) {
-                job = p.jobs[p.job_list[r]];
-                cached = r;
-            }
-            s_slot[s].chunk = c;
-            s_slot[s].job = job;
-            const char *row = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
-            const ChunkWin w = chunk_window(row, Vec::ESIZE, p.V, ck, c - r * ck.cpr);
-            mbar_arrive_expect_tx(&ring.full[s], w.bytes);
-            bulk_g2s(ring.stages + (size_t)s * kStageBytes, w.a0, w.bytes, &ring.full[s]);
-            if (++s == ring.n) {
-                s = 0;
-                ph ^= 1u;
-            }
+// Loads one unit's window straight from global memory; out-of-window entries -inf.
+// Vector t of lane l holds entries ebase + (l + 32 t) VE + e.
+template <class Vec, int NV>
+__device__ __forceinline__ void load_unit(Vec (&d)[NV], const ChunkWin &w, int lane) {
+    const int nvec = (int)(w.bytes >> 4);
+    const int64_t ebase = (int64_t)w.e0 - w.shift;
+#pragma unroll
+    for (int t = 0; t < NV; ++t) {
+        const int j = lane + 32 * t;
+        d[t] = j < nvec ? Vec::load(w.a0, j) : Vec::neg_inf();
+    }
+    if (w.shift != 0 || ebase + (int64_t)nvec * Vec::VE != w.e1) {
+#pragma unroll
+        for (int t = 0; t < NV; ++t) {
+            const int j = lane + 32 * t;
+            if (j < nvec && (j == 0 || j == nvec - 1)) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, w.e0, w.e1);
         }
     }
+}
 
-    const int ct = threadIdx.x;
-    int st = 0;
-    uint32_t ph = 0;
-    for (;;) {
-        if (!mbar_wait(&ring.full[st], ph, kWaitNs)) {
-            atomicOr(&p.ctrl->err, 4);
-            break;
+// One row per job: the correction (Gumbel-max over log(p - q)), the bonus draw
+// (Gumbel-max over x / T) or the greedy argmax.  Rows are cut into units of
+// 32 x kVPT vectors; every warp takes a contiguous range of units (so it loads a
+// job's descriptor about once), loads them itself and writes one partial per
+// unit.  The work is latency-bound, so the kernel runs many independent warps
+// rather than a shared-memory ring.
+template <class Vec>
+__global__ void __launch_bounds__(kTailThreads, kTailBlocksPerSM) tail_kernel(TailParams p) {
+    __shared__ __align__(16) unsigned char s_live[kTailWarps * kLiveBytesPerWarp];
+    pdl_wait();
+    pdl_launch_dependents();
+    constexpr int UE = 32 * kVPT * Vec::VE;  // entries per unit
+    const Chunking uk = {(p.V + UE - 1) / UE, UE};
+    const int njobs = p.ctrl->job_count;
+    const int64_t total = (int64_t)njobs * uk.cpr;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * kTailWarps, gw = (int64_t)blockIdx.x * kTailWarps + warp;
+    const int64_t u0 = total * gw / nw, u1 = total * (gw + 1) / nw;
+    const int64_t rowbytes = p.ld_row * Vec::ESIZE;
+    unsigned char *live_buf = s_live + kLiveBytesPerWarp * warp;
+    int cached = -1;
+    Job job;
+    for (int64_t u = u0; u < u1; ++u) {
+        const int r = (int)(u / uk.cpr);
+        if (r != cached) {
+            job = p.jobs[p.job_list[r]];
+            cached = r;
         }
-        const int c = s_slot[st].chunk;
-        if (c < 0) break;
-        const Job job = s_slot[st].job;
-        const int r = c / ck.cpr;
         const char *trow = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
-        const ChunkWin w = chunk_window(trow, Vec::ESIZE, p.V, ck, c - r * ck.cpr);
-        Vec d[kVPT];
-        load_chunk(d, ring.stages + (size_t)st * kStageBytes, w, ct);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ring.empty[st]);
-        if (++st == ring.n) {
-            st = 0;
-            ph ^= 1u;
-        }
+        const ChunkWin w = chunk_window(trow, Vec::ESIZE, p.V, uk, (int)(u - (int64_t)r * uk.cpr));
+        const uint32_t published = p.job_best[r];
+        Vec d[kTailNV];
+        load_unit(d, w, lane);
         const int64_t ebase = (int64_t)w.e0 - w.shift;
         const float tm = chunk_max(d);
         Part out;
@@ -996,7 +973,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) tail_kernel(TailParams p) {
         if (job.kind == JOB_ARGMAX) {
             const bool any_nan = __any_sync(0xffffffffu, tm != tm);
             float mm = (tm == tm) ? tm : kNegInf;
-            int ii = (tm == tm && tm > kNegInf) ? chunk_find(d, ebase, ct, tm) : -1;
+            int ii = (tm == tm && tm > kNegInf) ? chunk_find<32>(d, ebase, lane, tm) : -1;
             warp_argmax(mm, ii);
             out.m = any_nan ? __int_as_float(0x7fc00000) : mm;
             out.idx = ii;
@@ -1006,14 +983,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1) tail_kernel(TailParams p) {
             float best = resid ? job.seed_best : kNegInf;
             int bidx = resid ? job.seed_idx : -1;
             if (!resid && tm == tm && tm > kNegInf) {  // bonus: seed the bound with each lane's largest entry
-                const int v = chunk_find(d, ebase, ct, tm);
+                const int v = chunk_find<32>(d, ebase, lane, tm);
                 const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row, PURPOSE_BONUS,
                                             (uint32_t)v >> 2);
                 best = tm * job.invT + gumbel_of_word(word_of(r4, v & 3));
                 bidx = v;
             }
             // bound: the best score any warp has published for this job so far
-            const float thr = fmaxf(warp_max(best), float_of_ord(p.job_best[r]));
+            const float thr = fmaxf(warp_max(best), float_of_ord(published));
             GumbelRow gr;
             gr.drow = (const char *)p.draft + ((int64_t)job.b * p.Kmax + job.row) * rowbytes;
             gr.dtype = p.dtype;
@@ -1021,16 +998,15 @@ __global__ void __launch_bounds__(kPipeThreads, 1) tail_kernel(TailParams p) {
             gr.invT = job.invT;
             gr.shift_c = resid ? job.Ct : 0.f;
             gr.Cd = job.Cd;
-            gumbel_chunk(d, ebase, ct, gr, p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row,
-                         resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS, tm, thr, s_live + kLiveBytesPerWarp * warp,
-                         best, bidx);
+            gumbel_chunk<32>(d, ebase, lane, gr, p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row,
+                             resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS, tm, thr, live_buf, best, bidx);
             out.m = warp_max_nan(tm);
             warp_argmax(best, bidx);
             out.best = best;
             out.idx = bidx;
             if (lane == 0 && bidx >= 0) atomicMax(&p.job_best[r], ord_of(best));
         }
-        if (lane == 0) p.parts[(int64_t)c * kCW + warp] = out;
+        if (lane == 0) p.parts[u] = out;
     }
 }
 
@@ -1039,7 +1015,7 @@ struct FinalParams {
     const void *target;
     int dtype;
     int64_t ld_row;
-    int Kmax, V, cpr;
+    int Kmax, V, upr;
     uint64_t seed;
     uint32_t step;
     const Job *jobs;
@@ -1062,8 +1038,8 @@ __global__ void __launch_bounds__(kFinalThreads) final_kernel(FinalParams p) {
     const Job job = p.jobs[p.job_list[jb]];
     float m = kNegInf, best = kNegInf;
     int idx = -1;
-    const Part *parts = p.parts + (int64_t)jb * p.cpr * kCW;
-    for (int q = lane; q < p.cpr * kCW; q += 32) {
+    const Part *parts = p.parts + (int64_t)jb * p.upr;
+    for (int q = lane; q < p.upr; q += 32) {
         const Part pt = parts[q];
         m = max_nan_f32(m, pt.m);
         const float sc = job.kind == JOB_ARGMAX ? pt.m : pt.best;
@@ -1171,7 +1147,7 @@ struct ProfScope {
 
 struct Layout {
     size_t off_ctrl, off_row_start, off_parts, off_jobs, off_job_list, off_job_best, off_parts2, total;
-    int nseg, G, cpr;
+    int nseg, G, cpr, upr;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1195,8 +1171,10 @@ Layout make_layout(int B, int Kmax, int V, int esz, int sms, int main_rows_per_r
     o = align256(o + sizeof(int) * (size_t)B);
     L.off_job_best = o;
     o = align256(o + sizeof(uint32_t) * (size_t)B);
+    const int ue = 32 * kVPT * (16 / esz);  // entries per tail unit
+    L.upr = (V + ue - 1) / ue;
     L.off_parts2 = o;
-    o = align256(o + sizeof(Part) * (size_t)B * ck.cpr * kCW);
+    o = align256(o + sizeof(Part) * (size_t)B * L.upr);
     L.total = o;
     return L;
 }
@@ -1231,7 +1209,6 @@ int stages_for(size_t extra) {
     return n > kMaxStages ? kMaxStages : n;
 }
 size_t main_extra(int B) { return sizeof(int) * (size_t)(((B + 1) + 3) & ~3) + sizeof(MainRow) * kMaxDesc; }
-constexpr size_t kTailExtra = sizeof(SlotInfo) * kMaxStages + kLiveBytes;
 
 template <class Vec>
 int set_smem_attrs(int dev, size_t main_smem) {
@@ -1239,8 +1216,7 @@ int set_smem_attrs(int dev, size_t main_smem) {
     if (g_attr_set[dev][which]) return SPEC_OK;
     cudaError_t e = cudaFuncSetAttribute(main_kernel<Vec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)main_smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tail_kernel<Vec>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBudget);
+
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     g_attr_set[dev][which] = true;
     return SPEC_OK;
@@ -1254,7 +1230,6 @@ int launch_all(int dev, const Layout &L, const MainParams &mp, const AcceptParam
     cudaError_t e = cudaMemsetAsync(mp.ctrl, 0, sizeof(Ctrl), st);
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     const size_t main_smem = ring_bytes(mp.stages) + main_extra(mp.B);
-    const size_t tail_smem = ring_bytes(tp.stages) + kTailExtra;
     {
         ProfScope ps(st);
         main_kernel<Vec><<<L.G, kPipeThreads, main_smem, st>>>(mp);
@@ -1267,7 +1242,7 @@ int launch_all(int dev, const Layout &L, const MainParams &mp, const AcceptParam
     if (rc) return rc;
     {
         ProfScope ps(st);
-        rc = launch_pdl(tail_kernel<Vec>, dim3(L.G), dim3(kPipeThreads), tail_smem, st, tp);
+        rc = launch_pdl(tail_kernel<Vec>, dim3(L.G * kTailBlocksPerSM), dim3(kTailThreads), 0, st, tp);
     }
     if (rc) return rc;
     {
@@ -1362,7 +1337,6 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     tp.job_list = ap.job_list;
     tp.parts = (Part *)(w + L.off_parts2);
     tp.job_best = (uint32_t *)(w + L.off_job_best);
-    tp.stages = stages_for(kTailExtra);
     tp.ctrl = ctrl;
 
     FinalParams fp;
@@ -1371,7 +1345,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     fp.ld_row = ld_row;
     fp.Kmax = Kmax;
     fp.V = V;
-    fp.cpr = L.cpr;
+    fp.upr = L.upr;
     fp.seed = seed;
     fp.step = (uint32_t)step;
     fp.jobs = ap.jobs;
