@@ -825,6 +825,7 @@ constexpr int kTailBlocksPerSM = 3;
 // Per-warp list of live groups in shared memory (raw words + first index).
 constexpr int kLiveMax = 32 * kTailNV * 2;  // groups of four a warp can hold per unit (bf16: 2 per vector)
 constexpr size_t kLiveBytesPerWarp = (size_t)kLiveMax * (2 * sizeof(uint32_t) + sizeof(int));
+constexpr int kTailJobCache = 256;  // jobs whose descriptors each tail CTA keeps in shared memory
 
 // One staged chunk of a Gumbel-max row: z = x invT - shift_c is log p (correction)
 // or x / T (bonus).  Exact pruning, in order: the chunk or group bound
@@ -838,6 +839,8 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[NV], int64_t ebase, 
                                              uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
                                              uint32_t purpose, float tm, float thr, unsigned char *live_buf,
                                              float &best, int &bidx) {
+    // thr only ever holds an exact score of some entry (or -inf), so raising it to
+    // the warp's best as exact scores come in keeps the pruning exact.
     using GW = GroupWords<Vec>;
     constexpr int G = Vec::VE / 4;  // groups of four per vector
     const int lane = ct & 31;
@@ -863,35 +866,71 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[NV], int64_t ebase, 
                   "live list exceeds its per-warp region");
     uint32_t *lw = (uint32_t *)live_buf;
     int *lv0 = (int *)(live_buf + (size_t)kItems * GW::N * sizeof(uint32_t));
-    int pos = incl - cnt;
-#pragma unroll 1
-    while (live) {
-        const int sl = __ffs(live) - 1;
-        live &= live - 1;
-        uint32_t w[4];
-        GW::get(d, sl, w);
+    const int excl = incl - cnt;
 #pragma unroll
-        for (int q = 0; q < GW::N; ++q) lw[pos * GW::N + q] = w[q];
-        lv0[pos] = (int)(ebase + (int64_t)(ct + STRIDE * (sl / G)) * Vec::VE + 4 * (sl % G));
-        ++pos;
-    }
+    for (int t = 0; t < NV; ++t)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int sl = t * G + g;
+            if (!(live >> sl & 1u)) continue;
+            const int pos = excl + __popc(live & ((1u << sl) - 1u));
+            if (GW::N == 2) {
+                lw[pos * 2] = g == 0 ? d[t].v.x : d[t].v.z;
+                lw[pos * 2 + 1] = g == 0 ? d[t].v.y : d[t].v.w;
+            } else {
+                lw[pos * GW::N] = d[t].v.x;
+                lw[pos * GW::N + 1] = d[t].v.y;
+                lw[pos * GW::N + 2] = d[t].v.z;
+                lw[pos * GW::N + 3] = d[t].v.w;
+            }
+            lv0[pos] = (int)(ebase + (int64_t)(ct + STRIDE * t) * Vec::VE + 4 * g);
+        }
     __syncwarp();
     const bool aligned = (ebase & 3) == 0;
+    // Each lane takes two listed groups per round: their Philox blocks are
+    // independent, which keeps the scheduler busy through the 10-round chains.
 #pragma unroll 1
-    for (int item = lane; item < total; item += 32) {
-        uint32_t w[4];
+    for (int base = 0; base < total; base += 64) {
+        if (base) thr = fmaxf(thr, warp_max(best));  // later rounds prune against the best so far
+        uint32_t w[2][4];
+        int v0[2];
+        bool has[2];
+        uint4 r4[2];
 #pragma unroll
-        for (int q = 0; q < GW::N; ++q) w[q] = lw[item * GW::N + q];
-        const int v0 = lv0[item];
-        const uint4 r4 = rand_group(seed, step, b, row, purpose, (uint32_t)v0 >> 2);
+        for (int h = 0; h < 2; ++h) {
+            // (the first group of a row that starts off a 16-byte boundary has a
+            // negative base index: its leading entries are masked, the rest are real)
+            const int item = base + lane + 32 * h;
+            has[h] = item < total;
+            const int it2 = has[h] ? item : total - 1;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int v = v0 + k;
-            const float z = fmaf(GW::value(w, k), gr.invT, -gr.shift_c);
-            const uint32_t wd = aligned ? word_of(r4, k) : rand_word_slow(seed, step, b, row, purpose, v);
-            if (one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
-                const float sc = exact_score(gr, z, v, wd);
-                if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
+            for (int q = 0; q < GW::N; ++q) w[h][q] = lw[it2 * GW::N + q];
+            v0[h] = lv0[it2];
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) r4[h] = rand_group(seed, step, b, row, purpose, (uint32_t)v0[h] >> 2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!has[h]) continue;
+            if (aligned) {
+                // any survivor needs 1 - u_k <= e^(z_k - thr) <= e^(zmax - thr); the
+                // largest w >> 9 of the group gives the smallest 1 - u
+                const uint32_t kmax = max(max(r4[h].x >> 9, r4[h].y >> 9), max(r4[h].z >> 9, r4[h].w >> 9));
+                float xm = GW::value(w[h], 0);
+#pragma unroll
+                for (int k = 1; k < 4; ++k) xm = fmaxf(xm, GW::value(w[h], k));
+                const float zm = fmaf(xm, gr.invT, -gr.shift_c);
+                if (!(one_minus_u01(kmax << 9) <= ex2_approx((zm - thr) * kLog2e) * 1.001f)) continue;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int v = v0[h] + k;
+                const float z = fmaf(GW::value(w[h], k), gr.invT, -gr.shift_c);
+                const uint32_t wd = aligned ? word_of(r4[h], k) : rand_word_slow(seed, step, b, row, purpose, v);
+                if (one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
+                    const float sc = exact_score(gr, z, v, wd);
+                    if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
+                }
             }
         }
     }
@@ -942,6 +981,7 @@ __device__ __forceinline__ void load_unit(Vec (&d)[NV], const ChunkWin &w, int l
 template <class Vec>
 __global__ void __launch_bounds__(kTailThreads, kTailBlocksPerSM) tail_kernel(TailParams p) {
     __shared__ __align__(16) unsigned char s_live[kTailWarps * kLiveBytesPerWarp];
+    __shared__ Job s_jobs[kTailJobCache];
     pdl_wait();
     pdl_launch_dependents();
     constexpr int UE = 32 * kVPT * Vec::VE;  // entries per unit
@@ -950,17 +990,17 @@ __global__ void __launch_bounds__(kTailThreads, kTailBlocksPerSM) tail_kernel(Ta
     const int64_t total = (int64_t)njobs * uk.cpr;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kTailWarps, gw = (int64_t)blockIdx.x * kTailWarps + warp;
-    const int64_t u0 = total * gw / nw, u1 = total * (gw + 1) / nw;
     const int64_t rowbytes = p.ld_row * Vec::ESIZE;
     unsigned char *live_buf = s_live + kLiveBytesPerWarp * warp;
-    int cached = -1;
-    Job job;
-    for (int64_t u = u0; u < u1; ++u) {
+    const bool cache = njobs <= kTailJobCache;
+    if (cache)
+        for (int i = threadIdx.x; i < njobs; i += blockDim.x) s_jobs[i] = p.jobs[p.job_list[i]];
+    __syncthreads();
+    // Units are dealt round-robin: a row's units (whose cost depends on the row)
+    // spread over many warps instead of piling onto a few.
+    for (int64_t u = gw; u < total; u += nw) {
         const int r = (int)(u / uk.cpr);
-        if (r != cached) {
-            job = p.jobs[p.job_list[r]];
-            cached = r;
-        }
+        const Job job = cache ? s_jobs[r] : p.jobs[p.job_list[r]];
         const char *trow = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
         const ChunkWin w = chunk_window(trow, Vec::ESIZE, p.V, uk, (int)(u - (int64_t)r * uk.cpr));
         const uint32_t published = p.job_best[r];
