@@ -55,7 +55,9 @@ typedef enum {
     SPEC_EINVAL = 1,        /* bad argument (null pointer, size out of range) */
     SPEC_ECUDA = 2,         /* a CUDA runtime call or launch failed           */
     SPEC_EUNSUPPORTED = 3,  /* valid but outside what this build supports     */
-    SPEC_EWORKSPACE = 4     /* workspace pointer null or too small            */
+    SPEC_EWORKSPACE = 4,    /* workspace pointer null or too small            */
+    SPEC_ESCRATCH = 5       /* sizes need more than the fixed scratch of
+                               spec_verify_sample_noalloc                    */
 } spec_err;
 
 /* Logit element types. */
@@ -131,6 +133,38 @@ int spec_verify_sample(const void *target, const void *draft, int dtype, int B, 
                        const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
                        int32_t *out_accepted, float *out_p, float *out_q, int32_t *out_status, void *ws,
                        size_t ws_bytes, void *cuda_stream);
+
+/*
+ * spec_verify_sample without a workspace argument.  The method on the pages has no
+ * counterpart to this entry point: it exists for callers that cannot hand over
+ * device memory per call.  Examples are a C host program with no device allocator
+ * of its own, and a serving loop that sized its caches to fill the GPU at start-up
+ * and must not call cudaMalloc / cudaFree while decoding, since those calls can
+ * synchronise the whole device and stall the pipelined steps around them.
+ *
+ * Scratch is one array of SPEC_STATIC_SCRATCH_BYTES bytes that the library holds in
+ * its own module's device memory (one copy per device).  This entry point calls no
+ * allocating routine.  Arguments, outputs and results are those of
+ * spec_verify_sample, and the two agree on the same inputs.
+ *  - Set-up: the first call on each device looks the array's address up with that
+ *    device current (and sets the main kernel's shared-memory limit, as the
+ *    workspace entry points do).  Make that first call before any stream capture.
+ *  - Limit: sizes whose spec_verify_workspace_size(B, Kmax, V, dtype) exceeds
+ *    SPEC_STATIC_SCRATCH_BYTES return SPEC_ESCRATCH before anything is launched
+ *    (bf16, Kmax = 8 on a 152-SM device: B up to 512 fits at V = 151936, and B up
+ *    to 256 at V = 262144).
+ *  - Zeroing: the only scratch that must start at zero, a two-word control block,
+ *    is cleared on cuda_stream by every call before its first kernel.
+ *  - Races: every call on a device uses the same array, so two calls that can
+ *    overlap (different streams, or host threads without ordering between them)
+ *    corrupt each other's results.  Order the calls on one stream.
+ */
+#define SPEC_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+int spec_verify_sample_noalloc(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                               int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                               const float *temperature, uint64_t seed, uint64_t step,
+                               int32_t *out_tokens, int32_t *out_accepted, float *out_p, float *out_q,
+                               int32_t *out_status, void *cuda_stream);
 
 /*
  * Confidence-scheduled verify lengths ("DSpark paper review", Sec. 4.2.1 and

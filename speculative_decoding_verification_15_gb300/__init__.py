@@ -7,7 +7,7 @@ from . import _build, binding  # noqa: F401
 from .api import (schedule_verify_len, verify_greedy, verify_sample,  # noqa: F401
                   verify_sample_host, workspace)
 from .binding import (SpecError, spec_schedule_verify_len, spec_verify_greedy,  # noqa: F401
-                      spec_verify_sample, spec_verify_workspace_size)
+                      spec_verify_sample, spec_verify_sample_noalloc, spec_verify_workspace_size)
 
 
 def build(force: bool = False) -> str:

@@ -18,6 +18,7 @@ import torch
 from . import _build
 
 SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_EUNSUPPORTED, SPEC_EWORKSPACE = 0, 1, 2, 3, 4
+SPEC_ESCRATCH = 5
 SPEC_BF16, SPEC_F32 = 0, 1
 STATUS_OK, STATUS_BAD_TOKEN, STATUS_BAD_K, STATUS_BAD_TEMPERATURE, STATUS_NONFINITE = 0, 1, 2, 3, 4
 
@@ -58,6 +59,9 @@ def load(path: str | None = None):
         lib.spec_verify_sample.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P, P, P,
                                            P, SZ, P]
         lib.spec_verify_sample.restype = I32
+        lib.spec_verify_sample_noalloc.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P,
+                                                   P, P, P]
+        lib.spec_verify_sample_noalloc.restype = I32
         lib.spec_schedule_verify_len.argtypes = [P, P, I32, I32, P, I32, I32, I32, P, P, P]
         lib.spec_schedule_verify_len.restype = I32
         lib.spec_error_string.argtypes = [I32]
@@ -188,6 +192,39 @@ def spec_verify_sample(target, draft, draft_tokens, num_draft, temperature, seed
                                 _ptr(workspace), workspace.numel(), _stream_handle(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_verify_sample", rc, lib)
+
+
+def spec_verify_sample_noalloc(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int,
+                               out_tokens, out_accepted, out_p, out_q, out_status, stream=None) -> None:
+    """spec_verify_sample on the library's fixed per-device scratch (no workspace).
+    Calls on one device must not overlap; sizes beyond the scratch raise SpecError
+    with rc SPEC_ESCRATCH."""
+    lib = load()
+    K1 = target.shape[1]
+    Kmax = K1 - 1
+    B, V, ld = _logits_layout(target, K1)
+    dev = target.device
+    if draft.dtype != target.dtype or draft.device != dev:
+        raise TypeError("target and draft logits must share a dtype and a device")
+    if Kmax > 0 and _logits_layout(draft, Kmax) != (B, V, ld):
+        raise ValueError("draft logits must be [B, Kmax, V] with the target's row stride")
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, Kmax), dev)
+    if num_draft is not None:
+        _need(num_draft, "num_draft", torch.int32, (B,), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K1), dev)
+    _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
+    for t, n in ((out_p, "out_p"), (out_q, "out_q")):
+        if t is not None:
+            _need(t, n, torch.float32, (B, Kmax), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    rc = lib.spec_verify_sample_noalloc(_ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
+                                        _ptr(draft_tokens), _ptr(num_draft), _ptr(temperature),
+                                        int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_tokens),
+                                        _ptr(out_accepted), _ptr(out_p), _ptr(out_q), _ptr(out_status),
+                                        _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_sample_noalloc", rc, lib)
 
 
 def spec_schedule_verify_len(conf, max_len, step_time_us, budget: int, min_len: int, out_len, out_info=None,

@@ -1403,6 +1403,24 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
                               : launch_all<VecF32>(dev, L, mp, ap, tp, fp, st);
 }
 
+// Scratch of spec_verify_sample_noalloc: part of this module's device image, one
+// copy per device, so that entry point never calls an allocating routine.
+static __device__ __align__(256) unsigned char g_static_scratch[SPEC_STATIC_SCRATCH_BYTES];
+void *g_static_scratch_ptr[64];
+
+// Address of the current device's copy, looked up once with that device current.
+int static_scratch(int dev, void **out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_static_scratch_ptr[dev]) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
+        g_static_scratch_ptr[dev] = ptr;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1434,6 +1452,27 @@ int spec_verify_sample(const void *target, const void *draft, int dtype, int B, 
                        true);
 }
 
+int spec_verify_sample_noalloc(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                               int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                               const float *temperature, uint64_t seed, uint64_t step,
+                               int32_t *out_tokens, int32_t *out_accepted, float *out_p, float *out_q,
+                               int32_t *out_status, void *cuda_stream) {
+    if (B < 0 || Kmax < 0 || V <= 0 || ld_row < V) return SPEC_EINVAL;
+    if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_EINVAL;
+    if (B == 0) return SPEC_OK;
+    if (B > SPEC_MAX_BATCH || Kmax > SPEC_MAX_DRAFTS) return SPEC_EUNSUPPORTED;
+    int dev = 0, sms = 0;
+    int rc = device_info(&dev, &sms);
+    if (rc) return rc;
+    if (make_layout(B, Kmax, V, dtype == SPEC_BF16 ? 2 : 4, sms, 2 * Kmax).total > SPEC_STATIC_SCRATCH_BYTES)
+        return SPEC_ESCRATCH;
+    void *ws = nullptr;
+    if ((rc = static_scratch(dev, &ws))) return rc;
+    return verify_impl(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, temperature, seed,
+                       step, out_tokens, out_accepted, out_p, out_q, out_status, ws, SPEC_STATIC_SCRATCH_BYTES,
+                       cuda_stream, true);
+}
+
 const char *spec_error_string(int err) {
     switch (err) {
         case SPEC_OK: return "ok";
@@ -1441,6 +1480,7 @@ const char *spec_error_string(int err) {
         case SPEC_ECUDA: return "CUDA error";
         case SPEC_EUNSUPPORTED: return "unsupported size or layout";
         case SPEC_EWORKSPACE: return "workspace missing or too small";
+        case SPEC_ESCRATCH: return "sizes need more than the fixed scratch of spec_verify_sample_noalloc";
         default: return "unknown error";
     }
 }
