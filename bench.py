@@ -299,7 +299,7 @@ def run_ours(args) -> None:
     if rank == 0:
         peak, peak_kind = hbm_peak()
         achieved = main_bytes / (rows_ms * 1e-3) / 1e9
-        cpu = oracle_cpu_rate(batch, 3, min_seconds=2.0, max_reps=8) if world == 1 else None
+        cpu = oracle_cpu_rate(batch, 3, min_seconds=12.0, max_reps=1000) if world == 1 else None
         clocks = clk.summary()
         line = {
             "metric": METRIC, "value": world * verified * args.steps / (total_ms * 1e-3), "unit": UNIT,
