@@ -130,6 +130,31 @@ def dist_setup():
     return world, rank, local
 
 
+def replica_batch(rank: int) -> dict:
+    """The requests rank `rank` verifies: replicas share no request (the data seed
+    differs per rank), so ranks never exchange data."""
+    import synth
+
+    return synth.main(step=rank)
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over the ranks of the default process group (x with one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: units every rank processed over the slowest rank's time."""
+    return world * units_per_step * steps / (total_ms * 1e-3)
+
+
 def oracle_cpu_rate(batch: dict, seed: int, min_seconds: float, max_reps: int) -> dict:
     """Time the fp64 oracle on the host cores over whole copies of the batch."""
     import oracle
@@ -202,7 +227,7 @@ def run_ours(args) -> None:
     import speculative_decoding_verification_15_gb300 as pkg
     from speculative_decoding_verification_15_gb300 import binding
 
-    batch = synth.main(step=rank)
+    batch = replica_batch(rank)
     B, K, V = batch["B"], batch["K"], batch["V"]
     t = batch["target"].to(dev)
     d = batch["draft"].to(dev)
@@ -261,10 +286,7 @@ def run_ours(args) -> None:
         kern_ms.append(binding.profile_read(4))  # waits for this step's kernel events
     binding.profile_enable(False)
     total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dev)
     assert int((st != 0).sum()) == 0, "a request reported a non-zero status"
     emitted = int(acc.sum().item()) + B
     rows_ms = statistics.mean(k[0] for k in kern_ms)
@@ -302,7 +324,7 @@ def run_ours(args) -> None:
         cpu = oracle_cpu_rate(batch, 3, min_seconds=12.0, max_reps=1000) if world == 1 else None
         clocks = clk.summary()
         line = {
-            "metric": METRIC, "value": world * verified * args.steps / (total_ms * 1e-3), "unit": UNIT,
+            "metric": METRIC, "value": job_rate(world, verified, args.steps, total_ms), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",

@@ -14,7 +14,7 @@
 //  main_kernel    streams the rows of every draft position once -- target and draft
 //                 rows of sampling requests, target rows of greedy ones -- through a
 //                 bulk-copy (TMA) ring in shared memory: one persistent CTA per SM, a
-//                 producer warp issuing 16 KB cp.async.bulk copies, eight consumer
+//                 producer warp issuing 32 KB cp.async.bulk copies, sixteen consumer
 //                 warps reducing them.  Per (CTA, row, warp): max, sum of
 //                 2^(x log2e / T - max'), and the lowest argmax.  HBM-bound.
 //  accept_kernel  one CTA per request: combines the partials of its rows, sets the
@@ -22,9 +22,10 @@
 //                 emits the accepted drafts, and queues one job: the correction at
 //                 the first rejected row j (seeded with the segment argmaxes of row
 //                 j), the bonus draw on row k_b, or the greedy argmax of row k_b.
-//  tail_kernel    streams the one row of each job through the same ring: Gumbel-max
-//                 over log(max(0, p - q)) (draft values gathered only at entries
-//                 that can still win), Gumbel-max over the target row, or argmax.
+//  tail_kernel    one warp per 1024-entry unit of each job's row, loaded with its
+//                 own 16-byte loads: Gumbel-max over log(max(0, p - q)) (draft values
+//                 gathered only at entries that can still win), Gumbel-max over the
+//                 target row, or argmax.
 //  final_kernel   one warp per job: combines the tail partials into the token.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -929,7 +930,9 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[NV], int64_t ebase, 
                 const uint32_t wd = aligned ? word_of(r4[h], k) : rand_word_slow(seed, step, b, row, purpose, v);
                 if (one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
                     const float sc = exact_score(gr, z, v, wd);
-                    if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
+                    // -inf: no residual mass at v, never a candidate (a row without any
+                    // must reach the degenerate fallback)
+                    if (sc > kNegInf && better(sc, v, best, bidx)) { best = sc; bidx = v; }
                 }
             }
         }

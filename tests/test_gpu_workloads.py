@@ -1,0 +1,139 @@
+"""GPU parity on the five synthetic workloads at their full sizes, through the C ABI,
+in the configuration bench.py times (one call per step, the library's own launch
+shapes): the tiny 1000-step run in both modes, the B=8 bf16 batch, the B=64 K=7
+V=151936 bf16 batch (sampling and greedy), the confidence-scheduled ragged batch,
+and the mixed greedy/sampling fp32 stress batch with adversarial requests.
+
+Greedy results must be bit-exact.  Sampling results must equal the oracle's on
+every request it does not flag as a near-tie; flagged requests are counted and
+must stay rare.  p(x_i) and q(x_i) must be within 1e-5 of the oracle's."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import compare_sample, run_gpu_sample, to_dev
+
+pytestmark = pytest.mark.gpu
+
+CORES = len(os.sched_getaffinity(0))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def _oracle_sample(batch, seed, step):
+    nd = batch.get("num_draft")
+    return oracle.verify_sample(synth.as_oracle_array(batch["target"]), synth.as_oracle_array(batch["draft"]),
+                                batch["draft_tokens"].numpy(), None if nd is None else np.asarray(nd),
+                                batch["temperature"].numpy(), seed, step, nthreads=CORES)
+
+
+def _gpu_greedy(batch):
+    import speculative_decoding_verification_15_gb300 as pkg
+
+    d = to_dev(batch)
+    out = pkg.verify_greedy(d["target"], d["draft_tokens"], num_draft=d["num_draft"])
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def _check_greedy(batch):
+    gpu = _gpu_greedy(batch)
+    nd = batch.get("num_draft")
+    ref = oracle.verify_greedy(synth.as_oracle_array(batch["target"]), batch["draft_tokens"].numpy(),
+                               None if nd is None else np.asarray(nd))
+    assert (gpu["status"] == ref["status"]).all()
+    assert (gpu["accepted"] == ref["accepted"]).all()
+    assert (gpu["tokens"] == ref["tokens"]).all()
+    return ref
+
+
+def test_tiny_1000_steps_both_modes():
+    """B=1, K=4, V=1024 fp32, T=1: 1000 steps of independent inputs and seeds."""
+    n = flagged = 0
+    for step in range(1000):
+        batch = synth.tiny(step)
+        _check_greedy(batch)
+        gpu = run_gpu_sample(batch, batch["seed"], step)
+        ref = _oracle_sample(batch, batch["seed"], step)
+        r = compare_sample(gpu, ref, batch["temperature"].numpy())
+        n += r["n"]
+        flagged += r["flagged"]
+    assert flagged <= n // 100, (flagged, n)
+
+
+def test_small_batch():
+    """B=8, K=8, V=32000 bf16, T=0.8, draft noise sigma in {0.25, 0.5, 1, 2}."""
+    n = flagged = 0
+    for step in range(4):
+        batch = synth.small(step)
+        gpu = run_gpu_sample(batch, batch["seed"], step)
+        ref = _oracle_sample(batch, batch["seed"], step)
+        r = compare_sample(gpu, ref, batch["temperature"].numpy())
+        n += r["n"]
+        flagged += r["flagged"]
+    assert flagged <= max(1, n // 20), (flagged, n)
+
+
+def test_main_batch_full_size():
+    """B=64, K=7, V=151936 bf16, T ~ U[0.6, 1]: the benchmarked workload, every request."""
+    n = flagged = 0
+    for step in range(2):
+        batch = synth.main(step)
+        gpu = run_gpu_sample(batch, batch["seed"], step)
+        ref = _oracle_sample(batch, batch["seed"], step)
+        r = compare_sample(gpu, ref, batch["temperature"].numpy())
+        n += r["n"]
+        flagged += r["flagged"]
+        assert (ref["status"] == 0).all()
+    assert flagged <= max(1, n // 20), (flagged, n)
+    # the same logits in greedy mode, bit-exact
+    _check_greedy(synth.main(0))
+
+
+def test_ragged_scheduled_batch():
+    """B=256, Kmax=16, V=129280 bf16: verify lengths from the scheduler (GPU, checked
+    against the oracle), then a ragged verify with k_b = L_b."""
+    import speculative_decoding_verification_15_gb300 as pkg
+
+    sch = synth.ragged_schedule_inputs(0)
+    conf, tau = sch["conf"], sch["step_time_us"]
+    L, info = pkg.schedule_verify_len(conf.cuda(), tau.cuda(), sch["budget"], sch["min_len"])
+    L = L.cpu().numpy()
+    ref_s = oracle.schedule_verify_len(conf.numpy(), None, tau.numpy(), sch["budget"], sch["min_len"])
+    if ref_s["flags"] == 0:
+        assert (L == ref_s["len"]).all()
+    assert L.min() >= 1 and L.max() <= 16 and int(L.sum()) <= sch["budget"]
+    batch = synth.ragged(0, num_draft=[int(v) for v in L])
+    gpu = run_gpu_sample(batch, batch["seed"], 0)
+    ref = _oracle_sample(batch, batch["seed"], 0)
+    r = compare_sample(gpu, ref, batch["temperature"].numpy())
+    assert r["flagged"] <= max(1, r["n"] // 20), r
+
+
+def test_stress_mixed_adversarial():
+    """B=512, K=4, V=151936 fp32; even requests greedy, odd sampling at T=1, with
+    q == p, proposals outside p's top-50, and exact ties at the argmax."""
+    batch = synth.stress(0)
+    gpu = run_gpu_sample(batch, batch["seed"], 0)
+    ref = _oracle_sample(batch, batch["seed"], 0)
+    T = batch["temperature"].numpy()
+    r = compare_sample(gpu, ref, T)
+    assert r["flagged"] <= max(1, r["n"] // 20), r
+    assert (gpu["status"] == 0).all()
+    kinds = batch["kinds"]
+    K = batch["K"]
+    for b, kind in enumerate(kinds):
+        if kind == "q_eq_p":      # u q < p with q == p: every draft accepted
+            assert gpu["accepted"][b] == K
+        if kind == "tie":         # the draft proposes the higher of two tied maxima: rejected at 0
+            assert gpu["accepted"][b] == 0

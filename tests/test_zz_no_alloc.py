@@ -68,10 +68,10 @@ def test_noalloc_rejects_sizes_beyond_the_scratch():
     from speculative_decoding_verification_15_gb300 import binding
 
     lib = binding.load()
-    B, K, V = 4096, 8, 151936
-    assert binding.spec_verify_workspace_size(B, K, V, binding.SPEC_BF16) > 4 << 20
+    B, K, V = 8192, 8, 1 << 20
+    assert binding.spec_verify_workspace_size(B, K, V, binding.SPEC_F32) > 4 << 20
     P = ctypes.c_void_p(256)  # never dereferenced: the size check returns before any launch
-    rc = lib.spec_verify_sample_noalloc(P, P, binding.SPEC_BF16, B, K, V, V, P, None, P, 0, 0, P, P, None,
+    rc = lib.spec_verify_sample_noalloc(P, P, binding.SPEC_F32, B, K, V, V, P, None, P, 0, 0, P, P, None,
                                         None, P, None)
     assert rc == binding.SPEC_ESCRATCH
     assert b"fixed scratch" in lib.spec_error_string(rc)
