@@ -200,8 +200,9 @@ int spec_last_cuda_error(void);
  * Kernel timing for measurement.  While enabled, every verify call records CUDA
  * events on its stream around each kernel it launches; spec_profile_read waits for
  * the last call's events and writes up to n durations in milliseconds, in launch
- * order (greedy: rows, accept; sample: rows, accept, residual, final), returning
- * how many were written (negative spec_err on failure).
+ * order (the main pass, the acceptance scan, the tail pass, the token pass; greedy
+ * and sampling calls launch the same four), returning how many were written
+ * (negative spec_err on failure).
  */
 int spec_profile_enable(int on);
 int spec_profile_read(float *ms, int n);
