@@ -65,6 +65,10 @@ def _load():
         lib.oracle_verify_sample.restype = I32
         lib.oracle_verify_greedy.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, P, P, I32]
         lib.oracle_verify_greedy.restype = I32
+        lib.oracle_verify_sample_early_exit.argtypes = lib.oracle_verify_sample.argtypes
+        lib.oracle_verify_sample_early_exit.restype = I32
+        lib.oracle_verify_greedy_early_exit.argtypes = lib.oracle_verify_greedy.argtypes
+        lib.oracle_verify_greedy_early_exit.restype = I32
         lib.oracle_schedule_verify_len.argtypes = [P, P, I32, I32, P, I32, I32, I32, P, P, P]
         lib.oracle_schedule_verify_len.restype = I32
         _lib = lib
@@ -140,11 +144,13 @@ def _logit_array(a):
 
 
 def verify_sample(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int,
-                  nthreads: int = 1) -> dict:
+                  nthreads: int = 1, early_exit: bool = False) -> dict:
     """Sampling verify of a padded batch.
 
     target [B, K+1, V] and draft [B, K, V] as float32 or bf16 bit patterns (uint16);
     draft_tokens [B, K] int32; num_draft [B] int32 or None; temperature [B] float32.
+    early_exit: read rows in position order and stop at the first rejection (status 4
+    only for rows read; p and q stay -1 past the first rejected position).
     """
     lib = _load()
     t, dt = _logit_array(target)
@@ -159,7 +165,8 @@ def verify_sample(target, draft, draft_tokens, num_draft, temperature, seed: int
     out = dict(tokens=np.full((B, K + 1), -1, np.int32), accepted=np.zeros(B, np.int32),
                p=np.full((B, K), -1.0), q=np.full((B, K), -1.0), status=np.zeros(B, np.int32),
                flags=np.zeros(B, np.int32), gap=np.zeros(B))
-    rc = lib.oracle_verify_sample(_ptr(t), _ptr(d), dt, B, K, V, V, _ptr(x), _ptr(nd), _ptr(T),
+    fn = lib.oracle_verify_sample_early_exit if early_exit else lib.oracle_verify_sample
+    rc = fn(_ptr(t), _ptr(d), dt, B, K, V, V, _ptr(x), _ptr(nd), _ptr(T),
                                   seed & (2**64 - 1), step & (2**64 - 1),
                                   _ptr(out["tokens"]), _ptr(out["accepted"]), _ptr(out["p"]),
                                   _ptr(out["q"]), _ptr(out["status"]), _ptr(out["flags"]),
@@ -168,7 +175,8 @@ def verify_sample(target, draft, draft_tokens, num_draft, temperature, seed: int
     return out
 
 
-def verify_greedy(target, draft_tokens, num_draft, nthreads: int = 1) -> dict:
+def verify_greedy(target, draft_tokens, num_draft, nthreads: int = 1, early_exit: bool = False) -> dict:
+    """Greedy verify of a padded batch; early_exit as in verify_sample."""
     lib = _load()
     t, dt = _logit_array(target)
     B, K1, V = t.shape
@@ -177,7 +185,8 @@ def verify_greedy(target, draft_tokens, num_draft, nthreads: int = 1) -> dict:
     nd = None if num_draft is None else _c(num_draft, np.int32)
     out = dict(tokens=np.full((B, K + 1), -1, np.int32), accepted=np.zeros(B, np.int32),
                status=np.zeros(B, np.int32))
-    rc = lib.oracle_verify_greedy(_ptr(t), dt, B, K, V, V, _ptr(x), _ptr(nd), _ptr(out["tokens"]),
+    fn = lib.oracle_verify_greedy_early_exit if early_exit else lib.oracle_verify_greedy
+    rc = fn(_ptr(t), dt, B, K, V, V, _ptr(x), _ptr(nd), _ptr(out["tokens"]),
                                   _ptr(out["accepted"]), _ptr(out["status"]), nthreads)
     assert rc == 0
     return out

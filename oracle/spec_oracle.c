@@ -222,6 +222,10 @@ typedef struct {
     uint64_t seed, step;
     int32_t *out_tokens, *out_accepted, *out_status, *out_flags;
     double *out_p, *out_q, *out_gap;
+    /* early exit: read the rows position by position and stop at the first
+     * rejection [PPR, ALX]; only rows read are checked for non-finite values and
+     * p/q stay -1 past the first rejected position */
+    int early_exit;
 } verify_args;
 
 static void load_row(const void *base, int dtype, int64_t row, int64_t ld_row, int V, double *dst) {
@@ -269,7 +273,7 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
     if (!status)
         for (i = 0; i < kb; ++i)
             if (x[i] < 0 || x[i] >= V) status = ST_BAD_TOKEN;
-    if (!status) {
+    if (!status && !a->early_exit) {
         /* rows of the draft positions: target 0..k_b-1, draft 0..k_b-1 (sampling only).
          * Reading: the target row k_b is checked only when it is read, i.e. when every
          * draft is accepted and the bonus (or greedy) token comes from it. */
@@ -295,7 +299,7 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
         int y = 0;
         for (i = 0; i <= kb; ++i) {
             load_row(a->target, a->dtype, (int64_t)b * K1 + i, a->ld_row, V, xt);
-            if (i == kb && !isfinite(row_max_nan(xt, V))) {
+            if ((i == kb || a->early_exit) && !isfinite(row_max_nan(xt, V))) {
                 fail_request(a, b, ST_NONFINITE);
                 return;
             }
@@ -318,6 +322,10 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
             double P, Q, u, ratio;
             load_row(a->target, a->dtype, (int64_t)b * K1 + i, a->ld_row, V, xt);
             load_row(a->draft, a->dtype, (int64_t)b * a->Kmax + i, a->ld_row, V, xd);
+            if (a->early_exit && (!isfinite(row_max_nan(xt, V)) || !isfinite(row_max_nan(xd, V)))) {
+                fail_request(a, b, ST_NONFINITE);
+                return;
+            }
             oracle_row_logprobs(xt, V, T, lpt);
             oracle_row_logprobs(xd, V, T, lpd);
             P = exp(lpt[x[i]]);
@@ -335,6 +343,7 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
                 tok[i] = x[i]; ++A; continue;
             }
             rejected = 1; /* first rejection: position A == i [PPR] */
+            if (a->early_exit) break;
         }
     }
 
@@ -420,12 +429,14 @@ static int run_verify(const verify_args *a, int nthreads) {
  * out_status [B], out_flags [B] (near-tie bits), out_gap [B] (top-2 gap of the
  * Gumbel draw, +inf if none).  nthreads: OpenMP threads over requests.
  */
-int oracle_verify_sample(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
-                         int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
-                         const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
-                         int32_t *out_accepted, double *out_p, double *out_q, int32_t *out_status,
-                         int32_t *out_flags, double *out_gap, int nthreads) {
+static int verify_sample_args(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                              int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                              const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+                              int32_t *out_accepted, double *out_p, double *out_q, int32_t *out_status,
+                              int32_t *out_flags, double *out_gap, int nthreads, int early_exit) {
     verify_args a;
+    memset(&a, 0, sizeof a);
+    a.early_exit = early_exit;
     a.target = target; a.draft = draft; a.dtype = dtype; a.B = B; a.Kmax = Kmax; a.V = V;
     a.ld_row = ld_row; a.draft_tokens = draft_tokens; a.num_draft = num_draft;
     a.temperature = temperature; a.seed = seed; a.step = step;
@@ -434,16 +445,57 @@ int oracle_verify_sample(const void *target, const void *draft, int dtype, int B
     return run_verify(&a, nthreads);
 }
 
+int oracle_verify_sample(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                         int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                         const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+                         int32_t *out_accepted, double *out_p, double *out_q, int32_t *out_status,
+                         int32_t *out_flags, double *out_gap, int nthreads) {
+    return verify_sample_args(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, temperature,
+                              seed, step, out_tokens, out_accepted, out_p, out_q, out_status, out_flags,
+                              out_gap, nthreads, 0);
+}
+
+/* The same with early exit: rows are read in position order and reading stops at
+ * the first rejected position, so a non-finite row after it is never seen (status
+ * 0) and p/q are -1 after it.  Tokens and accepted counts equal the full scan's
+ * whenever every row read is finite. */
+int oracle_verify_sample_early_exit(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                                    int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                                    const float *temperature, uint64_t seed, uint64_t step,
+                                    int32_t *out_tokens, int32_t *out_accepted, double *out_p, double *out_q,
+                                    int32_t *out_status, int32_t *out_flags, double *out_gap, int nthreads) {
+    return verify_sample_args(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, temperature,
+                              seed, step, out_tokens, out_accepted, out_p, out_q, out_status, out_flags,
+                              out_gap, nthreads, 1);
+}
+
 /* Greedy verify for a batch (draft logits are never read). */
-int oracle_verify_greedy(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
-                         const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
-                         int32_t *out_accepted, int32_t *out_status, int nthreads) {
+static int verify_greedy_args(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                              const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
+                              int32_t *out_accepted, int32_t *out_status, int nthreads, int early_exit) {
     verify_args a;
     memset(&a, 0, sizeof a);
     a.target = target; a.dtype = dtype; a.B = B; a.Kmax = Kmax; a.V = V; a.ld_row = ld_row;
     a.draft_tokens = draft_tokens; a.num_draft = num_draft;
     a.out_tokens = out_tokens; a.out_accepted = out_accepted; a.out_status = out_status;
+    a.early_exit = early_exit;
     return run_verify(&a, nthreads);
+}
+
+int oracle_verify_greedy(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                         const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
+                         int32_t *out_accepted, int32_t *out_status, int nthreads) {
+    return verify_greedy_args(target, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, out_tokens,
+                              out_accepted, out_status, nthreads, 0);
+}
+
+/* Greedy verify with early exit: target rows in position order up to the first
+ * mismatch (or row k_b); only those are checked for non-finite values. */
+int oracle_verify_greedy_early_exit(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                                    const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
+                                    int32_t *out_accepted, int32_t *out_status, int nthreads) {
+    return verify_greedy_args(target, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, out_tokens,
+                              out_accepted, out_status, nthreads, 1);
 }
 
 /* ------------------------------------------------------------------------- */
