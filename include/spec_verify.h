@@ -83,8 +83,8 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
 /*
  * Bytes of device workspace that spec_verify_greedy / spec_verify_sample need for
  * (B, Kmax, V, dtype) on the current device.  Returns 0 for invalid sizes.  The
- * workspace holds per-segment row statistics and the residual-draw job list; its
- * contents need no initialisation and are garbage after a call.
+ * workspace holds a control block and the per-segment row statistics of the main
+ * pass; its contents need no initialisation and are garbage after a call.
  */
 size_t spec_verify_workspace_size(int B, int Kmax, int V, int dtype);
 
@@ -147,12 +147,12 @@ int spec_verify_sample(const void *target, const void *draft, int dtype, int B, 
  * allocating routine.  Arguments, outputs and results are those of
  * spec_verify_sample, and the two agree on the same inputs.
  *  - Set-up: the first call on each device looks the array's address up with that
- *    device current (and sets the main kernel's shared-memory limit, as the
+ *    device current (and sets the kernels' shared-memory limits, as the
  *    workspace entry points do).  Make that first call before any stream capture.
  *  - Limit: sizes whose spec_verify_workspace_size(B, Kmax, V, dtype) exceeds
  *    SPEC_STATIC_SCRATCH_BYTES return SPEC_ESCRATCH before anything is launched
- *    (bf16, Kmax = 8 on a 152-SM device: B up to 512 fits at V = 151936, and B up
- *    to 256 at V = 262144).
+ *    (Kmax = 8 on a 152-SM device: B up to 1007 fits, for either logit type and
+ *    any V; the scratch grows with B * Kmax, not with V).
  *  - Zeroing: the only scratch that must start at zero, a two-word control block,
  *    is cleared on cuda_stream by every call before its first kernel.
  *  - Races: every call on a device uses the same array, so two calls that can
@@ -200,9 +200,10 @@ int spec_last_cuda_error(void);
  * Kernel timing for measurement.  While enabled, every verify call records CUDA
  * events on its stream around each kernel it launches; spec_profile_read waits for
  * the last call's events and writes up to n durations in milliseconds, in launch
- * order (the main pass, the acceptance scan, the tail pass, the token pass; greedy
- * and sampling calls launch the same four), returning how many were written
- * (negative spec_err on failure).
+ * order (the main pass over the draft positions' rows, then the commit pass that
+ * combines them, runs the acceptance scan and draws the extra token; greedy and
+ * sampling calls launch the same two), returning how many were written (negative
+ * spec_err on failure).
  */
 int spec_profile_enable(int on);
 int spec_profile_read(float *ms, int n);

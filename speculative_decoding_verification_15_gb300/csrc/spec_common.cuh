@@ -18,19 +18,7 @@ constexpr float kNegInf = -__builtin_huge_valf();
 // bounds use 17 so that rounding can never make a pruned element win.
 constexpr float kGumbelMax = 17.0f;
 
-enum RowKind : int { ROW_STATS = 0, ROW_BONUS = 1, ROW_ARGMAX = 2 };
 enum Purpose : uint32_t { PURPOSE_ACCEPT = 0, PURPOSE_RESIDUAL = 1, PURPOSE_BONUS = 2 };
-
-// One partial result per (warp, row segment).
-//   ROW_STATS : m = raw max (NaN-propagating), s = sum 2^(x*c - fl(m*c))
-//   ROW_ARGMAX: m = raw max, idx = lowest index holding it
-//   ROW_BONUS : m = raw max, best = max (x/T + g), idx = its lowest index
-struct __align__(16) Part {
-    float m;
-    float s;
-    float best;
-    int idx;
-};
 
 // ------------------------------------------------------------------ Philox
 __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
@@ -84,6 +72,13 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
 __device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// max of two bf16 pairs; a NaN lane yields the other operand
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
 
@@ -260,7 +255,7 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
-__device__ __forceinline__ double warp_sum_d(double x) {
+__device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
@@ -286,6 +281,33 @@ __device__ __forceinline__ void warp_argmax(float &s, int &i) {
         const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
         if (better(s2, i2, s, i)) { s = s2; i = i2; }
     }
+}
+
+// ------------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Split cluster barrier.  Every thread of every CTA of the cluster executes each
+// call, in the order arrive, wait, arrive, wait, ... (the .aligned forms need the
+// whole warp).  arrive_relaxed orders nothing; arrive releases this thread's
+// earlier memory operations and wait acquires the other CTAs' released ones.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// 16-byte store into the shared memory of CTA `rank` of this cluster, at the
+// address that `local` has in this CTA's shared memory.
+__device__ __forceinline__ void st_cluster_v4(void *local, uint32_t rank, uint4 v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
 }
 
 }  // namespace specv

@@ -50,41 +50,20 @@ constexpr int kChunkMaxBytes = kStageBytes - 32; // payload; an aligned superset
 constexpr int kVPT = kStageBytes / 16 / kCT;     // 16-byte vectors per consumer thread (4)
 constexpr size_t kSmemBudget = 226 * 1024;       // dynamic shared memory per CTA (227 KB minus static)
 constexpr uint64_t kWaitNs = 2000000000ull;      // bound on every mbarrier wait (2 s)
-constexpr int kAcceptThreads = 512;
-constexpr int kFinalThreads = 256;
-constexpr int kMaxRowsPerRequest = 2 * SPEC_MAX_DRAFTS;
 constexpr int kMaxDesc = 512;                    // per-CTA row descriptors kept in smem
 constexpr float kRescaleAt = 1024.f;             // lane chunk sum that moves the reference
 
-enum JobKind : int { JOB_RESID = 0, JOB_BONUS = 1, JOB_ARGMAX = 2 };
-
 struct Part {
-    float m;     // raw max of the segment (NaN-propagating)
-    float s;     // main pass: sum 2^(x c - fl(m c)); unused in the tail pass
-    int idx;     // lowest index of the max (main pass, argmax jobs) or of the best score
-    float best;  // tail pass: best Gumbel score
-};
-
-struct Job {
-    int b, row, kind;
-    float invT, Ct, Cd;  // log p_v = x_v invT - Ct, log q_v = y_v invT - Cd (correction)
-    float seed_best;     // exact score of the best candidate found by accept_kernel
-    int seed_idx;
+    float m;    // raw max of the segment (NaN-propagating)
+    float s;    // sum 2^(x c - fl(m c)) over the segment (sampling rows)
+    int idx;    // lowest index of the max
+    float pad;
 };
 
 struct Ctrl {
-    int err;        // non-zero: a bounded wait gave up
-    int job_count;  // jobs queued by accept_kernel
+    int err;  // non-zero: a bounded wait gave up
+    int pad;
 };
-
-// Order-preserving map of a float onto uint32 (for atomicMax on scores).
-__device__ __forceinline__ uint32_t ord_of(float f) {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float float_of_ord(uint32_t o) {
-    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
-}
 
 // ------------------------------------------------------------------ chunking
 // Rows are cut into cpr chunks of ce elements (ce a multiple of 8, at most
@@ -104,7 +83,6 @@ __host__ __device__ inline Chunking make_chunking(int V, int esz) {
 }
 
 __host__ __device__ inline int64_t cta_first(int64_t total, int G, int i) { return total * i / G; }
-__host__ __device__ inline int cta_of(int64_t total, int G, int64_t c) { return (int)(((c + 1) * G - 1) / total); }
 
 // Rows one CTA can touch, an upper bound.
 __host__ inline int segs_per_cta(int64_t total_max, int G, int cpr) {
@@ -434,7 +412,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
             const float M = warp_max_nan(m);
             const float MC = M * mr.c;
             const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - MC);
-            out.s = (float)warp_sum_d((double)sc);
+            out.s = warp_sum(sc);
             float mm = m;
             int ii = aidx;
             warp_argmax(mm, ii);
@@ -449,7 +427,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
             out.s = 0.f;
             out.idx = ii;
         }
-        out.best = 0.f;
+        out.pad = 0.f;
         if (lane == 0) p.parts[part_slot(blockIdx.x, p.nseg, r - first_row, warp)] = out;
     };
 
@@ -513,42 +491,51 @@ __global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
     }
 }
 
-// =================================================================== combine helpers
-// Partials of flat row r: CTAs [lo, hi] x kCW warps.
-struct RowParts {
-    int lo, hi, seg_lo;
-    __device__ __forceinline__ int n() const { return (hi - lo + 1) * kCW; }
-};
-
-__device__ __forceinline__ RowParts row_parts(int64_t total, int G, int cpr, int r) {
-    RowParts rp;
-    rp.lo = cta_of(total, G, (int64_t)r * cpr);
-    rp.hi = cta_of(total, G, (int64_t)r * cpr + cpr - 1);
-    rp.seg_lo = r;
-    return rp;
-}
-
-// Partial q of row r, or nullptr when its CTA has an empty chunk range (possible
-// when there are fewer chunks than CTAs): such CTAs lie between the row's first
-// and last CTA but wrote nothing.
-__device__ __forceinline__ const Part *part_of(const Part *parts, int64_t total, int G, int cpr, int nseg, int r,
-                                                const RowParts &rp, int q) {
-    const int cta = rp.lo + q / kCW;
-    const int64_t c0 = cta_first(total, G, cta);
-    if (c0 == cta_first(total, G, cta + 1)) return nullptr;
-    const int seg = r - (int)(c0 / cpr);
-    return &parts[part_slot(cta, nseg, seg, q % kCW)];
-}
-
 struct RowRes {
-    float M;    // raw row max
-    float l2S;  // log2 sum_v 2^(x_v c - fl(M c)) (stats rows)
-    float xv;   // logit at the draft token (stats rows)
+    float M;    // raw row max (NaN-propagating)
+    float l2S;  // log2 sum_v 2^(x_v c - fl(M c)) (sampling rows)
     int idx;    // lowest argmax
 };
 
-// =================================================================== accept_kernel
-struct AcceptParams {
+// =================================================================== commit_kernel
+// One cluster of C CTAs per request.  Every CTA of a cluster combines the
+// request's row partials and runs the acceptance scan -- the same arithmetic on
+// the same data, so all of them reach the same decision -- and then reduces its
+// share of the one row the request still needs: the first rejected target row j
+// (correction), or row k_b (bonus draw, or greedy argmax when every draft
+// matched).
+//  * Positions are independent until the scan, so one warp per draft position
+//    combines that position's target and draft rows, decides its acceptance bit
+//    and, if it rejects, scores the correction candidates that the main pass
+//    left (the segment argmaxes of the target row).  One barrier later the first
+//    rejected position is known together with a bound for its Gumbel-max.
+//  * The job row is cut into 8 C units; CTA r takes units r, r + C, r + 2C, ...,
+//    one per warp, so the shares interleave across the vocabulary and the work,
+//    which follows the logits (and the Zipf-like prior of real vocabularies),
+//    spreads evenly.  Units are staged into shared memory by bulk copies, in
+//    rounds of at most kRoundMaxBytes.
+//  * The CTAs' results meet in rank 0's shared memory; rank 0 writes the outputs.
+// Everything stays in fp32 and 32-bit integers: sm_103a has little fp64
+// throughput, and a software 64-bit division per warp and row would cost more
+// than the combine itself (the main pass's CTA ranges come from a table that
+// each CTA builds once, one division per thread).
+constexpr int kCommitThreads = 256;
+constexpr int kCommitWarps = kCommitThreads / 32;
+constexpr int kCommitBlocksPerSM = 4;
+constexpr int kMaxCluster = 8;
+constexpr int kUnitsPerCTA = kCommitWarps;  // row units per CTA: one per warp
+constexpr int kShareMaxBytes = 36 * 1024;   // row bytes per CTA before the cluster grows
+constexpr int kRoundMaxBytes = 40 * 1024;   // bytes staged per round
+constexpr int kUnitGroups = 4;              // groups of four each lane tests per block
+constexpr int kBlockGroups = 32 * kUnitGroups;  // groups per block (the unit of work of a warp)
+constexpr int kLiveMax = 64 + kBlockGroups;     // a warp's live list: < 64 carried over + one block
+constexpr int kLocalScanMax = 1024;         // B up to which each CTA counts rows itself
+constexpr int kCommitSmemMax = 64 * 1024;   // dynamic shared memory limit set on the kernel
+constexpr int kMaxCtas = 1024;              // main-pass CTAs the range table holds
+
+enum JobKind : int { JOB_NONE = 0, JOB_RESID = 1, JOB_BONUS = 2, JOB_ARGMAX = 3 };
+
+struct CommitParams {
     const void *target;
     const void *draft;
     int dtype;
@@ -556,21 +543,44 @@ struct AcceptParams {
     int B, Kmax, V;
     const int32_t *draft_tokens;
     const int32_t *num_draft;
-    const float *temperature;  // NULL: greedy
+    const float *temperature;  // NULL: every request greedy
     uint64_t seed;
     uint32_t step;
-    const int *row_start;
+    const int *row_start;      // from main_kernel; read only when B > kLocalScanMax
     const Part *parts;
     int nseg, G, cpr;
+    int C, ue, NS, slot;       // cluster size, entries per unit, units per round, bytes per unit slot
     int32_t *out_tokens;
     int32_t *out_accepted;
     float *out_p;
     float *out_q;
     int32_t *out_status;
-    Job *jobs;
-    int *job_list;
-    uint32_t *job_best;
     Ctrl *ctrl;
+};
+
+// What the warp of draft position i leaves for the scan.
+struct PosRes {
+    int rej;          // sampling: draft i rejected; greedy: target argmax != x_i
+    int tidx;         // target row argmax
+    float shift, Cd;  // log p_v = x_v / T - shift and log q_v = y_v / T - Cd on row i
+    float seed;       // best exact correction score among the row's segment argmaxes
+    int seed_idx;     // its index, -1 if none
+    int nonfinite;    // a row of position i holds NaN or +inf, or is all -inf
+    float pad;
+};
+
+struct JobDesc {
+    int kind, row, A, token;  // token: the greedy mismatch's argmax (JOB_NONE)
+    float invT, shift, Cd;    // z = x invT - shift is log p (correction) or x / T (bonus); q likewise with Cd
+    float seed;               // exact score of the correction's best seed candidate
+    int seed_idx;
+};
+
+struct __align__(16) SliceRes {  // one CTA's result, pushed into rank 0's shared memory
+    float best;    // best exact score (Gumbel-max) or largest finite value (argmax)
+    int idx;       // its lowest index, -1 if none
+    float rawmax;  // NaN-propagating max of every raw value the CTA read
+    int failed;    // a bounded wait gave up
 };
 
 // Exact score of the correction draw at one entry: log(p - q) + g, with p > q.
@@ -578,358 +588,184 @@ __device__ __forceinline__ float resid_score(float lp, float lq, uint32_t w) {
     return lp + logf(-expm1f(lq - lp)) + gumbel_of_word(w);
 }
 
-__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(AcceptParams p) {
-    __shared__ RowRes s_rows[kMaxRowsPerRequest];
-    pdl_wait();
-    pdl_launch_dependents();
-    const int b = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const int K1 = p.Kmax + 1;
-    int32_t *tok = p.out_tokens + (int64_t)b * K1;
-    for (int i = tid; i < K1; i += blockDim.x) tok[i] = -1;
-    if (p.out_p)
-        for (int i = tid; i < p.Kmax; i += blockDim.x) p.out_p[(int64_t)b * p.Kmax + i] = -1.f;
-    if (p.out_q)
-        for (int i = tid; i < p.Kmax; i += blockDim.x) p.out_q[(int64_t)b * p.Kmax + i] = -1.f;
-
-    // statuses, in order: k_b, temperature, tokens, non-finite rows
-    const int kb = p.num_draft ? p.num_draft[b] : p.Kmax;
-    int status = SPEC_STATUS_OK;
-    float T = 0.f;
-    if (kb < 0 || kb > p.Kmax) status = SPEC_STATUS_BAD_K;
-    if (status == SPEC_STATUS_OK && p.temperature) {
-        T = p.temperature[b];
-        if (!(T >= 0.f) || isinf(T)) status = SPEC_STATUS_BAD_TEMPERATURE;
-    }
-    if (p.ctrl->err) status = SPEC_STATUS_INTERNAL;
-    const bool greedy = (T == 0.f);
-    const int32_t *x = p.draft_tokens + (int64_t)b * p.Kmax;
-    if (status == SPEC_STATUS_OK) {
-        bool bad = false;
-        for (int i = tid; i < kb; i += blockDim.x) bad |= (x[i] < 0 || x[i] >= p.V);
-        if (__syncthreads_or(bad)) status = SPEC_STATUS_BAD_TOKEN;
-    }
-    const float c = greedy ? 0.f : __fdiv_rn(kLog2e, T);
-    const int64_t total = (int64_t)p.row_start[p.B] * p.cpr;
-    const int r0 = p.row_start[b];
-    const int nrows = status == SPEC_STATUS_OK ? (greedy ? kb : 2 * kb) : 0;
-
-    // combine the partials of every row of this request, one warp per row
-    bool nonfinite = false;
-    for (int rr = warp; rr < nrows; rr += nwarps) {
-        const int r = r0 + rr;
-        // the draft token's logit: independent of the partials, so issued first
-        float xv = 0.f;
-        if (!greedy) {
-            const bool is_draft = rr >= kb;
-            const int i = is_draft ? rr - kb : rr;
-            const int64_t row = is_draft ? ((int64_t)b * p.Kmax + i) : ((int64_t)b * K1 + i);
-            xv = load_logit(is_draft ? p.draft : p.target, p.dtype, row * p.ld_row + x[i]);
-        }
-        const RowParts rp = row_parts(total, p.G, p.cpr, r);
-        float m = kNegInf;
-        for (int q = lane; q < rp.n(); q += 32) {
-            const Part *pt = part_of(p.parts, total, p.G, p.cpr, p.nseg, r, rp, q);
-            if (pt) m = max_nan_f32(m, pt->m);
-        }
-        const float M = warp_max_nan(m);
-        double sum = 0.0;
-        float bm = kNegInf;
-        int bi = -1;
-        const float MC = M * c;
-        for (int q = lane; q < rp.n(); q += 32) {
-            const Part *pt = part_of(p.parts, total, p.G, p.cpr, p.nseg, r, rp, q);
-            if (!pt) continue;
-            if (!greedy && pt->m != kNegInf && pt->s != 0.f) sum += (double)pt->s * (double)exp2f(pt->m * c - MC);
-            if (better(pt->m, pt->idx, bm, bi)) { bm = pt->m; bi = pt->idx; }
-        }
-        warp_argmax(bm, bi);
-        RowRes res;
-        res.M = M;
-        res.idx = bi;
-        res.l2S = 0.f;
-        res.xv = 0.f;
-        if (!greedy) {
-            sum = warp_sum_d(sum);
-            res.l2S = log2f((float)sum);
-            res.xv = xv;
-        }
-        nonfinite |= !(fabsf(M) < __int_as_float(0x7f800000));
-        if (lane == 0) s_rows[rr] = res;
-    }
-    if (__syncthreads_or(nonfinite) && status == SPEC_STATUS_OK) status = SPEC_STATUS_NONFINITE;
-
-    if (status != SPEC_STATUS_OK) {
-        if (tid == 0) {
-            p.out_status[b] = status;
-            p.out_accepted[b] = 0;
-        }
-        return;
-    }
-    if (warp != 0) return;
-
-    // acceptance scan, 32 positions at a time; A = first rejected position
-    int A = kb;
-    int token = -1;
-    if (greedy) {
-        for (int i0 = 0; i0 < kb && A == kb; i0 += 32) {
-            const int i = i0 + lane;
-            const bool mism = i < kb && s_rows[i].idx != x[i];
-            const unsigned msk = __ballot_sync(0xffffffffu, mism);
-            if (msk) A = i0 + __ffs(msk) - 1;
-        }
-        if (A < kb) token = s_rows[A].idx;
-    } else {
-        for (int i0 = 0; i0 < kb; i0 += 32) {
-            const int i = i0 + lane;
-            bool rej = false;
-            if (i < kb) {
-                const RowRes tr = s_rows[i], dr = s_rows[kb + i];
-                const float l2p = fmaf(tr.xv, c, -(tr.M * c)) - tr.l2S;  // log2 p_i(x_i)
-                const float l2q = fmaf(dr.xv, c, -(dr.M * c)) - dr.l2S;  // log2 q_i(x_i)
-                if (p.out_p) p.out_p[(int64_t)b * p.Kmax + i] = exp2f(l2p);
-                if (p.out_q) p.out_q[(int64_t)b * p.Kmax + i] = exp2f(l2q);
-                // accept iff u q < p, i.e. log2 u < log2 p - log2 q (Q = 0 < P accepts; P = 0 rejects)
-                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
-                rej = !(log2f(u01(r4.x)) < l2p - l2q);
-            }
-            const unsigned msk = __ballot_sync(0xffffffffu, rej);
-            if (msk && A == kb) A = i0 + __ffs(msk) - 1;
-        }
-    }
-    for (int i = lane; i < A; i += 32) tok[i] = x[i];
-
-    if (greedy && A < kb) {
-        if (lane == 0) tok[A] = token;
-    } else {
-        Job job;
-        job.b = b;
-        job.row = A;
-        job.kind = greedy ? JOB_ARGMAX : (A < kb ? JOB_RESID : JOB_BONUS);
-        job.invT = greedy ? 0.f : __fdiv_rn(1.f, T);
-        job.Ct = job.Cd = 0.f;
-        job.seed_best = kNegInf;
-        job.seed_idx = -1;
-        if (job.kind == JOB_RESID) {
-            const int j = A;
-            const RowRes tr = s_rows[j], dr = s_rows[kb + j];
-            job.Ct = (float)(((double)(tr.M * c) + (double)tr.l2S) * 0.6931471805599453);
-            job.Cd = (float)(((double)(dr.M * c) + (double)dr.l2S) * 0.6931471805599453);
-            // seed the correction draw with the segment argmaxes of target row j
-            const int r = r0 + j;
-            const RowParts rp = row_parts(total, p.G, p.cpr, r);
-            const int64_t drow = ((int64_t)b * p.Kmax + j) * p.ld_row;
-            float best = kNegInf;
-            int bidx = -1;
-            for (int q = lane; q < rp.n(); q += 32) {
-                const Part *pt = part_of(p.parts, total, p.G, p.cpr, p.nseg, r, rp, q);
-                if (!pt || pt->idx < 0) continue;
-                const int v = pt->idx;
-                const float lp = fmaf(pt->m, job.invT, -job.Ct);
-                const float lq = fmaf(load_logit(p.draft, p.dtype, drow + v), job.invT, -job.Cd);
-                if (!(lq < lp)) continue;
-                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)j, PURPOSE_RESIDUAL,
-                                            (uint32_t)v >> 2);
-                const float sc = resid_score(lp, lq, word_of(r4, v & 3));
-                if (better(sc, v, best, bidx)) { best = sc; bidx = v; }
-            }
-            warp_argmax(best, bidx);
-            job.seed_best = best;
-            job.seed_idx = bidx;
-        }
-        if (lane == 0) {
-            p.jobs[b] = job;
-            const int pos = atomicAdd(&p.ctrl->job_count, 1);
-            p.job_list[pos] = b;
-            p.job_best[pos] = ord_of(job.seed_best);
-        }
-    }
-    if (lane == 0) {
-        p.out_status[b] = SPEC_STATUS_OK;
-        p.out_accepted[b] = A;
-    }
-}
-
-// =================================================================== tail_kernel
-// Exact score of one entry that survived the bound (rare; kept out of line so the
-// hot loop stays small).  Returns -inf when the entry has no residual mass.
-struct GumbelRow {
-    const char *drow;  // draft row (correction only)
-    int dtype;
-    bool resid;
-    float invT, shift_c, Cd;
-};
-
-__device__ __noinline__ float exact_score(const GumbelRow &gr, float z, int v, uint32_t wd) {
-    if (gr.resid) {
-        const float lq = fmaf(load_logit(gr.drow, gr.dtype, v), gr.invT, -gr.Cd);
+// Exact score of entry v of the job row (z = x_v invT - shift); -inf when the
+// correction has no mass at v.
+__device__ __noinline__ float entry_score(bool resid, float invT, float Cd, const char *drow, int dtype, float z,
+                                          int v, uint32_t wd) {
+    if (resid) {
+        const float lq = fmaf(load_logit(drow, dtype, v), invT, -Cd);
         if (!(lq < z)) return kNegInf;
         return resid_score(z, lq, wd);
     }
     return z + gumbel_of_word(wd);
 }
 
-// Random word of entry v when the window is not aligned to groups of four.
-__device__ __noinline__ uint32_t rand_word_slow(uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
-                                                uint32_t purpose, int v) {
-    return word_of(rand_group(seed, step, b, row, purpose, (uint32_t)v >> 2), v & 3);
+// ------------------------------------------------------------------ staged units
+// A unit slot holds the bulk copy of row elements [e0, e1) (its 16-byte aligned
+// superset); slot element 0 is row element sbase = e0 - shift.
+struct UnitView {
+    const unsigned char *slot;
+    int sbase, e1;
+    int g0, g1;   // groups of four [g0, g1)
+    int aligned;  // every group starts on an 8-byte (bf16) / 16-byte (fp32) boundary
+};
+
+template <int ESZ>
+__device__ __forceinline__ float smem_val(const unsigned char *buf, int i) {
+    if (ESZ == 2) return __uint_as_float((uint32_t)(*(const uint16_t *)(buf + 2 * i)) << 16);
+    return *(const float *)(buf + 4 * i);
 }
 
-// Raw words of group slot s (vector s / G, group s % G) of a thread's chunk data,
-// and the four logits they hold.
-template <class Vec>
-struct GroupWords;
-
-template <>
-struct GroupWords<VecBF16> {
-    static constexpr int N = 2;  // 4 bf16 = 2 words
-    template <int NV>
-    __device__ __forceinline__ static void get(const VecBF16 (&d)[NV], int s, uint32_t (&w)[4]) {
-        uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-        for (int t = 0; t < NV; ++t) {
-            if (s == 2 * t) { w0 = d[t].v.x; w1 = d[t].v.y; }
-            if (s == 2 * t + 1) { w0 = d[t].v.z; w1 = d[t].v.w; }
+// The four raw values of group g (entries 4g .. 4g+3); entries at or past e1 read
+// as -inf.
+template <int ESZ>
+__device__ __forceinline__ void group_vals(const UnitView &u, int g, float (&x)[4]) {
+    const int off = 4 * g - u.sbase;
+    if (u.aligned) {
+        if (ESZ == 2) {
+            const uint2 w = *(const uint2 *)(u.slot + 2 * off);
+            x[0] = bf16_lo(w.x);
+            x[1] = bf16_hi(w.x);
+            x[2] = bf16_lo(w.y);
+            x[3] = bf16_hi(w.y);
+        } else {
+            const float4 w = *(const float4 *)(u.slot + 4 * off);
+            x[0] = w.x;
+            x[1] = w.y;
+            x[2] = w.z;
+            x[3] = w.w;
         }
-        w[0] = w0;
-        w[1] = w1;
-    }
-    __device__ __forceinline__ static float value(const uint32_t (&w)[4], int k) {
-        return (k & 1) ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1]);
-    }
-};
-
-template <>
-struct GroupWords<VecF32> {
-    static constexpr int N = 4;
-    template <int NV>
-    __device__ __forceinline__ static void get(const VecF32 (&d)[NV], int s, uint32_t (&w)[4]) {
-        uint4 v = d[0].v;
+        if (4 * g + 3 >= u.e1) {
 #pragma unroll
-        for (int t = 1; t < NV; ++t)
-            if (s == t) v = d[t].v;
-        w[0] = v.x;
-        w[1] = v.y;
-        w[2] = v.z;
-        w[3] = v.w;
-    }
-    __device__ __forceinline__ static float value(const uint32_t (&w)[4], int k) { return __uint_as_float(w[k]); }
-};
-
-// Tail pass: one warp per unit of 32 lanes x kVPT vectors of a row, loaded with its
-// own 16-byte loads (one extra vector per lane covers a window that does not start
-// on a 16-byte boundary).
-constexpr int kTailNV = kVPT + 1;
-constexpr int kTailWarps = 8;
-constexpr int kTailThreads = kTailWarps * 32;
-constexpr int kTailBlocksPerSM = 3;
-// Per-warp list of live groups in shared memory (raw words + first index).
-constexpr int kLiveMax = 32 * kTailNV * 2;  // groups of four a warp can hold per unit (bf16: 2 per vector)
-constexpr size_t kLiveBytesPerWarp = (size_t)kLiveMax * (2 * sizeof(uint32_t) + sizeof(int));
-constexpr int kTailJobCache = 256;  // jobs whose descriptors each tail CTA keeps in shared memory
-
-// One staged chunk of a Gumbel-max row: z = x invT - shift_c is log p (correction)
-// or x / T (bonus).  Exact pruning, in order: the chunk or group bound
-// z + 17 < thr (no word gives more than 16.64 of noise), then per entry
-// 1 - u > 1.001 e^(z - thr) (g >= thr - z needs -log u <= e^(z - thr), and
-// -log u >= 1 - u).  Each lane appends its live groups of four to the warp's
-// list; the warp then draws one Philox block per listed group, 32 at a time, so
-// the work follows the number of live groups rather than the busiest lane.
-template <int STRIDE, class Vec, int NV>
-__device__ __forceinline__ void gumbel_chunk(const Vec (&d)[NV], int64_t ebase, int ct, const GumbelRow &gr,
-                                             uint64_t seed, uint32_t step, uint32_t b, uint32_t row,
-                                             uint32_t purpose, float tm, float thr, unsigned char *live_buf,
-                                             float &best, int &bidx) {
-    // thr only ever holds an exact score of some entry (or -inf), so raising it to
-    // the warp's best as exact scores come in keeps the pruning exact.
-    using GW = GroupWords<Vec>;
-    constexpr int G = Vec::VE / 4;  // groups of four per vector
-    const int lane = ct & 31;
-    uint32_t live = 0;
-    if (fmaf(tm, gr.invT, -gr.shift_c) + kGumbelMax >= thr) {
+            for (int k = 0; k < 4; ++k)
+                if (4 * g + k >= u.e1) x[k] = kNegInf;
+        }
+    } else {
 #pragma unroll
-        for (int t = 0; t < NV; ++t)
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-                if (fmaf(d[t].gmax(g), gr.invT, -gr.shift_c) + kGumbelMax >= thr) live |= 1u << (t * G + g);
+        for (int k = 0; k < 4; ++k) {
+            const int v = 4 * g + k;
+            x[k] = v < u.e1 ? smem_val<ESZ>(u.slot, v - u.sbase) : kNegInf;
+        }
     }
-    const int cnt = __popc(live);
+}
+
+// NaN-propagating max of group g's raw values (entries at or past e1 as -inf).
+template <int ESZ>
+__device__ __forceinline__ float group_max(const UnitView &u, int g) {
+    if (ESZ == 2 && u.aligned && 4 * g + 3 < u.e1) {
+        const uint2 w = *(const uint2 *)(u.slot + 2 * (4 * g - u.sbase));
+        const uint32_t m = max_nan_bf16x2(w.x, w.y);
+        return max_nan_f32(bf16_lo(m), bf16_hi(m));
+    }
+    float x[4];
+    group_vals<ESZ>(u, g, x);
+    return max_nan_f32(max_nan_f32(x[0], x[1]), max_nan_f32(x[2], x[3]));
+}
+
+// Gumbel-max over the staged units with exact pruning.  An entry can beat the
+// bound thr -- always the exact score of some entry, or -inf -- only if
+// z + 17 >= thr (no word gives more than 16.64 of noise) and
+// 1 - u <= 1.001 e^(z - thr) (g >= thr - z needs -log u <= e^(z - thr), and
+// -log u >= 1 - u).  A warp tests its blocks' groups by their largest z and
+// appends the live ones (group, slot and z) to its list in shared memory; every
+// 64 listed groups it draws their Philox blocks, two groups per lane (two
+// independent chains), so the Philox work follows the number of live groups and
+// every draw slot is used.
+
+// Append the live groups of block [gb, ge) of the unit in slot k; returns the new
+// (warp-uniform) list length.  CHECK_RAW: fold every raw value into rawmax (rows
+// the main pass did not read); otherwise the row is known to be finite.
+template <int ESZ, bool CHECK_RAW>
+__device__ __forceinline__ int zfilter_block(const UnitView &u, int k, int gb, int ge, float tz, float invT,
+                                             float shift, float &rawmax, uint32_t *lg, float *lz, int nlive) {
+    const int lane = threadIdx.x & 31;
+    const int gfull = u.e1 >> 2;  // groups below gfull lie entirely before e1
+    uint32_t lv = 0;
+    float zs[kUnitGroups];
+#pragma unroll
+    for (int t = 0; t < kUnitGroups; ++t) {
+        const int g = gb + lane + 32 * t;
+        zs[t] = kNegInf;
+        if (g < ge) {
+            float gm;
+            if (ESZ == 2 && u.aligned && g < gfull) {
+                const uint2 w = *(const uint2 *)(u.slot + 2 * (4 * g - u.sbase));
+                if (CHECK_RAW) {
+                    const uint32_t m = max_nan_bf16x2(w.x, w.y);
+                    gm = max_nan_f32(bf16_lo(m), bf16_hi(m));
+                } else {
+                    const uint32_t m = max_bf16x2(w.x, w.y);
+                    gm = fmaxf(bf16_lo(m), bf16_hi(m));
+                }
+            } else {
+                float x[4];
+                group_vals<ESZ>(u, g, x);
+                gm = CHECK_RAW ? max_nan_f32(max_nan_f32(x[0], x[1]), max_nan_f32(x[2], x[3]))
+                               : fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            }
+            if (CHECK_RAW) rawmax = max_nan_f32(rawmax, gm);
+            zs[t] = fmaf(gm, invT, -shift);
+            if (zs[t] > kNegInf && zs[t] >= tz) lv |= 1u << t;
+        }
+    }
+    const int cnt = __popc(lv);
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (total == 0) return;
-    constexpr int kItems = 32 * NV * G;  // most groups one warp can list per chunk
-    static_assert((size_t)kItems * (GW::N * sizeof(uint32_t) + sizeof(int)) <= kLiveBytesPerWarp,
-                  "live list exceeds its per-warp region");
-    uint32_t *lw = (uint32_t *)live_buf;
-    int *lv0 = (int *)(live_buf + (size_t)kItems * GW::N * sizeof(uint32_t));
-    const int excl = incl - cnt;
+    int pos = nlive + incl - cnt;
 #pragma unroll
-    for (int t = 0; t < NV; ++t)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const int sl = t * G + g;
-            if (!(live >> sl & 1u)) continue;
-            const int pos = excl + __popc(live & ((1u << sl) - 1u));
-            if (GW::N == 2) {
-                lw[pos * 2] = g == 0 ? d[t].v.x : d[t].v.z;
-                lw[pos * 2 + 1] = g == 0 ? d[t].v.y : d[t].v.w;
-            } else {
-                lw[pos * GW::N] = d[t].v.x;
-                lw[pos * GW::N + 1] = d[t].v.y;
-                lw[pos * GW::N + 2] = d[t].v.z;
-                lw[pos * GW::N + 3] = d[t].v.w;
-            }
-            lv0[pos] = (int)(ebase + (int64_t)(ct + STRIDE * t) * Vec::VE + 4 * g);
+    for (int t = 0; t < kUnitGroups; ++t)
+        if (lv >> t & 1u) {
+            lg[pos] = ((uint32_t)(gb + lane + 32 * t) << 3) | (uint32_t)k;
+            lz[pos] = zs[t];
+            ++pos;
         }
     __syncwarp();
-    const bool aligned = (ebase & 3) == 0;
-    // Each lane takes two listed groups per round: their Philox blocks are
-    // independent, which keeps the scheduler busy through the 10-round chains.
-#pragma unroll 1
-    for (int base = 0; base < total; base += 64) {
-        if (base) thr = fmaxf(thr, warp_max(best));  // later rounds prune against the best so far
-        uint32_t w[2][4];
-        int v0[2];
-        bool has[2];
-        uint4 r4[2];
+    return nlive + __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// Draw the listed groups [base, base + n), n <= 64, two per lane; update thr to
+// the warp's best afterwards.
+template <int ESZ>
+__device__ __forceinline__ void live_round(const uint32_t *lg, const float *lz, int base, int n,
+                                           const UnitView *uvs, const JobDesc &jd, const CommitParams &p,
+                                           uint32_t b, const char *drow, float &thr, float &best, int &bidx) {
+    const int lane = threadIdx.x & 31;
+    const bool resid = jd.kind == JOB_RESID;
+    const uint32_t purpose = resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS;
+    uint32_t gk[2];
+    float zm[2];
+    bool has[2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            // (the first group of a row that starts off a 16-byte boundary has a
-            // negative base index: its leading entries are masked, the rest are real)
-            const int item = base + lane + 32 * h;
-            has[h] = item < total;
-            const int it2 = has[h] ? item : total - 1;
+    for (int h = 0; h < 2; ++h) {
+        const int item = lane + 32 * h;
+        has[h] = item < n;
+        const int e = base + (has[h] ? item : 0);
+        gk[h] = lg[e];
+        zm[h] = lz[e];
+    }
+    uint4 r4[2];
 #pragma unroll
-            for (int q = 0; q < GW::N; ++q) w[h][q] = lw[it2 * GW::N + q];
-            v0[h] = lv0[it2];
-        }
+    for (int h = 0; h < 2; ++h) r4[h] = rand_group(p.seed, p.step, b, (uint32_t)jd.row, purpose, gk[h] >> 3);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) r4[h] = rand_group(seed, step, b, row, purpose, (uint32_t)v0[h] >> 2);
+    for (int h = 0; h < 2; ++h) {
+        // any survivor needs 1 - u_k <= e^(z_k - thr) <= e^(zmax - thr); the largest
+        // w >> 9 of the group gives the smallest 1 - u
+        const uint32_t kmax = max(max(r4[h].x >> 9, r4[h].y >> 9), max(r4[h].z >> 9, r4[h].w >> 9));
+        if (has[h] && one_minus_u01(kmax << 9) <= ex2_approx((zm[h] - thr) * kLog2e) * 1.001f) {
+            const int g = (int)(gk[h] >> 3);
+            float x[4];
+            group_vals<ESZ>(uvs[gk[h] & 7u], g, x);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (!has[h]) continue;
-            if (aligned) {
-                // any survivor needs 1 - u_k <= e^(z_k - thr) <= e^(zmax - thr); the
-                // largest w >> 9 of the group gives the smallest 1 - u
-                const uint32_t kmax = max(max(r4[h].x >> 9, r4[h].y >> 9), max(r4[h].z >> 9, r4[h].w >> 9));
-                float xm = GW::value(w[h], 0);
-#pragma unroll
-                for (int k = 1; k < 4; ++k) xm = fmaxf(xm, GW::value(w[h], k));
-                const float zm = fmaf(xm, gr.invT, -gr.shift_c);
-                if (!(one_minus_u01(kmax << 9) <= ex2_approx((zm - thr) * kLog2e) * 1.001f)) continue;
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int v = v0[h] + k;
-                const float z = fmaf(GW::value(w[h], k), gr.invT, -gr.shift_c);
-                const uint32_t wd = aligned ? word_of(r4[h], k) : rand_word_slow(seed, step, b, row, purpose, v);
+            for (int q = 0; q < 4; ++q) {
+                const float z = fmaf(x[q], jd.invT, -jd.shift);
+                const uint32_t wd = word_of(r4[h], q);
                 if (one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
-                    const float sc = exact_score(gr, z, v, wd);
+                    const int v = 4 * g + q;
+                    const float sc = entry_score(resid, jd.invT, jd.Cd, drow, p.dtype, z, v, wd);
                     // -inf: no residual mass at v, never a candidate (a row without any
                     // must reach the degenerate fallback)
                     if (sc > kNegInf && better(sc, v, best, bidx)) { best = sc; bidx = v; }
@@ -937,190 +773,546 @@ __device__ __forceinline__ void gumbel_chunk(const Vec (&d)[NV], int64_t ebase, 
             }
         }
     }
-    __syncwarp();  // the list is rewritten by the next chunk
+    thr = fmaxf(thr, warp_max(best));
+    __syncwarp();  // the items drawn here are overwritten by the next appends
 }
 
-struct TailParams {
-    const void *target;
-    const void *draft;
-    int dtype;
-    int64_t ld_row;
-    int Kmax, V;
-    uint64_t seed;
-    uint32_t step;
-    const Job *jobs;
-    const int *job_list;
-    uint32_t *job_best;  // [jobs] ord_of(best score seen), shared across warps
-    Part *parts;         // [job * units per row + unit]
-    Ctrl *ctrl;
-};
-
-// Loads one unit's window straight from global memory; out-of-window entries -inf.
-// Vector t of lane l holds entries ebase + (l + 32 t) VE + e.
-template <class Vec, int NV>
-__device__ __forceinline__ void load_unit(Vec (&d)[NV], const ChunkWin &w, int lane) {
-    const int nvec = (int)(w.bytes >> 4);
-    const int64_t ebase = (int64_t)w.e0 - w.shift;
-#pragma unroll
-    for (int t = 0; t < NV; ++t) {
-        const int j = lane + 32 * t;
-        d[t] = j < nvec ? Vec::load(w.a0, j) : Vec::neg_inf();
-    }
-    if (w.shift != 0 || ebase + (int64_t)nvec * Vec::VE != w.e1) {
-#pragma unroll
-        for (int t = 0; t < NV; ++t) {
-            const int j = lane + 32 * t;
-            if (j < nvec && (j == 0 || j == nvec - 1)) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, w.e0, w.e1);
-        }
-    }
-}
-
-// One row per job: the correction (Gumbel-max over log(p - q)), the bonus draw
-// (Gumbel-max over x / T) or the greedy argmax.  Rows are cut into units of
-// 32 x kVPT vectors; every warp takes a contiguous range of units (so it loads a
-// job's descriptor about once), loads them itself and writes one partial per
-// unit.  The work is latency-bound, so the kernel runs many independent warps
-// rather than a shared-memory ring.
-template <class Vec>
-__global__ void __launch_bounds__(kTailThreads, kTailBlocksPerSM) tail_kernel(TailParams p) {
-    __shared__ __align__(16) unsigned char s_live[kTailWarps * kLiveBytesPerWarp];
-    __shared__ Job s_jobs[kTailJobCache];
-    pdl_wait();
-    pdl_launch_dependents();
-    constexpr int UE = 32 * kVPT * Vec::VE;  // entries per unit
-    const Chunking uk = {(p.V + UE - 1) / UE, UE};
-    const int njobs = p.ctrl->job_count;
-    const int64_t total = (int64_t)njobs * uk.cpr;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t nw = (int64_t)gridDim.x * kTailWarps, gw = (int64_t)blockIdx.x * kTailWarps + warp;
-    const int64_t rowbytes = p.ld_row * Vec::ESIZE;
-    unsigned char *live_buf = s_live + kLiveBytesPerWarp * warp;
-    const bool cache = njobs <= kTailJobCache;
-    if (cache)
-        for (int i = threadIdx.x; i < njobs; i += blockDim.x) s_jobs[i] = p.jobs[p.job_list[i]];
+// Reduce (best, idx) with the lowest index on ties, rawmax NaN-propagating and
+// failed as an or over the CTA; every thread returns the CTA's result.
+__device__ __forceinline__ SliceRes block_reduce(SliceRes r, SliceRes *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    warp_argmax(r.best, r.idx);
+    r.rawmax = warp_max_nan(r.rawmax);
+    r.failed = __any_sync(0xffffffffu, r.failed != 0);
+    __syncthreads();  // red may still be read from an earlier use
+    if (lane == 0) red[warp] = r;
     __syncthreads();
-    // Units are dealt round-robin: a row's units (whose cost depends on the row)
-    // spread over many warps instead of piling onto a few.
-    for (int64_t u = gw; u < total; u += nw) {
-        const int r = (int)(u / uk.cpr);
-        const Job job = cache ? s_jobs[r] : p.jobs[p.job_list[r]];
-        const char *trow = (const char *)p.target + ((int64_t)job.b * (p.Kmax + 1) + job.row) * rowbytes;
-        const ChunkWin w = chunk_window(trow, Vec::ESIZE, p.V, uk, (int)(u - (int64_t)r * uk.cpr));
-        const uint32_t published = p.job_best[r];
-        Vec d[kTailNV];
-        load_unit(d, w, lane);
-        const int64_t ebase = (int64_t)w.e0 - w.shift;
-        const float tm = chunk_max(d);
-        Part out;
-        out.s = 0.f;
-        if (job.kind == JOB_ARGMAX) {
-            const bool any_nan = __any_sync(0xffffffffu, tm != tm);
-            float mm = (tm == tm) ? tm : kNegInf;
-            int ii = (tm == tm && tm > kNegInf) ? chunk_find<32>(d, ebase, lane, tm) : -1;
-            warp_argmax(mm, ii);
-            out.m = any_nan ? __int_as_float(0x7fc00000) : mm;
-            out.idx = ii;
-            out.best = 0.f;
-        } else {
-            const bool resid = job.kind == JOB_RESID;
-            float best = resid ? job.seed_best : kNegInf;
-            int bidx = resid ? job.seed_idx : -1;
-            if (!resid && tm == tm && tm > kNegInf) {  // bonus: seed the bound with each lane's largest entry
-                const int v = chunk_find<32>(d, ebase, lane, tm);
-                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row, PURPOSE_BONUS,
-                                            (uint32_t)v >> 2);
-                best = tm * job.invT + gumbel_of_word(word_of(r4, v & 3));
-                bidx = v;
-            }
-            // bound: the best score any warp has published for this job so far
-            const float thr = fmaxf(warp_max(best), float_of_ord(published));
-            GumbelRow gr;
-            gr.drow = (const char *)p.draft + ((int64_t)job.b * p.Kmax + job.row) * rowbytes;
-            gr.dtype = p.dtype;
-            gr.resid = resid;
-            gr.invT = job.invT;
-            gr.shift_c = resid ? job.Ct : 0.f;
-            gr.Cd = job.Cd;
-            gumbel_chunk<32>(d, ebase, lane, gr, p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row,
-                             resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS, tm, thr, live_buf, best, bidx);
-            out.m = warp_max_nan(tm);
-            warp_argmax(best, bidx);
-            out.best = best;
-            out.idx = bidx;
-            if (lane == 0 && bidx >= 0) atomicMax(&p.job_best[r], ord_of(best));
-        }
-        if (lane == 0) p.parts[u] = out;
+    SliceRes o = red[0];
+    for (int w = 1; w < kCommitWarps; ++w) {
+        const SliceRes q = red[w];
+        if (better(q.best, q.idx, o.best, o.idx)) { o.best = q.best; o.idx = q.idx; }
+        o.rawmax = max_nan_f32(o.rawmax, q.rawmax);
+        o.failed |= q.failed;
     }
+    return o;
 }
 
-// =================================================================== final_kernel
-struct FinalParams {
-    const void *target;
-    int dtype;
-    int64_t ld_row;
-    int Kmax, V, upr;
-    uint64_t seed;
-    uint32_t step;
-    const Job *jobs;
-    const int *job_list;
-    const Part *parts;
-    Ctrl *ctrl;
-    int32_t *out_tokens;
-    int32_t *out_accepted;
-    float *out_p;
-    float *out_q;
-    int32_t *out_status;
+// ------------------------------------------------------------------ main-pass partials
+// cf[c] = first chunk of main-pass CTA c (cf[G] = all chunks), fr[c] = its first row.
+__device__ __forceinline__ int cta_of_chunk(const int *cf, int G, int ch) {
+    int lo = 0, hi = G - 1;  // largest c with cf[c] <= ch: a CTA that holds chunk ch
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cf[mid] <= ch) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+struct RowSpan {
+    int lo, hi;  // CTAs that read the row
+    __device__ __forceinline__ int n() const { return (hi - lo + 1) * kCW; }
 };
 
-__global__ void __launch_bounds__(kFinalThreads) final_kernel(FinalParams p) {
-    pdl_wait();
+__device__ __forceinline__ RowSpan row_span(const int *cf, int G, int cpr, int r) {
+    return {cta_of_chunk(cf, G, r * cpr), cta_of_chunk(cf, G, r * cpr + cpr - 1)};
+}
+
+// Partial q of row r, or nullptr for a CTA with an empty range (possible when
+// there are fewer chunks than CTAs: such CTAs sit between a row's first and last).
+__device__ __forceinline__ const Part *part_at(const Part *parts, const int *cf, const int *fr, int nseg, int r,
+                                               const RowSpan &sp, int q) {
+    const int cta = sp.lo + q / kCW;
+    if (cf[cta] == cf[cta + 1]) return nullptr;
+    return &parts[part_slot(cta, nseg, r - fr[cta], q % kCW)];
+}
+
+// Combine one row's partials held one per lane (ok: the lane holds one).
+__device__ __forceinline__ RowRes finish_row(const Part &pt, bool ok, float c, bool greedy) {
+    const float M = warp_max_nan(ok ? pt.m : kNegInf);
+    const float MC = M * c;
+    float sum = 0.f;
+    if (ok && !greedy && pt.m != kNegInf && pt.s != 0.f) sum = pt.s * exp2f(pt.m * c - MC);
+    float bm = ok ? pt.m : kNegInf;
+    int bi = ok ? pt.idx : -1;
+    warp_argmax(bm, bi);
+    RowRes res;
+    res.M = M;
+    res.idx = bi;
+    res.l2S = greedy ? 0.f : log2f(warp_sum(sum));
+    return res;
+}
+
+// Combine one row's partials, any number of them (two passes over the partials).
+__device__ RowRes combine_row(const Part *parts, const int *cf, const int *fr, int nseg, int r, const RowSpan &sp,
+                              float c, bool greedy) {
     const int lane = threadIdx.x & 31;
-    const int jb = blockIdx.x * (kFinalThreads / 32) + (threadIdx.x >> 5);
-    const int njobs = p.ctrl->job_count;
-    if (jb >= njobs) return;
-    const Job job = p.jobs[p.job_list[jb]];
-    float m = kNegInf, best = kNegInf;
-    int idx = -1;
-    const Part *parts = p.parts + (int64_t)jb * p.upr;
-    for (int q = lane; q < p.upr; q += 32) {
-        const Part pt = parts[q];
-        m = max_nan_f32(m, pt.m);
-        const float sc = job.kind == JOB_ARGMAX ? pt.m : pt.best;
-        if (better(sc, pt.idx, best, idx)) { best = sc; idx = pt.idx; }
+    float m = kNegInf;
+    for (int q = lane; q < sp.n(); q += 32) {
+        const Part *pt = part_at(parts, cf, fr, nseg, r, sp, q);
+        if (pt) m = max_nan_f32(m, pt->m);
     }
-    m = warp_max_nan(m);
-    warp_argmax(best, idx);
-    const int64_t K1 = p.Kmax + 1;
+    const float M = warp_max_nan(m);
+    const float MC = M * c;
+    float sum = 0.f;
+    float bm = kNegInf;
+    int bi = -1;
+    for (int q = lane; q < sp.n(); q += 32) {
+        const Part *pt = part_at(parts, cf, fr, nseg, r, sp, q);
+        if (!pt) continue;
+        if (!greedy && pt->m != kNegInf && pt->s != 0.f) sum += pt->s * exp2f(pt->m * c - MC);
+        if (better(pt->m, pt->idx, bm, bi)) { bm = pt->m; bi = pt->idx; }
+    }
+    warp_argmax(bm, bi);
+    RowRes res;
+    res.M = M;
+    res.idx = bi;
+    res.l2S = greedy ? 0.f : log2f(warp_sum(sum));
+    return res;
+}
+
+__host__ __device__ inline size_t commit_round_bytes(int NS, int slot) {
+    return ((size_t)NS * slot + 127) & ~(size_t)127;
+}
+__host__ __device__ inline size_t commit_smem_bytes(int NS, int slot, int Kmax, int G) {
+    return commit_round_bytes(NS, slot) + sizeof(PosRes) * (size_t)Kmax + sizeof(RowSpan) * 2 * (size_t)Kmax +
+           5 * sizeof(float) * (size_t)Kmax + 2 * sizeof(int) * (size_t)(G + 1);
+}
+
+template <int ESZ>
+__global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_kernel(CommitParams p) {
+    extern __shared__ __align__(128) unsigned char cdyn[];
+    __shared__ uint64_t s_bar;
+    __shared__ uint32_t s_live_g[kCommitWarps][kLiveMax];
+    __shared__ float s_live_z[kCommitWarps][kLiveMax];
+    __shared__ SliceRes s_red[kCommitWarps];
+    __shared__ SliceRes s_inbox[kMaxCluster];
+    __shared__ UnitView s_uv[kUnitsPerCTA];
+    __shared__ JobDesc s_job;
+    __shared__ int s_sum[2 * kCommitWarps];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const int b = blockIdx.x / p.C;
+    cluster_arrive_relaxed();  // paired with the wait before the first remote store
+
+    unsigned char *buf = cdyn;
+    PosRes *s_pos = (PosRes *)(cdyn + commit_round_bytes(p.NS, p.slot));
+    RowSpan *s_span = (RowSpan *)(s_pos + p.Kmax);  // [target rows | draft rows]
+    float *s_xt = (float *)(s_span + 2 * p.Kmax);    // target logit at x_i
+    float *s_xd = s_xt + p.Kmax;                     // draft logit at x_i
+    float *s_l2u = s_xd + p.Kmax;                    // log2 of the acceptance uniform u_i
+    float *s_pp = s_l2u + p.Kmax;
+    float *s_qq = s_pp + p.Kmax;
+    int *s_cf = (int *)(s_qq + p.Kmax);
+    int *s_fr = s_cf + (p.G + 1);
+    if (tid == 0) {
+        mbar_init(&s_bar, 1);
+        mbar_init_fence();
+    }
+
+    // ---- inputs only: this part overlaps the end of main_kernel
+    const int kb_raw = p.num_draft ? p.num_draft[b] : p.Kmax;
     int status = SPEC_STATUS_OK;
-    if (p.ctrl->err) status = SPEC_STATUS_INTERNAL;
-    else if (job.kind != JOB_RESID && !(fabsf(m) < __int_as_float(0x7f800000))) status = SPEC_STATUS_NONFINITE;
-    if (status == SPEC_STATUS_OK && job.kind == JOB_RESID && idx < 0) {
-        // p <= q everywhere (only by rounding): draw from p_j with the same noise
-        const int64_t trow = ((int64_t)job.b * K1 + job.row) * p.ld_row;
-        best = kNegInf;
-        for (int v = lane; v < p.V; v += 32) {
-            const float lp = fmaf(load_logit(p.target, p.dtype, trow + v), job.invT, -job.Ct);
-            if (!(lp > kNegInf)) continue;
-            const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)job.b, (uint32_t)job.row, PURPOSE_RESIDUAL,
-                                        (uint32_t)v >> 2);
-            const float sc = lp + gumbel_of_word(word_of(r4, v & 3));
-            if (better(sc, v, best, idx)) { best = sc; idx = v; }
-        }
-        warp_argmax(best, idx);
+    float T = 0.f;
+    if (kb_raw < 0 || kb_raw > p.Kmax) status = SPEC_STATUS_BAD_K;
+    if (status == SPEC_STATUS_OK && p.temperature) {
+        T = p.temperature[b];
+        if (!(T >= 0.f) || isinf(T)) status = SPEC_STATUS_BAD_TEMPERATURE;
     }
-    if (status != SPEC_STATUS_OK) {
-        for (int i = lane; i < K1; i += 32) p.out_tokens[job.b * K1 + i] = -1;
-        for (int i = lane; i < p.Kmax; i += 32) {
-            if (p.out_p) p.out_p[(int64_t)job.b * p.Kmax + i] = -1.f;
-            if (p.out_q) p.out_q[(int64_t)job.b * p.Kmax + i] = -1.f;
+    const int kb = status == SPEC_STATUS_BAD_K ? 0 : kb_raw;
+    const bool greedy = (T == 0.f);
+    const int32_t *x = p.draft_tokens + (int64_t)b * p.Kmax;
+    if (status == SPEC_STATUS_OK) {
+        bool bad = false;
+        for (int i = tid; i < kb; i += kCommitThreads) bad |= (x[i] < 0 || x[i] >= p.V);
+        if (__syncthreads_or(bad)) status = SPEC_STATUS_BAD_TOKEN;
+    }
+    const float c = greedy ? 0.f : __fdiv_rn(kLog2e, T);
+    const float invT = greedy ? 0.f : __fdiv_rn(1.f, T);
+    const int npos = status == SPEC_STATUS_OK ? kb : 0;
+    if (!greedy) {
+        for (int i = tid; i < npos; i += kCommitThreads) {
+            const int xi = x[i];
+            s_xt[i] = load_logit(p.target, p.dtype, ((int64_t)b * (p.Kmax + 1) + i) * p.ld_row + xi);
+            s_xd[i] = load_logit(p.draft, p.dtype, ((int64_t)b * p.Kmax + i) * p.ld_row + xi);
+            const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
+            s_l2u[i] = log2f(u01(r4.x));
         }
+    }
+    // flat main-pass index of this request's first row, the number of rows, the
+    // main pass's CTA ranges and the CTAs that read each row of this request
+    int r0 = 0, R = 0;
+    if (p.B <= kLocalScanMax) {
+        int before = 0, all = 0;
+        for (int bb = tid; bb < p.B; bb += kCommitThreads) {
+            const int n = request_main_rows(p.num_draft, p.temperature, p.Kmax, bb);
+            all += n;
+            if (bb < b) before += n;
+        }
+        before = warp_sum_i(before);
+        all = warp_sum_i(all);
         if (lane == 0) {
-            p.out_status[job.b] = status;
-            p.out_accepted[job.b] = 0;
+            s_sum[warp] = before;
+            s_sum[kCommitWarps + warp] = all;
         }
-        return;
+        __syncthreads();
+        for (int w = 0; w < kCommitWarps; ++w) {
+            r0 += s_sum[w];
+            R += s_sum[kCommitWarps + w];
+        }
+    } else {
+        pdl_wait();
+        r0 = p.row_start[b];
+        R = p.row_start[p.B];
     }
-    if (lane == 0) p.out_tokens[job.b * K1 + job.row] = idx;
+    const int64_t total = (int64_t)R * p.cpr;
+    for (int cc = tid; cc <= p.G; cc += kCommitThreads) {
+        const int64_t f = cta_first(total, p.G, cc);
+        s_cf[cc] = (int)f;
+        s_fr[cc] = (int)(f / p.cpr);
+    }
+    __syncthreads();
+    const int nrows = greedy ? npos : 2 * npos;  // flat rows r0 .. r0 + nrows - 1
+    for (int rr = tid; rr < nrows; rr += kCommitThreads) {
+        const int slot = rr < npos ? rr : p.Kmax + (rr - npos);
+        s_span[slot] = row_span(s_cf, p.G, p.cpr, r0 + rr);
+    }
+    pdl_wait();
+    __syncthreads();
+
+    // ---- main_kernel's partials are complete from here on
+    if (p.ctrl->err) status = SPEC_STATUS_INTERNAL;
+    const int nw = status == SPEC_STATUS_OK ? npos : 0;
+    // one warp per draft position: target row i (flat r0 + i) and, sampling, draft
+    // row i (flat r0 + k_b + i)
+    for (int i = warp; i < nw; i += kCommitWarps) {
+        const int rt = r0 + i, rd = r0 + kb + i;
+        const RowSpan st = s_span[i];
+        const RowSpan sd = greedy ? st : s_span[p.Kmax + i];
+        const bool fast = st.n() <= 32 && sd.n() <= 32;
+        const char *drow = (const char *)p.draft + ((int64_t)b * p.Kmax + i) * p.ld_row * ESZ;
+        Part pt = {};  // this lane's target partial: a correction candidate
+        bool okt = false;
+        float dv = 0.f;  // draft logit at the candidate, fetched before it is known to be needed
+        RowRes tr, dr;
+        if (fast) {
+            Part pd = {};
+            bool okd = false;
+            if (lane < st.n()) {
+                const Part *q = part_at(p.parts, s_cf, s_fr, p.nseg, rt, st, lane);
+                if (q) { pt = *q; okt = true; }
+            }
+            if (!greedy && lane < sd.n()) {
+                const Part *q = part_at(p.parts, s_cf, s_fr, p.nseg, rd, sd, lane);
+                if (q) { pd = *q; okd = true; }
+            }
+            if (!greedy && okt && pt.idx >= 0) dv = load_logit(drow, p.dtype, pt.idx);
+            tr = finish_row(pt, okt, c, greedy);
+            if (!greedy) dr = finish_row(pd, okd, c, false);
+        } else {
+            tr = combine_row(p.parts, s_cf, s_fr, p.nseg, rt, st, c, greedy);
+            if (!greedy) dr = combine_row(p.parts, s_cf, s_fr, p.nseg, rd, sd, c, false);
+        }
+        PosRes pr;
+        pr.tidx = tr.idx;
+        pr.nonfinite = !(fabsf(tr.M) < __int_as_float(0x7f800000)) ||
+                       (!greedy && !(fabsf(dr.M) < __int_as_float(0x7f800000)));
+        pr.shift = pr.Cd = 0.f;
+        pr.seed = kNegInf;
+        pr.seed_idx = -1;
+        pr.pad = 0.f;
+        if (greedy) {
+            pr.rej = tr.idx != x[i];
+        } else {
+            const float l2p = fmaf(s_xt[i], c, -(tr.M * c)) - tr.l2S;  // log2 p_i(x_i)
+            const float l2q = fmaf(s_xd[i], c, -(dr.M * c)) - dr.l2S;  // log2 q_i(x_i)
+            // accept iff u q < p, i.e. log2 u < log2 p - log2 q (Q = 0 < P accepts; P = 0 rejects)
+            pr.rej = !(s_l2u[i] < l2p - l2q);
+            // log p_v = x_v / T - (M c + log2 S) ln 2, and q likewise
+            pr.shift = (tr.M * c + tr.l2S) * 0.6931471805599453f;
+            pr.Cd = (dr.M * c + dr.l2S) * 0.6931471805599453f;
+            if (lane == 0) {
+                s_pp[i] = exp2f(l2p);
+                s_qq[i] = exp2f(l2q);
+            }
+            if (pr.rej && !pr.nonfinite) {
+                // exact correction scores at the segment argmaxes of target row i
+                float sb = kNegInf;
+                int si = -1;
+                for (int q = lane; q < st.n(); q += 32) {
+                    Part cand = pt;
+                    bool ok = okt;
+                    float dq = dv;
+                    if (!fast) {
+                        const Part *qq = part_at(p.parts, s_cf, s_fr, p.nseg, rt, st, q);
+                        ok = qq != nullptr;
+                        if (ok) {
+                            cand = *qq;
+                            if (cand.idx >= 0) dq = load_logit(drow, p.dtype, cand.idx);
+                        }
+                    }
+                    if (!ok || cand.idx < 0) continue;
+                    const int v = cand.idx;
+                    const float z = fmaf(cand.m, invT, -pr.shift);
+                    const float lq = fmaf(dq, invT, -pr.Cd);
+                    if (!(lq < z)) continue;  // no residual mass at v
+                    const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_RESIDUAL,
+                                                (uint32_t)v >> 2);
+                    const float sc = resid_score(z, lq, word_of(r4, v & 3));
+                    if (sc > kNegInf && better(sc, v, sb, si)) { sb = sc; si = v; }
+                }
+                warp_argmax(sb, si);
+                pr.seed = sb;
+                pr.seed_idx = si;
+            }
+        }
+        if (lane == 0) s_pos[i] = pr;
+    }
+    __syncthreads();
+
+    // ---- the scan (warp 0): A = first rejected position; it then starts the job
+    // row's first round of copies
+    const int64_t rowbytes = p.ld_row * ESZ;
+    const Chunking uk = {p.C * kUnitsPerCTA, p.ue};
+    const int nunits = (p.V + p.ue - 1) / p.ue;  // units holding entries
+    // warp 0: unit views of round rd into s_uv, then one copy per lane k < NS
+    auto issue_round = [&](const char *jrow, int rd) {
+        ChunkWin w;
+        w.bytes = 0;
+        const int u = (int)rank + p.C * (rd * p.NS + lane);
+        UnitView uv;
+        uv.slot = buf + (size_t)lane * p.slot;
+        uv.sbase = uv.e1 = uv.g0 = uv.g1 = 0;
+        uv.aligned = 0;
+        if (lane < p.NS && u < nunits) {
+            w = chunk_window(jrow, ESZ, p.V, uk, u);
+            uv.sbase = w.e0 - w.shift;
+            uv.e1 = w.e1;
+            uv.g0 = w.e0 >> 2;
+            uv.g1 = (w.e1 + 3) >> 2;
+            uv.aligned = (w.shift & 3) == 0;
+        }
+        if (lane < p.NS) s_uv[lane] = uv;
+        const int bytes = warp_sum_i((int)w.bytes);
+        if (lane == 0) mbar_arrive_expect_tx(&s_bar, (uint32_t)bytes);
+        __syncwarp();
+        if (w.bytes) bulk_g2s(buf + (size_t)lane * p.slot, w.a0, w.bytes, &s_bar);
+    };
+    if (warp == 0) {
+        JobDesc jd;
+        jd.kind = JOB_NONE;
+        jd.row = 0;
+        jd.A = 0;
+        jd.token = -1;
+        jd.invT = invT;
+        jd.shift = jd.Cd = 0.f;
+        jd.seed = kNegInf;
+        jd.seed_idx = -1;
+        int st = status;
+        if (st == SPEC_STATUS_OK) {
+            bool nf = false;
+            for (int i = lane; i < kb; i += 32) nf |= s_pos[i].nonfinite != 0;
+            if (__any_sync(0xffffffffu, nf)) st = SPEC_STATUS_NONFINITE;
+        }
+        if (st == SPEC_STATUS_OK) {
+            int A = kb;
+            for (int i0 = 0; i0 < kb && A == kb; i0 += 32) {
+                const int i = i0 + lane;
+                const unsigned msk = __ballot_sync(0xffffffffu, i < kb && s_pos[i].rej != 0);
+                if (msk) A = i0 + __ffs(msk) - 1;
+            }
+            jd.A = A;
+            if (greedy) {
+                if (A < kb) {
+                    jd.token = s_pos[A].tidx;
+                } else {
+                    jd.kind = JOB_ARGMAX;
+                    jd.row = kb;
+                }
+            } else if (A < kb) {
+                const PosRes pr = s_pos[A];
+                jd.kind = JOB_RESID;
+                jd.row = A;
+                jd.shift = pr.shift;
+                jd.Cd = pr.Cd;
+                jd.seed = pr.seed;
+                jd.seed_idx = pr.seed_idx;
+            } else {
+                jd.kind = JOB_BONUS;
+                jd.row = kb;
+            }
+        }
+        if (jd.kind != JOB_NONE)
+            issue_round((const char *)p.target + ((int64_t)b * (p.Kmax + 1) + jd.row) * rowbytes, 0);
+        if (lane == 0) {
+            s_job = jd;
+            s_sum[0] = st;
+        }
+    }
+    __syncthreads();
+    const JobDesc jd = s_job;
+    status = s_sum[0];
+
+    // ---- this CTA's units of the job row (unit rank + C k in slot k of its round).
+    // A round's units are cut into blocks of kBlockGroups groups, dealt to the warps
+    // round-robin, so every warp gets a mix of the units.
+    const char *jrow = (const char *)p.target + ((int64_t)b * (p.Kmax + 1) + jd.row) * rowbytes;
+    const char *drow =
+        jd.kind == JOB_RESID ? (const char *)p.draft + ((int64_t)b * p.Kmax + jd.row) * rowbytes : nullptr;
+    const int nrounds = jd.kind == JOB_NONE ? 0 : kUnitsPerCTA / p.NS;
+    const int bpu = (((p.ue + 3) >> 2) + kBlockGroups - 1) / kBlockGroups;  // blocks per full unit
+    SliceRes mine;
+    mine.best = jd.seed;
+    mine.idx = jd.seed_idx;
+    mine.rawmax = kNegInf;
+    mine.failed = 0;
+    float thr = jd.seed;
+    uint32_t phase = 0;
+    for (int rd = 0; rd < nrounds; ++rd) {
+        // one thread waits, so that a CTA whose copies are in flight takes no issue
+        // slots from the CTAs sharing its SM; the others then take the completed
+        // phase themselves (it completes at once), which makes the bytes visible to them
+        bool ok = true;
+        if (tid == 0) ok = mbar_wait(&s_bar, phase, kWaitNs);
+        if (__syncthreads_or(!ok)) {
+            // give up on this request; wait (bounded) for the copies in flight first
+            if (tid == 0) mbar_wait(&s_bar, phase, kWaitNs);
+            mine.failed = 1;
+            break;
+        }
+        mbar_try_wait(&s_bar, phase);
+        phase ^= 1u;
+        const int nblk = p.NS * bpu;
+        if (jd.kind == JOB_BONUS) {
+            // seed the bound with each thread's largest entry (exact score)
+            float m = kNegInf;
+            int mi = -1;
+            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
+                const UnitView uv = s_uv[bi / bpu];
+                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+                for (int g = gb + lane; g < ge; g += 32) {
+                    float xv[4];
+                    group_vals<ESZ>(uv, g, xv);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (xv[q] > m) { m = xv[q]; mi = 4 * g + q; }
+                }
+            }
+            SliceRes seed;
+            seed.best = kNegInf;
+            seed.idx = -1;
+            seed.rawmax = kNegInf;
+            seed.failed = 0;
+            if (mi >= 0) {
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_BONUS,
+                                            (uint32_t)mi >> 2);
+                seed.best = fmaf(m, jd.invT, -jd.shift) + gumbel_of_word(word_of(r4, mi & 3));
+                seed.idx = mi;
+            }
+            seed = block_reduce(seed, s_red);
+            if (better(seed.best, seed.idx, mine.best, mine.idx)) { mine.best = seed.best; mine.idx = seed.idx; }
+            thr = fmaxf(thr, seed.best);
+        }
+        if (jd.kind == JOB_ARGMAX) {
+            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
+                const UnitView uv = s_uv[bi / bpu];
+                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+                float m = kNegInf;
+                int mi = -1;
+                for (int g = gb + lane; g < ge; g += 32) {
+                    float xv[4];
+                    group_vals<ESZ>(uv, g, xv);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        mine.rawmax = max_nan_f32(mine.rawmax, xv[q]);
+                        if (xv[q] > m) { m = xv[q]; mi = 4 * g + q; }
+                    }
+                }
+                if (better(m, mi, mine.best, mine.idx)) { mine.best = m; mine.idx = mi; }
+            }
+        } else {
+            uint32_t *lg = s_live_g[warp];
+            float *lz = s_live_z[warp];
+            int nlive = 0;
+            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
+                const int k = bi / bpu;
+                const UnitView uv = s_uv[k];
+                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+                if (gb >= ge) continue;
+                nlive = jd.kind == JOB_BONUS
+                            ? zfilter_block<ESZ, true>(uv, k, gb, ge, thr - kGumbelMax, jd.invT, jd.shift,
+                                                       mine.rawmax, lg, lz, nlive)
+                            : zfilter_block<ESZ, false>(uv, k, gb, ge, thr - kGumbelMax, jd.invT, jd.shift,
+                                                        mine.rawmax, lg, lz, nlive);
+                while (nlive >= 64) {  // draw the newest 64; the rest stay listed
+                    nlive -= 64;
+                    live_round<ESZ>(lg, lz, nlive, 64, s_uv, jd, p, (uint32_t)b, drow, thr, mine.best, mine.idx);
+                }
+            }
+            if (nlive > 0)
+                live_round<ESZ>(lg, lz, 0, nlive, s_uv, jd, p, (uint32_t)b, drow, thr, mine.best, mine.idx);
+        }
+        __syncthreads();  // every warp is done with the round's slots and views
+        if (warp == 0 && rd + 1 < nrounds) issue_round(jrow, rd + 1);
+    }
+    const SliceRes res = block_reduce(mine, s_red);
+
+    // ---- the CTAs' results meet in rank 0
+    cluster_wait();  // every CTA of the cluster is running
+    if (tid == 0) st_cluster_v4(&s_inbox[rank], 0, make_uint4(__float_as_uint(res.best), (uint32_t)res.idx,
+                                                               __float_as_uint(res.rawmax), (uint32_t)res.failed));
+    cluster_arrive();
+    cluster_wait();
+    if (rank != 0) return;
+
+    int token = jd.token;
+    if (status == SPEC_STATUS_OK && jd.kind != JOB_NONE) {
+        SliceRes o = s_inbox[0];
+        for (int r = 1; r < p.C; ++r) {
+            const SliceRes q = s_inbox[r];
+            if (better(q.best, q.idx, o.best, o.idx)) { o.best = q.best; o.idx = q.idx; }
+            o.rawmax = max_nan_f32(o.rawmax, q.rawmax);
+            o.failed |= q.failed;
+        }
+        if (o.failed) status = SPEC_STATUS_INTERNAL;
+        else if (jd.kind != JOB_RESID && !(fabsf(o.rawmax) < __int_as_float(0x7f800000)))
+            status = SPEC_STATUS_NONFINITE;
+        token = o.idx;
+        if (status == SPEC_STATUS_OK && jd.kind == JOB_RESID && o.idx < 0) {
+            // p <= q everywhere (only by rounding): draw from p_j with the same noise
+            const int64_t trow = ((int64_t)b * (p.Kmax + 1) + jd.row) * p.ld_row;
+            SliceRes f;
+            f.best = kNegInf;
+            f.idx = -1;
+            f.rawmax = kNegInf;
+            f.failed = 0;
+            for (int v = tid; v < p.V; v += kCommitThreads) {
+                const float lp = fmaf(load_logit(p.target, p.dtype, trow + v), jd.invT, -jd.shift);
+                if (!(lp > kNegInf)) continue;
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
+                                            (uint32_t)v >> 2);
+                const float sc = lp + gumbel_of_word(word_of(r4, v & 3));
+                if (better(sc, v, f.best, f.idx)) { f.best = sc; f.idx = v; }
+            }
+            token = block_reduce(f, s_red).idx;
+        }
+    }
+
+    // ---- outputs of request b
+    const bool ok = status == SPEC_STATUS_OK;
+    const int A = ok ? jd.A : 0;
+    const int K1 = p.Kmax + 1;
+    int32_t *tok = p.out_tokens + (int64_t)b * K1;
+    for (int i = tid; i < K1; i += kCommitThreads) tok[i] = !ok ? -1 : (i < A ? x[i] : (i == A ? token : -1));
+    const bool pq = ok && !greedy;
+    if (p.out_p)
+        for (int i = tid; i < p.Kmax; i += kCommitThreads) p.out_p[(int64_t)b * p.Kmax + i] = pq && i < kb ? s_pp[i] : -1.f;
+    if (p.out_q)
+        for (int i = tid; i < p.Kmax; i += kCommitThreads) p.out_q[(int64_t)b * p.Kmax + i] = pq && i < kb ? s_qq[i] : -1.f;
+    if (tid == 0) {
+        p.out_status[b] = status;
+        p.out_accepted[b] = A;
+    }
 }
 
 // =================================================================== host side
@@ -1189,8 +1381,9 @@ struct ProfScope {
 };
 
 struct Layout {
-    size_t off_ctrl, off_row_start, off_parts, off_jobs, off_job_list, off_job_best, off_parts2, total;
-    int nseg, G, cpr, upr;
+    size_t off_ctrl, off_row_start, off_parts, total;
+    int nseg, G, cpr;  // main pass: partial segments per CTA, CTAs, chunks per row
+    int C, ue, NS, slot;  // commit pass: cluster size, entries per unit, units per round, bytes per slot
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1208,39 +1401,23 @@ Layout make_layout(int B, int Kmax, int V, int esz, int sms, int main_rows_per_r
     o = align256(o + sizeof(int) * (size_t)(B + 1));
     L.off_parts = o;
     o = align256(o + sizeof(Part) * (size_t)L.G * L.nseg * kCW);
-    L.off_jobs = o;
-    o = align256(o + sizeof(Job) * (size_t)B);
-    L.off_job_list = o;
-    o = align256(o + sizeof(int) * (size_t)B);
-    L.off_job_best = o;
-    o = align256(o + sizeof(uint32_t) * (size_t)B);
-    const int ue = 32 * kVPT * (16 / esz);  // entries per tail unit
-    L.upr = (V + ue - 1) / ue;
-    L.off_parts2 = o;
-    o = align256(o + sizeof(Part) * (size_t)B * L.upr);
     L.total = o;
+    // commit pass: a row splits into 8 C units, C CTAs (one cluster) per request with
+    // one unit per warp; a CTA's share stays near kShareMaxBytes, and its units are
+    // staged NS at a time (NS a power of two, so that the warps split evenly)
+    const int64_t rowb = (int64_t)V * esz;
+    const int64_t c_need = (rowb + kShareMaxBytes - 1) / kShareMaxBytes;
+    L.C = (int)(c_need < 1 ? 1 : (c_need > kMaxCluster ? kMaxCluster : c_need));
+    const int units = L.C * kUnitsPerCTA;
+    L.ue = (((V + units - 1) / units) + 7) & ~7;
+    L.slot = L.ue * esz + 32;  // an aligned superset of a unit's window fits
+    L.NS = kUnitsPerCTA;
+    while (L.NS > 1 && (int64_t)L.NS * L.slot > kRoundMaxBytes) L.NS >>= 1;
     return L;
 }
 
 int check_launch() {
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
-    return SPEC_OK;
-}
-
-template <class K, class P>
-int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const P &params) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, params);
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     return SPEC_OK;
 }
@@ -1254,21 +1431,27 @@ int stages_for(size_t extra) {
 size_t main_extra(int B) { return sizeof(int) * (size_t)(((B + 1) + 3) & ~3) + sizeof(MainRow) * kMaxDesc; }
 
 template <class Vec>
-int set_smem_attrs(int dev, size_t main_smem) {
+int set_smem_attrs(int dev) {
     const int which = Vec::ESIZE == 2 ? 0 : 1;
     if (g_attr_set[dev][which]) return SPEC_OK;
     cudaError_t e = cudaFuncSetAttribute(main_kernel<Vec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)main_smem);
-
+                                         (int)kSmemBudget);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(commit_kernel<Vec::ESIZE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kCommitSmemMax);
+    // the largest shared-memory carveout, so that kCommitBlocksPerSM CTAs fit an SM
+    // and every cluster of a launch is resident at once
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(commit_kernel<Vec::ESIZE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     g_attr_set[dev][which] = true;
     return SPEC_OK;
 }
 
 template <class Vec>
-int launch_all(int dev, const Layout &L, const MainParams &mp, const AcceptParams &ap, const TailParams &tp,
-               const FinalParams &fp, cudaStream_t st) {
-    int rc = set_smem_attrs<Vec>(dev, kSmemBudget);
+int launch_all(int dev, const Layout &L, const MainParams &mp, const CommitParams &cp, cudaStream_t st) {
+    int rc = set_smem_attrs<Vec>(dev);
     if (rc) return rc;
     cudaError_t e = cudaMemsetAsync(mp.ctrl, 0, sizeof(Ctrl), st);
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
@@ -1278,22 +1461,28 @@ int launch_all(int dev, const Layout &L, const MainParams &mp, const AcceptParam
         main_kernel<Vec><<<L.G, kPipeThreads, main_smem, st>>>(mp);
     }
     if ((rc = check_launch())) return rc;
-    {
-        ProfScope ps(st);
-        rc = launch_pdl(accept_kernel, dim3(mp.B), dim3(kAcceptThreads), 0, st, ap);
-    }
-    if (rc) return rc;
-    {
-        ProfScope ps(st);
-        rc = launch_pdl(tail_kernel<Vec>, dim3(L.G * kTailBlocksPerSM), dim3(kTailThreads), 0, st, tp);
-    }
-    if (rc) return rc;
-    {
-        ProfScope ps(st);
-        const int wpb = kFinalThreads / 32;
-        rc = launch_pdl(final_kernel, dim3((mp.B + wpb - 1) / wpb), dim3(kFinalThreads), 0, st, fp);
-    }
-    return rc;
+    ProfScope ps(st);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(mp.B * L.C));
+    cfg.blockDim = dim3(kCommitThreads);
+    cfg.dynamicSmemBytes = commit_smem_bytes(L.NS, L.slot, mp.Kmax, L.G);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[3];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)L.C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    // let a cluster share SMs, so that clusters placed while main_kernel drains do
+    // not fragment the free slots and leave later clusters waiting for a second wave
+    attr[2].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+    attr[2].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
+    cfg.attrs = attr;
+    cfg.numAttrs = 3;
+    e = cudaLaunchKernelEx(&cfg, commit_kernel<Vec::ESIZE>, cp);
+    if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
+    return SPEC_OK;
 }
 
 int verify_impl(const void *target, const void *draft, int dtype, int B, int Kmax, int V, int64_t ld_row,
@@ -1314,7 +1503,11 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     int dev = 0, sms = 0;
     int rc = device_info(&dev, &sms);
     if (rc) return rc;
+    if (sms > kMaxCtas) return SPEC_EUNSUPPORTED;
     const Layout L = make_layout(B, Kmax, V, esz, sms, sample ? 2 * Kmax : Kmax);
+    // chunk indices of the main pass and commit units are 32-bit; one unit slot
+    // must fit a staging round
+    if ((int64_t)B * 2 * Kmax * L.cpr >= ((int64_t)1 << 31) || L.slot > kRoundMaxBytes) return SPEC_EUNSUPPORTED;
     if (!ws) return SPEC_EWORKSPACE;
     if (ws_bytes < L.total) return SPEC_EWORKSPACE;
     rc = prof_prepare();
@@ -1339,71 +1532,37 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     mp.stages = stages_for(main_extra(B));
     mp.ctrl = ctrl;
 
-    AcceptParams ap;
-    ap.target = target;
-    ap.draft = draft;
-    ap.dtype = dtype;
-    ap.ld_row = ld_row;
-    ap.B = B;
-    ap.Kmax = Kmax;
-    ap.V = V;
-    ap.draft_tokens = draft_tokens;
-    ap.num_draft = num_draft;
-    ap.temperature = temps;
-    ap.seed = seed;
-    ap.step = (uint32_t)step;
-    ap.row_start = mp.row_start;
-    ap.parts = mp.parts;
-    ap.nseg = L.nseg;
-    ap.G = L.G;
-    ap.cpr = L.cpr;
-    ap.out_tokens = out_tokens;
-    ap.out_accepted = out_accepted;
-    ap.out_p = sample ? out_p : nullptr;
-    ap.out_q = sample ? out_q : nullptr;
-    ap.out_status = out_status;
-    ap.jobs = (Job *)(w + L.off_jobs);
-    ap.job_list = (int *)(w + L.off_job_list);
-    ap.job_best = (uint32_t *)(w + L.off_job_best);
-    ap.ctrl = ctrl;
-
-    TailParams tp;
-    tp.target = target;
-    tp.draft = draft;
-    tp.dtype = dtype;
-    tp.ld_row = ld_row;
-    tp.Kmax = Kmax;
-    tp.V = V;
-    tp.seed = seed;
-    tp.step = (uint32_t)step;
-    tp.jobs = ap.jobs;
-    tp.job_list = ap.job_list;
-    tp.parts = (Part *)(w + L.off_parts2);
-    tp.job_best = (uint32_t *)(w + L.off_job_best);
-    tp.ctrl = ctrl;
-
-    FinalParams fp;
-    fp.target = target;
-    fp.dtype = dtype;
-    fp.ld_row = ld_row;
-    fp.Kmax = Kmax;
-    fp.V = V;
-    fp.upr = L.upr;
-    fp.seed = seed;
-    fp.step = (uint32_t)step;
-    fp.jobs = ap.jobs;
-    fp.job_list = ap.job_list;
-    fp.parts = tp.parts;
-    fp.ctrl = ctrl;
-    fp.out_tokens = out_tokens;
-    fp.out_accepted = out_accepted;
-    fp.out_p = ap.out_p;
-    fp.out_q = ap.out_q;
-    fp.out_status = out_status;
+    CommitParams cp;
+    cp.target = target;
+    cp.draft = draft;
+    cp.dtype = dtype;
+    cp.ld_row = ld_row;
+    cp.B = B;
+    cp.Kmax = Kmax;
+    cp.V = V;
+    cp.draft_tokens = draft_tokens;
+    cp.num_draft = num_draft;
+    cp.temperature = temps;
+    cp.seed = seed;
+    cp.step = (uint32_t)step;
+    cp.row_start = mp.row_start;
+    cp.parts = mp.parts;
+    cp.nseg = L.nseg;
+    cp.G = L.G;
+    cp.cpr = L.cpr;
+    cp.C = L.C;
+    cp.ue = L.ue;
+    cp.NS = L.NS;
+    cp.slot = L.slot;
+    cp.out_tokens = out_tokens;
+    cp.out_accepted = out_accepted;
+    cp.out_p = sample ? out_p : nullptr;
+    cp.out_q = sample ? out_q : nullptr;
+    cp.out_status = out_status;
+    cp.ctrl = ctrl;
 
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    return dtype == SPEC_BF16 ? launch_all<VecBF16>(dev, L, mp, ap, tp, fp, st)
-                              : launch_all<VecF32>(dev, L, mp, ap, tp, fp, st);
+    return dtype == SPEC_BF16 ? launch_all<VecBF16>(dev, L, mp, cp, st) : launch_all<VecF32>(dev, L, mp, cp, st);
 }
 
 // Scratch of spec_verify_sample_noalloc: part of this module's device image, one
