@@ -41,28 +41,19 @@ using namespace specv;
 namespace {
 
 // ------------------------------------------------------------------ configuration
-constexpr int kCW = 16;                          // consumer warps per CTA (4 per scheduler)
-constexpr int kCT = kCW * 32;                    // consumer threads
-constexpr int kPipeThreads = kCT + 32;           // + one producer warp
-constexpr int kMaxStages = 8;                    // ring depth: as many as shared memory allows
-constexpr int kStageBytes = 32768;               // one chunk (plus alignment slack)
-constexpr int kChunkMaxBytes = kStageBytes - 32; // payload; an aligned superset fits a stage
-constexpr int kVPT = kStageBytes / 16 / kCT;     // 16-byte vectors per consumer thread (4)
-constexpr size_t kSmemBudget = 226 * 1024;       // dynamic shared memory per CTA (227 KB minus static)
+constexpr int kCW = 16;                          // warps per main-pass CTA
+constexpr int kCT = kCW * 32;                    // threads per main-pass CTA
+constexpr int kMainBlocksPerSM = 2;              // main-pass CTAs per SM (64 registers a thread)
+constexpr int kVPT = 8;                          // 16-byte loads in flight per thread and chunk
+constexpr int kChunkMaxBytes = kCT * kVPT * 16 - 32;  // an aligned superset of a chunk fits kCT x kVPT loads
 constexpr uint64_t kWaitNs = 2000000000ull;      // bound on every mbarrier wait (2 s)
 constexpr int kMaxDesc = 512;                    // per-CTA row descriptors kept in smem
-constexpr float kRescaleAt = 1024.f;             // lane chunk sum that moves the reference
 
 struct Part {
     float m;    // raw max of the segment (NaN-propagating)
     float s;    // sum 2^(x c - fl(m c)) over the segment (sampling rows)
     int idx;    // lowest index of the max
     float pad;
-};
-
-struct Ctrl {
-    int err;  // non-zero: a bounded wait gave up
-    int pad;
 };
 
 // ------------------------------------------------------------------ chunking
@@ -142,31 +133,25 @@ __device__ __forceinline__ void mask_vec<VecF32>(VecF32 &d, int64_t first, int e
     d.v = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Loads this consumer thread's vectors of a staged chunk; out-of-window entries -inf.
-// Vector t of thread ct holds global elements ebase + (ct + kCT t) VE + e.  Only a
-// window that does not start and end on 16-byte boundaries needs masking, which
-// is decided once per chunk (the branch is uniform across the CTA).
+// Loads this thread's vectors of a chunk straight from global memory (16-byte
+// loads that bypass L1); entries outside the chunk's window read as -inf.  Vector
+// t of thread ct holds global elements ebase + (ct + kCT t) VE + e.  Only a window
+// that does not start and end on 16-byte boundaries needs masking, which is
+// decided once per chunk (the branch is uniform across the CTA).
 template <class Vec>
-__device__ __forceinline__ void load_chunk(Vec (&d)[kVPT], const char *stage, const ChunkWin &w, int ct) {
+__device__ __forceinline__ void load_chunk(Vec (&d)[kVPT], const ChunkWin &w, int ct) {
     const int nvec = (int)(w.bytes >> 4);
     const int64_t ebase = (int64_t)w.e0 - w.shift;
-    const bool ragged = w.shift != 0 || ebase + (int64_t)nvec * Vec::VE != w.e1;
-    if (!ragged) {
+#pragma unroll
+    for (int t = 0; t < kVPT; ++t) {
+        const int j = ct + kCT * t;
+        d[t] = j < nvec ? Vec::load(w.a0, j) : Vec::neg_inf();
+    }
+    if (w.shift != 0 || ebase + (int64_t)nvec * Vec::VE != w.e1) {
 #pragma unroll
         for (int t = 0; t < kVPT; ++t) {
             const int j = ct + kCT * t;
-            d[t] = j < nvec ? Vec{lds128(stage + 16 * j)} : Vec::neg_inf();
-        }
-    } else {
-#pragma unroll
-        for (int t = 0; t < kVPT; ++t) {
-            const int j = ct + kCT * t;
-            if (j < nvec) {
-                d[t].v = lds128(stage + 16 * j);
-                if (j == 0 || j == nvec - 1) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, w.e0, w.e1);
-            } else {
-                d[t] = Vec::neg_inf();
-            }
+            if (j < nvec && (j == 0 || j == nvec - 1)) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, w.e0, w.e1);
         }
     }
 }
@@ -182,13 +167,13 @@ __device__ __forceinline__ float chunk_max(const Vec (&d)[NV]) {
 // First entry equal to x among a thread's vectors; vector t of thread ct holds
 // entries ebase + (ct + STRIDE t) VE + e.
 template <int STRIDE, class Vec, int NV>
-__device__ __forceinline__ int chunk_find(const Vec (&d)[NV], int64_t ebase, int ct, float x) {
+__device__ __forceinline__ int chunk_find(const Vec (&d)[NV], int ebase, int ct, float x) {
     int found = -1;
 #pragma unroll
     for (int t = 0; t < NV; ++t)
 #pragma unroll
         for (int e = 0; e < Vec::VE; ++e)
-            if (found < 0 && d[t].get(e) == x) found = (int)(ebase + (int64_t)(ct + STRIDE * t) * Vec::VE + e);
+            if (found < 0 && d[t].get(e) == x) found = ebase + (ct + STRIDE * t) * Vec::VE + e;
     return found;
 }
 
@@ -196,76 +181,15 @@ __device__ __forceinline__ int chunk_find(const Vec (&d)[NV], int64_t ebase, int
 template <class Vec>
 __device__ __forceinline__ float chunk_expsum(const Vec (&d)[kVPT], float c, float ms) {
     const float2 cc = make_float2(c, c), mm = make_float2(-ms, -ms);
-    float2 acc[Vec::VE / 2];
-#pragma unroll
-    for (int e = 0; e < Vec::VE / 2; ++e) acc[e] = make_float2(0.f, 0.f);
+    float2 acc = make_float2(0.f, 0.f);  // one pair: the warps of the SM supply the parallelism
 #pragma unroll
     for (int t = 0; t < kVPT; ++t)
 #pragma unroll
         for (int e = 0; e < Vec::VE; e += 2) {
             const float2 y = ffma2(make_float2(d[t].get(e), d[t].get(e + 1)), cc, mm);
-            acc[e / 2] = fadd2(acc[e / 2], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
+            acc = fadd2(acc, make_float2(ex2_approx(y.x), ex2_approx(y.y)));
         }
-#pragma unroll
-    for (int e = 1; e < Vec::VE / 2; ++e) acc[0] = fadd2(acc[0], acc[e]);
-    return acc[0].x + acc[0].y;
-}
-
-// ------------------------------------------------------------------ ring
-struct Ring {
-    char *stages;
-    uint64_t *full;
-    uint64_t *empty;
-    int n;  // stages
-};
-
-__host__ __device__ constexpr size_t ring_bytes(int n) {
-    return (size_t)n * kStageBytes + 2 * (size_t)kMaxStages * sizeof(uint64_t);
-}
-
-__device__ __forceinline__ Ring ring_at(unsigned char *smem, int n) {
-    Ring r;
-    r.stages = (char *)smem;
-    r.full = (uint64_t *)(smem + (size_t)n * kStageBytes);
-    r.empty = r.full + kMaxStages;
-    r.n = n;
-    return r;
-}
-
-__device__ __forceinline__ void ring_init(const Ring &r) {
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < r.n; ++s) {
-            mbar_init(&r.full[s], 1);
-            mbar_init(&r.empty[s], kCW);
-        }
-        mbar_init_fence();
-    }
-}
-
-// Producer (one thread): stage chunks c0 .. c1-1; window(c) gives the source.
-template <class Window>
-__device__ void ring_produce(const Ring &r, int64_t c0, int64_t c1, Window window, int *err) {
-    int s = 0;
-    uint32_t ph = 0;
-    for (int64_t c = c0; c < c1; ++c) {
-        if (!mbar_wait(&r.empty[s], ph ^ 1u, kWaitNs)) {
-            atomicOr(err, 1);
-            // wait (bounded) for the copies this thread still has in flight
-            const int64_t issued = c - c0;
-            for (int64_t back = 1; back <= r.n && issued - back >= 0; ++back) {
-                const int64_t i2 = issued - back;
-                mbar_wait(&r.full[i2 % r.n], (uint32_t)(i2 / r.n) & 1u, kWaitNs);
-            }
-            return;
-        }
-        const ChunkWin w = window(c);
-        mbar_arrive_expect_tx(&r.full[s], w.bytes);
-        bulk_g2s(r.stages + (size_t)s * kStageBytes, w.a0, w.bytes, &r.full[s]);
-        if (++s == r.n) {
-            s = 0;
-            ph ^= 1u;
-        }
-    }
+    return acc.x + acc.y;
 }
 
 // ------------------------------------------------------------------ per-request rows
@@ -327,11 +251,9 @@ struct MainParams {
     int B, Kmax, V;
     const int32_t *num_draft;
     const float *temperature;  // NULL: every request greedy
-    int *row_start;            // [B+1], written by block 0 for accept_kernel
+    int *row_start;            // [B+1], written by block 0 for commit_kernel
     Part *parts;
     int nseg;
-    int stages;
-    Ctrl *ctrl;
 };
 
 struct MainRow {
@@ -356,13 +278,16 @@ __device__ __forceinline__ MainRow main_row(const MainParams &p, const int *rs, 
     return m;
 }
 
+// Static contiguous ranges of the flattened chunk list, one per CTA (two CTAs per
+// SM, so that one CTA's arithmetic overlaps the other's loads).  Each thread issues
+// kVPT independent 16-byte loads per chunk before it reduces them.  This streams as
+// fast as a bulk-copy ring through shared memory did on this path, with no producer
+// warp, no ring and no waits.
 template <class Vec>
-__global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
+__global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const Ring ring = ring_at(smem, p.stages);
-    int *s_rs = (int *)(smem + ring_bytes(p.stages));
-    MainRow *s_desc = (MainRow *)(smem + ring_bytes(p.stages) + sizeof(int) * (size_t)(((p.B + 1) + 3) & ~3));
-    ring_init(ring);
+    int *s_rs = (int *)smem;
+    MainRow *s_desc = (MainRow *)(smem + sizeof(int) * (size_t)(((p.B + 1) + 3) & ~3));
     scan_request_rows(s_rs, p.B, p.num_draft, p.temperature, p.Kmax);  // ends with __syncthreads
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.row_start[i] = s_rs[i];
@@ -370,38 +295,19 @@ __global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
 
     const Chunking ck = make_chunking(p.V, Vec::ESIZE);
     const int G = gridDim.x;
-    const int64_t total = (int64_t)s_rs[p.B] * ck.cpr;
+    const int64_t total = (int64_t)s_rs[p.B] * ck.cpr;  // < 2^31 (checked by the host)
     if (total == 0) return;
-    const int64_t c0 = cta_first(total, G, blockIdx.x), c1 = cta_first(total, G, blockIdx.x + 1);
+    const int c0 = (int)cta_first(total, G, blockIdx.x), c1 = (int)cta_first(total, G, blockIdx.x + 1);
     if (c0 == c1) return;
-    const int first_row = (int)(c0 / ck.cpr);
-    const int nrows = (int)((c1 - 1) / ck.cpr) - first_row + 1;
+    const int first_row = c0 / ck.cpr;
+    const int nrows = (c1 - 1) / ck.cpr - first_row + 1;
     const bool table = nrows <= kMaxDesc;
     if (table)
         for (int i = threadIdx.x; i < nrows; i += blockDim.x) s_desc[i] = main_row<Vec>(p, s_rs, first_row + i);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int k0 = (int)(c0 - (int64_t)first_row * ck.cpr);
-
-    if (warp == kCW) {  // producer
-        if (lane == 0) {
-            int r = first_row, k = k0;
-            MainRow mr = table ? s_desc[0] : main_row<Vec>(p, s_rs, r);
-            ring_produce(ring, c0, c1, [&](int64_t) {
-                const ChunkWin w = chunk_window(mr.ptr, Vec::ESIZE, p.V, ck, k);
-                if (++k == ck.cpr) {
-                    k = 0;
-                    ++r;
-                    if (r < first_row + nrows) mr = table ? s_desc[r - first_row] : main_row<Vec>(p, s_rs, r);
-                }
-                return w;
-            }, &p.ctrl->err);
-        }
-        return;
-    }
-
-    const int ct = threadIdx.x;  // consumer thread 0 .. kCT-1
-    int r = first_row, k = k0;
+    const int ct = threadIdx.x;
+    int r = first_row, k = c0 - first_row * ck.cpr;
     MainRow mr = table ? s_desc[0] : main_row<Vec>(p, s_rs, r);
     float m = kNegInf, mc = 0.f, s = 0.f;
     int aidx = -1;
@@ -431,43 +337,25 @@ __global__ void __launch_bounds__(kPipeThreads, 1) main_kernel(MainParams p) {
         if (lane == 0) p.parts[part_slot(blockIdx.x, p.nseg, r - first_row, warp)] = out;
     };
 
-    int st = 0;
-    uint32_t ph = 0;
-    for (int64_t cc = c0; cc < c1; ++cc) {
-        if (!mbar_wait(&ring.full[st], ph, kWaitNs)) {
-            atomicOr(&p.ctrl->err, 2);
-            break;
-        }
+    for (int cc = c0; cc < c1; ++cc) {
         const ChunkWin w = chunk_window(mr.ptr, Vec::ESIZE, p.V, ck, k);
         Vec d[kVPT];
-        load_chunk(d, ring.stages + (size_t)st * kStageBytes, w, ct);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ring.empty[st]);
-        if (++st == ring.n) {
-            st = 0;
-            ph ^= 1u;
-        }
-        const int64_t ebase = (int64_t)w.e0 - w.shift;
+        load_chunk(d, w, ct);
+        const int ebase = w.e0 - w.shift;
         if (mr.c != 0.f) {
-            // s is kept relative to a per-lane reference entry m (mc = fl(m c)); any
-            // reference gives the exact sum, so it only moves when this chunk's terms
-            // grow past kRescaleAt (an entry more than 5 log2-units above m), on the
-            // first finite chunk, or for NaN / +inf.
-            float cs = chunk_expsum(d, mr.c, mc);
-            if (m == kNegInf || !(cs < kRescaleAt)) {
-                const float tm = chunk_max(d);
-                if (!(tm <= m)) {  // new reference, or NaN
-                    const float mcn = tm * mr.c;
-                    s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
-                    m = tm;
-                    mc = mcn;
-                    aidx = chunk_find<kCT>(d, ebase, ct, tm);
-                    cs = chunk_expsum(d, mr.c, mc);
-                } else if (m == kNegInf) {
-                    cs = 0.f;  // every entry so far is -inf
-                }
+            // s is kept relative to the lane's running max m (mc = fl(m c)), so every
+            // term is at most 1; the max moves (and s is rescaled) only when a chunk
+            // holds a larger entry, which a row sees a few times at most.  NaN or +inf
+            // makes m non-finite, which the commit pass reports.
+            const float tm = chunk_max(d);
+            if (!(tm <= m)) {
+                const float mcn = tm * mr.c;
+                s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
+                m = tm;
+                mc = mcn;
+                aidx = chunk_find<kCT>(d, ebase, ct, tm);
             }
-            s += cs;
+            if (m != kNegInf) s += chunk_expsum(d, mr.c, mc);
         } else {
             const float tm = chunk_max(d);
             if (tm != tm) {
@@ -555,7 +443,6 @@ struct CommitParams {
     float *out_p;
     float *out_q;
     int32_t *out_status;
-    Ctrl *ctrl;
 };
 
 // What the warp of draft position i leaves for the scan.
@@ -826,14 +713,20 @@ __device__ __forceinline__ const Part *part_at(const Part *parts, const int *cf,
     return &parts[part_slot(cta, nseg, r - fr[cta], q % kCW)];
 }
 
-// Combine one row's partials held one per lane (ok: the lane holds one).
-__device__ __forceinline__ RowRes finish_row(const Part &pt, bool ok, float c, bool greedy) {
-    const float M = warp_max_nan(ok ? pt.m : kNegInf);
+// Combine one row's partials held at most two per lane (ok[h]: slot h holds one;
+// slot 0 holds the lower partial index, so ties keep the lowest entry index).
+__device__ __forceinline__ RowRes finish_row(const Part (&pt)[2], const bool (&ok)[2], float c, bool greedy) {
+    const float M = warp_max_nan(max_nan_f32(ok[0] ? pt[0].m : kNegInf, ok[1] ? pt[1].m : kNegInf));
     const float MC = M * c;
     float sum = 0.f;
-    if (ok && !greedy && pt.m != kNegInf && pt.s != 0.f) sum = pt.s * exp2f(pt.m * c - MC);
-    float bm = ok ? pt.m : kNegInf;
-    int bi = ok ? pt.idx : -1;
+    float bm = kNegInf;
+    int bi = -1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (!ok[h]) continue;
+        if (!greedy && pt[h].m != kNegInf && pt[h].s != 0.f) sum += pt[h].s * exp2f(pt[h].m * c - MC);
+        if (better(pt[h].m, pt[h].idx, bm, bi)) { bm = pt[h].m; bi = pt[h].idx; }
+    }
     warp_argmax(bm, bi);
     RowRes res;
     res.M = M;
@@ -981,7 +874,6 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     __syncthreads();
 
     // ---- main_kernel's partials are complete from here on
-    if (p.ctrl->err) status = SPEC_STATUS_INTERNAL;
     const int nw = status == SPEC_STATUS_OK ? npos : 0;
     // one warp per draft position: target row i (flat r0 + i) and, sampling, draft
     // row i (flat r0 + k_b + i)
@@ -989,24 +881,28 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
         const int rt = r0 + i, rd = r0 + kb + i;
         const RowSpan st = s_span[i];
         const RowSpan sd = greedy ? st : s_span[p.Kmax + i];
-        const bool fast = st.n() <= 32 && sd.n() <= 32;
+        const bool fast = st.n() <= 64 && sd.n() <= 64;  // at most two partials per lane and row
         const char *drow = (const char *)p.draft + ((int64_t)b * p.Kmax + i) * p.ld_row * ESZ;
-        Part pt = {};  // this lane's target partial: a correction candidate
-        bool okt = false;
-        float dv = 0.f;  // draft logit at the candidate, fetched before it is known to be needed
+        Part pt[2] = {}, pd[2] = {};  // this lane's target partials: correction candidates
+        bool okt[2] = {false, false}, okd[2] = {false, false};
+        float dv[2] = {0.f, 0.f};  // draft logits at the candidates, fetched before they are known to be needed
         RowRes tr, dr;
         if (fast) {
-            Part pd = {};
-            bool okd = false;
-            if (lane < st.n()) {
-                const Part *q = part_at(p.parts, s_cf, s_fr, p.nseg, rt, st, lane);
-                if (q) { pt = *q; okt = true; }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int q = lane + 32 * h;
+                if (q < st.n()) {
+                    const Part *pp = part_at(p.parts, s_cf, s_fr, p.nseg, rt, st, q);
+                    if (pp) { pt[h] = *pp; okt[h] = true; }
+                }
+                if (!greedy && q < sd.n()) {
+                    const Part *pp = part_at(p.parts, s_cf, s_fr, p.nseg, rd, sd, q);
+                    if (pp) { pd[h] = *pp; okd[h] = true; }
+                }
             }
-            if (!greedy && lane < sd.n()) {
-                const Part *q = part_at(p.parts, s_cf, s_fr, p.nseg, rd, sd, lane);
-                if (q) { pd = *q; okd = true; }
-            }
-            if (!greedy && okt && pt.idx >= 0) dv = load_logit(drow, p.dtype, pt.idx);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (!greedy && okt[h] && pt[h].idx >= 0) dv[h] = load_logit(drow, p.dtype, pt[h].idx);
             tr = finish_row(pt, okt, c, greedy);
             if (!greedy) dr = finish_row(pd, okd, c, false);
         } else {
@@ -1040,9 +936,10 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
                 float sb = kNegInf;
                 int si = -1;
                 for (int q = lane; q < st.n(); q += 32) {
-                    Part cand = pt;
-                    bool ok = okt;
-                    float dq = dv;
+                    const bool h1 = q >= 32;  // the fast path holds partial q in slot q / 32
+                    Part cand = h1 ? pt[1] : pt[0];
+                    bool ok = h1 ? okt[1] : okt[0];
+                    float dq = h1 ? dv[1] : dv[0];
                     if (!fast) {
                         const Part *qq = part_at(p.parts, s_cf, s_fr, p.nseg, rt, st, q);
                         ok = qq != nullptr;
@@ -1381,7 +1278,7 @@ struct ProfScope {
 };
 
 struct Layout {
-    size_t off_ctrl, off_row_start, off_parts, total;
+    size_t off_row_start, off_parts, total;
     int nseg, G, cpr;  // main pass: partial segments per CTA, CTAs, chunks per row
     int C, ue, NS, slot;  // commit pass: cluster size, entries per unit, units per round, bytes per slot
 };
@@ -1390,13 +1287,11 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 Layout make_layout(int B, int Kmax, int V, int esz, int sms, int main_rows_per_request) {
     Layout L;
-    L.G = sms;
+    L.G = kMainBlocksPerSM * sms;
     const Chunking ck = make_chunking(V, esz);
     L.cpr = ck.cpr;
     L.nseg = segs_per_cta((int64_t)B * main_rows_per_request * ck.cpr, L.G, ck.cpr);
     size_t o = 0;
-    L.off_ctrl = o;
-    o = align256(o + sizeof(Ctrl));
     L.off_row_start = o;
     o = align256(o + sizeof(int) * (size_t)(B + 1));
     L.off_parts = o;
@@ -1422,23 +1317,15 @@ int check_launch() {
     return SPEC_OK;
 }
 
-// Ring depth from the shared-memory budget left after the per-CTA tables.
-int stages_for(size_t extra) {
-    const size_t avail = kSmemBudget - extra - 2 * (size_t)kMaxStages * sizeof(uint64_t);
-    int n = (int)(avail / kStageBytes);
-    return n > kMaxStages ? kMaxStages : n;
-}
+// Dynamic shared memory of main_kernel: the row scan and the row descriptors.
 size_t main_extra(int B) { return sizeof(int) * (size_t)(((B + 1) + 3) & ~3) + sizeof(MainRow) * kMaxDesc; }
 
 template <class Vec>
 int set_smem_attrs(int dev) {
     const int which = Vec::ESIZE == 2 ? 0 : 1;
     if (g_attr_set[dev][which]) return SPEC_OK;
-    cudaError_t e = cudaFuncSetAttribute(main_kernel<Vec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBudget);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(commit_kernel<Vec::ESIZE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kCommitSmemMax);
+    cudaError_t e = cudaFuncSetAttribute(commit_kernel<Vec::ESIZE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kCommitSmemMax);
     // the largest shared-memory carveout, so that kCommitBlocksPerSM CTAs fit an SM
     // and every cluster of a launch is resident at once
     if (e == cudaSuccess)
@@ -1453,12 +1340,9 @@ template <class Vec>
 int launch_all(int dev, const Layout &L, const MainParams &mp, const CommitParams &cp, cudaStream_t st) {
     int rc = set_smem_attrs<Vec>(dev);
     if (rc) return rc;
-    cudaError_t e = cudaMemsetAsync(mp.ctrl, 0, sizeof(Ctrl), st);
-    if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
-    const size_t main_smem = ring_bytes(mp.stages) + main_extra(mp.B);
     {
         ProfScope ps(st);
-        main_kernel<Vec><<<L.G, kPipeThreads, main_smem, st>>>(mp);
+        main_kernel<Vec><<<L.G, kCT, main_extra(mp.B), st>>>(mp);
     }
     if ((rc = check_launch())) return rc;
     ProfScope ps(st);
@@ -1480,7 +1364,7 @@ int launch_all(int dev, const Layout &L, const MainParams &mp, const CommitParam
     attr[2].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
     cfg.attrs = attr;
     cfg.numAttrs = 3;
-    e = cudaLaunchKernelEx(&cfg, commit_kernel<Vec::ESIZE>, cp);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kernel<Vec::ESIZE>, cp);
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     return SPEC_OK;
 }
@@ -1503,7 +1387,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     int dev = 0, sms = 0;
     int rc = device_info(&dev, &sms);
     if (rc) return rc;
-    if (sms > kMaxCtas) return SPEC_EUNSUPPORTED;
+    if (kMainBlocksPerSM * sms > kMaxCtas) return SPEC_EUNSUPPORTED;
     const Layout L = make_layout(B, Kmax, V, esz, sms, sample ? 2 * Kmax : Kmax);
     // chunk indices of the main pass and commit units are 32-bit; one unit slot
     // must fit a staging round
@@ -1514,7 +1398,6 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     if (rc) return rc;
 
     char *w = (char *)ws;
-    Ctrl *ctrl = (Ctrl *)(w + L.off_ctrl);
     const float *temps = sample ? temperature : nullptr;
 
     MainParams mp;
@@ -1529,8 +1412,6 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     mp.row_start = (int *)(w + L.off_row_start);
     mp.parts = (Part *)(w + L.off_parts);
     mp.nseg = L.nseg;
-    mp.stages = stages_for(main_extra(B));
-    mp.ctrl = ctrl;
 
     CommitParams cp;
     cp.target = target;
@@ -1559,7 +1440,6 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     cp.out_p = sample ? out_p : nullptr;
     cp.out_q = sample ? out_q : nullptr;
     cp.out_status = out_status;
-    cp.ctrl = ctrl;
 
     cudaStream_t st = (cudaStream_t)cuda_stream;
     return dtype == SPEC_BF16 ? launch_all<VecBF16>(dev, L, mp, cp, st) : launch_all<VecF32>(dev, L, mp, cp, st);
