@@ -153,8 +153,8 @@ int spec_verify_sample(const void *target, const void *draft, int dtype, int B, 
  *    SPEC_STATIC_SCRATCH_BYTES return SPEC_ESCRATCH before anything is launched
  *    (Kmax = 8 on a 152-SM device: B up to 1007 fits, for either logit type and
  *    any V; the scratch grows with B * Kmax, not with V).
- *  - Zeroing: the only scratch that must start at zero, a two-word control block,
- *    is cleared on cuda_stream by every call before its first kernel.
+ *  - Zeroing: none of the scratch needs to start at zero; every call writes what
+ *    it reads.
  *  - Races: every call on a device uses the same array, so two calls that can
  *    overlap (different streams, or host threads without ordering between them)
  *    corrupt each other's results.  Order the calls on one stream.

@@ -9,24 +9,21 @@
 //    committed plus one token (correction, or bonus from the row after the drafts).
 //  * "Bringing DSpark to vLLM Metal" -- greedy path: target argmax vs draft token.
 //
-// Kernels per call (fixed grids, no host synchronisation; each launch after the
-// first is a programmatic dependent launch):
+// Kernels per call (fixed grids, no host synchronisation; the second is a
+// programmatic dependent launch):
 //  main_kernel    streams the rows of every draft position once -- target and draft
-//                 rows of sampling requests, target rows of greedy ones -- through a
-//                 bulk-copy (TMA) ring in shared memory: one persistent CTA per SM, a
-//                 producer warp issuing 32 KB cp.async.bulk copies, sixteen consumer
-//                 warps reducing them.  Per (CTA, row, warp): max, sum of
-//                 2^(x log2e / T - max'), and the lowest argmax.  HBM-bound.
-//  accept_kernel  one CTA per request: combines the partials of its rows, sets the
-//                 status, computes p(x_i) and q(x_i), runs the acceptance scan,
-//                 emits the accepted drafts, and queues one job: the correction at
-//                 the first rejected row j (seeded with the segment argmaxes of row
-//                 j), the bonus draw on row k_b, or the greedy argmax of row k_b.
-//  tail_kernel    one warp per 1024-entry unit of each job's row, loaded with its
-//                 own 16-byte loads: Gumbel-max over log(max(0, p - q)) (draft values
-//                 gathered only at entries that can still win), Gumbel-max over the
-//                 target row, or argmax.
-//  final_kernel   one warp per job: combines the tail partials into the token.
+//                 rows of sampling requests, target rows of greedy ones -- with plain
+//                 16-byte loads: two 512-thread CTAs per SM over static contiguous
+//                 ranges of the flattened chunk list.  Per (CTA, row segment, warp):
+//                 max, sum of 2^(x log2e / T - max'), and the lowest argmax.
+//                 HBM-bound.
+//  commit_kernel  one cluster of up to 8 CTAs per request: combines the partials of
+//                 its rows (one warp per draft position), runs the acceptance scan,
+//                 emits the accepted drafts, and draws the one extra token -- the
+//                 correction at the first rejected row j (Gumbel-max over
+//                 log(max(0, p - q))), the bonus from row k_b, or the greedy argmax
+//                 of row k_b -- over the row staged into shared memory by bulk
+//                 copies, the CTAs' results meeting in rank 0 over DSMEM.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
