@@ -71,6 +71,10 @@ def _load():
         lib.oracle_verify_greedy_early_exit.restype = I32
         lib.oracle_schedule_verify_len.argtypes = [P, P, I32, I32, P, I32, I32, I32, P, P, P]
         lib.oracle_schedule_verify_len.restype = I32
+        lib.oracle_schedule_threshold.argtypes = [P, P, I32, I32, ctypes.c_float, P]
+        lib.oracle_schedule_threshold.restype = I32
+        lib.oracle_schedule_verify_len_stale.argtypes = [P, P, P, I32, I32, P, I32, I32, I32, P, P, P]
+        lib.oracle_schedule_verify_len_stale.restype = I32
         _lib = lib
         return lib
 
@@ -204,6 +208,39 @@ def schedule_verify_len(conf, max_len, step_time_us, budget: int, min_len: int) 
     flags = np.zeros(1, np.int32)
     rc = lib.oracle_schedule_verify_len(_ptr(c), _ptr(ml), B, K, _ptr(tau), tau.size, budget, min_len,
                                         _ptr(out_len), _ptr(info), _ptr(flags))
+    if rc != 0:
+        return None
+    return dict(len=out_len, n=int(info[0]), expected_tokens=float(info[1]),
+                tokens_per_us=float(info[2]), flags=int(flags[0]))
+
+
+def schedule_threshold(conf, max_len, threshold: float) -> np.ndarray | None:
+    """Static threshold truncation: L_b = the first position whose confidence is
+    below the threshold (NaN counts as below), else maxlen_b; None if invalid."""
+    lib = _load()
+    c = _c(conf, np.float32)
+    B, K = c.shape
+    ml = None if max_len is None else _c(max_len, np.int32)
+    out = np.zeros(B, np.int32)
+    if lib.oracle_schedule_threshold(_ptr(c), _ptr(ml), B, K, float(threshold), _ptr(out)) != 0:
+        return None
+    return out
+
+
+def schedule_verify_len_stale(conf_stale, conf, max_len, step_time_us, budget: int, min_len: int) -> dict | None:
+    """Two-step-stale batch sizing: the total n* from conf_stale, the slots by conf."""
+    lib = _load()
+    cs = _c(conf_stale, np.float32)
+    c = _c(conf, np.float32)
+    B, K = c.shape
+    assert cs.shape == c.shape
+    ml = None if max_len is None else _c(max_len, np.int32)
+    tau = _c(step_time_us, np.float32)
+    out_len = np.zeros(B, np.int32)
+    info = np.zeros(3)
+    flags = np.zeros(1, np.int32)
+    rc = lib.oracle_schedule_verify_len_stale(_ptr(cs), _ptr(c), _ptr(ml), B, K, _ptr(tau), tau.size, budget,
+                                              min_len, _ptr(out_len), _ptr(info), _ptr(flags))
     if rc != 0:
         return None
     return dict(len=out_len, n=int(info[0]), expected_tokens=float(info[1]),

@@ -610,3 +610,87 @@ int oracle_schedule_verify_len(const float *conf, const int32_t *max_len, int B,
     free(S); free(mand); free(mlen); free(cand);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Scheduler variants [PPR prefix scheduler; VBK 4.2.2, 3]                    */
+/* ------------------------------------------------------------------------- */
+/*
+ * Static threshold truncation [PPR "Prefix scheduler": scan left to right and
+ * truncate at the first position whose confidence falls below the threshold;
+ * VBK Sec. 3: cut draft tokens whose confidence is below a fixed cutoff].
+ * L_b = the first i < maxlen_b with c_{b,i} < threshold (NaN counts as below),
+ * else maxlen_b; maxlen_b = clamp(max_len[b], 0, Kmax) (NULL: Kmax).  Reading:
+ * the score compared is the per-position confidence, as both passages state.
+ */
+int oracle_schedule_threshold(const float *conf, const int32_t *max_len, int B, int Kmax, float threshold,
+                              int32_t *out_len) {
+    int b, i;
+    if (B < 0 || Kmax < 0 || isnan(threshold)) return 1;
+    for (b = 0; b < B; ++b) {
+        int ml = max_len ? max_len[b] : Kmax, L;
+        if (ml < 0) ml = 0;
+        if (ml > Kmax) ml = Kmax;
+        L = ml;
+        for (i = 0; i < ml; ++i) {
+            const double c = (double)conf[(int64_t)b * Kmax + i];
+            if (!(c >= (double)threshold)) { /* below, or NaN */
+                L = i;
+                break;
+            }
+        }
+        out_len[b] = L;
+    }
+    return 0;
+}
+
+/*
+ * Two-step-stale batch sizing [VBK 4.2.2, production: the engine prepares the
+ * next batch while the GPU is busy, so the batch size comes from the scores of
+ * two steps earlier and the tokens are chosen with the latest scores].
+ * n* = the total that oracle_schedule_verify_len picks from conf_stale (same
+ * table, budget, min_len and max_len); then every request keeps its mandatory
+ * m_b slots and the n* - sum m_b remaining slots go to the candidates ranked by
+ * the survival of conf (latest), as in the plain scheduler.
+ * out_info[3] = {n*, B + sum E under conf, (B + sum E) / tau[n*]};
+ * *out_flags: bit 1 from the stale search, bit 2 a survival tie across the cut
+ * of the latest ranking.
+ */
+int oracle_schedule_verify_len_stale(const float *conf_stale, const float *conf, const int32_t *max_len, int B,
+                                     int Kmax, const float *step_time_us, int n_table, int budget, int min_len,
+                                     int32_t *out_len, double *out_info, int32_t *out_flags) {
+    double info[3];
+    int32_t flags_stale = 0, flags_now = 0, nstar, b, rc;
+    int32_t *len_now = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+    rc = oracle_schedule_verify_len(conf_stale, max_len, B, Kmax, step_time_us, n_table, budget, min_len,
+                                    out_len, info, &flags_stale);
+    if (rc) {
+        free(len_now);
+        return rc;
+    }
+    nstar = (int32_t)info[0];
+    /* the latest scores under a table on which n* is the only usable total: the
+     * plain scheduler then grants exactly the n* - sum m_b best candidates */
+    {
+        /* (the table must also reach B * min_len, which argument checking requires) */
+        const int top = nstar > B * min_len ? nstar : B * min_len;
+        float *tau1 = (float *)malloc(sizeof(float) * (size_t)(top + 1));
+        int n;
+        for (n = 0; n <= top; ++n) tau1[n] = n == nstar ? 1.0f : -1.0f;
+        rc = oracle_schedule_verify_len(conf, max_len, B, Kmax, tau1, top + 1, top, min_len, len_now, info,
+                                        &flags_now);
+        free(tau1);
+    }
+    if (rc || (int32_t)info[0] != nstar) {
+        free(len_now);
+        return 1;
+    }
+    for (b = 0; b < B; ++b) out_len[b] = len_now[b];
+    if (out_info) {
+        out_info[0] = (double)nstar;
+        out_info[1] = info[1];
+        out_info[2] = (step_time_us[nstar] > 0.0f) ? info[1] / (double)step_time_us[nstar] : 0.0;
+    }
+    if (out_flags) *out_flags = (flags_stale & 1) | (flags_now & 2);
+    free(len_now);
+    return 0;
+}

@@ -131,3 +131,96 @@ def test_prefix_property_and_budget(oracle_mod):
         dropped = [S[b, i] for b in range(B) for i in range(L[b], K)]
         if kept and dropped:
             assert min(kept) >= max(dropped)
+
+
+# ---------------------------------------------------------------------------
+# Scheduler variants: static threshold truncation ("Accelerating Large-Model
+# Inference ... DSpark", prefix scheduler: scan left to right, truncate at the
+# first score below the threshold; "DSpark paper review" Sec. 3: a fixed cutoff)
+# and two-step-stale batch sizing ("DSpark paper review" Sec. 4.2.2: the batch
+# size from the scores of two steps earlier, the tokens from the latest ones).
+
+def test_threshold_hand_computed(oracle_mod):
+    conf = np.array([[0.9, 0.8, 0.3, 0.9], [0.2, 0.9, 0.9, 0.9], [0.5, 0.5, 0.5, 0.5]], np.float32)
+    assert list(oracle_mod.schedule_threshold(conf, None, 0.5)) == [2, 0, 4]  # 0.5 >= 0.5 is kept
+    assert list(oracle_mod.schedule_threshold(conf, np.array([1, 3, 2], np.int32), 0.5)) == [1, 0, 2]
+    assert list(oracle_mod.schedule_threshold(conf, None, 0.0)) == [4, 4, 4]
+    assert list(oracle_mod.schedule_threshold(conf, None, 1.01)) == [0, 0, 0]
+
+
+def test_threshold_nan_truncates(oracle_mod):
+    conf = np.array([[0.9, np.nan, 0.9]], np.float32)
+    assert list(oracle_mod.schedule_threshold(conf, None, 0.1)) == [1]
+    assert oracle_mod.schedule_threshold(conf, None, float("nan")) is None
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_threshold_invariants(oracle_mod, seed):
+    """Every kept position is at or above the threshold, the first cut one is
+    below it, and raising the threshold never lengthens a draft."""
+    rng = np.random.default_rng(seed)
+    B, K = 200, 16
+    conf = (rng.beta(4, 1.5, size=(B, K)) * 0.95 ** np.arange(K)).astype(np.float32)
+    ml = rng.integers(0, K + 1, size=B).astype(np.int32)
+    prev = None
+    for thr in (0.2, 0.4, 0.6, 0.8):
+        L = oracle_mod.schedule_threshold(conf, ml, thr)
+        for b in range(B):
+            assert 0 <= L[b] <= ml[b]
+            assert (conf[b, :L[b]] >= np.float32(thr)).all()
+            if L[b] < ml[b]:
+                assert conf[b, L[b]] < np.float32(thr)
+        if prev is not None:
+            assert (L <= prev).all()
+        prev = L
+
+
+def test_stale_equals_plain_when_scores_agree(oracle_mod):
+    rng = np.random.default_rng(3)
+    conf = rng.beta(4, 1.5, size=(20, 6)).astype(np.float32)
+    tau = (12 + 0.3 * np.arange(121)).astype(np.float32)
+    a = oracle_mod.schedule_verify_len(conf, None, tau, 90, 1)
+    s = oracle_mod.schedule_verify_len_stale(conf, conf, None, tau, 90, 1)
+    assert (a["len"] == s["len"]).all() and a["n"] == s["n"]
+    assert abs(a["expected_tokens"] - s["expected_tokens"]) < 1e-12
+
+
+def test_stale_hand_computed(oracle_mod):
+    """Stale scores size the batch, the latest ones pick the slots.  Stale:
+    request 0 confident, request 1 not; latest: the reverse.  min_len 0 and
+    tau = 10 + n: F(n) = E(n) / (10 + n)."""
+    stale = np.array([[0.9, 0.9], [0.1, 0.1]], np.float32)
+    now = np.array([[0.1, 0.1], [0.9, 0.9]], np.float32)
+    tau = (10.0 + np.arange(5)).astype(np.float32)
+    # stale ranking 0.9, 0.81, 0.1, 0.01: F = 0, 0.9/11, 1.71/12, 1.81/13, 1.82/14 -> n* = 2
+    s = oracle_mod.schedule_verify_len_stale(stale, now, None, tau, 4, 0)
+    assert s["n"] == 2
+    assert list(s["len"]) == [0, 2]  # the two slots go to request 1 under the latest scores
+    assert abs(s["expected_tokens"] - (2 + 0.9 + 0.81)) < 1e-6
+    assert abs(s["tokens_per_us"] - (2 + 0.9 + 0.81) / 12) < 1e-7
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_stale_allocation_is_best_for_the_latest_scores(oracle_mod, seed):
+    """Exhaustive: among every allocation of n* slots (each request a prefix of at
+    least m_b and at most maxlen_b), none has a larger expected accepted length
+    under the latest scores."""
+    rng = np.random.default_rng(seed)
+    B, K = int(rng.integers(1, 4)), int(rng.integers(1, 5))
+    stale = rng.uniform(0.05, 1.0, size=(B, K)).astype(np.float32)
+    now = rng.uniform(0.05, 1.0, size=(B, K)).astype(np.float32)
+    ml = rng.integers(0, K + 1, size=B).astype(np.int32)
+    min_len = int(rng.integers(0, 2))
+    tau = (8 + rng.uniform(0.5, 3.0) * np.arange(B * K + 1)).astype(np.float32)
+    s = oracle_mod.schedule_verify_len_stale(stale, now, ml, tau, B * K, min_len)
+    assert s is not None
+    surv = np.cumprod(now.astype(np.float64), axis=1)
+    mand = np.minimum(min_len, ml)
+    best = -1.0
+    for L in itertools.product(*[range(int(mand[b]), int(ml[b]) + 1) for b in range(B)]):
+        if sum(L) != s["n"]:
+            continue
+        best = max(best, sum(surv[b, :L[b]].sum() for b in range(B)))
+    got = sum(surv[b, :s["len"][b]].sum() for b in range(B))
+    assert sum(s["len"]) == s["n"]
+    assert got >= best - 1e-12
