@@ -190,6 +190,33 @@ int spec_schedule_verify_len(const float *conf, const int32_t *max_len, int B, i
                              const float *step_time_us, int n_table, int budget, int min_len,
                              int32_t *out_len, double *out_info, void *cuda_stream);
 
+/*
+ * Two-step-stale batch sizing ("DSpark paper review", Sec. 4.2.2, production
+ * variant).  The engine prepares the next batch while the GPU is still busy, so
+ * the total number of verified slots n* comes from the scores of two steps
+ * earlier (conf_stale), chosen exactly as spec_schedule_verify_len chooses it.
+ * The n* slots then go to the requests by the latest scores (conf): every
+ * request keeps its m_b mandatory slots and the rest are the best survivals of
+ * conf (ties: lower b, then lower i).
+ *  conf_stale, conf  [B, Kmax] float32; the other arguments as for
+ *                    spec_schedule_verify_len
+ *  out_info          [3] double {n*, B + sum E under conf, that / step_time_us[n*]}
+ */
+int spec_schedule_verify_len_stale(const float *conf_stale, const float *conf, const int32_t *max_len, int B,
+                                   int Kmax, const float *step_time_us, int n_table, int budget, int min_len,
+                                   int32_t *out_len, double *out_info, void *cuda_stream);
+
+/*
+ * Static threshold truncation ("Accelerating Large-Model Inference ... DSpark",
+ * prefix scheduler: scan left to right and truncate at the first score below the
+ * threshold; "DSpark paper review", Sec. 3: a fixed confidence cutoff).
+ * out_len[b] = the first i < maxlen_b with conf[b, i] < threshold (NaN counts as
+ * below), else maxlen_b = clamp(max_len[b], 0, Kmax) (max_len NULL: Kmax).
+ * SPEC_EINVAL for a NaN threshold.  Uses no workspace.
+ */
+int spec_schedule_threshold(const float *conf, const int32_t *max_len, int B, int Kmax, float threshold,
+                            int32_t *out_len, void *cuda_stream);
+
 /* Short text for a return code. */
 const char *spec_error_string(int err);
 

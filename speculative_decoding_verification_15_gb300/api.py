@@ -76,6 +76,27 @@ def schedule_verify_len(conf, step_time_us, budget: int, min_len: int, max_len=N
     return out_len, info
 
 
+def schedule_verify_len_stale(conf_stale, conf, step_time_us, budget: int, min_len: int, max_len=None,
+                              stream=None):
+    dev = conf.device
+    B = conf.shape[0]
+    out_len = torch.empty(B, dtype=torch.int32, device=dev)
+    info = torch.empty(3, dtype=torch.float64, device=dev)
+    binding.spec_schedule_verify_len_stale(conf_stale.to(device=dev, dtype=torch.float32).contiguous(),
+                                           conf.to(torch.float32).contiguous(), _as_i32(max_len, dev),
+                                           step_time_us.to(device=dev, dtype=torch.float32).contiguous(), budget,
+                                           min_len, out_len, info, stream)
+    return out_len, info
+
+
+def schedule_threshold(conf, threshold: float, max_len=None, stream=None):
+    dev = conf.device
+    out_len = torch.empty(conf.shape[0], dtype=torch.int32, device=dev)
+    binding.spec_schedule_threshold(conf.to(torch.float32).contiguous(), _as_i32(max_len, dev), threshold,
+                                    out_len, stream)
+    return out_len
+
+
 def verify_sample_host(target_h, draft_h, tokens_h, temperature_h, seed: int, step: int, num_draft_h=None,
                        device=None, dev_buffers: dict | None = None) -> dict:
     """End-to-end call from host (ideally pinned) tensors: copy in, verify, copy the

@@ -64,6 +64,10 @@ def load(path: str | None = None):
         lib.spec_verify_sample_noalloc.restype = I32
         lib.spec_schedule_verify_len.argtypes = [P, P, I32, I32, P, I32, I32, I32, P, P, P]
         lib.spec_schedule_verify_len.restype = I32
+        lib.spec_schedule_verify_len_stale.argtypes = [P, P, P, I32, I32, P, I32, I32, I32, P, P, P]
+        lib.spec_schedule_verify_len_stale.restype = I32
+        lib.spec_schedule_threshold.argtypes = [P, P, I32, I32, ctypes.c_float, P, P]
+        lib.spec_schedule_threshold.restype = I32
         lib.spec_error_string.argtypes = [I32]
         lib.spec_error_string.restype = ctypes.c_char_p
         lib.spec_last_cuda_error.argtypes = []
@@ -246,6 +250,44 @@ def spec_schedule_verify_len(conf, max_len, step_time_us, budget: int, min_len: 
                                       _ptr(out_info), _stream_handle(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_schedule_verify_len", rc, lib)
+
+
+def spec_schedule_verify_len_stale(conf_stale, conf, max_len, step_time_us, budget: int, min_len: int, out_len,
+                                   out_info=None, stream=None) -> None:
+    lib = load()
+    if conf.dim() != 2 or conf_stale.shape != conf.shape:
+        raise ValueError("conf and conf_stale must both be [B, Kmax]")
+    B, Kmax = conf.shape
+    dev = conf.device
+    _need(conf, "conf", torch.float32, None, dev)
+    _need(conf_stale, "conf_stale", torch.float32, None, dev)
+    if max_len is not None:
+        _need(max_len, "max_len", torch.int32, (B,), dev)
+    _need(step_time_us, "step_time_us", torch.float32, None, dev)
+    _need(out_len, "out_len", torch.int32, (B,), dev)
+    if out_info is not None:
+        _need(out_info, "out_info", torch.float64, (3,), dev)
+    rc = lib.spec_schedule_verify_len_stale(_ptr(conf_stale), _ptr(conf), _ptr(max_len), B, Kmax,
+                                            _ptr(step_time_us), step_time_us.numel(), int(budget), int(min_len),
+                                            _ptr(out_len), _ptr(out_info), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_schedule_verify_len_stale", rc, lib)
+
+
+def spec_schedule_threshold(conf, max_len, threshold: float, out_len, stream=None) -> None:
+    lib = load()
+    if conf.dim() != 2:
+        raise ValueError("conf must be [B, Kmax]")
+    B, Kmax = conf.shape
+    dev = conf.device
+    _need(conf, "conf", torch.float32, None, dev)
+    if max_len is not None:
+        _need(max_len, "max_len", torch.int32, (B,), dev)
+    _need(out_len, "out_len", torch.int32, (B,), dev)
+    rc = lib.spec_schedule_threshold(_ptr(conf), _ptr(max_len), B, Kmax, float(threshold), _ptr(out_len),
+                                     _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_schedule_threshold", rc, lib)
 
 
 def profile_enable(on: bool) -> None:

@@ -11,6 +11,15 @@
 // all candidate slots in shared memory (survival descending, then request, then
 // position), an inclusive scan of the sorted survivals, the throughput of every
 // admissible total, its argmax (smallest total on ties), and per-request counts.
+//
+// Variants:
+//  * two-step-stale sizing (Sec. 4.2.2, production): the engine prepares the next
+//    batch while the GPU still runs, so the total comes from the scores of two
+//    steps earlier and the slots from the latest scores -- the same kernel sorts
+//    twice;
+//  * static threshold truncation ("Accelerating Large-Model Inference ... DSpark",
+//    prefix scheduler; the review's Sec. 3 fixed cutoff): each draft stops at the
+//    first position whose confidence is below a threshold -- one thread a request.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,33 +33,23 @@ __device__ __forceinline__ bool before(double ka, int ia, double kb, int ib) {
     return ka > kb || (ka == kb && ia < ib);
 }
 
-__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *conf, const int32_t *max_len, int B,
-                                                                 int Kmax, const float *tau, int n_table,
-                                                                 int budget, int min_len, int npow2,
-                                                                 int32_t *out_len, double *out_info) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    double *key = (double *)smem;                     // [npow2]  survival, later prefix sums
-    int *id = (int *)(key + npow2);                   // [npow2]  b * Kmax + i
-    int *cnt = id + npow2;                            // [B]
-    __shared__ int s_n0, s_ncand;
-    __shared__ double s_E0;
-    __shared__ double s_redF[kSchedThreads / 32];
-    __shared__ int s_redN[kSchedThreads / 32];
-    __shared__ double s_wsum[kSchedThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-
+// Survival products of conf and the candidate slots: key[b Kmax + i] = S_{b,i}
+// for the slots a request may add (m_b <= i < maxlen_b), -1 elsewhere; returns
+// n0 = sum m_b, the number of candidates and E0 = sum of the mandatory
+// survivals through shared memory.  Every thread of the CTA calls it.
+__device__ void build_keys(const float *conf, const int32_t *max_len, int B, int Kmax, int min_len, int npow2,
+                           double *key, int *id, int *s_n0, int *s_ncand, double *s_E0) {
+    const int tid = threadIdx.x;
     if (tid == 0) {
-        s_n0 = 0;
-        s_ncand = 0;
-        s_E0 = 0.0;
+        *s_n0 = 0;
+        *s_ncand = 0;
+        *s_E0 = 0.0;
     }
     for (int i = tid; i < npow2; i += kSchedThreads) {
         key[i] = -1.0;  // padding sorts after every survival (>= 0)
         id[i] = 0x7fffffff;
     }
     __syncthreads();
-
-    // survival products and candidate slots
     for (int b = tid; b < B; b += kSchedThreads) {
         int ml = max_len ? max_len[b] : Kmax;
         ml = ml < 0 ? 0 : (ml > Kmax ? Kmax : ml);
@@ -68,14 +67,17 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
                 id[b * Kmax + i] = b * Kmax + i;
             }
         }
-        cnt[b] = 0;
-        atomicAdd(&s_n0, mand);
-        atomicAdd(&s_ncand, ml - mand);
-        atomicAdd(&s_E0, e0);
+        atomicAdd(s_n0, mand);
+        atomicAdd(s_ncand, ml - mand);
+        atomicAdd(s_E0, e0);
     }
     __syncthreads();
+}
 
-    // bitonic sort: `before` order (survival descending, then b, then i)
+// Bitonic sort of (key, id) in the `before` order (survival descending, then b,
+// then i), then key[j] = the sum of the j+1 largest survivals (padding adds 0).
+__device__ void sort_and_scan(double *key, int *id, int npow2, double *s_wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     for (int k = 2; k <= npow2; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
             for (int i = tid; i < npow2; i += kSchedThreads) {
@@ -96,8 +98,6 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
             __syncthreads();
         }
     }
-
-    // inclusive scan of the sorted survivals (padding contributes 0)
     const int per = (npow2 + kSchedThreads - 1) / kSchedThreads;
     const int lo = tid * per < npow2 ? tid * per : npow2;
     const int hi = lo + per < npow2 ? lo + per : npow2;
@@ -118,6 +118,29 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
         key[i] = run;
     }
     __syncthreads();
+}
+
+// One CTA.  conf sizes the batch: the total n* with the best expected throughput
+// over the whole table.  conf_alloc (NULL: conf) ranks the slots that fill it.
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *conf, const float *conf_alloc,
+                                                                 const int32_t *max_len, int B, int Kmax,
+                                                                 const float *tau, int n_table, int budget,
+                                                                 int min_len, int npow2, int32_t *out_len,
+                                                                 double *out_info) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    double *key = (double *)smem;                     // [npow2]  survival, later prefix sums
+    int *id = (int *)(key + npow2);                   // [npow2]  b * Kmax + i
+    int *cnt = id + npow2;                            // [B]
+    __shared__ int s_n0, s_ncand;
+    __shared__ double s_E0;
+    __shared__ double s_redF[kSchedThreads / 32];
+    __shared__ int s_redN[kSchedThreads / 32];
+    __shared__ double s_wsum[kSchedThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+    for (int b = tid; b < B; b += kSchedThreads) cnt[b] = 0;
+    build_keys(conf, max_len, B, Kmax, min_len, npow2, key, id, &s_n0, &s_ncand, &s_E0);
+    sort_and_scan(key, id, npow2, s_wsum);
 
     // throughput of every admissible total, best over the whole table
     const int n0 = s_n0;
@@ -157,6 +180,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
     }
     __syncthreads();
     const int nstar = s_redN[0];
+    if (conf_alloc) {  // the latest scores pick the n* slots (same mandatory slots and candidates)
+        build_keys(conf_alloc, max_len, B, Kmax, min_len, npow2, key, id, &s_n0, &s_ncand, &s_E0);
+        sort_and_scan(key, id, npow2, s_wsum);
+    }
     const int take = nstar - n0 > 0 ? nstar - n0 : 0;
     for (int t = tid; t < take; t += kSchedThreads) atomicAdd(&cnt[id[t] / Kmax], 1);
     __syncthreads();
@@ -174,11 +201,30 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
     }
 }
 
+// Static threshold truncation: one thread per request scans its confidences left
+// to right and stops at the first one below the threshold (NaN counts as below).
+__global__ void threshold_kernel(const float *conf, const int32_t *max_len, int B, int Kmax, float threshold,
+                                 int32_t *out_len) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    int ml = max_len ? max_len[b] : Kmax;
+    ml = ml < 0 ? 0 : (ml > Kmax ? Kmax : ml);
+    int L = ml;
+    for (int i = 0; i < ml; ++i)
+        if (!(conf[(int64_t)b * Kmax + i] >= threshold)) {
+            L = i;
+            break;
+        }
+    out_len[b] = L;
+}
+
 }  // namespace
 
-extern "C" int spec_schedule_verify_len(const float *conf, const int32_t *max_len, int B, int Kmax,
-                                        const float *step_time_us, int n_table, int budget, int min_len,
-                                        int32_t *out_len, double *out_info, void *cuda_stream) {
+namespace {
+
+int launch_schedule(const float *conf, const float *conf_alloc, const int32_t *max_len, int B, int Kmax,
+                    const float *step_time_us, int n_table, int budget, int min_len, int32_t *out_len,
+                    double *out_info, void *cuda_stream) {
     if (B < 0 || Kmax < 0 || min_len < 0 || n_table < 1 || budget < 0) return SPEC_EINVAL;
     if ((int64_t)budget < (int64_t)B * min_len || (int64_t)n_table - 1 < (int64_t)B * min_len) return SPEC_EINVAL;
     if (!step_time_us || (B > 0 && !out_len) || (B > 0 && Kmax > 0 && !conf)) return SPEC_EINVAL;
@@ -189,7 +235,37 @@ extern "C" int spec_schedule_verify_len(const float *conf, const int32_t *max_le
     cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return SPEC_ECUDA;
     schedule_kernel<<<1, kSchedThreads, smem, (cudaStream_t)cuda_stream>>>(
-        conf, max_len, B, Kmax, step_time_us, n_table, budget, min_len, npow2, out_len, out_info);
+        conf, conf_alloc, max_len, B, Kmax, step_time_us, n_table, budget, min_len, npow2, out_len, out_info);
     e = cudaGetLastError();
+    return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+}  // namespace
+
+extern "C" int spec_schedule_verify_len(const float *conf, const int32_t *max_len, int B, int Kmax,
+                                        const float *step_time_us, int n_table, int budget, int min_len,
+                                        int32_t *out_len, double *out_info, void *cuda_stream) {
+    return launch_schedule(conf, nullptr, max_len, B, Kmax, step_time_us, n_table, budget, min_len, out_len,
+                           out_info, cuda_stream);
+}
+
+extern "C" int spec_schedule_verify_len_stale(const float *conf_stale, const float *conf, const int32_t *max_len,
+                                              int B, int Kmax, const float *step_time_us, int n_table,
+                                              int budget, int min_len, int32_t *out_len, double *out_info,
+                                              void *cuda_stream) {
+    if (B > 0 && Kmax > 0 && (!conf || !conf_stale)) return SPEC_EINVAL;
+    return launch_schedule(conf_stale, conf, max_len, B, Kmax, step_time_us, n_table, budget, min_len, out_len,
+                           out_info, cuda_stream);
+}
+
+extern "C" int spec_schedule_threshold(const float *conf, const int32_t *max_len, int B, int Kmax,
+                                       float threshold, int32_t *out_len, void *cuda_stream) {
+    if (B < 0 || Kmax < 0 || threshold != threshold) return SPEC_EINVAL;
+    if (B == 0) return SPEC_OK;
+    if (!out_len || (Kmax > 0 && !conf)) return SPEC_EINVAL;
+    if (B > SPEC_MAX_BATCH) return SPEC_EUNSUPPORTED;
+    threshold_kernel<<<(B + 255) / 256, 256, 0, (cudaStream_t)cuda_stream>>>(conf, max_len, B, Kmax, threshold,
+                                                                           out_len);
+    const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
