@@ -135,6 +135,35 @@ int spec_verify_sample(const void *target, const void *draft, int dtype, int B, 
                        size_t ws_bytes, void *cuda_stream);
 
 /*
+ * Flattened ragged layout ("DSpark paper review", Sec. 4, production results: to
+ * verify a different number of tokens per request in one batch, the engine
+ * flattens every token and tracks each one's request).  The same computation as
+ * spec_verify_greedy / spec_verify_sample, with no padding rows.  Request b's k_b
+ * draft positions are cu_draft[b] .. cu_draft[b+1] - 1 (k_b = cu_draft[b+1] -
+ * cu_draft[b]), and:
+ *  draft row i       at row cu_draft[b] + i of draft (ld_row elements a row);
+ *  target row i      at row cu_draft[b] + b + i of target, i = 0 .. k_b (k_b + 1 rows);
+ *  draft token x_i   draft_tokens[cu_draft[b] + i];
+ *  out_tokens        k_b + 1 slots from cu_draft[b] + b (accepted drafts, then the
+ *                    correction or bonus token, then -1);
+ *  out_p / out_q     k_b entries from cu_draft[b];
+ *  out_accepted, out_status  [B] as before.
+ * Kmax is the caller's bound on every k_b: it sizes the workspace
+ * (spec_verify_workspace_size(B, Kmax, V, dtype)), and a request with k_b outside
+ * [0, Kmax] reports status 2.  cu_draft need not start at 0.  The arrays must hold
+ * the rows and slots the offsets name; the library cannot check their sizes.
+ */
+int spec_verify_greedy_flat(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                            const int32_t *cu_draft, const int32_t *draft_tokens, int32_t *out_tokens,
+                            int32_t *out_accepted, int32_t *out_status, void *ws, size_t ws_bytes,
+                            void *cuda_stream);
+int spec_verify_sample_flat(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                            int64_t ld_row, const int32_t *cu_draft, const int32_t *draft_tokens,
+                            const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+                            int32_t *out_accepted, float *out_p, float *out_q, int32_t *out_status, void *ws,
+                            size_t ws_bytes, void *cuda_stream);
+
+/*
  * spec_verify_sample without a workspace argument.  The method on the pages has no
  * counterpart to this entry point: it exists for callers that cannot hand over
  * device memory per call.  Examples are a C host program with no device allocator

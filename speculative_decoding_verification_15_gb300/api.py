@@ -76,6 +76,42 @@ def schedule_verify_len(conf, step_time_us, budget: int, min_len: int, max_len=N
     return out_len, info
 
 
+def verify_sample_flat(target, draft, cu_draft, draft_tokens, temperature, seed: int, step: int, Kmax: int,
+                       stream=None) -> dict:
+    """Flattened ragged layout (no padding rows): target [sum_b (k_b + 1), V], draft
+    [sum_b k_b, V], cu_draft [B + 1] offsets of the draft positions, draft_tokens
+    [sum_b k_b]; Kmax bounds every k_b.  Outputs are flattened the same way."""
+    dev = target.device
+    cu = _as_i32(cu_draft, dev)
+    B = cu.numel() - 1
+    n_tok = target.shape[0]
+    out = dict(tokens=torch.empty(n_tok, dtype=torch.int32, device=dev),
+               accepted=torch.empty(B, dtype=torch.int32, device=dev),
+               p=torch.empty(draft.shape[0], dtype=torch.float32, device=dev),
+               q=torch.empty(draft.shape[0], dtype=torch.float32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    ws = workspace(dev, binding.spec_verify_workspace_size(B, Kmax, target.shape[1], binding._dtype_code(target)))
+    binding.spec_verify_sample_flat(target, draft, cu, _as_i32(draft_tokens, dev),
+                                    temperature.to(device=dev, dtype=torch.float32).contiguous(), seed, step,
+                                    out["tokens"], out["accepted"], out["p"], out["q"], out["status"], ws, Kmax,
+                                    stream)
+    return out
+
+
+def verify_greedy_flat(target, cu_draft, draft_tokens, Kmax: int, stream=None) -> dict:
+    """Greedy verify in the flattened ragged layout (see verify_sample_flat)."""
+    dev = target.device
+    cu = _as_i32(cu_draft, dev)
+    B = cu.numel() - 1
+    out = dict(tokens=torch.empty(target.shape[0], dtype=torch.int32, device=dev),
+               accepted=torch.empty(B, dtype=torch.int32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    ws = workspace(dev, binding.spec_verify_workspace_size(B, Kmax, target.shape[1], binding._dtype_code(target)))
+    binding.spec_verify_greedy_flat(target, cu, _as_i32(draft_tokens, dev), out["tokens"], out["accepted"],
+                                    out["status"], ws, Kmax, stream)
+    return out
+
+
 def schedule_verify_len_stale(conf_stale, conf, step_time_us, budget: int, min_len: int, max_len=None,
                               stream=None):
     dev = conf.device

@@ -59,6 +59,11 @@ def load(path: str | None = None):
         lib.spec_verify_sample.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P, P, P,
                                            P, SZ, P]
         lib.spec_verify_sample.restype = I32
+        lib.spec_verify_greedy_flat.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, P, P, P, SZ, P]
+        lib.spec_verify_greedy_flat.restype = I32
+        lib.spec_verify_sample_flat.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P, P, P,
+                                                P, SZ, P]
+        lib.spec_verify_sample_flat.restype = I32
         lib.spec_verify_sample_noalloc.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P,
                                                    P, P, P]
         lib.spec_verify_sample_noalloc.restype = I32
@@ -229,6 +234,62 @@ def spec_verify_sample_noalloc(target, draft, draft_tokens, num_draft, temperatu
                                         _stream_handle(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_verify_sample_noalloc", rc, lib)
+
+
+def _flat_rows(t: torch.Tensor, name: str):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be [rows, V] with V contiguous")
+    return t.shape[1], t.stride(0)
+
+
+def spec_verify_greedy_flat(target, cu_draft, draft_tokens, out_tokens, out_accepted, out_status, workspace,
+                            Kmax: int, stream=None) -> None:
+    """Flattened layout: target [sum_b (k_b + 1), V]; cu_draft [B + 1] int32 offsets of the
+    draft positions; draft_tokens [sum_b k_b] int32; out_tokens [sum_b (k_b + 1)]."""
+    lib = load()
+    dev = target.device
+    V, ld = _flat_rows(target, "target")
+    B = cu_draft.numel() - 1
+    _need(cu_draft, "cu_draft", torch.int32, None, dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, None, dev)
+    _need(out_tokens, "out_tokens", torch.int32, None, dev)
+    _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    rc = lib.spec_verify_greedy_flat(_ptr(target), _dtype_code(target), B, int(Kmax), V, ld, _ptr(cu_draft),
+                                     _ptr(draft_tokens), _ptr(out_tokens), _ptr(out_accepted), _ptr(out_status),
+                                     _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_greedy_flat", rc, lib)
+
+
+def spec_verify_sample_flat(target, draft, cu_draft, draft_tokens, temperature, seed: int, step: int, out_tokens,
+                            out_accepted, out_p, out_q, out_status, workspace, Kmax: int, stream=None) -> None:
+    """Flattened layout; draft [sum_b k_b, V]; out_p / out_q [sum_b k_b] or None."""
+    lib = load()
+    dev = target.device
+    V, ld = _flat_rows(target, "target")
+    Vd, ldd = _flat_rows(draft, "draft")
+    if Vd != V or ldd != ld or draft.dtype != target.dtype:
+        raise ValueError("draft must match target in V, row stride and dtype")
+    B = cu_draft.numel() - 1
+    _need(cu_draft, "cu_draft", torch.int32, None, dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, None, dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, None, dev)
+    _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    for t, n in ((out_p, "out_p"), (out_q, "out_q")):
+        if t is not None:
+            _need(t, n, torch.float32, None, dev)
+    _need(workspace, "workspace", torch.uint8, None, dev)
+    rc = lib.spec_verify_sample_flat(_ptr(target), _ptr(draft), _dtype_code(target), B, int(Kmax), V, ld,
+                                     _ptr(cu_draft), _ptr(draft_tokens), _ptr(temperature),
+                                     int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_tokens),
+                                     _ptr(out_accepted), _ptr(out_p), _ptr(out_q), _ptr(out_status),
+                                     _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_sample_flat", rc, lib)
 
 
 def spec_schedule_verify_len(conf, max_len, step_time_us, budget: int, min_len: int, out_len, out_info=None,

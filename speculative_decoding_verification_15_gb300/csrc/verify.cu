@@ -190,9 +190,39 @@ __device__ __forceinline__ float chunk_expsum(const Vec (&d)[kVPT], float c, flo
 }
 
 // ------------------------------------------------------------------ per-request rows
-__device__ __forceinline__ int request_main_rows(const int32_t *num_draft, const float *temperature, int Kmax,
-                                                 int b) {
-    const int kb = num_draft ? num_draft[b] : Kmax;
+// Where request b lives.  Padded layout (cu NULL): draft positions b Kmax + i,
+// target rows b (Kmax + 1) + i, k_b = num_draft[b] (NULL: Kmax).  Flattened
+// layout: draft positions cu[b] + i, target rows (and output token slots)
+// cu[b] + b + i, k_b = cu[b + 1] - cu[b].
+struct ReqBase {
+    int kb;         // k_b, unchecked
+    int64_t d0;     // first draft position: draft row, draft token and p/q index
+    int64_t t0;     // first target row and first output token slot
+    int ntok, npq;  // output token slots and p/q slots of the request
+};
+
+__device__ __forceinline__ ReqBase req_base(const int32_t *cu, const int32_t *num_draft, int Kmax, int b) {
+    ReqBase r;
+    if (cu) {
+        const int c0 = cu[b];
+        r.kb = cu[b + 1] - c0;
+        r.d0 = c0;
+        r.t0 = (int64_t)c0 + b;
+        r.ntok = r.kb + 1 > 0 ? r.kb + 1 : 0;
+        r.npq = r.kb > 0 ? r.kb : 0;
+    } else {
+        r.kb = num_draft ? num_draft[b] : Kmax;
+        r.d0 = (int64_t)b * Kmax;
+        r.t0 = (int64_t)b * (Kmax + 1);
+        r.ntok = Kmax + 1;
+        r.npq = Kmax;
+    }
+    return r;
+}
+
+__device__ __forceinline__ int request_main_rows(const int32_t *cu, const int32_t *num_draft,
+                                                 const float *temperature, int Kmax, int b) {
+    const int kb = req_base(cu, num_draft, Kmax, b).kb;
     if (kb < 0 || kb > Kmax) return 0;
     if (temperature) {
         const float T = temperature[b];
@@ -205,13 +235,14 @@ __device__ __forceinline__ int request_main_rows(const int32_t *num_draft, const
 // s[b] = main-pass rows of requests 0..b-1 (s[B] = total), in shared memory.
 // Row order inside a request: sampling [target 0..k-1 | draft 0..k-1], greedy
 // [target 0..k-1].
-__device__ void scan_request_rows(int *s, int B, const int32_t *num_draft, const float *temperature, int Kmax) {
+__device__ void scan_request_rows(int *s, int B, const int32_t *cu, const int32_t *num_draft,
+                                  const float *temperature, int Kmax) {
     __shared__ int warp_tot[32];
     const int nthr = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int per = (B + nthr - 1) / nthr;
     const int lo = min(tid * per, B), hi = min(lo + per, B);
     int local = 0;
-    for (int i = lo; i < hi; ++i) local += request_main_rows(num_draft, temperature, Kmax, i);
+    for (int i = lo; i < hi; ++i) local += request_main_rows(cu, num_draft, temperature, Kmax, i);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -225,7 +256,7 @@ __device__ void scan_request_rows(int *s, int B, const int32_t *num_draft, const
     int run = wbase + incl - local;
     for (int i = lo; i < hi; ++i) {
         s[i] = run;
-        run += request_main_rows(num_draft, temperature, Kmax, i);
+        run += request_main_rows(cu, num_draft, temperature, Kmax, i);
     }
     if (tid == nthr - 1) s[B] = wbase + incl;
     __syncthreads();
@@ -246,6 +277,7 @@ struct MainParams {
     const void *draft;
     int64_t ld_row;
     int B, Kmax, V;
+    const int32_t *cu;         // flattened layout offsets [B+1], or NULL (padded)
     const int32_t *num_draft;
     const float *temperature;  // NULL: every request greedy
     int *row_start;            // [B+1], written by block 0 for commit_kernel
@@ -262,14 +294,14 @@ template <class Vec>
 __device__ __forceinline__ MainRow main_row(const MainParams &p, const int *rs, int r) {
     const int b = find_request(rs, p.B, r);
     const int local = r - rs[b];
-    const int kb = p.num_draft ? p.num_draft[b] : p.Kmax;
+    const ReqBase rb = req_base(p.cu, p.num_draft, p.Kmax, b);
     const float T = p.temperature ? p.temperature[b] : 0.f;
     const int64_t rowbytes = p.ld_row * Vec::ESIZE;
     MainRow m;
-    if (T == 0.f || local < kb) {
-        m.ptr = (const char *)p.target + ((int64_t)b * (p.Kmax + 1) + local) * rowbytes;
+    if (T == 0.f || local < rb.kb) {
+        m.ptr = (const char *)p.target + (rb.t0 + local) * rowbytes;
     } else {
-        m.ptr = (const char *)p.draft + ((int64_t)b * p.Kmax + (local - kb)) * rowbytes;
+        m.ptr = (const char *)p.draft + (rb.d0 + (local - rb.kb)) * rowbytes;
     }
     m.c = T == 0.f ? 0.f : __fdiv_rn(kLog2e, T);
     return m;
@@ -285,7 +317,7 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
     extern __shared__ __align__(128) unsigned char smem[];
     int *s_rs = (int *)smem;
     MainRow *s_desc = (MainRow *)(smem + sizeof(int) * (size_t)(((p.B + 1) + 3) & ~3));
-    scan_request_rows(s_rs, p.B, p.num_draft, p.temperature, p.Kmax);  // ends with __syncthreads
+    scan_request_rows(s_rs, p.B, p.cu, p.num_draft, p.temperature, p.Kmax);  // ends with __syncthreads
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.row_start[i] = s_rs[i];
     pdl_launch_dependents();
@@ -427,6 +459,7 @@ struct CommitParams {
     int64_t ld_row;
     int B, Kmax, V;
     const int32_t *draft_tokens;
+    const int32_t *cu;         // flattened layout offsets [B+1], or NULL (padded)
     const int32_t *num_draft;
     const float *temperature;  // NULL: every request greedy
     uint64_t seed;
@@ -801,7 +834,8 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     }
 
     // ---- inputs only: this part overlaps the end of main_kernel
-    const int kb_raw = p.num_draft ? p.num_draft[b] : p.Kmax;
+    const ReqBase rbase = req_base(p.cu, p.num_draft, p.Kmax, b);
+    const int kb_raw = rbase.kb;
     int status = SPEC_STATUS_OK;
     float T = 0.f;
     if (kb_raw < 0 || kb_raw > p.Kmax) status = SPEC_STATUS_BAD_K;
@@ -811,7 +845,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     }
     const int kb = status == SPEC_STATUS_BAD_K ? 0 : kb_raw;
     const bool greedy = (T == 0.f);
-    const int32_t *x = p.draft_tokens + (int64_t)b * p.Kmax;
+    const int32_t *x = p.draft_tokens + rbase.d0;
     if (status == SPEC_STATUS_OK) {
         bool bad = false;
         for (int i = tid; i < kb; i += kCommitThreads) bad |= (x[i] < 0 || x[i] >= p.V);
@@ -823,8 +857,8 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     if (!greedy) {
         for (int i = tid; i < npos; i += kCommitThreads) {
             const int xi = x[i];
-            s_xt[i] = load_logit(p.target, p.dtype, ((int64_t)b * (p.Kmax + 1) + i) * p.ld_row + xi);
-            s_xd[i] = load_logit(p.draft, p.dtype, ((int64_t)b * p.Kmax + i) * p.ld_row + xi);
+            s_xt[i] = load_logit(p.target, p.dtype, (rbase.t0 + i) * p.ld_row + xi);
+            s_xd[i] = load_logit(p.draft, p.dtype, (rbase.d0 + i) * p.ld_row + xi);
             const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
             s_l2u[i] = log2f(u01(r4.x));
         }
@@ -835,7 +869,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     if (p.B <= kLocalScanMax) {
         int before = 0, all = 0;
         for (int bb = tid; bb < p.B; bb += kCommitThreads) {
-            const int n = request_main_rows(p.num_draft, p.temperature, p.Kmax, bb);
+            const int n = request_main_rows(p.cu, p.num_draft, p.temperature, p.Kmax, bb);
             all += n;
             if (bb < b) before += n;
         }
@@ -879,7 +913,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
         const RowSpan st = s_span[i];
         const RowSpan sd = greedy ? st : s_span[p.Kmax + i];
         const bool fast = st.n() <= 64 && sd.n() <= 64;  // at most two partials per lane and row
-        const char *drow = (const char *)p.draft + ((int64_t)b * p.Kmax + i) * p.ld_row * ESZ;
+        const char *drow = (const char *)p.draft + (rbase.d0 + i) * p.ld_row * ESZ;
         Part pt[2] = {}, pd[2] = {};  // this lane's target partials: correction candidates
         bool okt[2] = {false, false}, okd[2] = {false, false};
         float dv[2] = {0.f, 0.f};  // draft logits at the candidates, fetched before they are known to be needed
@@ -1037,7 +1071,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
             }
         }
         if (jd.kind != JOB_NONE)
-            issue_round((const char *)p.target + ((int64_t)b * (p.Kmax + 1) + jd.row) * rowbytes, 0);
+            issue_round((const char *)p.target + (rbase.t0 + jd.row) * rowbytes, 0);
         if (lane == 0) {
             s_job = jd;
             s_sum[0] = st;
@@ -1050,9 +1084,8 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     // ---- this CTA's units of the job row (unit rank + C k in slot k of its round).
     // A round's units are cut into blocks of kBlockGroups groups, dealt to the warps
     // round-robin, so every warp gets a mix of the units.
-    const char *jrow = (const char *)p.target + ((int64_t)b * (p.Kmax + 1) + jd.row) * rowbytes;
-    const char *drow =
-        jd.kind == JOB_RESID ? (const char *)p.draft + ((int64_t)b * p.Kmax + jd.row) * rowbytes : nullptr;
+    const char *jrow = (const char *)p.target + (rbase.t0 + jd.row) * rowbytes;
+    const char *drow = jd.kind == JOB_RESID ? (const char *)p.draft + (rbase.d0 + jd.row) * rowbytes : nullptr;
     const int nrounds = jd.kind == JOB_NONE ? 0 : kUnitsPerCTA / p.NS;
     const int bpu = (((p.ue + 3) >> 2) + kBlockGroups - 1) / kBlockGroups;  // blocks per full unit
     SliceRes mine;
@@ -1174,7 +1207,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
         token = o.idx;
         if (status == SPEC_STATUS_OK && jd.kind == JOB_RESID && o.idx < 0) {
             // p <= q everywhere (only by rounding): draw from p_j with the same noise
-            const int64_t trow = ((int64_t)b * (p.Kmax + 1) + jd.row) * p.ld_row;
+            const int64_t trow = (rbase.t0 + jd.row) * p.ld_row;
             SliceRes f;
             f.best = kNegInf;
             f.idx = -1;
@@ -1195,14 +1228,14 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     // ---- outputs of request b
     const bool ok = status == SPEC_STATUS_OK;
     const int A = ok ? jd.A : 0;
-    const int K1 = p.Kmax + 1;
-    int32_t *tok = p.out_tokens + (int64_t)b * K1;
-    for (int i = tid; i < K1; i += kCommitThreads) tok[i] = !ok ? -1 : (i < A ? x[i] : (i == A ? token : -1));
+    int32_t *tok = p.out_tokens + rbase.t0;
+    for (int i = tid; i < rbase.ntok; i += kCommitThreads)
+        tok[i] = !ok ? -1 : (i < A ? x[i] : (i == A ? token : -1));
     const bool pq = ok && !greedy;
     if (p.out_p)
-        for (int i = tid; i < p.Kmax; i += kCommitThreads) p.out_p[(int64_t)b * p.Kmax + i] = pq && i < kb ? s_pp[i] : -1.f;
+        for (int i = tid; i < rbase.npq; i += kCommitThreads) p.out_p[rbase.d0 + i] = pq && i < kb ? s_pp[i] : -1.f;
     if (p.out_q)
-        for (int i = tid; i < p.Kmax; i += kCommitThreads) p.out_q[(int64_t)b * p.Kmax + i] = pq && i < kb ? s_qq[i] : -1.f;
+        for (int i = tid; i < rbase.npq; i += kCommitThreads) p.out_q[rbase.d0 + i] = pq && i < kb ? s_qq[i] : -1.f;
     if (tid == 0) {
         p.out_status[b] = status;
         p.out_accepted[b] = A;
@@ -1367,7 +1400,7 @@ int launch_all(int dev, const Layout &L, const MainParams &mp, const CommitParam
 }
 
 int verify_impl(const void *target, const void *draft, int dtype, int B, int Kmax, int V, int64_t ld_row,
-                const int32_t *draft_tokens, const int32_t *num_draft, const float *temperature,
+                const int32_t *draft_tokens, const int32_t *cu, const int32_t *num_draft, const float *temperature,
                 uint64_t seed, uint64_t step, int32_t *out_tokens, int32_t *out_accepted, float *out_p,
                 float *out_q, int32_t *out_status, void *ws, size_t ws_bytes, void *cuda_stream,
                 bool sample) {
@@ -1404,6 +1437,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     mp.B = B;
     mp.Kmax = Kmax;
     mp.V = V;
+    mp.cu = cu;
     mp.num_draft = num_draft;
     mp.temperature = temps;
     mp.row_start = (int *)(w + L.off_row_start);
@@ -1419,6 +1453,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     cp.Kmax = Kmax;
     cp.V = V;
     cp.draft_tokens = draft_tokens;
+    cp.cu = cu;
     cp.num_draft = num_draft;
     cp.temperature = temps;
     cp.seed = seed;
@@ -1476,7 +1511,7 @@ int spec_verify_greedy(const void *target, int dtype, int B, int Kmax, int V, in
                        const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
                        int32_t *out_accepted, int32_t *out_status, void *ws, size_t ws_bytes,
                        void *cuda_stream) {
-    return verify_impl(target, nullptr, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, nullptr, 0, 0,
+    return verify_impl(target, nullptr, dtype, B, Kmax, V, ld_row, draft_tokens, nullptr, num_draft, nullptr, 0, 0,
                        out_tokens, out_accepted, nullptr, nullptr, out_status, ws, ws_bytes, cuda_stream,
                        false);
 }
@@ -1486,7 +1521,7 @@ int spec_verify_sample(const void *target, const void *draft, int dtype, int B, 
                        const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
                        int32_t *out_accepted, float *out_p, float *out_q, int32_t *out_status, void *ws,
                        size_t ws_bytes, void *cuda_stream) {
-    return verify_impl(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, temperature, seed,
+    return verify_impl(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, nullptr, num_draft, temperature, seed,
                        step, out_tokens, out_accepted, out_p, out_q, out_status, ws, ws_bytes, cuda_stream,
                        true);
 }
@@ -1507,9 +1542,29 @@ int spec_verify_sample_noalloc(const void *target, const void *draft, int dtype,
         return SPEC_ESCRATCH;
     void *ws = nullptr;
     if ((rc = static_scratch(dev, &ws))) return rc;
-    return verify_impl(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, temperature, seed,
+    return verify_impl(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, nullptr, num_draft, temperature, seed,
                        step, out_tokens, out_accepted, out_p, out_q, out_status, ws, SPEC_STATIC_SCRATCH_BYTES,
                        cuda_stream, true);
+}
+
+int spec_verify_greedy_flat(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                            const int32_t *cu_draft, const int32_t *draft_tokens, int32_t *out_tokens,
+                            int32_t *out_accepted, int32_t *out_status, void *ws, size_t ws_bytes,
+                            void *cuda_stream) {
+    if (B > 0 && !cu_draft) return SPEC_EINVAL;
+    return verify_impl(target, nullptr, dtype, B, Kmax, V, ld_row, draft_tokens, cu_draft, nullptr, nullptr, 0, 0,
+                       out_tokens, out_accepted, nullptr, nullptr, out_status, ws, ws_bytes, cuda_stream, false);
+}
+
+int spec_verify_sample_flat(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                            int64_t ld_row, const int32_t *cu_draft, const int32_t *draft_tokens,
+                            const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+                            int32_t *out_accepted, float *out_p, float *out_q, int32_t *out_status, void *ws,
+                            size_t ws_bytes, void *cuda_stream) {
+    if (B > 0 && !cu_draft) return SPEC_EINVAL;
+    return verify_impl(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, cu_draft, nullptr, temperature,
+                       seed, step, out_tokens, out_accepted, out_p, out_q, out_status, ws, ws_bytes, cuda_stream,
+                       true);
 }
 
 const char *spec_error_string(int err) {
