@@ -292,6 +292,22 @@ def run_ours(args) -> None:
     rows_ms = statistics.mean(k[0] for k in kern_ms)
     per_kernel = [statistics.mean(k[j] for k in kern_ms) for j in range(len(kern_ms[0]))]
 
+    # Early exit on the same workload, timed the same way and reported beside the
+    # headline: one kernel, each request's rows read in position order up to its
+    # first rejection.
+    ee_ms = []
+    for i in range(args.warmup + args.steps):
+        flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        binding.spec_verify_sample_early_exit(t, d, x, None, T, 3, i, tokens, acc, pp, qq, st, stream)
+        e1.record(stream)
+        ee_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    ee_ms = [a.elapsed_time(b) for a, b in ee_ms[args.warmup:]]
+    assert int((st != 0).sum()) == 0, "a request reported a non-zero status (early exit)"
+    ee_rows = int((2 * torch.clamp(acc + 1, max=K) + (acc == K).to(torch.int32)).sum().item())
+
     # end to end: pinned host inputs -> device, verify, outputs -> host, every step
     th, dh = t.cpu().pin_memory(), d.cpu().pin_memory()
     xh, Th = x.cpu().pin_memory(), T.cpu().pin_memory()
@@ -342,6 +358,9 @@ def run_ours(args) -> None:
             "step_algorithmic_bytes": algo_bytes,
             "e2e": {"value": world * verified / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "early_exit": {"ms_per_step": statistics.mean(ee_ms),
+                           "value": world * verified / (statistics.mean(ee_ms) * 1e-3), "unit": UNIT,
+                           "rows_read_per_step": ee_rows, "rows_full_scan": B * (2 * K + 1)},
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -164,6 +164,31 @@ int spec_verify_sample_flat(const void *target, const void *draft, int dtype, in
                             size_t ws_bytes, void *cuda_stream);
 
 /*
+ * Early-exit verify ("Accelerating Large-Model Inference ... DSpark", Sec. 1: only
+ * the longest accepted prefix and one more token are committed, so no row after
+ * the first rejected position is needed; "From draft-then-verify to DSpark": the
+ * rejection test at each position in turn).  Same arguments, layout and results
+ * as spec_verify_sample / spec_verify_greedy (padded layout), except that:
+ *  - the rows are read in position order and reading stops at the first rejection
+ *    (sampling) or mismatch (greedy); target row k_b only when every draft passes;
+ *  - status 4 (non-finite) covers only the rows read, so a request whose bad row
+ *    lies after its first rejection reports status 0;
+ *  - out_p / out_q hold p_i(x_i), q_i(x_i) up to and including the first rejected
+ *    position and -1 after it.
+ * Tokens and accepted counts equal spec_verify_sample's whenever every row read
+ * is finite.  One kernel, one cluster of CTAs per request walking its positions;
+ * no workspace.
+ */
+int spec_verify_sample_early_exit(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                                  int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                                  const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+                                  int32_t *out_accepted, float *out_p, float *out_q, int32_t *out_status,
+                                  void *cuda_stream);
+int spec_verify_greedy_early_exit(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                                  const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
+                                  int32_t *out_accepted, int32_t *out_status, void *cuda_stream);
+
+/*
  * spec_verify_sample without a workspace argument.  The method on the pages has no
  * counterpart to this entry point: it exists for callers that cannot hand over
  * device memory per call.  Examples are a C host program with no device allocator
@@ -258,8 +283,8 @@ int spec_last_cuda_error(void);
  * the last call's events and writes up to n durations in milliseconds, in launch
  * order (the main pass over the draft positions' rows, then the commit pass that
  * combines them, runs the acceptance scan and draws the extra token; greedy and
- * sampling calls launch the same two), returning how many were written (negative
- * spec_err on failure).
+ * sampling calls launch the same two; the early-exit calls launch one), returning
+ * how many were written (negative spec_err on failure).
  */
 int spec_profile_enable(int on);
 int spec_profile_read(float *ms, int n);

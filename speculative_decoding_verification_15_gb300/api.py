@@ -76,6 +76,36 @@ def schedule_verify_len(conf, step_time_us, budget: int, min_len: int, max_len=N
     return out_len, info
 
 
+def verify_sample_early_exit(target, draft, draft_tokens, temperature, seed: int, step: int, num_draft=None,
+                             stream=None) -> dict:
+    """Sampling verify that stops reading at each request's first rejection."""
+    dev = target.device
+    B, K1, V = target.shape
+    K = K1 - 1
+    out = dict(tokens=torch.empty((B, K1), dtype=torch.int32, device=dev),
+               accepted=torch.empty(B, dtype=torch.int32, device=dev),
+               p=torch.empty((B, K), dtype=torch.float32, device=dev),
+               q=torch.empty((B, K), dtype=torch.float32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    binding.spec_verify_sample_early_exit(target, draft, _as_i32(draft_tokens, dev), _as_i32(num_draft, dev),
+                                          temperature.to(device=dev, dtype=torch.float32).contiguous(), seed, step,
+                                          out["tokens"], out["accepted"], out["p"], out["q"], out["status"],
+                                          stream)
+    return out
+
+
+def verify_greedy_early_exit(target, draft_tokens, num_draft=None, stream=None) -> dict:
+    """Greedy verify that stops reading at each request's first mismatch."""
+    dev = target.device
+    B, K1, V = target.shape
+    out = dict(tokens=torch.empty((B, K1), dtype=torch.int32, device=dev),
+               accepted=torch.empty(B, dtype=torch.int32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    binding.spec_verify_greedy_early_exit(target, _as_i32(draft_tokens, dev), _as_i32(num_draft, dev),
+                                          out["tokens"], out["accepted"], out["status"], stream)
+    return out
+
+
 def verify_sample_flat(target, draft, cu_draft, draft_tokens, temperature, seed: int, step: int, Kmax: int,
                        stream=None) -> dict:
     """Flattened ragged layout (no padding rows): target [sum_b (k_b + 1), V], draft

@@ -64,6 +64,11 @@ def load(path: str | None = None):
         lib.spec_verify_sample_flat.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P, P, P,
                                                 P, SZ, P]
         lib.spec_verify_sample_flat.restype = I32
+        lib.spec_verify_sample_early_exit.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P,
+                                                      P, P, P]
+        lib.spec_verify_sample_early_exit.restype = I32
+        lib.spec_verify_greedy_early_exit.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, P, P, P]
+        lib.spec_verify_greedy_early_exit.restype = I32
         lib.spec_verify_sample_noalloc.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P,
                                                    P, P, P]
         lib.spec_verify_sample_noalloc.restype = I32
@@ -201,6 +206,60 @@ def spec_verify_sample(target, draft, draft_tokens, num_draft, temperature, seed
                                 _ptr(workspace), workspace.numel(), _stream_handle(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_verify_sample", rc, lib)
+
+
+def spec_verify_sample_early_exit(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int,
+                                  out_tokens, out_accepted, out_p, out_q, out_status, stream=None) -> None:
+    """spec_verify_sample that reads rows in position order and stops at the first
+    rejection (no workspace); tensors as for spec_verify_sample."""
+    lib = load()
+    K1 = target.shape[1]
+    Kmax = K1 - 1
+    B, V, ld = _logits_layout(target, K1)
+    dev = target.device
+    if draft.dtype != target.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    if Kmax > 0:
+        Bd, Vd, ldd = _logits_layout(draft, Kmax)
+        if (Bd, Vd, ldd) != (B, V, ld):
+            raise ValueError("draft logits must be [B, Kmax, V] with the target's row stride")
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, Kmax), dev)
+    if num_draft is not None:
+        _need(num_draft, "num_draft", torch.int32, (B,), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K1), dev)
+    _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
+    for t, n in ((out_p, "out_p"), (out_q, "out_q")):
+        if t is not None:
+            _need(t, n, torch.float32, (B, Kmax), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    rc = lib.spec_verify_sample_early_exit(_ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
+                                           _ptr(draft_tokens), _ptr(num_draft), _ptr(temperature),
+                                           int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_tokens),
+                                           _ptr(out_accepted), _ptr(out_p), _ptr(out_q), _ptr(out_status),
+                                           _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_sample_early_exit", rc, lib)
+
+
+def spec_verify_greedy_early_exit(target, draft_tokens, num_draft, out_tokens, out_accepted, out_status,
+                                  stream=None) -> None:
+    lib = load()
+    K1 = target.shape[1]
+    Kmax = K1 - 1
+    B, V, ld = _logits_layout(target, K1)
+    dev = target.device
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, Kmax), dev)
+    if num_draft is not None:
+        _need(num_draft, "num_draft", torch.int32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K1), dev)
+    _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    rc = lib.spec_verify_greedy_early_exit(_ptr(target), _dtype_code(target), B, Kmax, V, ld, _ptr(draft_tokens),
+                                           _ptr(num_draft), _ptr(out_tokens), _ptr(out_accepted),
+                                           _ptr(out_status), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_verify_greedy_early_exit", rc, lib)
 
 
 def spec_verify_sample_noalloc(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int,

@@ -29,6 +29,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "spec_common.cuh"
 #include "spec_verify.h"
@@ -801,6 +802,147 @@ __host__ __device__ inline size_t commit_smem_bytes(int NS, int slot, int Kmax, 
            5 * sizeof(float) * (size_t)Kmax + 2 * sizeof(int) * (size_t)(G + 1);
 }
 
+// Warp-collective (one whole warp): the unit views of round rd of this CTA's share
+// of the job row into uvs, then one bulk copy per lane k < NS into slot k, all on
+// one barrier phase.  Unit rank + C k lands in slot k of its round.
+template <int ESZ>
+__device__ __forceinline__ void issue_job_round(const CommitParams &p, uint32_t rank, const char *jrow, int rd,
+                                                unsigned char *buf, uint64_t *bar, UnitView *uvs) {
+    const int lane = threadIdx.x & 31;
+    const Chunking uk = {p.C * kUnitsPerCTA, p.ue};
+    const int nunits = (p.V + p.ue - 1) / p.ue;  // units holding entries
+    ChunkWin w;
+    w.bytes = 0;
+    const int u = (int)rank + p.C * (rd * p.NS + lane);
+    UnitView uv;
+    uv.slot = buf + (size_t)lane * p.slot;
+    uv.sbase = uv.e1 = uv.g0 = uv.g1 = 0;
+    uv.aligned = 0;
+    if (lane < p.NS && u < nunits) {
+        w = chunk_window(jrow, ESZ, p.V, uk, u);
+        uv.sbase = w.e0 - w.shift;
+        uv.e1 = w.e1;
+        uv.g0 = w.e0 >> 2;
+        uv.g1 = (w.e1 + 3) >> 2;
+        uv.aligned = (w.shift & 3) == 0;
+    }
+    if (lane < p.NS) uvs[lane] = uv;
+    const int bytes = warp_sum_i((int)w.bytes);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)bytes);
+    __syncwarp();
+    if (w.bytes) bulk_g2s(buf + (size_t)lane * p.slot, w.a0, w.bytes, bar);
+}
+
+// This CTA's share of the job row, round 0 already in flight: the pruned Gumbel-max
+// (correction or bonus) or the argmax, over the staged units.  A round's units are
+// cut into blocks of kBlockGroups groups, dealt to the warps round-robin, so every
+// warp gets a mix of the units.  Every thread of the CTA calls it; every thread
+// gets the CTA's result.
+template <int ESZ>
+__device__ SliceRes job_row_rounds(const CommitParams &p, const JobDesc &jd, uint32_t b, uint32_t rank,
+                                   const char *jrow, const char *drow, unsigned char *buf, uint64_t *bar,
+                                   UnitView *uvs, uint32_t (*live_g)[kLiveMax], float (*live_z)[kLiveMax],
+                                   SliceRes *red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nrounds = jd.kind == JOB_NONE ? 0 : kUnitsPerCTA / p.NS;
+    const int bpu = (((p.ue + 3) >> 2) + kBlockGroups - 1) / kBlockGroups;  // blocks per full unit
+    SliceRes mine;
+    mine.best = jd.seed;
+    mine.idx = jd.seed_idx;
+    mine.rawmax = kNegInf;
+    mine.failed = 0;
+    float thr = jd.seed;
+    uint32_t phase = 0;
+    for (int rd = 0; rd < nrounds; ++rd) {
+        // one thread waits, so that a CTA whose copies are in flight takes no issue
+        // slots from the CTAs sharing its SM; the others then take the completed
+        // phase themselves (it completes at once), which makes the bytes visible to them
+        bool ok = true;
+        if (tid == 0) ok = mbar_wait(bar, phase, kWaitNs);
+        if (__syncthreads_or(!ok)) {
+            // give up on this request; wait (bounded) for the copies in flight first
+            if (tid == 0) mbar_wait(bar, phase, kWaitNs);
+            mine.failed = 1;
+            break;
+        }
+        mbar_try_wait(bar, phase);
+        phase ^= 1u;
+        const int nblk = p.NS * bpu;
+        if (jd.kind == JOB_BONUS) {
+            // seed the bound with each thread's largest entry (exact score)
+            float m = kNegInf;
+            int mi = -1;
+            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
+                const UnitView uv = uvs[bi / bpu];
+                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+                for (int g = gb + lane; g < ge; g += 32) {
+                    float xv[4];
+                    group_vals<ESZ>(uv, g, xv);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (xv[q] > m) { m = xv[q]; mi = 4 * g + q; }
+                }
+            }
+            SliceRes seed;
+            seed.best = kNegInf;
+            seed.idx = -1;
+            seed.rawmax = kNegInf;
+            seed.failed = 0;
+            if (mi >= 0) {
+                const uint4 r4 = rand_group(p.seed, p.step, b, (uint32_t)jd.row, PURPOSE_BONUS,
+                                            (uint32_t)mi >> 2);
+                seed.best = fmaf(m, jd.invT, -jd.shift) + gumbel_of_word(word_of(r4, mi & 3));
+                seed.idx = mi;
+            }
+            seed = block_reduce(seed, red);
+            if (better(seed.best, seed.idx, mine.best, mine.idx)) { mine.best = seed.best; mine.idx = seed.idx; }
+            thr = fmaxf(thr, seed.best);
+        }
+        if (jd.kind == JOB_ARGMAX) {
+            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
+                const UnitView uv = uvs[bi / bpu];
+                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+                float m = kNegInf;
+                int mi = -1;
+                for (int g = gb + lane; g < ge; g += 32) {
+                    float xv[4];
+                    group_vals<ESZ>(uv, g, xv);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        mine.rawmax = max_nan_f32(mine.rawmax, xv[q]);
+                        if (xv[q] > m) { m = xv[q]; mi = 4 * g + q; }
+                    }
+                }
+                if (better(m, mi, mine.best, mine.idx)) { mine.best = m; mine.idx = mi; }
+            }
+        } else {
+            uint32_t *lg = live_g[warp];
+            float *lz = live_z[warp];
+            int nlive = 0;
+            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
+                const int k = bi / bpu;
+                const UnitView uv = uvs[k];
+                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+                if (gb >= ge) continue;
+                nlive = jd.kind == JOB_BONUS
+                            ? zfilter_block<ESZ, true>(uv, k, gb, ge, thr - kGumbelMax, jd.invT, jd.shift,
+                                                       mine.rawmax, lg, lz, nlive)
+                            : zfilter_block<ESZ, false>(uv, k, gb, ge, thr - kGumbelMax, jd.invT, jd.shift,
+                                                        mine.rawmax, lg, lz, nlive);
+                while (nlive >= 64) {  // draw the newest 64; the rest stay listed
+                    nlive -= 64;
+                    live_round<ESZ>(lg, lz, nlive, 64, uvs, jd, p, b, drow, thr, mine.best, mine.idx);
+                }
+            }
+            if (nlive > 0)
+                live_round<ESZ>(lg, lz, 0, nlive, uvs, jd, p, b, drow, thr, mine.best, mine.idx);
+        }
+        __syncthreads();  // every warp is done with the round's slots and views
+        if (warp == 0 && rd + 1 < nrounds) issue_job_round<ESZ>(p, rank, jrow, rd + 1, buf, bar, uvs);
+    }
+    return block_reduce(mine, red);
+}
+
 template <int ESZ>
 __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_kernel(CommitParams p) {
     extern __shared__ __align__(128) unsigned char cdyn[];
@@ -942,8 +1084,12 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
         }
         PosRes pr;
         pr.tidx = tr.idx;
+        // A NaN can leave a lane's running max finite again (a later chunk's max
+        // replaces it) but not its sum, so sampling rows check the sums too.
         pr.nonfinite = !(fabsf(tr.M) < __int_as_float(0x7f800000)) ||
-                       (!greedy && !(fabsf(dr.M) < __int_as_float(0x7f800000)));
+                       (!greedy && !(fabsf(dr.M) < __int_as_float(0x7f800000) &&
+                                     fabsf(tr.l2S) < __int_as_float(0x7f800000) &&
+                                     fabsf(dr.l2S) < __int_as_float(0x7f800000)));
         pr.shift = pr.Cd = 0.f;
         pr.seed = kNegInf;
         pr.seed_idx = -1;
@@ -1001,31 +1147,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     // ---- the scan (warp 0): A = first rejected position; it then starts the job
     // row's first round of copies
     const int64_t rowbytes = p.ld_row * ESZ;
-    const Chunking uk = {p.C * kUnitsPerCTA, p.ue};
-    const int nunits = (p.V + p.ue - 1) / p.ue;  // units holding entries
-    // warp 0: unit views of round rd into s_uv, then one copy per lane k < NS
-    auto issue_round = [&](const char *jrow, int rd) {
-        ChunkWin w;
-        w.bytes = 0;
-        const int u = (int)rank + p.C * (rd * p.NS + lane);
-        UnitView uv;
-        uv.slot = buf + (size_t)lane * p.slot;
-        uv.sbase = uv.e1 = uv.g0 = uv.g1 = 0;
-        uv.aligned = 0;
-        if (lane < p.NS && u < nunits) {
-            w = chunk_window(jrow, ESZ, p.V, uk, u);
-            uv.sbase = w.e0 - w.shift;
-            uv.e1 = w.e1;
-            uv.g0 = w.e0 >> 2;
-            uv.g1 = (w.e1 + 3) >> 2;
-            uv.aligned = (w.shift & 3) == 0;
-        }
-        if (lane < p.NS) s_uv[lane] = uv;
-        const int bytes = warp_sum_i((int)w.bytes);
-        if (lane == 0) mbar_arrive_expect_tx(&s_bar, (uint32_t)bytes);
-        __syncwarp();
-        if (w.bytes) bulk_g2s(buf + (size_t)lane * p.slot, w.a0, w.bytes, &s_bar);
-    };
+    auto issue_round = [&](const char *jrow, int rd) { issue_job_round<ESZ>(p, rank, jrow, rd, buf, &s_bar, s_uv); };
     if (warp == 0) {
         JobDesc jd;
         jd.kind = JOB_NONE;
@@ -1081,108 +1203,11 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     const JobDesc jd = s_job;
     status = s_sum[0];
 
-    // ---- this CTA's units of the job row (unit rank + C k in slot k of its round).
-    // A round's units are cut into blocks of kBlockGroups groups, dealt to the warps
-    // round-robin, so every warp gets a mix of the units.
+    // ---- this CTA's units of the job row (round 0 is in flight)
     const char *jrow = (const char *)p.target + (rbase.t0 + jd.row) * rowbytes;
     const char *drow = jd.kind == JOB_RESID ? (const char *)p.draft + (rbase.d0 + jd.row) * rowbytes : nullptr;
-    const int nrounds = jd.kind == JOB_NONE ? 0 : kUnitsPerCTA / p.NS;
-    const int bpu = (((p.ue + 3) >> 2) + kBlockGroups - 1) / kBlockGroups;  // blocks per full unit
-    SliceRes mine;
-    mine.best = jd.seed;
-    mine.idx = jd.seed_idx;
-    mine.rawmax = kNegInf;
-    mine.failed = 0;
-    float thr = jd.seed;
-    uint32_t phase = 0;
-    for (int rd = 0; rd < nrounds; ++rd) {
-        // one thread waits, so that a CTA whose copies are in flight takes no issue
-        // slots from the CTAs sharing its SM; the others then take the completed
-        // phase themselves (it completes at once), which makes the bytes visible to them
-        bool ok = true;
-        if (tid == 0) ok = mbar_wait(&s_bar, phase, kWaitNs);
-        if (__syncthreads_or(!ok)) {
-            // give up on this request; wait (bounded) for the copies in flight first
-            if (tid == 0) mbar_wait(&s_bar, phase, kWaitNs);
-            mine.failed = 1;
-            break;
-        }
-        mbar_try_wait(&s_bar, phase);
-        phase ^= 1u;
-        const int nblk = p.NS * bpu;
-        if (jd.kind == JOB_BONUS) {
-            // seed the bound with each thread's largest entry (exact score)
-            float m = kNegInf;
-            int mi = -1;
-            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
-                const UnitView uv = s_uv[bi / bpu];
-                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
-                for (int g = gb + lane; g < ge; g += 32) {
-                    float xv[4];
-                    group_vals<ESZ>(uv, g, xv);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (xv[q] > m) { m = xv[q]; mi = 4 * g + q; }
-                }
-            }
-            SliceRes seed;
-            seed.best = kNegInf;
-            seed.idx = -1;
-            seed.rawmax = kNegInf;
-            seed.failed = 0;
-            if (mi >= 0) {
-                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_BONUS,
-                                            (uint32_t)mi >> 2);
-                seed.best = fmaf(m, jd.invT, -jd.shift) + gumbel_of_word(word_of(r4, mi & 3));
-                seed.idx = mi;
-            }
-            seed = block_reduce(seed, s_red);
-            if (better(seed.best, seed.idx, mine.best, mine.idx)) { mine.best = seed.best; mine.idx = seed.idx; }
-            thr = fmaxf(thr, seed.best);
-        }
-        if (jd.kind == JOB_ARGMAX) {
-            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
-                const UnitView uv = s_uv[bi / bpu];
-                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
-                float m = kNegInf;
-                int mi = -1;
-                for (int g = gb + lane; g < ge; g += 32) {
-                    float xv[4];
-                    group_vals<ESZ>(uv, g, xv);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        mine.rawmax = max_nan_f32(mine.rawmax, xv[q]);
-                        if (xv[q] > m) { m = xv[q]; mi = 4 * g + q; }
-                    }
-                }
-                if (better(m, mi, mine.best, mine.idx)) { mine.best = m; mine.idx = mi; }
-            }
-        } else {
-            uint32_t *lg = s_live_g[warp];
-            float *lz = s_live_z[warp];
-            int nlive = 0;
-            for (int bi = warp; bi < nblk; bi += kCommitWarps) {
-                const int k = bi / bpu;
-                const UnitView uv = s_uv[k];
-                const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
-                if (gb >= ge) continue;
-                nlive = jd.kind == JOB_BONUS
-                            ? zfilter_block<ESZ, true>(uv, k, gb, ge, thr - kGumbelMax, jd.invT, jd.shift,
-                                                       mine.rawmax, lg, lz, nlive)
-                            : zfilter_block<ESZ, false>(uv, k, gb, ge, thr - kGumbelMax, jd.invT, jd.shift,
-                                                        mine.rawmax, lg, lz, nlive);
-                while (nlive >= 64) {  // draw the newest 64; the rest stay listed
-                    nlive -= 64;
-                    live_round<ESZ>(lg, lz, nlive, 64, s_uv, jd, p, (uint32_t)b, drow, thr, mine.best, mine.idx);
-                }
-            }
-            if (nlive > 0)
-                live_round<ESZ>(lg, lz, 0, nlive, s_uv, jd, p, (uint32_t)b, drow, thr, mine.best, mine.idx);
-        }
-        __syncthreads();  // every warp is done with the round's slots and views
-        if (warp == 0 && rd + 1 < nrounds) issue_round(jrow, rd + 1);
-    }
-    const SliceRes res = block_reduce(mine, s_red);
+    const SliceRes res = job_row_rounds<ESZ>(p, jd, (uint32_t)b, rank, jrow, drow, buf, &s_bar, s_uv, s_live_g,
+                                             s_live_z, s_red);
 
     // ---- the CTAs' results meet in rank 0
     cluster_wait();  // every CTA of the cluster is running
@@ -1239,6 +1264,430 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     if (tid == 0) {
         p.out_status[b] = status;
         p.out_accepted[b] = A;
+    }
+}
+
+// =================================================================== early_exit_kernel
+// Early-exit verify ("Accelerating Large-Model Inference ... DSpark", Sec. 1: the
+// longest accepted prefix is committed plus one token, so no row after the first
+// rejected position is needed; "From draft-then-verify to DSpark": the rejection
+// test at each position in order).  One cluster of C CTAs per request walks the
+// draft positions in order.  At position i every CTA streams its share of target
+// row i (and draft row i) with plain 16-byte loads and reduces it; the shares'
+// statistics meet over DSMEM -- every CTA reads all of them, in rank order, so
+// every CTA reaches the same decision -- and the walk stops at the first
+// rejection (or greedy mismatch, or non-finite row).  The correction is then drawn
+// over that row, or the bonus over row k_b, by the same staged Gumbel-max as
+// commit_kernel.  No workspace and no global synchronisation: a request's rows
+// after its first rejection are never read.
+constexpr int kEEVecs = 8;  // 16-byte loads per thread per batch
+
+struct __align__(16) EEPart {
+    float mt;   // target share: raw max (NaN-propagating)
+    float st;   // target share: sum 2^(x c - fl(mt c))
+    int it;     // target share: lowest argmax
+    float md;   // draft share: raw max
+    float sd;   // draft share: sum 2^(y c - fl(md c))
+    float seed; // best exact correction score among the share's warp argmaxes
+    int seed_idx;
+    int pad;
+};
+
+// This thread's vectors of a share window: vector j = j0 + tid + kCommitThreads t.
+template <class Vec>
+__device__ __forceinline__ void ee_load(Vec (&d)[kEEVecs], const ChunkWin &w, int j0) {
+    const int nvec = (int)(w.bytes >> 4);
+    const int ebase = w.e0 - w.shift;
+#pragma unroll
+    for (int t = 0; t < kEEVecs; ++t) {
+        const int j = j0 + (int)threadIdx.x + kCommitThreads * t;
+        d[t] = j < nvec ? Vec::load(w.a0, j) : Vec::neg_inf();
+        if (j < nvec && (j == 0 || j == nvec - 1) && (w.shift != 0 || ebase + nvec * Vec::VE != w.e1))
+            mask_vec(d[t], ebase + (int64_t)j * Vec::VE, w.e0, w.e1);
+    }
+}
+
+// Per-thread running statistics of one share window (as main_kernel's lanes).
+template <class Vec>
+__device__ void ee_thread_stats(const ChunkWin &w, float c, float &m, float &mc, float &s, int &aidx,
+                                bool &nan_seen) {
+    const int nvec = (int)(w.bytes >> 4);
+    const int ebase = w.e0 - w.shift;
+    for (int j0 = 0; j0 < nvec; j0 += kCommitThreads * kEEVecs) {
+        Vec d[kEEVecs];
+        ee_load(d, w, j0);
+        float tm = d[0].vmax();
+#pragma unroll
+        for (int t = 1; t < kEEVecs; ++t) tm = max_nan_f32(tm, d[t].vmax());
+        if (c != 0.f) {
+            if (!(tm <= m)) {
+                const float mcn = tm * c;
+                s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
+                m = tm;
+                mc = mcn;
+                aidx = chunk_find<kCommitThreads>(d, ebase + j0 * Vec::VE, (int)threadIdx.x, tm);
+            }
+            if (m != kNegInf) {
+                const float2 cc = make_float2(c, c), mm = make_float2(-mc, -mc);
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int t = 0; t < kEEVecs; ++t)
+#pragma unroll
+                    for (int e = 0; e < Vec::VE; e += 2) {
+                        const float2 y = ffma2(make_float2(d[t].get(e), d[t].get(e + 1)), cc, mm);
+                        acc = fadd2(acc, make_float2(ex2_approx(y.x), ex2_approx(y.y)));
+                    }
+                s += acc.x + acc.y;
+            }
+        } else {
+            if (tm != tm) {
+                nan_seen = true;
+            } else if (tm > m) {
+                m = tm;
+                aidx = chunk_find<kCommitThreads>(d, ebase + j0 * Vec::VE, (int)threadIdx.x, tm);
+            }
+        }
+    }
+}
+
+// Block reduction of the threads' statistics of one row; every thread returns the
+// CTA's (max, sum relative to fl(max c), lowest argmax).  wm / wi keep the warps'
+// maxima and argmaxes (correction seed candidates).  c == 0: max and argmax only,
+// with NaN propagated.
+__device__ void ee_block_stats(float m, float mc, float s, int aidx, bool nan_seen, float c, float *wm, int *wi,
+                               float *ws, float &M, float &S, int &I) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float Mw, Sw = 0.f;
+    if (c != 0.f) {
+        Mw = warp_max_nan(m);
+        const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - Mw * c);
+        Sw = warp_sum(sc);
+    } else {
+        const bool any_nan = __any_sync(0xffffffffu, nan_seen);
+        Mw = warp_max_nan(m);
+        if (any_nan) Mw = __int_as_float(0x7fc00000);
+    }
+    float bm = m;
+    int bi = aidx;
+    warp_argmax(bm, bi);
+    __syncthreads();  // wm / wi / ws may still be read from the previous row
+    if (lane == 0) {
+        wm[warp] = Mw;
+        wi[warp] = bi;
+        ws[warp] = Sw;
+    }
+    __syncthreads();
+    M = wm[0];
+    for (int w = 1; w < kCommitWarps; ++w) M = max_nan_f32(M, wm[w]);
+    S = 0.f;
+    float ab = kNegInf;
+    I = -1;
+    for (int w = 0; w < kCommitWarps; ++w) {
+        if (c != 0.f && wm[w] != kNegInf && ws[w] != 0.f) S += ws[w] * exp2f(wm[w] * c - M * c);
+        if (better(wm[w], wi[w], ab, I)) { ab = wm[w]; I = wi[w]; }
+    }
+}
+
+// Every CTA of the cluster writes its part to its own slot, then reads every
+// CTA's slot (rank order) into all[]; every thread calls it, the whole cluster
+// the same number of times.  Slots alternate by parity, so a slot is rewritten
+// only after the next exchange's barrier, which every reader passes after
+// reading.
+__device__ __forceinline__ void ee_exchange(const EEPart &mine, EEPart *slot, EEPart *all, int C) {
+    const int tid = threadIdx.x;
+    if (tid == 0) *slot = mine;
+    cluster_arrive();
+    cluster_wait();
+    if (tid < C) {
+        const uint32_t local = smem_addr(slot);
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"((uint32_t)tid));
+        uint4 a, b2;
+        asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w) : "r"(remote) : "memory");
+        asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(b2.x), "=r"(b2.y), "=r"(b2.z), "=r"(b2.w) : "r"(remote + 16) : "memory");
+        EEPart q;
+        q.mt = __uint_as_float(a.x);
+        q.st = __uint_as_float(a.y);
+        q.it = (int)a.z;
+        q.md = __uint_as_float(a.w);
+        q.sd = __uint_as_float(b2.x);
+        q.seed = __uint_as_float(b2.y);
+        q.seed_idx = (int)b2.z;
+        q.pad = 0;
+        all[tid] = q;
+    }
+    __syncthreads();
+}
+
+__host__ __device__ inline size_t ee_smem_bytes(int NS, int slot, int Kmax) {
+    return commit_round_bytes(NS, slot) + 5 * sizeof(float) * (size_t)Kmax;
+}
+
+template <int ESZ>
+__global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit_kernel(CommitParams p) {
+    using Vec = typename std::conditional<ESZ == 2, VecBF16, VecF32>::type;
+    extern __shared__ __align__(128) unsigned char cdyn[];
+    __shared__ uint64_t s_bar;
+    __shared__ uint32_t s_live_g[kCommitWarps][kLiveMax];
+    __shared__ float s_live_z[kCommitWarps][kLiveMax];
+    __shared__ SliceRes s_red[kCommitWarps];
+    __shared__ SliceRes s_inbox[kMaxCluster];
+    __shared__ UnitView s_uv[kUnitsPerCTA];
+    __shared__ EEPart s_slot[3];  // two alternating exchange slots and the seed slot
+    __shared__ EEPart s_all[kMaxCluster];
+    __shared__ float s_wm[kCommitWarps], s_ws[kCommitWarps];
+    __shared__ int s_wi[kCommitWarps];
+    __shared__ float s_tm[kCommitWarps];  // target share: per-warp maxima (seed candidates)
+    __shared__ int s_ti[kCommitWarps];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const int b = blockIdx.x / p.C;
+    cluster_arrive_relaxed();
+
+    unsigned char *buf = cdyn;
+    float *s_xt = (float *)(cdyn + commit_round_bytes(p.NS, p.slot));
+    float *s_xd = s_xt + p.Kmax;
+    float *s_l2u = s_xd + p.Kmax;
+    float *s_pp = s_l2u + p.Kmax;
+    float *s_qq = s_pp + p.Kmax;
+    if (tid == 0) {
+        mbar_init(&s_bar, 1);
+        mbar_init_fence();
+    }
+
+    const ReqBase rbase = req_base(p.cu, p.num_draft, p.Kmax, b);
+    const int kb_raw = rbase.kb;
+    int status = SPEC_STATUS_OK;
+    float T = 0.f;
+    if (kb_raw < 0 || kb_raw > p.Kmax) status = SPEC_STATUS_BAD_K;
+    if (status == SPEC_STATUS_OK && p.temperature) {
+        T = p.temperature[b];
+        if (!(T >= 0.f) || isinf(T)) status = SPEC_STATUS_BAD_TEMPERATURE;
+    }
+    const int kb = status == SPEC_STATUS_BAD_K ? 0 : kb_raw;
+    const bool greedy = (T == 0.f);
+    const int32_t *x = p.draft_tokens + rbase.d0;
+    if (status == SPEC_STATUS_OK) {
+        bool bad = false;
+        for (int i = tid; i < kb; i += kCommitThreads) bad |= (x[i] < 0 || x[i] >= p.V);
+        if (__syncthreads_or(bad)) status = SPEC_STATUS_BAD_TOKEN;
+    }
+    const float c = greedy ? 0.f : __fdiv_rn(kLog2e, T);
+    const float invT = greedy ? 0.f : __fdiv_rn(1.f, T);
+    const int npos = status == SPEC_STATUS_OK ? kb : 0;
+    for (int i = tid; i < p.Kmax; i += kCommitThreads) {
+        s_pp[i] = -1.f;
+        s_qq[i] = -1.f;
+        if (i < npos && !greedy) {
+            const int xi = x[i];
+            s_xt[i] = load_logit(p.target, p.dtype, (rbase.t0 + i) * p.ld_row + xi);
+            s_xd[i] = load_logit(p.draft, p.dtype, (rbase.d0 + i) * p.ld_row + xi);
+            const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
+            s_l2u[i] = log2f(u01(r4.x));
+        }
+    }
+    cluster_wait();  // every CTA of the cluster is running
+    __syncthreads();
+
+    const int64_t rowbytes = p.ld_row * ESZ;
+    const int sh = (((p.V + p.C - 1) / p.C) + 7) & ~7;  // share of a row per CTA
+    const Chunking shk = {p.C, sh};
+    const bool has_share = (int64_t)rank * sh < p.V;
+    auto share_window = [&](const char *row) {
+        ChunkWin w;
+        if (has_share) {
+            w = chunk_window(row, ESZ, p.V, shk, (int)rank);
+        } else {
+            w.a0 = row;
+            w.bytes = 0;
+            w.e0 = w.e1 = w.shift = 0;
+        }
+        return w;
+    };
+    auto nonfinite = [](float v) { return !(fabsf(v) < __int_as_float(0x7f800000)); };
+
+    JobDesc jd;
+    jd.kind = JOB_NONE;
+    jd.row = 0;
+    jd.A = 0;
+    jd.token = -1;
+    jd.invT = invT;
+    jd.shift = jd.Cd = 0.f;
+    jd.seed = kNegInf;
+    jd.seed_idx = -1;
+    int A = kb;
+    int nx = 0;  // exchanges so far (slot parity)
+    if (status == SPEC_STATUS_OK) {
+        for (int i = 0; i < kb; ++i) {
+            // ---- this CTA's share of target row i (and draft row i)
+            const char *trow = (const char *)p.target + (rbase.t0 + i) * rowbytes;
+            float m = kNegInf, mc = 0.f, s = 0.f;
+            int aidx = -1;
+            bool nan_seen = false;
+            ee_thread_stats<Vec>(share_window(trow), c, m, mc, s, aidx, nan_seen);
+            EEPart part;
+            ee_block_stats(m, mc, s, aidx, nan_seen, c, s_wm, s_wi, s_ws, part.mt, part.st, part.it);
+            if (tid < kCommitWarps) {  // the target share's warp argmaxes: correction seed candidates
+                s_tm[tid] = s_wm[tid];
+                s_ti[tid] = s_wi[tid];
+            }
+            part.md = 0.f;
+            part.sd = 0.f;
+            if (!greedy) {
+                const char *drow = (const char *)p.draft + (rbase.d0 + i) * rowbytes;
+                float m2 = kNegInf, mc2 = 0.f, s2 = 0.f;
+                int a2 = -1;
+                bool n2 = false;
+                ee_thread_stats<Vec>(share_window(drow), c, m2, mc2, s2, a2, n2);
+                int i2;
+                ee_block_stats(m2, mc2, s2, a2, n2, c, s_wm, s_wi, s_ws, part.md, part.sd, i2);
+            }
+            part.seed = kNegInf;
+            part.seed_idx = -1;
+            part.pad = 0;
+            // ---- the shares meet; every CTA combines them in rank order
+            ee_exchange(part, &s_slot[nx & 1], s_all, p.C);
+            ++nx;
+            float Mt = s_all[0].mt, Md = s_all[0].md;
+            for (int r = 1; r < p.C; ++r) {
+                Mt = max_nan_f32(Mt, s_all[r].mt);
+                Md = max_nan_f32(Md, s_all[r].md);
+            }
+            float St = 0.f, Sd = 0.f, bm = kNegInf;
+            int It = -1;
+            for (int r = 0; r < p.C; ++r) {
+                const EEPart q = s_all[r];
+                if (!greedy && q.mt != kNegInf && q.st != 0.f) St += q.st * exp2f(q.mt * c - Mt * c);
+                if (!greedy && q.md != kNegInf && q.sd != 0.f) Sd += q.sd * exp2f(q.md * c - Md * c);
+                if (better(q.mt, q.it, bm, It)) { bm = q.mt; It = q.it; }
+            }
+            if (nonfinite(Mt) || (!greedy && (nonfinite(Md) || nonfinite(St) || nonfinite(Sd)))) {
+                status = SPEC_STATUS_NONFINITE;
+                break;
+            }
+            if (greedy) {
+                if (It != x[i]) {
+                    A = i;
+                    jd.token = It;
+                    break;
+                }
+                continue;
+            }
+            const float l2St = log2f(St), l2Sd = log2f(Sd);
+            const float l2p = fmaf(s_xt[i], c, -(Mt * c)) - l2St;  // log2 p_i(x_i)
+            const float l2q = fmaf(s_xd[i], c, -(Md * c)) - l2Sd;  // log2 q_i(x_i)
+            if (tid == 0) {
+                s_pp[i] = exp2f(l2p);
+                s_qq[i] = exp2f(l2q);
+            }
+            // accept iff u q < p, i.e. log2 u < log2 p - log2 q (Q = 0 < P accepts; P = 0 rejects)
+            if (s_l2u[i] < l2p - l2q) continue;
+            A = i;
+            jd.kind = JOB_RESID;
+            jd.row = i;
+            jd.shift = (Mt * c + l2St) * 0.6931471805599453f;
+            jd.Cd = (Md * c + l2Sd) * 0.6931471805599453f;
+            // exact correction scores at this CTA's warp argmaxes of target row i; the
+            // best over the cluster bounds the draw
+            const char *drow = (const char *)p.draft + (rbase.d0 + i) * rowbytes;
+            float sb = kNegInf;
+            int si = -1;
+            if (warp == 0) {
+                if (lane < kCommitWarps && s_ti[lane] >= 0) {
+                    const int v = s_ti[lane];
+                    const float z = fmaf(s_tm[lane], invT, -jd.shift);
+                    const float lq = fmaf(load_logit(drow, p.dtype, v), invT, -jd.Cd);
+                    if (lq < z) {
+                        const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_RESIDUAL,
+                                                    (uint32_t)v >> 2);
+                        const float sc = resid_score(z, lq, word_of(r4, v & 3));
+                        if (sc > kNegInf) { sb = sc; si = v; }
+                    }
+                }
+                warp_argmax(sb, si);
+            }
+            EEPart sp;
+            sp.mt = sp.st = sp.md = sp.sd = 0.f;
+            sp.it = sp.pad = 0;
+            sp.seed = __shfl_sync(0xffffffffu, sb, 0);
+            sp.seed_idx = __shfl_sync(0xffffffffu, si, 0);
+            if (warp == 0 && lane == 0) s_slot[2] = sp;
+            __syncthreads();
+            ee_exchange(s_slot[2], &s_slot[2], s_all, p.C);
+            for (int r = 0; r < p.C; ++r)
+                if (better(s_all[r].seed, s_all[r].seed_idx, jd.seed, jd.seed_idx)) {
+                    jd.seed = s_all[r].seed;
+                    jd.seed_idx = s_all[r].seed_idx;
+                }
+            break;
+        }
+        if (status == SPEC_STATUS_OK && A == kb && jd.token < 0 && jd.kind == JOB_NONE) {
+            jd.row = kb;
+            jd.kind = greedy ? JOB_ARGMAX : JOB_BONUS;
+        }
+    }
+    jd.A = A;
+
+    // ---- the one extra token: staged Gumbel-max over the job row (or argmax)
+    const char *jrow = (const char *)p.target + (rbase.t0 + jd.row) * rowbytes;
+    const char *jdrow = jd.kind == JOB_RESID ? (const char *)p.draft + (rbase.d0 + jd.row) * rowbytes : nullptr;
+    if (warp == 0 && jd.kind != JOB_NONE) issue_job_round<ESZ>(p, rank, jrow, 0, buf, &s_bar, s_uv);
+    __syncthreads();
+    const SliceRes res = job_row_rounds<ESZ>(p, jd, (uint32_t)b, rank, jrow, jdrow, buf, &s_bar, s_uv, s_live_g,
+                                             s_live_z, s_red);
+    if (tid == 0) st_cluster_v4(&s_inbox[rank], 0, make_uint4(__float_as_uint(res.best), (uint32_t)res.idx,
+                                                               __float_as_uint(res.rawmax), (uint32_t)res.failed));
+    cluster_arrive();
+    cluster_wait();
+    if (rank != 0) return;
+
+    int token = jd.token;
+    if (status == SPEC_STATUS_OK && jd.kind != JOB_NONE) {
+        SliceRes o = s_inbox[0];
+        for (int r = 1; r < p.C; ++r) {
+            const SliceRes q = s_inbox[r];
+            if (better(q.best, q.idx, o.best, o.idx)) { o.best = q.best; o.idx = q.idx; }
+            o.rawmax = max_nan_f32(o.rawmax, q.rawmax);
+            o.failed |= q.failed;
+        }
+        if (o.failed) status = SPEC_STATUS_INTERNAL;
+        else if (jd.kind != JOB_RESID && nonfinite(o.rawmax)) status = SPEC_STATUS_NONFINITE;
+        token = o.idx;
+        if (status == SPEC_STATUS_OK && jd.kind == JOB_RESID && o.idx < 0) {
+            // p <= q everywhere (only by rounding): draw from p_j with the same noise
+            const int64_t trow = (rbase.t0 + jd.row) * p.ld_row;
+            SliceRes f;
+            f.best = kNegInf;
+            f.idx = -1;
+            f.rawmax = kNegInf;
+            f.failed = 0;
+            for (int v = tid; v < p.V; v += kCommitThreads) {
+                const float lp = fmaf(load_logit(p.target, p.dtype, trow + v), jd.invT, -jd.shift);
+                if (!(lp > kNegInf)) continue;
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
+                                            (uint32_t)v >> 2);
+                const float sc = lp + gumbel_of_word(word_of(r4, v & 3));
+                if (better(sc, v, f.best, f.idx)) { f.best = sc; f.idx = v; }
+            }
+            token = block_reduce(f, s_red).idx;
+        }
+    }
+    const bool ok = status == SPEC_STATUS_OK;
+    const int Aout = ok ? A : 0;
+    int32_t *tok = p.out_tokens + rbase.t0;
+    for (int i = tid; i < rbase.ntok; i += kCommitThreads)
+        tok[i] = !ok ? -1 : (i < Aout ? x[i] : (i == Aout ? token : -1));
+    const bool pq = ok && !greedy;
+    if (p.out_p)
+        for (int i = tid; i < rbase.npq; i += kCommitThreads) p.out_p[rbase.d0 + i] = pq && i < kb ? s_pp[i] : -1.f;
+    if (p.out_q)
+        for (int i = tid; i < rbase.npq; i += kCommitThreads) p.out_q[rbase.d0 + i] = pq && i < kb ? s_qq[i] : -1.f;
+    if (tid == 0) {
+        p.out_status[b] = status;
+        p.out_accepted[b] = Aout;
     }
 }
 
@@ -1363,6 +1812,42 @@ int set_smem_attrs(int dev) {
                                  (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     g_attr_set[dev][which] = true;
+    return SPEC_OK;
+}
+
+template <class Vec>
+int launch_early_exit(int dev, const Layout &L, const CommitParams &cp, cudaStream_t st) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int which = 2 + (Vec::ESIZE == 2 ? 0 : 1);
+        if (!g_attr_set[dev][which]) {
+            cudaError_t e = cudaFuncSetAttribute(early_exit_kernel<Vec::ESIZE>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kCommitSmemMax);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(early_exit_kernel<Vec::ESIZE>,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
+            g_attr_set[dev][which] = true;
+        }
+    }
+    ProfScope ps(st);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cp.B * L.C));
+    cfg.blockDim = dim3(kCommitThreads);
+    cfg.dynamicSmemBytes = ee_smem_bytes(L.NS, L.slot, cp.Kmax);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)L.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+    attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, early_exit_kernel<Vec::ESIZE>, cp);
+    if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     return SPEC_OK;
 }
 
@@ -1495,6 +1980,55 @@ int static_scratch(int dev, void **out) {
     return SPEC_OK;
 }
 
+// Early-exit verify: one kernel, no workspace (see early_exit_kernel).
+int early_exit_impl(const void *target, const void *draft, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                    const int32_t *draft_tokens, const int32_t *num_draft, const float *temperature,
+                    uint64_t seed, uint64_t step, int32_t *out_tokens, int32_t *out_accepted, float *out_p,
+                    float *out_q, int32_t *out_status, void *cuda_stream, bool sample) {
+    if (B < 0 || Kmax < 0 || V <= 0 || ld_row < V) return SPEC_EINVAL;
+    if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_EINVAL;
+    if (B == 0) return SPEC_OK;
+    if (B > SPEC_MAX_BATCH || Kmax > SPEC_MAX_DRAFTS) return SPEC_EUNSUPPORTED;
+    if (!target || !out_tokens || !out_accepted || !out_status) return SPEC_EINVAL;
+    if (Kmax > 0 && !draft_tokens) return SPEC_EINVAL;
+    if (sample && (!temperature || (Kmax > 0 && !draft))) return SPEC_EINVAL;
+    const int esz = dtype == SPEC_BF16 ? 2 : 4;
+    if (((uintptr_t)target % esz) || (draft && ((uintptr_t)draft % esz))) return SPEC_EINVAL;
+    int dev = 0, sms = 0;
+    int rc = device_info(&dev, &sms);
+    if (rc) return rc;
+    const Layout L = make_layout(B, Kmax, V, esz, sms, sample ? 2 * Kmax : Kmax);
+    if (L.slot > kRoundMaxBytes || ee_smem_bytes(L.NS, L.slot, Kmax) > (size_t)kCommitSmemMax)
+        return SPEC_EUNSUPPORTED;
+    rc = prof_prepare();
+    if (rc) return rc;
+    CommitParams cp = {};
+    cp.target = target;
+    cp.draft = draft;
+    cp.dtype = dtype;
+    cp.ld_row = ld_row;
+    cp.B = B;
+    cp.Kmax = Kmax;
+    cp.V = V;
+    cp.draft_tokens = draft_tokens;
+    cp.cu = nullptr;
+    cp.num_draft = num_draft;
+    cp.temperature = sample ? temperature : nullptr;
+    cp.seed = seed;
+    cp.step = (uint32_t)step;
+    cp.C = L.C;
+    cp.ue = L.ue;
+    cp.NS = L.NS;
+    cp.slot = L.slot;
+    cp.out_tokens = out_tokens;
+    cp.out_accepted = out_accepted;
+    cp.out_p = sample ? out_p : nullptr;
+    cp.out_q = sample ? out_q : nullptr;
+    cp.out_status = out_status;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    return dtype == SPEC_BF16 ? launch_early_exit<VecBF16>(dev, L, cp, st) : launch_early_exit<VecF32>(dev, L, cp, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1565,6 +2099,22 @@ int spec_verify_sample_flat(const void *target, const void *draft, int dtype, in
     return verify_impl(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, cu_draft, nullptr, temperature,
                        seed, step, out_tokens, out_accepted, out_p, out_q, out_status, ws, ws_bytes, cuda_stream,
                        true);
+}
+
+int spec_verify_sample_early_exit(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
+                                  int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
+                                  const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+                                  int32_t *out_accepted, float *out_p, float *out_q, int32_t *out_status,
+                                  void *cuda_stream) {
+    return early_exit_impl(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, temperature, seed,
+                           step, out_tokens, out_accepted, out_p, out_q, out_status, cuda_stream, true);
+}
+
+int spec_verify_greedy_early_exit(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
+                                  const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
+                                  int32_t *out_accepted, int32_t *out_status, void *cuda_stream) {
+    return early_exit_impl(target, nullptr, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, nullptr, 0, 0,
+                           out_tokens, out_accepted, nullptr, nullptr, out_status, cuda_stream, false);
 }
 
 const char *spec_error_string(int err) {
