@@ -340,8 +340,27 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
     int r = first_row, k = c0 - first_row * ck.cpr;
     MainRow mr = table ? s_desc[0] : main_row<Vec>(p, s_rs, r);
     float m = kNegInf, mc = 0.f, s = 0.f;
-    int aidx = -1;
+    int kat = -1;  // chunk of the row where this lane's running max was last raised
     bool nan_seen = false;
+    // The lowest index holding the warp's maximum M.  Lanes find their max's index
+    // only here, once per row segment: the lanes whose running max equals M reload
+    // the chunk where it was raised (its first occurrence in this lane's entries is
+    // there) and scan it.  Finding it as each chunk raised a lane's max cost a scan
+    // of every chunk by nearly every warp, since some lane of 32 almost always
+    // raises its max.
+    auto warp_first_index_of = [&](float M) {
+        int idx = -1;
+        if (kat >= 0 && m == M) {
+            const ChunkWin w2 = chunk_window(mr.ptr, Vec::ESIZE, p.V, ck, kat);
+            Vec d2[kVPT];
+            load_chunk(d2, w2, ct);
+            idx = chunk_find<kCT>(d2, w2.e0 - w2.shift, ct, M);
+        }
+        uint32_t v = (uint32_t)idx;  // -1: none (largest as unsigned)
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+        return (int)v;
+    };
     auto flush = [&]() {
         Part out;
         if (mr.c != 0.f) {
@@ -349,19 +368,14 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
             const float MC = M * mr.c;
             const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - MC);
             out.s = warp_sum(sc);
-            float mm = m;
-            int ii = aidx;
-            warp_argmax(mm, ii);
             out.m = M;
-            out.idx = ii;
+            out.idx = warp_first_index_of(M);
         } else {
             const bool any_nan = __any_sync(0xffffffffu, nan_seen);
-            float mm = m;
-            int ii = aidx;
-            warp_argmax(mm, ii);
+            const float mm = warp_max_nan(m);  // greedy lanes keep m free of NaN
+            out.idx = warp_first_index_of(mm);
             out.m = any_nan ? __int_as_float(0x7fc00000) : mm;
             out.s = 0.f;
-            out.idx = ii;
         }
         out.pad = 0.f;
         if (lane == 0) p.parts[part_slot(blockIdx.x, p.nseg, r - first_row, warp)] = out;
@@ -371,7 +385,6 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
         const ChunkWin w = chunk_window(mr.ptr, Vec::ESIZE, p.V, ck, k);
         Vec d[kVPT];
         load_chunk(d, w, ct);
-        const int ebase = w.e0 - w.shift;
         if (mr.c != 0.f) {
             // s is kept relative to the lane's running max m (mc = fl(m c)), so every
             // term is at most 1; the max moves (and s is rescaled) only when a chunk
@@ -383,7 +396,7 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
                 s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
                 m = tm;
                 mc = mcn;
-                aidx = chunk_find<kCT>(d, ebase, ct, tm);
+                kat = k;
             }
             if (m != kNegInf) s += chunk_expsum(d, mr.c, mc);
         } else {
@@ -392,7 +405,7 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
                 nan_seen = true;
             } else if (tm > m) {
                 m = tm;
-                aidx = chunk_find<kCT>(d, ebase, ct, tm);
+                kat = k;
             }
         }
         if (++k == ck.cpr || cc + 1 == c1) {  // row segment ends
@@ -403,7 +416,7 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
             m = kNegInf;
             mc = 0.f;
             s = 0.f;
-            aidx = -1;
+            kat = -1;
             nan_seen = false;
         }
     }
@@ -1280,7 +1293,9 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
 // over that row, or the bonus over row k_b, by the same staged Gumbel-max as
 // commit_kernel.  No workspace and no global synchronisation: a request's rows
 // after its first rejection are never read.
-constexpr int kEEVecs = 8;  // 16-byte loads per thread per batch
+constexpr int kEEVecs = 8;       // 16-byte loads per thread per batch
+constexpr int kEEAhead = 2;      // positions whose shares are prefetched into L2 ahead of the walk
+constexpr uint32_t kEEPiece = 16384;  // bytes per bulk prefetch
 
 struct __align__(16) EEPart {
     float mt;   // target share: raw max (NaN-propagating)
@@ -1307,12 +1322,12 @@ __device__ __forceinline__ void ee_load(Vec (&d)[kEEVecs], const ChunkWin &w, in
     }
 }
 
-// Per-thread running statistics of one share window (as main_kernel's lanes).
+// Per-thread running statistics of one share window (as main_kernel's lanes);
+// kat: the batch where the thread's running max was last raised.
 template <class Vec>
-__device__ void ee_thread_stats(const ChunkWin &w, float c, float &m, float &mc, float &s, int &aidx,
+__device__ void ee_thread_stats(const ChunkWin &w, float c, float &m, float &mc, float &s, int &kat,
                                 bool &nan_seen) {
     const int nvec = (int)(w.bytes >> 4);
-    const int ebase = w.e0 - w.shift;
     for (int j0 = 0; j0 < nvec; j0 += kCommitThreads * kEEVecs) {
         Vec d[kEEVecs];
         ee_load(d, w, j0);
@@ -1325,7 +1340,7 @@ __device__ void ee_thread_stats(const ChunkWin &w, float c, float &m, float &mc,
                 s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
                 m = tm;
                 mc = mcn;
-                aidx = chunk_find<kCommitThreads>(d, ebase + j0 * Vec::VE, (int)threadIdx.x, tm);
+                kat = j0;
             }
             if (m != kNegInf) {
                 const float2 cc = make_float2(c, c), mm = make_float2(-mc, -mc);
@@ -1344,17 +1359,33 @@ __device__ void ee_thread_stats(const ChunkWin &w, float c, float &m, float &mc,
                 nan_seen = true;
             } else if (tm > m) {
                 m = tm;
-                aidx = chunk_find<kCommitThreads>(d, ebase + j0 * Vec::VE, (int)threadIdx.x, tm);
+                kat = j0;
             }
         }
     }
+}
+
+// Lowest index of the warp's maximum M over the share (the lanes holding it reload
+// the batch where their max was raised, as main_kernel's flush does).
+template <class Vec>
+__device__ int ee_warp_index(const ChunkWin &w, int kat, float m, float M) {
+    int idx = -1;
+    if (kat >= 0 && m == M) {
+        Vec d[kEEVecs];
+        ee_load(d, w, kat);
+        idx = chunk_find<kCommitThreads>(d, w.e0 - w.shift + kat * Vec::VE, (int)threadIdx.x, M);
+    }
+    uint32_t v = (uint32_t)idx;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return (int)v;
 }
 
 // Block reduction of the threads' statistics of one row; every thread returns the
 // CTA's (max, sum relative to fl(max c), lowest argmax).  wm / wi keep the warps'
 // maxima and argmaxes (correction seed candidates).  c == 0: max and argmax only,
 // with NaN propagated.
-__device__ void ee_block_stats(float m, float mc, float s, int aidx, bool nan_seen, float c, float *wm, int *wi,
+__device__ void ee_block_stats(float m, float mc, float s, int widx, bool nan_seen, float c, float *wm, int *wi,
                                float *ws, float &M, float &S, int &I) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float Mw, Sw = 0.f;
@@ -1367,13 +1398,10 @@ __device__ void ee_block_stats(float m, float mc, float s, int aidx, bool nan_se
         Mw = warp_max_nan(m);
         if (any_nan) Mw = __int_as_float(0x7fc00000);
     }
-    float bm = m;
-    int bi = aidx;
-    warp_argmax(bm, bi);
     __syncthreads();  // wm / wi / ws may still be read from the previous row
     if (lane == 0) {
         wm[warp] = Mw;
-        wi[warp] = bi;
+        wi[warp] = widx;
         ws[warp] = Sw;
     }
     __syncthreads();
@@ -1508,6 +1536,21 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
         return w;
     };
     auto nonfinite = [](float v) { return !(fabsf(v) < __int_as_float(0x7f800000)); };
+    // Warp 0 asks L2 for this CTA's shares of position j's rows (target and, when
+    // sampling, draft row j; target row k_b alone for j = k_b), so that the walk's
+    // loads there find them in L2.  The 16-byte-aligned window of a share lies in
+    // pages that hold the share's own entries.
+    auto prefetch_position = [&](int j) {
+        if (warp != 0 || j > kb || !has_share) return;
+        const int nrows = (j < kb && !greedy) ? 2 : 1;
+        for (int r = 0; r < nrows; ++r) {
+            const char *row = r == 0 ? (const char *)p.target + (rbase.t0 + j) * rowbytes
+                                     : (const char *)p.draft + (rbase.d0 + j) * rowbytes;
+            const ChunkWin w = share_window(row);
+            for (uint32_t off = (uint32_t)lane * kEEPiece; off < w.bytes; off += 32u * kEEPiece)
+                prefetch_l2_bulk(w.a0 + off, min(kEEPiece, w.bytes - off));
+        }
+    };
 
     JobDesc jd;
     jd.kind = JOB_NONE;
@@ -1521,15 +1564,19 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
     int A = kb;
     int nx = 0;  // exchanges so far (slot parity)
     if (status == SPEC_STATUS_OK) {
+        for (int j = 1; j < kEEAhead; ++j) prefetch_position(j);
         for (int i = 0; i < kb; ++i) {
+            prefetch_position(i + kEEAhead);
             // ---- this CTA's share of target row i (and draft row i)
             const char *trow = (const char *)p.target + (rbase.t0 + i) * rowbytes;
             float m = kNegInf, mc = 0.f, s = 0.f;
-            int aidx = -1;
+            int kat = -1;
             bool nan_seen = false;
-            ee_thread_stats<Vec>(share_window(trow), c, m, mc, s, aidx, nan_seen);
+            const ChunkWin tw = share_window(trow);
+            ee_thread_stats<Vec>(tw, c, m, mc, s, kat, nan_seen);
+            const int widx = ee_warp_index<Vec>(tw, kat, m, warp_max_nan(m));
             EEPart part;
-            ee_block_stats(m, mc, s, aidx, nan_seen, c, s_wm, s_wi, s_ws, part.mt, part.st, part.it);
+            ee_block_stats(m, mc, s, widx, nan_seen, c, s_wm, s_wi, s_ws, part.mt, part.st, part.it);
             if (tid < kCommitWarps) {  // the target share's warp argmaxes: correction seed candidates
                 s_tm[tid] = s_wm[tid];
                 s_ti[tid] = s_wi[tid];
@@ -1539,11 +1586,11 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
             if (!greedy) {
                 const char *drow = (const char *)p.draft + (rbase.d0 + i) * rowbytes;
                 float m2 = kNegInf, mc2 = 0.f, s2 = 0.f;
-                int a2 = -1;
+                int k2 = -1;
                 bool n2 = false;
-                ee_thread_stats<Vec>(share_window(drow), c, m2, mc2, s2, a2, n2);
-                int i2;
-                ee_block_stats(m2, mc2, s2, a2, n2, c, s_wm, s_wi, s_ws, part.md, part.sd, i2);
+                ee_thread_stats<Vec>(share_window(drow), c, m2, mc2, s2, k2, n2);
+                int i2;  // the draft row's argmax is not needed
+                ee_block_stats(m2, mc2, s2, -1, n2, c, s_wm, s_wi, s_ws, part.md, part.sd, i2);
             }
             part.seed = kNegInf;
             part.seed_idx = -1;
