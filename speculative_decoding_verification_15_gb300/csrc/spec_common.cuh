@@ -302,12 +302,6 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 
 // 16-byte store into the shared memory of CTA `rank` of this cluster, at the
 // address that `local` has in this CTA's shared memory.
-// Bulk prefetch of [p, p + bytes) into L2 (no completion to wait for): p 16-byte
-// aligned, bytes a multiple of 16.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void st_cluster_v4(void *local, uint32_t rank, uint4 v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));

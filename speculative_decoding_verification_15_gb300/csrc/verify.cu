@@ -1293,9 +1293,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
 // over that row, or the bonus over row k_b, by the same staged Gumbel-max as
 // commit_kernel.  No workspace and no global synchronisation: a request's rows
 // after its first rejection are never read.
-constexpr int kEEVecs = 8;       // 16-byte loads per thread per batch
-constexpr int kEEAhead = 2;      // positions whose shares are prefetched into L2 ahead of the walk
-constexpr uint32_t kEEPiece = 16384;  // bytes per bulk prefetch
+constexpr int kEEVecs = 8;  // 16-byte loads per thread per batch
 
 struct __align__(16) EEPart {
     float mt;   // target share: raw max (NaN-propagating)
@@ -1536,21 +1534,6 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
         return w;
     };
     auto nonfinite = [](float v) { return !(fabsf(v) < __int_as_float(0x7f800000)); };
-    // Warp 0 asks L2 for this CTA's shares of position j's rows (target and, when
-    // sampling, draft row j; target row k_b alone for j = k_b), so that the walk's
-    // loads there find them in L2.  The 16-byte-aligned window of a share lies in
-    // pages that hold the share's own entries.
-    auto prefetch_position = [&](int j) {
-        if (warp != 0 || j > kb || !has_share) return;
-        const int nrows = (j < kb && !greedy) ? 2 : 1;
-        for (int r = 0; r < nrows; ++r) {
-            const char *row = r == 0 ? (const char *)p.target + (rbase.t0 + j) * rowbytes
-                                     : (const char *)p.draft + (rbase.d0 + j) * rowbytes;
-            const ChunkWin w = share_window(row);
-            for (uint32_t off = (uint32_t)lane * kEEPiece; off < w.bytes; off += 32u * kEEPiece)
-                prefetch_l2_bulk(w.a0 + off, min(kEEPiece, w.bytes - off));
-        }
-    };
 
     JobDesc jd;
     jd.kind = JOB_NONE;
@@ -1564,9 +1547,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
     int A = kb;
     int nx = 0;  // exchanges so far (slot parity)
     if (status == SPEC_STATUS_OK) {
-        for (int j = 1; j < kEEAhead; ++j) prefetch_position(j);
         for (int i = 0; i < kb; ++i) {
-            prefetch_position(i + kEEAhead);
             // ---- this CTA's share of target row i (and draft row i)
             const char *trow = (const char *)p.target + (rbase.t0 + i) * rowbytes;
             float m = kNegInf, mc = 0.f, s = 0.f;
