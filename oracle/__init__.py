@@ -75,6 +75,9 @@ def _load():
         lib.oracle_schedule_threshold.restype = I32
         lib.oracle_schedule_verify_len_stale.argtypes = [P, P, P, I32, I32, P, I32, I32, I32, P, P, P]
         lib.oracle_schedule_verify_len_stale.restype = I32
+        lib.oracle_markov_draft.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, I32, P, U64, U64, I32, P, P, P,
+                                            P, I32]
+        lib.oracle_markov_draft.restype = I32
         _lib = lib
         return lib
 
@@ -245,3 +248,36 @@ def schedule_verify_len_stale(conf_stale, conf, max_len, step_time_us, budget: i
         return None
     return dict(len=out_len, n=int(info[0]), expected_tokens=float(info[1]),
                 tokens_per_us=float(info[2]), flags=int(flags[0]))
+
+
+# ------------------------------------------------------------------ Markov-head drafting
+def markov_draft(base, anchor, emb, proj, temperature, seed: int, step: int, topk: int = 0,
+                 nthreads: int = 1, want_logits: bool = True) -> dict:
+    """Semi-autoregressive drafting of one block with a rank-r Markov head.
+
+    base [B, K, V] float32 or bf16 bit patterns (uint16): the backbone's logits;
+    anchor [B] int32: the token before the block; emb, proj [V, r] in base's dtype;
+    temperature [B] float32 (0: greedy) or None (all greedy); topk = 0: the whole
+    vocabulary, else only the topk largest base logits are corrected and drawn from.
+    Returns tokens [B, K], logits [B, K, V] (the corrected z, -inf outside the
+    candidates), status [B] and tie [B] (first position decided within the near-tie
+    band, K if none).
+    """
+    lib = _load()
+    u, du = _logit_array(base)
+    e, de = _logit_array(emb)
+    pr, dp = _logit_array(proj)
+    assert du == de == dp
+    B, K, V = u.shape
+    r = e.shape[1]
+    assert e.shape == (V, r) and pr.shape == (V, r)
+    a = _c(anchor, np.int32)
+    T = None if temperature is None else _c(temperature, np.float32)
+    out = dict(tokens=np.full((B, K), -1, np.int32),
+               logits=np.zeros((B, K, V)) if want_logits else None,
+               status=np.zeros(B, np.int32), tie=np.zeros(B, np.int32))
+    rc = lib.oracle_markov_draft(_ptr(u), du, B, K, V, V, _ptr(a), _ptr(e), _ptr(pr), r, _ptr(T),
+                                 seed & (2**64 - 1), step & (2**64 - 1), topk, _ptr(out["tokens"]),
+                                 _ptr(out["logits"]), _ptr(out["status"]), _ptr(out["tie"]), nthreads)
+    assert rc == 0
+    return out

@@ -22,7 +22,12 @@
  *         the startup step-time table; production variant searches the whole
  *         table instead of stopping at the first drop).
  *  [MTL]  "Bringing DSpark to vLLM Metal" (mhdimo.github.io) -- "Correctness is
- *         the feature": greedy path compares the target's argmax with the draft.
+ *         the feature": greedy path compares the target's argmax with the draft;
+ *         "Making the draft cheaper": top-K Markov drafting (the correction only
+ *         on the candidates picked from the base logits).
+ *  [PPR2] "Accelerating Large-Model Inference ..." -- the drafting-engine table
+ *         (layer 2, Markov head: a low-rank bias applied left to right, the bias at
+ *         position k+1 set by the token chosen at position k).
  *  [SC11] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2,
  *         3", SC'11 -- Philox4x32-10.
  *
@@ -692,5 +697,121 @@ int oracle_schedule_verify_len_stale(const float *conf_stale, const float *conf,
     }
     if (out_flags) *out_flags = (flags_stale & 1) | (flags_now & 2);
     free(len_now);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Markov-head drafting [PPR2], [VBK] Sec. 4.1, [MTL]                         */
+/* ------------------------------------------------------------------------- */
+#define REL_TIE_MARKOV 1e-4 /* near-tie band of the draw (the GPU's bias is an fp32 dot product) */
+
+/*
+ * Semi-autoregressive drafting of one block.  For request b and positions
+ * k = 0 .. K-1, left to right:
+ *   prev = anchor[b] (k = 0) or x_{k-1};
+ *   bias_v = sum_j emb[prev, j] * proj[v, j]   (rank-r factors, both [V, r]);
+ *   z_v = U[b, k, v] + bias_v for v in the candidate set, -inf elsewhere;
+ *   candidates: every v (topk = 0), or the topk entries with the largest base
+ *   logit U[b, k, v], lower v first among equal values [MTL];
+ *   x_k = argmax_v z_v (T_b = 0, lowest v on ties), else the Gumbel-max draw
+ *   argmax_v z_v / T_b + g_v with g_v from purpose 3 at row k.
+ * Readings (the pages name the bias "low-rank" and its input "the token chosen at
+ * the previous position", and give the default rank 256, not the factorisation):
+ * the bias row of token prev is the product of prev's row of an embedding factor
+ * with a projection factor; the temperature of the draw is the request's
+ * temperature; the draw uses the library's counter-based noise with its own
+ * purpose.  Status: 1 anchor outside [0, V), 3 bad temperature, 4 a corrected row
+ * with NaN or +inf among the candidates or no finite candidate; a request with a
+ * non-zero status has every token -1.
+ * out_logits [B, K, V] (may be NULL): the corrected logits z (the draft
+ * distribution the verify step needs is softmax(z / T)).  out_tie [B]: the first
+ * position whose two best scores lie within REL_TIE_MARKOV * max(1, |best|)
+ * (K if none): the draws from there on are not decided by fp64 alone.
+ */
+typedef struct {
+    double val;
+    int v;
+} mcand_t;
+
+static int mcand_desc(const void *pa, const void *pb) {
+    const mcand_t *a = (const mcand_t *)pa, *b = (const mcand_t *)pb;
+    if (a->val > b->val) return -1;
+    if (a->val < b->val) return 1;
+    return a->v < b->v ? -1 : (a->v > b->v);
+}
+
+int oracle_markov_draft(const void *base, int dtype, int B, int K, int V, int64_t ld_row, const int32_t *anchor,
+                        const void *emb, const void *proj, int rank, const float *temperature, uint64_t seed,
+                        uint64_t step, int topk, int32_t *out_tokens, double *out_logits, int32_t *out_status,
+                        int32_t *out_tie, int nthreads) {
+    int b;
+    if (B < 0 || K < 0 || V <= 0 || rank <= 0 || ld_row < V || topk < 0 || !anchor || !emb || !proj ||
+        !out_tokens || !out_status || !out_tie)
+        return 1;
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+    for (b = 0; b < B; ++b) {
+        double *u = (double *)malloc(sizeof(double) * (size_t)V);
+        double *z = (double *)malloc(sizeof(double) * (size_t)V);
+        double *h = (double *)malloc(sizeof(double) * (size_t)rank);
+        mcand_t *cs = (mcand_t *)malloc(sizeof(mcand_t) * (size_t)V);
+        const double T = temperature ? (double)temperature[b] : 0.0;
+        int st = ST_OK, k, v, j, prev = anchor[b], tie = K;
+        if (prev < 0 || prev >= V) st = ST_BAD_TOKEN;
+        if (st == ST_OK && (!(T >= 0.0) || isinf(T))) st = ST_BAD_T;
+        for (k = 0; k < K && st == ST_OK; ++k) {
+            const int ncand = (topk == 0 || topk > V) ? V : topk;
+            double best = -INFINITY, second = -INFINITY;
+            int bi = -1, bad = 0;
+            load_row(base, dtype, (int64_t)b * K + k, ld_row, V, u);
+            for (j = 0; j < rank; ++j) h[j] = decode(emb, dtype, (int64_t)prev * rank + j);
+            for (v = 0; v < V; ++v) z[v] = -INFINITY;
+            if (ncand == V) {
+                for (v = 0; v < V; ++v) cs[v].v = v;
+            } else {
+                for (v = 0; v < V; ++v) {
+                    cs[v].val = isnan(u[v]) ? INFINITY : u[v]; /* a NaN is a candidate: it must be seen */
+                    cs[v].v = v;
+                }
+                qsort(cs, (size_t)V, sizeof(mcand_t), mcand_desc);
+            }
+            for (v = 0; v < ncand; ++v) {
+                const int c = cs[v].v;
+                double bias = 0.0;
+                for (j = 0; j < rank; ++j) bias += h[j] * decode(proj, dtype, (int64_t)c * rank + j);
+                z[c] = u[c] + bias;
+            }
+            if (out_logits)
+                for (v = 0; v < V; ++v) out_logits[((int64_t)b * K + k) * V + v] = z[v];
+            for (v = 0; v < V; ++v) {
+                double sc;
+                if (isnan(z[v]) || z[v] == INFINITY) bad = 1;
+                if (!(z[v] > -INFINITY)) continue;
+                sc = (T == 0.0) ? z[v] : z[v] / T + oracle_gumbel(oracle_rand_word(seed, step, b, k, 3, v));
+                if (sc > best) {
+                    second = best;
+                    best = sc;
+                    bi = v;
+                } else if (sc > second) {
+                    second = sc;
+                }
+            }
+            if (bad || bi < 0) {
+                st = ST_NONFINITE;
+                break;
+            }
+            if (tie == K && best - second < REL_TIE_MARKOV * (fabs(best) > 1.0 ? fabs(best) : 1.0)) tie = k;
+            out_tokens[(int64_t)b * K + k] = bi;
+            prev = bi;
+        }
+        if (st != ST_OK)
+            for (k = 0; k < K; ++k) out_tokens[(int64_t)b * K + k] = -1;
+        out_status[b] = st;
+        out_tie[b] = st == ST_OK ? tie : K;
+        free(u);
+        free(z);
+        free(h);
+        free(cs);
+    }
     return 0;
 }
