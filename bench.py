@@ -308,6 +308,27 @@ def run_ours(args) -> None:
     assert int((st != 0).sum()) == 0, "a request reported a non-zero status (early exit)"
     ee_rows = int((2 * torch.clamp(acc + 1, max=K) + (acc == K).to(torch.int32)).sum().item())
 
+    # Markov-head drafting of the same block shape (B, K, V), rank 256, random
+    # factors: the draft-side step before verify, timed beside the headline.
+    mk = synth.markov(0, B=B, K=K, V=V, r=256, dtype=t.dtype)
+    mk_dev = {n: mk[n].to(dev) for n in ("base", "anchor", "emb", "proj", "temperature")}
+    mk_tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+    mk_z = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    mk_st = torch.empty(B, dtype=torch.int32, device=dev)
+    mk_ev = []
+    for i in range(args.warmup + min(args.steps, 10)):
+        flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        binding.spec_markov_draft(mk_dev["base"], mk_dev["anchor"], mk_dev["emb"], mk_dev["proj"],
+                                  mk_dev["temperature"], 6, i, mk_tok, mk_z, mk_st, stream)
+        e1.record(stream)
+        mk_ev.append((e0, e1))
+    torch.cuda.synchronize()
+    mk_ms = statistics.mean(a.elapsed_time(b) for a, b in mk_ev[args.warmup:])
+    assert int((mk_st != 0).sum()) == 0, "a Markov draft request reported a non-zero status"
+    del mk_dev, mk_z
+
     # end to end: pinned host inputs -> device, verify, outputs -> host, every step
     th, dh = t.cpu().pin_memory(), d.cpu().pin_memory()
     xh, Th = x.cpu().pin_memory(), T.cpu().pin_memory()
@@ -361,6 +382,8 @@ def run_ours(args) -> None:
             "early_exit": {"ms_per_step": statistics.mean(ee_ms),
                            "value": world * verified / (statistics.mean(ee_ms) * 1e-3), "unit": UNIT,
                            "rows_read_per_step": ee_rows, "rows_full_scan": B * (2 * K + 1)},
+            "markov_draft": {"ms_per_call": mk_ms, "positions": K, "rank": 256,
+                             "draft_tokens_per_s": world * B * K / (mk_ms * 1e-3)},
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -79,6 +79,7 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
 #define SPEC_MAX_BATCH 8192        /* B                                   */
 #define SPEC_MAX_DRAFTS 255        /* Kmax                                */
 #define SPEC_MAX_SCHED_ITEMS 8192  /* B * Kmax for the scheduler          */
+#define SPEC_MARKOV_MAX_RANK 512   /* rank r of the Markov head's factors (a multiple of 4) */
 
 /*
  * Bytes of device workspace that spec_verify_greedy / spec_verify_sample need for
@@ -187,6 +188,39 @@ int spec_verify_sample_early_exit(const void *target, const void *draft, int dty
 int spec_verify_greedy_early_exit(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
                                   const int32_t *draft_tokens, const int32_t *num_draft, int32_t *out_tokens,
                                   int32_t *out_accepted, int32_t *out_status, void *cuda_stream);
+
+/*
+ * Markov-head drafting of one block ("Accelerating Large-Model Inference ...
+ * DSpark", drafting-engine table, layer 2: the backbone's logits are corrected left
+ * to right by a low-rank bias set by the token chosen at the previous position;
+ * "DSpark paper review" Sec. 4.1: the head runs once per position, default rank
+ * 256).  For request b and positions k = 0 .. K-1 in order:
+ *   prev = anchor[b] (k = 0) or x_{k-1};
+ *   z_v  = base[b, k, v] + sum_j emb[prev, j] * proj[v, j];
+ *   x_k  = argmax_v z_v (temperature NULL or T_b = 0; lowest v on ties), else the
+ *          Gumbel-max draw argmax_v z_v / T_b + g_v with noise purpose 3 at row k.
+ * z is computed in fp32 (the products of the stored factors are exact).
+ *
+ *  base         [B, K, ld_row] backbone logits of type dtype
+ *  anchor       [B] int32: the token before the block
+ *  emb, proj    [V, rank] row-major factors of type dtype (row prev of emb, row v of
+ *               proj); rank a multiple of 4, at most SPEC_MARKOV_MAX_RANK
+ *  temperature  [B] float, or NULL for greedy drafting
+ *  out_tokens   [B, K] int32 draft tokens
+ *  out_logits   [B, K, V] float corrected logits z (the draft distribution that
+ *               verify needs is softmax(z / T)); rows of a failed request are
+ *               unspecified
+ *  out_status   [B]: 0, 1 (anchor outside [0, V)), 3 (bad temperature) or 4 (a
+ *               corrected row with NaN or +inf, or all -inf); a failed request has
+ *               every token -1
+ * All pointers are device pointers owned by the caller.  2 K kernel launches on
+ * the stream, no host synchronisation, no workspace.  Host-checkable errors return
+ * before any launch.
+ */
+int spec_markov_draft(const void *base, int dtype, int B, int K, int V, int64_t ld_row, const int32_t *anchor,
+                      const void *emb, const void *proj, int rank, const float *temperature, uint64_t seed,
+                      uint64_t step, int32_t *out_tokens, float *out_logits, int32_t *out_status,
+                      void *cuda_stream);
 
 /*
  * spec_verify_sample without a workspace argument.  The method on the pages has no

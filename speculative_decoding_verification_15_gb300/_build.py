@@ -13,7 +13,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libspecverify.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["verify.cu", "schedule.cu"]
+SOURCES = ["verify.cu", "schedule.cu", "markov.cu"]
 HEADERS = ["spec_common.cuh"]
 
 NVCC_FLAGS = [

@@ -106,6 +106,20 @@ def verify_greedy_early_exit(target, draft_tokens, num_draft=None, stream=None) 
     return out
 
 
+def markov_draft(base, anchor, emb, proj, temperature=None, seed: int = 0, step: int = 0, stream=None) -> dict:
+    """Markov-head drafting of one block: tokens [B, K], corrected logits [B, K, V]
+    (float32) and status [B]."""
+    dev = base.device
+    B, K, V = base.shape
+    out = dict(tokens=torch.empty((B, K), dtype=torch.int32, device=dev),
+               logits=torch.empty((B, K, V), dtype=torch.float32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    T = None if temperature is None else temperature.to(device=dev, dtype=torch.float32).contiguous()
+    binding.spec_markov_draft(base, _as_i32(anchor, dev), emb, proj, T, seed, step, out["tokens"], out["logits"],
+                              out["status"], stream)
+    return out
+
+
 def verify_sample_flat(target, draft, cu_draft, draft_tokens, temperature, seed: int, step: int, Kmax: int,
                        stream=None) -> dict:
     """Flattened ragged layout (no padding rows): target [sum_b (k_b + 1), V], draft

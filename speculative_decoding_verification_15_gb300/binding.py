@@ -69,6 +69,8 @@ def load(path: str | None = None):
         lib.spec_verify_sample_early_exit.restype = I32
         lib.spec_verify_greedy_early_exit.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, P, P, P]
         lib.spec_verify_greedy_early_exit.restype = I32
+        lib.spec_markov_draft.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, I32, P, U64, U64, P, P, P, P]
+        lib.spec_markov_draft.restype = I32
         lib.spec_verify_sample_noalloc.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P,
                                                    P, P, P]
         lib.spec_verify_sample_noalloc.restype = I32
@@ -260,6 +262,34 @@ def spec_verify_greedy_early_exit(target, draft_tokens, num_draft, out_tokens, o
                                            _ptr(out_status), _stream_handle(stream))
     if rc != SPEC_OK:
         raise SpecError("spec_verify_greedy_early_exit", rc, lib)
+
+
+def spec_markov_draft(base, anchor, emb, proj, temperature, seed: int, step: int, out_tokens, out_logits,
+                      out_status, stream=None) -> None:
+    """Markov-head drafting of one block.  base [B, K, V] (or a [B, K, ld] view with
+    unit stride over V), emb / proj [V, r] contiguous in base's dtype, anchor [B]
+    int32, temperature [B] float32 or None; outputs tokens [B, K] int32, logits
+    [B, K, V] float32, status [B] int32."""
+    lib = load()
+    B, K = base.shape[0], base.shape[1]
+    _, V, ld = _logits_layout(base, K) if K > 0 else (B, base.shape[2], base.shape[2])
+    dev = base.device
+    if emb.dtype != base.dtype or proj.dtype != base.dtype:
+        raise TypeError("the factors must have the base logits' dtype")
+    if emb.dim() != 2 or emb.shape[0] != V or proj.shape != emb.shape or not emb.is_contiguous() \
+            or not proj.is_contiguous():
+        raise ValueError("emb and proj must be contiguous [V, r]")
+    _need(anchor, "anchor", torch.int32, (B,), dev)
+    if temperature is not None:
+        _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K), dev)
+    _need(out_logits, "out_logits", torch.float32, (B, K, V), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    rc = lib.spec_markov_draft(_ptr(base), _dtype_code(base), B, K, V, ld, _ptr(anchor), _ptr(emb), _ptr(proj),
+                               emb.shape[1], _ptr(temperature), int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
+                               _ptr(out_tokens), _ptr(out_logits), _ptr(out_status), _stream_handle(stream))
+    if rc != SPEC_OK:
+        raise SpecError("spec_markov_draft", rc, lib)
 
 
 def spec_verify_sample_noalloc(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int,

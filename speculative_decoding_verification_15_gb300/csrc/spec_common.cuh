@@ -18,7 +18,10 @@ constexpr float kNegInf = -__builtin_huge_valf();
 // bounds use 17 so that rounding can never make a pruned element win.
 constexpr float kGumbelMax = 17.0f;
 
-enum Purpose : uint32_t { PURPOSE_ACCEPT = 0, PURPOSE_RESIDUAL = 1, PURPOSE_BONUS = 2 };
+enum Purpose : uint32_t { PURPOSE_ACCEPT = 0, PURPOSE_RESIDUAL = 1, PURPOSE_BONUS = 2, PURPOSE_DRAFT = 3 };
+
+// Records the CUDA error that spec_last_cuda_error() reports (host; defined in verify.cu).
+void note_cuda_error(int e);
 
 // ------------------------------------------------------------------ Philox
 __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
@@ -55,7 +58,7 @@ __device__ __forceinline__ float one_minus_u01(uint32_t w) {
 
 // Gumbel noise g = -log(-log u) from the word, accurate for u near 1 (where the
 // winners of a Gumbel-max draw come from): -log u = -log1p(-(1 - u)) with 1 - u exact.
-__device__ __noinline__ float gumbel_of_word(uint32_t w) {
+static __device__ __noinline__ float gumbel_of_word(uint32_t w) {
     const float e = -log1pf(-one_minus_u01(w));
     return -logf(e);
 }

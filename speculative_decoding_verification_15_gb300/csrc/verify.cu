@@ -2059,6 +2059,10 @@ int early_exit_impl(const void *target, const void *draft, int dtype, int B, int
 
 }  // namespace
 
+namespace specv {
+void note_cuda_error(int e) { t_last_cuda_error = e; }
+}  // namespace specv
+
 extern "C" {
 
 size_t spec_verify_workspace_size(int B, int Kmax, int V, int dtype) {

@@ -236,6 +236,26 @@ def stress(step: int = 0, B: int = 512, V: int = 151936, n_adv: int = 8) -> dict
                 B=B, K=K, V=V, dtype=torch.float32, seed=5, step=step, name="stress", kinds=kinds)
 
 
+def markov(step: int = 0, B: int = 64, K: int = 7, V: int = 151936, r: int = 256,
+           dtype: torch.dtype = torch.bfloat16, greedy_every: int = 0) -> dict:
+    """Inputs of one Markov-head drafting block: backbone logits U ~ N(0, 3^2) + Zipf,
+    factors emb ~ N(0, 0.5^2) and proj ~ N(0, 0.1^2) ([V, r]; the bias of a token
+    then has standard deviation ~0.8), anchors uniform over the vocabulary,
+    T_b ~ U[0.6, 1.0] (every greedy_every-th request greedy if greedy_every > 0).
+    Random weights: no trained head is used."""
+    g = _gen(1000 * 6 + step)
+    prior = zipf_prior(V)
+    base = _round(3.0 * torch.randn((B, K, V), generator=g, dtype=torch.float64) + prior, dtype)
+    emb = _round(0.5 * torch.randn((V, r), generator=g, dtype=torch.float64), dtype)
+    proj = _round(0.1 * torch.randn((V, r), generator=g, dtype=torch.float64), dtype)
+    anchor = torch.randint(0, V, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    temps = (0.6 + 0.4 * torch.rand(B, generator=g, dtype=torch.float64)).to(torch.float32)
+    if greedy_every > 0:
+        temps[::greedy_every] = 0.0
+    return dict(base=base, emb=emb, proj=proj, anchor=anchor, temperature=temps, B=B, K=K, V=V, r=r,
+                dtype=dtype, seed=6, step=step, name="markov")
+
+
 def as_oracle_array(x: torch.Tensor) -> np.ndarray:
     """CPU tensor -> numpy for the oracle (bf16 as uint16 bit patterns)."""
     x = x.contiguous()
