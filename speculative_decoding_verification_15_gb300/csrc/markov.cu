@@ -99,6 +99,104 @@ __global__ void __launch_bounds__(kMkThreads) markov_bias_kernel(MarkovParams p,
     }
 }
 
+// bf16 factors: the same z through bf16 tensor-core products with fp32 accumulation
+// (mma.sync m16n8k16; the products of bf16 values are exact).  One CTA per 64
+// vocabulary entries, all requests in chunks of 64: the chunk's embedding rows H
+// [64][r] and the entries' projection rows P [64][r] sit in shared memory as bf16
+// with rows padded by 8 elements (the fragment loads of a warp then hit 32
+// different banks).  Warp w owns entries 8w .. 8w+7 and all four 16-request
+// tiles; per 16-wide slice of r it loads one B fragment and four A fragments.
+constexpr int kMmCols = 64;
+constexpr int kMmReqs = 64;
+
+__host__ __device__ inline size_t mma_smem_bytes(int r) {
+    return sizeof(uint16_t) * (size_t)(kMmCols + kMmReqs) * (r + 8) + sizeof(int) * kMmReqs;
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__global__ void __launch_bounds__(kMkThreads) markov_bias_mma_kernel(MarkovParams p, int k) {
+    extern __shared__ __align__(16) uint16_t mms[];
+    const int rs = p.r + 8;  // row stride in elements (16-byte rows)
+    uint16_t *Ps = mms;                        // [64 entries][rs]
+    uint16_t *Hs = mms + (size_t)kMmCols * rs;  // [64 requests][rs]
+    int *okv = reinterpret_cast<int *>(Hs + (size_t)kMmReqs * rs);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int v0 = blockIdx.x * kMmCols;
+    const int ncol = min(kMmCols, p.V - v0);
+    const int vpr = p.r >> 3;  // 16-byte vectors per row
+    for (int i = tid; i < kMmCols * vpr; i += kMkThreads) {
+        const int c = i / vpr, q = i - c * vpr;
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (c < ncol) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.proj + (int64_t)(v0 + c) * p.r + 8 * q);
+        *reinterpret_cast<uint4 *>(Ps + c * rs + 8 * q) = x;
+    }
+    const int g = lane >> 2, t2 = (lane & 3) * 2;
+    for (int b0 = 0; b0 < p.B; b0 += kMmReqs) {
+        __syncthreads();  // Hs and okv of the previous chunk are no longer read
+        if (tid < kMmReqs) {
+            const int b = b0 + tid;
+            int ok = 0;
+            if (b < p.B) {
+                const int prev = k == 0 ? p.anchor[b] : p.tokens[(int64_t)b * p.K + k - 1];
+                ok = (prev >= 0 && prev < p.V) ? prev + 1 : 0;  // 1 + the row to gather, 0: none
+            }
+            okv[tid] = ok;
+        }
+        __syncthreads();
+        for (int i = tid; i < kMmReqs * vpr; i += kMkThreads) {
+            const int m = i / vpr, q = i - m * vpr;
+            const int ok = okv[m];
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (ok) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.emb + (int64_t)(ok - 1) * p.r + 8 * q);
+            *reinterpret_cast<uint4 *>(Hs + m * rs + 8 * q) = x;
+        }
+        __syncthreads();
+        float acc[4][4];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+        const uint16_t *pb = Ps + (warp * 8 + g) * rs + t2;
+        for (int kk = 0; kk < p.r; kk += 16) {
+            uint32_t bf[2];
+            bf[0] = *reinterpret_cast<const uint32_t *>(pb + kk);
+            bf[1] = *reinterpret_cast<const uint32_t *>(pb + kk + 8);
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const uint16_t *pa = Hs + (mt * 16 + g) * rs + kk + t2;
+                uint32_t af[4];
+                af[0] = *reinterpret_cast<const uint32_t *>(pa);
+                af[1] = *reinterpret_cast<const uint32_t *>(pa + 8 * rs);
+                af[2] = *reinterpret_cast<const uint32_t *>(pa + 8);
+                af[3] = *reinterpret_cast<const uint32_t *>(pa + 8 * rs + 8);
+                mma_bf16_16816(acc[mt], af, bf);
+            }
+        }
+        // C fragment: rows (requests) g and g + 8 of each tile, entries t2, t2 + 1 of the warp's 8
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = mt * 16 + g + (e >= 2 ? 8 : 0);
+                const int n = warp * 8 + t2 + (e & 1);
+                const int b = b0 + m;
+                if (b < p.B && n < ncol) {
+                    const int64_t row = (int64_t)b * p.K + k;
+                    const int v = v0 + n;
+                    p.z[row * p.V + v] = okv[m] ? load_logit(p.base, p.dtype, row * p.ld_row + v) + acc[mt][e]
+                                                : __int_as_float(0x7fc00000);
+                }
+            }
+    }
+}
+
 // One CTA per request.  k = -1: the status of a block with no positions (K = 0).
 __global__ void __launch_bounds__(kMkSampleThreads) markov_sample_kernel(MarkovParams p, int k) {
     __shared__ float red_s[kMkSampleThreads / 32];
@@ -182,12 +280,26 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
             return SPEC_ECUDA;
         }
     }
+    // bf16 factors with 16-byte rows (r a multiple of 16, aligned bases): tensor cores
+    const bool mma = p.dtype == SPEC_BF16 && (p.r % 16) == 0 && ((uintptr_t)p.emb % 16) == 0 &&
+                     ((uintptr_t)p.proj % 16) == 0;
+    const size_t msmem = mma_smem_bytes(p.r);
+    if (mma && msmem > 48 * 1024) {
+        e = cudaFuncSetAttribute(markov_bias_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+        if (e != cudaSuccess) {
+            note_cuda_error((int)e);
+            return SPEC_ECUDA;
+        }
+    }
     if (p.K == 0) {
         markov_sample_kernel<<<p.B, kMkSampleThreads, 0, stream>>>(p, -1);
     } else {
-        const int nb = (p.V + kMkCols - 1) / kMkCols;
+        const int nb = (p.V + kMkCols - 1) / kMkCols, nbm = (p.V + kMmCols - 1) / kMmCols;
         for (int k = 0; k < p.K; ++k) {
-            markov_bias_kernel<<<nb, kMkThreads, smem, stream>>>(p, k);
+            if (mma)
+                markov_bias_mma_kernel<<<nbm, kMkThreads, msmem, stream>>>(p, k);
+            else
+                markov_bias_kernel<<<nb, kMkThreads, smem, stream>>>(p, k);
             markov_sample_kernel<<<p.B, kMkSampleThreads, 0, stream>>>(p, k);
         }
     }
