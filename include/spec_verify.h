@@ -54,7 +54,7 @@ typedef enum {
     SPEC_OK = 0,
     SPEC_EINVAL = 1,        /* bad argument (null pointer, size out of range) */
     SPEC_ECUDA = 2,         /* a CUDA runtime call or launch failed           */
-    SPEC_EUNSUPPORTED = 3,  /* valid but outside what this build supports     */
+    SPEC_EUNSUPPORTED = 3,  /* valid but outside what this library supports   */
     SPEC_EWORKSPACE = 4,    /* workspace pointer null or too small            */
     SPEC_ESCRATCH = 5       /* sizes need more than the fixed scratch of
                                spec_verify_sample_noalloc                    */
@@ -75,7 +75,7 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
  * A request with a non-zero status has out_accepted[b] = 0, every token -1 and
  * out_p / out_q -1. */
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define SPEC_MAX_BATCH 8192        /* B                                   */
 #define SPEC_MAX_DRAFTS 255        /* Kmax                                */
 #define SPEC_MAX_SCHED_ITEMS 8192  /* B * Kmax for the scheduler          */
