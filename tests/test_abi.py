@@ -77,3 +77,64 @@ def test_scheduler_host_argument_errors(lib):
 def test_error_strings(lib):
     assert lib.spec_error_string(0) == b"ok"
     assert b"workspace" in lib.spec_error_string(4)
+
+
+def test_early_exit_host_argument_errors(lib):
+    """The early-exit calls check their arguments as the two-kernel calls do."""
+    EINVAL, EUNSUP = 1, 3
+    P = ctypes.c_void_p(16)
+
+    def ee(**kw):
+        a = dict(target=P, draft=P, dtype=0, B=2, Kmax=3, V=100, ld=100, x=P, nd=None, T=P, tok=P, acc=P, st=P)
+        a.update(kw)
+        return lib.spec_verify_sample_early_exit(a["target"], a["draft"], a["dtype"], a["B"], a["Kmax"], a["V"],
+                                                 a["ld"], a["x"], a["nd"], a["T"], 0, 0, a["tok"], a["acc"], None,
+                                                 None, a["st"], None)
+
+    assert ee(B=0) == 0
+    assert ee(B=-1) == EINVAL and ee(V=0) == EINVAL and ee(ld=99) == EINVAL and ee(dtype=2) == EINVAL
+    assert ee(Kmax=256) == EUNSUP and ee(B=8193) == EUNSUP
+    assert ee(target=None) == EINVAL and ee(tok=None) == EINVAL and ee(st=None) == EINVAL
+    assert ee(x=None) == EINVAL and ee(T=None) == EINVAL and ee(draft=None) == EINVAL
+    assert ee(target=ctypes.c_void_p(17)) == EINVAL  # bf16 rows need 2-byte alignment
+    assert lib.spec_verify_greedy_early_exit(None, 0, 1, 1, 10, 10, P, None, P, P, P, None) == EINVAL
+    assert lib.spec_verify_greedy_early_exit(P, 0, 0, 1, 10, 10, None, None, None, None, None, None) == 0
+
+
+def test_flat_host_argument_errors(lib):
+    EINVAL = 1
+    P = ctypes.c_void_p(16)
+    # no offsets
+    assert lib.spec_verify_greedy_flat(P, 0, 2, 3, 100, 100, None, P, P, P, P, P, 1 << 30, None) == EINVAL
+    assert lib.spec_verify_sample_flat(P, P, 0, 2, 3, 100, 100, None, P, P, 0, 0, P, P, None, None, P, P, 1 << 30,
+                                       None) == EINVAL
+    assert lib.spec_verify_greedy_flat(P, 0, 0, 3, 100, 100, None, None, None, None, None, None, 0, None) == 0
+
+
+def test_markov_host_argument_errors(lib):
+    """spec_markov_draft rejects bad sizes, ranks, pointers and alignment before any launch."""
+    EINVAL, EUNSUP = 1, 3
+    P = ctypes.c_void_p(16)
+
+    def mk(**kw):
+        a = dict(base=P, dtype=0, B=2, K=3, V=100, ld=100, anchor=P, emb=P, proj=P, r=8, T=P, tok=P, z=P, st=P)
+        a.update(kw)
+        return lib.spec_markov_draft(a["base"], a["dtype"], a["B"], a["K"], a["V"], a["ld"], a["anchor"], a["emb"],
+                                     a["proj"], a["r"], a["T"], 0, 0, a["tok"], a["z"], a["st"], None)
+
+    assert mk(B=0) == 0
+    assert mk(B=-1) == EINVAL and mk(K=-1) == EINVAL and mk(V=0) == EINVAL and mk(ld=99) == EINVAL
+    assert mk(r=0) == EINVAL and mk(dtype=5) == EINVAL
+    assert mk(r=513) == EUNSUP and mk(r=6) == EUNSUP  # at most 512, a multiple of 4
+    assert mk(B=8193) == EUNSUP and mk(K=256) == EUNSUP
+    assert mk(anchor=None) == EINVAL and mk(emb=None) == EINVAL and mk(proj=None) == EINVAL
+    assert mk(st=None) == EINVAL and mk(base=None) == EINVAL and mk(tok=None) == EINVAL and mk(z=None) == EINVAL
+    assert mk(emb=ctypes.c_void_p(17)) == EINVAL and mk(z=ctypes.c_void_p(18)) == EINVAL
+
+
+def test_threshold_host_argument_errors(lib):
+    EINVAL = 1
+    P = ctypes.c_void_p(16)
+    assert lib.spec_schedule_threshold(P, None, 4, 4, ctypes.c_float(float("nan")), P, None) == EINVAL
+    assert lib.spec_schedule_threshold(None, None, 4, 4, ctypes.c_float(0.5), P, None) == EINVAL
+    assert lib.spec_schedule_threshold(P, None, 0, 4, ctypes.c_float(0.5), None, None) == 0
