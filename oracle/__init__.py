@@ -61,7 +61,7 @@ def _load():
         lib.oracle_gumbel_sample.argtypes = [P, I32, U64, U64, I32, I32, I32]
         lib.oracle_gumbel_sample.restype = I32
         lib.oracle_verify_sample.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64,
-                                             P, P, P, P, P, P, P, I32]
+                                             P, P, P, P, P, P, P, P, I32]
         lib.oracle_verify_sample.restype = I32
         lib.oracle_verify_greedy.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, P, P, I32]
         lib.oracle_verify_greedy.restype = I32
@@ -158,6 +158,9 @@ def verify_sample(target, draft, draft_tokens, num_draft, temperature, seed: int
     draft_tokens [B, K] int32; num_draft [B] int32 or None; temperature [B] float32.
     early_exit: read rows in position order and stop at the first rejection (status 4
     only for rows read; p and q stay -1 past the first rejected position).
+    Near-tie outputs: flags [B] (bits FL_*), flag_pos [B] (first scanned position whose
+    acceptance test is a threshold near-tie, -1 if none) and gap [B] (top-2 gap of the
+    Gumbel draw).
     """
     lib = _load()
     t, dt = _logit_array(target)
@@ -171,13 +174,13 @@ def verify_sample(target, draft, draft_tokens, num_draft, temperature, seed: int
     T = _c(temperature, np.float32)
     out = dict(tokens=np.full((B, K + 1), -1, np.int32), accepted=np.zeros(B, np.int32),
                p=np.full((B, K), -1.0), q=np.full((B, K), -1.0), status=np.zeros(B, np.int32),
-               flags=np.zeros(B, np.int32), gap=np.zeros(B))
+               flags=np.zeros(B, np.int32), flag_pos=np.full(B, -1, np.int32), gap=np.zeros(B))
     fn = lib.oracle_verify_sample_early_exit if early_exit else lib.oracle_verify_sample
     rc = fn(_ptr(t), _ptr(d), dt, B, K, V, V, _ptr(x), _ptr(nd), _ptr(T),
                                   seed & (2**64 - 1), step & (2**64 - 1),
                                   _ptr(out["tokens"]), _ptr(out["accepted"]), _ptr(out["p"]),
                                   _ptr(out["q"]), _ptr(out["status"]), _ptr(out["flags"]),
-                                  _ptr(out["gap"]), nthreads)
+                                  _ptr(out["flag_pos"]), _ptr(out["gap"]), nthreads)
     assert rc == 0
     return out
 

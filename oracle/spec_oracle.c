@@ -226,6 +226,7 @@ typedef struct {
     const float *temperature; /* NULL: greedy for every request */
     uint64_t seed, step;
     int32_t *out_tokens, *out_accepted, *out_status, *out_flags;
+    int32_t *out_flag_pos; /* first scanned position with a threshold near-tie, -1 if none */
     double *out_p, *out_q, *out_gap;
     /* early exit: read the rows position by position and stop at the first
      * rejection [PPR, ALX]; only rows read are checked for non-finite values and
@@ -249,6 +250,7 @@ static void fail_request(const verify_args *a, int b, int status) {
     a->out_status[b] = status;
     a->out_accepted[b] = 0;
     if (a->out_flags) a->out_flags[b] = 0;
+    if (a->out_flag_pos) a->out_flag_pos[b] = -1;
     if (a->out_gap) a->out_gap[b] = INFINITY;
 }
 
@@ -258,7 +260,7 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
     int32_t *tok = a->out_tokens + (int64_t)b * K1;
     const int32_t *x = a->draft_tokens + (int64_t)b * a->Kmax;
     int kb = a->num_draft ? a->num_draft[b] : a->Kmax;
-    int i, v, status = ST_OK, greedy, A = 0, flags = 0;
+    int i, v, status = ST_OK, greedy, A = 0, flags = 0, flag_pos = -1;
     double T = 0.0;
     double min_gap = INFINITY;
 
@@ -292,6 +294,7 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
         }
     }
     a->out_status[b] = status;
+    if (a->out_flag_pos) a->out_flag_pos[b] = -1;
     if (status) {
         a->out_accepted[b] = 0;
         if (a->out_flags) a->out_flags[b] = 0;
@@ -342,7 +345,10 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
             u = oracle_u01(oracle_rand_word(a->seed, a->step, b, i, 0, 0));
             if (Q > 0.0) {
                 ratio = P / Q;
-                if (fabs(u - ratio) < REL_TIE * ratio) flags |= FL_THRESH;
+                if (fabs(u - ratio) < REL_TIE * ratio) {
+                    flags |= FL_THRESH;
+                    if (flag_pos < 0) flag_pos = i;
+                }
                 if (u < ratio) { tok[i] = x[i]; ++A; continue; }
             } else if (P > 0.0) {
                 tok[i] = x[i]; ++A; continue;
@@ -403,6 +409,7 @@ static void verify_one(const verify_args *a, int b, double *xt, double *xd, doub
     }
     a->out_accepted[b] = A;
     if (a->out_flags) a->out_flags[b] = flags;
+    if (a->out_flag_pos) a->out_flag_pos[b] = flag_pos;
     if (a->out_gap) a->out_gap[b] = min_gap;
 }
 
@@ -431,14 +438,17 @@ static int run_verify(const verify_args *a, int nthreads) {
  * (b*(Kmax+1)+i)*ld_row, draft row (b,i) at (b*Kmax+i)*ld_row, V contiguous.
  * temperature[b] == 0 marks a greedy request (reading).  out_tokens [B,Kmax+1]
  * (-1 = unused), out_accepted [B], out_p/out_q [B,Kmax] (-1 where not computed),
- * out_status [B], out_flags [B] (near-tie bits), out_gap [B] (top-2 gap of the
- * Gumbel draw, +inf if none).  nthreads: OpenMP threads over requests.
+ * out_status [B], out_flags [B] (near-tie bits), out_flag_pos [B] (the first
+ * scanned position with a threshold near-tie, -1 if none; may be NULL), out_gap [B]
+ * (top-2 gap of the Gumbel draw, +inf if none).  nthreads: OpenMP threads over
+ * requests.
  */
 static int verify_sample_args(const void *target, const void *draft, int dtype, int B, int Kmax, int V,
                               int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
                               const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
                               int32_t *out_accepted, double *out_p, double *out_q, int32_t *out_status,
-                              int32_t *out_flags, double *out_gap, int nthreads, int early_exit) {
+                              int32_t *out_flags, int32_t *out_flag_pos, double *out_gap, int nthreads,
+                              int early_exit) {
     verify_args a;
     memset(&a, 0, sizeof a);
     a.early_exit = early_exit;
@@ -446,7 +456,8 @@ static int verify_sample_args(const void *target, const void *draft, int dtype, 
     a.ld_row = ld_row; a.draft_tokens = draft_tokens; a.num_draft = num_draft;
     a.temperature = temperature; a.seed = seed; a.step = step;
     a.out_tokens = out_tokens; a.out_accepted = out_accepted; a.out_status = out_status;
-    a.out_flags = out_flags; a.out_p = out_p; a.out_q = out_q; a.out_gap = out_gap;
+    a.out_flags = out_flags; a.out_flag_pos = out_flag_pos; a.out_p = out_p; a.out_q = out_q;
+    a.out_gap = out_gap;
     return run_verify(&a, nthreads);
 }
 
@@ -454,10 +465,10 @@ int oracle_verify_sample(const void *target, const void *draft, int dtype, int B
                          int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
                          const float *temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
                          int32_t *out_accepted, double *out_p, double *out_q, int32_t *out_status,
-                         int32_t *out_flags, double *out_gap, int nthreads) {
+                         int32_t *out_flags, int32_t *out_flag_pos, double *out_gap, int nthreads) {
     return verify_sample_args(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, temperature,
                               seed, step, out_tokens, out_accepted, out_p, out_q, out_status, out_flags,
-                              out_gap, nthreads, 0);
+                              out_flag_pos, out_gap, nthreads, 0);
 }
 
 /* The same with early exit: rows are read in position order and reading stops at
@@ -468,10 +479,11 @@ int oracle_verify_sample_early_exit(const void *target, const void *draft, int d
                                     int64_t ld_row, const int32_t *draft_tokens, const int32_t *num_draft,
                                     const float *temperature, uint64_t seed, uint64_t step,
                                     int32_t *out_tokens, int32_t *out_accepted, double *out_p, double *out_q,
-                                    int32_t *out_status, int32_t *out_flags, double *out_gap, int nthreads) {
+                                    int32_t *out_status, int32_t *out_flags, int32_t *out_flag_pos,
+                                    double *out_gap, int nthreads) {
     return verify_sample_args(target, draft, dtype, B, Kmax, V, ld_row, draft_tokens, num_draft, temperature,
                               seed, step, out_tokens, out_accepted, out_p, out_q, out_status, out_flags,
-                              out_gap, nthreads, 1);
+                              out_flag_pos, out_gap, nthreads, 1);
 }
 
 /* Greedy verify for a batch (draft logits are never read). */
@@ -703,7 +715,24 @@ int oracle_schedule_verify_len_stale(const float *conf_stale, const float *conf,
 /* ------------------------------------------------------------------------- */
 /* Markov-head drafting [PPR2], [VBK] Sec. 4.1, [MTL]                         */
 /* ------------------------------------------------------------------------- */
-#define REL_TIE_MARKOV 1e-3 /* near-tie band of the draw: covers an fp32 rank-256 dot product divided by T */
+/*
+ * Near-tie band of a draw.  An fp32 implementation forms bias_v as a sum of r
+ * products and adds it to the base logit; the products of the stored factors are
+ * exact (bf16 x bf16) or carry one rounding (fp32), and a tensor-core style sum
+ * aligns and truncates its terms, so |error| <= r * 2^-22 * S_v with
+ * S_v = sum_j |emb[prev, j] * proj[v, j]| covers any summation order and rounding
+ * mode; adding the base costs |z_v| 2^-24.  The draw then scales by 1 / T (two
+ * roundings), adds the fp32 Gumbel noise (a few ulp of |g|, bounded by 8 ulp here)
+ * and rounds the sum (|score| 2^-24).  Position k is flagged when the best entry and
+ * some other entry are closer than the sum of their two bounds: only there can an
+ * fp32 score order differ from the exact one (an exact tie, gap 0, counts too).
+ */
+static double markov_score_bound(double S, double z, double T, double g, double score, int rank) {
+    const double u = 1.0 / 16777216.0;
+    const double ez = (double)rank * 4.0 * u * S + fabs(z) * u;
+    if (T == 0.0) return ez;
+    return ez / T + fabs(z / T) * 2.0 * u + fabs(g) * 8.0 * u + fabs(score) * u;
+}
 
 /*
  * Semi-autoregressive drafting of one block.  For request b and positions
@@ -725,8 +754,9 @@ int oracle_schedule_verify_len_stale(const float *conf_stale, const float *conf,
  * non-zero status has every token -1.
  * out_logits [B, K, V] (may be NULL): the corrected logits z (the draft
  * distribution the verify step needs is softmax(z / T)).  out_tie [B]: the first
- * position whose two best scores lie within REL_TIE_MARKOV * max(1, |best|)
- * (K if none): the draws from there on are not decided by fp64 alone.
+ * position where the best score and another lie within the sum of their fp32 error
+ * bounds (markov_score_bound; K if none): the draws from there on are not decided
+ * by fp64 alone.
  */
 typedef struct {
     double val;
@@ -754,6 +784,9 @@ int oracle_markov_draft(const void *base, int dtype, int B, int K, int V, int64_
         double *u = (double *)malloc(sizeof(double) * (size_t)V);
         double *z = (double *)malloc(sizeof(double) * (size_t)V);
         double *h = (double *)malloc(sizeof(double) * (size_t)rank);
+        double *sabs = (double *)malloc(sizeof(double) * (size_t)V);  /* S_v of markov_score_bound */
+        double *scv = (double *)malloc(sizeof(double) * (size_t)V);   /* score of every entry */
+        double *gv = (double *)malloc(sizeof(double) * (size_t)V);    /* its noise (0 when greedy) */
         mcand_t *cs = (mcand_t *)malloc(sizeof(mcand_t) * (size_t)V);
         const double T = temperature ? (double)temperature[b] : 0.0;
         int st = ST_OK, k, v, j, prev = anchor[b], tie = K;
@@ -775,19 +808,29 @@ int oracle_markov_draft(const void *base, int dtype, int B, int K, int V, int64_
                 }
                 qsort(cs, (size_t)V, sizeof(mcand_t), mcand_desc);
             }
+            for (v = 0; v < V; ++v) sabs[v] = 0.0;
             for (v = 0; v < ncand; ++v) {
                 const int c = cs[v].v;
-                double bias = 0.0;
-                for (j = 0; j < rank; ++j) bias += h[j] * decode(proj, dtype, (int64_t)c * rank + j);
+                double bias = 0.0, sa = 0.0;
+                for (j = 0; j < rank; ++j) {
+                    const double t = h[j] * decode(proj, dtype, (int64_t)c * rank + j);
+                    bias += t;
+                    sa += fabs(t);
+                }
                 z[c] = u[c] + bias;
+                sabs[c] = sa;
             }
             if (out_logits)
                 for (v = 0; v < V; ++v) out_logits[((int64_t)b * K + k) * V + v] = z[v];
             for (v = 0; v < V; ++v) {
                 double sc;
+                scv[v] = -INFINITY;
+                gv[v] = 0.0;
                 if (isnan(z[v]) || z[v] == INFINITY) bad = 1;
                 if (!(z[v] > -INFINITY)) continue;
-                sc = (T == 0.0) ? z[v] : z[v] / T + oracle_gumbel(oracle_rand_word(seed, step, b, k, 3, v));
+                if (T != 0.0) gv[v] = oracle_gumbel(oracle_rand_word(seed, step, b, k, 3, v));
+                sc = (T == 0.0) ? z[v] : z[v] / T + gv[v];
+                scv[v] = sc;
                 if (sc > best) {
                     second = best;
                     best = sc;
@@ -796,11 +839,18 @@ int oracle_markov_draft(const void *base, int dtype, int B, int K, int V, int64_
                     second = sc;
                 }
             }
+            (void)second;
             if (bad || bi < 0) {
                 st = ST_NONFINITE;
                 break;
             }
-            if (tie == K && best - second < REL_TIE_MARKOV * (fabs(best) > 1.0 ? fabs(best) : 1.0)) tie = k;
+            if (tie == K) {
+                const double eb = markov_score_bound(sabs[bi], z[bi], T, gv[bi], best, rank);
+                for (v = 0; v < V && tie == K; ++v)
+                    if (v != bi && scv[v] > -INFINITY &&
+                        best - scv[v] <= eb + markov_score_bound(sabs[v], z[v], T, gv[v], scv[v], rank))
+                        tie = k;
+            }
             out_tokens[(int64_t)b * K + k] = bi;
             prev = bi;
         }
@@ -811,6 +861,9 @@ int oracle_markov_draft(const void *base, int dtype, int B, int K, int V, int64_
         free(u);
         free(z);
         free(h);
+        free(sabs);
+        free(scv);
+        free(gv);
         free(cs);
     }
     return 0;

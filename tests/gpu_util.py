@@ -37,24 +37,61 @@ def run_oracle_sample(batch: dict, seed: int, step: int, nthreads: int = 8) -> d
 
 
 def compare_sample(gpu: dict, ref: dict, temperature: np.ndarray, num_draft=None, K=None) -> dict:
-    """Statuses everywhere, accepted lengths and tokens on every request the oracle
-    does not flag as a near-tie (greedy requests: always), p/q within P_ATOL."""
+    """Compare one batch of the CUDA path with the oracle, request by request.
+
+    The benchmark spec's parity rule: greedy requests bit-exact; sampling requests
+    identical in accepted length and tokens except at a near-tie, where the
+    threshold gap (bit 1) or the top-2 Gumbel gap (bit 2) is below 1e-5 relative,
+    or where the residual has no support (bit 4, reachable only by rounding).
+    What a near-tie leaves open is only what follows it:
+      - bit 1 at position f: drafts 0 .. f-1 are still accepted by both and their
+        tokens equal (the decision at f and everything after may differ);
+      - bit 2 or 4 only: the accepted length and the accepted drafts are equal;
+        the drawn token may differ.
+    Bit 8 (the residual's conditioning band) is counted, never excluded: a request
+    carrying only bit 8 must match exactly.  Statuses match everywhere; p/q match
+    within P_ATOL wherever both sides computed them.  Returns the counts.
+    """
     B = ref["status"].shape[0]
     assert (gpu["status"] == ref["status"]).all(), (gpu["status"], ref["status"])
-    flagged = ref["flags"] != 0
+    flags = ref["flags"]
+    fpos = ref.get("flag_pos")
     greedy = temperature == 0
-    check = (ref["status"] == 0) & (~flagged | greedy)
-    bad = np.nonzero(check & (gpu["accepted"] != ref["accepted"]))[0]
-    assert bad.size == 0, f"accepted differ at {bad[:10]}: gpu {gpu['accepted'][bad[:10]]} oracle {ref['accepted'][bad[:10]]}"
-    tok_bad = np.nonzero(check & (gpu["tokens"] != ref["tokens"]).any(axis=1))[0]
-    assert tok_bad.size == 0, f"tokens differ at {tok_bad[:10]}:\n{gpu['tokens'][tok_bad[:4]]}\n{ref['tokens'][tok_bad[:4]]}"
-    bad_status = ref["status"] != 0
+    ok = ref["status"] == 0
+    counts = dict(n=B, thresh=0, gumbel=0, degenerate=0, illcond=0, mismatched_flagged=0)
+    for b in range(B):
+        if not ok[b]:
+            continue
+        fl = 0 if greedy[b] else int(flags[b])
+        ga, ra = int(gpu["accepted"][b]), int(ref["accepted"][b])
+        gt, rt = gpu["tokens"][b], ref["tokens"][b]
+        counts["thresh"] += bool(fl & oracle.FL_THRESH)
+        counts["gumbel"] += bool(fl & oracle.FL_GUMBEL)
+        counts["degenerate"] += bool(fl & oracle.FL_DEGENERATE)
+        counts["illcond"] += bool(fl & oracle.FL_ILLCOND)
+        exact = ga == ra and np.array_equal(gt, rt)
+        if fl & oracle.FL_THRESH:
+            f = int(fpos[b]) if fpos is not None else 0
+            assert 0 <= f <= ra, (b, f, ra)
+            assert ga >= f and np.array_equal(gt[:f], rt[:f]), (b, f, gt, rt)
+        elif fl & (oracle.FL_GUMBEL | oracle.FL_DEGENERATE):
+            assert ga == ra and np.array_equal(gt[:ra], rt[:ra]), (b, gt, rt)
+            assert (gt[ra + 1:] == -1).all()
+        else:
+            assert exact, f"request {b} (flags {fl}) differs: accepted gpu {ga} oracle {ra}\n{gt}\n{rt}"
+        if not exact:
+            counts["mismatched_flagged"] += 1
+    bad_status = ~ok
     assert (gpu["accepted"][bad_status] == 0).all() and (gpu["tokens"][bad_status] == -1).all()
     if gpu.get("p") is not None:
-        valid = ref["p"] >= 0
-        assert ((gpu["p"] >= 0) == valid).all()
-        assert np.abs(gpu["p"][valid] - ref["p"][valid]).max(initial=0) <= P_ATOL
-        assert np.abs(gpu["q"][valid] - ref["q"][valid]).max(initial=0) <= P_ATOL
-        assert (gpu["p"][~valid] == -1).all() and (gpu["q"][~valid] == -1).all()
-    return dict(n=B, flagged=int((flagged & ~greedy & (ref["status"] == 0)).sum()),
-                mismatched_flagged=int((flagged & ~greedy & (gpu["accepted"] != ref["accepted"])).sum()))
+        gv, rv = gpu["p"] >= 0, ref["p"] >= 0
+        both = gv & rv
+        # the positions each side computed agree except after a decision that a
+        # near-tie left open (early exit stops at its own first rejection)
+        same_decisions = gpu["accepted"] == ref["accepted"]
+        assert (gv[same_decisions] == rv[same_decisions]).all()
+        assert np.abs(gpu["p"][both] - ref["p"][both]).max(initial=0) <= P_ATOL
+        assert np.abs(gpu["q"][both] - ref["q"][both]).max(initial=0) <= P_ATOL
+        assert (gpu["p"][~gv] == -1).all() and (gpu["q"][~gv] == -1).all()
+    counts["flagged"] = counts["thresh"] + counts["gumbel"] + counts["degenerate"]
+    return counts
