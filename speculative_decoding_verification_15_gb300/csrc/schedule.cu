@@ -29,27 +29,32 @@ namespace {
 
 constexpr int kSchedThreads = 1024;
 
-__device__ __forceinline__ bool before(double ka, int ia, double kb, int ib) {
+// Survivals are non-negative doubles, so their bit patterns order like their values:
+// the sort compares 64-bit integers (sm_103a's fp64 compare rate is a small fraction
+// of its integer rate).
+__device__ __forceinline__ bool before(unsigned long long ka, int ia, unsigned long long kb, int ib) {
     return ka > kb || (ka == kb && ia < ib);
 }
 
-// Survival products of conf and the candidate slots: key[b Kmax + i] = S_{b,i}
-// for the slots a request may add (m_b <= i < maxlen_b), -1 elsewhere; returns
-// n0 = sum m_b, the number of candidates and E0 = sum of the mandatory
-// survivals through shared memory.  Every thread of the CTA calls it.
+// Survival products of conf and the candidate slots: key[b Kmax + i] = the bits of
+// S_{b,i} for the slots a request may add (m_b <= i < maxlen_b), 0 with the largest
+// id elsewhere (after every survival, zeros included); returns n0 = sum m_b, the
+// number of candidates and E0 = sum of the mandatory survivals through shared
+// memory.  Every thread of the CTA calls it.
 __device__ void build_keys(const float *conf, const int32_t *max_len, int B, int Kmax, int min_len, int npow2,
-                           double *key, int *id, int *s_n0, int *s_ncand, double *s_E0) {
-    const int tid = threadIdx.x;
+                           unsigned long long *key, int *id, int *s_n0, int *s_ncand, double *s_E0,
+                           double *s_wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) {
         *s_n0 = 0;
         *s_ncand = 0;
-        *s_E0 = 0.0;
     }
     for (int i = tid; i < npow2; i += kSchedThreads) {
-        key[i] = -1.0;  // padding sorts after every survival (>= 0)
+        key[i] = 0ull;
         id[i] = 0x7fffffff;
     }
     __syncthreads();
+    double e0sum = 0.0;
     for (int b = tid; b < B; b += kSchedThreads) {
         int ml = max_len ? max_len[b] : Kmax;
         ml = ml < 0 ? 0 : (ml > Kmax ? Kmax : ml);
@@ -63,20 +68,33 @@ __device__ void build_keys(const float *conf, const int32_t *max_len, int B, int
             if (i < mand) {
                 e0 += surv;
             } else if (i < ml) {
-                key[b * Kmax + i] = surv;
+                key[b * Kmax + i] = (unsigned long long)__double_as_longlong(surv);
                 id[b * Kmax + i] = b * Kmax + i;
             }
         }
         atomicAdd(s_n0, mand);
         atomicAdd(s_ncand, ml - mand);
-        atomicAdd(s_E0, e0);
+        e0sum += e0;
+    }
+    // E0 summed in request order: each thread's requests, then the threads in order
+    double incl = e0sum;
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[wid] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        double tot = 0.0;
+        for (int w = 0; w < kSchedThreads / 32; ++w) tot += s_wsum[w];
+        *s_E0 = tot;
     }
     __syncthreads();
 }
 
 // Bitonic sort of (key, id) in the `before` order (survival descending, then b,
 // then i), then key[j] = the sum of the j+1 largest survivals (padding adds 0).
-__device__ void sort_and_scan(double *key, int *id, int npow2, double *s_wsum) {
+__device__ void sort_and_scan(unsigned long long *key, int *id, int npow2, double *s_wsum) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     for (int k = 2; k <= npow2; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
@@ -86,7 +104,7 @@ __device__ void sort_and_scan(double *key, int *id, int npow2, double *s_wsum) {
                     const bool up = (i & k) == 0;
                     const bool ordered = before(key[i], id[i], key[ixj], id[ixj]);
                     if (up != ordered) {
-                        const double tk = key[i];
+                        const unsigned long long tk = key[i];
                         key[i] = key[ixj];
                         key[ixj] = tk;
                         const int ti = id[i];
@@ -102,7 +120,7 @@ __device__ void sort_and_scan(double *key, int *id, int npow2, double *s_wsum) {
     const int lo = tid * per < npow2 ? tid * per : npow2;
     const int hi = lo + per < npow2 ? lo + per : npow2;
     double local = 0.0;
-    for (int i = lo; i < hi; ++i) local += key[i] > 0.0 ? key[i] : 0.0;
+    for (int i = lo; i < hi; ++i) local += __longlong_as_double((long long)key[i]);
     double incl = local;
     for (int o = 1; o < 32; o <<= 1) {
         const double y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -114,10 +132,14 @@ __device__ void sort_and_scan(double *key, int *id, int npow2, double *s_wsum) {
     for (int w = 0; w < wid; ++w) base += s_wsum[w];
     double run = base + incl - local;
     for (int i = lo; i < hi; ++i) {
-        run += key[i] > 0.0 ? key[i] : 0.0;
-        key[i] = run;
+        run += __longlong_as_double((long long)key[i]);
+        key[i] = (unsigned long long)__double_as_longlong(run);  // from here on: the prefix sums
     }
     __syncthreads();
+}
+
+__device__ __forceinline__ double prefix_at(const unsigned long long *key, int j) {
+    return __longlong_as_double((long long)key[j]);
 }
 
 // One CTA.  conf sizes the batch: the total n* with the best expected throughput
@@ -128,7 +150,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
                                                                  int min_len, int npow2, int32_t *out_len,
                                                                  double *out_info) {
     extern __shared__ __align__(16) unsigned char smem[];
-    double *key = (double *)smem;                     // [npow2]  survival, later prefix sums
+    unsigned long long *key = (unsigned long long *)smem;  // [npow2]  survival bits, later prefix-sum bits
     int *id = (int *)(key + npow2);                   // [npow2]  b * Kmax + i
     int *cnt = id + npow2;                            // [B]
     __shared__ int s_n0, s_ncand;
@@ -139,7 +161,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
     for (int b = tid; b < B; b += kSchedThreads) cnt[b] = 0;
-    build_keys(conf, max_len, B, Kmax, min_len, npow2, key, id, &s_n0, &s_ncand, &s_E0);
+    build_keys(conf, max_len, B, Kmax, min_len, npow2, key, id, &s_n0, &s_ncand, &s_E0, s_wsum);
     sort_and_scan(key, id, npow2, s_wsum);
 
     // throughput of every admissible total, best over the whole table
@@ -150,7 +172,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
     double bestF = -__longlong_as_double(0x7ff0000000000000LL);
     int bestN = n0;
     for (int n = n0 + tid; n <= nhi; n += kSchedThreads) {
-        const double E = s_E0 + (n > n0 ? key[n - n0 - 1] : 0.0);
+        const double E = s_E0 + (n > n0 ? prefix_at(key, n - n0 - 1) : 0.0);
         const double t = (double)tau[n];
         const double F = (t > 0.0 && isfinite(t)) ? ((double)B + E) / t : -__longlong_as_double(0x7ff0000000000000LL);
         if (F > bestF || (F == bestF && n < bestN)) {
@@ -181,7 +203,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
     __syncthreads();
     const int nstar = s_redN[0];
     if (conf_alloc) {  // the latest scores pick the n* slots (same mandatory slots and candidates)
-        build_keys(conf_alloc, max_len, B, Kmax, min_len, npow2, key, id, &s_n0, &s_ncand, &s_E0);
+        build_keys(conf_alloc, max_len, B, Kmax, min_len, npow2, key, id, &s_n0, &s_ncand, &s_E0, s_wsum);
         sort_and_scan(key, id, npow2, s_wsum);
     }
     const int take = nstar - n0 > 0 ? nstar - n0 : 0;
@@ -193,7 +215,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float *co
         out_len[b] = (min_len < ml ? min_len : ml) + cnt[b];
     }
     if (tid == 0 && out_info) {
-        const double E = s_E0 + (take > 0 ? key[take - 1] : 0.0);
+        const double E = s_E0 + (take > 0 ? prefix_at(key, take - 1) : 0.0);
         out_info[0] = (double)nstar;
         out_info[1] = (double)B + E;
         const double t = (nstar >= 0 && nstar < n_table) ? (double)tau[nstar] : 0.0;
