@@ -24,7 +24,9 @@
  * Conventions for every entry point:
  *  - Array pointers are DEVICE pointers owned by the caller; the library keeps no
  *    reference after the call returns and allocates no device memory per call.
- *    Scratch space is the caller's workspace (size from the *_workspace_size query).
+ *    Logit pointers must lie on the current device (or in managed memory), else
+ *    SPEC_EINVAL.  Scratch space is the caller's workspace (size from the
+ *    *_workspace_size query).
  *  - Calls are asynchronous on `cuda_stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and never synchronise the host.
  *  - Logits are row-major with V contiguous and a row stride of ld_row elements
@@ -69,7 +71,8 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
 #define SPEC_STATUS_BAD_K 2            /* num_draft[b] outside [0, Kmax]                          */
 #define SPEC_STATUS_BAD_TEMPERATURE 3  /* temperature[b] < 0, NaN or infinite                     */
 #define SPEC_STATUS_NONFINITE 4        /* a row that was read holds NaN or +inf, or is all -inf   */
-#define SPEC_STATUS_INTERNAL 5         /* a bounded internal wait gave up; results are not valid */
+#define SPEC_STATUS_INTERNAL 5         /* a bounded internal wait gave up, or the workspace was not
+                                          zeroed before its first use; results are not valid   */
 /* Rows read: target and draft rows 0..k_b-1 (target only for greedy requests); the
  * target row k_b only when every draft is accepted (it holds the bonus token).
  * A request with a non-zero status has out_accepted[b] = 0, every token -1 and
@@ -82,10 +85,24 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
 #define SPEC_MARKOV_MAX_RANK 512   /* rank r of the Markov head's factors (a multiple of 4) */
 
 /*
- * Bytes of device workspace that spec_verify_greedy / spec_verify_sample need for
- * (B, Kmax, V, dtype) on the current device.  Returns 0 for invalid sizes.  The
- * workspace holds a control block and the per-segment row statistics of the main
- * pass; its contents need no initialisation and are garbage after a call.
+ * Bytes of device workspace that spec_verify_greedy / spec_verify_sample (and their
+ * _flat forms) need for (B, Kmax, V, dtype).  Returns 0 for invalid sizes.  The
+ * workspace holds the main pass's chunk-ticket counter (always at its start), one
+ * 16-byte statistic and 16 two-byte seed pointers per chunk of every row the main
+ * pass reads (rows of at most 64 KB chunks), and per request a piece counter, a
+ * shared bound and the commit pieces' results:
+ *   256 + align256(4 (B + 1)) + 2 align256(4 B) + align256(16 B R cpr)
+ *       + align256(32 B R cpr) + align256(16 B P),
+ * with R = 2 Kmax main-pass rows a request (sampling), cpr = the chunks a row
+ * (ceil(V / floor(65504 / elsize)) for elsize 2 or 4, then ceil(V / ce) with
+ * ce = ceil(V / cpr) rounded up to a multiple of 8) and P = ceil(ceil(V / 1024) / 8)
+ * commit pieces a request.
+ * ZERO-FILL the workspace once before its first use (cudaMemset(ws, 0, bytes)):
+ * the ticket counter must start at 0.  Every call leaves it ready for the next
+ * call, so one workspace serves any number of calls made in stream order; calls
+ * that may overlap need one workspace each.  A call on a workspace that was not
+ * zeroed reports status 5 for the requests it could not verify, and leaves the
+ * workspace ready for the next call.
  */
 size_t spec_verify_workspace_size(int B, int Kmax, int V, int dtype);
 
@@ -238,11 +255,12 @@ int spec_markov_draft(const void *base, int dtype, int B, int K, int V, int64_t 
  *    device current (and sets the kernels' shared-memory limits, as the
  *    workspace entry points do).  Make that first call before any stream capture.
  *  - Limit: sizes whose spec_verify_workspace_size(B, Kmax, V, dtype) exceeds
- *    SPEC_STATIC_SCRATCH_BYTES return SPEC_ESCRATCH before anything is launched
- *    (Kmax = 8 on a 152-SM device: B up to 1007 fits, for either logit type and
- *    any V; the scratch grows with B * Kmax, not with V).
- *  - Zeroing: none of the scratch needs to start at zero; every call writes what
- *    it reads.
+ *    SPEC_STATIC_SCRATCH_BYTES return SPEC_ESCRATCH before anything is launched.
+ *    The scratch grows with B * Kmax * (chunks a row) (see the formula at
+ *    spec_verify_workspace_size): at V = 151936, Kmax = 7 fits B up to 1140 for
+ *    bf16 logits (5 chunks a row) and B up to 596 for fp32 (10 chunks a row).
+ *  - Zeroing: the array is zero when the module loads, and every call leaves the
+ *    part that must start at zero (the chunk-ticket counter) at zero.
  *  - Races: every call on a device uses the same array, so two calls that can
  *    overlap (different streams, or host threads without ordering between them)
  *    corrupt each other's results.  Order the calls on one stream.

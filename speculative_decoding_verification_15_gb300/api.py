@@ -17,14 +17,17 @@ _ws_cache: dict[int, torch.Tensor] = {}
 
 
 def workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    """A cached uint8 workspace of at least nbytes on device (grown on demand)."""
+    """A cached uint8 workspace of at least nbytes on device (grown on demand).
+
+    It is zero-filled when allocated: the verify calls need a zeroed workspace
+    before its first use and leave it ready for the next call."""
     idx = torch.device(device).index
     if idx is None:
         idx = torch.cuda.current_device()
     with _ws_lock:
         ws = _ws_cache.get(idx)
         if ws is None or ws.numel() < nbytes:
-            ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=torch.device("cuda", idx))
+            ws = torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=torch.device("cuda", idx))
             _ws_cache[idx] = ws
         return ws
 

@@ -105,10 +105,23 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream_handle(stream) -> ctypes.c_void_p:
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    """The stream to launch on: the given one (it must belong to `device`), else the
+    current stream of `device`, the device that holds the call's tensors."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call(lib, name: str, device, *args):
+    """Call entry point `name` with `device` current: the library launches on the
+    current device and looks its per-device state (SM count, scratch) up there."""
+    with torch.cuda.device(device):
+        rc = getattr(lib, name)(*args)
+    if rc != SPEC_OK:
+        raise SpecError(name, rc, lib)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -167,11 +180,9 @@ def spec_verify_greedy(target, draft_tokens, num_draft, out_tokens, out_accepted
     _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
     _need(out_status, "out_status", torch.int32, (B,), dev)
     _need(workspace, "workspace", torch.uint8, None, dev)
-    rc = lib.spec_verify_greedy(_ptr(target), _dtype_code(target), B, Kmax, V, ld, _ptr(draft_tokens),
+    _call(lib, "spec_verify_greedy", dev, _ptr(target), _dtype_code(target), B, Kmax, V, ld, _ptr(draft_tokens),
                                 _ptr(num_draft), _ptr(out_tokens), _ptr(out_accepted), _ptr(out_status),
-                                _ptr(workspace), workspace.numel(), _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_verify_greedy", rc, lib)
+                                _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
 
 
 def spec_verify_sample(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int, out_tokens,
@@ -201,13 +212,11 @@ def spec_verify_sample(target, draft, draft_tokens, num_draft, temperature, seed
         _need(out_q, "out_q", torch.float32, (B, Kmax), dev)
     _need(out_status, "out_status", torch.int32, (B,), dev)
     _need(workspace, "workspace", torch.uint8, None, dev)
-    rc = lib.spec_verify_sample(_ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
+    _call(lib, "spec_verify_sample", dev, _ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
                                 _ptr(draft_tokens), _ptr(num_draft), _ptr(temperature),
                                 int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_tokens),
                                 _ptr(out_accepted), _ptr(out_p), _ptr(out_q), _ptr(out_status),
-                                _ptr(workspace), workspace.numel(), _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_verify_sample", rc, lib)
+                                _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
 
 
 def spec_verify_sample_early_exit(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int,
@@ -235,13 +244,11 @@ def spec_verify_sample_early_exit(target, draft, draft_tokens, num_draft, temper
         if t is not None:
             _need(t, n, torch.float32, (B, Kmax), dev)
     _need(out_status, "out_status", torch.int32, (B,), dev)
-    rc = lib.spec_verify_sample_early_exit(_ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
+    _call(lib, "spec_verify_sample_early_exit", dev, _ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
                                            _ptr(draft_tokens), _ptr(num_draft), _ptr(temperature),
                                            int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_tokens),
                                            _ptr(out_accepted), _ptr(out_p), _ptr(out_q), _ptr(out_status),
-                                           _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_verify_sample_early_exit", rc, lib)
+                                           _stream_handle(stream, dev))
 
 
 def spec_verify_greedy_early_exit(target, draft_tokens, num_draft, out_tokens, out_accepted, out_status,
@@ -257,11 +264,9 @@ def spec_verify_greedy_early_exit(target, draft_tokens, num_draft, out_tokens, o
     _need(out_tokens, "out_tokens", torch.int32, (B, K1), dev)
     _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
     _need(out_status, "out_status", torch.int32, (B,), dev)
-    rc = lib.spec_verify_greedy_early_exit(_ptr(target), _dtype_code(target), B, Kmax, V, ld, _ptr(draft_tokens),
+    _call(lib, "spec_verify_greedy_early_exit", dev, _ptr(target), _dtype_code(target), B, Kmax, V, ld, _ptr(draft_tokens),
                                            _ptr(num_draft), _ptr(out_tokens), _ptr(out_accepted),
-                                           _ptr(out_status), _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_verify_greedy_early_exit", rc, lib)
+                                           _ptr(out_status), _stream_handle(stream, dev))
 
 
 def spec_markov_draft(base, anchor, emb, proj, temperature, seed: int, step: int, out_tokens, out_logits,
@@ -285,11 +290,9 @@ def spec_markov_draft(base, anchor, emb, proj, temperature, seed: int, step: int
     _need(out_tokens, "out_tokens", torch.int32, (B, K), dev)
     _need(out_logits, "out_logits", torch.float32, (B, K, V), dev)
     _need(out_status, "out_status", torch.int32, (B,), dev)
-    rc = lib.spec_markov_draft(_ptr(base), _dtype_code(base), B, K, V, ld, _ptr(anchor), _ptr(emb), _ptr(proj),
+    _call(lib, "spec_markov_draft", dev, _ptr(base), _dtype_code(base), B, K, V, ld, _ptr(anchor), _ptr(emb), _ptr(proj),
                                emb.shape[1], _ptr(temperature), int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
-                               _ptr(out_tokens), _ptr(out_logits), _ptr(out_status), _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_markov_draft", rc, lib)
+                               _ptr(out_tokens), _ptr(out_logits), _ptr(out_status), _stream_handle(stream, dev))
 
 
 def spec_verify_sample_noalloc(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int,
@@ -316,13 +319,11 @@ def spec_verify_sample_noalloc(target, draft, draft_tokens, num_draft, temperatu
         if t is not None:
             _need(t, n, torch.float32, (B, Kmax), dev)
     _need(out_status, "out_status", torch.int32, (B,), dev)
-    rc = lib.spec_verify_sample_noalloc(_ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
+    _call(lib, "spec_verify_sample_noalloc", dev, _ptr(target), _ptr(draft), _dtype_code(target), B, Kmax, V, ld,
                                         _ptr(draft_tokens), _ptr(num_draft), _ptr(temperature),
                                         int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_tokens),
                                         _ptr(out_accepted), _ptr(out_p), _ptr(out_q), _ptr(out_status),
-                                        _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_verify_sample_noalloc", rc, lib)
+                                        _stream_handle(stream, dev))
 
 
 def _flat_rows(t: torch.Tensor, name: str):
@@ -345,11 +346,9 @@ def spec_verify_greedy_flat(target, cu_draft, draft_tokens, out_tokens, out_acce
     _need(out_accepted, "out_accepted", torch.int32, (B,), dev)
     _need(out_status, "out_status", torch.int32, (B,), dev)
     _need(workspace, "workspace", torch.uint8, None, dev)
-    rc = lib.spec_verify_greedy_flat(_ptr(target), _dtype_code(target), B, int(Kmax), V, ld, _ptr(cu_draft),
+    _call(lib, "spec_verify_greedy_flat", dev, _ptr(target), _dtype_code(target), B, int(Kmax), V, ld, _ptr(cu_draft),
                                      _ptr(draft_tokens), _ptr(out_tokens), _ptr(out_accepted), _ptr(out_status),
-                                     _ptr(workspace), workspace.numel(), _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_verify_greedy_flat", rc, lib)
+                                     _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
 
 
 def spec_verify_sample_flat(target, draft, cu_draft, draft_tokens, temperature, seed: int, step: int, out_tokens,
@@ -372,13 +371,11 @@ def spec_verify_sample_flat(target, draft, cu_draft, draft_tokens, temperature, 
         if t is not None:
             _need(t, n, torch.float32, None, dev)
     _need(workspace, "workspace", torch.uint8, None, dev)
-    rc = lib.spec_verify_sample_flat(_ptr(target), _ptr(draft), _dtype_code(target), B, int(Kmax), V, ld,
+    _call(lib, "spec_verify_sample_flat", dev, _ptr(target), _ptr(draft), _dtype_code(target), B, int(Kmax), V, ld,
                                      _ptr(cu_draft), _ptr(draft_tokens), _ptr(temperature),
                                      int(seed) & (2**64 - 1), int(step) & (2**64 - 1), _ptr(out_tokens),
                                      _ptr(out_accepted), _ptr(out_p), _ptr(out_q), _ptr(out_status),
-                                     _ptr(workspace), workspace.numel(), _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_verify_sample_flat", rc, lib)
+                                     _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
 
 
 def spec_schedule_verify_len(conf, max_len, step_time_us, budget: int, min_len: int, out_len, out_info=None,
@@ -395,11 +392,9 @@ def spec_schedule_verify_len(conf, max_len, step_time_us, budget: int, min_len: 
     _need(out_len, "out_len", torch.int32, (B,), dev)
     if out_info is not None:
         _need(out_info, "out_info", torch.float64, (3,), dev)
-    rc = lib.spec_schedule_verify_len(_ptr(conf), _ptr(max_len), B, Kmax, _ptr(step_time_us),
+    _call(lib, "spec_schedule_verify_len", dev, _ptr(conf), _ptr(max_len), B, Kmax, _ptr(step_time_us),
                                       step_time_us.numel(), int(budget), int(min_len), _ptr(out_len),
-                                      _ptr(out_info), _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_schedule_verify_len", rc, lib)
+                                      _ptr(out_info), _stream_handle(stream, dev))
 
 
 def spec_schedule_verify_len_stale(conf_stale, conf, max_len, step_time_us, budget: int, min_len: int, out_len,
@@ -417,11 +412,9 @@ def spec_schedule_verify_len_stale(conf_stale, conf, max_len, step_time_us, budg
     _need(out_len, "out_len", torch.int32, (B,), dev)
     if out_info is not None:
         _need(out_info, "out_info", torch.float64, (3,), dev)
-    rc = lib.spec_schedule_verify_len_stale(_ptr(conf_stale), _ptr(conf), _ptr(max_len), B, Kmax,
+    _call(lib, "spec_schedule_verify_len_stale", dev, _ptr(conf_stale), _ptr(conf), _ptr(max_len), B, Kmax,
                                             _ptr(step_time_us), step_time_us.numel(), int(budget), int(min_len),
-                                            _ptr(out_len), _ptr(out_info), _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_schedule_verify_len_stale", rc, lib)
+                                            _ptr(out_len), _ptr(out_info), _stream_handle(stream, dev))
 
 
 def spec_schedule_threshold(conf, max_len, threshold: float, out_len, stream=None) -> None:
@@ -434,10 +427,8 @@ def spec_schedule_threshold(conf, max_len, threshold: float, out_len, stream=Non
     if max_len is not None:
         _need(max_len, "max_len", torch.int32, (B,), dev)
     _need(out_len, "out_len", torch.int32, (B,), dev)
-    rc = lib.spec_schedule_threshold(_ptr(conf), _ptr(max_len), B, Kmax, float(threshold), _ptr(out_len),
-                                     _stream_handle(stream))
-    if rc != SPEC_OK:
-        raise SpecError("spec_schedule_threshold", rc, lib)
+    _call(lib, "spec_schedule_threshold", dev, _ptr(conf), _ptr(max_len), B, Kmax, float(threshold), _ptr(out_len),
+                                     _stream_handle(stream, dev))
 
 
 def profile_enable(on: bool) -> None:

@@ -13,21 +13,23 @@
 // programmatic dependent launch):
 //  main_kernel    streams the rows of every draft position once -- target and draft
 //                 rows of sampling requests, target rows of greedy ones -- with plain
-//                 16-byte loads: two 512-thread CTAs per SM over static contiguous
-//                 ranges of the flattened chunk list.  Per (CTA, row segment, warp):
-//                 max, sum of 2^(x log2e / T - max'), and the lowest argmax.
+//                 16-byte loads: two 512-thread CTAs per SM take the chunks (at most
+//                 64 KB of a row) by dynamic tickets.  Per chunk: max, sum of
+//                 2^(x log2e / T - max'), and (greedy rows) the lowest argmax.
 //                 HBM-bound.
-//  commit_kernel  one cluster of up to 8 CTAs per request: combines the partials of
-//                 its rows (one warp per draft position), runs the acceptance scan,
-//                 emits the accepted drafts, and draws the one extra token -- the
-//                 correction at the first rejected row j (Gumbel-max over
-//                 log(max(0, p - q))), the bonus from row k_b, or the greedy argmax
-//                 of row k_b -- over the row staged into shared memory by bulk
-//                 copies, the CTAs' results meeting in rank 0 over DSMEM.
+//  commit_kernel  P CTAs ("pieces") per request: each combines the request's chunk
+//                 partials, runs the acceptance scan, and reduces its interleaved
+//                 share of the one row still needed -- the correction at the first
+//                 rejected row j (Gumbel-max over log(max(0, p - q))), the bonus from
+//                 row k_b, or the greedy argmax of row k_b -- staged into shared
+//                 memory by bulk copies; the last piece to finish combines the
+//                 pieces and writes the request's outputs.
+// The early-exit calls launch one kernel (early_exit_kernel, below).
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -45,19 +47,17 @@ constexpr int kMainBlocksPerSM = 2;              // main-pass CTAs per SM (64 re
 constexpr int kVPT = 8;                          // 16-byte loads in flight per thread and chunk
 constexpr int kChunkMaxBytes = kCT * kVPT * 16 - 32;  // an aligned superset of a chunk fits kCT x kVPT loads
 constexpr uint64_t kWaitNs = 2000000000ull;      // bound on every mbarrier wait (2 s)
-constexpr int kMaxDesc = 512;                    // per-CTA row descriptors kept in smem
 
-struct Part {
-    float m;    // raw max of the segment (NaN-propagating)
-    float s;    // sum 2^(x c - fl(m c)) over the segment (sampling rows)
-    int idx;    // lowest index of the max
-    float pad;
+struct __align__(16) Part {
+    float m;         // raw max of the chunk (NaN-propagating)
+    float s;         // sum 2^(x c - fl(m c)) over the chunk (sampling rows)
+    int idx;         // lowest index of the max (greedy rows; -1 otherwise)
+    uint32_t epoch;  // tag of the call that wrote it
 };
 
 // ------------------------------------------------------------------ chunking
 // Rows are cut into cpr chunks of ce elements (ce a multiple of 8, at most
-// kChunkMaxBytes); the flattened chunk list of all rows is split into G equal
-// contiguous ranges, one per CTA.
+// kChunkMaxBytes); chunk k of main-pass row r has the flat index r cpr + k.
 struct Chunking {
     int cpr, ce;
 };
@@ -71,17 +71,6 @@ __host__ __device__ inline Chunking make_chunking(int V, int esz) {
     return {cpr, ce};
 }
 
-__host__ __device__ inline int64_t cta_first(int64_t total, int G, int i) { return total * i / G; }
-
-// Rows one CTA can touch, an upper bound.
-__host__ inline int segs_per_cta(int64_t total_max, int G, int cpr) {
-    const int64_t per = (total_max + G - 1) / G;
-    return (int)((per + cpr - 1) / cpr) + 1;
-}
-
-__device__ __forceinline__ int64_t part_slot(int cta, int nseg, int seg, int warp) {
-    return ((int64_t)cta * nseg + seg) * kCW + warp;
-}
 
 // Global byte window of chunk k of a row: the 16-byte aligned superset [a0, a1) of
 // elements [e0, e1); smem element 0 is global element e0 - shift.
@@ -175,13 +164,17 @@ __device__ __forceinline__ int chunk_find(const Vec (&d)[NV], int ebase, int ct,
     return found;
 }
 
-// sum_e 2^(x_e c - ms) over the thread's vectors, two lanes per instruction
-template <class Vec>
-__device__ __forceinline__ float chunk_expsum(const Vec (&d)[kVPT], float c, float ms) {
+// sum_e 2^(x_e c - ms) over the thread's vectors, two lanes per instruction.
+// Every sum is kept relative to a reference fl(m c) -- the product rounded once,
+// with __fmul_rn so that the compiler cannot fuse it into a later FMA -- and every
+// later use of that reference (rescaling partials, log p) rounds it the same way:
+// at small T, m c is in the thousands and one ulp of it is 5e-4.
+template <class Vec, int NV>
+__device__ __forceinline__ float chunk_expsum(const Vec (&d)[NV], float c, float ms) {
     const float2 cc = make_float2(c, c), mm = make_float2(-ms, -ms);
     float2 acc = make_float2(0.f, 0.f);  // one pair: the warps of the SM supply the parallelism
 #pragma unroll
-    for (int t = 0; t < kVPT; ++t)
+    for (int t = 0; t < NV; ++t)
 #pragma unroll
         for (int e = 0; e < Vec::VE; e += 2) {
             const float2 y = ffma2(make_float2(d[t].get(e), d[t].get(e + 1)), cc, mm);
@@ -272,197 +265,23 @@ __device__ __forceinline__ int find_request(const int *rs, int B, int r) {
     return lo;
 }
 
-// =================================================================== main_kernel
-struct MainParams {
-    const void *target;
-    const void *draft;
-    int64_t ld_row;
-    int B, Kmax, V;
-    const int32_t *cu;         // flattened layout offsets [B+1], or NULL (padded)
-    const int32_t *num_draft;
-    const float *temperature;  // NULL: every request greedy
-    int *row_start;            // [B+1], written by block 0 for commit_kernel
-    Part *parts;
-    int nseg;
-};
-
-struct MainRow {
-    const char *ptr;
-    float c;      // log2(e) / T, or 0 for a greedy row
-};
-
-template <class Vec>
-__device__ __forceinline__ MainRow main_row(const MainParams &p, const int *rs, int r) {
-    const int b = find_request(rs, p.B, r);
-    const int local = r - rs[b];
-    const ReqBase rb = req_base(p.cu, p.num_draft, p.Kmax, b);
-    const float T = p.temperature ? p.temperature[b] : 0.f;
-    const int64_t rowbytes = p.ld_row * Vec::ESIZE;
-    MainRow m;
-    if (T == 0.f || local < rb.kb) {
-        m.ptr = (const char *)p.target + (rb.t0 + local) * rowbytes;
-    } else {
-        m.ptr = (const char *)p.draft + (rb.d0 + (local - rb.kb)) * rowbytes;
-    }
-    m.c = T == 0.f ? 0.f : __fdiv_rn(kLog2e, T);
-    return m;
-}
-
-// Static contiguous ranges of the flattened chunk list, one per CTA (two CTAs per
-// SM, so that one CTA's arithmetic overlaps the other's loads).  Each thread issues
-// kVPT independent 16-byte loads per chunk before it reduces them.  This streams as
-// fast as a bulk-copy ring through shared memory did on this path, with no producer
-// warp, no ring and no waits.
-template <class Vec>
-__global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    int *s_rs = (int *)smem;
-    MainRow *s_desc = (MainRow *)(smem + sizeof(int) * (size_t)(((p.B + 1) + 3) & ~3));
-    scan_request_rows(s_rs, p.B, p.cu, p.num_draft, p.temperature, p.Kmax);  // ends with __syncthreads
-    if (blockIdx.x == 0)
-        for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.row_start[i] = s_rs[i];
-    pdl_launch_dependents();
-
-    const Chunking ck = make_chunking(p.V, Vec::ESIZE);
-    const int G = gridDim.x;
-    const int64_t total = (int64_t)s_rs[p.B] * ck.cpr;  // < 2^31 (checked by the host)
-    if (total == 0) return;
-    const int c0 = (int)cta_first(total, G, blockIdx.x), c1 = (int)cta_first(total, G, blockIdx.x + 1);
-    if (c0 == c1) return;
-    const int first_row = c0 / ck.cpr;
-    const int nrows = (c1 - 1) / ck.cpr - first_row + 1;
-    const bool table = nrows <= kMaxDesc;
-    if (table)
-        for (int i = threadIdx.x; i < nrows; i += blockDim.x) s_desc[i] = main_row<Vec>(p, s_rs, first_row + i);
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ct = threadIdx.x;
-    int r = first_row, k = c0 - first_row * ck.cpr;
-    MainRow mr = table ? s_desc[0] : main_row<Vec>(p, s_rs, r);
-    float m = kNegInf, mc = 0.f, s = 0.f;
-    int kat = -1;  // chunk of the row where this lane's running max was last raised
-    bool nan_seen = false;
-    // The lowest index holding the warp's maximum M.  Lanes find their max's index
-    // only here, once per row segment: the lanes whose running max equals M reload
-    // the chunk where it was raised (its first occurrence in this lane's entries is
-    // there) and scan it.  Finding it as each chunk raised a lane's max cost a scan
-    // of every chunk by nearly every warp, since some lane of 32 almost always
-    // raises its max.
-    auto warp_first_index_of = [&](float M) {
-        int idx = -1;
-        if (kat >= 0 && m == M) {
-            const ChunkWin w2 = chunk_window(mr.ptr, Vec::ESIZE, p.V, ck, kat);
-            Vec d2[kVPT];
-            load_chunk(d2, w2, ct);
-            idx = chunk_find<kCT>(d2, w2.e0 - w2.shift, ct, M);
-        }
-        uint32_t v = (uint32_t)idx;  // -1: none (largest as unsigned)
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-        return (int)v;
-    };
-    auto flush = [&]() {
-        Part out;
-        if (mr.c != 0.f) {
-            const float M = warp_max_nan(m);
-            const float MC = M * mr.c;
-            const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - MC);
-            out.s = warp_sum(sc);
-            out.m = M;
-            out.idx = warp_first_index_of(M);
-        } else {
-            const bool any_nan = __any_sync(0xffffffffu, nan_seen);
-            const float mm = warp_max_nan(m);  // greedy lanes keep m free of NaN
-            out.idx = warp_first_index_of(mm);
-            out.m = any_nan ? __int_as_float(0x7fc00000) : mm;
-            out.s = 0.f;
-        }
-        out.pad = 0.f;
-        if (lane == 0) p.parts[part_slot(blockIdx.x, p.nseg, r - first_row, warp)] = out;
-    };
-
-    for (int cc = c0; cc < c1; ++cc) {
-        const ChunkWin w = chunk_window(mr.ptr, Vec::ESIZE, p.V, ck, k);
-        Vec d[kVPT];
-        load_chunk(d, w, ct);
-        if (mr.c != 0.f) {
-            // s is kept relative to the lane's running max m (mc = fl(m c)), so every
-            // term is at most 1; the max moves (and s is rescaled) only when a chunk
-            // holds a larger entry, which a row sees a few times at most.  NaN or +inf
-            // makes m non-finite, which the commit pass reports.
-            const float tm = chunk_max(d);
-            if (!(tm <= m)) {
-                const float mcn = tm * mr.c;
-                s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
-                m = tm;
-                mc = mcn;
-                kat = k;
-            }
-            if (m != kNegInf) s += chunk_expsum(d, mr.c, mc);
-        } else {
-            const float tm = chunk_max(d);
-            if (tm != tm) {
-                nan_seen = true;
-            } else if (tm > m) {
-                m = tm;
-                kat = k;
-            }
-        }
-        if (++k == ck.cpr || cc + 1 == c1) {  // row segment ends
-            flush();
-            k = 0;
-            ++r;
-            if (r < first_row + nrows) mr = table ? s_desc[r - first_row] : main_row<Vec>(p, s_rs, r);
-            m = kNegInf;
-            mc = 0.f;
-            s = 0.f;
-            kat = -1;
-            nan_seen = false;
-        }
-    }
-}
-
-struct RowRes {
-    float M;    // raw row max (NaN-propagating)
-    float l2S;  // log2 sum_v 2^(x_v c - fl(M c)) (sampling rows)
-    int idx;    // lowest argmax
-};
-
-// =================================================================== commit_kernel
-// One cluster of C CTAs per request.  Every CTA of a cluster combines the
-// request's row partials and runs the acceptance scan -- the same arithmetic on
-// the same data, so all of them reach the same decision -- and then reduces its
-// share of the one row the request still needs: the first rejected target row j
-// (correction), or row k_b (bonus draw, or greedy argmax when every draft
-// matched).
-//  * Positions are independent until the scan, so one warp per draft position
-//    combines that position's target and draft rows, decides its acceptance bit
-//    and, if it rejects, scores the correction candidates that the main pass
-//    left (the segment argmaxes of the target row).  One barrier later the first
-//    rejected position is known together with a bound for its Gumbel-max.
-//  * The job row is cut into 8 C units; CTA r takes units r, r + C, r + 2C, ...,
-//    one per warp, so the shares interleave across the vocabulary and the work,
-//    which follows the logits (and the Zipf-like prior of real vocabularies),
-//    spreads evenly.  Units are staged into shared memory by bulk copies, in
-//    rounds of at most kRoundMaxBytes.
-//  * The CTAs' results meet in rank 0's shared memory; rank 0 writes the outputs.
-// Everything stays in fp32 and 32-bit integers: sm_103a has little fp64
-// throughput, and a software 64-bit division per warp and row would cost more
-// than the combine itself (the main pass's CTA ranges come from a table that
-// each CTA builds once, one division per thread).
-constexpr int kCommitThreads = 256;
+// =================================================================== shared by the commit and early-exit kernels
+// The job row's exact draws: staged units of a row in shared memory, the pruned
+// Gumbel-max over them (live lists, Philox blocks drawn only for groups that can
+// still win), CTA reductions.  Everything stays in fp32 and 32-bit integers:
+// sm_103a has little fp64 throughput.
+constexpr int kCommitThreads = 256;           // early-exit CTA threads
 constexpr int kCommitWarps = kCommitThreads / 32;
 constexpr int kCommitBlocksPerSM = 4;
 constexpr int kMaxCluster = 8;
-constexpr int kUnitsPerCTA = kCommitWarps;  // row units per CTA: one per warp
-constexpr int kShareMaxBytes = 36 * 1024;   // row bytes per CTA before the cluster grows
-constexpr int kRoundMaxBytes = 40 * 1024;   // bytes staged per round
+constexpr int kUnitsPerCTA = kCommitWarps;  // early exit: row units per CTA, one per warp
+constexpr int kShareMaxBytes = 36 * 1024;   // early exit: row bytes per CTA before the cluster grows
+constexpr int kRoundMaxBytes = 40 * 1024;   // early exit: bytes staged per round
 constexpr int kUnitGroups = 4;              // groups of four each lane tests per block
 constexpr int kBlockGroups = 32 * kUnitGroups;  // groups per block (the unit of work of a warp)
 constexpr int kLiveMax = 64 + kBlockGroups;     // a warp's live list: < 64 carried over + one block
-constexpr int kLocalScanMax = 1024;         // B up to which each CTA counts rows itself
-constexpr int kCommitSmemMax = 64 * 1024;   // dynamic shared memory limit set on the kernel
-constexpr int kMaxCtas = 1024;              // main-pass CTAs the range table holds
+constexpr int kLocalScanMax = 1024;         // B up to which each commit CTA counts rows itself
+constexpr int kCommitSmemMax = 64 * 1024;   // dynamic shared memory limit set on the kernels
 
 enum JobKind : int { JOB_NONE = 0, JOB_RESID = 1, JOB_BONUS = 2, JOB_ARGMAX = 3 };
 
@@ -478,9 +297,6 @@ struct CommitParams {
     const float *temperature;  // NULL: every request greedy
     uint64_t seed;
     uint32_t step;
-    const int *row_start;      // from main_kernel; read only when B > kLocalScanMax
-    const Part *parts;
-    int nseg, G, cpr;
     int C, ue, NS, slot;       // cluster size, entries per unit, units per round, bytes per unit slot
     int32_t *out_tokens;
     int32_t *out_accepted;
@@ -494,7 +310,7 @@ struct PosRes {
     int rej;          // sampling: draft i rejected; greedy: target argmax != x_i
     int tidx;         // target row argmax
     float shift, Cd;  // log p_v = x_v / T - shift and log q_v = y_v / T - Cd on row i
-    float seed;       // best exact correction score among the row's segment argmaxes
+    float seed;       // best exact correction score known before the draw (-inf: none)
     int seed_idx;     // its index, -1 if none
     int nonfinite;    // a row of position i holds NaN or +inf, or is all -inf
     float pad;
@@ -503,15 +319,30 @@ struct PosRes {
 struct JobDesc {
     int kind, row, A, token;  // token: the greedy mismatch's argmax (JOB_NONE)
     float invT, shift, Cd;    // z = x invT - shift is log p (correction) or x / T (bonus); q likewise with Cd
-    float seed;               // exact score of the correction's best seed candidate
+    float seed;               // exact score of the correction's best seed candidate (-inf: none)
     int seed_idx;
+    int status;               // the request's status so far
+    uint32_t epoch;           // tag of the call that decided it
 };
 
-struct __align__(16) SliceRes {  // one CTA's result, pushed into rank 0's shared memory
+struct RowRes {
+    float M;    // raw row max (NaN-propagating)
+    float l2S;  // log2 sum_v 2^(x_v c - fl(M c)) (sampling rows)
+    int idx;    // lowest argmax
+};
+
+struct __align__(16) SliceRes {  // one CTA's result of a job row share
     float best;    // best exact score (Gumbel-max) or largest finite value (argmax)
     int idx;       // its lowest index, -1 if none
     float rawmax;  // NaN-propagating max of every raw value the CTA read
     int failed;    // a bounded wait gave up
+};
+
+struct __align__(16) PieceRes {  // a commit piece's result, stored for the last piece
+    float best;
+    int idx;
+    float rawmax;
+    uint32_t tag;  // the call's tag; its complement when a bounded wait gave up
 };
 
 // Exact score of the correction draw at one entry: log(p - q) + g, with p > q.
@@ -662,8 +493,9 @@ __device__ __forceinline__ int zfilter_block(const UnitView &u, int k, int gb, i
 // the warp's best afterwards.
 template <int ESZ>
 __device__ __forceinline__ void live_round(const uint32_t *lg, const float *lz, int base, int n,
-                                           const UnitView *uvs, const JobDesc &jd, const CommitParams &p,
-                                           uint32_t b, const char *drow, float &thr, float &best, int &bidx) {
+                                           const UnitView *uvs, const JobDesc &jd, uint64_t seed, uint32_t step,
+                                           int dtype, uint32_t b, const char *drow, float &thr, float &best,
+                                           int &bidx) {
     const int lane = threadIdx.x & 31;
     const bool resid = jd.kind == JOB_RESID;
     const uint32_t purpose = resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS;
@@ -680,7 +512,7 @@ __device__ __forceinline__ void live_round(const uint32_t *lg, const float *lz, 
     }
     uint4 r4[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) r4[h] = rand_group(p.seed, p.step, b, (uint32_t)jd.row, purpose, gk[h] >> 3);
+    for (int h = 0; h < 2; ++h) r4[h] = rand_group(seed, step, b, (uint32_t)jd.row, purpose, gk[h] >> 3);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         // any survivor needs 1 - u_k <= e^(z_k - thr) <= e^(zmax - thr); the largest
@@ -696,7 +528,7 @@ __device__ __forceinline__ void live_round(const uint32_t *lg, const float *lz, 
                 const uint32_t wd = word_of(r4[h], q);
                 if (one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
                     const int v = 4 * g + q;
-                    const float sc = entry_score(resid, jd.invT, jd.Cd, drow, p.dtype, z, v, wd);
+                    const float sc = entry_score(resid, jd.invT, jd.Cd, drow, dtype, z, v, wd);
                     // -inf: no residual mass at v, never a candidate (a row without any
                     // must reach the degenerate fallback)
                     if (sc > kNegInf && better(sc, v, best, bidx)) { best = sc; bidx = v; }
@@ -709,8 +541,9 @@ __device__ __forceinline__ void live_round(const uint32_t *lg, const float *lz, 
 }
 
 // Reduce (best, idx) with the lowest index on ties, rawmax NaN-propagating and
-// failed as an or over the CTA; every thread returns the CTA's result.
-__device__ __forceinline__ SliceRes block_reduce(SliceRes r, SliceRes *red) {
+// failed as an or over a CTA of nwarps warps; every thread returns the CTA's
+// result.
+__device__ __forceinline__ SliceRes block_reduce_n(SliceRes r, SliceRes *red, int nwarps) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     warp_argmax(r.best, r.idx);
     r.rawmax = warp_max_nan(r.rawmax);
@@ -719,7 +552,7 @@ __device__ __forceinline__ SliceRes block_reduce(SliceRes r, SliceRes *red) {
     if (lane == 0) red[warp] = r;
     __syncthreads();
     SliceRes o = red[0];
-    for (int w = 1; w < kCommitWarps; ++w) {
+    for (int w = 1; w < nwarps; ++w) {
         const SliceRes q = red[w];
         if (better(q.best, q.idx, o.best, o.idx)) { o.best = q.best; o.idx = q.idx; }
         o.rawmax = max_nan_f32(o.rawmax, q.rawmax);
@@ -728,91 +561,326 @@ __device__ __forceinline__ SliceRes block_reduce(SliceRes r, SliceRes *red) {
     return o;
 }
 
-// ------------------------------------------------------------------ main-pass partials
-// cf[c] = first chunk of main-pass CTA c (cf[G] = all chunks), fr[c] = its first row.
-__device__ __forceinline__ int cta_of_chunk(const int *cf, int G, int ch) {
-    int lo = 0, hi = G - 1;  // largest c with cf[c] <= ch: a CTA that holds chunk ch
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cf[mid] <= ch) lo = mid; else hi = mid - 1;
-    }
-    return lo;
+__device__ __forceinline__ SliceRes block_reduce(SliceRes r, SliceRes *red) {
+    return block_reduce_n(r, red, kCommitWarps);
 }
 
-struct RowSpan {
-    int lo, hi;  // CTAs that read the row
-    __device__ __forceinline__ int n() const { return (hi - lo + 1) * kCW; }
+// =================================================================== main_kernel
+struct MainParams {
+    const void *target;
+    const void *draft;
+    int64_t ld_row;
+    int B, Kmax, V;
+    const int32_t *cu;         // flattened layout offsets [B+1], or NULL (padded)
+    const int32_t *num_draft;
+    const float *temperature;  // NULL: every request greedy
+    int *row_start;            // [B+1], written by block 0 for commit_kernel
+    uint32_t *done;            // [B] piece counters of commit_kernel, zeroed here by block 0
+    uint32_t *best;            // [B] commit pieces' best exact score so far (ordered bits), zeroed here
+    uint32_t *ticket;          // dynamic chunk tickets (0 between calls)
+    Part *parts;               // [chunks] one per chunk of every main-pass row
+    uint16_t *cand;            // [chunks][kCW] sampling rows: the window vector holding each warp's
+                               // maximum (0xffff: none), the correction's seed candidates
+    uint32_t epoch;            // tag of this call, stored with every partial
 };
 
-__device__ __forceinline__ RowSpan row_span(const int *cf, int G, int cpr, int r) {
-    return {cta_of_chunk(cf, G, r * cpr), cta_of_chunk(cf, G, r * cpr + cpr - 1)};
+// What every thread of a main-pass CTA needs about one chunk (written by thread 0).
+struct ChunkDesc {
+    const char *a0;  // 16-byte aligned start of the chunk's window
+    uint32_t bytes;  // window bytes (a multiple of 16)
+    int e0, e1;      // row elements [e0, e1) of the chunk
+    int shift;       // window element 0 is row element e0 - shift
+    float c;         // log2(e) / T, or 0 for a greedy row
+    uint32_t t;      // the chunk (flat index); >= total when the CTA is done
+};
+
+// Row r of the main pass (request order; inside a request, sampling rows are
+// [target 0..k-1 | draft 0..k-1] and greedy rows [target 0..k-1]).
+// sc[b] = log2(e) / T_b (0: greedy), computed once per CTA with the row scan.
+template <class Vec>
+__device__ __forceinline__ ChunkDesc chunk_desc(const MainParams &p, const int *rs, const float *sc,
+                                                const Chunking &ck, uint32_t t, uint32_t total) {
+    ChunkDesc d;
+    d.t = t;
+    d.a0 = nullptr;
+    d.bytes = 0;
+    d.e0 = d.e1 = d.shift = 0;
+    d.c = 0.f;
+    if (t >= total) return d;
+    const int r = (int)(t / (uint32_t)ck.cpr), k = (int)(t - (uint32_t)r * (uint32_t)ck.cpr);
+    const int b = find_request(rs, p.B, r);
+    const int local = r - rs[b];
+    const ReqBase rb = req_base(p.cu, p.num_draft, p.Kmax, b);
+    const float c = sc[b];
+    const int64_t rowbytes = p.ld_row * Vec::ESIZE;
+    const char *row = (c == 0.f || local < rb.kb) ? (const char *)p.target + (rb.t0 + local) * rowbytes
+                                                   : (const char *)p.draft + (rb.d0 + (local - rb.kb)) * rowbytes;
+    const ChunkWin w = chunk_window(row, Vec::ESIZE, p.V, ck, k);
+    d.a0 = w.a0;
+    d.bytes = w.bytes;
+    d.e0 = w.e0;
+    d.e1 = w.e1;
+    d.shift = w.shift;
+    d.c = c;
+    return d;
 }
 
-// Partial q of row r, or nullptr for a CTA with an empty range (possible when
-// there are fewer chunks than CTAs: such CTAs sit between a row's first and last).
-__device__ __forceinline__ const Part *part_at(const Part *parts, const int *cf, const int *fr, int nseg, int r,
-                                               const RowSpan &sp, int q) {
-    const int cta = sp.lo + q / kCW;
-    if (cf[cta] == cf[cta + 1]) return nullptr;
-    return &parts[part_slot(cta, nseg, r - fr[cta], q % kCW)];
-}
+struct WarpStat {
+    float m;  // NaN-propagating max of the warp's entries
+    float s;  // sampling: sum 2^(x c - fl(m c)); greedy: unused
+    int idx;  // greedy: lowest index of m (-1: none)
+    int pad;
+};
 
-// Combine one row's partials held at most two per lane (ok[h]: slot h holds one;
-// slot 0 holds the lower partial index, so ties keep the lowest entry index).
-__device__ __forceinline__ RowRes finish_row(const Part (&pt)[2], const bool (&ok)[2], float c, bool greedy) {
-    const float M = warp_max_nan(max_nan_f32(ok[0] ? pt[0].m : kNegInf, ok[1] ? pt[1].m : kNegInf));
-    const float MC = M * c;
-    float sum = 0.f;
-    float bm = kNegInf;
-    int bi = -1;
+// Lowest index of the warp maximum M among a thread group's vectors t0 .. t0+NV-1
+// of a chunk (greedy rows).  Entry e of vector t of thread ct is element
+// ebase + (ct + kCT t) VE + e, so the first t whose vector maximum equals M, then
+// the lowest lane holding it, then that lane's first entry, give the lowest index.
+template <int T0, class Vec, int NV>
+__device__ __forceinline__ int warp_first_index(const Vec (&d)[NV], const float (&vm)[NV], float M, int ebase,
+                                                int ct) {
+    if (!(M > kNegInf)) return -1;  // all -inf (or NaN): no argmax here
+    int idx = -1;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        if (!ok[h]) continue;
-        if (!greedy && pt[h].m != kNegInf && pt[h].s != 0.f) sum += pt[h].s * exp2f(pt[h].m * c - MC);
-        if (better(pt[h].m, pt[h].idx, bm, bi)) { bm = pt[h].m; bi = pt[h].idx; }
+    for (int t = 0; t < NV; ++t) {
+        const unsigned bal = __ballot_sync(0xffffffffu, vm[t] == M);
+        if (idx < 0 && bal) {
+            int e = Vec::VE;
+#pragma unroll
+            for (int q = Vec::VE - 1; q >= 0; --q)
+                if (d[t].get(q) == M) e = q;
+            const int mine = ebase + (ct + kCT * (T0 + t)) * Vec::VE + e;
+            idx = __shfl_sync(0xffffffffu, mine, __ffs(bal) - 1);
+        }
     }
-    warp_argmax(bm, bi);
-    RowRes res;
-    res.M = M;
-    res.idx = bi;
-    res.l2S = greedy ? 0.f : log2f(warp_sum(sum));
-    return res;
+    return idx;
 }
 
-// Combine one row's partials, any number of them (two passes over the partials).
-__device__ RowRes combine_row(const Part *parts, const int *cf, const int *fr, int nseg, int r, const RowSpan &sp,
-                              float c, bool greedy) {
+// Loads vectors t0 .. t0+NV-1 of this thread's share of a chunk (vector t of thread
+// ct is window vector ct + kCT t); entries outside the chunk read as -inf.
+template <int T0, class Vec, int NV>
+__device__ __forceinline__ void load_half(Vec (&d)[NV], const ChunkDesc &cd, int ct) {
+    const int nvec = (int)(cd.bytes >> 4);
+    const int64_t ebase = (int64_t)cd.e0 - cd.shift;
+#pragma unroll
+    for (int t = 0; t < NV; ++t) {
+        const int j = ct + kCT * (T0 + t);
+        d[t] = j < nvec ? Vec::load(cd.a0, j) : Vec::neg_inf();
+    }
+    if (cd.shift != 0 || ebase + (int64_t)nvec * Vec::VE != cd.e1) {
+#pragma unroll
+        for (int t = 0; t < NV; ++t) {
+            const int j = ct + kCT * (T0 + t);
+            if (j < nvec && (j == 0 || j == nvec - 1)) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, cd.e0, cd.e1);
+        }
+    }
+}
+
+// A new maximum tm replaces the running one m when it is larger, or NaN; a NaN m
+// is never replaced (a later all -inf window must not hide it).
+__device__ __forceinline__ bool raises_max(float tm, float m) { return m == m && (tm > m || tm != tm); }
+
+// A lane's running statistics over one half of a chunk: m its max, mc = fl(m c),
+// s = sum 2^(x c - mc) (sampling rows; the max moves, and s is rescaled, only when
+// a half holds a larger entry).  Returns the half's lane max (NaN-propagating).
+// For sampling rows it also keeps mv, the vector (T0 + t) where the lane's max was
+// last raised: a cheap pointer to the warp's argmax, kept as a correction seed.
+template <int T0, class Vec, int NV>
+__device__ __forceinline__ float half_stats(const Vec (&d)[NV], float (&vm)[NV], float c, float &m, float &mc,
+                                            float &s, int &mv) {
+#pragma unroll
+    for (int t = 0; t < NV; ++t) vm[t] = d[t].vmax();
+    float tm = vm[0];
+    int tv = 0;
+#pragma unroll
+    for (int t = 1; t < NV; ++t) {
+        if (vm[t] > tm) tv = t;
+        tm = max_nan_f32(tm, vm[t]);
+    }
+    if (c != 0.f) {
+        if (raises_max(tm, m)) {
+            const float mcn = __fmul_rn(tm, c);
+            s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
+            m = tm;
+            mc = mcn;
+            mv = T0 + tv;
+        }
+        if (m != kNegInf) s += chunk_expsum(d, c, mc);
+    } else {
+        m = max_nan_f32(m, tm);
+    }
+    return tm;
+}
+
+// One row's statistics from its cpr per-chunk partials (pp[0 .. cpr), read through
+// L2: other CTAs of this kernel wrote them); a warp.  stale: some partial does not
+// carry this call's tag (a chunk the main pass did not write in this call).
+__device__ __forceinline__ Part load_part(const Part *pp) {
+    const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(pp));
+    Part x;
+    x.m = __uint_as_float(w.x);
+    x.s = __uint_as_float(w.y);
+    x.idx = (int)w.z;
+    x.epoch = w.w;
+    return x;
+}
+
+__device__ __forceinline__ RowRes combine_parts(const Part *pp, int cpr, float c, bool greedy, uint32_t epoch,
+                                                bool &stale) {
     const int lane = threadIdx.x & 31;
-    float m = kNegInf;
-    for (int q = lane; q < sp.n(); q += 32) {
-        const Part *pt = part_at(parts, cf, fr, nseg, r, sp, q);
-        if (pt) m = max_nan_f32(m, pt->m);
+    // a lane holds partials lane and lane + 32; rows of more than 64 chunks reread the rest
+    const Part p0 = lane < cpr ? load_part(pp + lane) : Part{kNegInf, 0.f, -1, epoch};
+    const Part p1 = lane + 32 < cpr ? load_part(pp + lane + 32) : Part{kNegInf, 0.f, -1, epoch};
+    bool st = p0.epoch != epoch || p1.epoch != epoch;
+    float m = max_nan_f32(p0.m, p1.m);
+    for (int q = lane + 64; q < cpr; q += 32) {
+        const Part x = load_part(pp + q);
+        st |= x.epoch != epoch;
+        m = max_nan_f32(m, x.m);
     }
+    stale |= __any_sync(0xffffffffu, st);
     const float M = warp_max_nan(m);
-    const float MC = M * c;
+    const float MC = __fmul_rn(M, c);
     float sum = 0.f;
-    float bm = kNegInf;
-    int bi = -1;
-    for (int q = lane; q < sp.n(); q += 32) {
-        const Part *pt = part_at(parts, cf, fr, nseg, r, sp, q);
-        if (!pt) continue;
-        if (!greedy && pt->m != kNegInf && pt->s != 0.f) sum += pt->s * exp2f(pt->m * c - MC);
-        if (better(pt->m, pt->idx, bm, bi)) { bm = pt->m; bi = pt->idx; }
-    }
-    warp_argmax(bm, bi);
-    RowRes res;
-    res.M = M;
-    res.idx = bi;
-    res.l2S = greedy ? 0.f : log2f(warp_sum(sum));
-    return res;
+    uint32_t bi = 0xffffffffu;
+    auto take = [&](const Part &x) {
+        if (!greedy && x.m != kNegInf && x.s != 0.f) sum += x.s * exp2f(__fmul_rn(x.m, c) - MC);
+        if (greedy && x.m == M && x.idx >= 0) bi = min(bi, (uint32_t)x.idx);
+    };
+    take(p0);
+    take(p1);
+    for (int q = lane + 64; q < cpr; q += 32) take(load_part(pp + q));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) bi = min(bi, __shfl_xor_sync(0xffffffffu, bi, o));
+    RowRes r;
+    r.M = M;
+    r.idx = (int)bi;
+    r.l2S = greedy ? 0.f : log2f(warp_sum(sum));
+    return r;
 }
 
+// Every needed row once, in chunks of at most 64 KB handed out by dynamic tickets:
+// a CTA's first two chunks are its block index and that plus the grid size, every
+// later one comes from an atomic counter, two chunks ahead, so that every thread
+// knows the next chunk while it still reduces the current one.  Each thread holds
+// a chunk's kVPT 16-byte vectors in two halves and reloads a half with the next
+// chunk's as soon as it has reduced it, so its loads never stop for the
+// reductions, the barrier and the CTA-level combine that end each chunk.  Per
+// chunk: warp maxima and exp-sums (greedy rows: warp maxima and their lowest
+// indices), combined across the CTA's warps by warp 0 into one Part per chunk,
+// stored at the chunk's index; on sampling rows each warp also leaves a pointer to
+// the vector holding its maximum, the correction draw's seed candidates.
+template <class Vec>
+__global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams p) {
+    constexpr int kH = kVPT / 2;  // vectors per half
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ WarpStat s_ws[2][kCW];
+    __shared__ ChunkDesc s_desc[3];
+    int *s_rs = (int *)smem;                                   // [B+1] first main-pass row of each request
+    float *s_c = (float *)(smem + sizeof(int) * (size_t)(p.B + 1));  // [B] log2(e) / T (0: greedy)
+    scan_request_rows(s_rs, p.B, p.cu, p.num_draft, p.temperature, p.Kmax);  // ends with __syncthreads
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+        const float T = p.temperature ? p.temperature[i] : 0.f;
+        s_c[i] = (T > 0.f && !isinf(T)) ? __fdiv_rn(kLog2e, T) : 0.f;
+    }
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.row_start[i] = s_rs[i];
+        for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+            p.done[i] = 0u;
+            p.best[i] = 0u;
+        }
+    }
+    pdl_launch_dependents();
+    __syncthreads();
+
+    const Chunking ck = make_chunking(p.V, Vec::ESIZE);
+    const uint32_t total = (uint32_t)s_rs[p.B] * (uint32_t)ck.cpr;  // < 2^31 (checked by the host)
+    const uint32_t G = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ct = threadIdx.x;
+    if (threadIdx.x == 0) {
+        s_desc[0] = chunk_desc<Vec>(p, s_rs, s_c, ck, blockIdx.x, total);
+        s_desc[1] = chunk_desc<Vec>(p, s_rs, s_c, ck, G + blockIdx.x, total);
+    }
+    __syncthreads();
+    // the current chunk's index, scale and first window element stay in registers;
+    // the next chunk's window is read from shared memory where it is used
+    uint32_t t = s_desc[0].t;
+    float c = s_desc[0].c;
+    int ebase = s_desc[0].e0 - s_desc[0].shift;
+    Vec a[kH], bv[kH];
+    if (t < total) {
+        load_half<0>(a, s_desc[0], ct);
+        load_half<kH>(bv, s_desc[0], ct);
+    }
+    int n = 0;
+    while (t < total) {
+        if (threadIdx.x == 0)
+            s_desc[(n + 2) % 3] = chunk_desc<Vec>(p, s_rs, s_c, ck, 2 * G + atomicAdd(p.ticket, 1u), total);
+        const ChunkDesc &nx = s_desc[(n + 1) % 3];
+        float m = kNegInf, mc = 0.f, s = 0.f;
+        int mv = -1;
+        float vma[kH], vmb[kH];
+        const float ta = half_stats<0>(a, vma, c, m, mc, s, mv);
+        int ia = -1;
+        float Ma = kNegInf;
+        if (c == 0.f) {
+            Ma = warp_max_nan(ta);
+            ia = warp_first_index<0>(a, vma, Ma, ebase, ct);
+        }
+        if (nx.t < total) load_half<0>(a, nx, ct);
+        const float tb = half_stats<kH>(bv, vmb, c, m, mc, s, mv);
+        WarpStat ws;
+        ws.pad = 0;
+        if (c != 0.f) {
+            // the lanes' sums, each relative to its own fl(m c), rescaled to the warp's
+            const float M = warp_max_nan(m);
+            const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - __fmul_rn(M, c));
+            ws.m = M;
+            ws.s = warp_sum(sc);
+            ws.idx = -1;
+            // the window vector of the lowest lane that holds the warp maximum
+            const unsigned own = __ballot_sync(0xffffffffu, m == M && mv >= 0);
+            const int src = own ? __ffs(own) - 1 : 0;
+            const int vec = __shfl_sync(0xffffffffu, mv, src);
+            if (lane == 0)
+                p.cand[(size_t)t * kCW + warp] = own ? (uint16_t)(warp * 32 + src + kCT * vec) : (uint16_t)0xffffu;
+        } else {
+            // entries of half a precede those of half b: a's index wins a tie
+            const float Mb = warp_max_nan(tb);
+            const int ib = warp_first_index<kH>(bv, vmb, Mb, ebase, ct);
+            ws.m = max_nan_f32(Ma, Mb);
+            ws.s = 0.f;
+            ws.idx = (Ma >= Mb) ? ia : ib;
+        }
+        if (nx.t < total) load_half<kH>(bv, nx, ct);
+        if (lane == 0) s_ws[n & 1][warp] = ws;
+        __syncthreads();
+        if (warp == 0) {
+            // the CTA's warps combined: max, sum relative to fl(max c), lowest argmax
+            const WarpStat q = lane < kCW ? s_ws[n & 1][lane] : WarpStat{kNegInf, 0.f, -1, 0};
+            const float Mc = warp_max_nan(q.m);
+            Part out;
+            out.m = Mc;
+            float tl = 0.f;
+            if (c != 0.f) tl = (q.m == kNegInf || q.s == 0.f) ? 0.f : q.s * exp2f(__fmul_rn(q.m, c) - __fmul_rn(Mc, c));
+            out.s = warp_sum(tl);
+            uint32_t v = (q.m == Mc && q.idx >= 0) ? (uint32_t)q.idx : 0xffffffffu;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+            out.idx = (int)v;
+            out.epoch = p.epoch;
+            if (lane == 0) p.parts[t] = out;
+        }
+        ++n;
+        t = nx.t;
+        c = nx.c;
+        ebase = nx.e0 - nx.shift;
+    }
+}
+
+// ------------------------------------------------------------------ staged job rows (early exit)
 __host__ __device__ inline size_t commit_round_bytes(int NS, int slot) {
     return ((size_t)NS * slot + 127) & ~(size_t)127;
-}
-__host__ __device__ inline size_t commit_smem_bytes(int NS, int slot, int Kmax, int G) {
-    return commit_round_bytes(NS, slot) + sizeof(PosRes) * (size_t)Kmax + sizeof(RowSpan) * 2 * (size_t)Kmax +
-           5 * sizeof(float) * (size_t)Kmax + 2 * sizeof(int) * (size_t)(G + 1);
 }
 
 // Warp-collective (one whole warp): the unit views of round rd of this CTA's share
@@ -944,11 +1012,11 @@ __device__ SliceRes job_row_rounds(const CommitParams &p, const JobDesc &jd, uin
                                                         mine.rawmax, lg, lz, nlive);
                 while (nlive >= 64) {  // draw the newest 64; the rest stay listed
                     nlive -= 64;
-                    live_round<ESZ>(lg, lz, nlive, 64, uvs, jd, p, b, drow, thr, mine.best, mine.idx);
+                    live_round<ESZ>(lg, lz, nlive, 64, uvs, jd, p.seed, p.step, p.dtype, b, drow, thr, mine.best, mine.idx);
                 }
             }
             if (nlive > 0)
-                live_round<ESZ>(lg, lz, 0, nlive, uvs, jd, p, b, drow, thr, mine.best, mine.idx);
+                live_round<ESZ>(lg, lz, 0, nlive, uvs, jd, p.seed, p.step, p.dtype, b, drow, thr, mine.best, mine.idx);
         }
         __syncthreads();  // every warp is done with the round's slots and views
         if (warp == 0 && rd + 1 < nrounds) issue_job_round<ESZ>(p, rank, jrow, rd + 1, buf, bar, uvs);
@@ -956,33 +1024,237 @@ __device__ SliceRes job_row_rounds(const CommitParams &p, const JobDesc &jd, uin
     return block_reduce(mine, red);
 }
 
+// =================================================================== commit_kernel
+// P CTAs ("pieces") per request, each with kJobThreads threads.  Every piece of
+// request b
+//  1. decides the request -- the same arithmetic on the same data in every piece,
+//     so all of them agree: it combines each row's per-chunk partials, runs the
+//     acceptance scan and finds the one row still needed (the first rejected
+//     target row j for the correction, row k_b for the bonus draw or, greedy, for
+//     the argmax when every draft matched);
+//  2. stages its units of that row -- units piece, piece + P, piece + 2P, ... of
+//     kUnitE entries, so the pieces interleave across the vocabulary and share the
+//     work of a Zipf-like head evenly -- into shared memory by bulk copies, and
+//     reduces them: the pruned Gumbel-max, or the argmax;
+//  3. stores its result and bumps the request's counter; the piece that completes
+//     the count combines the P results and writes the request's outputs.
+// No CTA waits for another: pieces meet through the counter (last arriver).
+constexpr int kJobThreads = 128;
+constexpr int kJobWarps = kJobThreads / 32;
+constexpr int kJobBlocksPerSM = 8;
+constexpr int kUnitE = 1024;       // entries per unit (a multiple of 8)
+constexpr int kUnitsPerPiece = 8;  // units a piece stages (a live group's slot index takes 3 bits)
+
+struct JobParams {
+    const void *target;
+    const void *draft;
+    int dtype;
+    int64_t ld_row;
+    int B, Kmax, V;
+    const int32_t *draft_tokens;
+    const int32_t *cu;         // flattened layout offsets [B+1], or NULL (padded)
+    const int32_t *num_draft;
+    const float *temperature;  // NULL: every request greedy
+    uint64_t seed;
+    uint32_t step;
+    uint32_t epoch;            // tag the main pass stored with this call's partials
+    const int *row_start;      // from main_kernel; read only when B > kLocalScanMax
+    const Part *parts;
+    const uint16_t *cand;      // [chunks][kCW] the main pass's seed-candidate vectors
+    int cpr, ce;               // main pass: chunks per row, entries per chunk
+    int P;                     // pieces per request
+    int slot;                  // bytes per unit slot
+    uint32_t *ticket;          // main_kernel's ticket counter, reset here for the next call
+    uint32_t *done;            // [B] pieces finished (zeroed by main_kernel)
+    uint32_t *best;            // [B] best exact score any piece has found (ordered bits; 0: none)
+    PieceRes *pres;            // [B * P]
+    int32_t *out_tokens;
+    int32_t *out_accepted;
+    float *out_p;
+    float *out_q;
+    int32_t *out_status;
+};
+
+// Float <-> unsigned with the same order (for atomicMax over scores); 0 means none.
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ordered_float(uint32_t u) {
+    if (u == 0u) return kNegInf;
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__host__ __device__ inline int job_units(int V) { return (V + kUnitE - 1) / kUnitE; }
+__host__ __device__ inline int job_pieces(int V) { return (job_units(V) + kUnitsPerPiece - 1) / kUnitsPerPiece; }
+__host__ __device__ inline int job_slot_bytes(int esz) { return ((kUnitE * esz + 32) + 127) & ~127; }
+__host__ __device__ inline size_t job_smem_bytes(int esz, int Kmax) {
+    return (size_t)kUnitsPerPiece * job_slot_bytes(esz) + sizeof(PosRes) * (size_t)Kmax +
+           sizeof(RowRes) * 2 * (size_t)Kmax + 5 * sizeof(float) * (size_t)Kmax;
+}
+
+// This piece's share of the job row, staged: the pruned Gumbel-max (correction or
+// bonus) or the argmax.  Every thread calls it and gets the CTA's result.
 template <int ESZ>
-__global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_kernel(CommitParams p) {
-    extern __shared__ __align__(128) unsigned char cdyn[];
+__device__ SliceRes job_piece(const JobParams &p, const JobDesc &jd, uint32_t b, const char *drow,
+                              const UnitView *uvs, int nu, uint32_t (*live_g)[kLiveMax],
+                              float (*live_z)[kLiveMax], SliceRes *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool resid = jd.kind == JOB_RESID;
+    constexpr int bpu = ((kUnitE / 4) + kBlockGroups - 1) / kBlockGroups;  // blocks per unit
+    const int nblk = nu * bpu;
+    SliceRes mine;
+    mine.best = kNegInf;
+    mine.idx = -1;
+    mine.rawmax = kNegInf;
+    mine.failed = 0;
+    if (jd.kind == JOB_ARGMAX) {
+        for (int bi = warp; bi < nblk; bi += kJobWarps) {
+            const UnitView uv = uvs[bi / bpu];
+            const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+            for (int g = gb + lane; g < ge; g += 32) {
+                float xv[4];
+                group_vals<ESZ>(uv, g, xv);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    mine.rawmax = max_nan_f32(mine.rawmax, xv[q]);
+                    if (better(xv[q], 4 * g + q, mine.best, mine.idx) && xv[q] > kNegInf) {
+                        mine.best = xv[q];
+                        mine.idx = 4 * g + q;
+                    }
+                }
+            }
+        }
+        return block_reduce_n(mine, red, kJobWarps);
+    }
+    // seed: the correction's comes from this piece's share of the main pass's
+    // candidates (scored while the copies landed); otherwise the exact score of each
+    // thread's largest entry bounds the draw from below.  Either way the pieces of a
+    // request share the best bound any of them knows (see below)
+    mine.best = jd.seed;
+    mine.idx = jd.seed_idx;
+    if (jd.kind != JOB_RESID) {
+        float m = kNegInf;
+        int mi = -1;
+        for (int bi = warp; bi < nblk; bi += kJobWarps) {
+            const UnitView uv = uvs[bi / bpu];
+            const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+            for (int g = gb + lane; g < ge; g += 32) {
+                float xv[4];
+                group_vals<ESZ>(uv, g, xv);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (xv[q] > m) { m = xv[q]; mi = 4 * g + q; }
+            }
+        }
+        SliceRes seed;
+        seed.best = kNegInf;
+        seed.idx = -1;
+        seed.rawmax = kNegInf;
+        seed.failed = 0;
+        if (mi >= 0) {
+            const uint4 r4 = rand_group(p.seed, p.step, b, (uint32_t)jd.row, resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS,
+                                        (uint32_t)mi >> 2);
+            const float z = fmaf(m, jd.invT, -jd.shift);
+            const float sc = entry_score(resid, jd.invT, jd.Cd, drow, p.dtype, z, mi, word_of(r4, mi & 3));
+            if (sc > kNegInf) {
+                seed.best = sc;
+                seed.idx = mi;
+            }
+        }
+        seed = block_reduce_n(seed, red, kJobWarps);
+        mine.best = seed.best;
+        mine.idx = seed.idx;
+        if (threadIdx.x == 0 && seed.best > kNegInf) atomicMax(p.best + b, ordered_bits(seed.best));
+    }
+    // The bound is shared with the request's other pieces: each publishes the best
+    // exact score it knows, and reads theirs one block ahead of using it.  Every
+    // published value is the exact score of an entry, so it never exceeds the draw's
+    // maximum and the pruning stays exact.
+    const bool share = true;
+    float thr = mine.best, published = mine.best;
+    uint32_t shared_bits = share ? ld_relaxed_u32(p.best + b) : 0u;
+    uint32_t *lg = live_g[warp];
+    float *lz = live_z[warp];
+    int nlive = 0;
+    for (int bi = warp; bi < nblk; bi += kJobWarps) {
+        const int k = bi / bpu;
+        const UnitView uv = uvs[k];
+        const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
+        if (share) {
+            thr = fmaxf(thr, ordered_float(shared_bits));
+            shared_bits = ld_relaxed_u32(p.best + b);
+            if (lane == 0 && thr > published) {
+                atomicMax(p.best + b, ordered_bits(thr));
+                published = thr;
+            }
+        }
+        if (gb >= ge) continue;
+        nlive = resid ? zfilter_block<ESZ, false>(uv, k, gb, ge, thr - kGumbelMax, jd.invT, jd.shift, mine.rawmax, lg,
+                                                  lz, nlive)
+                      : zfilter_block<ESZ, true>(uv, k, gb, ge, thr - kGumbelMax, jd.invT, jd.shift, mine.rawmax, lg,
+                                                 lz, nlive);
+        while (nlive >= 64) {  // draw the newest 64; the rest stay listed
+            nlive -= 64;
+            live_round<ESZ>(lg, lz, nlive, 64, uvs, jd, p.seed, p.step, p.dtype, b, drow, thr, mine.best, mine.idx);
+        }
+    }
+    if (nlive > 0)
+        live_round<ESZ>(lg, lz, 0, nlive, uvs, jd, p.seed, p.step, p.dtype, b, drow, thr, mine.best, mine.idx);
+    return block_reduce_n(mine, red, kJobWarps);
+}
+
+// One row's statistics from its cpr per-chunk partials, by one thread.
+__device__ __forceinline__ RowRes row_from_parts(const Part *pp, int cpr, float c, bool greedy, uint32_t epoch,
+                                                 bool &stale) {
+    float M = kNegInf;
+    for (int q = 0; q < cpr; ++q) {
+        const Part x = pp[q];
+        stale |= x.epoch != epoch;
+        M = max_nan_f32(M, x.m);
+    }
+    const float MC = __fmul_rn(M, c);
+    float sum = 0.f;
+    int bi = -1;
+    for (int q = 0; q < cpr; ++q) {
+        const Part x = pp[q];
+        if (!greedy && x.m != kNegInf && x.s != 0.f) sum += x.s * exp2f(__fmul_rn(x.m, c) - MC);
+        if (greedy && x.m == M && x.idx >= 0 && (bi < 0 || x.idx < bi)) bi = x.idx;
+    }
+    RowRes r;
+    r.M = M;
+    r.idx = bi;
+    r.l2S = greedy ? 0.f : log2f(sum);
+    return r;
+}
+
+template <int ESZ>
+__global__ void __launch_bounds__(kJobThreads, kJobBlocksPerSM) commit_kernel(JobParams p) {
+    extern __shared__ __align__(128) unsigned char jdyn[];
     __shared__ uint64_t s_bar;
-    __shared__ uint32_t s_live_g[kCommitWarps][kLiveMax];
-    __shared__ float s_live_z[kCommitWarps][kLiveMax];
-    __shared__ SliceRes s_red[kCommitWarps];
-    __shared__ SliceRes s_inbox[kMaxCluster];
-    __shared__ UnitView s_uv[kUnitsPerCTA];
+    __shared__ uint32_t s_live_g[kJobWarps][kLiveMax];
+    __shared__ float s_live_z[kJobWarps][kLiveMax];
+    __shared__ SliceRes s_red[kJobWarps];
+    __shared__ UnitView s_uv[kUnitsPerPiece];
     __shared__ JobDesc s_job;
-    __shared__ int s_sum[2 * kCommitWarps];
+    __shared__ int s_sum[2 * kJobWarps];
+    __shared__ int s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t rank = cluster_ctarank();
-    const int b = blockIdx.x / p.C;
-    cluster_arrive_relaxed();  // paired with the wait before the first remote store
-
-    unsigned char *buf = cdyn;
-    PosRes *s_pos = (PosRes *)(cdyn + commit_round_bytes(p.NS, p.slot));
-    RowSpan *s_span = (RowSpan *)(s_pos + p.Kmax);  // [target rows | draft rows]
-    float *s_xt = (float *)(s_span + 2 * p.Kmax);    // target logit at x_i
-    float *s_xd = s_xt + p.Kmax;                     // draft logit at x_i
-    float *s_l2u = s_xd + p.Kmax;                    // log2 of the acceptance uniform u_i
+    const int b = blockIdx.x / p.P, piece = blockIdx.x - b * p.P;
+    unsigned char *slots = jdyn;
+    PosRes *s_pos = (PosRes *)(jdyn + (size_t)kUnitsPerPiece * p.slot);
+    RowRes *s_rows = (RowRes *)(s_pos + p.Kmax);  // [2 Kmax] target rows, then draft rows
+    float *s_xt = (float *)(s_rows + 2 * p.Kmax); // target logit at x_i
+    float *s_xd = s_xt + p.Kmax;                  // draft logit at x_i
+    float *s_l2u = s_xd + p.Kmax;                 // log2 of the acceptance uniform u_i
     float *s_pp = s_l2u + p.Kmax;
     float *s_qq = s_pp + p.Kmax;
-    int *s_cf = (int *)(s_qq + p.Kmax);
-    int *s_fr = s_cf + (p.G + 1);
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         mbar_init_fence();
@@ -1003,14 +1275,14 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
     const int32_t *x = p.draft_tokens + rbase.d0;
     if (status == SPEC_STATUS_OK) {
         bool bad = false;
-        for (int i = tid; i < kb; i += kCommitThreads) bad |= (x[i] < 0 || x[i] >= p.V);
+        for (int i = tid; i < kb; i += kJobThreads) bad |= (x[i] < 0 || x[i] >= p.V);
         if (__syncthreads_or(bad)) status = SPEC_STATUS_BAD_TOKEN;
     }
     const float c = greedy ? 0.f : __fdiv_rn(kLog2e, T);
     const float invT = greedy ? 0.f : __fdiv_rn(1.f, T);
     const int npos = status == SPEC_STATUS_OK ? kb : 0;
     if (!greedy) {
-        for (int i = tid; i < npos; i += kCommitThreads) {
+        for (int i = tid; i < npos; i += kJobThreads) {
             const int xi = x[i];
             s_xt[i] = load_logit(p.target, p.dtype, (rbase.t0 + i) * p.ld_row + xi);
             s_xd[i] = load_logit(p.draft, p.dtype, (rbase.d0 + i) * p.ld_row + xi);
@@ -1018,149 +1290,68 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
             s_l2u[i] = log2f(u01(r4.x));
         }
     }
-    // flat main-pass index of this request's first row, the number of rows, the
-    // main pass's CTA ranges and the CTAs that read each row of this request
-    int r0 = 0, R = 0;
+    // flat main-pass index of this request's first row
+    int r0 = 0;
     if (p.B <= kLocalScanMax) {
-        int before = 0, all = 0;
-        for (int bb = tid; bb < p.B; bb += kCommitThreads) {
-            const int n = request_main_rows(p.cu, p.num_draft, p.temperature, p.Kmax, bb);
-            all += n;
-            if (bb < b) before += n;
-        }
+        int before = 0;
+        for (int bb = tid; bb < b; bb += kJobThreads)
+            before += request_main_rows(p.cu, p.num_draft, p.temperature, p.Kmax, bb);
         before = warp_sum_i(before);
-        all = warp_sum_i(all);
-        if (lane == 0) {
-            s_sum[warp] = before;
-            s_sum[kCommitWarps + warp] = all;
-        }
+        if (lane == 0) s_sum[warp] = before;
         __syncthreads();
-        for (int w = 0; w < kCommitWarps; ++w) {
-            r0 += s_sum[w];
-            R += s_sum[kCommitWarps + w];
-        }
-    } else {
-        pdl_wait();
-        r0 = p.row_start[b];
-        R = p.row_start[p.B];
-    }
-    const int64_t total = (int64_t)R * p.cpr;
-    for (int cc = tid; cc <= p.G; cc += kCommitThreads) {
-        const int64_t f = cta_first(total, p.G, cc);
-        s_cf[cc] = (int)f;
-        s_fr[cc] = (int)(f / p.cpr);
-    }
-    __syncthreads();
-    const int nrows = greedy ? npos : 2 * npos;  // flat rows r0 .. r0 + nrows - 1
-    for (int rr = tid; rr < nrows; rr += kCommitThreads) {
-        const int slot = rr < npos ? rr : p.Kmax + (rr - npos);
-        s_span[slot] = row_span(s_cf, p.G, p.cpr, r0 + rr);
+        for (int w = 0; w < kJobWarps; ++w) r0 += s_sum[w];
     }
     pdl_wait();
+    // ---- main_kernel is complete from here on
+    if (blockIdx.x == 0 && tid == 0) *p.ticket = 0u;  // every ticket of this call is taken
+    if (p.B > kLocalScanMax) r0 = p.row_start[b];
+    const int nrows = greedy ? npos : 2 * npos;  // flat rows r0 .. r0 + nrows - 1
+    const int items = nrows * p.cpr;
+    const bool staged = (size_t)items * sizeof(Part) <= (size_t)kUnitsPerPiece * p.slot;
+    const Part *gparts = p.parts + (int64_t)r0 * p.cpr;
+    Part *s_parts = (Part *)slots;  // the unit slots hold the partials until the job is known
+    if (staged)
+        for (int it = tid; it < items; it += kJobThreads) s_parts[it] = gparts[it];
     __syncthreads();
+    const Part *rp = staged ? s_parts : gparts;
 
-    // ---- main_kernel's partials are complete from here on
-    const int nw = status == SPEC_STATUS_OK ? npos : 0;
-    // one warp per draft position: target row i (flat r0 + i) and, sampling, draft
-    // row i (flat r0 + k_b + i)
-    for (int i = warp; i < nw; i += kCommitWarps) {
-        const int rt = r0 + i, rd = r0 + kb + i;
-        const RowSpan st = s_span[i];
-        const RowSpan sd = greedy ? st : s_span[p.Kmax + i];
-        const bool fast = st.n() <= 64 && sd.n() <= 64;  // at most two partials per lane and row
-        const char *drow = (const char *)p.draft + (rbase.d0 + i) * p.ld_row * ESZ;
-        Part pt[2] = {}, pd[2] = {};  // this lane's target partials: correction candidates
-        bool okt[2] = {false, false}, okd[2] = {false, false};
-        float dv[2] = {0.f, 0.f};  // draft logits at the candidates, fetched before they are known to be needed
-        RowRes tr, dr;
-        if (fast) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int q = lane + 32 * h;
-                if (q < st.n()) {
-                    const Part *pp = part_at(p.parts, s_cf, s_fr, p.nseg, rt, st, q);
-                    if (pp) { pt[h] = *pp; okt[h] = true; }
-                }
-                if (!greedy && q < sd.n()) {
-                    const Part *pp = part_at(p.parts, s_cf, s_fr, p.nseg, rd, sd, q);
-                    if (pp) { pd[h] = *pp; okd[h] = true; }
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                if (!greedy && okt[h] && pt[h].idx >= 0) dv[h] = load_logit(drow, p.dtype, pt[h].idx);
-            tr = finish_row(pt, okt, c, greedy);
-            if (!greedy) dr = finish_row(pd, okd, c, false);
-        } else {
-            tr = combine_row(p.parts, s_cf, s_fr, p.nseg, rt, st, c, greedy);
-            if (!greedy) dr = combine_row(p.parts, s_cf, s_fr, p.nseg, rd, sd, c, false);
-        }
+    // ---- the decision: one thread per row, then one thread per position
+    bool stale = false;
+    for (int r = tid; r < nrows; r += kJobThreads)
+        s_rows[r] = row_from_parts(rp + (int64_t)r * p.cpr, p.cpr, c, greedy && r < npos, p.epoch, stale);
+    stale = __syncthreads_or(stale);
+    for (int i = tid; i < npos; i += kJobThreads) {
+        const RowRes tr = s_rows[i];
         PosRes pr;
         pr.tidx = tr.idx;
-        // A NaN can leave a lane's running max finite again (a later chunk's max
-        // replaces it) but not its sum, so sampling rows check the sums too.
-        pr.nonfinite = !(fabsf(tr.M) < __int_as_float(0x7f800000)) ||
-                       (!greedy && !(fabsf(dr.M) < __int_as_float(0x7f800000) &&
-                                     fabsf(tr.l2S) < __int_as_float(0x7f800000) &&
-                                     fabsf(dr.l2S) < __int_as_float(0x7f800000)));
         pr.shift = pr.Cd = 0.f;
         pr.seed = kNegInf;
         pr.seed_idx = -1;
         pr.pad = 0.f;
         if (greedy) {
+            pr.nonfinite = !(fabsf(tr.M) < __int_as_float(0x7f800000));
             pr.rej = tr.idx != x[i];
         } else {
-            const float l2p = fmaf(s_xt[i], c, -(tr.M * c)) - tr.l2S;  // log2 p_i(x_i)
-            const float l2q = fmaf(s_xd[i], c, -(dr.M * c)) - dr.l2S;  // log2 q_i(x_i)
+            const RowRes dr = s_rows[npos + i];
+            // a NaN leaves its chunk's max NaN; +inf makes the sum NaN: both show here
+            pr.nonfinite = !(fabsf(tr.M) < __int_as_float(0x7f800000) && fabsf(dr.M) < __int_as_float(0x7f800000) &&
+                             fabsf(tr.l2S) < __int_as_float(0x7f800000) &&
+                             fabsf(dr.l2S) < __int_as_float(0x7f800000));
+            const float l2p = fmaf(s_xt[i], c, -__fmul_rn(tr.M, c)) - tr.l2S;  // log2 p_i(x_i)
+            const float l2q = fmaf(s_xd[i], c, -__fmul_rn(dr.M, c)) - dr.l2S;  // log2 q_i(x_i)
             // accept iff u q < p, i.e. log2 u < log2 p - log2 q (Q = 0 < P accepts; P = 0 rejects)
             pr.rej = !(s_l2u[i] < l2p - l2q);
-            // log p_v = x_v / T - (M c + log2 S) ln 2, and q likewise
-            pr.shift = (tr.M * c + tr.l2S) * 0.6931471805599453f;
-            pr.Cd = (dr.M * c + dr.l2S) * 0.6931471805599453f;
-            if (lane == 0) {
-                s_pp[i] = exp2f(l2p);
-                s_qq[i] = exp2f(l2q);
-            }
-            if (pr.rej && !pr.nonfinite) {
-                // exact correction scores at the segment argmaxes of target row i
-                float sb = kNegInf;
-                int si = -1;
-                for (int q = lane; q < st.n(); q += 32) {
-                    const bool h1 = q >= 32;  // the fast path holds partial q in slot q / 32
-                    Part cand = h1 ? pt[1] : pt[0];
-                    bool ok = h1 ? okt[1] : okt[0];
-                    float dq = h1 ? dv[1] : dv[0];
-                    if (!fast) {
-                        const Part *qq = part_at(p.parts, s_cf, s_fr, p.nseg, rt, st, q);
-                        ok = qq != nullptr;
-                        if (ok) {
-                            cand = *qq;
-                            if (cand.idx >= 0) dq = load_logit(drow, p.dtype, cand.idx);
-                        }
-                    }
-                    if (!ok || cand.idx < 0) continue;
-                    const int v = cand.idx;
-                    const float z = fmaf(cand.m, invT, -pr.shift);
-                    const float lq = fmaf(dq, invT, -pr.Cd);
-                    if (!(lq < z)) continue;  // no residual mass at v
-                    const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_RESIDUAL,
-                                                (uint32_t)v >> 2);
-                    const float sc = resid_score(z, lq, word_of(r4, v & 3));
-                    if (sc > kNegInf && better(sc, v, sb, si)) { sb = sc; si = v; }
-                }
-                warp_argmax(sb, si);
-                pr.seed = sb;
-                pr.seed_idx = si;
-            }
+            // log p_v = x_v / T - (fl(M c) + log2 S) ln 2, and q likewise
+            pr.shift = (__fmul_rn(tr.M, c) + tr.l2S) * 0.6931471805599453f;
+            pr.Cd = (__fmul_rn(dr.M, c) + dr.l2S) * 0.6931471805599453f;
+            s_pp[i] = exp2f(l2p);
+            s_qq[i] = exp2f(l2q);
         }
-        if (lane == 0) s_pos[i] = pr;
+        s_pos[i] = pr;
     }
     __syncthreads();
 
-    // ---- the scan (warp 0): A = first rejected position; it then starts the job
-    // row's first round of copies
-    const int64_t rowbytes = p.ld_row * ESZ;
-    auto issue_round = [&](const char *jrow, int rd) { issue_job_round<ESZ>(p, rank, jrow, rd, buf, &s_bar, s_uv); };
+    // ---- the scan (warp 0): A = first rejected position, and the job
     if (warp == 0) {
         JobDesc jd;
         jd.kind = JOB_NONE;
@@ -1171,7 +1362,9 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
         jd.shift = jd.Cd = 0.f;
         jd.seed = kNegInf;
         jd.seed_idx = -1;
+        jd.epoch = p.epoch;
         int st = status;
+        if (st == SPEC_STATUS_OK && stale) st = SPEC_STATUS_INTERNAL;
         if (st == SPEC_STATUS_OK) {
             bool nf = false;
             for (int i = lane; i < kb; i += 32) nf |= s_pos[i].nonfinite != 0;
@@ -1198,50 +1391,136 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
                 jd.row = A;
                 jd.shift = pr.shift;
                 jd.Cd = pr.Cd;
-                jd.seed = pr.seed;
-                jd.seed_idx = pr.seed_idx;
             } else {
                 jd.kind = JOB_BONUS;
                 jd.row = kb;
             }
         }
-        if (jd.kind != JOB_NONE)
-            issue_round((const char *)p.target + (rbase.t0 + jd.row) * rowbytes, 0);
-        if (lane == 0) {
-            s_job = jd;
-            s_sum[0] = st;
-        }
+        jd.status = st;
+        if (lane == 0) s_job = jd;
     }
     __syncthreads();
-    const JobDesc jd = s_job;
-    status = s_sum[0];
-
-    // ---- this CTA's units of the job row (round 0 is in flight)
-    const char *jrow = (const char *)p.target + (rbase.t0 + jd.row) * rowbytes;
-    const char *drow = jd.kind == JOB_RESID ? (const char *)p.draft + (rbase.d0 + jd.row) * rowbytes : nullptr;
-    const SliceRes res = job_row_rounds<ESZ>(p, jd, (uint32_t)b, rank, jrow, drow, buf, &s_bar, s_uv, s_live_g,
-                                             s_live_z, s_red);
-
-    // ---- the CTAs' results meet in rank 0
-    cluster_wait();  // every CTA of the cluster is running
-    if (tid == 0) st_cluster_v4(&s_inbox[rank], 0, make_uint4(__float_as_uint(res.best), (uint32_t)res.idx,
-                                                               __float_as_uint(res.rawmax), (uint32_t)res.failed));
-    cluster_arrive();
-    cluster_wait();
-    if (rank != 0) return;
+    JobDesc jd = s_job;
+    status = jd.status;
 
     int token = jd.token;
-    if (status == SPEC_STATUS_OK && jd.kind != JOB_NONE) {
-        SliceRes o = s_inbox[0];
-        for (int r = 1; r < p.C; ++r) {
-            const SliceRes q = s_inbox[r];
-            if (better(q.best, q.idx, o.best, o.idx)) { o.best = q.best; o.idx = q.idx; }
-            o.rawmax = max_nan_f32(o.rawmax, q.rawmax);
-            o.failed |= q.failed;
+    bool writer = piece == 0;
+    const int64_t rowbytes = p.ld_row * ESZ;
+    if (jd.kind != JOB_NONE) {
+        // ---- this piece's units of the job row: one bulk copy each, one barrier phase
+        const char *jrow = (const char *)p.target + (rbase.t0 + jd.row) * rowbytes;
+        const char *drow = jd.kind == JOB_RESID ? (const char *)p.draft + (rbase.d0 + jd.row) * rowbytes : nullptr;
+        const int nunits = job_units(p.V);
+        const int nu = min(kUnitsPerPiece, (nunits - piece + p.P - 1) / p.P);
+        if (warp == 0) {
+            const Chunking uk = {nunits, kUnitE};
+            ChunkWin w;
+            w.bytes = 0;
+            UnitView uv;
+            uv.slot = slots + (size_t)lane * p.slot;
+            uv.sbase = uv.e1 = uv.g0 = uv.g1 = 0;
+            uv.aligned = 0;
+            if (lane < nu) {
+                w = chunk_window(jrow, ESZ, p.V, uk, piece + p.P * lane);
+                uv.sbase = w.e0 - w.shift;
+                uv.e1 = w.e1;
+                uv.g0 = w.e0 >> 2;
+                uv.g1 = (w.e1 + 3) >> 2;
+                uv.aligned = (w.shift & 3) == 0;
+            }
+            if (lane < kUnitsPerPiece) s_uv[lane] = uv;
+            const int bytes = warp_sum_i((int)w.bytes);
+            if (lane == 0) mbar_arrive_expect_tx(&s_bar, (uint32_t)bytes);
+            __syncwarp();
+            if (w.bytes) bulk_g2s(slots + (size_t)lane * p.slot, w.a0, w.bytes, &s_bar);
         }
-        if (o.failed) status = SPEC_STATUS_INTERNAL;
-        else if (jd.kind != JOB_RESID && !(fabsf(o.rawmax) < __int_as_float(0x7f800000)))
-            status = SPEC_STATUS_NONFINITE;
+        // correction: this piece's share of the seed candidates of row A (the vector
+        // holding each warp's maximum of each main-pass chunk), scored while the
+        // copies land; the best one is shared with the other pieces
+        if (jd.kind == JOB_RESID) {
+            constexpr int VE = 16 / ESZ;
+            const Chunking mk = {p.cpr, p.ce};
+            const uint16_t *cands = p.cand + ((int64_t)r0 + jd.row) * p.cpr * kCW;
+            SliceRes sd;
+            sd.best = kNegInf;
+            sd.idx = -1;
+            sd.rawmax = kNegInf;
+            sd.failed = 0;
+            for (int q = piece + p.P * tid; q < p.cpr * kCW; q += p.P * kJobThreads) {
+                const uint32_t j = cands[q];
+                const ChunkWin w = chunk_window(jrow, ESZ, p.V, mk, q / kCW);
+                if (j == 0xffffu || (j + 1) * 16 > w.bytes) continue;
+                const uint4 raw = ld_stream_v4(w.a0 + 16 * (size_t)j);
+                const int ebase = w.e0 - w.shift + (int)j * VE;
+                float best = kNegInf;
+                int bv = -1;
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const int v = ebase + e;
+                    const float xv = ESZ == 2 ? VecBF16{raw}.get(e) : VecF32{raw}.get(e);
+                    if (v >= w.e0 && v < w.e1 && xv > best) { best = xv; bv = v; }
+                }
+                if (bv < 0) continue;
+                const float z = fmaf(best, jd.invT, -jd.shift);
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
+                                            (uint32_t)bv >> 2);
+                const float sc = entry_score(true, jd.invT, jd.Cd, drow, p.dtype, z, bv, word_of(r4, bv & 3));
+                if (sc > kNegInf && better(sc, bv, sd.best, sd.idx)) { sd.best = sc; sd.idx = bv; }
+            }
+            sd = block_reduce_n(sd, s_red, kJobWarps);
+            jd.seed = sd.best;
+            jd.seed_idx = sd.idx;
+            if (tid == 0 && sd.best > kNegInf) atomicMax(p.best + b, ordered_bits(sd.best));
+        }
+        // one thread waits (bounded), the others then take the completed phase
+        bool ok = true;
+        if (tid == 0) ok = mbar_wait(&s_bar, 0, kWaitNs);
+        SliceRes res;
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) mbar_wait(&s_bar, 0, kWaitNs);  // the copies in flight, bounded
+            res.best = kNegInf;
+            res.idx = -1;
+            res.rawmax = kNegInf;
+            res.failed = 1;
+        } else {
+            mbar_try_wait(&s_bar, 0);
+            res = job_piece<ESZ>(p, jd, (uint32_t)b, drow, s_uv, nu, s_live_g, s_live_z, s_red);
+        }
+        // ---- the pieces meet: the last to finish combines them
+        if (tid == 0) {
+            PieceRes pr;
+            pr.best = res.best;
+            pr.idx = res.idx;
+            pr.rawmax = res.rawmax;
+            pr.tag = res.failed ? ~p.epoch : p.epoch;
+            p.pres[(int64_t)b * p.P + piece] = pr;
+            __threadfence();
+            s_last = atomicAdd(p.done + b, 1u) == (uint32_t)(p.P - 1);
+        }
+        __syncthreads();
+        writer = s_last != 0;
+        if (!writer) return;
+        __threadfence();
+        SliceRes o;
+        o.best = kNegInf;
+        o.idx = -1;
+        o.rawmax = kNegInf;
+        o.failed = 0;
+        for (int q = tid; q < p.P; q += kJobThreads) {
+            const uint4 w4 = __ldcg((const uint4 *)(p.pres + (int64_t)b * p.P + q));
+            if (better(__uint_as_float(w4.x), (int)w4.y, o.best, o.idx)) {
+                o.best = __uint_as_float(w4.x);
+                o.idx = (int)w4.y;
+            }
+            o.rawmax = max_nan_f32(o.rawmax, __uint_as_float(w4.z));
+            o.failed |= w4.w != p.epoch;
+        }
+        o = block_reduce_n(o, s_red, kJobWarps);
+        if (status == SPEC_STATUS_OK) {
+            if (o.failed) status = SPEC_STATUS_INTERNAL;
+            else if (jd.kind != JOB_RESID && !(fabsf(o.rawmax) < __int_as_float(0x7f800000)))
+                status = SPEC_STATUS_NONFINITE;
+        }
         token = o.idx;
         if (status == SPEC_STATUS_OK && jd.kind == JOB_RESID && o.idx < 0) {
             // p <= q everywhere (only by rounding): draw from p_j with the same noise
@@ -1251,7 +1530,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
             f.idx = -1;
             f.rawmax = kNegInf;
             f.failed = 0;
-            for (int v = tid; v < p.V; v += kCommitThreads) {
+            for (int v = tid; v < p.V; v += kJobThreads) {
                 const float lp = fmaf(load_logit(p.target, p.dtype, trow + v), jd.invT, -jd.shift);
                 if (!(lp > kNegInf)) continue;
                 const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
@@ -1259,21 +1538,22 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) commit_ker
                 const float sc = lp + gumbel_of_word(word_of(r4, v & 3));
                 if (better(sc, v, f.best, f.idx)) { f.best = sc; f.idx = v; }
             }
-            token = block_reduce(f, s_red).idx;
+            token = block_reduce_n(f, s_red, kJobWarps).idx;
         }
     }
+    if (!writer) return;
 
     // ---- outputs of request b
-    const bool ok = status == SPEC_STATUS_OK;
-    const int A = ok ? jd.A : 0;
+    const bool okst = status == SPEC_STATUS_OK;
+    const int A = okst ? jd.A : 0;
     int32_t *tok = p.out_tokens + rbase.t0;
-    for (int i = tid; i < rbase.ntok; i += kCommitThreads)
-        tok[i] = !ok ? -1 : (i < A ? x[i] : (i == A ? token : -1));
-    const bool pq = ok && !greedy;
+    for (int i = tid; i < rbase.ntok; i += kJobThreads)
+        tok[i] = !okst ? -1 : (i < A ? x[i] : (i == A ? token : -1));
+    const bool pq = okst && !greedy;
     if (p.out_p)
-        for (int i = tid; i < rbase.npq; i += kCommitThreads) p.out_p[rbase.d0 + i] = pq && i < kb ? s_pp[i] : -1.f;
+        for (int i = tid; i < rbase.npq; i += kJobThreads) p.out_p[rbase.d0 + i] = pq && i < kb ? s_pp[i] : -1.f;
     if (p.out_q)
-        for (int i = tid; i < rbase.npq; i += kCommitThreads) p.out_q[rbase.d0 + i] = pq && i < kb ? s_qq[i] : -1.f;
+        for (int i = tid; i < rbase.npq; i += kJobThreads) p.out_q[rbase.d0 + i] = pq && i < kb ? s_qq[i] : -1.f;
     if (tid == 0) {
         p.out_status[b] = status;
         p.out_accepted[b] = A;
@@ -1333,8 +1613,8 @@ __device__ void ee_thread_stats(const ChunkWin &w, float c, float &m, float &mc,
 #pragma unroll
         for (int t = 1; t < kEEVecs; ++t) tm = max_nan_f32(tm, d[t].vmax());
         if (c != 0.f) {
-            if (!(tm <= m)) {
-                const float mcn = tm * c;
+            if (raises_max(tm, m)) {
+                const float mcn = __fmul_rn(tm, c);
                 s = (m == kNegInf) ? 0.f : s * ex2_approx(mc - mcn);
                 m = tm;
                 mc = mcn;
@@ -1389,7 +1669,7 @@ __device__ void ee_block_stats(float m, float mc, float s, int widx, bool nan_se
     float Mw, Sw = 0.f;
     if (c != 0.f) {
         Mw = warp_max_nan(m);
-        const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - Mw * c);
+        const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - __fmul_rn(Mw, c));
         Sw = warp_sum(sc);
     } else {
         const bool any_nan = __any_sync(0xffffffffu, nan_seen);
@@ -1409,7 +1689,7 @@ __device__ void ee_block_stats(float m, float mc, float s, int widx, bool nan_se
     float ab = kNegInf;
     I = -1;
     for (int w = 0; w < kCommitWarps; ++w) {
-        if (c != 0.f && wm[w] != kNegInf && ws[w] != 0.f) S += ws[w] * exp2f(wm[w] * c - M * c);
+        if (c != 0.f && wm[w] != kNegInf && ws[w] != 0.f) S += ws[w] * exp2f(__fmul_rn(wm[w], c) - __fmul_rn(M, c));
         if (better(wm[w], wi[w], ab, I)) { ab = wm[w]; I = wi[w]; }
     }
 }
@@ -1588,8 +1868,8 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
             int It = -1;
             for (int r = 0; r < p.C; ++r) {
                 const EEPart q = s_all[r];
-                if (!greedy && q.mt != kNegInf && q.st != 0.f) St += q.st * exp2f(q.mt * c - Mt * c);
-                if (!greedy && q.md != kNegInf && q.sd != 0.f) Sd += q.sd * exp2f(q.md * c - Md * c);
+                if (!greedy && q.mt != kNegInf && q.st != 0.f) St += q.st * exp2f(__fmul_rn(q.mt, c) - __fmul_rn(Mt, c));
+                if (!greedy && q.md != kNegInf && q.sd != 0.f) Sd += q.sd * exp2f(__fmul_rn(q.md, c) - __fmul_rn(Md, c));
                 if (better(q.mt, q.it, bm, It)) { bm = q.mt; It = q.it; }
             }
             if (nonfinite(Mt) || (!greedy && (nonfinite(Md) || nonfinite(St) || nonfinite(Sd)))) {
@@ -1605,8 +1885,8 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
                 continue;
             }
             const float l2St = log2f(St), l2Sd = log2f(Sd);
-            const float l2p = fmaf(s_xt[i], c, -(Mt * c)) - l2St;  // log2 p_i(x_i)
-            const float l2q = fmaf(s_xd[i], c, -(Md * c)) - l2Sd;  // log2 q_i(x_i)
+            const float l2p = fmaf(s_xt[i], c, -__fmul_rn(Mt, c)) - l2St;  // log2 p_i(x_i)
+            const float l2q = fmaf(s_xd[i], c, -__fmul_rn(Md, c)) - l2Sd;  // log2 q_i(x_i)
             if (tid == 0) {
                 s_pp[i] = exp2f(l2p);
                 s_qq[i] = exp2f(l2q);
@@ -1616,8 +1896,8 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
             A = i;
             jd.kind = JOB_RESID;
             jd.row = i;
-            jd.shift = (Mt * c + l2St) * 0.6931471805599453f;
-            jd.Cd = (Md * c + l2Sd) * 0.6931471805599453f;
+            jd.shift = (__fmul_rn(Mt, c) + l2St) * 0.6931471805599453f;
+            jd.Cd = (__fmul_rn(Md, c) + l2Sd) * 0.6931471805599453f;
             // exact correction scores at this CTA's warp argmaxes of target row i; the
             // best over the cluster bounds the draw
             const char *drow = (const char *)p.draft + (rbase.d0 + i) * rowbytes;
@@ -1784,27 +2064,47 @@ struct ProfScope {
     }
 };
 
+// Workspace of the two-kernel verify (caller-owned, 256-byte aligned pieces):
+//   ticket     main_kernel's chunk-ticket counter: zero before the first call,
+//              and every call leaves it zero (commit_kernel resets it);
+//   row_start  [B+1] first main-pass row of each request;
+//   done       [B] commit pieces finished (zeroed by main_kernel in every call);
+//   best       [B] the commit pieces' shared bound (zeroed by main_kernel);
+//   parts      one Part per chunk of every main-pass row (B * rows * cpr);
+//   cand       kCW seed-candidate vectors per chunk (B * rows * cpr * kCW, 16-bit);
+//   pres       [B * P] commit pieces' results.
 struct Layout {
-    size_t off_row_start, off_parts, total;
-    int nseg, G, cpr;  // main pass: partial segments per CTA, CTAs, chunks per row
-    int C, ue, NS, slot;  // commit pass: cluster size, entries per unit, units per round, bytes per slot
+    size_t off_ticket, off_row_start, off_done, off_best, off_parts, off_cand, off_pres, total;
+    int cpr;                 // main pass: chunks per row
+    int P, jslot;            // commit: pieces per request, bytes per unit slot
+    int C, ue, NS, slot;     // early exit: cluster size, entries per unit, units per round, bytes per slot
 };
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-Layout make_layout(int B, int Kmax, int V, int esz, int sms, int main_rows_per_request) {
+Layout make_layout(int B, int Kmax, int V, int esz, int main_rows_per_request) {
     Layout L;
-    L.G = kMainBlocksPerSM * sms;
     const Chunking ck = make_chunking(V, esz);
     L.cpr = ck.cpr;
-    L.nseg = segs_per_cta((int64_t)B * main_rows_per_request * ck.cpr, L.G, ck.cpr);
+    L.P = job_pieces(V);
+    L.jslot = job_slot_bytes(esz);
     size_t o = 0;
+    L.off_ticket = o;
+    o = align256(o + 16);
     L.off_row_start = o;
     o = align256(o + sizeof(int) * (size_t)(B + 1));
+    L.off_done = o;
+    o = align256(o + sizeof(uint32_t) * (size_t)B);
+    L.off_best = o;
+    o = align256(o + sizeof(uint32_t) * (size_t)B);
     L.off_parts = o;
-    o = align256(o + sizeof(Part) * (size_t)L.G * L.nseg * kCW);
+    o = align256(o + sizeof(Part) * (size_t)B * (size_t)main_rows_per_request * (size_t)ck.cpr);
+    L.off_cand = o;
+    o = align256(o + sizeof(uint16_t) * kCW * (size_t)B * (size_t)main_rows_per_request * (size_t)ck.cpr);
+    L.off_pres = o;
+    o = align256(o + sizeof(PieceRes) * (size_t)B * (size_t)L.P);
     L.total = o;
-    // commit pass: a row splits into 8 C units, C CTAs (one cluster) per request with
+    // early exit: a row splits into 8 C units, C CTAs (one cluster) per request with
     // one unit per warp; a CTA's share stays near kShareMaxBytes, and its units are
     // staged NS at a time (NS a power of two, so that the warps split evenly)
     const int64_t rowb = (int64_t)V * esz;
@@ -1824,8 +2124,33 @@ int check_launch() {
     return SPEC_OK;
 }
 
-// Dynamic shared memory of main_kernel: the row scan and the row descriptors.
-size_t main_extra(int B) { return sizeof(int) * (size_t)(((B + 1) + 3) & ~3) + sizeof(MainRow) * kMaxDesc; }
+// Tag of a call: every partial the main pass writes carries it, and the commit pass
+// reports status 5 for a request whose partials do not (a chunk the main pass did
+// not write in this call, as after a workspace that was not zeroed before first use).
+std::atomic<uint32_t> g_epoch{0};
+
+uint32_t next_epoch() {
+    uint32_t e;
+    do {
+        e = g_epoch.fetch_add(1u) + 1u;
+    } while (e == 0u || e == 0xffffffffu);
+    return e;
+}
+
+// The device pointer p must belong to device dev (or be managed memory).
+int check_device_pointer(const void *p, int dev) {
+    cudaPointerAttributes a;
+    const cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_EINVAL;
+    }
+    if (a.type == cudaMemoryTypeManaged) return SPEC_OK;
+    return (a.type == cudaMemoryTypeDevice && a.device == dev) ? SPEC_OK : SPEC_EINVAL;
+}
+
+// Dynamic shared memory of main_kernel: the row scan and the per-request scales.
+size_t main_extra(int B) { return sizeof(int) * (size_t)(B + 1) + sizeof(float) * (size_t)B; }
 
 template <class Vec>
 int set_smem_attrs(int dev) {
@@ -1833,11 +2158,13 @@ int set_smem_attrs(int dev) {
     if (g_attr_set[dev][which]) return SPEC_OK;
     cudaError_t e = cudaFuncSetAttribute(commit_kernel<Vec::ESIZE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kCommitSmemMax);
-    // the largest shared-memory carveout, so that kCommitBlocksPerSM CTAs fit an SM
-    // and every cluster of a launch is resident at once
+    // the largest shared-memory carveout, so that kJobBlocksPerSM pieces fit an SM
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(commit_kernel<Vec::ESIZE>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(main_kernel<Vec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)main_extra(SPEC_MAX_BATCH));
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     g_attr_set[dev][which] = true;
     return SPEC_OK;
@@ -1880,34 +2207,30 @@ int launch_early_exit(int dev, const Layout &L, const CommitParams &cp, cudaStre
 }
 
 template <class Vec>
-int launch_all(int dev, const Layout &L, const MainParams &mp, const CommitParams &cp, cudaStream_t st) {
-    int rc = set_smem_attrs<Vec>(dev);
+int launch_all(int dev, int sms, const Layout &L, const MainParams &mp, const JobParams &jp, cudaStream_t st) {
+    int rc;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        rc = set_smem_attrs<Vec>(dev);
+    }
     if (rc) return rc;
     {
         ProfScope ps(st);
-        main_kernel<Vec><<<L.G, kCT, main_extra(mp.B), st>>>(mp);
+        main_kernel<Vec><<<kMainBlocksPerSM * sms, kCT, main_extra(mp.B), st>>>(mp);
     }
     if ((rc = check_launch())) return rc;
     ProfScope ps(st);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(mp.B * L.C));
-    cfg.blockDim = dim3(kCommitThreads);
-    cfg.dynamicSmemBytes = commit_smem_bytes(L.NS, L.slot, mp.Kmax, L.G);
+    cfg.gridDim = dim3((unsigned)((int64_t)mp.B * L.P));
+    cfg.blockDim = dim3(kJobThreads);
+    cfg.dynamicSmemBytes = job_smem_bytes(Vec::ESIZE, mp.Kmax);
     cfg.stream = st;
-    cudaLaunchAttribute attr[3];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)L.C;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    // let a cluster share SMs, so that clusters placed while main_kernel drains do
-    // not fragment the free slots and leave later clusters waiting for a second wave
-    attr[2].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
-    attr[2].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
     cfg.attrs = attr;
-    cfg.numAttrs = 3;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kernel<Vec::ESIZE>, cp);
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kernel<Vec::ESIZE>, jp);
     if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
     return SPEC_OK;
 }
@@ -1930,18 +2253,20 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     int dev = 0, sms = 0;
     int rc = device_info(&dev, &sms);
     if (rc) return rc;
-    if (kMainBlocksPerSM * sms > kMaxCtas) return SPEC_EUNSUPPORTED;
-    const Layout L = make_layout(B, Kmax, V, esz, sms, sample ? 2 * Kmax : Kmax);
-    // chunk indices of the main pass and commit units are 32-bit; one unit slot
-    // must fit a staging round
-    if ((int64_t)B * 2 * Kmax * L.cpr >= ((int64_t)1 << 31) || L.slot > kRoundMaxBytes) return SPEC_EUNSUPPORTED;
+    if ((rc = check_device_pointer(target, dev))) return rc;
+    const Layout L = make_layout(B, Kmax, V, esz, sample ? 2 * Kmax : Kmax);
+    // chunk indices of the main pass are 32-bit; the commit grid is B * P CTAs
+    if ((int64_t)B * 2 * Kmax * L.cpr >= ((int64_t)1 << 31) || (int64_t)B * L.P >= ((int64_t)1 << 31))
+        return SPEC_EUNSUPPORTED;
+    if (job_smem_bytes(esz, Kmax) > (size_t)kCommitSmemMax) return SPEC_EUNSUPPORTED;
     if (!ws) return SPEC_EWORKSPACE;
-    if (ws_bytes < L.total) return SPEC_EWORKSPACE;
+    if (ws_bytes < L.total || ((uintptr_t)ws & 255)) return SPEC_EWORKSPACE;
     rc = prof_prepare();
     if (rc) return rc;
 
     char *w = (char *)ws;
     const float *temps = sample ? temperature : nullptr;
+    const uint32_t epoch = next_epoch();
 
     MainParams mp;
     mp.target = target;
@@ -1954,40 +2279,48 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     mp.num_draft = num_draft;
     mp.temperature = temps;
     mp.row_start = (int *)(w + L.off_row_start);
+    mp.done = (uint32_t *)(w + L.off_done);
+    mp.best = (uint32_t *)(w + L.off_best);
+    mp.ticket = (uint32_t *)(w + L.off_ticket);
     mp.parts = (Part *)(w + L.off_parts);
-    mp.nseg = L.nseg;
+    mp.cand = (uint16_t *)(w + L.off_cand);
+    mp.epoch = epoch;
 
-    CommitParams cp;
-    cp.target = target;
-    cp.draft = draft;
-    cp.dtype = dtype;
-    cp.ld_row = ld_row;
-    cp.B = B;
-    cp.Kmax = Kmax;
-    cp.V = V;
-    cp.draft_tokens = draft_tokens;
-    cp.cu = cu;
-    cp.num_draft = num_draft;
-    cp.temperature = temps;
-    cp.seed = seed;
-    cp.step = (uint32_t)step;
-    cp.row_start = mp.row_start;
-    cp.parts = mp.parts;
-    cp.nseg = L.nseg;
-    cp.G = L.G;
-    cp.cpr = L.cpr;
-    cp.C = L.C;
-    cp.ue = L.ue;
-    cp.NS = L.NS;
-    cp.slot = L.slot;
-    cp.out_tokens = out_tokens;
-    cp.out_accepted = out_accepted;
-    cp.out_p = sample ? out_p : nullptr;
-    cp.out_q = sample ? out_q : nullptr;
-    cp.out_status = out_status;
+    JobParams jp;
+    jp.target = target;
+    jp.draft = draft;
+    jp.dtype = dtype;
+    jp.ld_row = ld_row;
+    jp.B = B;
+    jp.Kmax = Kmax;
+    jp.V = V;
+    jp.draft_tokens = draft_tokens;
+    jp.cu = cu;
+    jp.num_draft = num_draft;
+    jp.temperature = temps;
+    jp.seed = seed;
+    jp.step = (uint32_t)step;
+    jp.epoch = epoch;
+    jp.row_start = mp.row_start;
+    jp.parts = mp.parts;
+    jp.cand = mp.cand;
+    jp.cpr = L.cpr;
+    jp.ce = make_chunking(V, esz).ce;
+    jp.P = L.P;
+    jp.slot = L.jslot;
+    jp.ticket = mp.ticket;
+    jp.done = mp.done;
+    jp.best = mp.best;
+    jp.pres = (PieceRes *)(w + L.off_pres);
+    jp.out_tokens = out_tokens;
+    jp.out_accepted = out_accepted;
+    jp.out_p = sample ? out_p : nullptr;
+    jp.out_q = sample ? out_q : nullptr;
+    jp.out_status = out_status;
 
     cudaStream_t st = (cudaStream_t)cuda_stream;
-    return dtype == SPEC_BF16 ? launch_all<VecBF16>(dev, L, mp, cp, st) : launch_all<VecF32>(dev, L, mp, cp, st);
+    return dtype == SPEC_BF16 ? launch_all<VecBF16>(dev, sms, L, mp, jp, st)
+                              : launch_all<VecF32>(dev, sms, L, mp, jp, st);
 }
 
 // Scratch of spec_verify_sample_noalloc: part of this module's device image, one
@@ -2025,7 +2358,8 @@ int early_exit_impl(const void *target, const void *draft, int dtype, int B, int
     int dev = 0, sms = 0;
     int rc = device_info(&dev, &sms);
     if (rc) return rc;
-    const Layout L = make_layout(B, Kmax, V, esz, sms, sample ? 2 * Kmax : Kmax);
+    if ((rc = check_device_pointer(target, dev))) return rc;
+    const Layout L = make_layout(B, Kmax, V, esz, sample ? 2 * Kmax : Kmax);
     if (L.slot > kRoundMaxBytes || ee_smem_bytes(L.NS, L.slot, Kmax) > (size_t)kCommitSmemMax)
         return SPEC_EUNSUPPORTED;
     rc = prof_prepare();
@@ -2068,9 +2402,7 @@ extern "C" {
 size_t spec_verify_workspace_size(int B, int Kmax, int V, int dtype) {
     if (B < 0 || Kmax < 0 || V <= 0 || (dtype != SPEC_BF16 && dtype != SPEC_F32)) return 0;
     if (B > SPEC_MAX_BATCH || Kmax > SPEC_MAX_DRAFTS) return 0;
-    int dev = 0, sms = 0;
-    if (device_info(&dev, &sms)) return 0;
-    return make_layout(B, Kmax, V, dtype == SPEC_BF16 ? 2 : 4, sms, 2 * Kmax).total;
+    return make_layout(B, Kmax, V, dtype == SPEC_BF16 ? 2 : 4, 2 * Kmax).total;
 }
 
 int spec_verify_greedy(const void *target, int dtype, int B, int Kmax, int V, int64_t ld_row,
@@ -2104,7 +2436,7 @@ int spec_verify_sample_noalloc(const void *target, const void *draft, int dtype,
     int dev = 0, sms = 0;
     int rc = device_info(&dev, &sms);
     if (rc) return rc;
-    if (make_layout(B, Kmax, V, dtype == SPEC_BF16 ? 2 : 4, sms, 2 * Kmax).total > SPEC_STATIC_SCRATCH_BYTES)
+    if (make_layout(B, Kmax, V, dtype == SPEC_BF16 ? 2 : 4, 2 * Kmax).total > SPEC_STATIC_SCRATCH_BYTES)
         return SPEC_ESCRATCH;
     void *ws = nullptr;
     if ((rc = static_scratch(dev, &ws))) return rc;

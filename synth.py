@@ -1,7 +1,9 @@
 """Seeded synthetic inputs for the verify/commit step and the verify-length scheduler.
 
 Shared by the tests (both the CUDA path and the oracle are fed from here) and by
-bench.py.  This module holds none of the verify method's arithmetic: it only draws
+bench.py.  Every generator draws on the CPU by default; with ``device`` given, the
+same recipe draws with that device's generator (other numbers from the same data
+seed), which is how bench.py makes its large batches quickly.  This module holds none of the verify method's arithmetic: it only draws
 logits, drafts, temperatures and confidences with ``torch.Generator`` on the CPU.
 Draft tokens are drawn the way a drafter would propose them (a categorical draw
 from softmax(draft / T) with torch's own sampler, or the draft's argmax when T = 0);
@@ -37,14 +39,14 @@ WORKLOADS = {"tiny": 1, "small": 2, "main": 3, "ragged": 4, "stress": 5}
 ZIPF_S = 1.1
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator()
+def _gen(seed: int, device=None) -> torch.Generator:
+    g = torch.Generator(device=device) if device is not None else torch.Generator()
     g.manual_seed(int(seed))
     return g
 
 
-def zipf_prior(V: int) -> torch.Tensor:
-    return -ZIPF_S * torch.log(torch.arange(V, dtype=torch.float64) + 1.0)
+def zipf_prior(V: int, device=None) -> torch.Tensor:
+    return -ZIPF_S * torch.log(torch.arange(V, dtype=torch.float64, device=device) + 1.0)
 
 
 def _round(x: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:
@@ -62,8 +64,8 @@ def _draw_drafts(d_rows: torch.Tensor, T: float, g: torch.Generator) -> torch.Te
 
 def make_batch(B: int, K: int, V: int, dtype: torch.dtype, seed: int, *, t_sigma: float = 3.0,
                zipf: bool = False, noise_sigmas=(1.0,), temperature=(1.0, 1.0), greedy_mask=None,
-               num_draft=None, unused_fill: float | None = None) -> dict:
-    """Draw one padded verify batch on the CPU.
+               num_draft=None, unused_fill: float | None = None, device=None) -> dict:
+    """Draw one padded verify batch (on the CPU, or with device's generator there).
 
     temperature: (lo, hi) for T_b ~ U[lo, hi] (lo == hi: constant).
     noise_sigmas: per-request draft noise sigma drawn uniformly from this tuple.
@@ -71,26 +73,28 @@ def make_batch(B: int, K: int, V: int, dtype: torch.dtype, seed: int, *, t_sigma
     num_draft: optional int [B] (ragged k_b); rows beyond it are filled with
     ``unused_fill`` (default NaN) so that reading them is detectable.
     """
-    g = _gen(seed)
-    prior = zipf_prior(V) if zipf else None
-    target = torch.empty((B, K + 1, V), dtype=dtype)
-    draft = torch.empty((B, K, V), dtype=dtype)
-    tokens = torch.zeros((B, K), dtype=torch.int32)
+    g = _gen(seed, device)
+    prior = zipf_prior(V, device) if zipf else None
+    target = torch.empty((B, K + 1, V), dtype=dtype, device=device)
+    draft = torch.empty((B, K, V), dtype=dtype, device=device)
+    tokens = torch.zeros((B, K), dtype=torch.int32, device=device)
     lo, hi = temperature
-    temps = (lo + (hi - lo) * torch.rand(B, generator=g, dtype=torch.float64)).to(torch.float32)
-    sig_idx = torch.randint(0, len(noise_sigmas), (B,), generator=g)
+    temps = (lo + (hi - lo) * torch.rand(B, generator=g, dtype=torch.float64, device=device)).to(torch.float32)
+    sig_idx = torch.randint(0, len(noise_sigmas), (B,), generator=g, device=device).tolist()
     if greedy_mask is not None:
-        temps = torch.where(torch.as_tensor(greedy_mask), torch.zeros_like(temps), temps)
+        temps = torch.where(torch.as_tensor(greedy_mask, device=device), torch.zeros_like(temps), temps)
+    temps_h = temps.tolist()
     fill = float("nan") if unused_fill is None else unused_fill
     for b in range(B):
         kb = K if num_draft is None else int(num_draft[b])
-        t = t_sigma * torch.randn((K + 1, V), generator=g, dtype=torch.float64)
+        t = t_sigma * torch.randn((K + 1, V), generator=g, dtype=torch.float64, device=device)
         if prior is not None:
             t = t + prior
-        d = t[:K] + noise_sigmas[int(sig_idx[b])] * torch.randn((K, V), generator=g, dtype=torch.float64)
+        d = t[:K] + noise_sigmas[int(sig_idx[b])] * torch.randn((K, V), generator=g, dtype=torch.float64,
+                                                                device=device)
         tb = _round(t, dtype)
         db = _round(d, dtype)
-        T = float(temps[b])
+        T = float(temps_h[b])
         if kb > 0:
             tokens[b, :kb] = _draw_drafts(db[:kb], T, g)
         if kb < K:
@@ -99,27 +103,27 @@ def make_batch(B: int, K: int, V: int, dtype: torch.dtype, seed: int, *, t_sigma
         target[b] = tb
         draft[b] = db
     return dict(target=target, draft=draft, draft_tokens=tokens,
-                num_draft=None if num_draft is None else torch.as_tensor(num_draft, dtype=torch.int32),
+                num_draft=None if num_draft is None else torch.as_tensor(num_draft, dtype=torch.int32, device=device),
                 temperature=temps, B=B, K=K, V=V, dtype=dtype)
 
 
-def tiny(step: int = 0) -> dict:
+def tiny(step: int = 0, device=None) -> dict:
     b = make_batch(1, 4, 1024, torch.float32, 1000 * 1 + step, t_sigma=3.0, noise_sigmas=(1.0,),
-                   temperature=(1.0, 1.0))
+                   temperature=(1.0, 1.0), device=device)
     b.update(seed=1, step=step, name="tiny")
     return b
 
 
-def small(step: int = 0, V: int = 32000) -> dict:
+def small(step: int = 0, V: int = 32000, device=None) -> dict:
     b = make_batch(8, 8, V, torch.bfloat16, 1000 * 2 + step, t_sigma=3.0, zipf=True,
-                   noise_sigmas=(0.25, 0.5, 1.0, 2.0), temperature=(0.8, 0.8))
+                   noise_sigmas=(0.25, 0.5, 1.0, 2.0), temperature=(0.8, 0.8), device=device)
     b.update(seed=2, step=step, name="small")
     return b
 
 
-def main(step: int = 0, B: int = 64) -> dict:
+def main(step: int = 0, B: int = 64, device=None) -> dict:
     b = make_batch(B, 7, 151936, torch.bfloat16, 1000 * 3 + step, t_sigma=4.0, zipf=True,
-                   noise_sigmas=(1.0,), temperature=(0.6, 1.0))
+                   noise_sigmas=(1.0,), temperature=(0.6, 1.0), device=device)
     b.update(seed=3, step=step, name="main")
     return b
 
@@ -163,17 +167,17 @@ def _gamma(shape: float, size, g: torch.Generator) -> torch.Tensor:
     return out.view(size)
 
 
-def ragged(step: int = 0, num_draft=None, V: int = 129280, B: int = 256, Kmax: int = 16) -> dict:
+def ragged(step: int = 0, num_draft=None, V: int = 129280, B: int = 256, Kmax: int = 16, device=None) -> dict:
     """Verify inputs of the ragged workload: 'small'-style logits at V, k_b = num_draft."""
     if num_draft is None:
         num_draft = [Kmax] * B
     b = make_batch(B, Kmax, V, torch.bfloat16, 1000 * 4 + 500 + step, t_sigma=3.0, zipf=True,
-                   noise_sigmas=(0.25, 0.5, 1.0, 2.0), temperature=(0.8, 0.8), num_draft=num_draft)
+                   noise_sigmas=(0.25, 0.5, 1.0, 2.0), temperature=(0.8, 0.8), num_draft=num_draft, device=device)
     b.update(seed=4, step=step, name="ragged")
     return b
 
 
-def stress(step: int = 0, B: int = 512, V: int = 151936, n_adv: int = 8) -> dict:
+def stress(step: int = 0, B: int = 512, V: int = 151936, n_adv: int = 8, device=None) -> dict:
     """Half greedy (even b), half sampling at T = 1 (odd b), fp32, with adversarial requests.
 
     Adversarial sets (n_adv each, drawn from the first requests of each parity):
@@ -185,12 +189,13 @@ def stress(step: int = 0, B: int = 512, V: int = 151936, n_adv: int = 8) -> dict
     Draft logits of greedy requests are never read; they are filled with NaN.
     """
     K = 4
-    g = _gen(1000 * 5 + step)
-    prior = zipf_prior(V)
-    target = torch.empty((B, K + 1, V), dtype=torch.float32)
-    draft = torch.empty((B, K, V), dtype=torch.float32)
-    tokens = torch.zeros((B, K), dtype=torch.int32)
-    temps = torch.where(torch.arange(B) % 2 == 0, 0.0, 1.0).to(torch.float32)
+    g = _gen(1000 * 5 + step, device)
+    prior = zipf_prior(V, device)
+    target = torch.empty((B, K + 1, V), dtype=torch.float32, device=device)
+    draft = torch.empty((B, K, V), dtype=torch.float32, device=device)
+    tokens = torch.zeros((B, K), dtype=torch.int32, device=device)
+    temps = torch.where(torch.arange(B, device=device) % 2 == 0, 0.0, 1.0).to(torch.float32)
+    temps_h = temps.tolist()
     kinds = ["plain"] * B
     odd = [b for b in range(B) if b % 2 == 1]
     even = [b for b in range(B) if b % 2 == 0]
@@ -201,7 +206,7 @@ def stress(step: int = 0, B: int = 512, V: int = 151936, n_adv: int = 8) -> dict
     for b in even[:n_adv]:
         kinds[b] = "tie"
     for b in range(B):
-        t = 4.0 * torch.randn((K + 1, V), generator=g, dtype=torch.float64) + prior
+        t = 4.0 * torch.randn((K + 1, V), generator=g, dtype=torch.float64, device=device) + prior
         if kinds[b] == "tie":
             t = t.to(torch.bfloat16).to(torch.float64)  # bf16-valued entries
             for i in range(K + 1):
@@ -209,27 +214,27 @@ def stress(step: int = 0, B: int = 512, V: int = 151936, n_adv: int = 8) -> dict
                 lo_i, hi_i = sorted(int(v) for v in top2)
                 t[i, hi_i] = t[i, lo_i]
         tb = t.to(torch.float32)
-        if temps[b] == 0.0:
-            db = torch.full((K, V), float("nan"), dtype=torch.float32)
+        if temps_h[b] == 0.0:
+            db = torch.full((K, V), float("nan"), dtype=torch.float32, device=device)
             if kinds[b] == "tie":
                 for i in range(K):
                     mx = tb[i].max()
                     idx = torch.nonzero(tb[i] == mx).flatten()
                     tokens[b, i] = int(idx.max())
             else:
-                d = t[:K] + 0.5 * torch.randn((K, V), generator=g, dtype=torch.float64)
+                d = t[:K] + 0.5 * torch.randn((K, V), generator=g, dtype=torch.float64, device=device)
                 tokens[b] = torch.argmax(d, dim=-1).to(torch.int32)
         else:
             if kinds[b] == "q_eq_p":
                 db = tb[:K].clone()
             else:
-                d = t[:K] + 1.0 * torch.randn((K, V), generator=g, dtype=torch.float64)
+                d = t[:K] + 1.0 * torch.randn((K, V), generator=g, dtype=torch.float64, device=device)
                 if kinds[b] == "top50_off":
                     for i in range(K):
                         top = torch.topk(t[i], 50).indices
                         d[i, top] = d[i, top] - 1e4
                 db = d.to(torch.float32)
-            tokens[b] = _draw_drafts(db, float(temps[b]), g)
+            tokens[b] = _draw_drafts(db, float(temps_h[b]), g)
         target[b] = tb
         draft[b] = db
     return dict(target=target, draft=draft, draft_tokens=tokens, num_draft=None, temperature=temps,

@@ -138,3 +138,36 @@ def test_threshold_host_argument_errors(lib):
     assert lib.spec_schedule_threshold(P, None, 4, 4, ctypes.c_float(float("nan")), P, None) == EINVAL
     assert lib.spec_schedule_threshold(None, None, 4, 4, ctypes.c_float(0.5), P, None) == EINVAL
     assert lib.spec_schedule_threshold(P, None, 0, 4, ctypes.c_float(0.5), None, None) == 0
+
+
+def _ws_formula(B, K, V, esz):
+    """The workspace size the header states for spec_verify_workspace_size."""
+    max_e = 65504 // esz
+    cpr = -(-V // max_e)
+    ce = (-(-V // cpr) + 7) & ~7
+    cpr = -(-V // ce)
+    P = -(-(-(-V // 1024)) // 8)
+
+    def a256(x):
+        return (x + 255) & ~255
+
+    return (256 + a256(4 * (B + 1)) + 2 * a256(4 * B) + a256(16 * B * 2 * K * cpr) + a256(32 * B * 2 * K * cpr)
+            + a256(16 * B * P))
+
+
+def test_workspace_size_formula(lib):
+    """spec_verify_workspace_size needs no GPU and follows the header's formula."""
+    for B, K, V in ((1, 0, 1), (1, 4, 1024), (64, 7, 151936), (8, 8, 32000), (256, 16, 129280), (512, 4, 151936),
+                    (8192, 255, 97), (3, 255, 1 << 20)):
+        for dt, esz in ((0, 2), (1, 4)):
+            assert lib.spec_verify_workspace_size(B, K, V, dt) == _ws_formula(B, K, V, esz), (B, K, V, dt)
+    assert lib.spec_verify_workspace_size(8193, 1, 10, 0) == 0 and lib.spec_verify_workspace_size(1, 256, 10, 0) == 0
+
+
+def test_fixed_scratch_limits_stated_in_the_header(lib):
+    """The batch sizes the header gives for spec_verify_sample_noalloc at V = 151936,
+    Kmax = 7: the largest B whose workspace fits SPEC_STATIC_SCRATCH_BYTES (4 MiB)."""
+    scratch = 4 << 20
+    for dt, bmax in ((0, 1140), (1, 596)):
+        assert lib.spec_verify_workspace_size(bmax, 7, 151936, dt) <= scratch
+        assert lib.spec_verify_workspace_size(bmax + 1, 7, 151936, dt) > scratch

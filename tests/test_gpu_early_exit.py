@@ -81,7 +81,7 @@ def test_tiny_many_steps_both_modes():
                              batch["temperature"].numpy())
         n += res["n"]
         flagged += res["flagged"]
-    assert flagged <= max(3, n // 100), (flagged, n)
+    assert flagged <= max(1, n // 200), (flagged, n)
 
 
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
@@ -95,7 +95,7 @@ def test_ragged_mixed_batch(dt):
     for step in range(2):
         res = compare_sample(gpu_ee_sample(batch, 5, step), oracle_ee_sample(batch, 5, step),
                              batch["temperature"].numpy())
-        assert res["flagged"] <= 2
+        assert res["flagged"] <= 1
 
 
 def test_main_batch_full_size():
@@ -106,7 +106,7 @@ def test_main_batch_full_size():
         ee = gpu_ee_sample(batch, batch["seed"], step)
         ref = oracle_ee_sample(batch, batch["seed"], step)
         res = compare_sample(ee, ref, batch["temperature"].numpy())
-        assert res["flagged"] <= 2
+        assert res["flagged"] <= 1
         full = run_gpu_sample(batch, batch["seed"], step)
         ok = ref["flags"] == 0
         assert (ee["tokens"][ok] == full["tokens"][ok]).all()

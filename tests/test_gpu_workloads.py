@@ -4,9 +4,11 @@ shapes): the tiny 1000-step run in both modes, the B=8 bf16 batch, the B=64 K=7
 V=151936 bf16 batch (sampling and greedy), the confidence-scheduled ragged batch,
 and the mixed greedy/sampling fp32 stress batch with adversarial requests.
 
-Greedy results must be bit-exact.  Sampling results must equal the oracle's on
-every request it does not flag as a near-tie; flagged requests are counted and
-must stay rare.  p(x_i) and q(x_i) must be within 1e-5 of the oracle's."""
+Greedy results must be bit-exact.  Sampling results must equal the oracle's except
+where the oracle flags a threshold or top-2 Gumbel gap below 1e-5 relative (or an
+empty residual), and there only from the flagged decision on; flagged requests are
+counted and must stay rare.  p(x_i) and q(x_i) must be within 1e-5 of the
+oracle's."""
 import os
 
 import numpy as np
@@ -68,7 +70,7 @@ def test_tiny_1000_steps_both_modes():
         r = compare_sample(gpu, ref, batch["temperature"].numpy())
         n += r["n"]
         flagged += r["flagged"]
-    assert flagged <= n // 100, (flagged, n)
+    assert flagged <= max(1, n // 200), (flagged, n)
 
 
 def test_small_batch():
@@ -81,7 +83,7 @@ def test_small_batch():
         r = compare_sample(gpu, ref, batch["temperature"].numpy())
         n += r["n"]
         flagged += r["flagged"]
-    assert flagged <= max(1, n // 20), (flagged, n)
+    assert flagged <= max(1, n // 200), (flagged, n)
 
 
 def test_main_batch_full_size():
@@ -95,7 +97,7 @@ def test_main_batch_full_size():
         n += r["n"]
         flagged += r["flagged"]
         assert (ref["status"] == 0).all()
-    assert flagged <= max(1, n // 20), (flagged, n)
+    assert flagged <= max(1, n // 200), (flagged, n)
     # the same logits in greedy mode, bit-exact
     _check_greedy(synth.main(0))
 
@@ -117,7 +119,7 @@ def test_ragged_scheduled_batch():
     gpu = run_gpu_sample(batch, batch["seed"], 0)
     ref = _oracle_sample(batch, batch["seed"], 0)
     r = compare_sample(gpu, ref, batch["temperature"].numpy())
-    assert r["flagged"] <= max(1, r["n"] // 20), r
+    assert r["flagged"] <= max(1, r["n"] // 200), r
 
 
 def test_stress_mixed_adversarial():
@@ -128,7 +130,7 @@ def test_stress_mixed_adversarial():
     ref = _oracle_sample(batch, batch["seed"], 0)
     T = batch["temperature"].numpy()
     r = compare_sample(gpu, ref, T)
-    assert r["flagged"] <= max(1, r["n"] // 20), r
+    assert r["flagged"] <= max(1, r["n"] // 200), r
     assert (gpu["status"] == 0).all()
     kinds = batch["kinds"]
     K = batch["K"]

@@ -45,7 +45,7 @@ def test_noalloc_matches_workspace_entry_point(dt):
     d = to_dev(batch)
     args = (d["target"], d["draft"], d["draft_tokens"], d["num_draft"], d["temperature"], 11, 4)
     ref = _outputs(B, K)
-    ws = torch.empty(binding.spec_verify_workspace_size(B, K, V, binding._dtype_code(d["target"])),
+    ws = torch.zeros(binding.spec_verify_workspace_size(B, K, V, binding._dtype_code(d["target"])),
                      dtype=torch.uint8, device="cuda")
     binding.spec_verify_sample(*args, ref["tokens"], ref["accepted"], ref["p"], ref["q"], ref["status"], ws)
     torch.cuda.synchronize()
