@@ -89,9 +89,9 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
  * _flat forms) need for (B, Kmax, V, dtype).  Returns 0 for invalid sizes.  The
  * workspace holds the main pass's chunk-ticket counter (always at its start), one
  * 16-byte statistic and 16 two-byte seed pointers per chunk of every row the main
- * pass reads (rows of at most 64 KB chunks), and per request a piece counter, a
- * shared bound and the commit pieces' results:
- *   256 + align256(4 (B + 1)) + 2 align256(4 B) + align256(16 B R cpr)
+ * pass reads (rows of at most 64 KB chunks), and per request a 128-byte line for the
+ * commit pieces' counter and shared bound, and the commit pieces' results:
+ *   256 + align256(4 (B + 1)) + align256(128 B) + align256(16 B R cpr)
  *       + align256(32 B R cpr) + align256(16 B P),
  * with R = 2 Kmax main-pass rows a request (sampling), cpr = the chunks a row
  * (ceil(V / floor(65504 / elsize)) for elsize 2 or 4, then ceil(V / ce) with
@@ -257,8 +257,8 @@ int spec_markov_draft(const void *base, int dtype, int B, int K, int V, int64_t 
  *  - Limit: sizes whose spec_verify_workspace_size(B, Kmax, V, dtype) exceeds
  *    SPEC_STATIC_SCRATCH_BYTES return SPEC_ESCRATCH before anything is launched.
  *    The scratch grows with B * Kmax * (chunks a row) (see the formula at
- *    spec_verify_workspace_size): at V = 151936, Kmax = 7 fits B up to 1140 for
- *    bf16 logits (5 chunks a row) and B up to 596 for fp32 (10 chunks a row).
+ *    spec_verify_workspace_size): at V = 151936, Kmax = 7 fits B up to 1104 for
+ *    bf16 logits (5 chunks a row) and B up to 586 for fp32 (10 chunks a row).
  *  - Zeroing: the array is zero when the module loads, and every call leaves the
  *    part that must start at zero (the chunk-ticket counter) at zero.
  *  - Races: every call on a device uses the same array, so two calls that can

@@ -152,6 +152,14 @@ __device__ __forceinline__ float load_logit(const void *base, int dtype, int64_t
     return __ldg((const float *)base + idx);
 }
 
+// The same with the element size fixed at compile time: no branch between
+// consecutive gathers, so they issue back to back.
+template <int ESZ>
+__device__ __forceinline__ float ld_elem(const void *base, int64_t idx) {
+    if (ESZ == 2) return __uint_as_float((uint32_t)__ldg((const unsigned short *)base + idx) << 16);
+    return __ldg((const float *)base + idx);
+}
+
 // ------------------------------------------------------------------ async copies
 // Bulk (TMA) copies global -> shared, completed on an mbarrier, and bounded waits.
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

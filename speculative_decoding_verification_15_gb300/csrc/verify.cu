@@ -513,26 +513,49 @@ __device__ __forceinline__ void live_round(const uint32_t *lg, const float *lz, 
     uint4 r4[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) r4[h] = rand_group(seed, step, b, (uint32_t)jd.row, purpose, gk[h] >> 3);
+    uint32_t sv = 0;  // bit 4h + q: entry q of group h passed the per-entry test
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         // any survivor needs 1 - u_k <= e^(z_k - thr) <= e^(zmax - thr); the largest
         // w >> 9 of the group gives the smallest 1 - u
         const uint32_t kmax = max(max(r4[h].x >> 9, r4[h].y >> 9), max(r4[h].z >> 9, r4[h].w >> 9));
         if (has[h] && one_minus_u01(kmax << 9) <= ex2_approx((zm[h] - thr) * kLog2e) * 1.001f) {
-            const int g = (int)(gk[h] >> 3);
             float x[4];
-            group_vals<ESZ>(uvs[gk[h] & 7u], g, x);
+            group_vals<ESZ>(uvs[gk[h] & 7u], (int)(gk[h] >> 3), x);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (one_minus_u01(word_of(r4[h], q)) <= ex2_approx((fmaf(x[q], jd.invT, -jd.shift) - thr) * kLog2e) *
+                                                             1.001f)
+                    sv |= 1u << (4 * h + q);
+        }
+    }
+    if (sv) {
+        // the survivors' draft logits are loaded together: one memory latency however
+        // many entries pass (a low bound lets many through)
+        float lq[8];
+        if (resid) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                lq[k] = (sv >> k & 1u) ? fmaf(ld_elem<ESZ>(drow, 4 * (int)(gk[k >> 2] >> 3) + (k & 3)), jd.invT,
+                                              -jd.Cd)
+                                       : 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!(sv >> (4 * h) & 15u)) continue;
+            float x[4];
+            group_vals<ESZ>(uvs[gk[h] & 7u], (int)(gk[h] >> 3), x);  // z again: fewer live registers
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+                const int k = 4 * h + q;
+                if (!(sv >> k & 1u)) continue;
+                const int v = 4 * (int)(gk[h] >> 3) + q;
                 const float z = fmaf(x[q], jd.invT, -jd.shift);
                 const uint32_t wd = word_of(r4[h], q);
-                if (one_minus_u01(wd) <= ex2_approx((z - thr) * kLog2e) * 1.001f) {
-                    const int v = 4 * g + q;
-                    const float sc = entry_score(resid, jd.invT, jd.Cd, drow, dtype, z, v, wd);
-                    // -inf: no residual mass at v, never a candidate (a row without any
-                    // must reach the degenerate fallback)
-                    if (sc > kNegInf && better(sc, v, best, bidx)) { best = sc; bidx = v; }
-                }
+                // -inf (no residual mass at v) is never a candidate: a row without any
+                // must reach the degenerate fallback
+                const float sc = resid ? (lq[k] < z ? resid_score(z, lq[k], wd) : kNegInf) : z + gumbel_of_word(wd);
+                if (sc > kNegInf && better(sc, v, best, bidx)) { best = sc; bidx = v; }
             }
         }
     }
@@ -566,6 +589,11 @@ __device__ __forceinline__ SliceRes block_reduce(SliceRes r, SliceRes *red) {
 }
 
 // =================================================================== main_kernel
+// commit_kernel's per-request words, one 128-byte line per request
+constexpr int kSyncWords = 32;
+constexpr int kSyncDone = 0;  // pieces finished
+constexpr int kSyncBest = 1;  // the pieces' shared bound
+
 struct MainParams {
     const void *target;
     const void *draft;
@@ -575,8 +603,7 @@ struct MainParams {
     const int32_t *num_draft;
     const float *temperature;  // NULL: every request greedy
     int *row_start;            // [B+1], written by block 0 for commit_kernel
-    uint32_t *done;            // [B] piece counters of commit_kernel, zeroed here by block 0
-    uint32_t *best;            // [B] commit pieces' best exact score so far (ordered bits), zeroed here
+    uint32_t *sync;            // [B][kSyncWords] commit_kernel's per-request words, zeroed here by block 0
     uint32_t *ticket;          // dynamic chunk tickets (0 between calls)
     Part *parts;               // [chunks] one per chunk of every main-pass row
     uint16_t *cand;            // [chunks][kCW] sampling rows: the window vector holding each warp's
@@ -786,8 +813,8 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i <= p.B; i += blockDim.x) p.row_start[i] = s_rs[i];
         for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
-            p.done[i] = 0u;
-            p.best[i] = 0u;
+            p.sync[(size_t)i * kSyncWords + kSyncDone] = 0u;
+            p.sync[(size_t)i * kSyncWords + kSyncBest] = 0u;
         }
     }
     pdl_launch_dependents();
@@ -1044,6 +1071,7 @@ constexpr int kJobWarps = kJobThreads / 32;
 constexpr int kJobBlocksPerSM = 8;
 constexpr int kUnitE = 1024;       // entries per unit (a multiple of 8)
 constexpr int kUnitsPerPiece = 8;  // units a piece stages (a live group's slot index takes 3 bits)
+constexpr int kCandPrefetch = 256; // seed-candidate pointers a piece fetches with the partials
 
 struct JobParams {
     const void *target;
@@ -1065,8 +1093,8 @@ struct JobParams {
     int P;                     // pieces per request
     int slot;                  // bytes per unit slot
     uint32_t *ticket;          // main_kernel's ticket counter, reset here for the next call
-    uint32_t *done;            // [B] pieces finished (zeroed by main_kernel)
-    uint32_t *best;            // [B] best exact score any piece has found (ordered bits; 0: none)
+    uint32_t *sync;            // [B][kSyncWords]: pieces finished, and the best exact score any piece
+                               // has found (ordered bits; 0: none); zeroed by main_kernel
     PieceRes *pres;            // [B * P]
     int32_t *out_tokens;
     int32_t *out_accepted;
@@ -1170,7 +1198,7 @@ __device__ SliceRes job_piece(const JobParams &p, const JobDesc &jd, uint32_t b,
         seed = block_reduce_n(seed, red, kJobWarps);
         mine.best = seed.best;
         mine.idx = seed.idx;
-        if (threadIdx.x == 0 && seed.best > kNegInf) atomicMax(p.best + b, ordered_bits(seed.best));
+        if (threadIdx.x == 0 && seed.best > kNegInf) atomicMax(p.sync + (size_t)b * kSyncWords + kSyncBest, ordered_bits(seed.best));
     }
     // The bound is shared with the request's other pieces: each publishes the best
     // exact score it knows, and reads theirs one block ahead of using it.  Every
@@ -1178,7 +1206,7 @@ __device__ SliceRes job_piece(const JobParams &p, const JobDesc &jd, uint32_t b,
     // maximum and the pruning stays exact.
     const bool share = true;
     float thr = mine.best, published = mine.best;
-    uint32_t shared_bits = share ? ld_relaxed_u32(p.best + b) : 0u;
+    uint32_t shared_bits = share ? ld_relaxed_u32(p.sync + (size_t)b * kSyncWords + kSyncBest) : 0u;
     uint32_t *lg = live_g[warp];
     float *lz = live_z[warp];
     int nlive = 0;
@@ -1188,9 +1216,9 @@ __device__ SliceRes job_piece(const JobParams &p, const JobDesc &jd, uint32_t b,
         const int gb = uv.g0 + (bi % bpu) * kBlockGroups, ge = min(gb + kBlockGroups, uv.g1);
         if (share) {
             thr = fmaxf(thr, ordered_float(shared_bits));
-            shared_bits = ld_relaxed_u32(p.best + b);
+            shared_bits = ld_relaxed_u32(p.sync + (size_t)b * kSyncWords + kSyncBest);
             if (lane == 0 && thr > published) {
-                atomicMax(p.best + b, ordered_bits(thr));
+                atomicMax(p.sync + (size_t)b * kSyncWords + kSyncBest, ordered_bits(thr));
                 published = thr;
             }
         }
@@ -1244,6 +1272,7 @@ __global__ void __launch_bounds__(kJobThreads, kJobBlocksPerSM) commit_kernel(Jo
     __shared__ JobDesc s_job;
     __shared__ int s_sum[2 * kJobWarps];
     __shared__ int s_last;
+    __shared__ uint16_t s_cand[kCandPrefetch];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x / p.P, piece = blockIdx.x - b * p.P;
@@ -1284,8 +1313,8 @@ __global__ void __launch_bounds__(kJobThreads, kJobBlocksPerSM) commit_kernel(Jo
     if (!greedy) {
         for (int i = tid; i < npos; i += kJobThreads) {
             const int xi = x[i];
-            s_xt[i] = load_logit(p.target, p.dtype, (rbase.t0 + i) * p.ld_row + xi);
-            s_xd[i] = load_logit(p.draft, p.dtype, (rbase.d0 + i) * p.ld_row + xi);
+            s_xt[i] = ld_elem<ESZ>(p.target, (rbase.t0 + i) * p.ld_row + xi);
+            s_xd[i] = ld_elem<ESZ>(p.draft, (rbase.d0 + i) * p.ld_row + xi);
             const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
             s_l2u[i] = log2f(u01(r4.x));
         }
@@ -1312,6 +1341,16 @@ __global__ void __launch_bounds__(kJobThreads, kJobBlocksPerSM) commit_kernel(Jo
     Part *s_parts = (Part *)slots;  // the unit slots hold the partials until the job is known
     if (staged)
         for (int it = tid; it < items; it += kJobThreads) s_parts[it] = gparts[it];
+    // this piece's seed-candidate pointers: slots q = piece + P j (j < nq) of each
+    // target row's chunk x warp list, fetched with the partials (row A's are used)
+    const int ncand = p.cpr * kCW;
+    const int nq = piece < ncand ? (ncand - piece + p.P - 1) / p.P : 0;
+    const bool cand_pre = !greedy && npos * nq <= kCandPrefetch;
+    if (cand_pre)
+        for (int it = tid; it < npos * nq; it += kJobThreads) {
+            const int i = it / nq, j = it - i * nq;
+            s_cand[it] = p.cand[((int64_t)r0 + i) * ncand + piece + p.P * j];
+        }
     __syncthreads();
     const Part *rp = staged ? s_parts : gparts;
 
@@ -1440,37 +1479,46 @@ __global__ void __launch_bounds__(kJobThreads, kJobBlocksPerSM) commit_kernel(Jo
         if (jd.kind == JOB_RESID) {
             constexpr int VE = 16 / ESZ;
             const Chunking mk = {p.cpr, p.ce};
-            const uint16_t *cands = p.cand + ((int64_t)r0 + jd.row) * p.cpr * kCW;
             SliceRes sd;
             sd.best = kNegInf;
             sd.idx = -1;
             sd.rawmax = kNegInf;
             sd.failed = 0;
-            for (int q = piece + p.P * tid; q < p.cpr * kCW; q += p.P * kJobThreads) {
-                const uint32_t j = cands[q];
+            for (int j = tid; j < nq; j += kJobThreads) {
+                const int q = piece + p.P * j;
+                const uint32_t cv = cand_pre ? s_cand[jd.row * nq + j] : p.cand[((int64_t)r0 + jd.row) * ncand + q];
                 const ChunkWin w = chunk_window(jrow, ESZ, p.V, mk, q / kCW);
-                if (j == 0xffffu || (j + 1) * 16 > w.bytes) continue;
-                const uint4 raw = ld_stream_v4(w.a0 + 16 * (size_t)j);
-                const int ebase = w.e0 - w.shift + (int)j * VE;
-                float best = kNegInf;
+                if (cv == 0xffffu || (cv + 1) * 16 > w.bytes) continue;
+                const int ebase = w.e0 - w.shift + (int)cv * VE;
+                // the target vector and the draft logits of its entries, loaded together
+                const uint4 raw = ld_stream_v4(w.a0 + 16 * (size_t)cv);
+                float lq[VE];
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const int v = ebase + e;
+                    lq[e] = (v >= w.e0 && v < w.e1) ? ld_elem<ESZ>(drow, v) : 0.f;
+                }
+                float bx = kNegInf, bq = 0.f;
                 int bv = -1;
 #pragma unroll
                 for (int e = 0; e < VE; ++e) {
                     const int v = ebase + e;
                     const float xv = ESZ == 2 ? VecBF16{raw}.get(e) : VecF32{raw}.get(e);
-                    if (v >= w.e0 && v < w.e1 && xv > best) { best = xv; bv = v; }
+                    if (v >= w.e0 && v < w.e1 && xv > bx) { bx = xv; bv = v; bq = lq[e]; }
                 }
                 if (bv < 0) continue;
-                const float z = fmaf(best, jd.invT, -jd.shift);
+                const float z = fmaf(bx, jd.invT, -jd.shift);
+                const float lqs = fmaf(bq, jd.invT, -jd.Cd);
+                if (!(lqs < z)) continue;  // no residual mass at bv
                 const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
                                             (uint32_t)bv >> 2);
-                const float sc = entry_score(true, jd.invT, jd.Cd, drow, p.dtype, z, bv, word_of(r4, bv & 3));
-                if (sc > kNegInf && better(sc, bv, sd.best, sd.idx)) { sd.best = sc; sd.idx = bv; }
+                const float sc = resid_score(z, lqs, word_of(r4, bv & 3));
+                if (better(sc, bv, sd.best, sd.idx)) { sd.best = sc; sd.idx = bv; }
             }
             sd = block_reduce_n(sd, s_red, kJobWarps);
             jd.seed = sd.best;
             jd.seed_idx = sd.idx;
-            if (tid == 0 && sd.best > kNegInf) atomicMax(p.best + b, ordered_bits(sd.best));
+            if (tid == 0 && sd.best > kNegInf) atomicMax(p.sync + (size_t)b * kSyncWords + kSyncBest, ordered_bits(sd.best));
         }
         // one thread waits (bounded), the others then take the completed phase
         bool ok = true;
@@ -1495,7 +1543,7 @@ __global__ void __launch_bounds__(kJobThreads, kJobBlocksPerSM) commit_kernel(Jo
             pr.tag = res.failed ? ~p.epoch : p.epoch;
             p.pres[(int64_t)b * p.P + piece] = pr;
             __threadfence();
-            s_last = atomicAdd(p.done + b, 1u) == (uint32_t)(p.P - 1);
+            s_last = atomicAdd(p.sync + (size_t)b * kSyncWords + kSyncDone, 1u) == (uint32_t)(p.P - 1);
         }
         __syncthreads();
         writer = s_last != 0;
@@ -1531,7 +1579,7 @@ __global__ void __launch_bounds__(kJobThreads, kJobBlocksPerSM) commit_kernel(Jo
             f.rawmax = kNegInf;
             f.failed = 0;
             for (int v = tid; v < p.V; v += kJobThreads) {
-                const float lp = fmaf(load_logit(p.target, p.dtype, trow + v), jd.invT, -jd.shift);
+                const float lp = fmaf(ld_elem<ESZ>(p.target, trow + v), jd.invT, -jd.shift);
                 if (!(lp > kNegInf)) continue;
                 const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
                                             (uint32_t)v >> 2);
@@ -1789,8 +1837,8 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
         s_qq[i] = -1.f;
         if (i < npos && !greedy) {
             const int xi = x[i];
-            s_xt[i] = load_logit(p.target, p.dtype, (rbase.t0 + i) * p.ld_row + xi);
-            s_xd[i] = load_logit(p.draft, p.dtype, (rbase.d0 + i) * p.ld_row + xi);
+            s_xt[i] = ld_elem<ESZ>(p.target, (rbase.t0 + i) * p.ld_row + xi);
+            s_xd[i] = ld_elem<ESZ>(p.draft, (rbase.d0 + i) * p.ld_row + xi);
             const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
             s_l2u[i] = log2f(u01(r4.x));
         }
@@ -1907,7 +1955,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
                 if (lane < kCommitWarps && s_ti[lane] >= 0) {
                     const int v = s_ti[lane];
                     const float z = fmaf(s_tm[lane], invT, -jd.shift);
-                    const float lq = fmaf(load_logit(drow, p.dtype, v), invT, -jd.Cd);
+                    const float lq = fmaf(ld_elem<ESZ>(drow, v), invT, -jd.Cd);
                     if (lq < z) {
                         const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_RESIDUAL,
                                                     (uint32_t)v >> 2);
@@ -1973,7 +2021,7 @@ __global__ void __launch_bounds__(kCommitThreads, kCommitBlocksPerSM) early_exit
             f.rawmax = kNegInf;
             f.failed = 0;
             for (int v = tid; v < p.V; v += kCommitThreads) {
-                const float lp = fmaf(load_logit(p.target, p.dtype, trow + v), jd.invT, -jd.shift);
+                const float lp = fmaf(ld_elem<ESZ>(p.target, trow + v), jd.invT, -jd.shift);
                 if (!(lp > kNegInf)) continue;
                 const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
                                             (uint32_t)v >> 2);
@@ -2068,13 +2116,14 @@ struct ProfScope {
 //   ticket     main_kernel's chunk-ticket counter: zero before the first call,
 //              and every call leaves it zero (commit_kernel resets it);
 //   row_start  [B+1] first main-pass row of each request;
-//   done       [B] commit pieces finished (zeroed by main_kernel in every call);
-//   best       [B] the commit pieces' shared bound (zeroed by main_kernel);
+//   sync       [B] 128-byte records, one line per request so that the pieces of
+//              different requests never contend for a line: pieces finished and the
+//              pieces' shared bound (both zeroed by main_kernel in every call);
 //   parts      one Part per chunk of every main-pass row (B * rows * cpr);
 //   cand       kCW seed-candidate vectors per chunk (B * rows * cpr * kCW, 16-bit);
 //   pres       [B * P] commit pieces' results.
 struct Layout {
-    size_t off_ticket, off_row_start, off_done, off_best, off_parts, off_cand, off_pres, total;
+    size_t off_ticket, off_row_start, off_sync, off_parts, off_cand, off_pres, total;
     int cpr;                 // main pass: chunks per row
     int P, jslot;            // commit: pieces per request, bytes per unit slot
     int C, ue, NS, slot;     // early exit: cluster size, entries per unit, units per round, bytes per slot
@@ -2093,10 +2142,8 @@ Layout make_layout(int B, int Kmax, int V, int esz, int main_rows_per_request) {
     o = align256(o + 16);
     L.off_row_start = o;
     o = align256(o + sizeof(int) * (size_t)(B + 1));
-    L.off_done = o;
-    o = align256(o + sizeof(uint32_t) * (size_t)B);
-    L.off_best = o;
-    o = align256(o + sizeof(uint32_t) * (size_t)B);
+    L.off_sync = o;
+    o = align256(o + sizeof(uint32_t) * kSyncWords * (size_t)B);
     L.off_parts = o;
     o = align256(o + sizeof(Part) * (size_t)B * (size_t)main_rows_per_request * (size_t)ck.cpr);
     L.off_cand = o;
@@ -2279,8 +2326,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     mp.num_draft = num_draft;
     mp.temperature = temps;
     mp.row_start = (int *)(w + L.off_row_start);
-    mp.done = (uint32_t *)(w + L.off_done);
-    mp.best = (uint32_t *)(w + L.off_best);
+    mp.sync = (uint32_t *)(w + L.off_sync);
     mp.ticket = (uint32_t *)(w + L.off_ticket);
     mp.parts = (Part *)(w + L.off_parts);
     mp.cand = (uint16_t *)(w + L.off_cand);
@@ -2309,8 +2355,7 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     jp.P = L.P;
     jp.slot = L.jslot;
     jp.ticket = mp.ticket;
-    jp.done = mp.done;
-    jp.best = mp.best;
+    jp.sync = mp.sync;
     jp.pres = (PieceRes *)(w + L.off_pres);
     jp.out_tokens = out_tokens;
     jp.out_accepted = out_accepted;

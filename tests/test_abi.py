@@ -151,7 +151,7 @@ def _ws_formula(B, K, V, esz):
     def a256(x):
         return (x + 255) & ~255
 
-    return (256 + a256(4 * (B + 1)) + 2 * a256(4 * B) + a256(16 * B * 2 * K * cpr) + a256(32 * B * 2 * K * cpr)
+    return (256 + a256(4 * (B + 1)) + a256(128 * B) + a256(16 * B * 2 * K * cpr) + a256(32 * B * 2 * K * cpr)
             + a256(16 * B * P))
 
 
@@ -168,6 +168,6 @@ def test_fixed_scratch_limits_stated_in_the_header(lib):
     """The batch sizes the header gives for spec_verify_sample_noalloc at V = 151936,
     Kmax = 7: the largest B whose workspace fits SPEC_STATIC_SCRATCH_BYTES (4 MiB)."""
     scratch = 4 << 20
-    for dt, bmax in ((0, 1140), (1, 596)):
+    for dt, bmax in ((0, 1104), (1, 586)):
         assert lib.spec_verify_workspace_size(bmax, 7, 151936, dt) <= scratch
         assert lib.spec_verify_workspace_size(bmax + 1, 7, 151936, dt) > scratch
