@@ -83,6 +83,7 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
 #define SPEC_MAX_DRAFTS 255        /* Kmax                                */
 #define SPEC_MAX_SCHED_ITEMS 8192  /* B * Kmax for the scheduler          */
 #define SPEC_MARKOV_MAX_RANK 512   /* rank r of the Markov head's factors (a multiple of 4) */
+#define SPEC_MARKOV_MAX_TOPK 1024  /* candidates a position of top-K Markov drafting corrects */
 
 /*
  * Bytes of device workspace that spec_verify_greedy / spec_verify_sample (and their
@@ -238,6 +239,32 @@ int spec_markov_draft(const void *base, int dtype, int B, int K, int V, int64_t 
                       const void *emb, const void *proj, int rank, const float *temperature, uint64_t seed,
                       uint64_t step, int32_t *out_tokens, float *out_logits, int32_t *out_status,
                       void *cuda_stream);
+
+/*
+ * Top-K Markov-head drafting ("Bringing DSpark to vLLM Metal" -- "Making the draft
+ * cheaper": only the top-K candidate rows of each position are corrected).  As
+ * spec_markov_draft, with the candidate set of row (b, k) restricted to the
+ * n = min(topk, V) entries with the largest backbone logit base[b, k, v] (a NaN
+ * counts as +inf; lower v first among equal values):
+ *   z_v = base[b, k, v] + sum_j emb[prev, j] * proj[v, j] for the candidates, -inf
+ *         for the others;
+ *   x_k = argmax over the candidates of z_v (greedy) or z_v / T_b + g_v (noise
+ *         purpose 3 at row k, as spec_markov_draft).
+ *  topk          1 .. SPEC_MARKOV_MAX_TOPK
+ *  out_logits    [B, K, V] float (z, -inf outside the candidates), or NULL
+ *  ws, ws_bytes  device workspace of at least spec_markov_topk_workspace_size
+ *                (B, K, V, topk) bytes, 16-byte aligned: the candidate lists
+ *                (B K n int32); nothing persists between calls
+ * Statuses and failed requests as spec_markov_draft (status 4 when a candidate's z
+ * is NaN or +inf, or no candidate is finite).  Two kernel launches (the selection
+ * of every row, then the walk over the positions), no host synchronisation.
+ */
+size_t spec_markov_topk_workspace_size(int B, int K, int V, int topk);
+int spec_markov_draft_topk(const void *base, int dtype, int B, int K, int V, int64_t ld_row,
+                           const int32_t *anchor, const void *emb, const void *proj, int rank,
+                           const float *temperature, uint64_t seed, uint64_t step, int topk,
+                           int32_t *out_tokens, float *out_logits, int32_t *out_status, void *ws,
+                           size_t ws_bytes, void *cuda_stream);
 
 /*
  * spec_verify_sample without a workspace argument.  The method on the pages has no

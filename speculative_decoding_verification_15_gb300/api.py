@@ -123,6 +123,23 @@ def markov_draft(base, anchor, emb, proj, temperature=None, seed: int = 0, step:
     return out
 
 
+def markov_draft_topk(base, anchor, emb, proj, topk: int, temperature=None, seed: int = 0, step: int = 0,
+                      want_logits: bool = True, stream=None) -> dict:
+    """Top-K Markov-head drafting of one block: tokens [B, K], corrected logits
+    [B, K, V] (float32, -inf outside each position's topk candidates; None unless
+    want_logits) and status [B]."""
+    dev = base.device
+    B, K, V = base.shape
+    out = dict(tokens=torch.empty((B, K), dtype=torch.int32, device=dev),
+               logits=torch.empty((B, K, V), dtype=torch.float32, device=dev) if want_logits else None,
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    T = None if temperature is None else temperature.to(device=dev, dtype=torch.float32).contiguous()
+    ws = torch.empty(max(binding.spec_markov_topk_workspace_size(B, K, V, topk), 16), dtype=torch.uint8, device=dev)
+    binding.spec_markov_draft_topk(base, _as_i32(anchor, dev), emb, proj, T, seed, step, topk, out["tokens"],
+                                   out["logits"], out["status"], ws, stream)
+    return out
+
+
 def verify_sample_flat(target, draft, cu_draft, draft_tokens, temperature, seed: int, step: int, Kmax: int,
                        stream=None) -> dict:
     """Flattened ragged layout (no padding rows): target [sum_b (k_b + 1), V], draft

@@ -71,6 +71,11 @@ def load(path: str | None = None):
         lib.spec_verify_greedy_early_exit.restype = I32
         lib.spec_markov_draft.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, I32, P, U64, U64, P, P, P, P]
         lib.spec_markov_draft.restype = I32
+        lib.spec_markov_topk_workspace_size.argtypes = [I32, I32, I32, I32]
+        lib.spec_markov_topk_workspace_size.restype = SZ
+        lib.spec_markov_draft_topk.argtypes = [P, I32, I32, I32, I32, I64, P, P, P, I32, P, U64, U64, I32, P, P, P,
+                                               P, SZ, P]
+        lib.spec_markov_draft_topk.restype = I32
         lib.spec_verify_sample_noalloc.argtypes = [P, P, I32, I32, I32, I32, I64, P, P, P, U64, U64, P, P, P,
                                                    P, P, P]
         lib.spec_verify_sample_noalloc.restype = I32
@@ -293,6 +298,40 @@ def spec_markov_draft(base, anchor, emb, proj, temperature, seed: int, step: int
     _call(lib, "spec_markov_draft", dev, _ptr(base), _dtype_code(base), B, K, V, ld, _ptr(anchor), _ptr(emb), _ptr(proj),
                                emb.shape[1], _ptr(temperature), int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
                                _ptr(out_tokens), _ptr(out_logits), _ptr(out_status), _stream_handle(stream, dev))
+
+
+def spec_markov_topk_workspace_size(B: int, K: int, V: int, topk: int) -> int:
+    return int(load().spec_markov_topk_workspace_size(B, K, V, topk))
+
+
+def spec_markov_draft_topk(base, anchor, emb, proj, temperature, seed: int, step: int, topk: int, out_tokens,
+                           out_logits, out_status, ws, stream=None) -> None:
+    """Top-K Markov-head drafting of one block: as spec_markov_draft, with only the
+    topk largest backbone logits of each position corrected and drawn from.
+    out_logits may be None; ws is a uint8 device tensor of at least
+    spec_markov_topk_workspace_size(B, K, V, topk) bytes."""
+    lib = load()
+    B, K = base.shape[0], base.shape[1]
+    _, V, ld = _logits_layout(base, K) if K > 0 else (B, base.shape[2], base.shape[2])
+    dev = base.device
+    if emb.dtype != base.dtype or proj.dtype != base.dtype:
+        raise TypeError("the factors must have the base logits' dtype")
+    if emb.dim() != 2 or emb.shape[0] != V or proj.shape != emb.shape or not emb.is_contiguous() \
+            or not proj.is_contiguous():
+        raise ValueError("emb and proj must be contiguous [V, r]")
+    _need(anchor, "anchor", torch.int32, (B,), dev)
+    if temperature is not None:
+        _need(temperature, "temperature", torch.float32, (B,), dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K), dev)
+    if out_logits is not None:
+        _need(out_logits, "out_logits", torch.float32, (B, K, V), dev)
+    _need(out_status, "out_status", torch.int32, (B,), dev)
+    if ws is not None and ws.device != dev:
+        raise ValueError("the workspace must be on the logits' device")
+    _call(lib, "spec_markov_draft_topk", dev, _ptr(base), _dtype_code(base), B, K, V, ld, _ptr(anchor), _ptr(emb),
+          _ptr(proj), emb.shape[1], _ptr(temperature), int(seed) & (2**64 - 1), int(step) & (2**64 - 1), int(topk),
+          _ptr(out_tokens), _ptr(out_logits), _ptr(out_status), _ptr(ws), 0 if ws is None else ws.numel(),
+          _stream_handle(stream, dev))
 
 
 def spec_verify_sample_noalloc(target, draft, draft_tokens, num_draft, temperature, seed: int, step: int,

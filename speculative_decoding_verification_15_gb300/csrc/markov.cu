@@ -270,6 +270,428 @@ __global__ void __launch_bounds__(kMkSampleThreads) markov_sample_kernel(MarkovP
     if (tid == 0) p.status[b] = st;
 }
 
+// ------------------------------------------------------------------ top-K drafting
+// "Bringing DSpark to vLLM Metal" -- "Making the draft cheaper": correct only the
+// top-K candidates of each position.  The candidates of row (b, k) are the topk
+// largest backbone logits U[b, k, .] (a NaN counts as +inf, so that it is seen;
+// lower v first among equal values); z_v = U + bias for them, -inf elsewhere, and
+// the draw runs over them alone.  The candidates do not depend on the token drawn
+// before, so all B K rows are selected at once, in parallel, before the sequential
+// walk over the positions.
+constexpr int kTkThreads = 512;     // selection CTA: one per row
+constexpr int kTkDrawThreads = 256; // draw CTA: one per request
+
+// Order-preserving key of a logit: NaN largest, -0 as +0 (equal values, equal keys).
+__device__ __forceinline__ uint32_t topk_key(float x) {
+    if (x != x) return 0xffffffffu;
+    const uint32_t u = __float_as_uint(x == 0.f ? 0.f : x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exact selection of row blockIdx.x by radix: the ncand-th largest key over four
+// 8-bit digits (each pass histograms the entries whose higher digits match), then
+// one pass in index order that lists the entries above that key and the
+// lowest-index entries equal to it (and fills the corrected row with -inf when
+// fill).  Five reads of the row: the fallback of the one-pass selection below.
+template <int ESZ>
+__device__ __noinline__ void topk_radix(const MarkovParams &p, int ncand, int32_t *cands, bool fill) {
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_pick[2];  // the digit, the entries above it
+    __shared__ int s_scan[kTkThreads / 32];
+    constexpr int VE = 16 / ESZ;  // entries a thread reads per step (consecutive)
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.x;  // b * K + k
+    const char *u = (const char *)p.base + row * p.ld_row * ESZ;
+    uint32_t prefix = 0u, pmask = 0u;
+    int rem = ncand;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += kTkThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int v0 = tid * VE; v0 < p.V; v0 += kTkThreads * VE) {
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                const int v = v0 + e;
+                if (v >= p.V) break;
+                const uint32_t key = topk_key(ld_elem<ESZ>(u, v));
+                if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane l holds bins 255 - 8 l .. 248 - 8 l; counts from the top down
+            uint32_t c[8], tot = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c[i] = hist[255 - 8 * lane - i];
+                tot += c[i];
+            }
+            uint32_t incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t above = incl - tot;  // entries in the bins above this lane's
+            const bool mine = above < (uint32_t)rem && incl >= (uint32_t)rem;
+            if (mine) {
+                uint32_t run = above;
+                for (int i = 0; i < 8; ++i) {
+                    if (run + c[i] >= (uint32_t)rem) {
+                        s_pick[0] = 255u - 8u * lane - i;
+                        s_pick[1] = run;
+                        break;
+                    }
+                    run += c[i];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= s_pick[0] << shift;
+        pmask |= 0xffu << shift;
+        rem -= (int)s_pick[1];
+        __syncthreads();  // s_pick is rewritten by the next pass
+    }
+    // prefix: the ncand-th largest key; rem: entries equal to it that are taken
+    float *zrow = (fill && p.z) ? p.z + row * p.V : nullptr;
+    int32_t *out = cands + row * ncand;
+    int eq_base = 0, out_base = 0;
+    for (int blk = 0; blk * kTkThreads * VE < p.V; ++blk) {
+        const int v0 = (blk * kTkThreads + tid) * VE;
+        uint32_t keys[VE];
+        int neq = 0, ngt = 0;
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+            const int v = v0 + e;
+            keys[e] = v < p.V ? topk_key(ld_elem<ESZ>(u, v)) : 0u;
+            if (v < p.V) {
+                neq += keys[e] == prefix;
+                ngt += keys[e] > prefix;
+                if (zrow) zrow[v] = kNegInf;
+            }
+        }
+        // exclusive scans (index order) of the equal entries and of the listed ones
+        // (at most 8 each a thread: packed in one word)
+        const int packed = (neq << 16) | ngt;
+        int incl = packed;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_scan[warp] = incl;
+        __syncthreads();
+        int wbase = 0, total = 0;
+        for (int w = 0; w < kTkThreads / 32; ++w) {
+            const int t = s_scan[w];
+            if (w < warp) wbase += t;
+            total += t;
+        }
+        __syncthreads();  // s_scan is rewritten by the next block
+        const int excl = wbase + incl - packed;
+        int eq_rank = eq_base + (excl >> 16);
+        int gt_seen = excl & 0xffff, eq_seen = excl >> 16;
+        // the position of an entry in the list: the listed entries before it
+        // (above-key ones, and equal ones taken) -- equal ones are taken while
+        // their rank is below rem
+        int pos = out_base + gt_seen + min(eq_base + eq_seen, rem) - min(eq_base, rem);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+            const int v = v0 + e;
+            if (v >= p.V) break;
+            if (keys[e] > prefix) {
+                out[pos++] = v;
+            } else if (keys[e] == prefix) {
+                if (eq_rank < rem) out[pos++] = v;
+                ++eq_rank;
+            }
+        }
+        const int beq = total >> 16, bgt = total & 0xffff;
+        out_base += bgt + min(eq_base + beq, rem) - min(eq_base, rem);
+        eq_base += beq;
+    }
+}
+
+constexpr int kTkKeep = 8;  // entries each selection thread keeps
+constexpr int kTkUnion = kTkThreads * kTkKeep;
+constexpr int kTkTieMax = 1024;  // entries equal to the threshold key ranked by index in the fast path
+
+// Keeps (key, v) in a thread's sorted list of its kTkKeep largest: strictly larger
+// keys only, so among equal keys the earlier (lower) index stays.
+__device__ __forceinline__ void topk_keep(uint32_t (&kk)[kTkKeep], int (&ki)[kTkKeep], uint32_t key, int v) {
+    if (key <= kk[kTkKeep - 1]) return;
+    bool placed = false;
+#pragma unroll
+    for (int s = kTkKeep - 1; s >= 0; --s) {
+        if (!placed) {
+            if (s > 0 && key > kk[s - 1]) {
+                kk[s] = kk[s - 1];
+                ki[s] = ki[s - 1];
+            } else {
+                kk[s] = key;
+                ki[s] = v;
+                placed = true;
+            }
+        }
+    }
+}
+
+// One CTA per row (b, k), one read of the row.  Each thread keeps its kTkKeep
+// largest (key, index) pairs (its entries come in index order); the CTA then
+// finds the ncand-th largest key of the union by radix (4 x 8-bit digits over the
+// union in shared memory), lists the union's entries above it, and ranks the
+// union's entries equal to it by index.  Exact unless some thread's smallest kept
+// key reaches that key (the thread may hold more) or too many entries tie at it:
+// then the row is selected again by radix over the whole row (topk_radix).
+template <int ESZ>
+__global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovParams p, int ncand, int32_t *cands) {
+    __shared__ uint32_t s_key[kTkUnion];
+    __shared__ int s_idx[kTkUnion];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_pick[2];
+    __shared__ int s_cnt[2];
+    constexpr int VE = 16 / ESZ;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.x;
+    const char *u = (const char *)p.base + row * p.ld_row * ESZ;
+    if (p.z) {  // the corrected row: -inf outside the candidates (they are written later)
+        float *zrow = p.z + row * p.V;
+        if ((p.V & 3) == 0) {
+            const float4 ni = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+            for (int i = tid; i < (p.V >> 2); i += kTkThreads) reinterpret_cast<float4 *>(zrow)[i] = ni;
+        } else {
+            for (int i = tid; i < p.V; i += kTkThreads) zrow[i] = kNegInf;
+        }
+    }
+    uint32_t kk[kTkKeep];
+    int ki[kTkKeep];
+#pragma unroll
+    for (int i = 0; i < kTkKeep; ++i) {
+        kk[i] = 0u;  // below every key (0 is the key of no value: NaN maps to the top)
+        ki[i] = -1;
+    }
+    // entry v is thread v mod kTkThreads's (neighbouring entries -- where a Zipf-like
+    // head puts the largest logits -- go to different threads), eight coalesced
+    // loads in flight per thread
+    constexpr int kU = 8;
+    for (int v0 = tid; v0 < p.V; v0 += kTkThreads * kU) {
+        float x[kU];
+#pragma unroll
+        for (int e = 0; e < kU; ++e) {
+            const int v = v0 + e * kTkThreads;
+            x[e] = v < p.V ? ld_elem<ESZ>(u, v) : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < kU; ++e) {
+            const int v = v0 + e * kTkThreads;
+            if (v < p.V) topk_keep(kk, ki, topk_key(x[e]), v);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kTkKeep; ++i) {
+        s_key[tid * kTkKeep + i] = ki[i] < 0 ? 0u : kk[i];
+        s_idx[tid * kTkKeep + i] = ki[i];
+    }
+    if (tid == 0) {
+        s_cnt[0] = 0;
+        s_cnt[1] = 0;
+    }
+    // the ncand-th largest key of the union (radix, as topk_radix over the row)
+    uint32_t prefix = 0u, pmask = 0u;
+    int rem = ncand;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int sh = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += kTkThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < kTkUnion; i += kTkThreads) {
+            const uint32_t key = s_key[i];
+            if (s_idx[i] >= 0 && (key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & 255u], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t c[8], tot = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c[i] = hist[255 - 8 * lane - i];
+                tot += c[i];
+            }
+            uint32_t incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t above = incl - tot;
+            if (above < (uint32_t)rem && incl >= (uint32_t)rem) {
+                uint32_t run = above;
+                for (int i = 0; i < 8; ++i) {
+                    if (run + c[i] >= (uint32_t)rem) {
+                        s_pick[0] = 255u - 8u * lane - i;
+                        s_pick[1] = run;
+                        break;
+                    }
+                    run += c[i];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= s_pick[0] << sh;
+        pmask |= 0xffu << sh;
+        rem -= (int)s_pick[1];
+        __syncthreads();
+    }
+    // prefix: the threshold key; rem of the entries equal to it are taken
+    const bool unsure = ki[kTkKeep - 1] >= 0 && kk[kTkKeep - 1] >= prefix;
+    if (__syncthreads_or(unsure)) {
+        topk_radix<ESZ>(p, ncand, cands, false);
+        return;
+    }
+    int32_t *out = cands + row * ncand;
+    // the union holds every entry of the row at or above the threshold: those above
+    // it are listed (ncand - rem of them, in any order), those equal to it gathered
+    // for ranking by index
+    __shared__ int s_tie[kTkTieMax];
+    for (int i = tid; i < kTkUnion; i += kTkThreads) {
+        if (s_idx[i] < 0) continue;
+        if (s_key[i] > prefix) {
+            out[atomicAdd(&s_cnt[0], 1)] = s_idx[i];
+        } else if (s_key[i] == prefix) {
+            const int slot = atomicAdd(&s_cnt[1], 1);
+            if (slot < kTkTieMax) s_tie[slot] = s_idx[i];
+        }
+    }
+    __syncthreads();
+    const int ne = s_cnt[1];
+    if (ne > kTkTieMax) {
+        topk_radix<ESZ>(p, ncand, cands, false);
+        return;
+    }
+    int n2 = 1;
+    while (n2 < ne) n2 <<= 1;
+    for (int i = ne + tid; i < n2; i += kTkThreads) s_tie[i] = 0x7fffffff;
+    __syncthreads();
+    for (int k2 = 2; k2 <= n2; k2 <<= 1)
+        for (int jj = k2 >> 1; jj > 0; jj >>= 1) {
+            for (int i = tid; i < n2; i += kTkThreads) {
+                const int x = i ^ jj;
+                if (x > i) {
+                    const int a = s_tie[i], c = s_tie[x];
+                    const bool up = (i & k2) == 0;
+                    if (up ? (a > c) : (a < c)) {
+                        s_tie[i] = c;
+                        s_tie[x] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    const int base = ncand - rem;
+    for (int i = tid; i < rem; i += kTkThreads) out[base + i] = s_tie[i];
+}
+
+// One CTA per request: the positions in order; at position k the bias of each of
+// the row's ncand candidates (one warp per candidate at a time: lanes split the
+// rank, fp32), then the draw over them.
+template <int ESZ>
+__global__ void __launch_bounds__(kTkDrawThreads) markov_topk_draw_kernel(MarkovParams p, int ncand,
+                                                                       const int32_t *cands) {
+    __shared__ float s_h[SPEC_MARKOV_MAX_RANK];
+    __shared__ float s_z[SPEC_MARKOV_MAX_TOPK];
+    __shared__ float red_s[kTkDrawThreads / 32];
+    __shared__ int red_i[kTkDrawThreads / 32];
+    __shared__ int s_tok;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = kTkDrawThreads / 32;
+    int prev = p.anchor[b];
+    int st = (prev < 0 || prev >= p.V) ? SPEC_STATUS_BAD_TOKEN : SPEC_STATUS_OK;
+    float T = 0.f;
+    if (st == SPEC_STATUS_OK && p.temperature) {
+        T = p.temperature[b];
+        if (!(T >= 0.f) || isinf(T)) st = SPEC_STATUS_BAD_TEMPERATURE;
+    }
+    const float invT = T == 0.f ? 0.f : __fdiv_rn(1.f, T);
+    for (int k = 0; k < p.K && st == SPEC_STATUS_OK; ++k) {
+        const int64_t row = (int64_t)b * p.K + k;
+        const int32_t *cl = cands + row * ncand;
+        const char *u = (const char *)p.base + row * p.ld_row * ESZ;
+        for (int j = tid; j < p.r; j += kTkDrawThreads) s_h[j] = ld_elem<ESZ>(p.emb, (int64_t)prev * p.r + j);
+        __syncthreads();
+        for (int ci = warp; ci < ncand; ci += NW) {
+            const int v = cl[ci];
+            float acc = 0.f;
+            for (int j = lane; j < p.r; j += 32) acc = fmaf(s_h[j], ld_elem<ESZ>(p.proj, (int64_t)v * p.r + j), acc);
+            acc = warp_sum(acc);
+            if (lane == 0) {
+                const float z = ld_elem<ESZ>(u, v) + acc;
+                s_z[ci] = z;
+                if (p.z) p.z[row * p.V + v] = z;
+            }
+        }
+        __syncthreads();
+        float best = kNegInf;
+        int bi = -1;
+        bool bad = false;
+        for (int ci = tid; ci < ncand; ci += kTkDrawThreads) {
+            const int v = cl[ci];
+            const float z = s_z[ci];
+            if (z != z || z == __int_as_float(0x7f800000)) bad = true;
+            if (!(z > kNegInf)) continue;
+            float sc = z;
+            if (T != 0.f) {
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)k, PURPOSE_DRAFT, (uint32_t)v >> 2);
+                sc = fmaf(z, invT, gumbel_of_word(word_of(r4, v & 3)));
+            }
+            if (better(sc, v, best, bi)) {
+                best = sc;
+                bi = v;
+            }
+        }
+        bad = __syncthreads_or(bad);
+        warp_argmax(best, bi);
+        if (lane == 0) {
+            red_s[warp] = best;
+            red_i[warp] = bi;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float bs = red_s[0];
+            int bx = red_i[0];
+            for (int w = 1; w < NW; ++w)
+                if (better(red_s[w], red_i[w], bs, bx)) {
+                    bs = red_s[w];
+                    bx = red_i[w];
+                }
+            s_tok = bx;
+        }
+        __syncthreads();
+        prev = s_tok;
+        if (bad || prev < 0) st = SPEC_STATUS_NONFINITE;
+        else if (tid == 0) p.tokens[row] = prev;
+        __syncthreads();  // s_h, s_z and s_tok are rewritten at the next position
+    }
+    if (st != SPEC_STATUS_OK)
+        for (int i = tid; i < p.K; i += kTkDrawThreads) p.tokens[(int64_t)b * p.K + i] = -1;
+    if (tid == 0) p.status[b] = st;
+}
+
+int markov_topk_impl(const MarkovParams &p, int ncand, int32_t *cands, cudaStream_t stream) {
+    if (p.K == 0) {
+        markov_sample_kernel<<<p.B, kMkSampleThreads, 0, stream>>>(p, -1);
+    } else if (p.dtype == SPEC_BF16) {
+        markov_topk_select_kernel<2><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
+        markov_topk_draw_kernel<2><<<p.B, kTkDrawThreads, 0, stream>>>(p, ncand, cands);
+    } else {
+        markov_topk_select_kernel<4><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
+        markov_topk_draw_kernel<4><<<p.B, kTkDrawThreads, 0, stream>>>(p, ncand, cands);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        note_cuda_error((int)e);
+        return SPEC_ECUDA;
+    }
+    return SPEC_OK;
+}
+
 int markov_impl(const MarkovParams &p, cudaStream_t stream) {
     const size_t smem = bias_smem_bytes(p.r);
     cudaError_t e = cudaSuccess;
@@ -345,4 +767,49 @@ extern "C" int spec_markov_draft(const void *base, int dtype, int B, int K, int 
     p.z = out_logits;
     p.status = out_status;
     return markov_impl(p, (cudaStream_t)cuda_stream);
+}
+
+extern "C" size_t spec_markov_topk_workspace_size(int B, int K, int V, int topk) {
+    if (B < 0 || K < 0 || V <= 0 || topk <= 0 || topk > SPEC_MARKOV_MAX_TOPK) return 0;
+    const size_t ncand = (size_t)(topk < V ? topk : V);
+    return (sizeof(int32_t) * (size_t)B * (size_t)K * ncand + 255) & ~(size_t)255;
+}
+
+extern "C" int spec_markov_draft_topk(const void *base, int dtype, int B, int K, int V, int64_t ld_row,
+                                      const int32_t *anchor, const void *emb, const void *proj, int rank,
+                                      const float *temperature, uint64_t seed, uint64_t step, int topk,
+                                      int32_t *out_tokens, float *out_logits, int32_t *out_status, void *ws,
+                                      size_t ws_bytes, void *cuda_stream) {
+    if (B < 0 || K < 0 || V <= 0 || ld_row < V || rank <= 0 || topk <= 0) return SPEC_EINVAL;
+    if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_EINVAL;
+    if (B == 0) return SPEC_OK;
+    if (B > SPEC_MAX_BATCH || K > SPEC_MAX_DRAFTS || rank > SPEC_MARKOV_MAX_RANK || (rank & 3) ||
+        topk > SPEC_MARKOV_MAX_TOPK)
+        return SPEC_EUNSUPPORTED;
+    if ((int64_t)B * K >= ((int64_t)1 << 31)) return SPEC_EUNSUPPORTED;
+    if (!anchor || !emb || !proj || !out_status) return SPEC_EINVAL;
+    if (K > 0 && (!base || !out_tokens)) return SPEC_EINVAL;
+    const int esz = dtype == SPEC_BF16 ? 2 : 4;
+    if (((uintptr_t)base % esz) || ((uintptr_t)emb % esz) || ((uintptr_t)proj % esz) || ((uintptr_t)out_logits % 4))
+        return SPEC_EINVAL;
+    const size_t need = spec_markov_topk_workspace_size(B, K, V, topk);
+    if (K > 0 && (!ws || ws_bytes < need || ((uintptr_t)ws & 15))) return SPEC_EWORKSPACE;
+    MarkovParams p;
+    p.base = base;
+    p.emb = emb;
+    p.proj = proj;
+    p.dtype = dtype;
+    p.B = B;
+    p.K = K;
+    p.V = V;
+    p.r = rank;
+    p.ld_row = ld_row;
+    p.anchor = anchor;
+    p.temperature = temperature;
+    p.seed = seed;
+    p.step = (uint32_t)step;
+    p.tokens = out_tokens;
+    p.z = out_logits;
+    p.status = out_status;
+    return markov_topk_impl(p, topk < V ? topk : V, (int32_t *)ws, (cudaStream_t)cuda_stream);
 }

@@ -132,6 +132,32 @@ def test_markov_host_argument_errors(lib):
     assert mk(emb=ctypes.c_void_p(17)) == EINVAL and mk(z=ctypes.c_void_p(18)) == EINVAL
 
 
+def test_markov_topk_host_argument_errors(lib):
+    """spec_markov_draft_topk: the candidate count, the workspace and the checks of
+    spec_markov_draft, before any launch; the workspace is B K min(topk, V) int32."""
+    EINVAL, EUNSUP, EWS = 1, 3, 4
+    P = ctypes.c_void_p(16)
+    ws_size = lib.spec_markov_topk_workspace_size
+    assert ws_size(64, 7, 151936, 64) == 64 * 7 * 64 * 4
+    assert ws_size(3, 2, 10, 64) == 256  # min(topk, V) = 10 candidates, 240 bytes rounded up to 256
+    assert ws_size(1, 1, 10, 0) == 0 and ws_size(1, 1, 10, 1025) == 0 and ws_size(-1, 1, 10, 4) == 0
+
+    def mk(**kw):
+        a = dict(base=P, dtype=0, B=2, K=3, V=100, ld=100, anchor=P, emb=P, proj=P, r=8, T=P, topk=16, tok=P, z=P,
+                 st=P, ws=P, wsb=1 << 20)
+        a.update(kw)
+        return lib.spec_markov_draft_topk(a["base"], a["dtype"], a["B"], a["K"], a["V"], a["ld"], a["anchor"],
+                                          a["emb"], a["proj"], a["r"], a["T"], 0, 0, a["topk"], a["tok"], a["z"],
+                                          a["st"], a["ws"], a["wsb"], None)
+
+    assert mk(B=0) == 0
+    assert mk(topk=0) == EINVAL and mk(topk=-3) == EINVAL and mk(topk=1025) == EUNSUP
+    assert mk(B=-1) == EINVAL and mk(V=0) == EINVAL and mk(ld=99) == EINVAL and mk(r=6) == EUNSUP
+    assert mk(anchor=None) == EINVAL and mk(tok=None) == EINVAL and mk(st=None) == EINVAL
+    assert mk(ws=None) == EWS and mk(wsb=2 * 3 * 16 * 4 - 1) == EWS and mk(ws=ctypes.c_void_p(24)) == EWS
+    assert mk(z=ctypes.c_void_p(18)) == EINVAL
+
+
 def test_threshold_host_argument_errors(lib):
     EINVAL = 1
     P = ctypes.c_void_p(16)
