@@ -329,6 +329,24 @@ def run_ours(args) -> None:
         def greedy(self, i):
             binding.spec_verify_greedy(self.t, self.x, self.nd, self.tok, self.acc, self.st, self.ws, stream)
 
+        def early_exit(self, i):
+            binding.spec_verify_sample_early_exit(self.t, self.d, self.x, self.nd, self.T, self.seed, i, self.tok,
+                                                  self.acc, self.p, self.q, self.st, stream)
+
+        def early_exit_line(self, n: int, warm: int) -> dict:
+            """The same batch through the early-exit call: µs per step and the rows it
+            reads (against the two-kernel step's rows)."""
+            ms = timed(self.early_exit, n, warm)
+            o = self.outputs()
+            assert (o["status"] == 0).all(), "a request reported a non-zero status (early exit)"
+            kb = np.asarray(self.kb)
+            greedy = np.asarray(self.temps) == 0
+            A = o["accepted"]
+            walked = np.minimum(A + 1, kb) + (A == kb)  # target rows, then the bonus/argmax row
+            rows = int(np.where(greedy, walked, 2 * np.minimum(A + 1, kb) + (A == kb)).sum())
+            full = int(np.where(greedy, kb + 1, 2 * kb + 1).sum())
+            return {"early_exit": {**_pcts(ms), "rows_read": rows, "rows_full_scan": full}}
+
         def outputs(self):
             torch.cuda.synchronize()
             return {"tokens": self.tok.cpu().numpy(), "accepted": self.acc.cpu().numpy(),
@@ -433,11 +451,13 @@ def run_ours(args) -> None:
         configs["tiny"] = entry("tiny: B=1 K=4 V=1024 fp32, sampling", timed(tb.sample, 200, 10), tb, 4,
                                 near=_parity_counts(tb.outputs(), tb.oracle_ref(209), tb.temps))
         configs["tiny_greedy"] = entry("tiny: greedy", timed(tb.greedy, 200, 10), tb, 4, greedy=True)
+        configs["tiny"].update(tb.early_exit_line(200, 10))
         del tb
         # small: 8.7 MB, fits L2 (flushed before every call)
         sb = Verify(synth.small(0, device=dev), seed=2)
         configs["small"] = entry("small: B=8 K=8 V=32000 bf16, sampling", timed(sb.sample, 100, 10), sb, 64,
                                  near=_parity_counts(sb.outputs(), sb.oracle_ref(109), sb.temps))
+        configs["small"].update(sb.early_exit_line(100, 10))
         del sb
         # ragged: the scheduler, the verify of its lengths, and both in one timed region
         sch = synth.ragged_schedule_inputs(0)
@@ -461,12 +481,14 @@ def run_ours(args) -> None:
                                   near=_parity_counts(rb.outputs(), rb.oracle_ref(54), rb.temps),
                                   extra={"scheduler": _pcts(s_ms), "scheduler_and_verify": _pcts(b_ms),
                                          "sum_L": sum(lens), "n_star": float(info[0].item())})
+        configs["ragged"].update(rb.early_exit_line(50, 5))
         del rb
         # stress: 2.18 GB fp32, even requests greedy, odd sampling, adversarial rows
         xb = Verify(synth.stress(0, device=dev), seed=5)
         x_ms = timed(xb.sample, 20, 3)
         configs["stress"] = entry("stress: B=512 K=4 V=151936 fp32, mixed greedy/sampling", x_ms, xb, 512 * 4,
                                   near=_parity_counts(xb.outputs(), xb.oracle_ref(22), xb.temps))
+        configs["stress"].update(xb.early_exit_line(20, 3))
         del xb
 
         # Markov-head drafting of the headline block shape (B, K, V), rank 256, random

@@ -412,100 +412,23 @@ __device__ __noinline__ void topk_radix(const MarkovParams &p, int ncand, int32_
     }
 }
 
-constexpr int kTkKeep = 8;  // entries each selection thread keeps
-constexpr int kTkUnion = kTkThreads * kTkKeep;
+constexpr int kTkGather = 4096;  // entries the fast selection gathers at most
 constexpr int kTkTieMax = 1024;  // entries equal to the threshold key ranked by index in the fast path
 
-// Keeps (key, v) in a thread's sorted list of its kTkKeep largest: strictly larger
-// keys only, so among equal keys the earlier (lower) index stays.
-__device__ __forceinline__ void topk_keep(uint32_t (&kk)[kTkKeep], int (&ki)[kTkKeep], uint32_t key, int v) {
-    if (key <= kk[kTkKeep - 1]) return;
-    bool placed = false;
-#pragma unroll
-    for (int s = kTkKeep - 1; s >= 0; --s) {
-        if (!placed) {
-            if (s > 0 && key > kk[s - 1]) {
-                kk[s] = kk[s - 1];
-                ki[s] = ki[s - 1];
-            } else {
-                kk[s] = key;
-                ki[s] = v;
-                placed = true;
-            }
-        }
-    }
-}
-
-// One CTA per row (b, k), one read of the row.  Each thread keeps its kTkKeep
-// largest (key, index) pairs (its entries come in index order); the CTA then
-// finds the ncand-th largest key of the union by radix (4 x 8-bit digits over the
-// union in shared memory), lists the union's entries above it, and ranks the
-// union's entries equal to it by index.  Exact unless some thread's smallest kept
-// key reaches that key (the thread may hold more) or too many entries tie at it:
-// then the row is selected again by radix over the whole row (topk_radix).
-template <int ESZ>
-__global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovParams p, int ncand, int32_t *cands) {
-    __shared__ uint32_t s_key[kTkUnion];
-    __shared__ int s_idx[kTkUnion];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t s_pick[2];
-    __shared__ int s_cnt[2];
-    constexpr int VE = 16 / ESZ;
+// Block (kTkThreads threads): the k-th largest of the n keys at keys (k <= n), by
+// radix over four 8-bit digits; returns it, with *take = how many of the keys equal
+// to it belong to the k largest.  Scratch: hist[256], pick[2].
+__device__ uint32_t radix_kth(const uint32_t *keys, int n, int k, uint32_t *hist, uint32_t *pick, int *take) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t row = blockIdx.x;
-    const char *u = (const char *)p.base + row * p.ld_row * ESZ;
-    if (p.z) {  // the corrected row: -inf outside the candidates (they are written later)
-        float *zrow = p.z + row * p.V;
-        if ((p.V & 3) == 0) {
-            const float4 ni = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
-            for (int i = tid; i < (p.V >> 2); i += kTkThreads) reinterpret_cast<float4 *>(zrow)[i] = ni;
-        } else {
-            for (int i = tid; i < p.V; i += kTkThreads) zrow[i] = kNegInf;
-        }
-    }
-    uint32_t kk[kTkKeep];
-    int ki[kTkKeep];
-#pragma unroll
-    for (int i = 0; i < kTkKeep; ++i) {
-        kk[i] = 0u;  // below every key (0 is the key of no value: NaN maps to the top)
-        ki[i] = -1;
-    }
-    // entry v is thread v mod kTkThreads's (neighbouring entries -- where a Zipf-like
-    // head puts the largest logits -- go to different threads), eight coalesced
-    // loads in flight per thread
-    constexpr int kU = 8;
-    for (int v0 = tid; v0 < p.V; v0 += kTkThreads * kU) {
-        float x[kU];
-#pragma unroll
-        for (int e = 0; e < kU; ++e) {
-            const int v = v0 + e * kTkThreads;
-            x[e] = v < p.V ? ld_elem<ESZ>(u, v) : 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < kU; ++e) {
-            const int v = v0 + e * kTkThreads;
-            if (v < p.V) topk_keep(kk, ki, topk_key(x[e]), v);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < kTkKeep; ++i) {
-        s_key[tid * kTkKeep + i] = ki[i] < 0 ? 0u : kk[i];
-        s_idx[tid * kTkKeep + i] = ki[i];
-    }
-    if (tid == 0) {
-        s_cnt[0] = 0;
-        s_cnt[1] = 0;
-    }
-    // the ncand-th largest key of the union (radix, as topk_radix over the row)
     uint32_t prefix = 0u, pmask = 0u;
-    int rem = ncand;
+    int rem = k;
     for (int pass = 0; pass < 4; ++pass) {
         const int sh = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += kTkThreads) hist[i] = 0u;
+        for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < kTkUnion; i += kTkThreads) {
-            const uint32_t key = s_key[i];
-            if (s_idx[i] >= 0 && (key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & 255u], 1u);
+        for (int i = tid; i < n; i += blockDim.x) {
+            const uint32_t key = keys[i];
+            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & 255u], 1u);
         }
         __syncthreads();
         if (warp == 0) {
@@ -526,8 +449,8 @@ __global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovPa
                 uint32_t run = above;
                 for (int i = 0; i < 8; ++i) {
                     if (run + c[i] >= (uint32_t)rem) {
-                        s_pick[0] = 255u - 8u * lane - i;
-                        s_pick[1] = run;
+                        pick[0] = 255u - 8u * lane - i;
+                        pick[1] = run;
                         break;
                     }
                     run += c[i];
@@ -535,37 +458,125 @@ __global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovPa
             }
         }
         __syncthreads();
-        prefix |= s_pick[0] << sh;
+        prefix |= pick[0] << sh;
         pmask |= 0xffu << sh;
-        rem -= (int)s_pick[1];
+        rem -= (int)pick[1];
         __syncthreads();
     }
-    // prefix: the threshold key; rem of the entries equal to it are taken
-    const bool unsure = ki[kTkKeep - 1] >= 0 && kk[kTkKeep - 1] >= prefix;
-    if (__syncthreads_or(unsure)) {
+    *take = rem;
+    return prefix;
+}
+
+// One CTA per row (b, k).  Entry v is thread v mod kTkThreads's (neighbouring
+// entries -- where a Zipf-like head puts the largest logits -- go to different
+// threads).  Pass 1: each thread's largest key; the ncand-th largest of those
+// maxima is a lower bound t0 of the row's ncand-th largest key (they are ncand
+// distinct entries).  Pass 2: every entry with key >= t0 is gathered into shared
+// memory (typically a few hundred).  The ncand-th largest key of the gathered set
+// (radix) is the row's; the entries above it are listed, and those equal to it
+// ranked by index.  Exact; when more than kTkGather entries pass t0 (or ncand
+// exceeds the thread count, or too many tie), the row is selected again by radix
+// over the whole row (topk_radix).
+template <int ESZ>
+__global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovParams p, int ncand, int32_t *cands) {
+    __shared__ uint32_t s_key[kTkGather];
+    __shared__ int s_idx[kTkGather];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_pick[2];
+    __shared__ int s_cnt[3];
+    __shared__ int s_tie[kTkTieMax];
+    const int tid = threadIdx.x;
+    const int64_t row = blockIdx.x;
+    const char *u = (const char *)p.base + row * p.ld_row * ESZ;
+    if (p.z) {  // the corrected row: -inf outside the candidates (they are written later)
+        float *zrow = p.z + row * p.V;
+        if ((p.V & 3) == 0) {
+            const float4 ni = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+            for (int i = tid; i < (p.V >> 2); i += kTkThreads) reinterpret_cast<float4 *>(zrow)[i] = ni;
+        } else {
+            for (int i = tid; i < p.V; i += kTkThreads) zrow[i] = kNegInf;
+        }
+    }
+    if (ncand > kTkThreads) {
         topk_radix<ESZ>(p, ncand, cands, false);
         return;
     }
+    constexpr int kU = 8;  // loads in flight per thread
+    uint32_t tmax = 0u;    // below every key (0 is the key of no value: NaN maps to the top)
+    for (int v0 = tid; v0 < p.V; v0 += kTkThreads * kU) {
+        float x[kU];
+#pragma unroll
+        for (int e = 0; e < kU; ++e) {
+            const int v = v0 + e * kTkThreads;
+            x[e] = v < p.V ? ld_elem<ESZ>(u, v) : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < kU; ++e)
+            if (v0 + e * kTkThreads < p.V) tmax = max(tmax, topk_key(x[e]));
+    }
+    s_key[tid] = tmax;
+    if (tid == 0) {
+        s_cnt[0] = 0;
+        s_cnt[1] = 0;
+        s_cnt[2] = 0;
+    }
+    int take;
+    const uint32_t t0 = radix_kth(s_key, kTkThreads, ncand, hist, s_pick, &take);
+    // pass 2: gather every entry at or above t0 (warp-aggregated appends; the loop
+    // runs on the warp's first entry, so every lane takes part in each ballot)
+    const int lane = tid & 31;
+    for (int w0 = tid - lane; w0 < p.V; w0 += kTkThreads * kU) {
+        const int v0 = w0 + lane;
+        float x[kU];
+#pragma unroll
+        for (int e = 0; e < kU; ++e) {
+            const int v = v0 + e * kTkThreads;
+            x[e] = v < p.V ? ld_elem<ESZ>(u, v) : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < kU; ++e) {
+            const int v = v0 + e * kTkThreads;
+            const uint32_t key = v < p.V ? topk_key(x[e]) : 0u;
+            const bool in = v < p.V && key >= t0;
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            if (bal) {
+                int base = 0;
+                if (lane == 0) base = atomicAdd(&s_cnt[0], __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const int slot = base + __popc(bal & ((1u << lane) - 1u));
+                if (in && slot < kTkGather) {
+                    s_key[slot] = key;
+                    s_idx[slot] = v;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int ng = s_cnt[0];
+    if (ng > kTkGather) {
+        topk_radix<ESZ>(p, ncand, cands, false);
+        return;
+    }
+    // the row's ncand-th largest key: that of the gathered set, which holds every
+    // entry at or above t0 <= it
+    int rem;
+    const uint32_t thr = radix_kth(s_key, ng, ncand, hist, s_pick, &rem);
     int32_t *out = cands + row * ncand;
-    // the union holds every entry of the row at or above the threshold: those above
-    // it are listed (ncand - rem of them, in any order), those equal to it gathered
-    // for ranking by index
-    __shared__ int s_tie[kTkTieMax];
-    for (int i = tid; i < kTkUnion; i += kTkThreads) {
-        if (s_idx[i] < 0) continue;
-        if (s_key[i] > prefix) {
-            out[atomicAdd(&s_cnt[0], 1)] = s_idx[i];
-        } else if (s_key[i] == prefix) {
-            const int slot = atomicAdd(&s_cnt[1], 1);
+    for (int i = tid; i < ng; i += kTkThreads) {
+        if (s_key[i] > thr) {
+            out[atomicAdd(&s_cnt[1], 1)] = s_idx[i];
+        } else if (s_key[i] == thr) {
+            const int slot = atomicAdd(&s_cnt[2], 1);
             if (slot < kTkTieMax) s_tie[slot] = s_idx[i];
         }
     }
     __syncthreads();
-    const int ne = s_cnt[1];
+    const int ne = s_cnt[2];
     if (ne > kTkTieMax) {
         topk_radix<ESZ>(p, ncand, cands, false);
         return;
     }
+    // the equal entries ranked by index (bitonic sort of at most kTkTieMax)
     int n2 = 1;
     while (n2 < ne) n2 <<= 1;
     for (int i = ne + tid; i < n2; i += kTkThreads) s_tie[i] = 0x7fffffff;
@@ -590,8 +601,8 @@ __global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovPa
 }
 
 // One CTA per request: the positions in order; at position k the bias of each of
-// the row's ncand candidates (one warp per candidate at a time: lanes split the
-// rank, fp32), then the draw over them.
+// the row's ncand candidates (four threads a candidate, fp32), then the draw over
+// them.
 template <int ESZ>
 __global__ void __launch_bounds__(kTkDrawThreads) markov_topk_draw_kernel(MarkovParams p, int ncand,
                                                                        const int32_t *cands) {
@@ -616,12 +627,21 @@ __global__ void __launch_bounds__(kTkDrawThreads) markov_topk_draw_kernel(Markov
         const char *u = (const char *)p.base + row * p.ld_row * ESZ;
         for (int j = tid; j < p.r; j += kTkDrawThreads) s_h[j] = ld_elem<ESZ>(p.emb, (int64_t)prev * p.r + j);
         __syncthreads();
-        for (int ci = warp; ci < ncand; ci += NW) {
-            const int v = cl[ci];
+        // four threads a candidate, each a quarter of the rank (interleaved), the
+        // loads unrolled so that they are in flight together
+        for (int c0 = 0; c0 < ncand; c0 += kTkDrawThreads / 4) {
+            const int ci = c0 + (tid >> 2), part = tid & 3;
             float acc = 0.f;
-            for (int j = lane; j < p.r; j += 32) acc = fmaf(s_h[j], ld_elem<ESZ>(p.proj, (int64_t)v * p.r + j), acc);
-            acc = warp_sum(acc);
-            if (lane == 0) {
+            int v = 0;
+            if (ci < ncand) {
+                v = cl[ci];
+                const char *pr = (const char *)p.proj + (int64_t)v * p.r * ESZ;
+#pragma unroll 8
+                for (int j = part; j < p.r; j += 4) acc = fmaf(s_h[j], ld_elem<ESZ>(pr, j), acc);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (ci < ncand && part == 0) {
                 const float z = ld_elem<ESZ>(u, v) + acc;
                 s_z[ci] = z;
                 if (p.z) p.z[row * p.V + v] = z;

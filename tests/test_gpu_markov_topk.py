@@ -93,6 +93,17 @@ def test_ties_and_nan_in_the_base_logits():
         compare(gpu, ref)
 
 
+def test_gather_overflow_falls_back_exactly():
+    """A constant row of V = 9000 (every entry ties: more than the fast path gathers)
+    and a row whose largest values sit in one thread's stride (v = 512 j): both take
+    the exact whole-row selection."""
+    m = synth.markov(11, B=3, K=2, V=9000, r=8, dtype=torch.bfloat16)
+    m["base"][0, 1, :] = 1.5
+    m["base"][2, 0, ::512] = 60.0
+    for topk in (5, 64):
+        compare(run_gpu(m, topk), run_oracle(m, topk))
+
+
 def test_topk_at_least_vocab_equals_full_vocab():
     import speculative_decoding_verification_15_gb300 as pkg
 
