@@ -18,8 +18,9 @@
 //                        and writes z.  Every projection row is read once per
 //                        position (from L2 after the first position: r x V x 2 B =
 //                        78 MB at V = 151936, r = 256 in bf16, fits the 129 MB L2).
-//  markov_sample_kernel  one CTA per request: Gumbel-max (or argmax) over z_k,
-//                        status, and the token that the next position's bias uses.
+//  markov_sample_kernel  one CTA per request: the pruned exact Gumbel-max (or the
+//                        argmax) over z_k, status, and the token that the next
+//                        position's bias uses.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,6 +35,7 @@ constexpr int kMkCols = 32;        // vocabulary entries per bias CTA
 constexpr int kMkThreads = 256;    // 8 warps: one request at a time each
 constexpr int kMkWarps = kMkThreads / 32;
 constexpr int kMkSampleThreads = 1024;
+constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every mbarrier wait (2 s)
 
 struct MarkovParams {
     const void *base;  // [B, K, ld_row] backbone logits
@@ -197,6 +199,155 @@ __global__ void __launch_bounds__(kMkThreads) markov_bias_mma_kernel(MarkovParam
     }
 }
 
+// bf16 factors, the same products with the projection rows streamed: a persistent
+// grid (two CTAs per SM at r = 256) walks the 64-entry column tiles; for each chunk
+// of 64 requests a CTA keeps their embedding rows H in shared memory and brings each
+// tile's 64 projection rows in by bulk copies (one per row, into rows padded by 8
+// elements so that a warp's fragment loads hit 32 banks), double-buffered on two
+// mbarriers, so the next tile's rows land while the tensor cores work on this one.
+// Warp w forms entries 8w .. 8w+7 of the tile for all 64 requests (mma.sync
+// m16n8k16, fp32 accumulate; the backbone logits are loaded before the products and
+// added after them).  A bulk-copy wait is bounded: if one gives up, the
+// CTA waits (bounded) for its copies in flight and writes NaN for the rest of its
+// tiles, so those requests report status 4.
+__host__ __device__ inline size_t tma_smem_bytes(int r) {
+    return sizeof(uint16_t) * (size_t)(kMmReqs + 2 * kMmCols) * (r + 8) + sizeof(int) * kMmReqs;
+}
+
+__global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovParams p, int k) {
+    extern __shared__ __align__(128) uint16_t tms[];
+    __shared__ __align__(8) uint64_t s_bar[2];
+    const int rs = p.r + 8;
+    uint16_t *Hs = tms;                                 // [64 requests][rs]
+    uint16_t *Ps = tms + (size_t)kMmReqs * rs;          // [2 stages][64 entries][rs]
+    int *okv = reinterpret_cast<int *>(Ps + 2 * (size_t)kMmCols * rs);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ntiles = (p.V + kMmCols - 1) / kMmCols;
+    const uint32_t rowbytes = (uint32_t)p.r * 2u;
+    const int vpr = p.r >> 3;  // 16-byte vectors per row
+    if (tid == 0) {
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    uint32_t used[2] = {0u, 0u};  // phases of each stage waited on so far (the same in every thread)
+    bool failed = false;
+    const int g = lane >> 2, t2 = (lane & 3) * 2;
+    for (int b0 = 0; b0 < p.B; b0 += kMmReqs) {
+        if (tid < kMmReqs) {
+            const int b = b0 + tid;
+            int ok = 0;
+            if (b < p.B) {
+                const int prev = k == 0 ? p.anchor[b] : p.tokens[(int64_t)b * p.K + k - 1];
+                ok = (prev >= 0 && prev < p.V) ? prev + 1 : 0;  // 1 + the row to gather, 0: none
+            }
+            okv[tid] = ok;
+        }
+        __syncthreads();
+        for (int i = tid; i < kMmReqs * vpr; i += kMkThreads) {
+            const int m = i / vpr, q = i - m * vpr;
+            const int ok = okv[m];
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (ok) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.emb + (int64_t)(ok - 1) * p.r + 8 * q);
+            *reinterpret_cast<uint4 *>(Hs + m * rs + 8 * q) = x;
+        }
+        // tile t into stage st: warp 0 registers the bytes, then its lanes issue one
+        // bulk copy per row
+        auto issue = [&](int t, int st) {
+            if (warp != 0) return;
+            const int v0 = t * kMmCols, nc = min(kMmCols, p.V - v0);
+            if (lane == 0) mbar_arrive_expect_tx(&s_bar[st], (uint32_t)nc * rowbytes);
+            __syncwarp();
+            for (int c = lane; c < nc; c += 32)
+                bulk_g2s(Ps + ((size_t)st * kMmCols + c) * rs, (const uint16_t *)p.proj + (int64_t)(v0 + c) * p.r,
+                         rowbytes, &s_bar[st]);
+        };
+        int i = 0;
+        if (!failed && (int)blockIdx.x < ntiles) issue(blockIdx.x, 0);
+        __syncthreads();  // H and okv are in
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int st = i & 1;
+            const int tn = t + gridDim.x;
+            if (!failed && tn < ntiles) issue(tn, st ^ 1);  // stage st ^ 1 was released at the last barrier
+            bool ok = !failed;
+            if (ok) {
+                if (tid == 0) ok = mbar_wait(&s_bar[st], used[st] & 1u, kWaitNs);
+                ok = !__syncthreads_or(!ok);
+                if (ok) mbar_try_wait(&s_bar[st], used[st] & 1u);  // every thread observes the completed phase
+                used[st] += 1u;
+                if (!ok) {
+                    failed = true;
+                    // the copies in flight still land: wait for them (bounded) before the
+                    // CTA can leave
+                    if (tid == 0) {
+                        mbar_wait(&s_bar[st], (used[st] - 1u) & 1u, kWaitNs);
+                        if (tn < ntiles) mbar_wait(&s_bar[st ^ 1], used[st ^ 1] & 1u, kWaitNs);
+                    }
+                    __syncthreads();
+                }
+            }
+            const int v0 = t * kMmCols, ncol = min(kMmCols, p.V - v0);
+            // this thread's 16 backbone logits of the tile (bf16, two to a register),
+            // loaded before the products so that their latency overlaps the tensor-core
+            // work; they are added after the products, as z = U + (emb . proj)
+            uint32_t upk[8];
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int m = mt * 16 + g + 8 * h;
+                    const int n = warp * 8 + t2;
+                    const int b = b0 + m;
+                    const unsigned short *ur =
+                        (const unsigned short *)p.base + ((int64_t)b * p.K + k) * p.ld_row + v0 + n;
+                    const uint32_t lo = (b < p.B && n < ncol) ? __ldg(ur) : 0u;
+                    const uint32_t hi = (b < p.B && n + 1 < ncol) ? __ldg(ur + 1) : 0u;
+                    upk[mt * 2 + h] = lo | (hi << 16);
+                }
+            float acc[4][4];
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+            if (ok) {
+                const uint16_t *pb = Ps + ((size_t)st * kMmCols + warp * 8 + g) * rs + t2;
+                for (int kk = 0; kk < p.r; kk += 16) {
+                    uint32_t bf[2];
+                    bf[0] = *reinterpret_cast<const uint32_t *>(pb + kk);
+                    bf[1] = *reinterpret_cast<const uint32_t *>(pb + kk + 8);
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        const uint16_t *pa = Hs + (mt * 16 + g) * rs + kk + t2;
+                        uint32_t af[4];
+                        af[0] = *reinterpret_cast<const uint32_t *>(pa);
+                        af[1] = *reinterpret_cast<const uint32_t *>(pa + 8 * rs);
+                        af[2] = *reinterpret_cast<const uint32_t *>(pa + 8);
+                        af[3] = *reinterpret_cast<const uint32_t *>(pa + 8 * rs + 8);
+                        mma_bf16_16816(acc[mt], af, bf);
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = mt * 16 + g + (e >= 2 ? 8 : 0);
+                    const int n = warp * 8 + t2 + (e & 1);
+                    const int b = b0 + m;
+                    if (b < p.B && n < ncol) {
+                        const int64_t row = (int64_t)b * p.K + k;
+                        const int v = v0 + n;
+                        const uint32_t w = upk[mt * 2 + (e >> 1)];
+                        const float uv = (e & 1) ? __uint_as_float(w & 0xffff0000u) : __uint_as_float(w << 16);
+                        p.z[row * p.V + v] = (ok && okv[m]) ? uv + acc[mt][e] : __int_as_float(0x7fc00000);
+                    }
+                }
+            __syncthreads();  // stage st and (after the chunk) H are free
+        }
+    }
+}
+
 // One CTA per request.  k = -1: the status of a block with no positions (K = 0).
 __global__ void __launch_bounds__(kMkSampleThreads) markov_sample_kernel(MarkovParams p, int k) {
     __shared__ float red_s[kMkSampleThreads / 32];
@@ -224,23 +375,96 @@ __global__ void __launch_bounds__(kMkSampleThreads) markov_sample_kernel(MarkovP
     bool bad = false;
     if (st == SPEC_STATUS_OK) {
         const float *zr = p.z + ((int64_t)b * p.K + k) * p.V;
-        const float invT = T == 0.f ? 0.f : __fdiv_rn(1.f, T);
-        // thread tid takes the groups of 4 entries tid, tid + 1024, ... (one Philox
-        // block per group)
-        for (int g = tid; 4 * g < p.V; g += kMkSampleThreads) {
-            const uint4 r4 = T == 0.f ? make_uint4(0, 0, 0, 0)
-                                      : rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)k, PURPOSE_DRAFT, (uint32_t)g);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int v = 4 * g + e;
-                if (v >= p.V) break;
+        if (T == 0.f) {
+            for (int v = tid; v < p.V; v += kMkSampleThreads) {
                 const float zv = zr[v];
                 if (zv != zv || zv == __int_as_float(0x7f800000)) bad = true;
-                if (!(zv > kNegInf)) continue;
-                const float sc = T == 0.f ? zv : fmaf(zv, invT, gumbel_of_word(word_of(r4, e)));
-                if (better(sc, v, best, bi)) {
-                    best = sc;
+                if (zv > kNegInf && better(zv, v, best, bi)) {
+                    best = zv;
                     bi = v;
+                }
+            }
+        } else {
+            // The draw argmax_v z_v / T + g_v, pruned exactly (as the verify's draws): a
+            // group of 4 entries can only beat a known exact score thr if
+            // z_max / T + 17 >= thr (no word gives more than 16.64 of noise), and an
+            // entry only if 1 - u <= 1.001 e^(z / T - thr).  thr starts at the best exact
+            // score of each thread's largest entry (pass 1, which also checks the row).
+            const float invT = __fdiv_rn(1.f, T);
+            float m = kNegInf;
+            int mi = -1;
+            if ((p.V & 3) == 0) {  // rows 16-byte aligned: four groups (float4) in flight a thread
+                const float4 *z4 = reinterpret_cast<const float4 *>(zr);
+                const int ng = p.V >> 2;
+                for (int g0 = tid; g0 < ng; g0 += 4 * kMkSampleThreads) {
+                    float4 q[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int g = g0 + u * kMkSampleThreads;
+                        q[u] = g < ng ? z4[g] : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int g = g0 + u * kMkSampleThreads;
+                        const float zq[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (zq[e] != zq[e] || zq[e] == __int_as_float(0x7f800000)) bad = true;
+                            if (zq[e] > m) {
+                                m = zq[e];
+                                mi = 4 * g + e;
+                            }
+                        }
+                    }
+                }
+            } else {
+                for (int v = tid; v < p.V; v += kMkSampleThreads) {
+                    const float zv = zr[v];
+                    if (zv != zv || zv == __int_as_float(0x7f800000)) bad = true;
+                    if (zv > m) {
+                        m = zv;
+                        mi = v;
+                    }
+                }
+            }
+            if (mi >= 0) {
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)k, PURPOSE_DRAFT, (uint32_t)mi >> 2);
+                best = fmaf(m, invT, gumbel_of_word(word_of(r4, mi & 3)));
+                bi = mi;
+            }
+            float thr = warp_max(best);
+            if ((tid & 31) == 0) red_s[tid >> 5] = thr;
+            __syncthreads();
+            for (int w = 0; w < kMkSampleThreads / 32; ++w) thr = fmaxf(thr, red_s[w]);
+            __syncthreads();  // red_s is reused below
+            const bool vec = (p.V & 3) == 0;  // rows 16-byte aligned: one float4 per group
+            for (int g = tid; 4 * g < p.V; g += kMkSampleThreads) {
+                float zq[4];
+                if (vec) {
+                    const float4 q4 = reinterpret_cast<const float4 *>(zr)[g];
+                    zq[0] = q4.x;
+                    zq[1] = q4.y;
+                    zq[2] = q4.z;
+                    zq[3] = q4.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) zq[e] = 4 * g + e < p.V ? zr[4 * g + e] : kNegInf;
+                }
+                const float zmax = fmaxf(fmaxf(zq[0], zq[1]), fmaxf(zq[2], zq[3]));
+                if (!(zmax > kNegInf) || fmaf(zmax, invT, kGumbelMax) < thr) continue;
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)k, PURPOSE_DRAFT, (uint32_t)g);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int v = 4 * g + e;
+                    if (v >= p.V || !(zq[e] > kNegInf)) continue;
+                    const uint32_t wd = word_of(r4, e);
+                    if (one_minus_u01(wd) > ex2_approx((fmaf(zq[e], invT, 0.f) - thr) * kLog2e) * 1.001f) continue;
+                    const float sc = fmaf(zq[e], invT, gumbel_of_word(wd));
+                    if (better(sc, v, best, bi)) {
+                        best = sc;
+                        bi = v;
+                        thr = fmaxf(thr, sc);
+                    }
                 }
             }
         }
@@ -733,12 +957,36 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
             return SPEC_ECUDA;
         }
     }
+    // bf16 factors streamed by bulk copies: a persistent grid of as many CTAs as fit
+    const size_t tsmem = tma_smem_bytes(p.r);
+    int tgrid = 0;
+    if (mma) {
+        if (tsmem > 48 * 1024) {
+            e = cudaFuncSetAttribute(markov_bias_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsmem);
+            if (e != cudaSuccess) {
+                note_cuda_error((int)e);
+                return SPEC_ECUDA;
+            }
+        }
+        int dev = 0, sms = 0, per = 0;
+        e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, markov_bias_tma_kernel, kMkThreads, tsmem);
+        if (e != cudaSuccess) {
+            note_cuda_error((int)e);
+            return SPEC_ECUDA;
+        }
+        const int ntiles = (p.V + kMmCols - 1) / kMmCols;
+        tgrid = per > 0 ? min(ntiles, per * sms) : 0;
+    }
     if (p.K == 0) {
         markov_sample_kernel<<<p.B, kMkSampleThreads, 0, stream>>>(p, -1);
     } else {
         const int nb = (p.V + kMkCols - 1) / kMkCols, nbm = (p.V + kMmCols - 1) / kMmCols;
         for (int k = 0; k < p.K; ++k) {
-            if (mma)
+            if (mma && tgrid > 0)
+                markov_bias_tma_kernel<<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
+            else if (mma)
                 markov_bias_mma_kernel<<<nbm, kMkThreads, msmem, stream>>>(p, k);
             else
                 markov_bias_kernel<<<nb, kMkThreads, smem, stream>>>(p, k);
