@@ -619,13 +619,14 @@ struct ChunkDesc {
     int shift;       // window element 0 is row element e0 - shift
     float c;         // log2(e) / T, or 0 for a greedy row
     uint32_t t;      // the chunk (flat index); >= total when the CTA is done
+    int req;         // its request
 };
 
 // Row r of the main pass (request order; inside a request, sampling rows are
 // [target 0..k-1 | draft 0..k-1] and greedy rows [target 0..k-1]).
 // sc[b] = log2(e) / T_b (0: greedy), computed once per CTA with the row scan.
-template <class Vec>
-__device__ __forceinline__ ChunkDesc chunk_desc(const MainParams &p, const int *rs, const float *sc,
+template <class Vec, class Params>
+__device__ __forceinline__ ChunkDesc chunk_desc(const Params &p, const int *rs, const float *sc,
                                                 const Chunking &ck, uint32_t t, uint32_t total) {
     ChunkDesc d;
     d.t = t;
@@ -633,6 +634,7 @@ __device__ __forceinline__ ChunkDesc chunk_desc(const MainParams &p, const int *
     d.bytes = 0;
     d.e0 = d.e1 = d.shift = 0;
     d.c = 0.f;
+    d.req = 0;
     if (t >= total) return d;
     const int r = (int)(t / (uint32_t)ck.cpr), k = (int)(t - (uint32_t)r * (uint32_t)ck.cpr);
     const int b = find_request(rs, p.B, r);
@@ -649,6 +651,7 @@ __device__ __forceinline__ ChunkDesc chunk_desc(const MainParams &p, const int *
     d.e1 = w.e1;
     d.shift = w.shift;
     d.c = c;
+    d.req = b;
     return d;
 }
 
@@ -737,53 +740,6 @@ __device__ __forceinline__ float half_stats(const Vec (&d)[NV], float (&vm)[NV],
         m = max_nan_f32(m, tm);
     }
     return tm;
-}
-
-// One row's statistics from its cpr per-chunk partials (pp[0 .. cpr), read through
-// L2: other CTAs of this kernel wrote them); a warp.  stale: some partial does not
-// carry this call's tag (a chunk the main pass did not write in this call).
-__device__ __forceinline__ Part load_part(const Part *pp) {
-    const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(pp));
-    Part x;
-    x.m = __uint_as_float(w.x);
-    x.s = __uint_as_float(w.y);
-    x.idx = (int)w.z;
-    x.epoch = w.w;
-    return x;
-}
-
-__device__ __forceinline__ RowRes combine_parts(const Part *pp, int cpr, float c, bool greedy, uint32_t epoch,
-                                                bool &stale) {
-    const int lane = threadIdx.x & 31;
-    // a lane holds partials lane and lane + 32; rows of more than 64 chunks reread the rest
-    const Part p0 = lane < cpr ? load_part(pp + lane) : Part{kNegInf, 0.f, -1, epoch};
-    const Part p1 = lane + 32 < cpr ? load_part(pp + lane + 32) : Part{kNegInf, 0.f, -1, epoch};
-    bool st = p0.epoch != epoch || p1.epoch != epoch;
-    float m = max_nan_f32(p0.m, p1.m);
-    for (int q = lane + 64; q < cpr; q += 32) {
-        const Part x = load_part(pp + q);
-        st |= x.epoch != epoch;
-        m = max_nan_f32(m, x.m);
-    }
-    stale |= __any_sync(0xffffffffu, st);
-    const float M = warp_max_nan(m);
-    const float MC = __fmul_rn(M, c);
-    float sum = 0.f;
-    uint32_t bi = 0xffffffffu;
-    auto take = [&](const Part &x) {
-        if (!greedy && x.m != kNegInf && x.s != 0.f) sum += x.s * exp2f(__fmul_rn(x.m, c) - MC);
-        if (greedy && x.m == M && x.idx >= 0) bi = min(bi, (uint32_t)x.idx);
-    };
-    take(p0);
-    take(p1);
-    for (int q = lane + 64; q < cpr; q += 32) take(load_part(pp + q));
-#pragma unroll
-    for (int o = 16; o; o >>= 1) bi = min(bi, __shfl_xor_sync(0xffffffffu, bi, o));
-    RowRes r;
-    r.M = M;
-    r.idx = (int)bi;
-    r.l2S = greedy ? 0.f : log2f(warp_sum(sum));
-    return r;
 }
 
 // Every needed row once, in chunks of at most 64 KB handed out by dynamic tickets:
@@ -1608,6 +1564,866 @@ __global__ void __launch_bounds__(kJobThreads, kJobBlocksPerSM) commit_kernel(Jo
     }
 }
 
+// =================================================================== fused verify (large batches)
+// For batches of at least one request per SM, one persistent kernel does the whole
+// step: the main pass as main_kernel, then -- in the same CTAs, once the chunk
+// tickets run out -- the commit work as items taken by tickets (commit_item).  With
+// many requests each SM runs several items, so their dependent chains overlap, and
+// the kernel boundary and the wait for the last main CTA go away; with few requests
+// the piece layout of commit_kernel overlaps more of them, so the host picks by B.
+namespace fused {
+
+// Per-request words of the commit items, in the request's 128-byte line of the
+// workspace (the line commit_kernel's pieces use), zeroed with the ticket counters
+// before every launch.  Both are 64-bit and carry the call's tag in their high half
+// as well, so a word of another call reads as empty.
+constexpr int kSyncWords = 16;  // 64-bit words a request: the 128-byte line commit_kernel uses
+constexpr int kSyncDone = 0;   // (tag, items of the request finished)
+constexpr int kSyncBest = 1;   // (tag, ordered bits of the best exact score an item found)
+// Ticket counters at the start of the workspace, zeroed in stream order before every
+// launch (so a workspace left in any state by another call serves this one).  Every chunk and
+// every item is taken by ticket: a ticket is only ever held by a running CTA, which
+// finishes its chunks before it waits for anything, so progress never depends on a
+// CTA that is not resident.
+constexpr int kCntChunk = 0;
+constexpr int kCntItem = 1;
+constexpr int kSV = 2;             // commit items: vectors a thread holds per slice of a chunk
+// a warp's live list: < 64 carried + one vector's groups (2 pieces of 4 entries per
+// bf16 vector, each listing 2 groups when the window is not group-aligned)
+constexpr int kItemLive = 64 + 32 * 2 * 2;
+constexpr int kCandPrefetch = 1024;  // seed-candidate pointers an item fetches with the partials
+
+struct VerifyParams {
+    const void *target;
+    const void *draft;
+    int dtype;
+    int64_t ld_row;
+    int B, Kmax, V;
+    const int32_t *draft_tokens;
+    const int32_t *cu;         // flattened layout offsets [B+1], or NULL (padded)
+    const int32_t *num_draft;
+    const float *temperature;  // NULL: every request greedy
+    uint64_t seed;
+    uint32_t step;
+    uint32_t epoch;            // tag of this call, stored with every partial
+    int cpr, ce;               // chunks per row, entries per chunk
+    int Q;                     // commit items per request (1 .. cpr)
+    uint32_t *counters;        // [kCntChunk, kCntItem], zero at launch
+    unsigned long long *sync;  // [B][kSyncWords]
+    Part *parts;               // [chunks] one per chunk of every main-pass row
+    uint16_t *cand;            // [chunks][kCW] sampling rows: the window vector holding each warp's
+                               // maximum (0xffff: none), the correction's seed candidates
+    PieceRes *pres;            // [B][Q] the commit items' results
+    int32_t *out_tokens;
+    int32_t *out_accepted;
+    float *out_p;
+    float *out_q;
+    int32_t *out_status;
+};
+
+// The window of chunk k of a job row (a row the main pass may not have read).
+__device__ __forceinline__ ChunkDesc job_chunk(const char *row, int esz, int V, const Chunking &ck, int k) {
+    const ChunkWin w = chunk_window(row, esz, V, ck, k);
+    ChunkDesc d;
+    d.a0 = w.a0;
+    d.bytes = w.bytes;
+    d.e0 = w.e0;
+    d.e1 = w.e1;
+    d.shift = w.shift;
+    d.c = 0.f;
+    d.t = (uint32_t)k;
+    d.req = 0;
+    return d;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// The shared bound of a request: the best exact score published in this call, or
+// -inf (a word of another call).
+__device__ __forceinline__ float bound_of(unsigned long long w, uint32_t epoch) {
+    return (uint32_t)(w >> 32) == epoch ? ordered_float((uint32_t)w) : kNegInf;
+}
+__device__ __forceinline__ void publish_bound(unsigned long long *w, uint32_t epoch, float s) {
+    atomicMax(w, ((unsigned long long)epoch << 32) | ordered_bits(s));
+}
+
+// One thread: the request's arrival count, the word's own or a fresh one for this
+// call; returns the items arrived, this one included.
+__device__ __forceinline__ uint32_t arrive(unsigned long long *w, uint32_t epoch) {
+    unsigned long long cur = ld_relaxed_u64(w);
+    for (;;) {
+        const unsigned long long nw =
+            (uint32_t)(cur >> 32) == epoch ? cur + 1ull : (((unsigned long long)epoch << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(w, cur, nw);
+        if (prev == cur) return (uint32_t)nw;
+        cur = prev;
+    }
+}
+
+// Whole CTA: wait until the n partials at pp all carry this call's tag (the CTAs
+// that write them are running and wait for nothing, so they arrive; a 16-byte
+// partial is written and read whole), keeping a copy in stage when n <= cap (the
+// last round's copies all carry the tag); false after kWaitNs.
+__device__ bool wait_parts(const Part *pp, int n, uint32_t epoch, int *flag, Part *stage, int cap) {
+    uint64_t t0 = 0;
+    unsigned ns = 64;
+    const bool keep = n <= cap;
+    for (int round = 0;; ++round) {
+        bool miss = false;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const uint4 w = __ldcg((const uint4 *)(pp + i));
+            miss |= w.w != epoch;
+            if (keep) *(uint4 *)(stage + i) = w;
+        }
+        if (!__syncthreads_or(miss)) return true;
+        if (threadIdx.x == 0) {
+            const uint64_t now = global_ns();
+            if (round == 0) t0 = now;
+            *flag = now - t0 > kWaitNs;
+        }
+        __syncthreads();
+        if (*flag) return false;
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+    }
+}
+
+// One row's statistics from its cpr per-chunk partials, by one thread: from the
+// shared-memory copy, or through L2 (other CTAs wrote them in this call).  stale:
+// some partial carries another call's tag.
+template <bool STAGED>
+__device__ __forceinline__ RowRes row_from_parts_tagged(const Part *pp, int cpr, float c, bool greedy, uint32_t epoch,
+                                                 bool &stale) {
+    float M = kNegInf;
+    for (int q = 0; q < cpr; ++q) {
+        const uint4 w = STAGED ? *(const uint4 *)(pp + q) : __ldcg((const uint4 *)(pp + q));
+        stale |= w.w != epoch;
+        M = max_nan_f32(M, __uint_as_float(w.x));
+    }
+    const float MC = __fmul_rn(M, c);
+    float sum = 0.f;
+    int bi = -1;
+    for (int q = 0; q < cpr; ++q) {
+        const uint4 w = STAGED ? *(const uint4 *)(pp + q) : __ldcg((const uint4 *)(pp + q));
+        const float m = __uint_as_float(w.x), s = __uint_as_float(w.y);
+        const int idx = (int)w.z;
+        if (!greedy && m != kNegInf && s != 0.f) sum += s * exp2f(__fmul_rn(m, c) - MC);
+        if (greedy && m == M && idx >= 0 && (bi < 0 || idx < bi)) bi = idx;
+    }
+    RowRes r;
+    r.M = M;
+    r.idx = bi;
+    r.l2S = greedy ? 0.f : log2f(sum);
+    return r;
+}
+
+// ------------------------------------------------------------------ commit items
+// Item (b, q) of the Q items of request b:
+//  1. waits until every chunk partial of b's rows carries this call's tag;
+//  2. decides the request -- the same arithmetic on the same partials in every item,
+//     so all of them agree: row statistics, p(x_i) and q(x_i), the acceptance scan,
+//     and the one row still needed (the first rejected target row j for the
+//     correction, row k_b for the bonus draw or, greedy, for the argmax when every
+//     draft matched);
+//  3. streams chunks q, q + Q, ... of that row into registers, as the main pass
+//     does, and reduces them: the pruned Gumbel-max, or the argmax;
+//  4. stores its result and bumps the request's counter; the item that completes
+//     the count combines the Q results and writes the request's outputs.
+// The pruned Gumbel-max is exact.  An entry can beat the bound thr -- always the
+// exact score of some entry, or -inf -- only if z + kGumbelMax >= thr (no word gives
+// more than 16.64 of noise) and 1 - u <= 1.001 e^(z - thr) (g >= thr - z needs
+// -log u <= e^(z - thr), and -log u >= 1 - u).  Each warp lists the groups of four
+// whose largest z passes the first test, and every 64 listed groups draws their
+// Philox blocks, two groups per lane; only entries passing the second test are
+// scored exactly.
+
+struct ItemShared {
+    SliceRes red[kCW];
+    JobDesc job;
+    ReqBase rb;  // the request's layout, kept here through the draw (fewer live registers)
+    int kb;
+    int greedy;
+    int flag;
+    int last;
+};
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// Lists the live groups of this thread's vector t of a job chunk in the warp's list
+// (a group is live when its largest z = x invT - shift is finite and at least tz);
+// returns the new length.  CHECK_RAW folds every raw value into rawmax (rows the
+// main pass did not read).  mis: the window is not group-aligned, so each 4-entry
+// piece of the vector lists both groups it overlaps, with the piece's max as their
+// bound (a group may be listed twice: harmless).
+template <bool CHECK_RAW, class Vec>
+__device__ __forceinline__ int item_filter(const Vec &d, int t, int ebase, bool mis, float tz, float invT,
+                                           float shift, float &rawmax, uint32_t *lg, float *lz, int nlive) {
+    constexpr int NG = Vec::VE / 4;  // 4-entry pieces per vector
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    const int per = mis ? 2 : 1;
+    const int v0 = ebase + ((int)threadIdx.x + kCT * t) * Vec::VE;
+    if (CHECK_RAW) rawmax = max_nan_f32(rawmax, d.vmax());
+#pragma unroll
+    for (int m = 0; m < NG; ++m) {
+        const float z = fmaf(d.gmax(m), invT, -shift);
+        const bool live = z > kNegInf && z >= tz;
+        const unsigned bal = __ballot_sync(0xffffffffu, live);
+        if (live) {
+            const int pos = nlive + __popc(bal & lt) * per;
+            const int g = (v0 + 4 * m) >> 2;  // floor: v0 + 4m may be -4 .. -1 at a row start
+            lg[pos] = (uint32_t)g;
+            lz[pos] = z;
+            if (mis) {
+                lg[pos + 1] = (uint32_t)(g + 1);
+                lz[pos + 1] = z;
+            }
+        }
+        nlive += __popc(bal) * per;
+    }
+    __syncwarp();
+    return nlive;
+}
+
+// Draws the listed groups [base, base + n), n <= 64, two per lane, and updates thr
+// to the warp's best afterwards.  Entries outside [0, V) are skipped.
+template <int ESZ>
+__device__ __forceinline__ void item_round(const uint32_t *lg, const float *lz, int base, int n,
+                                           const JobDesc &jd, const char *jrow, const char *drow,
+                                           const VerifyParams &p, uint32_t b, float &thr, float &best, int &bidx) {
+    const int lane = threadIdx.x & 31;
+    const bool resid = jd.kind == JOB_RESID;
+    const uint32_t purpose = resid ? PURPOSE_RESIDUAL : PURPOSE_BONUS;
+    int gk[2];
+    float zm[2];
+    bool has[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int item = lane + 32 * h;
+        has[h] = item < n;
+        const int e = base + (has[h] ? item : 0);
+        gk[h] = (int)lg[e];
+        zm[h] = lz[e];
+    }
+    uint4 r4[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) r4[h] = rand_group(p.seed, p.step, b, (uint32_t)jd.row, purpose, (uint32_t)gk[h]);
+    uint32_t sv = 0;  // bit 4h + q: entry q of group h passed the per-entry test
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        // any survivor needs 1 - u_k <= e^(z_k - thr) <= e^(zmax - thr); the largest
+        // w >> 9 of the group gives the smallest 1 - u
+        const uint32_t kmax = max(max(r4[h].x >> 9, r4[h].y >> 9), max(r4[h].z >> 9, r4[h].w >> 9));
+        if (has[h] && one_minus_u01(kmax << 9) <= ex2_approx((zm[h] - thr) * kLog2e) * 1.001f) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int v = 4 * gk[h] + q;
+                if (v < 0 || v >= p.V) continue;
+                const float z = fmaf(ld_elem<ESZ>(jrow, v), jd.invT, -jd.shift);
+                if (z > kNegInf && one_minus_u01(word_of(r4[h], q)) <= ex2_approx((z - thr) * kLog2e) * 1.001f)
+                    sv |= 1u << (4 * h + q);
+            }
+        }
+    }
+    // exact scores of the survivors, one entry at a time (rare: few registers)
+    while (sv) {
+        const int k = __ffs(sv) - 1;
+        sv &= sv - 1;
+        const int h = k >> 2, q = k & 3;
+        const int v = 4 * (h ? gk[1] : gk[0]) + q;
+        const uint32_t wd = word_of(h ? r4[1] : r4[0], q);
+        const float z = fmaf(ld_elem<ESZ>(jrow, v), jd.invT, -jd.shift);
+        float sc;
+        if (resid) {
+            // -inf (no residual mass at v) is never a candidate: a row without any
+            // must reach the degenerate fallback
+            const float zq = fmaf(ld_elem<ESZ>(drow, v), jd.invT, -jd.Cd);
+            sc = zq < z ? resid_score(z, zq, wd) : kNegInf;
+        } else {
+            sc = z + gumbel_of_word(wd);
+        }
+        if (sc > kNegInf && better(sc, v, best, bidx)) { best = sc; bidx = v; }
+    }
+    thr = fmaxf(thr, warp_max(best));
+    __syncwarp();  // the items drawn here are overwritten by the next appends
+}
+
+// One slice of a Gumbel-max job: share the bound with the request's other items
+// (each publishes the best exact score it knows and reads theirs one slice ahead of
+// using it; every published value is the exact score of an entry, so the pruning
+// stays exact), list the live groups, draw every full 64.
+template <bool CHECK_RAW, class Vec>
+__device__ __forceinline__ void item_slice(const Vec (&d)[kSV], int t0, int ebase, const JobDesc &jd,
+                                           const char *jrow, const char *drow, const VerifyParams &p, uint32_t b,
+                                           unsigned long long *sy, unsigned long long &shared_bits,
+                                           float &published, float &thr,
+                                           SliceRes &mine, uint32_t *lg, float *lz, int &nlive) {
+    const int lane = threadIdx.x & 31;
+    thr = fmaxf(thr, bound_of(shared_bits, p.epoch));
+    shared_bits = ld_relaxed_u64(sy + kSyncBest);
+    if (lane == 0 && thr > published) {
+        publish_bound(sy + kSyncBest, p.epoch, thr);
+        published = thr;
+    }
+#pragma unroll
+    for (int t = 0; t < kSV; ++t) {
+        nlive = item_filter<CHECK_RAW>(d[t], t0 + t, ebase, (ebase & 3) != 0, thr - kGumbelMax, jd.invT, jd.shift,
+                                       mine.rawmax, lg, lz, nlive);
+        while (nlive >= 64) {  // draw the newest 64; the rest stay listed
+            nlive -= 64;
+            item_round<Vec::ESIZE>(lg, lz, nlive, 64, jd, jrow, drow, p, b, thr, mine.best, mine.idx);
+        }
+    }
+}
+
+// One slice of an argmax job: the lowest index of the largest value, every raw
+// value folded into rawmax.  Entry e of vector t of thread ct is element
+// ebase + (ct + kCT (t0 + t)) VE + e.
+template <class Vec>
+__device__ __forceinline__ void item_argmax_slice(const Vec (&d)[kSV], int t0, int ebase, SliceRes &mine) {
+    float vm[kSV];
+    float tm = kNegInf;
+#pragma unroll
+    for (int t = 0; t < kSV; ++t) {
+        vm[t] = d[t].vmax();
+        tm = max_nan_f32(tm, vm[t]);
+    }
+    const float M = warp_max_nan(tm);
+    mine.rawmax = max_nan_f32(mine.rawmax, M);
+    if (!(M > kNegInf)) return;  // all -inf (or NaN): no argmax here
+#pragma unroll
+    for (int t = 0; t < kSV; ++t) {
+        const unsigned bal = __ballot_sync(0xffffffffu, vm[t] == M);
+        if (bal) {
+            int e = Vec::VE;
+#pragma unroll
+            for (int q = Vec::VE - 1; q >= 0; --q)
+                if (d[t].get(q) == M) e = q;
+            const int mine_idx = ebase + ((int)threadIdx.x + kCT * (t0 + t)) * Vec::VE + e;
+            const int idx = __shfl_sync(0xffffffffu, mine_idx, __ffs(bal) - 1);
+            if (better(M, idx, mine.best, mine.idx)) {
+                mine.best = M;
+                mine.idx = idx;
+            }
+            return;
+        }
+    }
+}
+
+// Loads this thread's vectors t0 .. t0+kSV-1 of a chunk (vector t of thread ct is
+// window vector ct + kCT t); entries outside the chunk read as -inf.
+template <class Vec>
+__device__ __forceinline__ void load_slice(Vec (&d)[kSV], const ChunkDesc &cd, int t0, int ct) {
+    const int nvec = (int)(cd.bytes >> 4);
+    const int64_t ebase = (int64_t)cd.e0 - cd.shift;
+#pragma unroll
+    for (int t = 0; t < kSV; ++t) {
+        const int j = ct + kCT * (t0 + t);
+        d[t] = j < nvec ? Vec::load(cd.a0, j) : Vec::neg_inf();
+        if (j < nvec && (j == 0 || j == nvec - 1)) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, cd.e0, cd.e1);
+    }
+}
+
+template <class Vec>
+__device__ __forceinline__ void commit_item(const VerifyParams &p, const int *s_rs, int item, ItemShared &sh) {
+    // the item's buffers, sized for the largest Kmax (fixed addresses: no registers)
+    // live groups and their largest z (the draw), or the request's partials (the decide)
+    __shared__ __align__(16) unsigned char s_buf[kCW * kItemLive * 8];
+    constexpr int kStageParts = kCW * kItemLive * 8 / (int)sizeof(Part);
+    __shared__ PosRes s_pos[SPEC_MAX_DRAFTS];
+    __shared__ RowRes s_rows[2 * SPEC_MAX_DRAFTS];  // target rows, then draft rows
+    __shared__ float s_xt[SPEC_MAX_DRAFTS], s_xd[SPEC_MAX_DRAFTS];  // target and draft logit at x_i
+    __shared__ float s_l2u[SPEC_MAX_DRAFTS];   // log2 of the acceptance uniform u_i
+    __shared__ float s_pp[SPEC_MAX_DRAFTS], s_qq[SPEC_MAX_DRAFTS];  // p(x_i), q(x_i)
+    __shared__ uint16_t s_cand[kCandPrefetch];  // seed-candidate pointers of the target rows
+    constexpr int ESZ = Vec::ESIZE;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = item / p.Q, q = item - b * p.Q;
+    unsigned long long *sy = p.sync + (size_t)b * kSyncWords;
+
+    // ---- the request's inputs
+    const ReqBase rbase = req_base(p.cu, p.num_draft, p.Kmax, b);
+    const int kb_raw = rbase.kb;
+    int status = SPEC_STATUS_OK;
+    float T = 0.f;
+    if (kb_raw < 0 || kb_raw > p.Kmax) status = SPEC_STATUS_BAD_K;
+    if (status == SPEC_STATUS_OK && p.temperature) {
+        T = p.temperature[b];
+        if (!(T >= 0.f) || isinf(T)) status = SPEC_STATUS_BAD_TEMPERATURE;
+    }
+    const int kb = status == SPEC_STATUS_BAD_K ? 0 : kb_raw;
+    const bool greedy = (T == 0.f);
+    const int32_t *x = p.draft_tokens + rbase.d0;
+    if (status == SPEC_STATUS_OK) {
+        bool bad = false;
+        for (int i = tid; i < kb; i += kCT) bad |= (x[i] < 0 || x[i] >= p.V);
+        if (__syncthreads_or(bad)) status = SPEC_STATUS_BAD_TOKEN;
+    }
+    const float c = greedy ? 0.f : __fdiv_rn(kLog2e, T);
+    const float invT = greedy ? 0.f : __fdiv_rn(1.f, T);
+    const int npos = status == SPEC_STATUS_OK ? kb : 0;
+    if (!greedy) {
+        for (int i = tid; i < npos; i += kCT) {
+            const int xi = x[i];
+            s_xt[i] = load_logit(p.target, p.dtype, (rbase.t0 + i) * p.ld_row + xi);
+            s_xd[i] = load_logit(p.draft, p.dtype, (rbase.d0 + i) * p.ld_row + xi);
+            const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)i, PURPOSE_ACCEPT, 0u);
+            s_l2u[i] = log2f(u01(r4.x));
+        }
+    }
+    // ---- wait until the main pass has stored every partial of the request's rows
+    const int r0 = s_rs[b];
+    const int nparts = (s_rs[b + 1] - r0) * p.cpr;
+    Part *stage = (Part *)s_buf;
+    const bool counted = wait_parts(p.parts + (int64_t)r0 * p.cpr, nparts, p.epoch, &sh.flag, stage, kStageParts);
+    const bool staged = nparts <= kStageParts;
+    const int nrows = greedy ? npos : 2 * npos;  // flat rows r0 .. r0 + nrows - 1
+    const int ncand = p.cpr * kCW;
+    const bool cand_pre = !greedy && counted && npos * ncand <= kCandPrefetch;
+    if (cand_pre)
+        for (int it = tid; it < npos * ncand; it += kCT) s_cand[it] = __ldcg(p.cand + (size_t)r0 * ncand + it);
+
+    // ---- the decision: one thread per row, then one thread per position
+    bool stale = false;
+    if (counted)
+        for (int r = tid; r < nrows; r += kCT)
+            s_rows[r] = staged ? row_from_parts_tagged<true>(stage + (int64_t)r * p.cpr, p.cpr, c, greedy && r < npos,
+                                                      p.epoch, stale)
+                               : row_from_parts_tagged<false>(p.parts + (int64_t)(r0 + r) * p.cpr, p.cpr, c,
+                                                       greedy && r < npos, p.epoch, stale);
+    stale = __syncthreads_or(stale);
+    if (counted) {
+        for (int i = tid; i < npos; i += kCT) {
+            const RowRes tr = s_rows[i];
+            PosRes pr;
+            pr.tidx = tr.idx;
+            pr.shift = pr.Cd = 0.f;
+            pr.seed = kNegInf;
+            pr.seed_idx = -1;
+            pr.pad = 0.f;
+            if (greedy) {
+                pr.nonfinite = !(fabsf(tr.M) < __int_as_float(0x7f800000));
+                pr.rej = tr.idx != x[i];
+            } else {
+                const RowRes dr = s_rows[npos + i];
+                // a NaN leaves its chunk's max NaN; +inf makes the sum NaN: both show here
+                pr.nonfinite = !(fabsf(tr.M) < __int_as_float(0x7f800000) &&
+                                 fabsf(dr.M) < __int_as_float(0x7f800000) &&
+                                 fabsf(tr.l2S) < __int_as_float(0x7f800000) &&
+                                 fabsf(dr.l2S) < __int_as_float(0x7f800000));
+                const float l2p = fmaf(s_xt[i], c, -__fmul_rn(tr.M, c)) - tr.l2S;  // log2 p_i(x_i)
+                const float l2q = fmaf(s_xd[i], c, -__fmul_rn(dr.M, c)) - dr.l2S;  // log2 q_i(x_i)
+                // accept iff u q < p, i.e. log2 u < log2 p - log2 q (Q = 0 < P accepts; P = 0 rejects)
+                pr.rej = !(s_l2u[i] < l2p - l2q);
+                // log p_v = x_v / T - (fl(M c) + log2 S) ln 2, and q likewise
+                pr.shift = (__fmul_rn(tr.M, c) + tr.l2S) * 0.6931471805599453f;
+                pr.Cd = (__fmul_rn(dr.M, c) + dr.l2S) * 0.6931471805599453f;
+                s_pp[i] = exp2f(l2p);
+                s_qq[i] = exp2f(l2q);
+            }
+            s_pos[i] = pr;
+        }
+    }
+    __syncthreads();
+
+    // ---- the scan (warp 0): A = first rejected position, and the job
+    if (warp == 0) {
+        JobDesc jd;
+        jd.kind = JOB_NONE;
+        jd.row = 0;
+        jd.A = 0;
+        jd.token = -1;
+        jd.invT = invT;
+        jd.shift = jd.Cd = 0.f;
+        jd.seed = kNegInf;
+        jd.seed_idx = -1;
+        jd.epoch = p.epoch;
+        int st = status;
+        if (st == SPEC_STATUS_OK && (!counted || stale)) st = SPEC_STATUS_INTERNAL;
+        if (st == SPEC_STATUS_OK) {
+            bool nf = false;
+            for (int i = lane; i < kb; i += 32) nf |= s_pos[i].nonfinite != 0;
+            if (__any_sync(0xffffffffu, nf)) st = SPEC_STATUS_NONFINITE;
+        }
+        if (st == SPEC_STATUS_OK) {
+            int A = kb;
+            for (int i0 = 0; i0 < kb && A == kb; i0 += 32) {
+                const int i = i0 + lane;
+                const unsigned msk = __ballot_sync(0xffffffffu, i < kb && s_pos[i].rej != 0);
+                if (msk) A = i0 + __ffs(msk) - 1;
+            }
+            jd.A = A;
+            if (greedy) {
+                if (A < kb) {
+                    jd.token = s_pos[A].tidx;
+                } else {
+                    jd.kind = JOB_ARGMAX;
+                    jd.row = kb;
+                }
+            } else if (A < kb) {
+                const PosRes pr = s_pos[A];
+                jd.kind = JOB_RESID;
+                jd.row = A;
+                jd.shift = pr.shift;
+                jd.Cd = pr.Cd;
+            } else {
+                jd.kind = JOB_BONUS;
+                jd.row = kb;
+            }
+        }
+        jd.status = st;
+        if (lane == 0) sh.job = jd;
+    }
+    if (tid == 0) {
+        sh.rb = rbase;
+        sh.kb = kb;
+        sh.greedy = greedy;
+    }
+    __syncthreads();
+    const JobDesc &jd = sh.job;  // read where used: fewer live registers
+    status = jd.status;
+
+    int token = jd.token;
+    if (jd.kind != JOB_NONE) {
+        const int64_t rowbytes = p.ld_row * ESZ;
+        const char *jrow = (const char *)p.target + (sh.rb.t0 + jd.row) * rowbytes;
+        const char *drow = jd.kind == JOB_RESID ? (const char *)p.draft + (sh.rb.d0 + jd.row) * rowbytes : nullptr;
+        const Chunking ck = {p.cpr, p.ce};
+        // the first slice's loads go out before the seeds are scored
+        constexpr int kSlices = kVPT / kSV;  // a chunk is kSlices slices of kSV vectors a thread
+        Vec cur[kSV], nxt[kSV];
+        int k = q, sl = 0, eb_cur = 0;
+        if (k < p.cpr) {
+            const ChunkDesc cd = job_chunk(jrow, ESZ, p.V, ck, k);
+            eb_cur = cd.e0 - cd.shift;
+            load_slice(cur, cd, 0, tid);
+        }
+        SliceRes mine;
+        mine.best = kNegInf;
+        mine.idx = -1;
+        mine.rawmax = kNegInf;
+        mine.failed = 0;
+        float thr = kNegInf;
+        if (jd.kind == JOB_RESID) {
+            // seeds: the main pass's candidates of row A (the vector holding each
+            // warp's maximum of each chunk), exact scores; the best is shared
+            constexpr int VE = 16 / ESZ;
+            SliceRes sd;
+            sd.best = kNegInf;
+            sd.idx = -1;
+            sd.rawmax = kNegInf;
+            sd.failed = 0;
+            for (int j = tid; j < ncand; j += kCT) {
+                const uint32_t cv = cand_pre ? s_cand[jd.row * ncand + j]
+                                             : __ldcg(p.cand + ((size_t)r0 + jd.row) * ncand + j);
+                const ChunkWin w = chunk_window(jrow, ESZ, p.V, ck, j / kCW);
+                if (cv == 0xffffu || (cv + 1) * 16 > w.bytes) continue;
+                const int eb = w.e0 - w.shift + (int)cv * VE;
+                // the target vector and the draft logits of its entries, loaded together
+                const uint4 raw = ld_stream_v4(w.a0 + 16 * (size_t)cv);
+                float lq[VE];
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const int v = eb + e;
+                    lq[e] = (v >= w.e0 && v < w.e1) ? ld_elem<ESZ>(drow, v) : 0.f;
+                }
+                float bx = kNegInf, bq = 0.f;
+                int bvi = -1;
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const int v = eb + e;
+                    const float xv = ESZ == 2 ? VecBF16{raw}.get(e) : VecF32{raw}.get(e);
+                    if (v >= w.e0 && v < w.e1 && xv > bx) { bx = xv; bvi = v; bq = lq[e]; }
+                }
+                if (bvi < 0) continue;
+                const float z = fmaf(bx, jd.invT, -jd.shift);
+                const float zq = fmaf(bq, jd.invT, -jd.Cd);
+                if (!(zq < z)) continue;  // no residual mass at bvi
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
+                                            (uint32_t)bvi >> 2);
+                const float s = resid_score(z, zq, word_of(r4, bvi & 3));
+                if (better(s, bvi, sd.best, sd.idx)) { sd.best = s; sd.idx = bvi; }
+            }
+            sd = block_reduce_n(sd, sh.red, kCW);
+            mine.best = sd.best;
+            mine.idx = sd.idx;
+            thr = sd.best;
+            if (tid == 0 && sd.best > kNegInf) publish_bound(sy + kSyncBest, p.epoch, sd.best);
+        }
+        uint32_t *lg = (uint32_t *)s_buf + warp * kItemLive;
+        float *lz = (float *)(s_buf + kCW * kItemLive * 4) + warp * kItemLive;
+        int nlive = 0;
+        float published = thr;
+        unsigned long long shared_bits = ld_relaxed_u64(sy + kSyncBest);
+        bool first = true;
+        while (k < p.cpr) {
+            // the next slice: the rest of this chunk, then chunk k + Q
+            int k2 = k, sl2 = sl + 1;
+            if (sl2 == kSlices) {
+                sl2 = 0;
+                k2 = k + p.Q;
+            }
+            const bool more = k2 < p.cpr;
+            int eb_next = eb_cur;
+            if (more) {
+                const ChunkDesc nd = job_chunk(jrow, ESZ, p.V, ck, k2);
+                eb_next = nd.e0 - nd.shift;
+                load_slice(nxt, nd, sl2 * kSV, tid);
+            }
+            if (jd.kind == JOB_ARGMAX) {
+                item_argmax_slice(cur, sl * kSV, eb_cur, mine);
+            } else {
+                if (jd.kind == JOB_BONUS && first) {
+                    // bonus seed: the exact score of each lane's largest entry of the
+                    // first slice; the warp's best bounds its draws from below
+                    float m = kNegInf;
+                    int mi = -1;
+#pragma unroll
+                    for (int t = 0; t < kSV; ++t)
+#pragma unroll
+                        for (int e = 0; e < Vec::VE; ++e) {
+                            const float xv = cur[t].get(e);
+                            if (xv > m) { m = xv; mi = eb_cur + (tid + kCT * t) * Vec::VE + e; }
+                        }
+                    if (mi >= 0) {
+                        const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_BONUS,
+                                                    (uint32_t)mi >> 2);
+                        const float s = fmaf(m, jd.invT, -jd.shift) + gumbel_of_word(word_of(r4, mi & 3));
+                        if (better(s, mi, mine.best, mine.idx)) { mine.best = s; mine.idx = mi; }
+                    }
+                    thr = warp_max(mine.best);
+                }
+                first = false;
+                if (jd.kind == JOB_RESID)
+                    item_slice<false>(cur, sl * kSV, eb_cur, jd, jrow, drow, p, (uint32_t)b, sy, shared_bits,
+                                      published, thr, mine, lg, lz, nlive);
+                else
+                    item_slice<true>(cur, sl * kSV, eb_cur, jd, jrow, drow, p, (uint32_t)b, sy, shared_bits,
+                                     published, thr, mine, lg, lz, nlive);
+            }
+#pragma unroll
+            for (int t = 0; t < kSV; ++t) cur[t] = nxt[t];
+            k = k2;
+            sl = sl2;
+            eb_cur = eb_next;
+        }
+        if (jd.kind != JOB_ARGMAX && nlive > 0)
+            item_round<ESZ>(lg, lz, 0, nlive, jd, jrow, drow, p, (uint32_t)b, thr, mine.best, mine.idx);
+        const SliceRes res = block_reduce_n(mine, sh.red, kCW);
+
+        // ---- the items meet: the last to finish combines them
+        if (tid == 0) {
+            PieceRes pr;
+            pr.best = res.best;
+            pr.idx = res.idx;
+            pr.rawmax = res.rawmax;
+            pr.tag = p.epoch;
+            p.pres[(int64_t)b * p.Q + q] = pr;
+            __threadfence();
+            sh.last = arrive(sy + kSyncDone, p.epoch) == (uint32_t)p.Q;
+        }
+        __syncthreads();
+        if (!sh.last) return;
+        __threadfence();
+        SliceRes o;
+        o.best = kNegInf;
+        o.idx = -1;
+        o.rawmax = kNegInf;
+        o.failed = 0;
+        for (int i = tid; i < p.Q; i += kCT) {
+            const uint4 w4 = __ldcg((const uint4 *)(p.pres + (int64_t)b * p.Q + i));
+            if (better(__uint_as_float(w4.x), (int)w4.y, o.best, o.idx)) {
+                o.best = __uint_as_float(w4.x);
+                o.idx = (int)w4.y;
+            }
+            o.rawmax = max_nan_f32(o.rawmax, __uint_as_float(w4.z));
+            o.failed |= w4.w != p.epoch;
+        }
+        o = block_reduce_n(o, sh.red, kCW);
+        if (status == SPEC_STATUS_OK) {
+            if (o.failed) status = SPEC_STATUS_INTERNAL;
+            else if (jd.kind != JOB_RESID && !(fabsf(o.rawmax) < __int_as_float(0x7f800000)))
+                status = SPEC_STATUS_NONFINITE;
+        }
+        token = o.idx;
+        if (status == SPEC_STATUS_OK && jd.kind == JOB_RESID && o.idx < 0) {
+            // p <= q everywhere (only by rounding): draw from p_j with the same noise
+            const int64_t trow = (sh.rb.t0 + jd.row) * p.ld_row;
+            SliceRes f;
+            f.best = kNegInf;
+            f.idx = -1;
+            f.rawmax = kNegInf;
+            f.failed = 0;
+            for (int v = tid; v < p.V; v += kCT) {
+                const float lp = fmaf(load_logit(p.target, p.dtype, trow + v), jd.invT, -jd.shift);
+                if (!(lp > kNegInf)) continue;
+                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)jd.row, PURPOSE_RESIDUAL,
+                                            (uint32_t)v >> 2);
+                const float s = lp + gumbel_of_word(word_of(r4, v & 3));
+                if (better(s, v, f.best, f.idx)) { f.best = s; f.idx = v; }
+            }
+            token = block_reduce_n(f, sh.red, kCW).idx;
+        }
+    } else {
+        // no row left to reduce: the items only meet
+        if (tid == 0) {
+            __threadfence();
+            sh.last = arrive(sy + kSyncDone, p.epoch) == (uint32_t)p.Q;
+        }
+        __syncthreads();
+        if (!sh.last) return;
+    }
+
+    // ---- outputs of request b (the last item)
+    const ReqBase ob = sh.rb;
+    const int okb = sh.kb;
+    const int32_t *ox = p.draft_tokens + ob.d0;
+    const bool okst = status == SPEC_STATUS_OK;
+    const int A = okst ? jd.A : 0;
+    int32_t *tok = p.out_tokens + ob.t0;
+    for (int i = tid; i < ob.ntok; i += kCT) tok[i] = !okst ? -1 : (i < A ? ox[i] : (i == A ? token : -1));
+    const bool pq = okst && !sh.greedy;
+    if (p.out_p)
+        for (int i = tid; i < ob.npq; i += kCT) p.out_p[ob.d0 + i] = pq && i < okb ? s_pp[i] : -1.f;
+    if (p.out_q)
+        for (int i = tid; i < ob.npq; i += kCT) p.out_q[ob.d0 + i] = pq && i < okb ? s_qq[i] : -1.f;
+    if (tid == 0) {
+        p.out_status[b] = status;
+        p.out_accepted[b] = A;
+    }
+}
+
+// One persistent kernel, kMainBlocksPerSM CTAs of kCT threads per SM.
+//  Main pass: every row of every draft position read once -- target and draft rows
+//  of sampling requests, target rows of greedy ones -- in chunks of at most 64 KB
+//  taken by tickets.  A CTA keeps a chunk's kVPT 16-byte vectors per thread
+//  in two halves and reloads a half with the next chunk's as soon as it has reduced
+//  it, so its loads never stop for the reductions, the barrier and the CTA-level
+//  combine that end each chunk.  Per chunk: warp maxima and exp-sums (greedy rows:
+//  warp maxima and their lowest indices), combined by warp 0 into one Part stored at
+//  the chunk's index; on sampling rows each warp also leaves a pointer to the vector
+//  holding its maximum, the correction draw's seed candidates.
+//  Commit: when the chunk tickets run out, the CTA takes commit items by tickets
+//  until none are left (commit_item).
+template <class Vec>
+__global__ void __launch_bounds__(kCT, kMainBlocksPerSM) verify_kernel(VerifyParams p) {
+    constexpr int kH = kVPT / 2;  // vectors per half
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ WarpStat s_ws[2][kCW];
+    __shared__ ChunkDesc s_desc[3];
+    __shared__ uint32_t s_item[2];
+    __shared__ ItemShared s_sh;
+    int *s_rs = (int *)smem;  // [B+1] first main-pass row of each request
+    float *s_c = (float *)(smem + align16(sizeof(int) * (size_t)(p.B + 1)));  // [B] log2(e) / T (0: greedy)
+    scan_request_rows(s_rs, p.B, p.cu, p.num_draft, p.temperature, p.Kmax);  // ends with __syncthreads
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+        const float T = p.temperature ? p.temperature[i] : 0.f;
+        s_c[i] = (T > 0.f && !isinf(T)) ? __fdiv_rn(kLog2e, T) : 0.f;
+    }
+    __syncthreads();
+
+    const Chunking ck = {p.cpr, p.ce};
+    const uint32_t total = (uint32_t)s_rs[p.B] * (uint32_t)ck.cpr;  // < 2^31 (checked by the host)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ct = threadIdx.x;
+    if (threadIdx.x == 0) {
+        const uint32_t t0 = atomicAdd(p.counters + kCntChunk, 2u);
+        s_desc[0] = chunk_desc<Vec>(p, s_rs, s_c, ck, t0, total);
+        s_desc[1] = chunk_desc<Vec>(p, s_rs, s_c, ck, t0 + 1u, total);
+    }
+    __syncthreads();
+    // the current chunk's index, scale and first window element stay in registers;
+    // the next chunk's window is read from shared memory where it is used
+    uint32_t t = s_desc[0].t;
+    float c = s_desc[0].c;
+    int ebase = s_desc[0].e0 - s_desc[0].shift;
+    Vec a[kH], bv[kH];
+    if (t < total) {
+        load_half<0>(a, s_desc[0], ct);
+        load_half<kH>(bv, s_desc[0], ct);
+    }
+    int n = 0;
+    while (t < total) {
+        if (threadIdx.x == 0)
+            s_desc[(n + 2) % 3] = chunk_desc<Vec>(p, s_rs, s_c, ck, atomicAdd(p.counters + kCntChunk, 1u), total);
+        const ChunkDesc &nx = s_desc[(n + 1) % 3];
+        float m = kNegInf, mc = 0.f, s = 0.f;
+        int mv = -1;
+        float vma[kH], vmb[kH];
+        const float ta = half_stats<0>(a, vma, c, m, mc, s, mv);
+        int ia = -1;
+        float Ma = kNegInf;
+        if (c == 0.f) {
+            Ma = warp_max_nan(ta);
+            ia = warp_first_index<0>(a, vma, Ma, ebase, ct);
+        }
+        if (nx.t < total) load_half<0>(a, nx, ct);
+        const float tb = half_stats<kH>(bv, vmb, c, m, mc, s, mv);
+        WarpStat ws;
+        ws.pad = 0;
+        if (c != 0.f) {
+            // the lanes' sums, each relative to its own fl(m c), rescaled to the warp's
+            const float M = warp_max_nan(m);
+            const float sc = (m == kNegInf || s == 0.f) ? 0.f : s * ex2_approx(mc - __fmul_rn(M, c));
+            ws.m = M;
+            ws.s = warp_sum(sc);
+            ws.idx = -1;
+            // the window vector of the lowest lane that holds the warp maximum
+            const unsigned own = __ballot_sync(0xffffffffu, m == M && mv >= 0);
+            const int src = own ? __ffs(own) - 1 : 0;
+            const int vec = __shfl_sync(0xffffffffu, mv, src);
+            if (lane == 0)
+                p.cand[(size_t)t * kCW + warp] = own ? (uint16_t)(warp * 32 + src + kCT * vec) : (uint16_t)0xffffu;
+        } else {
+            // entries of half a precede those of half b: a's index wins a tie
+            const float Mb = warp_max_nan(tb);
+            const int ib = warp_first_index<kH>(bv, vmb, Mb, ebase, ct);
+            ws.m = max_nan_f32(Ma, Mb);
+            ws.s = 0.f;
+            ws.idx = (Ma >= Mb) ? ia : ib;
+        }
+        if (nx.t < total) load_half<kH>(bv, nx, ct);
+        if (lane == 0) s_ws[n & 1][warp] = ws;
+        __syncthreads();
+        if (warp == 0) {
+            // the CTA's warps combined: max, sum relative to fl(max c), lowest argmax
+            const WarpStat q = lane < kCW ? s_ws[n & 1][lane] : WarpStat{kNegInf, 0.f, -1, 0};
+            const float Mc = warp_max_nan(q.m);
+            Part out;
+            out.m = Mc;
+            float tl = 0.f;
+            if (c != 0.f) tl = (q.m == kNegInf || q.s == 0.f) ? 0.f : q.s * exp2f(__fmul_rn(q.m, c) - __fmul_rn(Mc, c));
+            out.s = warp_sum(tl);
+            uint32_t v = (q.m == Mc && q.idx >= 0) ? (uint32_t)q.idx : 0xffffffffu;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+            out.idx = (int)v;
+            out.epoch = p.epoch;
+            if (lane == 0) p.parts[t] = out;  // one 16-byte store: the tag and the values arrive together
+        }
+        ++n;
+        t = nx.t;
+        c = nx.c;
+        ebase = nx.e0 - nx.shift;
+    }
+
+    // ---- commit items
+    const uint32_t nitems = (uint32_t)p.B * (uint32_t)p.Q;
+    for (int it = 0;; ++it) {
+        if (threadIdx.x == 0) s_item[it & 1] = atomicAdd(p.counters + kCntItem, 1u);
+        __syncthreads();
+        const uint32_t item = s_item[it & 1];
+        if (item >= nitems) break;
+        commit_item<Vec>(p, s_rs, (int)item, s_sh);
+    }
+}
+
+
+}  // namespace fused
+
 // =================================================================== early_exit_kernel
 // Early-exit verify ("Accelerating Large-Model Inference ... DSpark", Sec. 1: the
 // longest accepted prefix is committed plus one token, so no row after the first
@@ -2253,6 +3069,34 @@ int launch_early_exit(int dev, const Layout &L, const CommitParams &cp, cudaStre
     return SPEC_OK;
 }
 
+// Dynamic shared memory of the fused verify kernel: the row scan and the scales.
+size_t fused_smem(int B) { return fused::align16(sizeof(int) * (size_t)(B + 1)) + sizeof(float) * (size_t)B; }
+
+template <class Vec>
+int launch_fused(int dev, int sms, const fused::VerifyParams &vp, size_t zero_bytes, cudaStream_t st) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const int which = Vec::ESIZE == 2 ? 0 : 1;
+        static bool set[64][2];
+        if (!set[dev][which]) {
+            // the largest B; no carveout preference: the main loop's loads in flight need L1
+            const cudaError_t e = cudaFuncSetAttribute(fused::verify_kernel<Vec>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)fused_smem(SPEC_MAX_BATCH));
+            if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
+            set[dev][which] = true;
+        }
+    }
+    // the ticket counters and the requests' lines start at zero whatever the workspace held
+    const cudaError_t e = cudaMemsetAsync(vp.counters, 0, zero_bytes, st);
+    if (e != cudaSuccess) { t_last_cuda_error = (int)e; return SPEC_ECUDA; }
+    {
+        ProfScope ps(st);
+        fused::verify_kernel<Vec><<<kMainBlocksPerSM * sms, kCT, fused_smem(vp.B), st>>>(vp);
+    }
+    return check_launch();
+}
+
 template <class Vec>
 int launch_all(int dev, int sms, const Layout &L, const MainParams &mp, const JobParams &jp, cudaStream_t st) {
     int rc;
@@ -2314,6 +3158,45 @@ int verify_impl(const void *target, const void *draft, int dtype, int B, int Kma
     char *w = (char *)ws;
     const float *temps = sample ? temperature : nullptr;
     const uint32_t epoch = next_epoch();
+
+    if (B >= sms && L.cpr <= L.P) {
+        // one request or more per SM: the fused kernel (its items' results fit the
+        // pieces' array: Q <= cpr <= P)
+        fused::VerifyParams vp;
+        vp.target = target;
+        vp.draft = draft;
+        vp.dtype = dtype;
+        vp.ld_row = ld_row;
+        vp.B = B;
+        vp.Kmax = Kmax;
+        vp.V = V;
+        vp.draft_tokens = draft_tokens;
+        vp.cu = cu;
+        vp.num_draft = num_draft;
+        vp.temperature = temps;
+        vp.seed = seed;
+        vp.step = (uint32_t)step;
+        vp.epoch = epoch;
+        vp.cpr = L.cpr;
+        vp.ce = make_chunking(V, esz).ce;
+        const int G = kMainBlocksPerSM * sms;
+        vp.Q = G / B < 1 ? 1 : (G / B > L.cpr ? L.cpr : G / B);
+        vp.counters = (uint32_t *)(w + L.off_ticket);
+        vp.sync = (unsigned long long *)(w + L.off_sync);
+        vp.parts = (Part *)(w + L.off_parts);
+        vp.cand = (uint16_t *)(w + L.off_cand);
+        vp.pres = (PieceRes *)(w + L.off_pres);
+        vp.out_tokens = out_tokens;
+        vp.out_accepted = out_accepted;
+        vp.out_p = sample ? out_p : nullptr;
+        vp.out_q = sample ? out_q : nullptr;
+        vp.out_status = out_status;
+        cudaStream_t st = (cudaStream_t)cuda_stream;
+        // one memset: the counters, row_start (unused here) and the requests' lines
+        const size_t zb = L.off_sync + sizeof(uint32_t) * kSyncWords * (size_t)B;
+        return dtype == SPEC_BF16 ? launch_fused<VecBF16>(dev, sms, vp, zb, st)
+                                  : launch_fused<VecF32>(dev, sms, vp, zb, st);
+    }
 
     MainParams mp;
     mp.target = target;

@@ -1,10 +1,13 @@
 """The verify calls' contract with their caller, on the GPU and through the C ABI:
 pointers must be on the current device, and a workspace must start with its ticket
-counter at zero.  A counter that is not zero (a workspace that was not zero-filled)
-makes the main pass skip chunks; the commit pass then finds partials carrying
-another call's tag and reports status 5 for those requests (nothing hangs: no wait
-depends on the skipped work), and leaves the counter zero, so the next call on the
-same workspace is correct."""
+counter at zero.  Batches of fewer requests than SMs run main_kernel + commit_kernel:
+there a counter that is not zero (a workspace that was not zero-filled) makes the
+main pass skip chunks; the commit pass then finds partials carrying another call's
+tag and reports status 5 for those requests (nothing hangs: no wait depends on the
+skipped work), and leaves the counter zero, so the next call on the same workspace
+is correct.  Larger batches run the single persistent kernel, whose counters and
+per-request lines are zeroed in stream order before every launch: any workspace
+contents serve, and one workspace may alternate between the two paths."""
 import ctypes
 
 import numpy as np
@@ -78,3 +81,53 @@ def test_workspace_with_a_nonzero_ticket_counter_reports_status_5_then_recovers(
            "status": outs["st"].cpu().numpy(), "p": outs["p"].cpu().numpy(), "q": outs["q"].cpu().numpy()}
     ref = run_oracle_sample(batch, 3, 1)
     compare_sample(gpu, ref, batch["temperature"].numpy())
+
+
+def _outs_np(outs):
+    return {"tokens": outs["tok"].cpu().numpy(), "accepted": outs["acc"].cpu().numpy(),
+            "status": outs["st"].cpu().numpy(), "p": outs["p"].cpu().numpy(), "q": outs["q"].cpu().numpy()}
+
+
+def _sized(B, K, V, seed):
+    batch = synth.make_batch(B, K, V, torch.bfloat16, seed, noise_sigmas=(0.3, 1.0), temperature=(0.6, 1.4),
+                             greedy_mask=[b % 7 == 3 for b in range(B)])
+    return batch, to_dev(batch)
+
+
+def test_single_kernel_path_ignores_what_the_workspace_held():
+    """B = 320 (at least one request per SM): a workspace of 0xA5 bytes, then one
+    of 0xFF bytes; both calls equal the oracle."""
+    from speculative_decoding_verification_15_gb300 import binding
+
+    lib = binding.load()
+    B, K, V = 320, 3, 5000
+    assert B >= torch.cuda.get_device_properties(0).multi_processor_count
+    batch, d = _sized(B, K, V, 3201)
+    ref = run_oracle_sample(batch, 3, 1)
+    ws = torch.full((binding.spec_verify_workspace_size(B, K, V, 0),), 0xA5, dtype=torch.uint8, device="cuda")
+    for fill in (0xA5, 0xFF):
+        ws.fill_(fill)
+        outs = _outs(B, K)
+        assert _call(lib, d["target"], d["draft"], d["draft_tokens"], d["temperature"], outs, ws, B, K, V) == 0
+        torch.cuda.synchronize()
+        compare_sample(_outs_np(outs), ref, batch["temperature"].numpy())
+        assert (outs["st"].cpu().numpy() == 0).all()
+
+
+def test_one_workspace_alternates_between_the_two_paths():
+    """B = 320 (single kernel), B = 16 (two kernels), B = 320 again on one zero-filled
+    workspace: every call equals the oracle."""
+    from speculative_decoding_verification_15_gb300 import binding
+
+    lib = binding.load()
+    K, V = 3, 5000
+    shapes = [(320, 3202), (16, 3203), (320, 3204), (16, 3205)]
+    size = max(binding.spec_verify_workspace_size(B, K, V, 0) for B, _ in shapes)
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    for B, seed in shapes:
+        batch, d = _sized(B, K, V, seed)
+        outs = _outs(B, K)
+        assert _call(lib, d["target"], d["draft"], d["draft_tokens"], d["temperature"], outs, ws, B, K, V) == 0
+        torch.cuda.synchronize()
+        compare_sample(_outs_np(outs), run_oracle_sample(batch, 3, 1), batch["temperature"].numpy())
+        assert (outs["st"].cpu().numpy() == 0).all()
