@@ -103,7 +103,9 @@ typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
  * call, so one workspace serves any number of calls made in stream order; calls
  * that may overlap need one workspace each.  A call on a workspace that was not
  * zeroed reports status 5 for the requests it could not verify, and leaves the
- * workspace ready for the next call.
+ * workspace ready for the next call.  Calls with B at or above the device's SM
+ * count run one persistent kernel, preceded in stream order by a memset of the
+ * counters and request lines: for them any workspace contents serve.
  */
 size_t spec_verify_workspace_size(int B, int Kmax, int V, int dtype);
 

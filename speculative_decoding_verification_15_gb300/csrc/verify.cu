@@ -1581,12 +1581,15 @@ constexpr int kSyncWords = 16;  // 64-bit words a request: the 128-byte line com
 constexpr int kSyncDone = 0;   // (tag, items of the request finished)
 constexpr int kSyncBest = 1;   // (tag, ordered bits of the best exact score an item found)
 // Ticket counters at the start of the workspace, zeroed in stream order before every
-// launch (so a workspace left in any state by another call serves this one).  Every chunk and
-// every item is taken by ticket: a ticket is only ever held by a running CTA, which
-// finishes its chunks before it waits for anything, so progress never depends on a
-// CTA that is not resident.
+// launch (so a workspace left in any state by another call serves this one), and
+// zero again when the kernel ends: the last CTA to leave resets them, since the
+// two-kernel path expects its chunk counter (the same word) at zero.  Every chunk
+// and every item is taken by ticket: a ticket is only ever held by a running CTA,
+// which finishes its chunks before it waits for anything, so progress never depends
+// on a CTA that is not resident.
 constexpr int kCntChunk = 0;
 constexpr int kCntItem = 1;
+constexpr int kCntExit = 2;
 constexpr int kSV = 2;             // commit items: vectors a thread holds per slice of a chunk
 // a warp's live list: < 64 carried + one vector's groups (2 pieces of 4 entries per
 // bf16 vector, each listing 2 groups when the window is not group-aligned)
@@ -1608,7 +1611,7 @@ struct VerifyParams {
     uint32_t epoch;            // tag of this call, stored with every partial
     int cpr, ce;               // chunks per row, entries per chunk
     int Q;                     // commit items per request (1 .. cpr)
-    uint32_t *counters;        // [kCntChunk, kCntItem], zero at launch
+    uint32_t *counters;        // [kCntChunk, kCntItem, kCntExit], zero at launch and at exit
     unsigned long long *sync;  // [B][kSyncWords]
     Part *parts;               // [chunks] one per chunk of every main-pass row
     uint16_t *cand;            // [chunks][kCW] sampling rows: the window vector holding each warp's
@@ -2418,6 +2421,12 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) verify_kernel(VerifyPar
         const uint32_t item = s_item[it & 1];
         if (item >= nitems) break;
         commit_item<Vec>(p, s_rs, (int)item, s_sh);
+    }
+    // the last CTA to leave: every ticket of this call is taken
+    if (threadIdx.x == 0 && atomicAdd(p.counters + kCntExit, 1u) == gridDim.x - 1) {
+        p.counters[kCntChunk] = 0u;
+        p.counters[kCntItem] = 0u;
+        p.counters[kCntExit] = 0u;
     }
 }
 

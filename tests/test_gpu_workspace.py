@@ -112,22 +112,25 @@ def test_single_kernel_path_ignores_what_the_workspace_held():
         torch.cuda.synchronize()
         compare_sample(_outs_np(outs), ref, batch["temperature"].numpy())
         assert (outs["st"].cpu().numpy() == 0).all()
+        assert int(ws[:4].view(torch.int32).item()) == 0  # the shared chunk counter
 
 
 def test_one_workspace_alternates_between_the_two_paths():
-    """B = 320 (single kernel), B = 16 (two kernels), B = 320 again on one zero-filled
-    workspace: every call equals the oracle."""
+    """B = 320 (single kernel, V = 5000), B = 16 (two kernels, K = 8, V = 151936: 1280
+    chunks, more than the two static chunks of each of main_kernel's CTAs, so the
+    ticket counter the single kernel shares must be zero again), then both once more,
+    on one zero-filled workspace: every call equals the oracle."""
     from speculative_decoding_verification_15_gb300 import binding
 
     lib = binding.load()
-    K, V = 3, 5000
-    shapes = [(320, 3202), (16, 3203), (320, 3204), (16, 3205)]
-    size = max(binding.spec_verify_workspace_size(B, K, V, 0) for B, _ in shapes)
+    shapes = [(320, 3, 5000, 3202), (16, 8, 151936, 3203), (320, 3, 5000, 3204), (16, 8, 151936, 3205)]
+    size = max(binding.spec_verify_workspace_size(B, K, V, 0) for B, K, V, _ in shapes)
     ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
-    for B, seed in shapes:
+    for B, K, V, seed in shapes:
         batch, d = _sized(B, K, V, seed)
         outs = _outs(B, K)
         assert _call(lib, d["target"], d["draft"], d["draft_tokens"], d["temperature"], outs, ws, B, K, V) == 0
         torch.cuda.synchronize()
         compare_sample(_outs_np(outs), run_oracle_sample(batch, 3, 1), batch["temperature"].numpy())
         assert (outs["st"].cpu().numpy() == 0).all()
+        assert int(ws[:4].view(torch.int32).item()) == 0  # the shared chunk counter
