@@ -18,9 +18,10 @@
 //                        and writes z.  Every projection row is read once per
 //                        position (from L2 after the first position: r x V x 2 B =
 //                        78 MB at V = 151936, r = 256 in bf16, fits the 129 MB L2).
-//  markov_sample_kernel  one CTA per request: the pruned exact Gumbel-max (or the
-//                        argmax) over z_k, status, and the token that the next
-//                        position's bias uses.
+//  markov_sample_kernel  one cluster of 4 CTAs per request, each over a quarter of
+//                        the row: the pruned exact Gumbel-max (or the argmax) over
+//                        z_k, status, and the token that the next position's bias
+//                        uses.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,7 +35,9 @@ namespace {
 constexpr int kMkCols = 32;        // vocabulary entries per bias CTA
 constexpr int kMkThreads = 256;    // 8 warps: one request at a time each
 constexpr int kMkWarps = kMkThreads / 32;
-constexpr int kMkSampleThreads = 1024;
+constexpr int kSmC = 4;           // sample pass: CTAs (one cluster) per request
+constexpr int kSmThreads = 512;   // sample pass: threads per CTA
+constexpr int kSmBatch = 8;       // sample pass: 4-entry groups a thread has in flight
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every mbarrier wait (2 s)
 
 struct MarkovParams {
@@ -348,14 +351,74 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
     }
 }
 
-// One CTA per request.  k = -1: the status of a block with no positions (K = 0).
-__global__ void __launch_bounds__(kMkSampleThreads) markov_sample_kernel(MarkovParams p, int k) {
-    __shared__ float red_s[kMkSampleThreads / 32];
-    __shared__ int red_i[kMkSampleThreads / 32];
-    const int b = blockIdx.x, tid = threadIdx.x;
+// Status of a block with no positions (K = 0): the anchors and temperatures checked.
+__global__ void markov_status_kernel(MarkovParams p) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= p.B) return;
+    const int a = p.anchor[b];
+    int st = (a < 0 || a >= p.V) ? SPEC_STATUS_BAD_TOKEN : SPEC_STATUS_OK;
+    if (st == SPEC_STATUS_OK && p.temperature) {
+        const float T = p.temperature[b];
+        if (!(T >= 0.f) || isinf(T)) st = SPEC_STATUS_BAD_TEMPERATURE;
+    }
+    p.status[b] = st;
+}
+
+// Groups g of 4 entries of row zr (float4 loads when rows are 16-byte aligned; the
+// entries past V read as -inf).
+template <bool VEC>
+__device__ __forceinline__ float4 load_group(const float *zr, int g, int V) {
+    if constexpr (VEC) {
+        return reinterpret_cast<const float4 *>(zr)[g];
+    } else {
+        float q[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) q[e] = 4 * g + e < V ? zr[4 * g + e] : kNegInf;
+        return make_float4(q[0], q[1], q[2], q[3]);
+    }
+}
+
+// CTA argmax (lowest index among equal scores) of the threads' (s, i); every thread
+// gets the result.
+__device__ __forceinline__ void block_argmax_sm(float &s, int &i, float *red_s, int *red_i) {
+    warp_argmax(s, i);
+    const int tid = threadIdx.x;
+    if ((tid & 31) == 0) {
+        red_s[tid >> 5] = s;
+        red_i[tid >> 5] = i;
+    }
+    __syncthreads();
+    s = red_s[0];
+    i = red_i[0];
+    for (int w = 1; w < kSmThreads / 32; ++w)
+        if (better(red_s[w], red_i[w], s, i)) {
+            s = red_s[w];
+            i = red_i[w];
+        }
+    __syncthreads();  // red_s and red_i are reused
+}
+
+// One cluster of kSmC CTAs per request, CTA c reading the c-th contiguous share of
+// the row's 4-entry groups.  The draw argmax_v z_v / T + g_v is pruned exactly (as
+// the verify's draws): a group of 4 entries can only beat a known exact score thr if
+// z_max / T + 17 >= thr (no word gives more than 16.64 of noise), and an entry only
+// if 1 - u <= 1.001 e^(z / T - thr).  Pass 1 finds each thread's largest entry (and
+// checks the row); thr starts at the best exact score of those entries over the
+// whole cluster, exchanged through distributed shared memory; pass 2 draws the groups
+// that can still win.  The CTAs' results meet the same way and are combined in rank
+// order (lowest index among equal scores), so the token does not depend on the split.
+// T = 0: pass 1 alone gives the argmax.
+template <bool VEC>
+__global__ void __launch_bounds__(kSmThreads, 2) markov_sample_kernel(MarkovParams p, int k) {
+    __shared__ float red_s[kSmThreads / 32];
+    __shared__ int red_i[kSmThreads / 32];
+    __shared__ __align__(16) uint4 s_ex[2][kSmC];  // the two exchanges' slots, one per rank
+    const uint32_t rank = cluster_ctarank();
+    const int b = blockIdx.x / kSmC, tid = threadIdx.x;
+    cluster_arrive_relaxed();
     int st;
     float T = 0.f;
-    if (k <= 0) {
+    if (k == 0) {
         const int a = p.anchor[b];
         st = (a < 0 || a >= p.V) ? SPEC_STATUS_BAD_TOKEN : SPEC_STATUS_OK;
         if (st == SPEC_STATUS_OK && p.temperature) {
@@ -366,90 +429,90 @@ __global__ void __launch_bounds__(kMkSampleThreads) markov_sample_kernel(MarkovP
         st = p.status[b];
         if (p.temperature) T = p.temperature[b];
     }
-    if (k < 0) {
-        if (tid == 0) p.status[b] = st;
-        return;
-    }
-    float best = kNegInf;
-    int bi = -1;
+    const bool greedy = T == 0.f;
+    const float invT = greedy ? 0.f : __fdiv_rn(1.f, T);
+    const float *zr = p.z + ((int64_t)b * p.K + k) * p.V;
+    const int ng = (p.V + 3) >> 2;
+    const int g_lo = (int)((int64_t)ng * rank / kSmC), g_hi = (int)((int64_t)ng * (rank + 1) / kSmC);
+    constexpr int kStride = kSmBatch * kSmThreads;
+
+    // ---- pass 1: each thread's largest entry (the lowest index among equal ones)
+    float m = kNegInf;
+    int mi = -1;
     bool bad = false;
     if (st == SPEC_STATUS_OK) {
-        const float *zr = p.z + ((int64_t)b * p.K + k) * p.V;
-        if (T == 0.f) {
-            for (int v = tid; v < p.V; v += kMkSampleThreads) {
-                const float zv = zr[v];
-                if (zv != zv || zv == __int_as_float(0x7f800000)) bad = true;
-                if (zv > kNegInf && better(zv, v, best, bi)) {
-                    best = zv;
-                    bi = v;
+        for (int g0 = g_lo + tid; g0 < g_hi; g0 += kStride) {
+            float4 q[kSmBatch];
+#pragma unroll
+            for (int u = 0; u < kSmBatch; ++u) {
+                const int g = g0 + u * kSmThreads;
+                q[u] = g < g_hi ? load_group<VEC>(zr, g, p.V) : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+            }
+#pragma unroll
+            for (int u = 0; u < kSmBatch; ++u) {
+                const int g = g0 + u * kSmThreads;
+                const float zq[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (zq[e] != zq[e] || zq[e] == __int_as_float(0x7f800000)) bad = true;
+                    if (zq[e] > m) {
+                        m = zq[e];
+                        mi = 4 * g + e;
+                    }
                 }
             }
+        }
+    }
+    float best = kNegInf;  // greedy: z itself; sampling: the exact score
+    int bi = -1;
+    if (mi >= 0) {
+        bi = mi;
+        if (greedy) {
+            best = m;
         } else {
-            // The draw argmax_v z_v / T + g_v, pruned exactly (as the verify's draws): a
-            // group of 4 entries can only beat a known exact score thr if
-            // z_max / T + 17 >= thr (no word gives more than 16.64 of noise), and an
-            // entry only if 1 - u <= 1.001 e^(z / T - thr).  thr starts at the best exact
-            // score of each thread's largest entry (pass 1, which also checks the row).
-            const float invT = __fdiv_rn(1.f, T);
-            float m = kNegInf;
-            int mi = -1;
-            if ((p.V & 3) == 0) {  // rows 16-byte aligned: four groups (float4) in flight a thread
-                const float4 *z4 = reinterpret_cast<const float4 *>(zr);
-                const int ng = p.V >> 2;
-                for (int g0 = tid; g0 < ng; g0 += 4 * kMkSampleThreads) {
-                    float4 q[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int g = g0 + u * kMkSampleThreads;
-                        q[u] = g < ng ? z4[g] : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int g = g0 + u * kMkSampleThreads;
-                        const float zq[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (zq[e] != zq[e] || zq[e] == __int_as_float(0x7f800000)) bad = true;
-                            if (zq[e] > m) {
-                                m = zq[e];
-                                mi = 4 * g + e;
-                            }
-                        }
-                    }
-                }
-            } else {
-                for (int v = tid; v < p.V; v += kMkSampleThreads) {
-                    const float zv = zr[v];
-                    if (zv != zv || zv == __int_as_float(0x7f800000)) bad = true;
-                    if (zv > m) {
-                        m = zv;
-                        mi = v;
-                    }
-                }
+            const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)k, PURPOSE_DRAFT, (uint32_t)mi >> 2);
+            best = fmaf(m, invT, gumbel_of_word(word_of(r4, mi & 3)));
+        }
+    }
+    bad = __syncthreads_or(bad);
+    float s1 = best;
+    int i1 = bi;
+    block_argmax_sm(s1, i1, red_s, red_i);
+    cluster_wait();  // every CTA of the cluster is running
+    if (tid == 0)
+        for (uint32_t c = 0; c < kSmC; ++c)
+            st_cluster_v4(&s_ex[0][rank], c, make_uint4(__float_as_uint(s1), (uint32_t)i1, bad ? 1u : 0u, 0u));
+    cluster_arrive();
+    cluster_wait();
+    {
+        const uint4 x0 = s_ex[0][0];
+        s1 = __uint_as_float(x0.x);
+        i1 = (int)x0.y;
+        bad = x0.z != 0u;
+        for (int c = 1; c < kSmC; ++c) {
+            const uint4 x = s_ex[0][c];
+            bad |= x.z != 0u;
+            if (better(__uint_as_float(x.x), (int)x.y, s1, i1)) {
+                s1 = __uint_as_float(x.x);
+                i1 = (int)x.y;
             }
-            if (mi >= 0) {
-                const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)k, PURPOSE_DRAFT, (uint32_t)mi >> 2);
-                best = fmaf(m, invT, gumbel_of_word(word_of(r4, mi & 3)));
-                bi = mi;
-            }
-            float thr = warp_max(best);
-            if ((tid & 31) == 0) red_s[tid >> 5] = thr;
-            __syncthreads();
-            for (int w = 0; w < kMkSampleThreads / 32; ++w) thr = fmaxf(thr, red_s[w]);
-            __syncthreads();  // red_s is reused below
-            const bool vec = (p.V & 3) == 0;  // rows 16-byte aligned: one float4 per group
-            for (int g = tid; 4 * g < p.V; g += kMkSampleThreads) {
-                float zq[4];
-                if (vec) {
-                    const float4 q4 = reinterpret_cast<const float4 *>(zr)[g];
-                    zq[0] = q4.x;
-                    zq[1] = q4.y;
-                    zq[2] = q4.z;
-                    zq[3] = q4.w;
-                } else {
+        }
+    }
+
+    // ---- pass 2 (sampling): the groups that can beat thr
+    if (st == SPEC_STATUS_OK && !greedy && !bad && i1 >= 0) {
+        float thr = s1;
+        for (int g0 = g_lo + tid; g0 < g_hi; g0 += kStride) {
+            float4 q[kSmBatch];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) zq[e] = 4 * g + e < p.V ? zr[4 * g + e] : kNegInf;
-                }
+            for (int u = 0; u < kSmBatch; ++u) {
+                const int g = g0 + u * kSmThreads;
+                q[u] = g < g_hi ? load_group<VEC>(zr, g, p.V) : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+            }
+#pragma unroll
+            for (int u = 0; u < kSmBatch; ++u) {
+                const int g = g0 + u * kSmThreads;
+                const float zq[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
                 const float zmax = fmaxf(fmaxf(zq[0], zq[1]), fmaxf(zq[2], zq[3]));
                 if (!(zmax > kNegInf) || fmaf(zmax, invT, kGumbelMax) < thr) continue;
                 const uint4 r4 = rand_group(p.seed, p.step, (uint32_t)b, (uint32_t)k, PURPOSE_DRAFT, (uint32_t)g);
@@ -469,27 +532,32 @@ __global__ void __launch_bounds__(kMkSampleThreads) markov_sample_kernel(MarkovP
             }
         }
     }
-    bad = __syncthreads_or(bad);
-    warp_argmax(best, bi);
-    if ((tid & 31) == 0) {
-        red_s[tid >> 5] = best;
-        red_i[tid >> 5] = bi;
+    block_argmax_sm(best, bi, red_s, red_i);
+    if (tid == 0)
+        for (uint32_t c = 0; c < kSmC; ++c)
+            st_cluster_v4(&s_ex[1][rank], c, make_uint4(__float_as_uint(best), (uint32_t)bi, 0u, 0u));
+    cluster_arrive();
+    cluster_wait();  // no shared memory of another CTA is touched after this
+    if (rank != 0) return;
+    if (greedy) {
+        bi = i1;
+    } else {
+        best = __uint_as_float(s_ex[1][0].x);
+        bi = (int)s_ex[1][0].y;
+        for (int c = 1; c < kSmC; ++c) {
+            const uint4 x = s_ex[1][c];
+            if (better(__uint_as_float(x.x), (int)x.y, best, bi)) {
+                best = __uint_as_float(x.x);
+                bi = (int)x.y;
+            }
+        }
     }
-    __syncthreads();
-    if (tid < 32) {
-        best = red_s[tid];
-        bi = red_i[tid];
-        warp_argmax(best, bi);
-    }
-    if (tid == 0) red_i[0] = bi;
-    __syncthreads();
-    bi = red_i[0];
     if (st == SPEC_STATUS_OK && (bad || bi < 0)) st = SPEC_STATUS_NONFINITE;
     if (st == SPEC_STATUS_OK) {
         if (tid == 0) p.tokens[(int64_t)b * p.K + k] = bi;
     } else {
         // a failed request has every token -1 (later positions write their own)
-        for (int i = tid; i <= k; i += kMkSampleThreads) p.tokens[(int64_t)b * p.K + i] = -1;
+        for (int i = tid; i <= k; i += kSmThreads) p.tokens[(int64_t)b * p.K + i] = -1;
     }
     if (tid == 0) p.status[b] = st;
 }
@@ -918,9 +986,27 @@ __global__ void __launch_bounds__(kTkDrawThreads) markov_topk_draw_kernel(Markov
     if (tid == 0) p.status[b] = st;
 }
 
+// The sample pass of position k: one cluster of kSmC CTAs per request.
+cudaError_t launch_sample(const MarkovParams &p, int k, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * kSmC));
+    cfg.blockDim = dim3(kSmThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSmC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return (p.V & 3) == 0 ? cudaLaunchKernelEx(&cfg, markov_sample_kernel<true>, p, k)
+                          : cudaLaunchKernelEx(&cfg, markov_sample_kernel<false>, p, k);
+}
+
 int markov_topk_impl(const MarkovParams &p, int ncand, int32_t *cands, cudaStream_t stream) {
     if (p.K == 0) {
-        markov_sample_kernel<<<p.B, kMkSampleThreads, 0, stream>>>(p, -1);
+        markov_status_kernel<<<(p.B + 255) / 256, 256, 0, stream>>>(p);
     } else if (p.dtype == SPEC_BF16) {
         markov_topk_select_kernel<2><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
         markov_topk_draw_kernel<2><<<p.B, kTkDrawThreads, 0, stream>>>(p, ncand, cands);
@@ -980,7 +1066,7 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
         tgrid = per > 0 ? min(ntiles, per * sms) : 0;
     }
     if (p.K == 0) {
-        markov_sample_kernel<<<p.B, kMkSampleThreads, 0, stream>>>(p, -1);
+        markov_status_kernel<<<(p.B + 255) / 256, 256, 0, stream>>>(p);
     } else {
         const int nb = (p.V + kMkCols - 1) / kMkCols, nbm = (p.V + kMmCols - 1) / kMmCols;
         for (int k = 0; k < p.K; ++k) {
@@ -990,7 +1076,11 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
                 markov_bias_mma_kernel<<<nbm, kMkThreads, msmem, stream>>>(p, k);
             else
                 markov_bias_kernel<<<nb, kMkThreads, smem, stream>>>(p, k);
-            markov_sample_kernel<<<p.B, kMkSampleThreads, 0, stream>>>(p, k);
+            e = launch_sample(p, k, stream);
+            if (e != cudaSuccess) {
+                note_cuda_error((int)e);
+                return SPEC_ECUDA;
+            }
         }
     }
     e = cudaGetLastError();
