@@ -204,30 +204,54 @@ __global__ void __launch_bounds__(kMkThreads) markov_bias_mma_kernel(MarkovParam
 
 // bf16 factors, the same products with the projection rows streamed: a persistent
 // grid (two CTAs per SM at r = 256) walks the 64-entry column tiles; for each chunk
-// of 64 requests a CTA keeps their embedding rows H in shared memory and brings each
-// tile's 64 projection rows in by bulk copies (one per row, into rows padded by 8
-// elements so that a warp's fragment loads hit 32 banks), double-buffered on two
-// mbarriers, so the next tile's rows land while the tensor cores work on this one.
-// Warp w forms entries 8w .. 8w+7 of the tile for all 64 requests (mma.sync
-// m16n8k16, fp32 accumulate; the backbone logits are loaded before the products and
-// added after them).  A bulk-copy wait is bounded: if one gives up, the
-// CTA waits (bounded) for its copies in flight and writes NaN for the rest of its
-// tiles, so those requests report status 4.
+// of 64 requests a CTA keeps their embedding rows H in shared memory (rows padded by
+// 8 elements) and brings each tile's projection rows in by 8 bulk copies of 8 rows,
+// block j at j (16 r + 16) bytes: the 16 bytes between blocks put rows 8 j + beta,
+// j = 0 .. 7, on different banks, so that the tensor cores' B operand for the
+// entries {8 j + beta} (n-block beta) loads without conflicts by ldmatrix.  Two
+// tiles are in flight while a third is multiplied.  Warp w forms requests
+// 32 (w / 4) .. +31 and n-blocks 2 (w % 4), 2 (w % 4) + 1 (mma.sync m16n8k16, bf16
+// in, fp32 accumulate); the products then pass through shared memory (the stage just
+// consumed), so that U is read and z written with 16-byte accesses along the rows;
+// z = U + (emb . proj), U added after the products.  A bulk-copy wait is bounded: if
+// one gives up, the CTA waits (bounded) for its copies in flight and writes NaN for
+// the rest of its tiles, so those requests report status 4.
+constexpr int kCtStride = 68;  // floats a row of the staged product tile (64 + 4)
+
+__host__ __device__ inline size_t tma_stage_bytes(int r) {
+    const size_t rows = (size_t)8 * (16 * (size_t)r + 16);
+    const size_t ctile = sizeof(float) * (size_t)kMmReqs * kCtStride;
+    return rows > ctile ? rows : ctile;
+}
 __host__ __device__ inline size_t tma_smem_bytes(int r) {
-    return sizeof(uint16_t) * (size_t)(kMmReqs + 2 * kMmCols) * (r + 8) + sizeof(int) * kMmReqs;
+    return sizeof(uint16_t) * (size_t)kMmReqs * (r + 8) + 2 * tma_stage_bytes(r) + sizeof(int) * kMmReqs;
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t (&d)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(addr));
+}
+
+// VEC: U rows 8-byte aligned (ld_row % 4 == 0, base 8-byte aligned) and z rows
+// 16-byte aligned (V % 4 == 0, z 16-byte aligned): the epilogue's vector accesses.
+template <bool VEC>
 __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovParams p, int k) {
-    extern __shared__ __align__(128) uint16_t tms[];
+    extern __shared__ __align__(128) unsigned char tsm[];
     __shared__ __align__(8) uint64_t s_bar[2];
-    const int rs = p.r + 8;
-    uint16_t *Hs = tms;                                 // [64 requests][rs]
-    uint16_t *Ps = tms + (size_t)kMmReqs * rs;          // [2 stages][64 entries][rs]
-    int *okv = reinterpret_cast<int *>(Ps + 2 * (size_t)kMmCols * rs);
+    const int r = p.r, rs = r + 8;
+    const size_t sb = tma_stage_bytes(r);
+    const uint32_t blk = 16u * (uint32_t)r + 16u;  // bytes from one block of 8 rows to the next
+    const uint32_t rowbytes = (uint32_t)r * 2u;
+    uint16_t *Hs = reinterpret_cast<uint16_t *>(tsm);                // [64 requests][rs]
+    unsigned char *stages = tsm + sizeof(uint16_t) * (size_t)kMmReqs * rs;  // [2][sb]
+    int *okv = reinterpret_cast<int *>(stages + 2 * sb);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int mh = warp >> 2, nq = warp & 3;
+    const int li = lane >> 3, l8 = lane & 7;  // ldmatrix: this lane's matrix and row
+    const int g = lane >> 2, t4 = lane & 3;   // mma fragments: row group, column pair
     const int ntiles = (p.V + kMmCols - 1) / kMmCols;
-    const uint32_t rowbytes = (uint32_t)p.r * 2u;
-    const int vpr = p.r >> 3;  // 16-byte vectors per row
+    const int vpr = r >> 3;
     if (tid == 0) {
         mbar_init(&s_bar[0], 1);
         mbar_init(&s_bar[1], 1);
@@ -235,8 +259,8 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
     }
     __syncthreads();
     uint32_t used[2] = {0u, 0u};  // phases of each stage waited on so far (the same in every thread)
+    bool pend[2] = {false, false};
     bool failed = false;
-    const int g = lane >> 2, t2 = (lane & 3) * 2;
     for (int b0 = 0; b0 < p.B; b0 += kMmReqs) {
         if (tid < kMmReqs) {
             const int b = b0 + tid;
@@ -252,102 +276,139 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
             const int m = i / vpr, q = i - m * vpr;
             const int ok = okv[m];
             uint4 x = make_uint4(0, 0, 0, 0);
-            if (ok) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.emb + (int64_t)(ok - 1) * p.r + 8 * q);
+            if (ok) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.emb + (int64_t)(ok - 1) * r + 8 * q);
             *reinterpret_cast<uint4 *>(Hs + m * rs + 8 * q) = x;
         }
-        // tile t into stage st: warp 0 registers the bytes, then its lanes issue one
-        // bulk copy per row
+        // tile t into stage st: warp 0 registers the bytes, lanes 0..7 copy a block each
         auto issue = [&](int t, int st) {
+            if (failed || t >= ntiles) return;
+            pend[st] = true;
             if (warp != 0) return;
             const int v0 = t * kMmCols, nc = min(kMmCols, p.V - v0);
             if (lane == 0) mbar_arrive_expect_tx(&s_bar[st], (uint32_t)nc * rowbytes);
             __syncwarp();
-            for (int c = lane; c < nc; c += 32)
-                bulk_g2s(Ps + ((size_t)st * kMmCols + c) * rs, (const uint16_t *)p.proj + (int64_t)(v0 + c) * p.r,
-                         rowbytes, &s_bar[st]);
+            const int rows = min(8, nc - 8 * lane);
+            if (lane < 8 && rows > 0)
+                bulk_g2s(stages + (size_t)st * sb + (size_t)lane * blk,
+                         (const uint16_t *)p.proj + (int64_t)(v0 + 8 * lane) * r, (uint32_t)rows * rowbytes,
+                         &s_bar[st]);
         };
         int i = 0;
-        if (!failed && (int)blockIdx.x < ntiles) issue(blockIdx.x, 0);
+        issue(blockIdx.x, 0);
+        issue(blockIdx.x + gridDim.x, 1);
         __syncthreads();  // H and okv are in
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             const int st = i & 1;
-            const int tn = t + gridDim.x;
-            if (!failed && tn < ntiles) issue(tn, st ^ 1);  // stage st ^ 1 was released at the last barrier
+            unsigned char *sbase = stages + (size_t)st * sb;
             bool ok = !failed;
             if (ok) {
                 if (tid == 0) ok = mbar_wait(&s_bar[st], used[st] & 1u, kWaitNs);
                 ok = !__syncthreads_or(!ok);
                 if (ok) mbar_try_wait(&s_bar[st], used[st] & 1u);  // every thread observes the completed phase
                 used[st] += 1u;
+                pend[st] = false;
                 if (!ok) {
                     failed = true;
                     // the copies in flight still land: wait for them (bounded) before the
                     // CTA can leave
                     if (tid == 0) {
                         mbar_wait(&s_bar[st], (used[st] - 1u) & 1u, kWaitNs);
-                        if (tn < ntiles) mbar_wait(&s_bar[st ^ 1], used[st ^ 1] & 1u, kWaitNs);
+                        if (pend[st ^ 1]) mbar_wait(&s_bar[st ^ 1], used[st ^ 1] & 1u, kWaitNs);
                     }
+                    pend[st ^ 1] = false;
                     __syncthreads();
                 }
             }
             const int v0 = t * kMmCols, ncol = min(kMmCols, p.V - v0);
-            // this thread's 16 backbone logits of the tile (bf16, two to a register),
-            // loaded before the products so that their latency overlaps the tensor-core
-            // work; they are added after the products, as z = U + (emb . proj)
-            uint32_t upk[8];
+            // the epilogue's backbone logits, loaded before the products: request row
+            // 16 pass + tid / 16, entries 4 (tid % 16) .. +3 of the tile
+            const int eq = 4 * (tid & 15);
+            uint2 upk[4];
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int m = mt * 16 + g + 8 * h;
-                    const int n = warp * 8 + t2;
-                    const int b = b0 + m;
+            for (int ps = 0; ps < 4; ++ps) {
+                const int m = 16 * ps + (tid >> 4), b = b0 + m;
+                upk[ps] = make_uint2(0u, 0u);
+                if (b < p.B && eq < ncol) {
                     const unsigned short *ur =
-                        (const unsigned short *)p.base + ((int64_t)b * p.K + k) * p.ld_row + v0 + n;
-                    const uint32_t lo = (b < p.B && n < ncol) ? __ldg(ur) : 0u;
-                    const uint32_t hi = (b < p.B && n + 1 < ncol) ? __ldg(ur + 1) : 0u;
-                    upk[mt * 2 + h] = lo | (hi << 16);
-                }
-            float acc[4][4];
+                        (const unsigned short *)p.base + ((int64_t)b * p.K + k) * p.ld_row + v0 + eq;
+                    if (VEC && eq + 4 <= ncol) {
+                        upk[ps] = __ldg(reinterpret_cast<const uint2 *>(ur));
+                    } else {
+                        uint32_t h[4];
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-            if (ok) {
-                const uint16_t *pb = Ps + ((size_t)st * kMmCols + warp * 8 + g) * rs + t2;
-                for (int kk = 0; kk < p.r; kk += 16) {
-                    uint32_t bf[2];
-                    bf[0] = *reinterpret_cast<const uint32_t *>(pb + kk);
-                    bf[1] = *reinterpret_cast<const uint32_t *>(pb + kk + 8);
-#pragma unroll
-                    for (int mt = 0; mt < 4; ++mt) {
-                        const uint16_t *pa = Hs + (mt * 16 + g) * rs + kk + t2;
-                        uint32_t af[4];
-                        af[0] = *reinterpret_cast<const uint32_t *>(pa);
-                        af[1] = *reinterpret_cast<const uint32_t *>(pa + 8 * rs);
-                        af[2] = *reinterpret_cast<const uint32_t *>(pa + 8);
-                        af[3] = *reinterpret_cast<const uint32_t *>(pa + 8 * rs + 8);
-                        mma_bf16_16816(acc[mt], af, bf);
+                        for (int e = 0; e < 4; ++e) h[e] = eq + e < ncol ? (uint32_t)__ldg(ur + e) : 0u;
+                        upk[ps] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
                     }
                 }
             }
+            float acc[2][2][4];
 #pragma unroll
-            for (int mt = 0; mt < 4; ++mt)
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[a][c][e] = 0.f;
+            if (ok) {
+                const uint32_t a_addr = smem_addr(Hs + (size_t)(32 * mh + (li & 1) * 8 + l8) * rs + (li >> 1) * 8);
+                const uint32_t a_step = 16u * (uint32_t)rs * 2u;  // the next 16-request tile
+                const uint32_t b_addr = smem_addr(sbase) + (uint32_t)l8 * blk +
+                                        (uint32_t)(2 * nq + (li >> 1)) * rowbytes + (uint32_t)(li & 1) * 16u;
+#pragma unroll 2
+                for (int kk = 0; kk < r; kk += 16) {
+                    uint32_t a0[4], a1[4], bq[4];
+                    ldsm_x4(a0, a_addr + 2u * kk);
+                    ldsm_x4(a1, a_addr + a_step + 2u * kk);
+                    ldsm_x4(bq, b_addr + 2u * kk);
+                    const uint32_t bn0[2] = {bq[0], bq[1]}, bn1[2] = {bq[2], bq[3]};
+                    mma_bf16_16816(acc[0][0], a0, bn0);
+                    mma_bf16_16816(acc[0][1], a0, bn1);
+                    mma_bf16_16816(acc[1][0], a1, bn0);
+                    mma_bf16_16816(acc[1][1], a1, bn1);
+                }
+            }
+            __syncthreads();  // every warp is done with the stage's rows
+            // products into the stage as C [64 requests][kCtStride]: column c of n-block
+            // beta is tile entry 8 c + beta
+            float *Cs = reinterpret_cast<float *>(sbase);
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int m = 32 * mh + 16 * a + g, beta = 2 * nq + c;
+                    Cs[m * kCtStride + 16 * t4 + beta] = acc[a][c][0];
+                    Cs[m * kCtStride + 16 * t4 + 8 + beta] = acc[a][c][1];
+                    Cs[(m + 8) * kCtStride + 16 * t4 + beta] = acc[a][c][2];
+                    Cs[(m + 8) * kCtStride + 16 * t4 + 8 + beta] = acc[a][c][3];
+                }
+            __syncthreads();
+#pragma unroll
+            for (int ps = 0; ps < 4; ++ps) {
+                const int m = 16 * ps + (tid >> 4), b = b0 + m;
+                if (b >= p.B || eq >= ncol) continue;
+                const float4 cv = *reinterpret_cast<const float4 *>(Cs + m * kCtStride + eq);
+                const bool good = ok && okv[m] != 0;
+                const uint32_t w[2] = {upk[ps].x, upk[ps].y};
+                float o[4];
+                const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int m = mt * 16 + g + (e >= 2 ? 8 : 0);
-                    const int n = warp * 8 + t2 + (e & 1);
-                    const int b = b0 + m;
-                    if (b < p.B && n < ncol) {
-                        const int64_t row = (int64_t)b * p.K + k;
-                        const int v = v0 + n;
-                        const uint32_t w = upk[mt * 2 + (e >> 1)];
-                        const float uv = (e & 1) ? __uint_as_float(w & 0xffff0000u) : __uint_as_float(w << 16);
-                        p.z[row * p.V + v] = (ok && okv[m]) ? uv + acc[mt][e] : __int_as_float(0x7fc00000);
-                    }
+                    const uint32_t h = (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16);
+                    o[e] = good ? __uint_as_float(h) + cc[e] : __int_as_float(0x7fc00000);
                 }
-            __syncthreads();  // stage st and (after the chunk) H are free
+                float *zp = p.z + ((int64_t)b * p.K + k) * p.V + v0 + eq;
+                if (VEC && eq + 4 <= ncol) {
+                    *reinterpret_cast<float4 *>(zp) = make_float4(o[0], o[1], o[2], o[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (eq + e < ncol) zp[e] = o[e];
+                }
+            }
+            __syncthreads();  // stage st is free
+            issue(t + 2 * (int)gridDim.x, st);
         }
+        // the next chunk of requests rewrites H and okv; no copy is pending here
+        __syncthreads();
     }
 }
 
@@ -1043,12 +1104,19 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
             return SPEC_ECUDA;
         }
     }
-    // bf16 factors streamed by bulk copies: a persistent grid of as many CTAs as fit
+    // bf16 factors streamed by bulk copies: a persistent grid of as many CTAs as fit;
+    // vector accesses in the epilogue where U and z rows allow them
     const size_t tsmem = tma_smem_bytes(p.r);
+    const bool tvec = (p.ld_row % 4) == 0 && ((uintptr_t)p.base % 8) == 0 && (p.V % 4) == 0 &&
+                      ((uintptr_t)p.z % 16) == 0;
     int tgrid = 0;
     if (mma) {
         if (tsmem > 48 * 1024) {
-            e = cudaFuncSetAttribute(markov_bias_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsmem);
+            e = cudaFuncSetAttribute(markov_bias_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)tsmem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(markov_bias_tma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tsmem);
             if (e != cudaSuccess) {
                 note_cuda_error((int)e);
                 return SPEC_ECUDA;
@@ -1057,7 +1125,8 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
         int dev = 0, sms = 0, per = 0;
         e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, markov_bias_tma_kernel, kMkThreads, tsmem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, markov_bias_tma_kernel<true>, kMkThreads, tsmem);
         if (e != cudaSuccess) {
             note_cuda_error((int)e);
             return SPEC_ECUDA;
@@ -1070,8 +1139,10 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
     } else {
         const int nb = (p.V + kMkCols - 1) / kMkCols, nbm = (p.V + kMmCols - 1) / kMmCols;
         for (int k = 0; k < p.K; ++k) {
-            if (mma && tgrid > 0)
-                markov_bias_tma_kernel<<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
+            if (mma && tgrid > 0 && tvec)
+                markov_bias_tma_kernel<true><<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
+            else if (mma && tgrid > 0)
+                markov_bias_tma_kernel<false><<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
             else if (mma)
                 markov_bias_mma_kernel<<<nbm, kMkThreads, msmem, stream>>>(p, k);
             else

@@ -75,6 +75,28 @@ def test_small_mixed(dt):
     assert ties <= 1
 
 
+def test_bf16_tiles_two_request_chunks():
+    """bf16 factors on the tensor-core path: B = 70 (a full chunk of 64 requests and a
+    partial one), V = 5000 (the last 64-entry tile holds 8), r = 32 (the staged product
+    tile is larger than the tile's projection rows), every fifth request greedy."""
+    m = synth.markov(11, B=70, K=2, V=5000, r=32, dtype=torch.bfloat16, greedy_every=5)
+    assert compare(run_gpu(m), run_oracle(m)) <= 1
+
+
+def test_bf16_padded_rows():
+    """bf16, base rows padded to an odd stride (4101 entries for V = 4099): the
+    epilogue's scalar path; r = 48."""
+    import speculative_decoding_verification_15_gb300 as pkg
+
+    m = synth.markov(12, B=5, K=3, V=4099, r=48, dtype=torch.bfloat16)
+    padded = torch.full((5, 3, 4101), float("nan"), dtype=torch.bfloat16)
+    padded[:, :, :4099] = m["base"]
+    out = pkg.markov_draft(padded.cuda()[:, :, :4099], m["anchor"].cuda(), m["emb"].cuda(), m["proj"].cuda(),
+                           m["temperature"].cuda(), m["seed"], m["step"])
+    torch.cuda.synchronize()
+    assert compare({k: v.cpu().numpy() for k, v in out.items()}, run_oracle(m)) <= 1
+
+
 def test_greedy_and_rank_4():
     m = synth.markov(5, B=9, K=5, V=2053, r=4, dtype=torch.float32)
     assert compare(run_gpu(m, greedy=True), run_oracle(m, greedy=True)) <= 1
