@@ -353,17 +353,26 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
                 const uint32_t a_step = 16u * (uint32_t)rs * 2u;  // the next 16-request tile
                 const uint32_t b_addr = smem_addr(sbase) + (uint32_t)l8 * blk +
                                         (uint32_t)(2 * nq + (li >> 1)) * rowbytes + (uint32_t)(li & 1) * 16u;
-#pragma unroll 2
-                for (int kk = 0; kk < r; kk += 16) {
-                    uint32_t a0[4], a1[4], bq[4];
-                    ldsm_x4(a0, a_addr + 2u * kk);
-                    ldsm_x4(a1, a_addr + a_step + 2u * kk);
-                    ldsm_x4(bq, b_addr + 2u * kk);
-                    const uint32_t bn0[2] = {bq[0], bq[1]}, bn1[2] = {bq[2], bq[3]};
-                    mma_bf16_16816(acc[0][0], a0, bn0);
-                    mma_bf16_16816(acc[0][1], a0, bn1);
-                    mma_bf16_16816(acc[1][0], a1, bn0);
-                    mma_bf16_16816(acc[1][1], a1, bn1);
+                // fragments of the next 16-wide slice of r load while this one multiplies
+                uint32_t fa[2][4], fb[2][4], fc[2][4];  // [buffer]: A tile 0, A tile 1, B
+                auto frag = [&](int kk, uint32_t (&x)[4], uint32_t (&y)[4], uint32_t (&z)[4]) {
+                    ldsm_x4(x, a_addr + 2u * kk);
+                    ldsm_x4(y, a_addr + a_step + 2u * kk);
+                    ldsm_x4(z, b_addr + 2u * kk);
+                };
+                auto mma4 = [&](const uint32_t (&x)[4], const uint32_t (&y)[4], const uint32_t (&z)[4]) {
+                    const uint32_t bn0[2] = {z[0], z[1]}, bn1[2] = {z[2], z[3]};
+                    mma_bf16_16816(acc[0][0], x, bn0);
+                    mma_bf16_16816(acc[0][1], x, bn1);
+                    mma_bf16_16816(acc[1][0], y, bn0);
+                    mma_bf16_16816(acc[1][1], y, bn1);
+                };
+                frag(0, fa[0], fb[0], fc[0]);
+                for (int kk = 0; kk < r; kk += 32) {
+                    if (kk + 16 < r) frag(kk + 16, fa[1], fb[1], fc[1]);
+                    mma4(fa[0], fb[0], fc[0]);
+                    if (kk + 32 < r) frag(kk + 32, fa[0], fb[0], fc[0]);
+                    if (kk + 16 < r) mma4(fa[1], fb[1], fc[1]);
                 }
             }
             __syncthreads();  // every warp is done with the stage's rows
