@@ -689,14 +689,19 @@ __device__ __forceinline__ int warp_first_index(const Vec (&d)[NV], const float 
 // Loads vectors t0 .. t0+NV-1 of this thread's share of a chunk (vector t of thread
 // ct is window vector ct + kCT t); entries outside the chunk read as -inf.
 template <int T0, class Vec, int NV>
-__device__ __forceinline__ void load_half(Vec (&d)[NV], const ChunkDesc &cd, int ct) {
-    const int nvec = (int)(cd.bytes >> 4);
-    const int64_t ebase = (int64_t)cd.e0 - cd.shift;
+__device__ __forceinline__ void load_half_raw(Vec (&d)[NV], const char *a0, int nvec, int ct) {
 #pragma unroll
     for (int t = 0; t < NV; ++t) {
         const int j = ct + kCT * (T0 + t);
-        d[t] = j < nvec ? Vec::load(cd.a0, j) : Vec::neg_inf();
+        d[t] = j < nvec ? Vec::load(a0, j) : Vec::neg_inf();
     }
+}
+
+// The masks of the window's edge vectors that hold entries outside [e0, e1).
+template <int T0, class Vec, int NV>
+__device__ __forceinline__ void mask_half(Vec (&d)[NV], const ChunkDesc &cd, int ct) {
+    const int nvec = (int)(cd.bytes >> 4);
+    const int64_t ebase = (int64_t)cd.e0 - cd.shift;
     if (cd.shift != 0 || ebase + (int64_t)nvec * Vec::VE != cd.e1) {
 #pragma unroll
         for (int t = 0; t < NV; ++t) {
@@ -704,6 +709,12 @@ __device__ __forceinline__ void load_half(Vec (&d)[NV], const ChunkDesc &cd, int
             if (j < nvec && (j == 0 || j == nvec - 1)) mask_vec(d[t], ebase + (int64_t)j * Vec::VE, cd.e0, cd.e1);
         }
     }
+}
+
+template <int T0, class Vec, int NV>
+__device__ __forceinline__ void load_half(Vec (&d)[NV], const ChunkDesc &cd, int ct) {
+    load_half_raw<T0>(d, cd.a0, (int)(cd.bytes >> 4), ct);
+    mask_half<T0>(d, cd, ct);
 }
 
 // A new maximum tm replaces the running one m when it is larger, or NaN; a NaN m
@@ -761,6 +772,33 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
     __shared__ ChunkDesc s_desc[3];
     int *s_rs = (int *)smem;                                   // [B+1] first main-pass row of each request
     float *s_c = (float *)(smem + sizeof(int) * (size_t)(p.B + 1));  // [B] log2(e) / T (0: greedy)
+    const Chunking ck = make_chunking(p.V, Vec::ESIZE);
+    const int ct = threadIdx.x;
+    // The first chunk's loads go out before the row scan, on the guess that the batch
+    // is padded and full (every request Kmax drafts, and T > 0 when the call samples):
+    // chunk blockIdx.x is then row r = blockIdx.x / cpr of request r / R.  Every row
+    // of the padded layout exists, so a wrong guess only reads a window that the
+    // chunk's real descriptor, once the scan has produced it, does not match; that
+    // window is then reloaded.
+    Vec a[kH], bv[kH];
+    const char *g_a0 = nullptr;
+    uint32_t g_bytes = 0u;
+    if (p.cu == nullptr && p.Kmax > 0) {
+        const int R = p.temperature ? 2 * p.Kmax : p.Kmax;
+        const int r = (int)(blockIdx.x / (uint32_t)ck.cpr), kc = (int)(blockIdx.x - (uint32_t)r * (uint32_t)ck.cpr);
+        const int b = r / R, local = r - b * R;
+        if (b < p.B) {
+            const int64_t rowbytes = p.ld_row * Vec::ESIZE;
+            const char *row = local < p.Kmax
+                                  ? (const char *)p.target + ((int64_t)b * (p.Kmax + 1) + local) * rowbytes
+                                  : (const char *)p.draft + ((int64_t)b * p.Kmax + (local - p.Kmax)) * rowbytes;
+            const ChunkWin w = chunk_window(row, Vec::ESIZE, p.V, ck, kc);
+            g_a0 = w.a0;
+            g_bytes = w.bytes;
+            load_half_raw<0>(a, g_a0, (int)(g_bytes >> 4), ct);
+            load_half_raw<kH>(bv, g_a0, (int)(g_bytes >> 4), ct);
+        }
+    }
     scan_request_rows(s_rs, p.B, p.cu, p.num_draft, p.temperature, p.Kmax);  // ends with __syncthreads
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
         const float T = p.temperature ? p.temperature[i] : 0.f;
@@ -776,10 +814,9 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
     pdl_launch_dependents();
     __syncthreads();
 
-    const Chunking ck = make_chunking(p.V, Vec::ESIZE);
     const uint32_t total = (uint32_t)s_rs[p.B] * (uint32_t)ck.cpr;  // < 2^31 (checked by the host)
     const uint32_t G = gridDim.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ct = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         s_desc[0] = chunk_desc<Vec>(p, s_rs, s_c, ck, blockIdx.x, total);
         s_desc[1] = chunk_desc<Vec>(p, s_rs, s_c, ck, G + blockIdx.x, total);
@@ -790,10 +827,14 @@ __global__ void __launch_bounds__(kCT, kMainBlocksPerSM) main_kernel(MainParams 
     uint32_t t = s_desc[0].t;
     float c = s_desc[0].c;
     int ebase = s_desc[0].e0 - s_desc[0].shift;
-    Vec a[kH], bv[kH];
     if (t < total) {
-        load_half<0>(a, s_desc[0], ct);
-        load_half<kH>(bv, s_desc[0], ct);
+        if (g_a0 == s_desc[0].a0 && g_bytes == s_desc[0].bytes) {  // the guessed window is the chunk's
+            mask_half<0>(a, s_desc[0], ct);
+            mask_half<kH>(bv, s_desc[0], ct);
+        } else {
+            load_half<0>(a, s_desc[0], ct);
+            load_half<kH>(bv, s_desc[0], ct);
+        }
     }
     int n = 0;
     while (t < total) {
