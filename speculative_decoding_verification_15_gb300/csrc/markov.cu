@@ -25,6 +25,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "spec_common.cuh"
 #include "spec_verify.h"
 
@@ -839,7 +841,11 @@ __device__ uint32_t radix_kth(const uint32_t *keys, int n, int k, uint32_t *hist
 // ranked by index.  Exact; when more than kTkGather entries pass t0 (or ncand
 // exceeds the thread count, or too many tie), the row is selected again by radix
 // over the whole row (topk_radix).
-template <int ESZ>
+// VEC: rows 16-byte aligned; the passes then read 16-byte vectors (8 bf16 or 4 fp32
+// entries, vector j of the row is thread j mod kTkThreads's), take each vector's
+// NaN-propagating maximum, and look at single entries only in the vectors whose
+// maximum reaches the bound.
+template <int ESZ, bool VEC>
 __global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovParams p, int ncand, int32_t *cands) {
     __shared__ uint32_t s_key[kTkGather];
     __shared__ int s_idx[kTkGather];
@@ -864,17 +870,41 @@ __global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovPa
         return;
     }
     constexpr int kU = 8;  // loads in flight per thread
+    using Vv = typename std::conditional<ESZ == 2, VecBF16, VecF32>::type;
+    constexpr int VE = Vv::VE;
+    const int nfull = VEC ? p.V / VE : 0;  // whole vectors; the entries after them are read one by one
     uint32_t tmax = 0u;    // below every key (0 is the key of no value: NaN maps to the top)
-    for (int v0 = tid; v0 < p.V; v0 += kTkThreads * kU) {
-        float x[kU];
+    if (VEC) {
+        float m = kNegInf;
+        bool have = false;
+        for (int j0 = tid; j0 < nfull; j0 += kTkThreads * kU) {
+            Vv x[kU];
 #pragma unroll
-        for (int e = 0; e < kU; ++e) {
-            const int v = v0 + e * kTkThreads;
-            x[e] = v < p.V ? ld_elem<ESZ>(u, v) : 0.f;
+            for (int e = 0; e < kU; ++e) {
+                const int j = j0 + e * kTkThreads;
+                x[e] = j < nfull ? Vv::load(u, j) : Vv::neg_inf();
+            }
+#pragma unroll
+            for (int e = 0; e < kU; ++e) m = max_nan_f32(m, x[e].vmax());
+            have = true;
         }
+        for (int v = nfull * VE + tid; v < p.V; v += kTkThreads) {
+            m = max_nan_f32(m, ld_elem<ESZ>(u, v));
+            have = true;
+        }
+        tmax = have ? topk_key(m) : 0u;
+    } else {
+        for (int v0 = tid; v0 < p.V; v0 += kTkThreads * kU) {
+            float x[kU];
 #pragma unroll
-        for (int e = 0; e < kU; ++e)
-            if (v0 + e * kTkThreads < p.V) tmax = max(tmax, topk_key(x[e]));
+            for (int e = 0; e < kU; ++e) {
+                const int v = v0 + e * kTkThreads;
+                x[e] = v < p.V ? ld_elem<ESZ>(u, v) : 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < kU; ++e)
+                if (v0 + e * kTkThreads < p.V) tmax = max(tmax, topk_key(x[e]));
+        }
     }
     s_key[tid] = tmax;
     if (tid == 0) {
@@ -884,10 +914,42 @@ __global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovPa
     }
     int take;
     const uint32_t t0 = radix_kth(s_key, kTkThreads, ncand, hist, s_pick, &take);
-    // pass 2: gather every entry at or above t0 (warp-aggregated appends; the loop
-    // runs on the warp's first entry, so every lane takes part in each ballot)
+    // pass 2: gather every entry at or above t0
+    if (VEC) {
+        // a vector can hold such an entry only if its maximum is NaN or >= the value
+        // of t0 (t0 == 0: every entry; t0 the NaN key: NaN entries only)
+        const uint32_t tu = (t0 & 0x80000000u) ? (t0 & 0x7fffffffu) : ~t0;
+        const float tv = __uint_as_float(tu);
+        auto keep = [&](float x, int v) {
+            const uint32_t key = topk_key(x);
+            if (key >= t0) {
+                const int slot = atomicAdd(&s_cnt[0], 1);
+                if (slot < kTkGather) {
+                    s_key[slot] = key;
+                    s_idx[slot] = v;
+                }
+            }
+        };
+        for (int j0 = tid; j0 < nfull; j0 += kTkThreads * kU) {
+            Vv x[kU];
+#pragma unroll
+            for (int e = 0; e < kU; ++e) {
+                const int j = j0 + e * kTkThreads;
+                x[e] = j < nfull ? Vv::load(u, j) : Vv::neg_inf();
+            }
+#pragma unroll
+            for (int e = 0; e < kU; ++e) {
+                const int j = j0 + e * kTkThreads;
+                const float vm = x[e].vmax();
+                const bool maybe = t0 == 0u || vm != vm || (t0 != 0xffffffffu && vm >= tv);
+                if (j < nfull && maybe)
+                    for (int q = 0; q < VE; ++q) keep(x[e].get(q), j * VE + q);
+            }
+        }
+        for (int v = nfull * VE + tid; v < p.V; v += kTkThreads) keep(ld_elem<ESZ>(u, v), v);
+    }
     const int lane = tid & 31;
-    for (int w0 = tid - lane; w0 < p.V; w0 += kTkThreads * kU) {
+    for (int w0 = tid - lane; !VEC && w0 < p.V; w0 += kTkThreads * kU) {
         const int v0 = w0 + lane;
         float x[kU];
 #pragma unroll
@@ -964,8 +1026,14 @@ __global__ void __launch_bounds__(kTkThreads) markov_topk_select_kernel(MarkovPa
 
 // One CTA per request: the positions in order; at position k the bias of each of
 // the row's ncand candidates (four threads a candidate, fp32), then the draw over
-// them.
-template <int ESZ>
+// them.  The loads a position needs that do not depend on the token drawn before it
+// (its candidates' projection rows and backbone logits) go out together with the
+// one that does (the embedding row of that token), so that a position waits for
+// one round of loads.  FAST (bf16, r a multiple of 32, 16-byte aligned factor rows):
+// a candidate's four threads each hold every fourth 16-byte vector of its
+// projection row in registers; the candidate indices of the next position are read
+// while this one is drawn.
+template <int ESZ, bool FAST>
 __global__ void __launch_bounds__(kTkDrawThreads) markov_topk_draw_kernel(MarkovParams p, int ncand,
                                                                        const int32_t *cands) {
     __shared__ float s_h[SPEC_MARKOV_MAX_RANK];
@@ -973,6 +1041,7 @@ __global__ void __launch_bounds__(kTkDrawThreads) markov_topk_draw_kernel(Markov
     __shared__ float red_s[kTkDrawThreads / 32];
     __shared__ int red_i[kTkDrawThreads / 32];
     __shared__ int s_tok;
+    constexpr int kPV = SPEC_MARKOV_MAX_RANK / 32;  // FAST: vectors a thread holds (r / 32 used)
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = kTkDrawThreads / 32;
     int prev = p.anchor[b];
@@ -983,30 +1052,85 @@ __global__ void __launch_bounds__(kTkDrawThreads) markov_topk_draw_kernel(Markov
         if (!(T >= 0.f) || isinf(T)) st = SPEC_STATUS_BAD_TEMPERATURE;
     }
     const float invT = T == 0.f ? 0.f : __fdiv_rn(1.f, T);
+    const int part = tid & 3, nv = p.r >> 5;  // FAST: this thread's vectors part, part + 4, ... (nv of them)
+    int vnext = (FAST && (tid >> 2) < ncand && p.K > 0) ? cands[(int64_t)b * p.K * ncand + (tid >> 2)] : 0;
     for (int k = 0; k < p.K && st == SPEC_STATUS_OK; ++k) {
         const int64_t row = (int64_t)b * p.K + k;
         const int32_t *cl = cands + row * ncand;
         const char *u = (const char *)p.base + row * p.ld_row * ESZ;
-        for (int j = tid; j < p.r; j += kTkDrawThreads) s_h[j] = ld_elem<ESZ>(p.emb, (int64_t)prev * p.r + j);
-        __syncthreads();
-        // four threads a candidate, each a quarter of the rank (interleaved), the
-        // loads unrolled so that they are in flight together
-        for (int c0 = 0; c0 < ncand; c0 += kTkDrawThreads / 4) {
-            const int ci = c0 + (tid >> 2), part = tid & 3;
-            float acc = 0.f;
-            int v = 0;
-            if (ci < ncand) {
-                v = cl[ci];
-                const char *pr = (const char *)p.proj + (int64_t)v * p.r * ESZ;
-#pragma unroll 8
-                for (int j = part; j < p.r; j += 4) acc = fmaf(s_h[j], ld_elem<ESZ>(pr, j), acc);
+        if (FAST) {
+            // round 0's candidate (the most common case: ncand <= kTkDrawThreads / 4):
+            // its projection vectors and backbone logit load with the embedding row
+            const int ci0 = tid >> 2;
+            const int v0 = vnext;
+            uint4 pv[kPV];
+            float u0 = 0.f;
+            if (ci0 < ncand) {
+                const uint4 *pr = reinterpret_cast<const uint4 *>((const uint16_t *)p.proj + (int64_t)v0 * p.r);
+#pragma unroll
+                for (int i = 0; i < kPV; ++i)
+                    if (i < nv) pv[i] = __ldg(pr + part + 4 * i);
+                if (part == 0) u0 = ld_elem<ESZ>(u, v0);
             }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (ci < ncand && part == 0) {
-                const float z = ld_elem<ESZ>(u, v) + acc;
-                s_z[ci] = z;
-                if (p.z) p.z[row * p.V + v] = z;
+            for (int j = tid; j < p.r; j += kTkDrawThreads) s_h[j] = ld_elem<ESZ>(p.emb, (int64_t)prev * p.r + j);
+            __syncthreads();
+            for (int c0 = 0; c0 < ncand; c0 += kTkDrawThreads / 4) {
+                const int ci = c0 + (tid >> 2);
+                int v = v0;
+                if (c0 > 0 && ci < ncand) {
+                    v = cl[ci];
+                    const uint4 *pr = reinterpret_cast<const uint4 *>((const uint16_t *)p.proj + (int64_t)v * p.r);
+#pragma unroll
+                    for (int i = 0; i < kPV; ++i)
+                        if (i < nv) pv[i] = __ldg(pr + part + 4 * i);
+                    if (part == 0) u0 = ld_elem<ESZ>(u, v);
+                }
+                float acc = 0.f;
+                if (ci < ncand) {
+#pragma unroll
+                    for (int i = 0; i < kPV; ++i) {
+                        if (i >= nv) break;
+                        const float *h = s_h + 8 * (part + 4 * i);
+                        const uint32_t w[4] = {pv[i].x, pv[i].y, pv[i].z, pv[i].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc = fmaf(h[2 * e], bf16_lo(w[e]), acc);
+                            acc = fmaf(h[2 * e + 1], bf16_hi(w[e]), acc);
+                        }
+                    }
+                }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                if (ci < ncand && part == 0) {
+                    const float z = u0 + acc;
+                    s_z[ci] = z;
+                    if (p.z) p.z[row * p.V + v] = z;
+                }
+            }
+            // the next position's first candidates, read while this one is drawn
+            if (k + 1 < p.K && ci0 < ncand) vnext = cl[(int64_t)ncand + ci0];
+        } else {
+            for (int j = tid; j < p.r; j += kTkDrawThreads) s_h[j] = ld_elem<ESZ>(p.emb, (int64_t)prev * p.r + j);
+            __syncthreads();
+            // four threads a candidate, each a quarter of the rank (interleaved), the
+            // loads unrolled so that they are in flight together
+            for (int c0 = 0; c0 < ncand; c0 += kTkDrawThreads / 4) {
+                const int ci = c0 + (tid >> 2);
+                float acc = 0.f;
+                int v = 0;
+                if (ci < ncand) {
+                    v = cl[ci];
+                    const char *pr = (const char *)p.proj + (int64_t)v * p.r * ESZ;
+#pragma unroll 8
+                    for (int j = part; j < p.r; j += 4) acc = fmaf(s_h[j], ld_elem<ESZ>(pr, j), acc);
+                }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                if (ci < ncand && part == 0) {
+                    const float z = ld_elem<ESZ>(u, v) + acc;
+                    s_z[ci] = z;
+                    if (p.z) p.z[row * p.V + v] = z;
+                }
             }
         }
         __syncthreads();
@@ -1075,14 +1199,26 @@ cudaError_t launch_sample(const MarkovParams &p, int k, cudaStream_t stream) {
 }
 
 int markov_topk_impl(const MarkovParams &p, int ncand, int32_t *cands, cudaStream_t stream) {
+    const int esz = p.dtype == SPEC_BF16 ? 2 : 4;
+    const bool tvec = ((uintptr_t)p.base % 16) == 0 && ((p.ld_row * esz) % 16) == 0;
     if (p.K == 0) {
         markov_status_kernel<<<(p.B + 255) / 256, 256, 0, stream>>>(p);
     } else if (p.dtype == SPEC_BF16) {
-        markov_topk_select_kernel<2><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
-        markov_topk_draw_kernel<2><<<p.B, kTkDrawThreads, 0, stream>>>(p, ncand, cands);
+        if (tvec)
+            markov_topk_select_kernel<2, true><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
+        else
+            markov_topk_select_kernel<2, false><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
+        const bool fast = (p.r % 32) == 0 && ((uintptr_t)p.proj % 16) == 0;
+        if (fast)
+            markov_topk_draw_kernel<2, true><<<p.B, kTkDrawThreads, 0, stream>>>(p, ncand, cands);
+        else
+            markov_topk_draw_kernel<2, false><<<p.B, kTkDrawThreads, 0, stream>>>(p, ncand, cands);
     } else {
-        markov_topk_select_kernel<4><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
-        markov_topk_draw_kernel<4><<<p.B, kTkDrawThreads, 0, stream>>>(p, ncand, cands);
+        if (tvec)
+            markov_topk_select_kernel<4, true><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
+        else
+            markov_topk_select_kernel<4, false><<<p.B * p.K, kTkThreads, 0, stream>>>(p, ncand, cands);
+        markov_topk_draw_kernel<4, false><<<p.B, kTkDrawThreads, 0, stream>>>(p, ncand, cands);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
