@@ -615,6 +615,73 @@ def run_ours(args) -> None:
         torch.distributed.destroy_process_group()
 
 
+def run_profile_case(args) -> None:
+    """One workload's calls, warm-up and steps alike, with L2 flushed before each and
+    nothing timed or printed: the command that the ncu summaries under profiles/
+    capture (a few launches of one kernel, on the same inputs as the bench)."""
+    import torch
+
+    import __graft_entry__
+    import synth
+
+    __graft_entry__.build()
+    import speculative_decoding_verification_15_gb300 as pkg
+    from speculative_decoding_verification_15_gb300 import binding
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    case = args.profile_case
+    if case in ("main", "ragged", "stress"):
+        if case == "main":
+            batch = synth.main(0, device=dev)
+        elif case == "stress":
+            batch = synth.stress(0, device=dev)
+        else:
+            sch = synth.ragged_schedule_inputs(0)
+            L = torch.empty(sch["B"], dtype=torch.int32, device=dev)
+            info = torch.empty(3, dtype=torch.float64, device=dev)
+            binding.spec_schedule_verify_len(sch["conf"].to(dev), None, sch["step_time_us"].to(dev), sch["budget"],
+                                             sch["min_len"], L, info, stream)
+            batch = synth.ragged(0, num_draft=[int(v) for v in L.tolist()], device=dev)
+        B, K, V = batch["B"], batch["K"], batch["V"]
+        t, d = batch["target"].to(dev), batch["draft"].to(dev)
+        x, T = batch["draft_tokens"].to(dev), batch["temperature"].to(dev)
+        nd = batch.get("num_draft")
+        nd = None if nd is None else nd.to(dev)
+        tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        st = torch.empty(B, dtype=torch.int32, device=dev)
+        pp = torch.empty((B, K), dtype=torch.float32, device=dev)
+        qq = torch.empty((B, K), dtype=torch.float32, device=dev)
+        ws = pkg.workspace(dev, binding.spec_verify_workspace_size(B, K, V, binding._dtype_code(t)))
+
+        def call(i):
+            binding.spec_verify_sample(t, d, x, nd, T, 3, i, tok, acc, pp, qq, st, ws, stream)
+    else:
+        mk = synth.markov(0, dtype=torch.bfloat16)
+        m = {n: mk[n].to(dev) for n in ("base", "anchor", "emb", "proj", "temperature")}
+        B, K, V = mk["B"], mk["K"], mk["V"]
+        tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+        z = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+        st = torch.empty(B, dtype=torch.int32, device=dev)
+        tk_ws = torch.empty(binding.spec_markov_topk_workspace_size(B, K, V, 64), dtype=torch.uint8, device=dev)
+
+        def call(i):
+            if case == "markov":
+                binding.spec_markov_draft(m["base"], m["anchor"], m["emb"], m["proj"], m["temperature"], 6, i, tok,
+                                          z, st, stream)
+            else:
+                binding.spec_markov_draft_topk(m["base"], m["anchor"], m["emb"], m["proj"], m["temperature"], 6, i,
+                                               64, tok, z, st, tk_ws, stream)
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        call(i)
+    torch.cuda.synchronize()
+    assert int((st != 0).sum()) == 0, "a request reported a non-zero status"
+
+
 def _host_batch(vb, n: int | None = None) -> dict:
     """A host copy of the first n requests of a device batch, for the oracle."""
     n = vb.B if n is None else n
@@ -628,7 +695,12 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--profile-case", default=None, choices=["main", "ragged", "stress", "markov", "markov_topk"],
+                    help="run one workload's calls untimed (the target of an ncu capture) and print nothing")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
