@@ -264,23 +264,6 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
     bool pend[2] = {false, false};
     bool failed = false;
     for (int b0 = 0; b0 < p.B; b0 += kMmReqs) {
-        if (tid < kMmReqs) {
-            const int b = b0 + tid;
-            int ok = 0;
-            if (b < p.B) {
-                const int prev = k == 0 ? p.anchor[b] : p.tokens[(int64_t)b * p.K + k - 1];
-                ok = (prev >= 0 && prev < p.V) ? prev + 1 : 0;  // 1 + the row to gather, 0: none
-            }
-            okv[tid] = ok;
-        }
-        __syncthreads();
-        for (int i = tid; i < kMmReqs * vpr; i += kMkThreads) {
-            const int m = i / vpr, q = i - m * vpr;
-            const int ok = okv[m];
-            uint4 x = make_uint4(0, 0, 0, 0);
-            if (ok) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.emb + (int64_t)(ok - 1) * r + 8 * q);
-            *reinterpret_cast<uint4 *>(Hs + m * rs + 8 * q) = x;
-        }
         // tile t into stage st: warp 0 registers the bytes, lanes 0..7 copy a block each
         auto issue = [&](int t, int st) {
             if (failed || t >= ntiles) return;
@@ -295,9 +278,28 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
                          (const uint16_t *)p.proj + (int64_t)(v0 + 8 * lane) * r, (uint32_t)rows * rowbytes,
                          &s_bar[st]);
         };
+        // the first two tiles' copies go out before the embedding rows are gathered
+        // (the stages are free: no copy is pending between chunks of requests)
         int i = 0;
         issue(blockIdx.x, 0);
         issue(blockIdx.x + gridDim.x, 1);
+        if (tid < kMmReqs) {
+            const int b = b0 + tid;
+            int ok = 0;
+            if (b < p.B) {
+                const int prev = k == 0 ? p.anchor[b] : p.tokens[(int64_t)b * p.K + k - 1];
+                ok = (prev >= 0 && prev < p.V) ? prev + 1 : 0;  // 1 + the row to gather, 0: none
+            }
+            okv[tid] = ok;
+        }
+        __syncthreads();
+        for (int j = tid; j < kMmReqs * vpr; j += kMkThreads) {
+            const int m = j / vpr, q = j - m * vpr;
+            const int ok = okv[m];
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (ok) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.emb + (int64_t)(ok - 1) * r + 8 * q);
+            *reinterpret_cast<uint4 *>(Hs + m * rs + 8 * q) = x;
+        }
         __syncthreads();  // H and okv are in
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             const int st = i & 1;
@@ -420,6 +422,277 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
         }
         // the next chunk of requests rewrites H and okv; no copy is pending here
         __syncthreads();
+    }
+}
+
+// The same products with the work split by roles (one CTA per SM, 13 warps): warp 12
+// issues the bulk copies into kWsStages stages; warps 0..7 multiply, in two groups of
+// four that take alternate tiles (warp (group, w) forms requests 32 (w / 2) .. +31 and
+// n-blocks 4 (w % 2) .. +3: eight independent accumulators), and write the products
+// into the group's staged tile; warps 8..11 read a staged tile with the backbone
+// logits (loaded three tiles ahead) and write z.  The roles meet on mbarriers (stage full / stage
+// released, tile staged / tile written back), so the tensor cores work on the next
+// tile while the previous one is written out and the tile after it is copied in.
+// Every wait is bounded; after one gives up the roles stop waiting, the tiles not
+// multiplied are written as NaN (status 4), and the copies still in flight are
+// waited for (bounded) before the CTA leaves.
+constexpr int kWsStages = 4;
+constexpr int kWsMma = 8;  // multiplying warps
+constexpr int kWsEpi = 4;  // write-back warps
+constexpr int kWsThreads = 32 * (kWsMma + kWsEpi + 1);
+
+__host__ __device__ inline size_t ws_stage_bytes(int r) { return (size_t)8 * (16 * (size_t)r + 16); }
+__host__ __device__ inline size_t ws_smem_bytes(int r) {
+    return sizeof(uint16_t) * (size_t)kMmReqs * (r + 8) + kWsStages * ws_stage_bytes(r) +
+           2 * sizeof(float) * (size_t)kMmReqs * kCtStride + sizeof(int) * kMmReqs;
+}
+
+__device__ __forceinline__ bool ws_failed(const int *f) { return *(volatile const int *)f != 0; }
+
+template <bool VEC>
+__global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovParams p, int k) {
+    extern __shared__ __align__(128) unsigned char wsm[];
+    __shared__ __align__(8) uint64_t s_full[kWsStages], s_empty[kWsStages], s_cfull[2], s_cempty[2];
+    __shared__ int s_fail;
+    __shared__ uint32_t s_cons[kWsStages];  // copies of each stage the multiplying warps have waited for
+    const int r = p.r, rs = r + 8;
+    const size_t sb = ws_stage_bytes(r);
+    const uint32_t blk = 16u * (uint32_t)r + 16u;
+    const uint32_t rowbytes = (uint32_t)r * 2u;
+    uint16_t *Hs = reinterpret_cast<uint16_t *>(wsm);                          // [64][rs]
+    unsigned char *stages = wsm + sizeof(uint16_t) * (size_t)kMmReqs * rs;      // [kWsStages][sb]
+    float *Cb = reinterpret_cast<float *>(stages + kWsStages * sb);            // [2][64][kCtStride]
+    int *okv = reinterpret_cast<int *>(Cb + 2 * kMmReqs * kCtStride);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ntiles = (p.V + kMmCols - 1) / kMmCols;
+    const int nmine = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int vpr = r >> 3;
+    if (tid == 0) {
+        for (int s2 = 0; s2 < kWsStages; ++s2) {
+            mbar_init(&s_full[s2], 1);
+            mbar_init(&s_empty[s2], kWsMma / 2);
+            s_cons[s2] = 0u;
+        }
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(&s_cfull[c], kWsMma / 2);
+            mbar_init(&s_cempty[c], kWsEpi);
+        }
+        s_fail = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    uint32_t issued[kWsStages] = {};  // producer: copies issued into each stage
+    int gi = 0;  // tiles of this CTA before the current chunk of requests (phase bookkeeping)
+    for (int b0 = 0; b0 < p.B; b0 += kMmReqs) {
+        // producer: one tile's copies into stage gt % kWsStages, once the multiplying
+        // warps have released the stage's previous tile
+        auto produce = [&](int i) {
+            const int gt = gi + i, st = gt % kWsStages;
+            bool ok = !ws_failed(&s_fail);
+            if (ok && gt >= kWsStages && lane == 0) ok = mbar_wait(&s_empty[st], (uint32_t)((gt / kWsStages - 1) & 1), kWaitNs);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) s_fail = 1;
+                return;
+            }
+            const int t = (int)blockIdx.x + i * (int)gridDim.x;
+            const int v0 = t * kMmCols, nc = min(kMmCols, p.V - v0);
+            if (lane == 0) mbar_arrive_expect_tx(&s_full[st], (uint32_t)nc * rowbytes);
+            __syncwarp();
+            const int rows = min(8, nc - 8 * lane);
+            if (lane < 8 && rows > 0)
+                bulk_g2s(stages + (size_t)st * sb + (size_t)lane * blk,
+                         (const uint16_t *)p.proj + (int64_t)(v0 + 8 * lane) * r, (uint32_t)rows * rowbytes,
+                         &s_full[st]);
+            issued[st] += 1u;
+        };
+        const int first = min(nmine, kWsStages);
+        if (warp == kWsMma + kWsEpi)
+            for (int i = 0; i < first; ++i) produce(i);
+        if (tid < kMmReqs) {
+            const int b = b0 + tid;
+            int ok = 0;
+            if (b < p.B) {
+                const int prev = k == 0 ? p.anchor[b] : p.tokens[(int64_t)b * p.K + k - 1];
+                ok = (prev >= 0 && prev < p.V) ? prev + 1 : 0;  // 1 + the row to gather, 0: none
+            }
+            okv[tid] = ok;
+        }
+        __syncthreads();
+        for (int j = tid; j < kMmReqs * vpr; j += kWsThreads) {
+            const int m = j / vpr, q = j - m * vpr;
+            const int ok = okv[m];
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (ok) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.emb + (int64_t)(ok - 1) * r + 8 * q);
+            *reinterpret_cast<uint4 *>(Hs + m * rs + 8 * q) = x;
+        }
+        __syncthreads();  // H and okv are in
+        if (warp < kWsMma) {
+            // ---- multiply: warps 4 grp .. 4 grp + 3 take the tiles gt with gt % 2 == grp;
+            // warp (grp, wg) forms requests 32 (wg / 2) .. +31 and n-blocks 4 (wg % 2) .. +3
+            // (eight independent accumulators a warp)
+            const int grp = warp >> 2, wg = warp & 3, mh = wg >> 1, nh = wg & 1;
+            const int li = lane >> 3, l8 = lane & 7, g = lane >> 2, t4 = lane & 3;
+            const uint32_t a_addr = smem_addr(Hs + (size_t)(32 * mh + (li & 1) * 8 + l8) * rs + (li >> 1) * 8);
+            const uint32_t a_step = 16u * (uint32_t)rs * 2u;
+            for (int i = (grp - gi) & 1; i < nmine; i += 2) {
+                const int gt = gi + i, st = gt % kWsStages, cb = gt & 1;
+                if (ws_failed(&s_fail)) break;
+                if (!mbar_wait(&s_full[st], (uint32_t)((gt / kWsStages) & 1), kWaitNs)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (wg == 0 && lane == 0) atomicAdd(&s_cons[st], 1u);
+                float acc[2][4][4];
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[a][c][e] = 0.f;
+                // B: n-blocks 4 nh + 2 hb + (li >> 1), k half (li & 1), for hb = 0, 1
+                const uint32_t b_addr = smem_addr(stages + (size_t)st * sb) + (uint32_t)l8 * blk +
+                                        (uint32_t)(4 * nh + (li >> 1)) * rowbytes + (uint32_t)(li & 1) * 16u;
+                const uint32_t b_step = 2u * rowbytes;  // the next two n-blocks
+                uint32_t fa[2][4], fb[2][4], fc[2][4], fd[2][4];
+                auto frag = [&](int kk, int q) {
+                    ldsm_x4(fa[q], a_addr + 2u * kk);
+                    ldsm_x4(fb[q], a_addr + a_step + 2u * kk);
+                    ldsm_x4(fc[q], b_addr + 2u * kk);
+                    ldsm_x4(fd[q], b_addr + b_step + 2u * kk);
+                };
+                auto mma8 = [&](int q) {
+                    const uint32_t bn[4][2] = {{fc[q][0], fc[q][1]}, {fc[q][2], fc[q][3]},
+                                               {fd[q][0], fd[q][1]}, {fd[q][2], fd[q][3]}};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        mma_bf16_16816(acc[0][c], fa[q], bn[c]);
+                        mma_bf16_16816(acc[1][c], fb[q], bn[c]);
+                    }
+                };
+                frag(0, 0);
+                for (int kk = 0; kk < r; kk += 32) {
+                    if (kk + 16 < r) frag(kk + 16, 1);
+                    mma8(0);
+                    if (kk + 32 < r) frag(kk + 32, 0);
+                    if (kk + 16 < r) mma8(1);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[st]);  // this warp is done with the stage
+                if (gt >= 2 && !mbar_wait(&s_cempty[cb], (uint32_t)((gt / 2 - 1) & 1), kWaitNs)) {
+                    s_fail = 1;
+                    break;
+                }
+                float *Cs = Cb + (size_t)cb * kMmReqs * kCtStride;
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int m = 32 * mh + 16 * a + g, beta = 4 * nh + c;
+                        Cs[m * kCtStride + 16 * t4 + beta] = acc[a][c][0];
+                        Cs[m * kCtStride + 16 * t4 + 8 + beta] = acc[a][c][1];
+                        Cs[(m + 8) * kCtStride + 16 * t4 + beta] = acc[a][c][2];
+                        Cs[(m + 8) * kCtStride + 16 * t4 + 8 + beta] = acc[a][c][3];
+                    }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_cfull[cb]);
+            }
+        } else if (warp < kWsMma + kWsEpi) {
+            // ---- write back: 128 threads, request row 8 pass + e / 16, entries 4 (e % 16) .. +3;
+            // the backbone logits load three tiles ahead of their use
+            const int e = tid - 32 * kWsMma, eq = 4 * (e & 15);
+            auto load_u = [&](int i, uint2 (&upk)[8]) {
+                const int t = (int)blockIdx.x + i * (int)gridDim.x;
+                const int v0 = t * kMmCols, ncol = min(kMmCols, p.V - v0);
+#pragma unroll
+                for (int ps = 0; ps < 8; ++ps) {
+                    const int m = 8 * ps + (e >> 4), b = b0 + m;
+                    upk[ps] = make_uint2(0u, 0u);
+                    if (i < nmine && b < p.B && eq < ncol) {
+                        const unsigned short *ur =
+                            (const unsigned short *)p.base + ((int64_t)b * p.K + k) * p.ld_row + v0 + eq;
+                        if (VEC && eq + 4 <= ncol) {
+                            upk[ps] = __ldg(reinterpret_cast<const uint2 *>(ur));
+                        } else {
+                            uint32_t h[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) h[q] = eq + q < ncol ? (uint32_t)__ldg(ur + q) : 0u;
+                            upk[ps] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+                        }
+                    }
+                }
+            };
+            uint2 u1[8], u2[8], u3[8];  // tiles i + 1 .. i + 3, loaded three tiles ahead
+            load_u(0, u1);
+            load_u(1, u2);
+            load_u(2, u3);
+            for (int i = 0; i < nmine; ++i) {
+                const int gt = gi + i, cb = gt & 1;
+                const int t = (int)blockIdx.x + i * (int)gridDim.x;
+                const int v0 = t * kMmCols, ncol = min(kMmCols, p.V - v0);
+                uint2 upk[8];
+#pragma unroll
+                for (int ps = 0; ps < 8; ++ps) {
+                    upk[ps] = u1[ps];
+                    u1[ps] = u2[ps];
+                    u2[ps] = u3[ps];
+                }
+                load_u(i + 3, u3);
+                bool ok = !ws_failed(&s_fail);
+                if (ok && !mbar_wait(&s_cfull[cb], (uint32_t)((gt / 2) & 1), kWaitNs)) {
+                    s_fail = 1;
+                    ok = false;
+                }
+                const float *Cs = Cb + (size_t)cb * kMmReqs * kCtStride;
+#pragma unroll
+                for (int ps = 0; ps < 8; ++ps) {
+                    const int m = 8 * ps + (e >> 4), b = b0 + m;
+                    if (b >= p.B || eq >= ncol) continue;
+                    const bool good = ok && okv[m] != 0;
+                    const float4 cv = good ? *reinterpret_cast<const float4 *>(Cs + m * kCtStride + eq)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const uint32_t w[2] = {upk[ps].x, upk[ps].y};
+                    const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
+                    float o[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t h = (q & 1) ? (w[q >> 1] & 0xffff0000u) : (w[q >> 1] << 16);
+                        o[q] = good ? __uint_as_float(h) + cc[q] : __int_as_float(0x7fc00000);
+                    }
+                    float *zp = p.z + ((int64_t)b * p.K + k) * p.V + v0 + eq;
+                    if (VEC && eq + 4 <= ncol) {
+                        *reinterpret_cast<float4 *>(zp) = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (eq + q < ncol) zp[q] = o[q];
+                    }
+                }
+                __syncwarp();
+                if (ok && lane == 0) mbar_arrive(&s_cempty[cb]);
+            }
+        } else {
+            // ---- copies of the remaining tiles
+            for (int i = first; i < nmine; ++i) produce(i);
+        }
+        __syncthreads();
+        // after a give-up: the copies issued but not waited for still land; wait for
+        // them (bounded) before the shared memory is reused or the CTA leaves
+        if (tid == 32 * (kWsMma + kWsEpi) && ws_failed(&s_fail))
+            for (int s2 = 0; s2 < kWsStages; ++s2)
+                for (uint32_t ph = s_cons[s2]; ph < issued[s2]; ++ph) mbar_wait(&s_full[s2], ph & 1u, kWaitNs);
+        __syncthreads();
+        gi += nmine;
+        if (ws_failed(&s_fail)) {
+            // the rest of the requests' rows: NaN (their requests report status 4)
+            for (int bb = b0 + kMmReqs; bb < p.B; ++bb)
+                for (int t = (int)blockIdx.x; t < ntiles; t += (int)gridDim.x) {
+                    const int v0 = t * kMmCols, ncol = min(kMmCols, p.V - v0);
+                    for (int q = tid; q < ncol; q += kWsThreads)
+                        p.z[((int64_t)bb * p.K + k) * p.V + v0 + q] = __int_as_float(0x7fc00000);
+                }
+            break;
+        }
     }
 }
 
@@ -1279,12 +1552,33 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
         const int ntiles = (p.V + kMmCols - 1) / kMmCols;
         tgrid = per > 0 ? min(ntiles, per * sms) : 0;
     }
+    // the role-split kernel where its stages and two staged tiles fit (r <= 256)
+    const size_t wsmem = ws_smem_bytes(p.r);
+    int wgrid = 0;
+    if (mma && wsmem <= 227 * 1024) {
+        e = cudaFuncSetAttribute(markov_bias_ws_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(markov_bias_ws_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)wsmem);
+        int dev = 0, sms = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) {
+            note_cuda_error((int)e);
+            return SPEC_ECUDA;
+        }
+        wgrid = min((p.V + kMmCols - 1) / kMmCols, sms);
+    }
     if (p.K == 0) {
         markov_status_kernel<<<(p.B + 255) / 256, 256, 0, stream>>>(p);
     } else {
         const int nb = (p.V + kMkCols - 1) / kMkCols, nbm = (p.V + kMmCols - 1) / kMmCols;
         for (int k = 0; k < p.K; ++k) {
-            if (mma && tgrid > 0 && tvec)
+            if (wgrid > 0 && tvec)
+                markov_bias_ws_kernel<true><<<wgrid, kWsThreads, wsmem, stream>>>(p, k);
+            else if (wgrid > 0)
+                markov_bias_ws_kernel<false><<<wgrid, kWsThreads, wsmem, stream>>>(p, k);
+            else if (mma && tgrid > 0 && tvec)
                 markov_bias_tma_kernel<true><<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
             else if (mma && tgrid > 0)
                 markov_bias_tma_kernel<false><<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
