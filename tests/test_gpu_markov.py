@@ -83,6 +83,13 @@ def test_bf16_tiles_two_request_chunks():
     assert compare(run_gpu(m), run_oracle(m)) <= 1
 
 
+def test_bf16_rank_512():
+    """bf16 at the header's largest rank (r = 512): the two-CTA bias kernel (the
+    role-split one serves r <= 256), B = 66 (two request chunks), V = 3001."""
+    m = synth.markov(13, B=66, K=2, V=3001, r=512, dtype=torch.bfloat16, greedy_every=4)
+    assert compare(run_gpu(m), run_oracle(m)) <= 1
+
+
 def test_bf16_padded_rows():
     """bf16, base rows padded to an odd stride (4101 entries for V = 4099): the
     epilogue's scalar path; r = 48."""
