@@ -11,17 +11,18 @@
 //          library's Philox stream with purpose 3 at row k.
 //
 // Kernels per position (2 K launches per call, no host synchronisation):
-//  markov_bias_kernel    one CTA per 32 vocabulary entries: stages those entries'
-//                        projection rows in shared memory once, then one warp per
-//                        request computes the 32 dot products with the request's
-//                        embedding row (fp32, products of the stored values exact)
-//                        and writes z.  Every projection row is read once per
-//                        position (from L2 after the first position: r x V x 2 B =
-//                        78 MB at V = 151936, r = 256 in bf16, fits the 129 MB L2).
+//  bias                  z for every request and entry.  bf16 factors (rank a
+//                        multiple of 16): the tensor cores, markov_bias_ws_kernel
+//                        (r <= 256, one CTA per SM split by role) or
+//                        markov_bias_tma_kernel (two CTAs per SM); otherwise
+//                        markov_bias_kernel, fp32 dot products, one CTA per 32
+//                        entries.  Every projection row is read once per position.
 //  markov_sample_kernel  one cluster of 4 CTAs per request, each over a quarter of
 //                        the row: the pruned exact Gumbel-max (or the argmax) over
 //                        z_k, status, and the token that the next position's bias
 //                        uses.
+// Top-K drafting: markov_topk_select_kernel (every row's candidates, one launch),
+// then markov_topk_draw_kernel (the walk over the positions, a CTA per request).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -63,6 +64,10 @@ __host__ __device__ inline size_t bias_smem_bytes(int r) {
     return sizeof(float) * ((size_t)kMkCols * (r + 4) + (size_t)kMkWarps * r);
 }
 
+// fp32 (or unaligned / odd-rank bf16) factors: one CTA per 32 vocabulary entries
+// stages those entries' projection rows in shared memory once, then one warp per
+// request computes the 32 dot products with the request's embedding row (fp32; the
+// products of the stored values are exact) and writes z.
 __global__ void __launch_bounds__(kMkThreads) markov_bias_kernel(MarkovParams p, int k) {
     extern __shared__ __align__(16) float msm[];
     const int rs = p.r + 4;
@@ -107,18 +112,10 @@ __global__ void __launch_bounds__(kMkThreads) markov_bias_kernel(MarkovParams p,
 }
 
 // bf16 factors: the same z through bf16 tensor-core products with fp32 accumulation
-// (mma.sync m16n8k16; the products of bf16 values are exact).  One CTA per 64
-// vocabulary entries, all requests in chunks of 64: the chunk's embedding rows H
-// [64][r] and the entries' projection rows P [64][r] sit in shared memory as bf16
-// with rows padded by 8 elements (the fragment loads of a warp then hit 32
-// different banks).  Warp w owns entries 8w .. 8w+7 and all four 16-request
-// tiles; per 16-wide slice of r it loads one B fragment and four A fragments.
+// (mma.sync m16n8k16; the products of bf16 values are exact), over tiles of 64
+// vocabulary entries and chunks of 64 requests.
 constexpr int kMmCols = 64;
 constexpr int kMmReqs = 64;
-
-__host__ __device__ inline size_t mma_smem_bytes(int r) {
-    return sizeof(uint16_t) * (size_t)(kMmCols + kMmReqs) * (r + 8) + sizeof(int) * kMmReqs;
-}
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile(
@@ -126,82 +123,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-__global__ void __launch_bounds__(kMkThreads) markov_bias_mma_kernel(MarkovParams p, int k) {
-    extern __shared__ __align__(16) uint16_t mms[];
-    const int rs = p.r + 8;  // row stride in elements (16-byte rows)
-    uint16_t *Ps = mms;                        // [64 entries][rs]
-    uint16_t *Hs = mms + (size_t)kMmCols * rs;  // [64 requests][rs]
-    int *okv = reinterpret_cast<int *>(Hs + (size_t)kMmReqs * rs);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int v0 = blockIdx.x * kMmCols;
-    const int ncol = min(kMmCols, p.V - v0);
-    const int vpr = p.r >> 3;  // 16-byte vectors per row
-    for (int i = tid; i < kMmCols * vpr; i += kMkThreads) {
-        const int c = i / vpr, q = i - c * vpr;
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (c < ncol) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.proj + (int64_t)(v0 + c) * p.r + 8 * q);
-        *reinterpret_cast<uint4 *>(Ps + c * rs + 8 * q) = x;
-    }
-    const int g = lane >> 2, t2 = (lane & 3) * 2;
-    for (int b0 = 0; b0 < p.B; b0 += kMmReqs) {
-        __syncthreads();  // Hs and okv of the previous chunk are no longer read
-        if (tid < kMmReqs) {
-            const int b = b0 + tid;
-            int ok = 0;
-            if (b < p.B) {
-                const int prev = k == 0 ? p.anchor[b] : p.tokens[(int64_t)b * p.K + k - 1];
-                ok = (prev >= 0 && prev < p.V) ? prev + 1 : 0;  // 1 + the row to gather, 0: none
-            }
-            okv[tid] = ok;
-        }
-        __syncthreads();
-        for (int i = tid; i < kMmReqs * vpr; i += kMkThreads) {
-            const int m = i / vpr, q = i - m * vpr;
-            const int ok = okv[m];
-            uint4 x = make_uint4(0, 0, 0, 0);
-            if (ok) x = *reinterpret_cast<const uint4 *>((const uint16_t *)p.emb + (int64_t)(ok - 1) * p.r + 8 * q);
-            *reinterpret_cast<uint4 *>(Hs + m * rs + 8 * q) = x;
-        }
-        __syncthreads();
-        float acc[4][4];
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-        const uint16_t *pb = Ps + (warp * 8 + g) * rs + t2;
-        for (int kk = 0; kk < p.r; kk += 16) {
-            uint32_t bf[2];
-            bf[0] = *reinterpret_cast<const uint32_t *>(pb + kk);
-            bf[1] = *reinterpret_cast<const uint32_t *>(pb + kk + 8);
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                const uint16_t *pa = Hs + (mt * 16 + g) * rs + kk + t2;
-                uint32_t af[4];
-                af[0] = *reinterpret_cast<const uint32_t *>(pa);
-                af[1] = *reinterpret_cast<const uint32_t *>(pa + 8 * rs);
-                af[2] = *reinterpret_cast<const uint32_t *>(pa + 8);
-                af[3] = *reinterpret_cast<const uint32_t *>(pa + 8 * rs + 8);
-                mma_bf16_16816(acc[mt], af, bf);
-            }
-        }
-        // C fragment: rows (requests) g and g + 8 of each tile, entries t2, t2 + 1 of the warp's 8
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = mt * 16 + g + (e >= 2 ? 8 : 0);
-                const int n = warp * 8 + t2 + (e & 1);
-                const int b = b0 + m;
-                if (b < p.B && n < ncol) {
-                    const int64_t row = (int64_t)b * p.K + k;
-                    const int v = v0 + n;
-                    p.z[row * p.V + v] = okv[m] ? load_logit(p.base, p.dtype, row * p.ld_row + v) + acc[mt][e]
-                                                : __int_as_float(0x7fc00000);
-                }
-            }
-    }
 }
 
 // bf16 factors, the same products with the projection rows streamed: a persistent
@@ -1514,14 +1435,6 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
     // bf16 factors with 16-byte rows (r a multiple of 16, aligned bases): tensor cores
     const bool mma = p.dtype == SPEC_BF16 && (p.r % 16) == 0 && ((uintptr_t)p.emb % 16) == 0 &&
                      ((uintptr_t)p.proj % 16) == 0;
-    const size_t msmem = mma_smem_bytes(p.r);
-    if (mma && msmem > 48 * 1024) {
-        e = cudaFuncSetAttribute(markov_bias_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
-        if (e != cudaSuccess) {
-            note_cuda_error((int)e);
-            return SPEC_ECUDA;
-        }
-    }
     // bf16 factors streamed by bulk copies: a persistent grid of as many CTAs as fit;
     // vector accesses in the epilogue where U and z rows allow them
     const size_t tsmem = tma_smem_bytes(p.r);
@@ -1572,7 +1485,7 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
     if (p.K == 0) {
         markov_status_kernel<<<(p.B + 255) / 256, 256, 0, stream>>>(p);
     } else {
-        const int nb = (p.V + kMkCols - 1) / kMkCols, nbm = (p.V + kMmCols - 1) / kMmCols;
+        const int nb = (p.V + kMkCols - 1) / kMkCols;
         for (int k = 0; k < p.K; ++k) {
             if (wgrid > 0 && tvec)
                 markov_bias_ws_kernel<true><<<wgrid, kWsThreads, wsmem, stream>>>(p, k);
@@ -1582,8 +1495,6 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
                 markov_bias_tma_kernel<true><<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
             else if (mma && tgrid > 0)
                 markov_bias_tma_kernel<false><<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
-            else if (mma)
-                markov_bias_mma_kernel<<<nbm, kMkThreads, msmem, stream>>>(p, k);
             else
                 markov_bias_kernel<<<nb, kMkThreads, smem, stream>>>(p, k);
             e = launch_sample(p, k, stream);
