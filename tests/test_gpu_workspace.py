@@ -134,3 +134,20 @@ def test_one_workspace_alternates_between_the_two_paths():
         compare_sample(_outs_np(outs), run_oracle_sample(batch, 3, 1), batch["temperature"].numpy())
         assert (outs["st"].cpu().numpy() == 0).all()
         assert int(ws[:4].view(torch.int32).item()) == 0  # the shared chunk counter
+
+
+@pytest.mark.parametrize("offset", [0, -1])
+def test_batch_at_the_sm_count(offset):
+    """B = the SM count runs the single kernel with two commit items a request
+    (Q = 2 CTAs per SM / 1 request per SM); B = SM count - 1 runs the two kernels.
+    K = 3, V = 151936 bf16 (5 chunks a row), every seventh request greedy."""
+    import speculative_decoding_verification_15_gb300 as pkg
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, K, V = sms + offset, 3, 151936
+    batch, d = _sized(B, K, V, 3300 + B)
+    out = pkg.verify_sample(d["target"], d["draft"], d["draft_tokens"], d["temperature"], 3, 1)
+    torch.cuda.synchronize()
+    gpu = {k: v.cpu().numpy() for k, v in out.items()}
+    compare_sample(gpu, run_oracle_sample(batch, 3, 1), batch["temperature"].numpy())
+    assert (gpu["status"] == 0).all()
