@@ -92,6 +92,28 @@ def test_sample_flat_matches_padded_and_oracle(dt, base):
     compare_sample(gpu, ref, batch["temperature"].numpy())
 
 
+def test_sample_flat_single_kernel():
+    """The flattened layout at B = 256 (the single-kernel path), ragged k_b from 0 to
+    6, against the oracle."""
+    import speculative_decoding_verification_15_gb300 as pkg
+
+    B, K, V = 256, 6, 23011
+    nd = [(5 * b + 3) % (K + 1) for b in range(B)]
+    batch = synth.make_batch(B, K, V, torch.bfloat16, 41, zipf=True, noise_sigmas=(0.5, 1.0),
+                             temperature=(0.6, 1.0), num_draft=nd, greedy_mask=[b % 9 == 4 for b in range(B)])
+    f = flatten(batch)
+    out = pkg.verify_sample_flat(f["target"].cuda(), f["draft"].cuda(), f["cu"].cuda(), f["tokens"].cuda(),
+                                 batch["temperature"].cuda(), 5, 6, K)
+    torch.cuda.synchronize()
+    cu = f["cu"].numpy()
+    gpu = dict(tokens=unflatten_tokens(out["tokens"].cpu().numpy(), cu, f["kb"], K),
+               accepted=out["accepted"].cpu().numpy(), status=out["status"].cpu().numpy(),
+               p=unflatten_pq(out["p"].cpu().numpy(), cu, f["kb"], K), q=unflatten_pq(out["q"].cpu().numpy(), cu,
+                                                                                      f["kb"], K))
+    compare_sample(gpu, run_oracle_sample(batch, 5, 6), batch["temperature"].numpy())
+    assert (gpu["status"] == 0).all()
+
+
 def test_greedy_flat_matches_padded():
     import speculative_decoding_verification_15_gb300 as pkg
 
@@ -144,13 +166,16 @@ def test_scheduler_lengths_feed_flat_verify():
     compare_sample(gpu, run_oracle_sample(batch, 2, 8), batch["temperature"].numpy())
 
 
-def test_flat_verify_under_cuda_graph_capture():
+@pytest.mark.parametrize("B", [8, 200])
+def test_flat_verify_under_cuda_graph_capture(B):
     """Capture one flat sampling verify in a CUDA graph, then replay it on new
-    inputs copied into the captured buffers: same results as eager calls."""
+    inputs copied into the captured buffers: same results as eager calls.  B = 200
+    (at least one request per SM) captures the single kernel with the memset of
+    its counters before it."""
     from speculative_decoding_verification_15_gb300 import api, binding
 
-    B, K, V = 8, 4, 30000
-    nd = [4, 1, 0, 3, 4, 2, 4, 1]
+    K, V = 4, 30000
+    nd = ([4, 1, 0, 3, 4, 2, 4, 1] * 32)[:B]
     batches = [synth.make_batch(B, K, V, torch.bfloat16, 500 + i, zipf=True, noise_sigmas=(0.5, 1.0),
                                 temperature=(0.7, 1.0), num_draft=nd) for i in range(3)]
     flats = [flatten(b) for b in batches]
