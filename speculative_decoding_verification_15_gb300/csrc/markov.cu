@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "spec_common.cuh"
@@ -1422,66 +1423,73 @@ int markov_topk_impl(const MarkovParams &p, int ncand, int32_t *cands, cudaStrea
     return SPEC_OK;
 }
 
-int markov_impl(const MarkovParams &p, cudaStream_t stream) {
-    const size_t smem = bias_smem_bytes(p.r);
-    cudaError_t e = cudaSuccess;
-    if (smem > 48 * 1024) {  // ranks above 348: opt in to the larger shared memory
-        e = cudaFuncSetAttribute(markov_bias_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) {
-            note_cuda_error((int)e);
-            return SPEC_ECUDA;
+// Per device, set up once: the bias kernels' shared-memory limits (what the largest
+// rank each one serves needs) and the SM count; per rank, the occupancy of the two-CTA
+// bias kernel, queried the first time that rank is drawn.
+struct MarkovDevice {
+    bool ready = false;
+    int sms = 0;
+    int per[SPEC_MARKOV_MAX_RANK / 16 + 1];  // CTAs per SM of markov_bias_tma_kernel by r / 16; -1: not yet known
+};
+std::mutex g_mk_mu;
+MarkovDevice g_mk[64];
+
+int markov_device(int r, int *sms, int *per) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && (dev < 0 || dev >= 64)) return SPEC_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mk_mu);
+    MarkovDevice &d = g_mk[dev];
+    if (e == cudaSuccess && !d.ready) {
+        e = cudaFuncSetAttribute(markov_bias_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bias_smem_bytes(SPEC_MARKOV_MAX_RANK));
+        const int tmax = (int)tma_smem_bytes(SPEC_MARKOV_MAX_RANK), wmax = (int)ws_smem_bytes(256);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(markov_bias_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, tmax);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(markov_bias_tma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, tmax);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(markov_bias_ws_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, wmax);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(markov_bias_ws_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, wmax);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) {
+            for (int &x : d.per) x = -1;
+            d.ready = true;
         }
     }
-    // bf16 factors with 16-byte rows (r a multiple of 16, aligned bases): tensor cores
+    if (e == cudaSuccess && (r % 16) == 0 && d.per[r / 16] < 0) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, markov_bias_tma_kernel<true>, kMkThreads,
+                                                          tma_smem_bytes(r));
+        if (e == cudaSuccess) d.per[r / 16] = n;
+    }
+    if (e != cudaSuccess) {
+        note_cuda_error((int)e);
+        return SPEC_ECUDA;
+    }
+    *sms = d.sms;
+    *per = (r % 16) == 0 ? d.per[r / 16] : 0;
+    return SPEC_OK;
+}
+
+int markov_impl(const MarkovParams &p, cudaStream_t stream) {
+    int sms = 0, per = 0;
+    const int rc = markov_device(p.r, &sms, &per);
+    if (rc) return rc;
+    cudaError_t e = cudaSuccess;
+    const size_t smem = bias_smem_bytes(p.r);
+    // bf16 factors with 16-byte rows (r a multiple of 16, aligned bases): tensor cores,
+    // the role-split kernel where its stages and two staged tiles fit (r <= 256), else
+    // the two-CTA kernel; vector accesses in the epilogue where U and z rows allow them
     const bool mma = p.dtype == SPEC_BF16 && (p.r % 16) == 0 && ((uintptr_t)p.emb % 16) == 0 &&
                      ((uintptr_t)p.proj % 16) == 0;
-    // bf16 factors streamed by bulk copies: a persistent grid of as many CTAs as fit;
-    // vector accesses in the epilogue where U and z rows allow them
-    const size_t tsmem = tma_smem_bytes(p.r);
     const bool tvec = (p.ld_row % 4) == 0 && ((uintptr_t)p.base % 8) == 0 && (p.V % 4) == 0 &&
                       ((uintptr_t)p.z % 16) == 0;
-    int tgrid = 0;
-    if (mma) {
-        if (tsmem > 48 * 1024) {
-            e = cudaFuncSetAttribute(markov_bias_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)tsmem);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(markov_bias_tma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tsmem);
-            if (e != cudaSuccess) {
-                note_cuda_error((int)e);
-                return SPEC_ECUDA;
-            }
-        }
-        int dev = 0, sms = 0, per = 0;
-        e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, markov_bias_tma_kernel<true>, kMkThreads, tsmem);
-        if (e != cudaSuccess) {
-            note_cuda_error((int)e);
-            return SPEC_ECUDA;
-        }
-        const int ntiles = (p.V + kMmCols - 1) / kMmCols;
-        tgrid = per > 0 ? min(ntiles, per * sms) : 0;
-    }
-    // the role-split kernel where its stages and two staged tiles fit (r <= 256)
-    const size_t wsmem = ws_smem_bytes(p.r);
-    int wgrid = 0;
-    if (mma && wsmem <= 227 * 1024) {
-        e = cudaFuncSetAttribute(markov_bias_ws_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(markov_bias_ws_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)wsmem);
-        int dev = 0, sms = 0;
-        if (e == cudaSuccess) e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) {
-            note_cuda_error((int)e);
-            return SPEC_ECUDA;
-        }
-        wgrid = min((p.V + kMmCols - 1) / kMmCols, sms);
-    }
+    const int ntiles = (p.V + kMmCols - 1) / kMmCols;
+    const size_t tsmem = tma_smem_bytes(p.r), wsmem = ws_smem_bytes(p.r);
+    const int tgrid = mma && per > 0 ? min(ntiles, per * sms) : 0;
+    const int wgrid = mma && p.r <= 256 ? min(ntiles, sms) : 0;
     if (p.K == 0) {
         markov_status_kernel<<<(p.B + 255) / 256, 256, 0, stream>>>(p);
     } else {
