@@ -39,7 +39,7 @@ def run_oracle_sample(batch: dict, seed: int, step: int, nthreads: int = 8) -> d
 def compare_sample(gpu: dict, ref: dict, temperature: np.ndarray, num_draft=None, K=None) -> dict:
     """Compare one batch of the CUDA path with the oracle, request by request.
 
-    The benchmark spec's parity rule: greedy requests bit-exact; sampling requests
+    The parity rule: greedy requests bit-exact; sampling requests
     identical in accepted length and tokens except at a near-tie, where the
     threshold gap (bit 1) or the top-2 Gumbel gap (bit 2) is below 1e-5 relative,
     or where the residual has no support (bit 4, reachable only by rounding).
