@@ -23,7 +23,9 @@
 //                        uses.
 // Top-K drafting: markov_topk_select_kernel (every row's candidates, one launch),
 // then markov_topk_draw_kernel (the walk over the positions, a CTA per request).
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -369,20 +371,40 @@ __host__ __device__ inline size_t ws_smem_bytes(int r) {
            2 * sizeof(float) * (size_t)kMmReqs * kCtStride + sizeof(int) * kMmReqs;
 }
 
+// TM (r a multiple of 64): each tile's projection rows arrive as r / 64 tensor-map
+// copies of a 64-entry x 64-element box (8 KB), 128-byte swizzled, into 1024-byte
+// aligned stages; the dynamic shared memory then carries 1 KB of alignment slack.
+__host__ __device__ inline size_t ws_stage_bytes_tm(int r) { return (size_t)(r / 64) * 8192; }
+__host__ __device__ inline size_t ws_smem_bytes_tm(int r) {
+    return sizeof(uint16_t) * (size_t)kMmReqs * (r + 8) + 1024 + kWsStages * ws_stage_bytes_tm(r) +
+           2 * sizeof(float) * (size_t)kMmReqs * kCtStride + sizeof(int) * kMmReqs;
+}
+
+// One 2-D tensor-map copy of box {x, y} into shared memory, completed on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ bool ws_failed(const int *f) { return *(volatile const int *)f != 0; }
 
-template <bool VEC>
-__global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovParams p, int k) {
+template <bool VEC, bool TM>
+__global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovParams p, int k,
+                                                                      const __grid_constant__ CUtensorMap tmap) {
     extern __shared__ __align__(128) unsigned char wsm[];
     __shared__ __align__(8) uint64_t s_full[kWsStages], s_empty[kWsStages], s_cfull[2], s_cempty[2];
     __shared__ int s_fail;
     __shared__ uint32_t s_cons[kWsStages];  // copies of each stage the multiplying warps have waited for
     const int r = p.r, rs = r + 8;
-    const size_t sb = ws_stage_bytes(r);
+    const size_t sb = TM ? ws_stage_bytes_tm(r) : ws_stage_bytes(r);
     const uint32_t blk = 16u * (uint32_t)r + 16u;
     const uint32_t rowbytes = (uint32_t)r * 2u;
     uint16_t *Hs = reinterpret_cast<uint16_t *>(wsm);                          // [64][rs]
     unsigned char *stages = wsm + sizeof(uint16_t) * (size_t)kMmReqs * rs;      // [kWsStages][sb]
+    if (TM) stages += (1024u - (smem_addr(stages) & 1023u)) & 1023u;         // the swizzle's 1 KB atoms
     float *Cb = reinterpret_cast<float *>(stages + kWsStages * sb);            // [2][64][kCtStride]
     int *okv = reinterpret_cast<int *>(Cb + 2 * kMmReqs * kCtStride);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -419,6 +441,17 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
             }
             const int t = (int)blockIdx.x + i * (int)gridDim.x;
             const int v0 = t * kMmCols, nc = min(kMmCols, p.V - v0);
+            if (TM) {
+                // whole boxes (the rows past V are filled with zeros and counted)
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&s_full[st], (uint32_t)sb);
+                    for (int c = 0; c < r / 64; ++c)
+                        tma_load_2d(stages + (size_t)st * sb + (size_t)c * 8192, &tmap, 64 * c, v0, &s_full[st]);
+                }
+                __syncwarp();
+                issued[st] += 1u;
+                return;
+            }
             if (lane == 0) mbar_arrive_expect_tx(&s_full[st], (uint32_t)nc * rowbytes);
             __syncwarp();
             const int rows = min(8, nc - 8 * lane);
@@ -472,16 +505,28 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc[a][c][e] = 0.f;
-                // B: n-blocks 4 nh + 2 hb + (li >> 1), k half (li & 1), for hb = 0, 1
+                // B: n-blocks 4 nh + 2 hb + (li >> 1), k half (li & 1), for hb = 0, 1.
+                // Block copies: entries {8 j + beta} of n-block beta, block j at j blk.
+                // Tensor copies: entries 8 beta .. 8 beta + 7 of n-block beta, box c of
+                // elements 64 c .. 64 c + 63, row n at n * 128 with 16-byte chunk q stored
+                // at q ^ (n % 8) (n % 8 = l8 for this lane's row)
                 const uint32_t b_addr = smem_addr(stages + (size_t)st * sb) + (uint32_t)l8 * blk +
                                         (uint32_t)(4 * nh + (li >> 1)) * rowbytes + (uint32_t)(li & 1) * 16u;
                 const uint32_t b_step = 2u * rowbytes;  // the next two n-blocks
+                const uint32_t t_row = smem_addr(stages + (size_t)st * sb) + (uint32_t)(8 * (4 * nh + (li >> 1)) + l8) * 128u;
                 uint32_t fa[2][4], fb[2][4], fc[2][4], fd[2][4];
                 auto frag = [&](int kk, int q) {
                     ldsm_x4(fa[q], a_addr + 2u * kk);
                     ldsm_x4(fb[q], a_addr + a_step + 2u * kk);
-                    ldsm_x4(fc[q], b_addr + 2u * kk);
-                    ldsm_x4(fd[q], b_addr + b_step + 2u * kk);
+                    if (TM) {
+                        const uint32_t off = (uint32_t)(kk >> 6) * 8192u +
+                                             ((uint32_t)((((kk & 63) >> 3) + (li & 1)) ^ l8) << 4);
+                        ldsm_x4(fc[q], t_row + off);
+                        ldsm_x4(fd[q], t_row + 16u * 128u + off);
+                    } else {
+                        ldsm_x4(fc[q], b_addr + 2u * kk);
+                        ldsm_x4(fd[q], b_addr + b_step + 2u * kk);
+                    }
                 };
                 auto mma8 = [&](int q) {
                     const uint32_t bn[4][2] = {{fc[q][0], fc[q][1]}, {fc[q][2], fc[q][3]},
@@ -511,10 +556,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int m = 32 * mh + 16 * a + g, beta = 4 * nh + c;
-                        Cs[m * kCtStride + 16 * t4 + beta] = acc[a][c][0];
-                        Cs[m * kCtStride + 16 * t4 + 8 + beta] = acc[a][c][1];
-                        Cs[(m + 8) * kCtStride + 16 * t4 + beta] = acc[a][c][2];
-                        Cs[(m + 8) * kCtStride + 16 * t4 + 8 + beta] = acc[a][c][3];
+                        // column j of n-block beta: entry 8 j + beta (blocks), 8 beta + j (boxes)
+                        const int e0 = TM ? 8 * beta + 2 * t4 : 16 * t4 + beta;
+                        const int e1 = TM ? e0 + 1 : e0 + 8;
+                        Cs[m * kCtStride + e0] = acc[a][c][0];
+                        Cs[m * kCtStride + e1] = acc[a][c][1];
+                        Cs[(m + 8) * kCtStride + e0] = acc[a][c][2];
+                        Cs[(m + 8) * kCtStride + e1] = acc[a][c][3];
                     }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_cfull[cb]);
@@ -1448,10 +1496,18 @@ int markov_device(int r, int *sms, int *per) {
             e = cudaFuncSetAttribute(markov_bias_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, tmax);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(markov_bias_tma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, tmax);
+        const int wtm = (int)ws_smem_bytes_tm(256);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(markov_bias_ws_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, wmax);
+            e = cudaFuncSetAttribute(markov_bias_ws_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     wmax);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(markov_bias_ws_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, wmax);
+            e = cudaFuncSetAttribute(markov_bias_ws_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     wmax);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(markov_bias_ws_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, wtm);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(markov_bias_ws_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     wtm);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) {
             for (int &x : d.per) x = -1;
@@ -1473,6 +1529,36 @@ int markov_device(int r, int *sms, int *per) {
     return SPEC_OK;
 }
 
+// The driver's tensor-map encoder, looked up once (null if the driver has none).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// The projection rows [V, r] (bf16, r a multiple of 64) as a 2-D tensor map of
+// 64 x 64 boxes, 128-byte swizzled; false if it cannot be made.
+bool proj_tensor_map(const MarkovParams &p, CUtensorMap *map) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || (p.r % 64) != 0 || ((uintptr_t)p.proj % 16) != 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.r * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p.proj), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int markov_impl(const MarkovParams &p, cudaStream_t stream) {
     int sms = 0, per = 0;
     const int rc = markov_device(p.r, &sms, &per);
@@ -1490,15 +1576,22 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
     const size_t tsmem = tma_smem_bytes(p.r), wsmem = ws_smem_bytes(p.r);
     const int tgrid = mma && per > 0 ? min(ntiles, per * sms) : 0;
     const int wgrid = mma && p.r <= 256 ? min(ntiles, sms) : 0;
+    alignas(64) CUtensorMap tmap = {};
+    const bool tm = wgrid > 0 && proj_tensor_map(p, &tmap);
+    const size_t wsmem_tm = ws_smem_bytes_tm(p.r);
     if (p.K == 0) {
         markov_status_kernel<<<(p.B + 255) / 256, 256, 0, stream>>>(p);
     } else {
         const int nb = (p.V + kMkCols - 1) / kMkCols;
         for (int k = 0; k < p.K; ++k) {
-            if (wgrid > 0 && tvec)
-                markov_bias_ws_kernel<true><<<wgrid, kWsThreads, wsmem, stream>>>(p, k);
+            if (tm && tvec)
+                markov_bias_ws_kernel<true, true><<<wgrid, kWsThreads, wsmem_tm, stream>>>(p, k, tmap);
+            else if (tm)
+                markov_bias_ws_kernel<false, true><<<wgrid, kWsThreads, wsmem_tm, stream>>>(p, k, tmap);
+            else if (wgrid > 0 && tvec)
+                markov_bias_ws_kernel<true, false><<<wgrid, kWsThreads, wsmem, stream>>>(p, k, tmap);
             else if (wgrid > 0)
-                markov_bias_ws_kernel<false><<<wgrid, kWsThreads, wsmem, stream>>>(p, k);
+                markov_bias_ws_kernel<false, false><<<wgrid, kWsThreads, wsmem, stream>>>(p, k, tmap);
             else if (mma && tgrid > 0 && tvec)
                 markov_bias_tma_kernel<true><<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
             else if (mma && tgrid > 0)
