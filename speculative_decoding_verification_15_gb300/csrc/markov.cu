@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
 constexpr int kWsStages = 4;
 constexpr int kWsMma = 8;  // multiplying warps
 constexpr int kWsEpi = 4;  // write-back warps
-constexpr int kWsThreads = 32 * (kWsMma + kWsEpi + 1);
+constexpr int kWsThreads = 32 * (kWsMma + kWsEpi + 2);  // + the copy warp, + (TM) the backbone-logit copy warp
 
 __host__ __device__ inline size_t ws_stage_bytes(int r) { return (size_t)8 * (16 * (size_t)r + 16); }
 __host__ __device__ inline size_t ws_smem_bytes(int r) {
@@ -375,9 +375,13 @@ __host__ __device__ inline size_t ws_smem_bytes(int r) {
 // copies of a 64-entry x 64-element box (8 KB), 128-byte swizzled, into 1024-byte
 // aligned stages; the dynamic shared memory then carries 1 KB of alignment slack.
 __host__ __device__ inline size_t ws_stage_bytes_tm(int r) { return (size_t)(r / 64) * 8192; }
+// The backbone logits come the same way: a 3-D tensor map over base [B, K, ld_row],
+// one box of 64 entries x 64 requests of position k a tile, into two 8 KB slots filled
+// by a warp of their own.
+constexpr int kUSlotBytes = 64 * 64 * 2;
 __host__ __device__ inline size_t ws_smem_bytes_tm(int r) {
     return sizeof(uint16_t) * (size_t)kMmReqs * (r + 8) + 1024 + kWsStages * ws_stage_bytes_tm(r) +
-           2 * sizeof(float) * (size_t)kMmReqs * kCtStride + sizeof(int) * kMmReqs;
+           2 * (size_t)kUSlotBytes + 2 * sizeof(float) * (size_t)kMmReqs * kCtStride + sizeof(int) * kMmReqs;
 }
 
 // One 2-D tensor-map copy of box {x, y} into shared memory, completed on an mbarrier.
@@ -389,15 +393,26 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+            "r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ bool ws_failed(const int *f) { return *(volatile const int *)f != 0; }
 
 template <bool VEC, bool TM>
 __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovParams p, int k,
-                                                                      const __grid_constant__ CUtensorMap tmap) {
+                                                                      const __grid_constant__ CUtensorMap tmap,
+                                                                      const __grid_constant__ CUtensorMap umap) {
     extern __shared__ __align__(128) unsigned char wsm[];
     __shared__ __align__(8) uint64_t s_full[kWsStages], s_empty[kWsStages], s_cfull[2], s_cempty[2];
     __shared__ int s_fail;
     __shared__ uint32_t s_cons[kWsStages];  // copies of each stage the multiplying warps have waited for
+    __shared__ __align__(8) uint64_t s_ufull[2], s_uempty[2];  // TM: the backbone-logit slots
+    __shared__ uint32_t s_ucons[2];
     const int r = p.r, rs = r + 8;
     const size_t sb = TM ? ws_stage_bytes_tm(r) : ws_stage_bytes(r);
     const uint32_t blk = 16u * (uint32_t)r + 16u;
@@ -405,7 +420,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
     uint16_t *Hs = reinterpret_cast<uint16_t *>(wsm);                          // [64][rs]
     unsigned char *stages = wsm + sizeof(uint16_t) * (size_t)kMmReqs * rs;      // [kWsStages][sb]
     if (TM) stages += (1024u - (smem_addr(stages) & 1023u)) & 1023u;         // the swizzle's 1 KB atoms
-    float *Cb = reinterpret_cast<float *>(stages + kWsStages * sb);            // [2][64][kCtStride]
+    unsigned char *ubuf = stages + kWsStages * sb;                            // TM: [2][64 requests][64] bf16
+    float *Cb = reinterpret_cast<float *>(ubuf + (TM ? 2 * kUSlotBytes : 0));   // [2][64][kCtStride]
     int *okv = reinterpret_cast<int *>(Cb + 2 * kMmReqs * kCtStride);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ntiles = (p.V + kMmCols - 1) / kMmCols;
@@ -420,12 +436,16 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
         for (int c = 0; c < 2; ++c) {
             mbar_init(&s_cfull[c], kWsMma / 2);
             mbar_init(&s_cempty[c], kWsEpi);
+            mbar_init(&s_ufull[c], 1);
+            mbar_init(&s_uempty[c], kWsEpi);
+            s_ucons[c] = 0u;
         }
         s_fail = 0;
         mbar_init_fence();
     }
     __syncthreads();
     uint32_t issued[kWsStages] = {};  // producer: copies issued into each stage
+    uint32_t uissued[2] = {0u, 0u};   // backbone-logit copy warp (TM): copies issued into each slot
     int gi = 0;  // tiles of this CTA before the current chunk of requests (phase bookkeeping)
     for (int b0 = 0; b0 < p.B; b0 += kMmReqs) {
         // producer: one tile's copies into stage gt % kWsStages, once the multiplying
@@ -461,9 +481,30 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
                          &s_full[st]);
             issued[st] += 1u;
         };
+        // TM: tile i's backbone logits into slot gt % 2, once the write-back warps are
+        // done with the slot's previous tile (the backbone-logit copy warp)
+        auto produce_u = [&](int i) {
+            const int gt = gi + i, us = gt & 1;
+            bool ok = !ws_failed(&s_fail);
+            if (ok && gt >= 2 && lane == 0) ok = mbar_wait(&s_uempty[us], (uint32_t)((gt / 2 - 1) & 1), kWaitNs);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) s_fail = 1;
+                return;
+            }
+            const int t = (int)blockIdx.x + i * (int)gridDim.x;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&s_ufull[us], (uint32_t)kUSlotBytes);
+                tma_load_3d(ubuf + (size_t)us * kUSlotBytes, &umap, t * kMmCols, k, b0, &s_ufull[us]);
+            }
+            __syncwarp();
+            uissued[us] += 1u;
+        };
         const int first = min(nmine, kWsStages);
         if (warp == kWsMma + kWsEpi)
             for (int i = 0; i < first; ++i) produce(i);
+        if (TM && warp == kWsMma + kWsEpi + 1)
+            for (int i = 0; i < min(nmine, 2); ++i) produce_u(i);
         if (tid < kMmReqs) {
             const int b = b0 + tid;
             int ok = 0;
@@ -593,22 +634,37 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
                 }
             };
             uint2 u1[8], u2[8], u3[8];  // tiles i + 1 .. i + 3, loaded three tiles ahead
-            load_u(0, u1);
-            load_u(1, u2);
-            load_u(2, u3);
+            if (!TM) {
+                load_u(0, u1);
+                load_u(1, u2);
+                load_u(2, u3);
+            }
             for (int i = 0; i < nmine; ++i) {
                 const int gt = gi + i, cb = gt & 1;
                 const int t = (int)blockIdx.x + i * (int)gridDim.x;
                 const int v0 = t * kMmCols, ncol = min(kMmCols, p.V - v0);
                 uint2 upk[8];
+                const int us = gt & 1;
+                bool uok = true;
+                if (TM) {
+                    uok = !ws_failed(&s_fail) && mbar_wait(&s_ufull[us], (uint32_t)((gt / 2) & 1), kWaitNs);
+                    if (!uok) s_fail = 1;
+                    if (uok && e == 0) atomicAdd(&s_ucons[us], 1u);
+                    const unsigned char *ur = ubuf + (size_t)us * kUSlotBytes + 2 * eq;
 #pragma unroll
-                for (int ps = 0; ps < 8; ++ps) {
-                    upk[ps] = u1[ps];
-                    u1[ps] = u2[ps];
-                    u2[ps] = u3[ps];
+                    for (int ps = 0; ps < 8; ++ps)
+                        upk[ps] = uok ? *reinterpret_cast<const uint2 *>(ur + 128 * (8 * ps + (e >> 4)))
+                                      : make_uint2(0u, 0u);
+                } else {
+#pragma unroll
+                    for (int ps = 0; ps < 8; ++ps) {
+                        upk[ps] = u1[ps];
+                        u1[ps] = u2[ps];
+                        u2[ps] = u3[ps];
+                    }
+                    load_u(i + 3, u3);
                 }
-                load_u(i + 3, u3);
-                bool ok = !ws_failed(&s_fail);
+                bool ok = uok && !ws_failed(&s_fail);
                 if (ok && !mbar_wait(&s_cfull[cb], (uint32_t)((gt / 2) & 1), kWaitNs)) {
                     s_fail = 1;
                     ok = false;
@@ -640,10 +696,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
                 }
                 __syncwarp();
                 if (ok && lane == 0) mbar_arrive(&s_cempty[cb]);
+                if (TM && uok && lane == 0) mbar_arrive(&s_uempty[us]);
             }
-        } else {
+        } else if (warp == kWsMma + kWsEpi) {
             // ---- copies of the remaining tiles
             for (int i = first; i < nmine; ++i) produce(i);
+        } else if (TM) {
+            // ---- backbone-logit copies of the remaining tiles
+            for (int i = 2; i < nmine; ++i) produce_u(i);
         }
         __syncthreads();
         // after a give-up: the copies issued but not waited for still land; wait for
@@ -651,6 +711,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) markov_bias_ws_kernel(MarkovPar
         if (tid == 32 * (kWsMma + kWsEpi) && ws_failed(&s_fail))
             for (int s2 = 0; s2 < kWsStages; ++s2)
                 for (uint32_t ph = s_cons[s2]; ph < issued[s2]; ++ph) mbar_wait(&s_full[s2], ph & 1u, kWaitNs);
+        if (TM && tid == 32 * (kWsMma + kWsEpi + 1) && ws_failed(&s_fail))
+            for (int s2 = 0; s2 < 2; ++s2)
+                for (uint32_t ph = s_ucons[s2]; ph < uissued[s2]; ++ph) mbar_wait(&s_ufull[s2], ph & 1u, kWaitNs);
         __syncthreads();
         gi += nmine;
         if (ws_failed(&s_fail)) {
@@ -1559,6 +1622,21 @@ bool proj_tensor_map(const MarkovParams &p, CUtensorMap *map) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The backbone logits [B, K, ld_row] (bf16) as a 3-D tensor map {V, K, B} of
+// 64 x 1 x 64 boxes (a tile's entries of one position for a chunk of requests); false
+// if it cannot be made (rows not 16-byte aligned).
+bool base_tensor_map(const MarkovParams &p, CUtensorMap *map) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || (p.ld_row % 8) != 0 || ((uintptr_t)p.base % 16) != 0) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)p.K, (cuuint64_t)p.B};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.ld_row * 2, (cuuint64_t)p.ld_row * 2 * (cuuint64_t)p.K};
+    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int markov_impl(const MarkovParams &p, cudaStream_t stream) {
     int sms = 0, per = 0;
     const int rc = markov_device(p.r, &sms, &per);
@@ -1576,8 +1654,8 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
     const size_t tsmem = tma_smem_bytes(p.r), wsmem = ws_smem_bytes(p.r);
     const int tgrid = mma && per > 0 ? min(ntiles, per * sms) : 0;
     const int wgrid = mma && p.r <= 256 ? min(ntiles, sms) : 0;
-    alignas(64) CUtensorMap tmap = {};
-    const bool tm = wgrid > 0 && proj_tensor_map(p, &tmap);
+    alignas(64) CUtensorMap tmap = {}, umap = {};
+    const bool tm = wgrid > 0 && p.K > 0 && proj_tensor_map(p, &tmap) && base_tensor_map(p, &umap);
     const size_t wsmem_tm = ws_smem_bytes_tm(p.r);
     if (p.K == 0) {
         markov_status_kernel<<<(p.B + 255) / 256, 256, 0, stream>>>(p);
@@ -1585,13 +1663,13 @@ int markov_impl(const MarkovParams &p, cudaStream_t stream) {
         const int nb = (p.V + kMkCols - 1) / kMkCols;
         for (int k = 0; k < p.K; ++k) {
             if (tm && tvec)
-                markov_bias_ws_kernel<true, true><<<wgrid, kWsThreads, wsmem_tm, stream>>>(p, k, tmap);
+                markov_bias_ws_kernel<true, true><<<wgrid, kWsThreads, wsmem_tm, stream>>>(p, k, tmap, umap);
             else if (tm)
-                markov_bias_ws_kernel<false, true><<<wgrid, kWsThreads, wsmem_tm, stream>>>(p, k, tmap);
+                markov_bias_ws_kernel<false, true><<<wgrid, kWsThreads, wsmem_tm, stream>>>(p, k, tmap, umap);
             else if (wgrid > 0 && tvec)
-                markov_bias_ws_kernel<true, false><<<wgrid, kWsThreads, wsmem, stream>>>(p, k, tmap);
+                markov_bias_ws_kernel<true, false><<<wgrid, kWsThreads, wsmem, stream>>>(p, k, tmap, umap);
             else if (wgrid > 0)
-                markov_bias_ws_kernel<false, false><<<wgrid, kWsThreads, wsmem, stream>>>(p, k, tmap);
+                markov_bias_ws_kernel<false, false><<<wgrid, kWsThreads, wsmem, stream>>>(p, k, tmap, umap);
             else if (mma && tgrid > 0 && tvec)
                 markov_bias_tma_kernel<true><<<tgrid, kMkThreads, tsmem, stream>>>(p, k);
             else if (mma && tgrid > 0)
