@@ -349,17 +349,19 @@ __global__ void __launch_bounds__(kMkThreads, 2) markov_bias_tma_kernel(MarkovPa
     }
 }
 
-// The same products with the work split by roles (one CTA per SM, 13 warps): warp 12
-// issues the bulk copies into kWsStages stages; warps 0..7 multiply, in two groups of
-// four that take alternate tiles (warp (group, w) forms requests 32 (w / 2) .. +31 and
-// n-blocks 4 (w % 2) .. +3: eight independent accumulators), and write the products
-// into the group's staged tile; warps 8..11 read a staged tile with the backbone
-// logits (loaded three tiles ahead) and write z.  The roles meet on mbarriers (stage full / stage
-// released, tile staged / tile written back), so the tensor cores work on the next
-// tile while the previous one is written out and the tile after it is copied in.
-// Every wait is bounded; after one gives up the roles stop waiting, the tiles not
-// multiplied are written as NaN (status 4), and the copies still in flight are
-// waited for (bounded) before the CTA leaves.
+// The same products with the work split by roles (one CTA per SM, 14 warps): warp 12
+// issues the projection copies into kWsStages stages; warps 0..7 multiply, in two
+// groups of four that take alternate tiles (warp (group, w) forms requests 32 (w / 2)
+// .. +31 and n-blocks 4 (w % 2) .. +3: eight independent accumulators), and write the
+// products into the group's staged tile; warps 8..11 add the backbone logits and write
+// z.  The backbone logits are loaded by the write-back warps themselves three tiles
+// ahead, or (TM) copied by warp 13 through a tensor map into one of two slots.  The
+// roles meet on mbarriers (stage full / stage released, tile staged / tile written
+// back, logits in / slot released), so the tensor cores work on the next tile while
+// the previous one is written out and the tile after it is copied in.  Every wait is
+// bounded; after one gives up the roles stop waiting, the tiles not multiplied are
+// written as NaN (status 4), and the copies still in flight are waited for (bounded)
+// before the CTA leaves.
 constexpr int kWsStages = 4;
 constexpr int kWsMma = 8;  // multiplying warps
 constexpr int kWsEpi = 4;  // write-back warps
